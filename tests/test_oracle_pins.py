@@ -1,0 +1,550 @@
+"""Pins of the oracle against what the DGC pages and the mathematics fix (CPU only).
+
+Each test checks the oracle against something other than itself: published SplitMix64
+outputs, exact rational arithmetic (the definition of a correctly rounded fma/add), brute-force
+sorting on tiny inputs, hand-built codec streams, and sizes printed in the DGC review.
+"""
+import math
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import exact_fp32 as X
+import workloads
+from conftest import read_golden
+
+GOLD = 0x9E3779B97F4A7C15
+M64 = 2**64 - 1
+
+
+def _sm_mix(z):
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & M64
+    return z ^ (z >> 31)
+
+
+def sm_outputs(seed, count):
+    """SplitMix64 outputs; pinned to published values in test_python_splitmix_published."""
+    out, s = [], seed
+    for _ in range(count):
+        s = (s + GOLD) & M64
+        out.append(_sm_mix(s))
+    return out
+
+
+# ---------------------------------------------------------------------------------- SplitMix64
+def test_oracle_splitmix64_published_outputs(orc):
+    for _, vals in read_golden("splitmix64.txt"):
+        seed, outs = vals[0], vals[1:]
+        s = seed
+        for o in outs:
+            s = (s + GOLD) & M64
+            assert orc.mix64(s) == o
+
+
+def test_python_splitmix_published():
+    for _, vals in read_golden("splitmix64.txt"):
+        assert sm_outputs(vals[0], len(vals) - 1) == vals[1:]
+
+
+@pytest.mark.parametrize("seed", [0, 1234567, M64, 42])
+def test_sample_positions_follow_definition(orc, seed):
+    for s in [0, 1, 5, 160]:
+        seg_seed = sm_outputs(seed, s + 1)[-1]
+        xs = sm_outputs(seg_seed, 16)
+        for n_s in [1, 2, 999, 24_000_000, 2**32 - 1]:
+            for j in range(16):
+                p = orc.sample_position(seed, s, j, n_s)
+                assert p == (xs[j] * n_s) >> 64
+                assert 0 <= p < n_s
+
+
+# ---------------------------------------------------------------------------------- k rule
+@pytest.mark.parametrize("n,sparsity", [
+    (1_048_576, "0.999"), (1 << 30, "0.75"), (1 << 30, "0.9375"), (1 << 30, "0.984375"),
+    (1 << 30, "0.99609375"), (1 << 30, "0.999"), (24_000_000, "0.999"), (2_000_000, "0.999"),
+    (2_359_296, "0.999"), (64, "0.999"), (999, "0.999"), (1001, "0.999"), (1, "0.999"),
+    (0, "0.999"), (1000, "0"), (1000, "1"), (4096, "0.5"), (10_737_419, "0.999"),
+    (2**32 - 1, "0.999"), (123_457, "0.99"), (7, "0.3")])
+def test_count_is_ceiling_of_exact_fraction(orc, n, sparsity):
+    expect = math.ceil(n * (1 - Fraction(sparsity)))
+    assert orc.count(n, orc.ppb(1.0 - float(sparsity))) == expect
+
+
+def test_single_tensor_k_is_1049(orc):
+    # 0.1% of 1,048,576 is 1048.576: the rounded-up count is 1049.
+    assert orc.count(1_048_576, orc.ppb(1 - 0.999)) == 1049
+
+
+def test_warmup_schedule_is_powers_of_four():
+    # DGC review, Proposed method, bullet 6 (warm-up raises sparsity gradually); the schedule's
+    # first four densities are 4^-1..4^-4 exactly, then 0.1%.
+    for i, s in enumerate(workloads.WARMUP_SPARSITY[:4], start=1):
+        assert Fraction(s) == 1 - Fraction(1, 4**i)
+    assert workloads.WARMUP_SPARSITY[4] == 0.999
+
+
+def test_deepspeech_message_size_matches_dgc_review(orc):
+    # DGC review, Abstract: DeepSpeech's 488 MB gradient becomes 0.74 MB. 488 MB of binary32 is
+    # 122,000,000 entries; at 99.9% the six segments send 5 * 24,000 + 2,000 = 122,000 values,
+    # 6 bytes each in this format, i.e. 0.732 MB: within 2% of the printed figure.
+    off = workloads.deepspeech_segments()
+    assert off[-1] * 4 == 488_000_000
+    d = orc.ppb(1 - 0.999)
+    k = sum(orc.count(int(b - a), d) for a, b in zip(off[:-1], off[1:]))
+    assert k == 122_000
+    idx = np.arange(k, dtype=np.uint32) * 1000 + 7  # gaps of 999 < 65535: no escapes
+    msg = orc.encode(idx, np.ones(k, np.float32), int(off[-1]))
+    assert len(msg) == 32 + 6 * k
+    assert abs(len(msg) / 1e6 - 0.74) / 0.74 < 0.02
+
+
+# ---------------------------------------------------------------------------------- selection
+def brute_topk(v, k, among=None):
+    keys = [X.key(x) for x in v]
+    cand = range(len(v)) if among is None else among
+    order = sorted(cand, key=lambda i: (-keys[i], i))
+    return sorted(order[:k])
+
+
+def _tricky(rng, n, kind):
+    if kind == 0:
+        return rng.standard_normal(n).astype(np.float32)
+    if kind == 1:
+        return rng.integers(-3, 4, n).astype(np.float32)
+    if kind == 2:
+        return np.where(rng.random(n) < 0.5, np.float32(0.0), np.float32(-0.0)).astype(np.float32)
+    if kind == 3:
+        mags = np.array([0.5, 1.0, 2.0, 1e-30, 3.0e30], np.float32)
+    else:  # keys at the top of the range; only for tests that do no arithmetic
+        mags = np.array([0.5, 3.0e38, np.inf, 1e-45, 0.0], np.float32)
+    return (mags[rng.integers(0, mags.size, n)] * rng.choice([-1, 1], n)).astype(np.float32)
+
+
+@pytest.mark.parametrize("seed", range(120))
+def test_topk_matches_bruteforce(orc, seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 300))
+    v = _tricky(rng, n, seed % 5)
+    k = int(rng.integers(0, n + 1))
+    sel = orc.topk(v, np.arange(n, dtype=np.uint32), k)
+    assert np.nonzero(sel)[0].tolist() == brute_topk(v, k)
+
+
+def _exact_accumulate(g, u, v, m, scale=None):
+    """u' = fma(m, u, g'), v' = v + u' with g' = g * scale when scale is given; exact rational
+    arithmetic rounded once per operation."""
+    un = np.empty_like(u)
+    vn = np.empty_like(v)
+    for i in range(g.size):
+        gp = g[i] if scale is None else X.mul_f32(g[i], scale)
+        un[i] = X.fma_f32(m, u[i], gp)
+        vn[i] = X.add_f32(v[i], un[i])
+    return un, vn
+
+
+def _random_segments(rng, n, max_seg=4):
+    nseg = int(rng.integers(1, max_seg + 1))
+    cuts = np.sort(rng.integers(0, n + 1, nseg - 1))
+    return np.concatenate([[0], cuts, [n]]).astype(np.int64)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_exact_compress_matches_definition(orc, seed):
+    rng = np.random.default_rng(1000 + seed)
+    n = int(rng.integers(1, 400))
+    off = _random_segments(rng, n)
+    kind = seed % 4
+    g = _tricky(rng, n, kind)
+    u = (_tricky(rng, n, kind) * np.float32(0.5)).astype(np.float32)
+    v = _tricky(rng, n, (kind + 1) % 4)
+    m = np.float32(rng.choice([0.0, 0.5, 0.9, 1.0]))
+    sparsity = float(rng.choice([0.0, 0.5, 0.9, 0.99, 0.999, 1.0]))
+    mask = bool(seed % 2)
+    un, vn = _exact_accumulate(g, u, v, m)
+    exp_idx = []
+    for a, b in zip(off[:-1], off[1:]):
+        k = math.ceil((b - a) * (1 - Fraction(str(sparsity))))
+        exp_idx += [int(a) + i for i in brute_topk(vn[a:b], k)]
+    p = orc.make_params(orc.EXACT, sparsity, float(m), mask_momentum=mask)
+    uu, vv = u.copy(), v.copy()
+    idx, val, st = orc.compress(g, uu, vv, off, p)
+    assert idx.tolist() == exp_idx
+    assert [X.bits(x) for x in val] == [X.bits(vn[i]) for i in exp_idx]
+    v_exp, u_exp = vn.copy(), un.copy()
+    v_exp[exp_idx] = 0.0
+    if mask:
+        u_exp[exp_idx] = 0.0
+    assert vv.view(np.uint32).tolist() == v_exp.view(np.uint32).tolist()
+    assert uu.view(np.uint32).tolist() == u_exp.view(np.uint32).tolist()
+    assert sum(s["sent"] for s in st) == len(exp_idx)
+
+
+def _nonzero_normal(rng, n, scale=1.0):
+    x = (rng.standard_normal(n) * scale).astype(np.float32)
+    x[x == 0] = np.float32(0.25)
+    return x
+
+
+def test_sparsity0_masking_off_is_dense_momentum_sgd(orc):
+    # DGC review, Proposed method, bullet 3: momentum correction makes the sparse update follow
+    # dense momentum SGD. With nothing held back (sparsity 0) and no masking, every step sends
+    # exactly the momentum velocity u_t = m * u_{t-1} + g_t.
+    rng = np.random.default_rng(7)
+    n, m = 257, np.float32(0.9)
+    u = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    vel = np.zeros(n, np.float32)
+    p = orc.make_params(orc.EXACT, 0.0, 0.9, mask_momentum=False)
+    for _ in range(5):
+        g = _nonzero_normal(rng, n, 0.01)
+        vel = np.array([X.fma_f32(m, vel[i], g[i]) for i in range(n)], np.float32)
+        idx, val, _ = orc.compress(g, u, v, np.array([0, n]), p)
+        assert idx.tolist() == list(range(n))
+        assert val.view(np.uint32).tolist() == vel.view(np.uint32).tolist()
+        assert not v.any()
+
+
+def test_sparsity0_masking_on_is_plain_sgd(orc):
+    # DGC review, Proposed method, bullet 5: with momentum factor masking the momentum of a sent
+    # entry is cleared, so with sparsity 0 each step sends the fresh gradient itself.
+    rng = np.random.default_rng(8)
+    n = 300
+    u = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    p = orc.make_params(orc.EXACT, 0.0, 0.9, mask_momentum=True)
+    for _ in range(4):
+        g = _nonzero_normal(rng, n)
+        idx, val, _ = orc.compress(g, u, v, np.array([0, n]), p)
+        assert val.view(np.uint32).tolist() == g.view(np.uint32).tolist()
+        assert not u.any() and not v.any()
+
+
+def test_momentum0_sparsity0_sends_gradient(orc):
+    rng = np.random.default_rng(9)
+    n = 100
+    g = _nonzero_normal(rng, n)
+    u = _nonzero_normal(rng, n)
+    v = np.zeros(n, np.float32)
+    idx, val, _ = orc.compress(g, u, v, np.array([0, n]),
+                               orc.make_params(orc.EXACT, 0.0, 0.0, mask_momentum=False))
+    assert val.view(np.uint32).tolist() == g.view(np.uint32).tolist()
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_conservation_sent_plus_residual(orc, mode):
+    # DGC review, Proposed method, bullet 1: what is not sent stays in the local accumulator.
+    # Sent value + residual equals what an all-held-back step (sparsity 1) accumulates, bitwise.
+    rng = np.random.default_rng(11 + mode)
+    n = 5000
+    off = np.array([0, 1234, 1234, 4000, n])
+    g, u0, v0 = (_nonzero_normal(rng, n) for _ in range(3))
+    ua, va, ub, vb = u0.copy(), v0.copy(), u0.copy(), v0.copy()
+    pa = orc.make_params(mode, 0.99, 0.9, mask_momentum=True, sample_ratio=0.05, seed=3)
+    pb = orc.make_params(mode, 1.0, 0.9, mask_momentum=True, sample_ratio=0.05, seed=3)
+    idx, val, _ = orc.compress(g, ua, va, off, pa)
+    idx_b, _, _ = orc.compress(g, ub, vb, off, pb)
+    assert idx_b.size == 0 and idx.size > 0
+    sent = np.zeros(n, bool)
+    sent[idx] = True
+    assert val.view(np.uint32).tolist() == vb[idx].view(np.uint32).tolist()
+    assert not va[sent].any() and not ua[sent].any()
+    assert va[~sent].view(np.uint32).tolist() == vb[~sent].view(np.uint32).tolist()
+    assert ua[~sent].view(np.uint32).tolist() == ub[~sent].view(np.uint32).tolist()
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_accumulate_one_is_single_rounding_fma(orc, seed):
+    rng = np.random.default_rng(50 + seed)
+    for _ in range(200):
+        g, u, v = (np.float32(x) for x in rng.standard_normal(3) * 10.0 ** rng.integers(-6, 6, 3))
+        m = np.float32(rng.choice([0.9, 0.99, 0.5, 1.0, 0.0]))
+        uo, vo = orc.accumulate_one(g, u, v, m)
+        ue = X.fma_f32(m, u, g)
+        assert X.bits(uo) == X.bits(ue)
+        assert X.bits(vo) == X.bits(X.add_f32(v, ue))
+
+
+# ---------------------------------------------------------------------------------- clipping
+def test_clip_scale_closed_form(orc):
+    # DGC review, Proposed method, bullet 4: norm of (3, 4) is 5; bound 1 gives 1/5 in binary32.
+    s, clipped = orc.clip_scale(np.array([3.0, 4.0], np.float32), 1.0)
+    assert clipped and X.bits(s) == X.bits(X.round_f32(Fraction(1, 5)))
+    s, clipped = orc.clip_scale(np.array([3.0, 4.0], np.float32), 5.0)
+    assert not clipped and s == 1.0
+
+
+@pytest.mark.parametrize("n", [1, 2, 4095, 4096, 4097, 12289, 50_000])
+def test_sumsq_close_to_exact_sum(orc, n):
+    rng = np.random.default_rng(n)
+    g = (rng.standard_normal(n) * 10.0 ** rng.integers(-3, 3, n)).astype(np.float32)
+    exact = sum(Fraction(float(x)) ** 2 for x in g)
+    S = orc.sumsq(g)
+    assert abs(Fraction(S) - exact) <= exact * Fraction(n, 2**52)
+
+
+def test_sumsq_exact_on_integers(orc):
+    g = np.ones(4096 * 3 + 5, np.float32)
+    assert orc.sumsq(g) == g.size
+    g = np.arange(-2000, 2001, dtype=np.float32)
+    assert orc.sumsq(g) == sum(int(x) ** 2 for x in range(-2000, 2001))
+
+
+def test_clip_within_bound_is_bitwise_noop(orc):
+    rng = np.random.default_rng(21)
+    n = 9000
+    off = np.array([0, 100, 5000, n])
+    g, u, v = (_nonzero_normal(rng, n, 1e-3) for _ in range(3))
+    outs = []
+    for c in (0.0, 1e6):
+        uu, vv = u.copy(), v.copy()
+        idx, val, _ = orc.compress(g, uu, vv, off, orc.make_params(orc.EXACT, 0.99, 0.9,
+                                                                    clip_norm=c))
+        outs.append((idx.tolist(), val.tobytes(), uu.tobytes(), vv.tobytes()))
+    assert outs[0] == outs[1]
+
+
+def test_clipped_gradient_has_norm_c(orc):
+    # With momentum 0, sparsity 0 and masking, the sent values are the clipped gradient itself.
+    rng = np.random.default_rng(22)
+    n = 20_000
+    off = np.array([0, 7000, n])
+    g = _nonzero_normal(rng, n)
+    u = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    idx, val, st = orc.compress(g, u, v, off, orc.make_params(orc.EXACT, 0.0, 0.0, clip_norm=2.5))
+    for s, (a, b) in enumerate(zip(off[:-1], off[1:])):
+        norm = math.sqrt(sum(float(x) ** 2 for x in val[a:b]))
+        assert abs(norm - 2.5) / 2.5 < 1e-6
+        assert X.bits(val[a]) == X.bits(X.mul_f32(g[a], st[s]["clip_scale"]))
+
+
+# ---------------------------------------------------------------------------------- sampled
+def _expected_sampled(vn, off, sparsity, ratio, factor, seed):
+    d = 1 - Fraction(str(sparsity))
+    out, info = [], []
+    for s, (a, b) in enumerate(zip(off[:-1], off[1:])):
+        ns = int(b - a)
+        k = math.ceil(ns * d)
+        if k == 0:
+            info.append((0, 0, 0))
+            continue
+        ms = math.ceil(ns * Fraction(str(ratio)))
+        ks = math.ceil(ms * d)
+        seg_seed = sm_outputs(seed, s + 1)[-1]
+        pos = [(x * ns) >> 64 for x in sm_outputs(seg_seed, ms)]
+        keys = sorted((X.key(vn[a + p]) for p in pos), reverse=True)
+        t = keys[ks - 1]
+        C = [i for i in range(ns) if X.key(vn[a + i]) >= t]
+        resel = len(C) * 10**9 > round(factor * 10**9) * k
+        S = brute_topk(vn[a:b], k, among=C) if resel else C
+        out += [int(a) + i for i in S]
+        info.append((t, len(C), int(resel)))
+    return out, info
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_sampled_compress_matches_definition(orc, seed):
+    rng = np.random.default_rng(3000 + seed)
+    n = int(rng.integers(200, 3000))
+    off = _random_segments(rng, n, 3)
+    kind = [0, 1, 3][seed % 3]  # kind 1 and 3: many ties -> |C| >> k -> re-selection
+    g, u, v = (_tricky(rng, n, kind) for _ in range(3))
+    m = np.float32(0.9)
+    sparsity = float(rng.choice([0.5, 0.9, 0.99, 0.999]))
+    ratio = float(rng.choice([0.01, 0.05, 0.2]))
+    rseed = int(rng.integers(0, 2**63))
+    un, vn = _exact_accumulate(g, u, v, m)
+    exp_idx, info = _expected_sampled(vn, off, sparsity, ratio, 1.3, rseed)
+    p = orc.make_params(orc.SAMPLED, sparsity, 0.9, sample_ratio=ratio, reselect_factor=1.3,
+                        seed=rseed)
+    uu, vv = u.copy(), v.copy()
+    idx, val, st = orc.compress(g, uu, vv, off, p)
+    assert idx.tolist() == exp_idx
+    for s, (t, nc, resel) in enumerate(info):
+        if st[s]["k"]:
+            assert (st[s]["sample_key"], st[s]["candidates"], st[s]["reselected"]) == (t, nc, resel)
+
+
+def test_sampled_reselect_equals_exact_selection(orc):
+    # When re-selection runs, C holds every entry with |v| >= t and more than k of them, so the
+    # exact top-k over C is the exact top-k of the whole segment.
+    rng = np.random.default_rng(5)
+    n = 20_000
+    g = rng.integers(-2, 3, n).astype(np.float32)  # heavy ties -> |C| >> k
+    u = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    off = np.array([0, n])
+    ps = orc.make_params(orc.SAMPLED, 0.999, 0.9, sample_ratio=0.01, seed=1)
+    pe = orc.make_params(orc.EXACT, 0.999, 0.9)
+    i1, v1, st = orc.compress(g, u.copy(), v.copy(), off, ps)
+    i2, v2, _ = orc.compress(g, u.copy(), v.copy(), off, pe)
+    assert st[0]["reselected"] == 1
+    assert i1.tolist() == i2.tolist() and v1.tobytes() == v2.tobytes()
+
+
+# ---------------------------------------------------------------------------------- codec
+def golden_message(name):
+    n, entries, tokens, size = None, [], [], None
+    for tag, vals in read_golden(name):
+        if tag == "n":
+            n = vals[0]
+        elif tag == "entry":
+            entries.append(vals)
+        elif tag == "token":
+            tokens.append(vals)
+        elif tag == "size":
+            size = vals[0]
+    T = len(tokens)
+    msg = struct.pack("<4sHHQQQ", b"DGC1", 1, 0, n, T, len(entries))
+    msg += b"".join(struct.pack("<I", t[1]) for t in tokens)
+    msg += b"".join(struct.pack("<H", t[0]) for t in tokens)
+    msg += b"\0" * ((-len(msg)) % 4)
+    idx = np.array([e[0] for e in entries], np.uint32)
+    val = np.array([e[1] for e in entries], np.uint32).view(np.float32)
+    return n, idx, val, msg, size
+
+
+@pytest.mark.parametrize("name", ["codec_gaps.txt", "codec_single.txt", "codec_odd.txt",
+                                  "codec_empty.txt"])
+def test_codec_golden(orc, name):
+    n, idx, val, msg, size = golden_message(name)
+    assert len(msg) == size
+    assert orc.encode(idx, val, n) == msg
+    rc, dense = orc.decode_accumulate([msg], n)
+    assert rc == 0
+    exp = np.zeros(n, np.float32)
+    exp[idx] = exp[idx] + val  # +0 + x: a sent -0.0 lands as +0.0
+    assert dense.view(np.uint32).tolist() == exp.view(np.uint32).tolist()
+
+
+def test_decode_order_golden(orc):
+    rows = read_golden("decode_order.txt")
+    n = rows[0][1][0]
+    msgs = [orc.encode(np.array([r[1][0]], np.uint32),
+                       np.array([r[1][1]], np.uint32).view(np.float32), n)
+            for r in rows if r[0] == "learner"]
+    rc, dense = orc.decode_accumulate(msgs, n)
+    assert rc == 0
+    for tag, (pos, b) in ((t, v) for t, v in rows if t == "expect"):
+        assert X.bits(dense[pos]) == b
+
+
+def _walk_positions(msg):
+    n, T, nnz = struct.unpack_from("<QQQ", msg, 8)
+    runs = struct.unpack_from(f"<{T}H", msg, 32 + 4 * T)
+    pos, out = -1, []
+    for r in runs:
+        if r == 0xFFFF:
+            pos += 0xFFFF
+        else:
+            pos += r + 1
+            out.append(pos)
+    return out
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_codec_roundtrip_random(orc, seed):
+    rng = np.random.default_rng(700 + seed)
+    n = int(rng.integers(1, 2_000_000))
+    k = int(rng.integers(0, min(n, 3000) + 1))
+    idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+    val = _tricky(rng, k, seed % 4)
+    msg = orc.encode(idx, val, n)
+    assert _walk_positions(msg) == idx.tolist()  # the format is a bijection on (idx, val)
+    gaps = np.diff(np.concatenate([[-1], idx.astype(np.int64)])) - 1
+    T = k + int((gaps // 65535).sum())
+    assert len(msg) == 32 + 6 * T + (2 if T % 2 else 0)
+    rc, dense = orc.decode_accumulate([msg], n)
+    assert rc == 0
+    exp = np.zeros(n, np.float32)
+    exp[idx] += val
+    assert np.array_equal(dense.view(np.uint32), exp.view(np.uint32))
+
+
+def test_decode_sums_learners_in_order(orc):
+    rng = np.random.default_rng(31)
+    n, W = 5000, 7
+    msgs, parts = [], []
+    for _ in range(W):
+        idx = np.sort(rng.choice(n, size=400, replace=False)).astype(np.uint32)
+        val = (rng.standard_normal(400) * 10.0 ** rng.integers(-4, 4, 400)).astype(np.float32)
+        msgs.append(orc.encode(idx, val, n))
+        parts.append((idx, val))
+    base = rng.standard_normal(n).astype(np.float32)
+    for acc in (False, True):
+        exp = base.copy() if acc else np.zeros(n, np.float32)
+        for idx, val in parts:
+            exp[idx] = exp[idx] + val  # numpy binary32 addition, one rounding each
+        rc, dense = orc.decode_accumulate(msgs, n, dense=base, accumulate=acc)
+        assert rc == 0
+        assert np.array_equal(dense.view(np.uint32), exp.view(np.uint32))
+
+
+def test_decode_rejects_malformed(orc):
+    n = 1000
+    good = orc.encode(np.array([5, 999], np.uint32), np.array([1.0, 2.0], np.float32), n)
+    bad = [b"XGC1" + good[4:], good[:4] + struct.pack("<H", 2) + good[6:],
+           good[:8] + struct.pack("<Q", n + 1) + good[16:], good + b"\0\0\0\0", good[:31],
+           good[:32 + 8] + struct.pack("<H", 999) + good[32 + 10:]]  # second run past n
+    for b in bad:
+        base = np.full(n, 7.0, np.float32)
+        rc, dense = orc.decode_accumulate([good, b], n, dense=base, accumulate=True)
+        assert rc == orc.ECORRUPT
+        assert np.all(dense == 7.0)
+
+
+# ------------------------------------------------------------- fixed summation order (clipping)
+# The reading fixes the order of the binary64 sum of squares: tiles of 4096 entries from the
+# segment start, each summed in halves recursively, then the tile sums left to right. The
+# inputs below are powers of two whose partial sums round differently under any other order;
+# the expected values are worked out by hand (2^54 has spacing 4 between binary64 neighbours,
+# so 2^54 + 2 is a tie that rounds to the even 2^54).
+def _sparse(n, items):
+    g = np.zeros(n, np.float32)
+    for i, x in items:
+        g[i] = x
+    return g
+
+
+def test_sumsq_pairwise_inside_a_tile(orc):
+    # halves: (2^54 + 0 + 0 + 0) + (1 + 1 + 1 + 1) = 2^54 + 4 exactly; a running sum would
+    # drop each 1 and return 2^54.
+    g = _sparse(8, [(0, 2.0**27), (4, 1.0), (5, 1.0), (6, 1.0), (7, 1.0)])
+    assert orc.sumsq(g) == 2.0**54 + 4
+
+
+def test_sumsq_tiles_are_4096_long(orc):
+    # tile 0 = 2^54, tile 1 = 1+1+1+1 = 4 (summed inside the tile) -> 2^54 + 4. Tiles of 2048
+    # would add 2 and 2 to the running total one at a time and return 2^54.
+    g = _sparse(8192, [(0, 2.0**27), (4096, 1.0), (4097, 1.0), (6144, 1.0), (6145, 1.0)])
+    assert orc.sumsq(g) == 2.0**54 + 4
+
+
+def test_sumsq_tile_sums_left_to_right(orc):
+    # tiles 2^54, 0, 2, 2 added left to right: 2^54 + 2 rounds to 2^54 twice -> 2^54.
+    g = _sparse(16384, [(0, 2.0**27), (8192, 1.0), (8193, 1.0), (12288, 1.0), (12289, 1.0)])
+    assert orc.sumsq(g) == 2.0**54
+
+
+def test_reselect_not_taken_at_exactly_factor_times_k(orc):
+    # |C| = 13 = 1.3 * 10 is not more than 1.3k: C is sent as it is (13 entries, no re-selection).
+    n, big = 100, np.float32(5.0)
+    g = np.ones(n, np.float32)
+    g[np.arange(13) * 7] = big
+    off = np.array([0, n])
+    for seed in range(200):
+        exp_idx, info = _expected_sampled(g, off, 0.9, 1.0, 1.3, seed)
+        if info[0][1] == 13:
+            break
+    else:
+        pytest.fail("no seed gives |C| = 13")
+    assert info[0][2] == 0 and len(exp_idx) == 13
+    u = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    idx, _, st = orc.compress(g, u, v, off, orc.make_params(orc.SAMPLED, 0.9, 0.0,
+                                                             sample_ratio=1.0, seed=seed))
+    assert idx.tolist() == exp_idx
+    assert st[0]["candidates"] == 13 and st[0]["reselected"] == 0
