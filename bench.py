@@ -1,0 +1,445 @@
+#!/usr/bin/env python3
+"""Throughput of the DGC per-worker compressor on GB300: GB/s of fp32 gradient per step.
+
+A step is one pass of the whole hot path over a fresh synthetic gradient: dgc_compress
+(momentum-corrected accumulation, sampled 1% threshold with hierarchical re-selection, index-
+ordered compaction, masking) -> dgc_encode (32-bit values + 16-bit zero runs) ->
+dgc_decode_accumulate of the message into a dense gradient. The workload is the 2^30-entry
+(4 GiB) flat bucket: g ~ N(0, 1e-4) with 0.01% fixed outliers x100, momentum 0.9, 99.9%
+sparsity; the warm-up steps follow the warm-up schedule 75% -> 93.75% -> 98.4375% -> 99.6%.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank compresses its own bucket on its own GPU (independent replicas,
+no collective on the data path); rank 0 prints one JSON line with the max time over ranks.
+`--impl reference` times the oracle (the plain CPU restatement used by the tests) on the host on
+a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GB/s of fp32 gradient compressed (+% of HBM roofline), 1×GB300, 99.9% sparsity"
+UNIT = "GB/s"
+WORKLOAD = ("flat bucket of 2^30 fp32 entries (4 GiB), g ~ N(0, 1e-4) with 0.01% fixed "
+            "outliers x100; sampled 1% threshold, re-select if |C| > 1.3k; 99.9% sparsity; "
+            "compress + encode + decode per step")
+SEED = 20240
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=4)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--n", type=int, default=1 << 30)
+    ap.add_argument("--pool", type=int, default=3, help="distinct gradients cycled on device")
+    ap.add_argument("--e2e-steps", type=int, default=12)
+    ap.add_argument("--cpu-n", type=int, default=1 << 26)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ ranks and aggregation
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest x over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
+# ------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ---------------------------------------------------------------------- roofline inputs
+def measured_peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def stream_pass_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("compress.cu", "dgc_device.cuh"):
+        with open(os.path.join(ROOT, "sparsified_gradient_compression_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(n: int):
+    """DRAM bytes per launch of the streaming pass from the committed ncu summary, scaled to n
+    entries; None when the summary is missing or the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "stream_pass_sampled_traffic.txt")
+    try:
+        kv = {}
+        for line in open(path):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("source_sha256_16") != stream_pass_source_hash():
+            return None
+        per_entry = float(kv["dram_bytes_per_launch"]) / float(kv["entries_per_launch"])
+        return per_entry * n
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- our arm
+class Pipeline:
+    """Buffers for one worker's step on one GPU, and the step itself (public API calls only)."""
+
+    def __init__(self, n, params, dev):
+        import torch
+
+        import sparsified_gradient_compression_gb300 as dgc
+
+        self.dgc, self.n, self.dev = dgc, n, dev
+        self.seg = torch.tensor([0, n], dtype=torch.int64, device=dev)
+        self.cap = max(dgc.dgc_compress_max_out(n, 1, p) for p in params)
+        self.ws_bytes = max(dgc.dgc_compress_workspace(n, 1, p) for p in params)
+        self.u = torch.zeros(n, dtype=torch.float32, device=dev)
+        self.v = torch.zeros(n, dtype=torch.float32, device=dev)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.out_idx = torch.empty(self.cap, dtype=torch.int32, device=dev)
+        self.out_val = torch.empty(self.cap, dtype=torch.float32, device=dev)
+        self.out_count = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.stats = torch.zeros(dgc.STATS_BYTES, dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.msg_cap = dgc.dgc_encode_max_bytes(self.cap, n)
+        self.msg = torch.empty(self.msg_cap, dtype=torch.uint8, device=dev)
+        self.msg_bytes = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.ews_bytes = dgc.dgc_encode_workspace(self.cap)
+        self.ews = torch.empty(self.ews_bytes, dtype=torch.uint8, device=dev)
+        t_max = (self.msg_cap - 34) // 6  # the largest message the decoder may see
+        self.dws_bytes = dgc.dgc_decode_workspace([32 + 6 * t_max + (2 if t_max % 2 else 0)], n)
+        self.dws = torch.empty(self.dws_bytes, dtype=torch.uint8, device=dev)
+        self.dense = torch.empty(n, dtype=torch.float32, device=dev)
+        self.nb_host = torch.zeros(1, dtype=torch.int64, pin_memory=True)
+
+    def step(self, g, p, ev=None):
+        dgc = self.dgc
+        if ev:
+            ev[0].record()
+        dgc.dgc_compress(g, self.u, self.v, self.seg, p, self.out_idx, self.out_val,
+                         self.out_count, self.stats, self.status, self.ws, n=self.n,
+                         out_cap=self.cap, ws_bytes=self.ws_bytes)
+        if ev:
+            ev[1].record()
+        dgc.dgc_encode(self.out_idx, self.out_val, self.out_count, self.n, self.msg,
+                       self.msg_bytes, self.status, self.ews, max_count=self.cap,
+                       out_cap=self.msg_cap, ws_bytes=self.ews_bytes)
+        if ev:
+            ev[2].record()
+        self.nb_host.copy_(self.msg_bytes)  # the decoder takes message sizes on the host
+        nb = int(self.nb_host.item())
+        dgc.dgc_decode_accumulate([self.msg], [nb], self.dense, self.n, False, self.status,
+                                  self.dws, ws_bytes=self.dws_bytes)
+        if ev:
+            ev[3].record()
+        return nb
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import sparsified_gradient_compression_gb300 as dgc
+    import workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    dgc.build()
+    n = args.n
+    sched = list(workloads.WARMUP_SPARSITY[:4])
+    params = [dgc.make_params(mode=dgc.SELECT_SAMPLED, sparsity=s, momentum=0.9,
+                              sample_ratio=0.01, reselect_factor=1.3, seed=SEED + rank)
+              for s in sched + [0.999]]
+    p_main = params[-1]
+    pipe = Pipeline(n, params, dev)
+    # inputs resident in HBM: a pool of distinct gradients, one per step in turn
+    pool = []
+    for i in range(args.pool):
+        pool.append(torch.from_numpy(workloads.gradient("bucket1g", step=i, seed=rank, n=n)).to(dev))
+
+    for i in range(args.warmup):  # the warm-up schedule, then 99.9%
+        pipe.step(pool[i % len(pool)], params[min(i, len(params) - 1)])
+    torch.cuda.synchronize()
+    if dgc.dgc_read_status(pipe.status) != 0:
+        raise RuntimeError("warm-up steps reported an error")
+
+    K = args.steps
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    evs = [(E(), E(), E(), E()) for _ in range(K)]
+    kev = [(E(), E()) for _ in range(K)]
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_id)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = dgc.dgc_launch_count()
+    t_begin, t_end = E(), E()
+    t_begin.record()
+    nbytes = []
+    for i in range(K):
+        dgc.dgc_profile_stream_pass(kev[i][0], kev[i][1])
+        nbytes.append(pipe.step(pool[(args.warmup + i) % len(pool)], p_main, evs[i]))
+    t_end.record()
+    torch.cuda.synchronize()
+    dgc.dgc_profile_stream_pass(None, None)
+    launches = dgc.dgc_launch_count() - launches0
+    clk = clocks.stop()
+    barrier()
+    if dgc.dgc_read_status(pipe.status) != 0:
+        raise RuntimeError("timed steps reported an error")
+    sec = t_begin.elapsed_time(t_end) / 1e3
+    sec_max = max_over_ranks(sec, dev)
+    value = whole_job_value(4.0 * n * K, world, sec_max) / 1e9
+    t_compress = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    t_encode = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+    t_decode = sum(e[2].elapsed_time(e[3]) for e in evs) / K
+    t_kernel = sum(a.elapsed_time(b) for a, b in kev) / K
+    st = np.frombuffer(pipe.stats.cpu().numpy().tobytes(), dtype=[
+        ("k", "<u8"), ("candidates", "<u8"), ("sent", "<u8"), ("thresh_key", "<u4"),
+        ("sample_key", "<u4"), ("reselected", "<u4"), ("clip_scale", "<f4")])[0]
+    cand = int(st["candidates"])
+    alg_bytes = 20.0 * n + 12.0 * cand  # read g,u,v + write u,v; one (idx, v, u) per candidate
+    peak, peak_kind = measured_peak_hbm()
+    achieved = alg_bytes / (t_kernel / 1e3) / 1e9
+    traffic = recorded_traffic(n)
+
+    e2e = None if args.no_e2e else run_e2e(args, pipe, pool, p_main, K)
+    cpu = None
+    if not args.no_cpu and rank == 0 and world == 1:
+        cpu = run_cpu_baseline(args.cpu_n, steps=3)
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(sec_max * 1e3 / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; see workloads/)",
+        "config": {"workload": WORKLOAD, "n": n, "sparsity": 0.999, "k": int(st["k"]),
+                   "momentum": 0.9, "sample_ratio": 0.01, "reselect_factor": 1.3,
+                   "segments": 1, "l2": f"inputs larger than L2 ({4 * n >> 20} MiB per array; "
+                   f"{len(pool)} distinct gradients cycled)",
+                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "k_stream<1> (sampled accumulate + compact)",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None if traffic is None else round(traffic),
+                     "alg_bytes": alg_bytes, "kernel_ms": round(t_kernel, 4)},
+        "stages_ms": {"compress": round(t_compress, 4), "encode": round(t_encode, 4),
+                      "decode": round(t_decode, 4)},
+        "compress_gbs": round(4.0 * n / (t_compress / 1e3) / 1e9, 2),
+        "message_bytes": int(statistics.median(nbytes)),
+        "candidates": cand, "sent": int(st["sent"]),
+        "gpu_launches": int(launches), "clocks": clk,
+        "e2e": e2e, "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_e2e(args, pipe, pool, p, K_dev):
+    """The same step through the public API with host buffers: each step copies its gradient
+    from pinned host memory to the device and reads the encoded message back to the host."""
+    import torch
+
+    n, dev = pipe.n, pipe.dev
+    K = max(1, min(args.e2e_steps, K_dev))
+    hosts = []
+    for i in range(2):
+        h = torch.empty(n, dtype=torch.float32, pin_memory=True)
+        h.copy_(pool[i % len(pool)])
+        hosts.append(h)
+    g_dev = torch.empty(n, dtype=torch.float32, device=dev)
+    back = torch.empty(pipe.msg_cap, dtype=torch.uint8, pin_memory=True)
+    for i in range(2):
+        g_dev.copy_(hosts[i], non_blocking=True)
+        pipe.step(g_dev, p)
+    torch.cuda.synchronize()
+    d2h = 0
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(K):
+        g_dev.copy_(hosts[i % 2], non_blocking=True)
+        nb = pipe.step(g_dev, p)
+        back[:nb].copy_(pipe.msg[:nb], non_blocking=True)
+        d2h += nb + 8  # the message and its size
+    b.record()
+    torch.cuda.synchronize()
+    sec = a.elapsed_time(b) / 1e3
+    return {"value": round(4.0 * n * K / sec / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": int(d2h / K), "steps": K}
+
+
+# ------------------------------------------------------------------ CPU baseline / reference
+def run_cpu_baseline(n_cpu: int, steps: int):
+    """The oracle, single-threaded on one host core, on a bounded sample of the workload:
+    an n_cpu-entry bucket with the same recipe (one untimed step, then `steps` timed steps of
+    compress + encode + decode at 99.9%)."""
+    import numpy as np
+
+    import oracle
+    import workloads
+
+    p = oracle.make_params(oracle.SAMPLED, 0.999, 0.9, sample_ratio=0.01, reselect_factor=1.3,
+                           seed=SEED)
+    off = np.array([0, n_cpu], np.int64)
+    u = np.zeros(n_cpu, np.float32)
+    v = np.zeros(n_cpu, np.float32)
+    gs = [workloads.gradient("bucket1g", step=i, seed=0, n=n_cpu) for i in range(2)]
+    idx, val, _ = oracle.compress(gs[0], u, v, off, p)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        idx, val, _ = oracle.compress(gs[(i + 1) % 2], u, v, off, p)
+        m = oracle.encode(idx, val, n_cpu)
+        oracle.decode_accumulate([m], n_cpu)
+    sec = time.perf_counter() - t0
+    return {"value": round(4.0 * n_cpu * steps / sec / 1e9, 4), "unit": UNIT, "cores": 1,
+            "kind": "oracle", "seconds": round(sec, 2),
+            "sample": f"{n_cpu}-entry bucket of the same recipe, {steps} timed steps of "
+                      "compress+encode+decode at 99.9% after one untimed step"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    steps = max(1, args.steps)
+    # keep the whole run to a few minutes: about 40 ns per entry per step on one core
+    n_ref = 1 << 26
+    while n_ref > (1 << 16) and steps * n_ref * 40e-9 > 120:
+        n_ref >>= 1
+    cpu = run_cpu_baseline(n_ref, steps)
+    out = {"impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": UNIT,
+           "n_gpus": world, "steps": steps, "warmup": args.warmup,
+           "ms_per_step": round(cpu["seconds"] * 1e3 / steps, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic (seeded; see workloads/)",
+           "config": {"workload": WORKLOAD, "n": n_ref, "sample_of_n": args.n},
+           "cpu_baseline": cpu,
+           "e2e": {"value": cpu["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return 0
+    run_ours(args, world, rank, local)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,189 @@
+/*
+ * dgc.h -- C ABI of libdgc: the per-worker gradient compressor of Deep Gradient Compression
+ * (DGC) with AdaComp-style residual sparsification, its sparse message codec, and the
+ * decode-and-sum aggregator, as CUDA kernels for NVIDIA GB300 (sm_103a).
+ *
+ * Sources, by page title and section:
+ *   [DGC] "[Paper Review] Deep Gradient Compression: Reducing the Communication Bandwidth for
+ *         Distributed Training": Abstract, Motivation & Objective, Proposed method (six
+ *         bullets), Research questions (RQ4), Key findings.
+ *   [ADA] "AdaComp : Adaptive Residual Gradient Compression for Data-Parallel Distributed
+ *         Training": abstract and citation snippets.
+ *
+ * Conventions for every call:
+ *   - All array arguments are DEVICE pointers unless marked "host". The caller owns every
+ *     buffer; the library allocates no device memory and frees none.
+ *   - Work is enqueued on `stream` (a cudaStream_t; 0 is the legacy default stream). No call
+ *     synchronizes with the device except dgc_read_status.
+ *   - The return value reports errors that can be seen on the host before anything is
+ *     enqueued (DGC_EINVAL, DGC_EUNSUPPORTED, DGC_ECORRUPT for malformed sizes, DGC_ECUDA for a
+ *     failed launch); on such an error nothing is enqueued and no buffer is touched.
+ *   - Errors that only the device can see are written to `*status` (an int32 in device
+ *     memory): the first error wins and the library never clears it, so zero it before a
+ *     sequence of calls and read it with dgc_read_status.
+ *   - Scratch memory is the caller's `ws` buffer of at least the bytes the matching
+ *     *_workspace query returns (256-byte aligned). A call may overwrite all of it; calls that
+ *     share one workspace must be ordered (same stream, or synchronized).
+ *   - Indices are uint32: n must be below 2^32.
+ */
+#ifndef DGC_H
+#define DGC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dgc_stream_t; /* the same type as cudaStream_t */
+
+enum {
+    DGC_OK = 0,
+    DGC_EINVAL = -1,       /* bad argument or segment table */
+    DGC_ECAPACITY = -2,    /* an output buffer is too small */
+    DGC_ECUDA = -3,        /* a CUDA call failed */
+    DGC_ETIMEOUT = -4,     /* a bounded device-side wait gave up (results of the call invalid) */
+    DGC_ECORRUPT = -5,     /* a message is malformed */
+    DGC_EUNSUPPORTED = -6  /* a size the library does not handle (n >= 2^32) */
+};
+
+enum { DGC_SELECT_EXACT = 0, DGC_SELECT_SAMPLED = 1 };
+enum { DGC_FLAG_MASK_MOMENTUM = 1u };
+
+/* Compressor settings. [DGC] Proposed method: momentum correction (momentum), local gradient
+ * clipping (clip_norm), momentum factor masking (DGC_FLAG_MASK_MOMENTUM); [DGC] Abstract:
+ * 99.9% sparsity; [DGC] RQ4: hierarchical thresholding (sample_ratio, reselect_factor). */
+typedef struct {
+    uint32_t mode;          /* DGC_SELECT_EXACT or DGC_SELECT_SAMPLED */
+    uint32_t flags;         /* DGC_FLAG_MASK_MOMENTUM: clear u where a value is sent */
+    double sparsity;        /* fraction of each segment NOT sent, in [0, 1] */
+    float momentum;         /* m in u <- m*u + g (finite) */
+    float clip_norm;        /* per-segment L2 bound on g; <= 0 or +inf disables clipping */
+    double sample_ratio;    /* sampled mode: fraction of each segment sampled, in (0, 1] */
+    double reselect_factor; /* sampled mode: exact re-selection when |C| > factor*k, in [1,16] */
+    uint64_t seed;          /* sampled mode: seed of the sample positions */
+} dgc_params;
+
+/* Per-segment statistics of one dgc_compress call. */
+typedef struct {
+    uint64_t k;          /* ceil(n_s * (1 - sparsity)) */
+    uint64_t candidates; /* sampled: |C| = #{i : |v_i| >= t}; exact: |S| */
+    uint64_t sent;       /* |S| */
+    uint32_t thresh_key; /* smallest |v| key (bits & 0x7FFFFFFF) among sent entries, or
+                            0xFFFFFFFF when nothing was sent */
+    uint32_t sample_key; /* sampled: the threshold key t; exact: 0 */
+    uint32_t reselected; /* sampled: 1 if the exact re-selection ran */
+    float clip_scale;    /* factor applied to g (1 when not clipped) */
+} dgc_seg_stats;
+
+/* ------------------------------------------------------------------------- compressor */
+
+/* Bytes of workspace dgc_compress needs for n entries in nseg segments. */
+int dgc_compress_workspace(int64_t n, int32_t nseg, const dgc_params* params, size_t* bytes);
+
+/* Upper bound on the number of (index, value) pairs one dgc_compress call can emit; out_cap
+ * must be at least this. Exact mode: sum of k; sampled mode: the re-selection rule bounds
+ * |S| by reselect_factor * k per segment. */
+int dgc_compress_max_out(int64_t n, int32_t nseg, const dgc_params* params, int64_t* max_out);
+
+/* One compressor step over a flat buffer holding nseg segments (tensors), each compressed on
+ * its own. [DGC] Proposed method, bullets 1 and 3-5; [DGC] RQ4; [ADA] abstract.
+ *   1. k_s = ceil(n_s * (1 - sparsity)) per segment (integer arithmetic in parts per billion).
+ *   2. If 0 < clip_norm < inf: scale_s = clip_norm / ||g_s|| when ||g_s|| > clip_norm (the
+ *      squared norm summed in binary64 in a fixed order: 4096-entry tiles from the segment
+ *      start, each summed in halves recursively, tile sums added left to right).
+ *   3. u <- fma(m, u, g * scale); v <- v + u (binary32, round to nearest).
+ *   4. S = the k_s largest |v| (ties to the lower index) in exact mode; in sampled mode
+ *      t = the k_s'-th largest |v| among m_s = ceil(n_s * sample_ratio) positions drawn with
+ *      SplitMix64 (seed), C = {|v| >= t}, and S = exact top-k_s of C when
+ *      |C| > reselect_factor * k_s, else S = C.
+ *   5. out_idx/out_val receive (i, v_i) for i in S in ascending i (segments in order), then
+ *      v_i <- 0 and, with DGC_FLAG_MASK_MOMENTUM, u_i <- 0.
+ * Arguments:
+ *   g        device, n binary32, 16-byte aligned, read only (the fresh gradient)
+ *   u, v     device, n binary32 each, 16-byte aligned, updated in place (momentum, residual)
+ *   seg_off  device, nseg+1 int64: seg_off[0] = 0, seg_off[nseg] = n, non-decreasing (empty
+ *            segments allowed). Checked on the device: a bad table sets *status = DGC_EINVAL
+ *            and leaves every buffer but out_count and stats untouched.
+ *   out_idx  device, out_cap uint32; out_val device, out_cap binary32; out_cap must be at
+ *            least dgc_compress_max_out (else DGC_ECAPACITY is returned).
+ *   out_count device, one int64: |S| summed over segments.
+ *   stats    device, nseg dgc_seg_stats, or NULL.
+ *   status   device, one int32 (see conventions).
+ *   ws       device workspace, ws_bytes >= dgc_compress_workspace(...).
+ * Every result is deterministic: the same inputs give the same bits on every run. */
+int dgc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* seg_off,
+                 int32_t nseg, const dgc_params* params, uint32_t* out_idx, float* out_val,
+                 int64_t out_cap, int64_t* out_count, dgc_seg_stats* stats, int32_t* status,
+                 void* ws, size_t ws_bytes, dgc_stream_t stream);
+
+/* ------------------------------------------------------------------------------ codec */
+
+/* Message format, [DGC] Proposed method, bullet 2 (each sent value a 32-bit word, each run of
+ * zeros before it a 16-bit length); the byte layout is this library's reading:
+ *   bytes 0..31: "DGC1", u16 version = 1, u16 flags = 0, u64 n, u64 T, u64 nnz (little-endian)
+ *   then T binary32 values, then T u16 runs, then zero bytes up to a multiple of 4.
+ * Entry j skips r = idx_j - idx_{j-1} - 1 zeros (idx_{-1} = -1); a skip of 65535 or more is
+ * written as escape tokens (run 0xFFFF, value bits 0; each skips 65535 zeros and places no
+ * value) followed by the entry's token with the remainder. Size = 32 + 6T (+2 when T is odd). */
+
+/* Largest message dgc_encode can produce for at most max_count entries of an n-vector. */
+int dgc_encode_max_bytes(int64_t max_count, int64_t n, uint64_t* bytes);
+
+/* Bytes of workspace dgc_encode needs. */
+int dgc_encode_workspace(int64_t max_count, size_t* bytes);
+
+/* Encode count (device int64, at most max_count) ascending indices idx (device uint32) with
+ * values val (device binary32) of an n-vector into out (device, out_cap bytes, 16-byte
+ * aligned). *out_bytes (device u64) receives the message size. Indices that are not strictly
+ * ascending or not below n set *status = DGC_EINVAL; a message larger than out_cap sets
+ * DGC_ECAPACITY (*out_bytes still receives the size; out is not written). */
+int dgc_encode(const uint32_t* idx, const float* val, const int64_t* count, int64_t max_count,
+               int64_t n, uint8_t* out, uint64_t out_cap, uint64_t* out_bytes, int32_t* status,
+               void* ws, size_t ws_bytes, dgc_stream_t stream);
+
+/* ---------------------------------------------------------------------------- decoder */
+
+/* Bytes of workspace dgc_decode_accumulate needs for W messages of the given sizes (host). */
+int dgc_decode_workspace(int32_t W, const uint64_t* stream_bytes, int64_t n, size_t* bytes);
+
+/* Decode W messages and sum them into dense (device, n binary32): synchronous SGD adds up
+ * every learner's update ([DGC] Abstract, Motivation). The sum runs in learner order 0..W-1,
+ * one binary32 addition per received value, onto +0 (accumulate = 0) or onto dense's current
+ * contents (accumulate = 1), so the result is bitwise deterministic.
+ *   streams       host array of W device pointers (16-byte aligned)
+ *   stream_bytes  host array of W sizes; a size that no message can have returns DGC_ECORRUPT
+ * A message whose header (magic, version, n, T) or runs (a position at or past n) are wrong
+ * sets *status = DGC_ECORRUPT and is skipped; nothing is written outside dense[0, n). */
+int dgc_decode_accumulate(const uint8_t* const* streams, const uint64_t* stream_bytes,
+                          int32_t W, float* dense, int64_t n, int32_t accumulate,
+                          int32_t* status, void* ws, size_t ws_bytes, dgc_stream_t stream);
+
+/* -------------------------------------------------------------------------- utilities */
+
+/* Synchronize `stream`, then return the int32 at status_dev (or DGC_ECUDA). */
+int dgc_read_status(const int32_t* status_dev, dgc_stream_t stream);
+
+/* Static text for a status code. */
+const char* dgc_status_string(int code);
+
+/* Number of kernels this library has launched in this process (all calls, all threads). */
+uint64_t dgc_launch_count(void);
+
+/* Profiling hook for benchmarks: while begin and end are non-NULL, every dgc_compress call
+ * records `begin` on its stream right before its streaming pass (the accumulate-and-compact
+ * kernel that touches all n entries) and `end` right after it. dgc_profile_stream_pass(NULL,
+ * NULL) turns it off. The setting is process-wide and not synchronized between threads. */
+typedef struct CUevent_st* dgc_event_t; /* the same type as cudaEvent_t */
+void dgc_profile_stream_pass(dgc_event_t begin, dgc_event_t end);
+
+/* Self-test of the bounded device-side wait used by every cross-block scan: launches one
+ * block that waits on a flag nothing ever sets, with at most spin_limit polls, and must come
+ * back with *status = DGC_ETIMEOUT. Returns the launch status. */
+int dgc_selftest_wait_timeout(int32_t* status, uint32_t spin_limit, dgc_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DGC_H */

@@ -1,0 +1,245 @@
+"""Python binding of libdgc, the GB300 (sm_103a) DGC gradient compressor.
+
+Argument marshalling only: every function below has the name of a C entry point declared in
+``include/dgc.h``, turns torch tensors into device pointers, passes the current CUDA stream, and
+raises :class:`DGCError` when the C call returns a nonzero status. All arithmetic runs in the
+CUDA kernels of ``libdgc.so``; there is no CPU path. If the library has not been built, loading
+it fails with an error that says so (call :func:`build`).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB, build
+
+__all__ = [
+    "DGCError", "build", "lib", "dgc_params", "dgc_seg_stats", "make_params",
+    "dgc_compress_workspace", "dgc_compress_max_out", "dgc_compress",
+    "dgc_encode_max_bytes", "dgc_encode_workspace", "dgc_encode",
+    "dgc_decode_workspace", "dgc_decode_accumulate",
+    "dgc_read_status", "dgc_status_string", "dgc_launch_count", "dgc_selftest_wait_timeout",
+    "dgc_profile_stream_pass",
+    "SELECT_EXACT", "SELECT_SAMPLED", "FLAG_MASK_MOMENTUM",
+]
+
+OK, EINVAL, ECAPACITY, ECUDA, ETIMEOUT, ECORRUPT, EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+SELECT_EXACT, SELECT_SAMPLED = 0, 1
+FLAG_MASK_MOMENTUM = 1
+
+
+class dgc_params(ctypes.Structure):
+    _fields_ = [
+        ("mode", ctypes.c_uint32),
+        ("flags", ctypes.c_uint32),
+        ("sparsity", ctypes.c_double),
+        ("momentum", ctypes.c_float),
+        ("clip_norm", ctypes.c_float),
+        ("sample_ratio", ctypes.c_double),
+        ("reselect_factor", ctypes.c_double),
+        ("seed", ctypes.c_uint64),
+    ]
+
+
+class dgc_seg_stats(ctypes.Structure):
+    _fields_ = [
+        ("k", ctypes.c_uint64),
+        ("candidates", ctypes.c_uint64),
+        ("sent", ctypes.c_uint64),
+        ("thresh_key", ctypes.c_uint32),
+        ("sample_key", ctypes.c_uint32),
+        ("reselected", ctypes.c_uint32),
+        ("clip_scale", ctypes.c_float),
+    ]
+
+
+STATS_BYTES = ctypes.sizeof(dgc_seg_stats)
+
+
+class DGCError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {_status_text(code)} ({code})")
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libdgc.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"libdgc.so is not built ({LIB}); run "
+                               "sparsified_gradient_compression_gb300.build()")
+        L = ctypes.CDLL(LIB)
+        i32, i64, u32, u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64
+        vp, sz = ctypes.c_void_p, ctypes.c_size_t
+        P = ctypes.POINTER
+        L.dgc_compress_workspace.argtypes = [i64, i32, P(dgc_params), P(sz)]
+        L.dgc_compress_max_out.argtypes = [i64, i32, P(dgc_params), P(i64)]
+        L.dgc_compress.argtypes = [vp, vp, vp, i64, vp, i32, P(dgc_params), vp, vp, i64, vp, vp,
+                                   vp, vp, sz, vp]
+        L.dgc_encode_max_bytes.argtypes = [i64, i64, P(u64)]
+        L.dgc_encode_workspace.argtypes = [i64, P(sz)]
+        L.dgc_encode.argtypes = [vp, vp, vp, i64, i64, vp, u64, vp, vp, vp, sz, vp]
+        L.dgc_decode_workspace.argtypes = [i32, vp, i64, P(sz)]
+        L.dgc_decode_accumulate.argtypes = [vp, vp, i32, vp, i64, i32, vp, vp, sz, vp]
+        L.dgc_read_status.argtypes = [vp, vp]
+        L.dgc_status_string.argtypes = [ctypes.c_int]
+        L.dgc_status_string.restype = ctypes.c_char_p
+        L.dgc_launch_count.argtypes = []
+        L.dgc_launch_count.restype = u64
+        L.dgc_selftest_wait_timeout.argtypes = [vp, u32, vp]
+        L.dgc_profile_stream_pass.argtypes = [vp, vp]
+        L.dgc_profile_stream_pass.restype = None
+        for f in ("dgc_compress_workspace", "dgc_compress_max_out", "dgc_compress",
+                  "dgc_encode_max_bytes", "dgc_encode_workspace", "dgc_encode",
+                  "dgc_decode_workspace", "dgc_decode_accumulate", "dgc_read_status",
+                  "dgc_selftest_wait_timeout"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _status_text(code: int) -> str:
+    try:
+        return lib().dgc_status_string(int(code)).decode()
+    except Exception:  # the library itself failed to load
+        return "status"
+
+
+def _check(rc: int, where: str) -> int:
+    if rc != OK:
+        raise DGCError(rc, where)
+    return rc
+
+
+def _ptr(t) -> int | None:
+    """Device (or host) address of a tensor, or an int address passed through."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_params(mode=SELECT_EXACT, sparsity=0.999, momentum=0.9, clip_norm=0.0,
+                mask_momentum=True, sample_ratio=0.01, reselect_factor=1.3, seed=0) -> dgc_params:
+    return dgc_params(int(mode), FLAG_MASK_MOMENTUM if mask_momentum else 0, float(sparsity),
+                      float(momentum), float(clip_norm), float(sample_ratio),
+                      float(reselect_factor), int(seed) & (2**64 - 1))
+
+
+# --------------------------------------------------------------------------- compressor
+def dgc_compress_workspace(n: int, nseg: int, params: dgc_params) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().dgc_compress_workspace(int(n), int(nseg), ctypes.byref(params),
+                                        ctypes.byref(out)), "dgc_compress_workspace")
+    return out.value
+
+
+def dgc_compress_max_out(n: int, nseg: int, params: dgc_params) -> int:
+    out = ctypes.c_int64(0)
+    _check(lib().dgc_compress_max_out(int(n), int(nseg), ctypes.byref(params), ctypes.byref(out)),
+           "dgc_compress_max_out")
+    return out.value
+
+
+def dgc_compress(g, u, v, seg_off, params: dgc_params, out_idx, out_val, out_count, stats,
+                 status, ws, n: int | None = None, out_cap: int | None = None,
+                 ws_bytes: int | None = None, stream=None) -> int:
+    """g, u, v: float32 CUDA tensors of n entries; seg_off: int64 CUDA tensor (nseg+1);
+    out_idx (int32/uint32), out_val (float32): CUDA tensors of out_cap entries; out_count: int64
+    CUDA tensor (1); stats: uint8 CUDA tensor of nseg * STATS_BYTES or None; status: int32 CUDA
+    tensor (1); ws: uint8 CUDA tensor."""
+    n = g.numel() if n is None else n
+    nseg = seg_off.numel() - 1 if hasattr(seg_off, "numel") else None
+    out_cap = out_idx.numel() if out_cap is None else out_cap
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    return _check(lib().dgc_compress(_ptr(g), _ptr(u), _ptr(v), int(n), _ptr(seg_off), int(nseg),
+                                     ctypes.byref(params), _ptr(out_idx), _ptr(out_val),
+                                     int(out_cap), _ptr(out_count), _ptr(stats), _ptr(status),
+                                     _ptr(ws), int(ws_bytes), _stream(stream)), "dgc_compress")
+
+
+# -------------------------------------------------------------------------------- codec
+def dgc_encode_max_bytes(max_count: int, n: int) -> int:
+    out = ctypes.c_uint64(0)
+    _check(lib().dgc_encode_max_bytes(int(max_count), int(n), ctypes.byref(out)),
+           "dgc_encode_max_bytes")
+    return out.value
+
+
+def dgc_encode_workspace(max_count: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().dgc_encode_workspace(int(max_count), ctypes.byref(out)), "dgc_encode_workspace")
+    return out.value
+
+
+def dgc_encode(idx, val, count, n: int, out, out_bytes, status, ws, max_count: int | None = None,
+               out_cap: int | None = None, ws_bytes: int | None = None, stream=None) -> int:
+    max_count = idx.numel() if max_count is None else max_count
+    out_cap = out.numel() * out.element_size() if out_cap is None else out_cap
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    return _check(lib().dgc_encode(_ptr(idx), _ptr(val), _ptr(count), int(max_count), int(n),
+                                   _ptr(out), int(out_cap), _ptr(out_bytes), _ptr(status),
+                                   _ptr(ws), int(ws_bytes), _stream(stream)), "dgc_encode")
+
+
+def dgc_decode_workspace(stream_bytes, n: int) -> int:
+    W = len(stream_bytes)
+    arr = (ctypes.c_uint64 * max(W, 1))(*[int(b) for b in stream_bytes])
+    out = ctypes.c_size_t(0)
+    _check(lib().dgc_decode_workspace(W, ctypes.cast(arr, ctypes.c_void_p), int(n),
+                                      ctypes.byref(out)), "dgc_decode_workspace")
+    return out.value
+
+
+def dgc_decode_accumulate(streams, stream_bytes, dense, n: int, accumulate: bool, status, ws,
+                          ws_bytes: int | None = None, stream=None) -> int:
+    """streams: list of device addresses or uint8 CUDA tensors; stream_bytes: list of sizes."""
+    W = len(stream_bytes)
+    ptrs = (ctypes.c_void_p * max(W, 1))(*[_ptr(s) for s in streams])
+    sizes = (ctypes.c_uint64 * max(W, 1))(*[int(b) for b in stream_bytes])
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    return _check(lib().dgc_decode_accumulate(ctypes.cast(ptrs, ctypes.c_void_p),
+                                              ctypes.cast(sizes, ctypes.c_void_p), W,
+                                              _ptr(dense), int(n), int(bool(accumulate)),
+                                              _ptr(status), _ptr(ws), int(ws_bytes),
+                                              _stream(stream)), "dgc_decode_accumulate")
+
+
+# ----------------------------------------------------------------------------- utilities
+def dgc_read_status(status, stream=None) -> int:
+    return int(lib().dgc_read_status(_ptr(status), _stream(stream)))
+
+
+def dgc_status_string(code: int) -> str:
+    return lib().dgc_status_string(int(code)).decode()
+
+
+def dgc_launch_count() -> int:
+    return int(lib().dgc_launch_count())
+
+
+def dgc_profile_stream_pass(begin, end) -> None:
+    """begin/end: torch.cuda.Event objects (created with enable_timing=True), or None."""
+    b = None if begin is None else begin.cuda_event
+    e = None if end is None else end.cuda_event
+    lib().dgc_profile_stream_pass(b, e)
+
+
+def dgc_selftest_wait_timeout(status, spin_limit: int, stream=None) -> int:
+    return _check(lib().dgc_selftest_wait_timeout(_ptr(status), int(spin_limit), _stream(stream)),
+                  "dgc_selftest_wait_timeout")

@@ -1,0 +1,518 @@
+// codec.cu -- dgc_encode and dgc_decode_accumulate on sm_103a.
+//
+// Source: "[Paper Review] Deep Gradient Compression: Reducing the Communication Bandwidth for
+// Distributed Training", Proposed method, bullet 2 (each sent value as a 32-bit word and the
+// run of zeros before it as a 16-bit length), and Abstract / Motivation (synchronous SGD adds
+// up the learners' updates). Byte layout (this library's reading): 32-byte header
+// ("DGC1", u16 version 1, u16 flags 0, u64 n, u64 T, u64 nnz), T binary32 values, T u16 runs,
+// zero pad to a multiple of 4; a run of 0xFFFF is an escape that skips 65535 zeros.
+//
+// Encode: reduce-then-scan over the (ascending) entries. Block b owns a contiguous share; pass
+// 1 counts its tokens (1 + gap/65535 per entry), one block scans the G totals and writes the
+// header, pass 2 writes values and runs at their final offsets.
+//
+// Decode: pass 1 turns each message's runs into positions with a prefix sum over 2048-token
+// chunks (decoupled look-back inside each message) and records, for every 4096-entry tile of
+// the dense output, the first token of each message at or past the tile. Pass 2 gives each
+// tile to one block: it gathers the tile's tokens of all messages into shared memory, adds them
+// in message order 0..W-1 into a shared-memory copy of the tile, and writes the tile once. Each
+// dense entry is therefore written exactly once and summed in a fixed order.
+#include <vector>
+
+#include "dgc_device.cuh"
+
+namespace dgc {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kEncBlocks = 512;
+constexpr int kEncPer = 4;
+constexpr int kDecChunk = 2048;  // tokens per position chunk (8 per thread)
+constexpr int kDecTile = 4096;   // dense entries per output tile
+constexpr int kDecCap = 1024;    // tokens staged in shared memory at a time
+constexpr uint32_t kEscPos = 0xFFFFFFFFu;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ------------------------------------------------------------------------------ encode
+struct EncCtl {
+    int32_t abort;
+    uint32_t pad;
+    uint64_t T;
+};
+
+struct EncArgs {
+    const uint32_t* idx;
+    const float* val;
+    const int64_t* count;
+    uint64_t max_count;
+    uint64_t n;
+    uint8_t* out;
+    uint64_t out_cap;
+    uint64_t* out_bytes;
+    int32_t* status;
+    EncCtl* ctl;
+    uint64_t* tot;  // per-block token counts, then exclusive offsets
+};
+
+__device__ __forceinline__ bool enc_range(const EncArgs& a, uint64_t* lo, uint64_t* hi,
+                                          uint64_t* cnt) {
+    const int64_t c = *a.count;
+    if (c < 0 || (uint64_t)c > a.max_count) return false;
+    *cnt = (uint64_t)c;
+    const uint64_t per = ((uint64_t)c + gridDim.x - 1) / gridDim.x;
+    *lo = umin64((uint64_t)c, (uint64_t)blockIdx.x * per);
+    *hi = umin64((uint64_t)c, *lo + per);
+    return true;
+}
+
+__device__ __forceinline__ uint64_t enc_tokens(const EncArgs& a, uint64_t j, bool* bad) {
+    const int64_t cur = a.idx[j];
+    const int64_t prev = j ? (int64_t)a.idx[j - 1] : -1;
+    if ((uint64_t)cur >= a.n || cur <= prev) {
+        *bad = true;
+        return 1;
+    }
+    return 1 + (uint64_t)(cur - prev - 1) / kRunEscape;
+}
+
+__global__ void __launch_bounds__(kThreads) k_enc_count(EncArgs a) {
+    __shared__ uint64_t s_scan[33];
+    __shared__ int s_bad;
+    uint64_t lo, hi, cnt;
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    if (!enc_range(a, &lo, &hi, &cnt)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            report(a.status, DGC_EINVAL);
+            a.ctl->abort = 1;
+        }
+        return;
+    }
+    uint64_t t = 0;
+    bool bad = false;
+    for (uint64_t j = lo + threadIdx.x; j < hi; j += kThreads) t += enc_tokens(a, j, &bad);
+    if (bad) s_bad = 1;
+    uint64_t total;
+    block_excl_scan<kThreads>(t, s_scan, &total);
+    if (threadIdx.x == 0) {
+        a.tot[blockIdx.x] = total;
+        if (s_bad) {
+            report(a.status, DGC_EINVAL);
+            a.ctl->abort = 1;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(1024) k_enc_scan(EncArgs a, int nblocks) {
+    __shared__ uint64_t s_scan[33];
+    if (a.ctl->abort) {
+        if (threadIdx.x == 0) *a.out_bytes = 0;
+        return;
+    }
+    const uint64_t x = threadIdx.x < nblocks ? a.tot[threadIdx.x] : 0;
+    uint64_t T;
+    const uint64_t ex = block_excl_scan<1024>(x, s_scan, &T);
+    if (threadIdx.x < nblocks) a.tot[threadIdx.x] = ex;
+    if (threadIdx.x != 0) return;
+    const uint64_t bytes = 32 + 6 * T + ((T & 1) ? 2 : 0);
+    *a.out_bytes = bytes;
+    if (bytes > a.out_cap) {
+        report(a.status, DGC_ECAPACITY);
+        a.ctl->abort = 1;
+        return;
+    }
+    a.ctl->T = T;
+    uint64_t* h = reinterpret_cast<uint64_t*>(a.out);
+    h[0] = (uint64_t)kMagic | (1ull << 32);  // magic, version 1, flags 0
+    h[1] = a.n;
+    h[2] = T;
+    h[3] = (uint64_t)*a.count;
+    if (T & 1) *reinterpret_cast<uint16_t*>(a.out + 32 + 6 * T) = 0;
+}
+
+__global__ void __launch_bounds__(kThreads) k_enc_write(EncArgs a) {
+    __shared__ uint64_t s_scan[33];
+    if (a.ctl->abort) return;
+    uint64_t lo, hi, cnt;
+    if (!enc_range(a, &lo, &hi, &cnt)) return;
+    const uint64_t T = a.ctl->T;
+    uint32_t* vals = reinterpret_cast<uint32_t*>(a.out + 32);
+    uint16_t* runs = reinterpret_cast<uint16_t*>(a.out + 32 + 4 * T);
+    uint64_t carry = a.tot[blockIdx.x];
+    for (uint64_t c = lo; c < hi; c += (uint64_t)kThreads * kEncPer) {
+        uint64_t tk[kEncPer];
+        uint64_t mine = 0;
+        bool bad = false;
+#pragma unroll
+        for (int e = 0; e < kEncPer; ++e) {
+            const uint64_t j = c + (uint64_t)threadIdx.x * kEncPer + e;
+            tk[e] = (j < hi) ? enc_tokens(a, j, &bad) : 0;
+            mine += tk[e];
+        }
+        uint64_t total;
+        uint64_t p = carry + block_excl_scan<kThreads>(mine, s_scan, &total);
+#pragma unroll
+        for (int e = 0; e < kEncPer; ++e) {
+            const uint64_t j = c + (uint64_t)threadIdx.x * kEncPer + e;
+            if (j >= hi) break;
+            const int64_t prev = j ? (int64_t)a.idx[j - 1] : -1;
+            const uint64_t gap = (uint64_t)((int64_t)a.idx[j] - prev - 1);
+            for (uint64_t x = 1; x < tk[e]; ++x, ++p) {
+                vals[p] = 0u;
+                runs[p] = (uint16_t)kRunEscape;
+            }
+            vals[p] = __float_as_uint(a.val[j]);
+            runs[p] = (uint16_t)(gap % kRunEscape);
+            ++p;
+        }
+        carry += total;
+    }
+}
+
+// ------------------------------------------------------------------------------ decode
+struct DecStream {
+    const uint8_t* ptr;
+    uint64_t T;
+    uint64_t tok_base;
+    uint64_t chunk_base;
+};
+
+struct DecCtl {
+    uint32_t ticket;
+    uint32_t any_bad;
+};
+
+struct DecArgs {
+    const DecStream* tab;  // W + 1 entries (the last holds the totals)
+    int32_t W;
+    uint64_t n;
+    float* dense;
+    int32_t accumulate;
+    int32_t* status;
+    DecCtl* ctl;
+    uint32_t* bad;
+    uint32_t* pos;
+    uint64_t* st;
+    uint32_t* ts;  // (ntiles + 1) x W first-token table
+    uint64_t ntiles;
+    uint64_t nchunks;
+    uint32_t spin_limit;
+};
+
+__device__ __forceinline__ void mark_bad(const DecArgs& a, int w) {
+    a.bad[w] = 1;
+    atomicExch(&a.ctl->any_bad, 1u);
+    report(a.status, DGC_ECORRUPT);
+}
+
+// Zeroes the look-back words and checks every header (ctl was zeroed before this kernel).
+__global__ void k_dec_init(DecArgs a) {
+    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = tid; i <= a.nchunks; i += stride) a.st[i] = 0;
+    for (uint64_t w = tid; w < (uint64_t)a.W; w += stride) {
+        const DecStream d = a.tab[w];
+        const uint64_t* h = reinterpret_cast<const uint64_t*>(d.ptr);
+        const uint64_t h0 = h[0];
+        a.bad[w] = 0;
+        if ((uint32_t)h0 != kMagic || ((h0 >> 32) & 0xFFFFu) != 1u || h[1] != a.n || h[2] != d.T)
+            mark_bad(a, (int)w);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) k_dec_pos(DecArgs a) {
+    __shared__ uint64_t s_scan[33];
+    __shared__ uint32_t s_chunk;
+    __shared__ uint64_t s_base;
+    if (threadIdx.x == 0) s_chunk = atomicAdd(&a.ctl->ticket, 1u);
+    __syncthreads();
+    const uint64_t c = s_chunk;
+    // the message that owns chunk c
+    int lo = 0, hi = a.W;
+    while (hi - lo > 1) {  // the last message starting at or before c (empty ones own nothing)
+        const int mid = (lo + hi) >> 1;
+        if (a.tab[mid].chunk_base <= c) lo = mid; else hi = mid;
+    }
+    const int w = lo;
+    const DecStream d = a.tab[w];
+    const uint64_t lc = c - d.chunk_base;
+    const uint64_t tok0 = lc * kDecChunk;
+    const uint64_t tok1 = umin64(d.T, tok0 + kDecChunk);
+    const uint16_t* runs = reinterpret_cast<const uint16_t*>(d.ptr + 32 + 4 * d.T);
+    constexpr int kPer = kDecChunk / kThreads;
+    uint32_t adv[kPer];
+    uint64_t mine = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const uint64_t j = tok0 + (uint64_t)threadIdx.x * kPer + i;
+        adv[i] = 0;
+        if (j < tok1) {
+            const uint32_t r = runs[j];
+            adv[i] = (r == kRunEscape) ? kRunEscape : r + 1;
+        }
+        mine += adv[i];
+    }
+    uint64_t agg;
+    const uint64_t ex = block_excl_scan<kThreads>(mine, s_scan, &agg);
+    if (threadIdx.x < 32) {
+        uint64_t base = 0;
+        if (lc == 0) {
+            if (threadIdx.x == 0) st_relaxed(&a.st[c], kFlagInc | agg);
+        } else {
+            base = lookback_exclusive(a.st, (uint32_t)c, agg, a.spin_limit, a.status, nullptr);
+        }
+        if (threadIdx.x == 0) s_base = base;
+    }
+    __syncthreads();
+    uint64_t P = s_base + ex;  // advances before this thread's first token
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const uint64_t j = tok0 + (uint64_t)threadIdx.x * kPer + i;
+        if (j >= tok1) break;
+        const int64_t prev = (int64_t)P - 1;  // position of the previous token
+        P += adv[i];
+        const int64_t p = (int64_t)P - 1;
+        if ((uint64_t)p >= a.n) bad = true;
+        a.pos[d.tok_base + j] = (runs[j] == kRunEscape) ? kEscPos : (uint32_t)p;
+        // tiles whose first token of this message is j
+        int64_t t0 = (prev < 0) ? 0 : prev / kDecTile + 1;
+        int64_t t1 = p / kDecTile;
+        if (t1 > (int64_t)a.ntiles) t1 = (int64_t)a.ntiles;
+        for (int64_t t = t0; t <= t1; ++t) a.ts[(uint64_t)t * a.W + w] = (uint32_t)j;
+        if (j == d.T - 1)
+            for (int64_t t = p / kDecTile + 1; t <= (int64_t)a.ntiles; ++t)
+                a.ts[(uint64_t)t * a.W + w] = (uint32_t)d.T;
+    }
+    if (bad) mark_bad(a, w);
+}
+
+__global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
+    __shared__ float s_acc[kDecTile];
+    __shared__ uint32_t s_pos[kDecCap];
+    __shared__ float s_val[kDecCap];
+    __shared__ uint32_t s_off[kThreads + 1];
+    __shared__ uint32_t s_first[kThreads];
+    __shared__ uint64_t s_scan[33];
+    if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
+    const uint64_t t = blockIdx.x;
+    const uint64_t p0 = t * kDecTile;
+    const uint32_t len = (uint32_t)umin64(kDecTile, a.n - p0);
+    for (uint32_t i = threadIdx.x; i < kDecTile; i += kThreads)
+        s_acc[i] = (a.accumulate && i < len) ? a.dense[p0 + i] : 0.0f;
+    for (int wb = 0; wb < a.W; wb += kThreads) {
+        const int w = wb + threadIdx.x;
+        uint32_t cnt = 0, first = 0;
+        if (w < a.W && a.tab[w].T > 0) {
+            first = a.ts[t * a.W + w];
+            cnt = a.ts[(t + 1) * a.W + w] - first;
+        }
+        uint64_t total;
+        const uint64_t ex = block_excl_scan<kThreads>((uint64_t)cnt, s_scan, &total);
+        s_off[threadIdx.x] = (uint32_t)ex;
+        s_first[threadIdx.x] = first;
+        if (threadIdx.x == 0) s_off[kThreads] = (uint32_t)total;
+        __syncthreads();
+        const int nw = min(kThreads, a.W - wb);
+        for (uint32_t r0 = 0; r0 < total; r0 += kDecCap) {
+            const uint32_t m = (uint32_t)umin64(kDecCap, total - r0);
+            for (uint32_t i = threadIdx.x; i < m; i += kThreads) {
+                const uint32_t f = r0 + i;
+                int l = 0, h = nw;  // message of flattened token f
+                while (h - l > 1) {
+                    const int mid = (l + h) >> 1;
+                    if (s_off[mid] <= f) l = mid; else h = mid;
+                }
+                const DecStream& d = a.tab[wb + l];
+                const uint64_t j = s_first[l] + (f - s_off[l]);
+                s_pos[i] = a.pos[d.tok_base + j];
+                s_val[i] = reinterpret_cast<const float*>(d.ptr + 32)[j];
+            }
+            __syncthreads();
+            if (threadIdx.x < 32) {
+                for (int l = 0; l < nw; ++l) {
+                    const uint32_t lo = max(s_off[l], r0), hi = min(s_off[l + 1], r0 + m);
+                    for (uint32_t i = lo + threadIdx.x; i < hi; i += 32) {
+                        const uint32_t p = s_pos[i - r0];
+                        if (p != kEscPos && p >= p0 && p < p0 + len)
+                            s_acc[p - p0] = __fadd_rn(s_acc[p - p0], s_val[i - r0]);
+                    }
+                    __syncwarp();
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (uint32_t i = threadIdx.x; i < len; i += kThreads) a.dense[p0 + i] = s_acc[i];
+}
+
+struct DecLayout {
+    size_t ctl, tab, bad, pos, st, ts, total;
+    uint64_t sum_T, nchunks, ntiles;
+};
+
+bool stream_tokens(uint64_t bytes, uint64_t* T) {
+    if (bytes < 32) return false;
+    const uint64_t t = (bytes - 32) / 6;
+    if (32 + 6 * t + ((t & 1) ? 2 : 0) != bytes) return false;
+    *T = t;
+    return true;
+}
+
+int dec_layout(int32_t W, const uint64_t* stream_bytes, int64_t n, DecLayout* L,
+               std::vector<DecStream>* tab) {
+    L->sum_T = 0;
+    L->nchunks = 0;
+    for (int w = 0; w < W; ++w) {
+        uint64_t T;
+        if (!stream_tokens(stream_bytes[w], &T)) return DGC_ECORRUPT;
+        if (tab) (*tab)[w] = DecStream{nullptr, T, L->sum_T, L->nchunks};
+        L->sum_T += T;
+        L->nchunks += (T + kDecChunk - 1) / kDecChunk;
+    }
+    if (tab) (*tab)[W] = DecStream{nullptr, 0, L->sum_T, L->nchunks};
+    L->ntiles = ((uint64_t)n + kDecTile - 1) / kDecTile;
+    size_t o = 0;
+    auto take = [&](size_t b) { size_t at = o; o = align256(o + b); return at; };
+    L->ctl = take(sizeof(DecCtl));
+    L->tab = take(sizeof(DecStream) * (size_t)(W + 1));
+    L->bad = take(sizeof(uint32_t) * (size_t)(W > 0 ? W : 1));
+    L->pos = take(sizeof(uint32_t) * (size_t)L->sum_T);
+    L->st = take(sizeof(uint64_t) * (size_t)(L->nchunks + 1));
+    L->ts = take(sizeof(uint32_t) * (size_t)(L->ntiles + 1) * (size_t)(W > 0 ? W : 1));
+    L->total = o;
+    return DGC_OK;
+}
+
+}  // namespace
+}  // namespace dgc
+
+using namespace dgc;
+
+extern "C" int dgc_encode_max_bytes(int64_t max_count, int64_t n, uint64_t* bytes) {
+    if (!bytes || max_count < 0 || n < 0) return DGC_EINVAL;
+    if (n > 0xFFFFFFFFll) return DGC_EUNSUPPORTED;
+    const uint64_t T = (uint64_t)max_count + (uint64_t)n / kRunEscape;
+    *bytes = 32 + 6 * T + 2;
+    return DGC_OK;
+}
+
+extern "C" int dgc_encode_workspace(int64_t max_count, size_t* bytes) {
+    if (!bytes || max_count < 0) return DGC_EINVAL;
+    *bytes = align256(sizeof(EncCtl)) + align256(sizeof(uint64_t) * kEncBlocks);
+    return DGC_OK;
+}
+
+extern "C" int dgc_encode(const uint32_t* idx, const float* val, const int64_t* count,
+                          int64_t max_count, int64_t n, uint8_t* out, uint64_t out_cap,
+                          uint64_t* out_bytes, int32_t* status, void* ws, size_t ws_bytes,
+                          dgc_stream_t stream) {
+    if (max_count < 0 || n < 0) return DGC_EINVAL;
+    if (n > 0xFFFFFFFFll || max_count > 0xFFFFFFFFll) return DGC_EUNSUPPORTED;
+    if (!count || !out || !out_bytes || !status || !ws) return DGC_EINVAL;
+    if (max_count > 0 && (!idx || !val)) return DGC_EINVAL;
+    if (((uintptr_t)out & 15u) != 0 || ((uintptr_t)ws & 255u) != 0) return DGC_EINVAL;
+    size_t need;
+    dgc_encode_workspace(max_count, &need);
+    if (ws_bytes < need) return DGC_EINVAL;
+    EncArgs a{};
+    a.idx = idx;
+    a.val = val;
+    a.count = count;
+    a.max_count = (uint64_t)max_count;
+    a.n = (uint64_t)n;
+    a.out = out;
+    a.out_cap = out_cap;
+    a.out_bytes = out_bytes;
+    a.status = status;
+    char* w = static_cast<char*>(ws);
+    a.ctl = reinterpret_cast<EncCtl*>(w);
+    a.tot = reinterpret_cast<uint64_t*>(w + align256(sizeof(EncCtl)));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(a.ctl, 0, sizeof(EncCtl), s) != cudaSuccess) return DGC_ECUDA;
+    const int sms = dgc_internal_sm_count();
+    if (sms <= 0) return DGC_ECUDA;
+    const int G = std::min(kEncBlocks, 2 * sms);
+    k_enc_count<<<G, kThreads, 0, s>>>(a);
+    k_enc_scan<<<1, 1024, 0, s>>>(a, G);
+    k_enc_write<<<G, kThreads, 0, s>>>(a);
+    dgc_internal_count_launches(3);
+    if (cudaPeekAtLastError() != cudaSuccess) {
+        cudaGetLastError();
+        return DGC_ECUDA;
+    }
+    return DGC_OK;
+}
+
+extern "C" int dgc_decode_workspace(int32_t W, const uint64_t* stream_bytes, int64_t n,
+                                    size_t* bytes) {
+    if (!bytes || W < 0 || n < 0 || (W > 0 && !stream_bytes)) return DGC_EINVAL;
+    if (n > 0xFFFFFFFFll) return DGC_EUNSUPPORTED;
+    DecLayout L;
+    const int rc = dec_layout(W, stream_bytes, n, &L, nullptr);
+    if (rc) return rc;
+    *bytes = L.total;
+    return DGC_OK;
+}
+
+extern "C" int dgc_decode_accumulate(const uint8_t* const* streams, const uint64_t* stream_bytes,
+                                     int32_t W, float* dense, int64_t n, int32_t accumulate,
+                                     int32_t* status, void* ws, size_t ws_bytes,
+                                     dgc_stream_t stream) {
+    if (W < 0 || n < 0) return DGC_EINVAL;
+    if (n > 0xFFFFFFFFll) return DGC_EUNSUPPORTED;
+    if (W > 0 && (!streams || !stream_bytes)) return DGC_EINVAL;
+    if (!status || !ws || (n > 0 && !dense)) return DGC_EINVAL;
+    if (((uintptr_t)ws & 255u) != 0) return DGC_EINVAL;
+    for (int w = 0; w < W; ++w)
+        if (!streams[w] || ((uintptr_t)streams[w] & 15u) != 0) return DGC_EINVAL;
+    std::vector<DecStream> tab((size_t)W + 1);
+    DecLayout L;
+    int rc = dec_layout(W, stream_bytes, n, &L, &tab);
+    if (rc) return rc;
+    if (L.sum_T > 0xFFFFFFFFull) return DGC_EUNSUPPORTED;
+    if (ws_bytes < L.total) return DGC_EINVAL;
+    for (int w = 0; w < W; ++w) tab[w].ptr = streams[w];
+    char* p = static_cast<char*>(ws);
+    DecArgs a{};
+    a.tab = reinterpret_cast<const DecStream*>(p + L.tab);
+    a.W = W;
+    a.n = (uint64_t)n;
+    a.dense = dense;
+    a.accumulate = accumulate ? 1 : 0;
+    a.status = status;
+    a.ctl = reinterpret_cast<DecCtl*>(p + L.ctl);
+    a.bad = reinterpret_cast<uint32_t*>(p + L.bad);
+    a.pos = reinterpret_cast<uint32_t*>(p + L.pos);
+    a.st = reinterpret_cast<uint64_t*>(p + L.st);
+    a.ts = reinterpret_cast<uint32_t*>(p + L.ts);
+    a.ntiles = L.ntiles;
+    a.nchunks = L.nchunks;
+    a.spin_limit = kDefaultSpinLimit;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the table of messages goes to the device with the call (a pageable copy: staged before
+    // this function returns, so the host vector may go away)
+    if (cudaMemcpyAsync(p + L.tab, tab.data(), sizeof(DecStream) * tab.size(),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return DGC_ECUDA;
+    if (cudaMemsetAsync(p + L.ctl, 0, sizeof(DecCtl), s) != cudaSuccess) return DGC_ECUDA;
+    uint64_t launches = 0;
+    const uint64_t init_work = std::max<uint64_t>(L.nchunks + 1, (uint64_t)W);
+    k_dec_init<<<(unsigned)std::min<uint64_t>((init_work + 255) / 256, 1024), 256, 0, s>>>(a);
+    ++launches;
+    if (L.nchunks > 0) {
+        k_dec_pos<<<(unsigned)L.nchunks, kThreads, 0, s>>>(a);
+        ++launches;
+    }
+    if (L.ntiles > 0) {
+        k_dec_tiles<<<(unsigned)L.ntiles, kThreads, 0, s>>>(a);
+        ++launches;
+    }
+    dgc_internal_count_launches(launches);
+    if (cudaPeekAtLastError() != cudaSuccess) {
+        cudaGetLastError();
+        return DGC_ECUDA;
+    }
+    return DGC_OK;
+}

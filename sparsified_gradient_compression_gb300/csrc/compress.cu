@@ -1,0 +1,1086 @@
+// compress.cu -- dgc_compress: the DGC per-worker compressor on sm_103a.
+//
+// Sources: "[Paper Review] Deep Gradient Compression: Reducing the Communication Bandwidth for
+// Distributed Training" (Abstract; Proposed method bullets 1, 3, 4, 5; Research questions RQ4)
+// and "AdaComp : Adaptive Residual Gradient Compression for Data-Parallel Distributed
+// Training" (abstract; citation snippets on magnitude selection).
+//
+// One call enqueues this pipeline on the caller's stream (every kernel reads the segment table
+// and counters the previous ones left in the workspace, so no host round trip is needed):
+//
+//   plan          segment table: k, sample counts, seeds; validates seg_off; zeroes counters
+//   clip_tiles    [clipping] binary64 pairwise sum of g^2 per 4096-entry tile
+//   clip_scale    [clipping] tile sums left to right -> per-segment scale
+//   sample        gathers g,u,v at the SplitMix64 sample positions, recomputes v' there,
+//                 writes the sample keys and the first radix-select histogram
+//   find/hist x3  radix select of the sampled threshold t (11 + 10 + 10 key bits)
+//   fused         THE STREAMING PASS: u = fma(m,u,g*scale); v += u; candidates key(v) >= t
+//                 are compacted in index order through a decoupled look-back (sampled mode
+//                 also clears v,u of every candidate in the same store)
+//   candoff       per-segment candidate ranges; decides who re-selects
+//   compact_v     [exact mode, only if the sampled bound was too tight] re-compacts from v
+//   hist/find x6  radix select of the exact k-th (|v|, index) pair among candidates
+//   emit          writes S in index order (second look-back), clears v,u of sent entries
+//                 (exact) or restores those of unsent candidates (sampled); statistics
+//
+// Exact mode uses the sampled threshold only as a safe lower bound: a margin above the sample
+// rank makes |C| >= k overwhelmingly likely, and when it is not, compact_v re-reads v with a
+// zero threshold for that segment. Either way S is the exact top-k.
+#include <cmath>
+#include <cstring>
+
+#include "dgc_device.cuh"
+
+namespace dgc {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kRows = 8;                          // float4 rows per thread in the streaming pass
+constexpr int kTile = kThreads * kRows * 4;       // 8192 entries per streaming tile
+constexpr int kEmitRows = 4;
+constexpr int kEmitTile = kThreads * kEmitRows * 4;  // 4096 candidates per emit tile
+constexpr int kClipTile = 4096;
+constexpr int kHistBins = 2048;
+constexpr int kSamplePerThread = 4;
+constexpr uint64_t kExactSamplePpb = 10000000;    // exact mode samples 1% to bound t from below
+constexpr uint32_t kExactWholeBelow = 32768;      // smaller segments: every entry is a candidate
+
+// composite selection key X = (|v| key << 32) | ~index, selected from the top 11+10+10 key
+// bits then 11+11+10 index bits
+__constant__ int c_shift[6] = {52, 42, 32, 21, 10, 0};
+__constant__ int c_bits[6] = {11, 10, 10, 11, 11, 10};
+
+enum : uint32_t { kIdle = 0, kActive = 1 };
+
+struct SegInfo {
+    uint64_t seed;      // per-segment SplitMix64 seed
+    uint64_t prefix;    // radix-select prefix found so far
+    uint64_t sel_x;     // selected <=> X >= sel_x
+    uint32_t start, end;
+    uint32_t k;         // target count
+    uint32_t ms;        // sample draws (0: no sampling)
+    uint32_t rank;      // rank of the threshold among the samples
+    uint32_t thresh;    // candidate threshold key (kNoKey: none)
+    uint32_t need;      // radix select: items still to take
+    uint32_t state;     // kIdle / kActive
+    uint32_t cand_cnt;
+    uint32_t failed;    // exact mode: fewer candidates than k
+    uint32_t resel;     // sampled mode: re-selection ran
+    uint32_t min_key;
+    float scale;
+    uint32_t pad;
+};
+
+struct Ctl {
+    int32_t abort;
+    uint32_t active;
+    uint32_t any_failed;
+    uint32_t ticket_fused, ticket_compact, ticket_emit;
+    uint32_t total_samples, total_clip_tiles, total_cand, total_sent;
+    uint32_t emit_done;
+    uint32_t pad;
+};
+
+// Workspace layout (host computes it; every piece 256-byte aligned).
+struct Layout {
+    size_t ctl, segs, seg_start, samp_off, clip_off, cand_off, clip_part, skeys, histA, histB;
+    size_t st_fused, st_compact, st_emit, cidx, cval, cu, total;
+    uint64_t max_samples, max_clip_tiles, fused_tiles, emit_tiles;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct HostParams {
+    uint32_t mode, mask, clip_on;
+    uint64_t d_ppb, r_ppb, q_ppb;
+    float momentum, clip_norm;
+    uint64_t seed;
+};
+
+int check_params(const dgc_params* p, HostParams* hp) {
+    if (!p) return DGC_EINVAL;
+    if (p->mode != DGC_SELECT_EXACT && p->mode != DGC_SELECT_SAMPLED) return DGC_EINVAL;
+    if (!(p->sparsity >= 0.0 && p->sparsity <= 1.0)) return DGC_EINVAL;
+    if (!std::isfinite(p->momentum)) return DGC_EINVAL;
+    if (std::isnan(p->clip_norm)) return DGC_EINVAL;
+    hp->mode = p->mode;
+    hp->mask = (p->flags & DGC_FLAG_MASK_MOMENTUM) ? 1u : 0u;
+    hp->clip_on = (p->clip_norm > 0.0f && !std::isinf(p->clip_norm)) ? 1u : 0u;
+    hp->d_ppb = (uint64_t)llround((1.0 - p->sparsity) * 1e9);
+    hp->momentum = p->momentum;
+    hp->clip_norm = p->clip_norm;
+    hp->seed = p->seed;
+    if (p->mode == DGC_SELECT_SAMPLED) {
+        if (!(p->sample_ratio > 0.0 && p->sample_ratio <= 1.0)) return DGC_EINVAL;
+        hp->r_ppb = (uint64_t)llround(p->sample_ratio * 1e9);
+        if (hp->r_ppb == 0) return DGC_EINVAL;
+        if (!(p->reselect_factor >= 1.0 && p->reselect_factor <= 16.0)) return DGC_EINVAL;
+        hp->q_ppb = (uint64_t)llround(p->reselect_factor * 1e9);
+    } else {
+        hp->r_ppb = kExactSamplePpb;
+        hp->q_ppb = 0;
+    }
+    return DGC_OK;
+}
+
+Layout make_layout(int64_t n, int32_t nseg, const HostParams& hp) {
+    Layout L{};
+    const uint64_t un = (uint64_t)n;
+    L.max_samples = count_ppb(un, hp.r_ppb) + (uint64_t)nseg;
+    L.max_clip_tiles = hp.clip_on ? (un + kClipTile - 1) / kClipTile + (uint64_t)nseg : 0;
+    L.fused_tiles = (un + kTile - 1) / kTile;
+    L.emit_tiles = (un + kEmitTile - 1) / kEmitTile;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
+    L.ctl = take(sizeof(Ctl));
+    L.segs = take(sizeof(SegInfo) * (size_t)nseg);
+    L.seg_start = take(sizeof(uint32_t) * (size_t)(nseg + 1));
+    L.samp_off = take(sizeof(uint32_t) * (size_t)(nseg + 1));
+    L.clip_off = take(sizeof(uint32_t) * (size_t)(nseg + 1));
+    L.cand_off = take(sizeof(uint32_t) * (size_t)(nseg + 1));
+    L.clip_part = take(sizeof(double) * (size_t)L.max_clip_tiles);
+    L.skeys = take(sizeof(uint32_t) * (size_t)L.max_samples);
+    L.histA = take(sizeof(uint32_t) * (size_t)nseg * kHistBins);
+    L.histB = take(sizeof(uint32_t) * (size_t)nseg * kHistBins);
+    L.st_fused = take(sizeof(uint64_t) * (size_t)(L.fused_tiles + 1));
+    L.st_compact = take(sizeof(uint64_t) * (size_t)(L.fused_tiles + 1));
+    L.st_emit = take(sizeof(uint64_t) * (size_t)(L.emit_tiles + 1));
+    L.cidx = take(sizeof(uint32_t) * (size_t)un);
+    L.cval = take(sizeof(float) * (size_t)un);
+    L.cu = take(sizeof(float) * (size_t)un);
+    L.total = o;
+    return L;
+}
+
+uint64_t max_out_for(int64_t n, int32_t nseg, const HostParams& hp) {
+    const uint64_t un = (uint64_t)n;
+    uint64_t ksum = count_ppb(un, hp.d_ppb) + (uint64_t)nseg;  // >= sum of per-segment ceils
+    if (hp.d_ppb == 0) ksum = 0;
+    uint64_t bound = ksum;
+    if (hp.mode == DGC_SELECT_SAMPLED) {
+        // no re-selection means |C| * 1e9 <= q * k, i.e. |S| <= floor(q * k / 1e9) per segment
+        const unsigned __int128 b = (unsigned __int128)hp.q_ppb * ksum / kBillion + (uint64_t)nseg;
+        bound = b > un ? un : (uint64_t)b;
+    }
+    return bound < un ? bound : un;
+}
+
+// Everything the kernels need, passed by value.
+struct Args {
+    const float* g;
+    float* u;
+    float* v;
+    uint32_t n;
+    int32_t nseg;
+    const int64_t* seg_off;
+    HostParams hp;
+    uint32_t* out_idx;
+    float* out_val;
+    uint64_t out_cap;
+    int64_t* out_count;
+    dgc_seg_stats* stats;
+    int32_t* status;
+    Ctl* ctl;
+    SegInfo* segs;
+    uint32_t* seg_start;
+    uint32_t* samp_off;
+    uint32_t* clip_off;
+    uint32_t* cand_off;
+    double* clip_part;
+    uint32_t* skeys;
+    uint32_t* histA;
+    uint32_t* histB;
+    uint64_t* st_fused;
+    uint64_t* st_compact;
+    uint64_t* st_emit;
+    uint32_t* cidx;
+    float* cval;
+    float* cu;
+    uint64_t max_samples, fused_tiles, emit_tiles, max_clip_tiles;
+    uint32_t spin_limit;
+};
+
+// ------------------------------------------------------------------------------- plan
+// Block 0 builds the segment table; every block zeroes its share of the histograms and
+// look-back words.
+__global__ void __launch_bounds__(1024) k_plan(Args a) {
+    __shared__ uint32_t s_scan[33];
+    __shared__ uint32_t s_carry_samp, s_carry_clip;
+    __shared__ int s_bad;
+    if (blockIdx.x == 0) {
+        if (threadIdx.x == 0) {
+            s_carry_samp = 0;
+            s_carry_clip = 0;
+            s_bad = (a.seg_off[0] != 0 || a.seg_off[a.nseg] != (int64_t)a.n) ? 1 : 0;
+            Ctl c{};
+            *a.ctl = c;
+            *a.out_count = 0;
+        }
+        __syncthreads();
+        uint32_t active = 0;
+        for (int base = 0; base < a.nseg; base += 1024) {
+            const int s = base + threadIdx.x;
+            uint32_t ms = 0, clip_tiles = 0;
+            if (s < a.nseg) {
+                const int64_t lo = a.seg_off[s], hi = a.seg_off[s + 1];
+                if (hi < lo || lo < 0 || hi > (int64_t)a.n) atomicExch(&s_bad, 1);
+                const uint32_t st = (uint32_t)min(max(lo, (int64_t)0), (int64_t)a.n);
+                const uint32_t en = (uint32_t)min(max(hi, (int64_t)st), (int64_t)a.n);
+                const uint32_t ns = en - st;
+                SegInfo d{};
+                d.start = st;
+                d.end = en;
+                d.k = (uint32_t)count_ppb(ns, a.hp.d_ppb);
+                d.seed = mix64(a.hp.seed + kGolden * ((uint64_t)s + 1));
+                d.scale = 1.0f;
+                d.min_key = 0xFFFFFFFFu;
+                d.thresh = kNoKey;
+                if (d.k > 0) {
+                    if (a.hp.mode == DGC_SELECT_SAMPLED) {
+                        d.ms = (uint32_t)count_ppb(ns, a.hp.r_ppb);
+                        d.rank = (uint32_t)count_ppb(d.ms, a.hp.d_ppb);
+                    } else if (ns >= kExactWholeBelow) {
+                        const uint32_t m = (uint32_t)count_ppb(ns, a.hp.r_ppb);
+                        const uint32_t ks = (uint32_t)count_ppb(m, a.hp.d_ppb);
+                        const uint32_t margin = (uint32_t)ceilf(4.0f * sqrtf((float)ks)) + 16u;
+                        if ((uint64_t)ks + margin < m) {
+                            d.ms = m;
+                            d.rank = ks + margin;
+                        }
+                    }
+                    if (d.ms == 0) d.thresh = 0;  // exact mode, every entry a candidate
+                    if (d.ms > 0) {
+                        d.state = kActive;
+                        d.need = d.rank;
+                        ++active;
+                    }
+                }
+                ms = d.ms;
+                if (a.hp.clip_on) clip_tiles = (ns + kClipTile - 1) / kClipTile;
+                a.segs[s] = d;
+                a.seg_start[s] = st;
+            }
+            uint32_t tot;
+            const uint32_t ex = block_excl_scan<1024>(ms, s_scan, &tot);
+            if (s < a.nseg) a.samp_off[s] = s_carry_samp + ex;
+            __syncthreads();
+            if (threadIdx.x == 0) s_carry_samp += tot;
+            const uint32_t exc = block_excl_scan<1024>(clip_tiles, s_scan, &tot);
+            if (s < a.nseg) a.clip_off[s] = s_carry_clip + exc;
+            __syncthreads();
+            if (threadIdx.x == 0) s_carry_clip += tot;
+            __syncthreads();
+        }
+        active = warp_sum(active);
+        if ((threadIdx.x & 31) == 0 && active) atomicAdd(&a.ctl->active, active);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            a.samp_off[a.nseg] = s_carry_samp;
+            a.clip_off[a.nseg] = s_carry_clip;
+            a.seg_start[a.nseg] = a.n;
+            a.ctl->total_samples = s_carry_samp;
+            a.ctl->total_clip_tiles = s_carry_clip;
+            if (s_bad) {
+                a.ctl->abort = 1;
+                report(a.status, DGC_EINVAL);
+            }
+        }
+    }
+    // zero histograms and look-back words (grid-stride over all blocks)
+    const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    const size_t nh = (size_t)a.nseg * kHistBins;
+    for (size_t i = tid; i < nh; i += stride) {
+        a.histA[i] = 0;
+        a.histB[i] = 0;
+    }
+    for (size_t i = tid; i <= a.fused_tiles; i += stride) {
+        a.st_fused[i] = 0;
+        a.st_compact[i] = 0;
+    }
+    for (size_t i = tid; i <= a.emit_tiles; i += stride) a.st_emit[i] = 0;
+}
+
+// ----------------------------------------------------------------------------- clipping
+// Sum of squares of one 4096-entry tile in binary64, split in halves recursively: thread t
+// sums entries [16t, 16t+16) as a 4-level tree, lanes combine with xor-shuffles (pairs of
+// neighbouring 16-entry blocks first), then the 8 warp sums combine pairwise.
+__global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
+    __shared__ double s_w[8];
+    __shared__ int s_skip;
+    const uint32_t c = blockIdx.x;
+    if (threadIdx.x == 0) s_skip = a.ctl->abort || c >= a.ctl->total_clip_tiles;
+    __syncthreads();
+    if (s_skip) return;
+    const int s = upper_bound_minus1(a.clip_off, a.nseg, c);
+    const SegInfo& d = a.segs[s];
+    const uint64_t base = (uint64_t)d.start + (uint64_t)(c - a.clip_off[s]) * kClipTile +
+                          16u * threadIdx.x;
+    double q[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint64_t e = base + i;
+        const double x = (e < d.end) ? (double)a.g[e] : 0.0;
+        q[i] = x * x;
+    }
+#pragma unroll
+    for (int w = 1; w < 16; w <<= 1)
+#pragma unroll
+        for (int i = 0; i < 16; i += 2 * w) q[i] = q[i] + q[i + w];
+    double t = q[0];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) t = t + __shfl_xor_sync(kFull, t, o);
+    if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = t;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const double a01 = s_w[0] + s_w[1], a23 = s_w[2] + s_w[3];
+        const double a45 = s_w[4] + s_w[5], a67 = s_w[6] + s_w[7];
+        a.clip_part[c] = (a01 + a23) + (a45 + a67);
+    }
+}
+
+// Tile sums left to right; scale = c / sqrt(S) when sqrt(S) > c (binary64, correctly rounded
+// sqrt and division, rounded once to binary32).
+__global__ void k_clip_scale(Args a) {
+    const int s = blockIdx.x * blockDim.x + threadIdx.x;
+    if (a.ctl->abort || s >= a.nseg) return;
+    SegInfo& d = a.segs[s];
+    double S = 0.0;
+    for (uint32_t t = a.clip_off[s]; t < a.clip_off[s + 1]; ++t) S = S + a.clip_part[t];
+    const double norm = sqrt(S);
+    const double c = (double)a.hp.clip_norm;
+    d.scale = (norm > c) ? (float)(c / norm) : 1.0f;
+}
+
+__device__ __forceinline__ void accumulate(float g, float& u, float& v, float m, float scale) {
+    const float gp = (scale != 1.0f) ? __fmul_rn(g, scale) : g;
+    u = __fmaf_rn(m, u, gp);
+    v = __fadd_rn(v, u);
+}
+
+// ----------------------------------------------------------------------- histograms
+// Per-block histogram of one segment in shared memory, flushed to the segment's global
+// histogram when the block moves to another segment or ends.
+struct BlockHist {
+    uint32_t* s;       // kHistBins entries in shared memory
+    int cur;           // segment currently held, -1 none
+    __device__ void flush(uint32_t* ghist, int nbins) {
+        __syncthreads();
+        if (cur >= 0)
+            for (int b = threadIdx.x; b < nbins; b += blockDim.x) {
+                const uint32_t x = s[b];
+                if (x) {
+                    atomicAdd(&ghist[(size_t)cur * kHistBins + b], x);
+                    s[b] = 0;
+                }
+            }
+        __syncthreads();
+    }
+};
+
+// --------------------------------------------------------------------------- sampling
+// Sample draw j of segment s sits at start + floor(mix(seed_s + (j+1)g) * n_s / 2^64). The
+// post-accumulate value there is recomputed from the pre-step g, u, v with the same
+// operations the streaming pass uses, so it is bit-identical to what that pass will store.
+__global__ void __launch_bounds__(kThreads) k_sample(Args a) {
+    __shared__ uint32_t s_hist[kHistBins];
+    __shared__ int s_seg0, s_seg1, s_skip;
+    if (threadIdx.x == 0) s_skip = a.ctl->abort;
+    __syncthreads();
+    if (s_skip) return;
+    const uint32_t total = a.ctl->total_samples;
+    const uint64_t chunk0 = (uint64_t)blockIdx.x * kThreads * kSamplePerThread;
+    if (chunk0 >= total) return;
+    for (int b = threadIdx.x; b < kHistBins; b += kThreads) s_hist[b] = 0;
+    const uint64_t chunk_end = umin64(total, chunk0 + kThreads * kSamplePerThread);
+    if (threadIdx.x == 0) {
+        s_seg0 = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)chunk0);
+        s_seg1 = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)(chunk_end - 1));
+    }
+    __syncthreads();
+    const bool uniform = (s_seg0 == s_seg1);
+    float gv[kSamplePerThread], uv[kSamplePerThread], vv[kSamplePerThread];
+    int sg[kSamplePerThread];
+#pragma unroll
+    for (int r = 0; r < kSamplePerThread; ++r) {
+        const uint64_t jg = chunk0 + r * kThreads + threadIdx.x;
+        sg[r] = -1;
+        if (jg < chunk_end) {
+            const int s = uniform ? s_seg0 : upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)jg);
+            const SegInfo& d = a.segs[s];
+            const uint64_t j = jg - a.samp_off[s];
+            const uint64_t x = mix64(d.seed + kGolden * (j + 1));
+            const uint32_t pos = d.start + (uint32_t)__umul64hi(x, (uint64_t)(d.end - d.start));
+            gv[r] = __ldg(a.g + pos);
+            uv[r] = a.u[pos];
+            vv[r] = a.v[pos];
+            sg[r] = s;
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kSamplePerThread; ++r) {
+        if (sg[r] < 0) continue;
+        const uint64_t jg = chunk0 + r * kThreads + threadIdx.x;
+        float uu = uv[r], vn = vv[r];
+        accumulate(gv[r], uu, vn, a.hp.momentum, a.segs[sg[r]].scale);
+        const uint32_t key = key_of(vn);
+        a.skeys[jg] = key;
+        const uint32_t bin = key >> 20;
+        if (uniform) atomicAdd(&s_hist[bin], 1u);
+        else atomicAdd(&a.histA[(size_t)sg[r] * kHistBins + bin], 1u);
+    }
+    if (uniform) {
+        BlockHist h{s_hist, s_seg0};
+        h.flush(a.histA, kHistBins);
+    }
+}
+
+// ----------------------------------------------------------------- radix select: hist
+// Items are the sample keys (kind 0: X = key << 32) or the candidates (kind 1:
+// X = key << 32 | ~index). Level L counts, per active segment, the items whose bits above the
+// level match the prefix found so far, by the level's digit.
+template <int kKind>
+__device__ __forceinline__ uint64_t item_x(const Args& a, uint32_t i) {
+    if (kKind == 0) return (uint64_t)a.skeys[i] << 32;
+    return ((uint64_t)key_of(a.cval[i]) << 32) | (uint64_t)(~a.cidx[i]);
+}
+
+template <int kKind>
+__global__ void __launch_bounds__(kThreads) k_hist(Args a, int level) {
+    __shared__ uint32_t s_hist[kHistBins];
+    __shared__ int s_skip;
+    if (threadIdx.x == 0) s_skip = a.ctl->abort || a.ctl->active == 0;
+    __syncthreads();
+    if (s_skip) return;
+    const uint32_t* off = kKind == 0 ? a.samp_off : a.cand_off;
+    const uint32_t total = off[a.nseg];
+    uint32_t* ghist = (level & 1) ? a.histB : a.histA;
+    const int shift = c_shift[level], bits = c_bits[level];
+    const int nbins = 1 << bits;
+    const uint32_t mask = (uint32_t)nbins - 1;
+    for (int b = threadIdx.x; b < kHistBins; b += kThreads) s_hist[b] = 0;
+    __syncthreads();
+    BlockHist h{s_hist, -1};
+    constexpr int kPer = 8;
+    const uint32_t chunk = kThreads * kPer;
+    for (uint64_t c0 = (uint64_t)blockIdx.x * chunk; c0 < total; c0 += (uint64_t)gridDim.x * chunk) {
+        const uint32_t c1 = (uint32_t)umin64(total, c0 + chunk);
+        const int s0 = upper_bound_minus1(off, a.nseg, (uint32_t)c0);
+        const int s1 = upper_bound_minus1(off, a.nseg, c1 - 1);
+        if (s0 == s1) {
+            if (a.segs[s0].state != kActive) continue;
+            if (h.cur != s0) {
+                h.flush(ghist, nbins);
+                h.cur = s0;
+            }
+            const uint64_t prefix = a.segs[s0].prefix;
+            for (uint32_t i = (uint32_t)c0 + threadIdx.x; i < c1; i += kThreads) {
+                const uint64_t x = item_x<kKind>(a, i);
+                if ((x >> (shift + bits)) == prefix) atomicAdd(&s_hist[(x >> shift) & mask], 1u);
+            }
+        } else {
+            for (uint32_t i = (uint32_t)c0 + threadIdx.x; i < c1; i += kThreads) {
+                const int s = upper_bound_minus1(off, a.nseg, i);
+                const SegInfo& d = a.segs[s];
+                if (d.state != kActive) continue;
+                const uint64_t x = item_x<kKind>(a, i);
+                if ((x >> (shift + bits)) == d.prefix)
+                    atomicAdd(&ghist[(size_t)s * kHistBins + ((x >> shift) & mask)], 1u);
+            }
+        }
+    }
+    h.flush(ghist, nbins);
+}
+
+// ----------------------------------------------------------------- radix select: find
+// One block per segment: walk the level's bins from the top until `need` items are covered.
+// That bin extends the prefix. For the sample select the prefix after three levels is the
+// threshold key t. For the candidate select, once the bin holds exactly the items still
+// needed, everything at or above the prefix is selected (sel_x = prefix << shift).
+template <int kKind>
+__global__ void __launch_bounds__(kThreads) k_find(Args a, int level) {
+    __shared__ uint32_t s_scan[33];
+    __shared__ uint32_t s_bin, s_above, s_cnt;
+    __shared__ int s_found;
+    __shared__ int s_skip;
+    const int s = blockIdx.x;
+    SegInfo& d = a.segs[s];
+    if (threadIdx.x == 0) s_skip = a.ctl->abort || d.state != kActive;
+    __syncthreads();
+    if (s_skip) return;
+    const int bits = c_bits[level], shift = c_shift[level];
+    const int nbins = 1 << bits;
+    constexpr int kMaxPer = kHistBins / kThreads;  // 8
+    const int per = nbins / kThreads;              // 4 or 8
+    uint32_t* hist = ((level & 1) ? a.histB : a.histA) + (size_t)s * kHistBins;
+    uint32_t h[kMaxPer];
+    uint32_t local = 0;
+    // thread t owns positions [t*per, t*per + per) counted from the top bin down
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) {
+        h[i] = 0;
+        if (i < per) {
+            h[i] = hist[nbins - 1 - (threadIdx.x * per + i)];
+            local += h[i];
+        }
+    }
+    if (threadIdx.x == 0) s_found = 0;
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan<kThreads>(local, s_scan, &tot);
+    const uint32_t need = d.need;
+    if (ex < need && need <= ex + local) {
+        uint32_t cum = ex;
+#pragma unroll
+        for (int i = 0; i < kMaxPer; ++i) {
+            if (i < per && cum < need && need <= cum + h[i]) {
+                s_bin = (uint32_t)(nbins - 1 - (threadIdx.x * per + i));
+                s_above = cum;
+                s_cnt = h[i];
+                s_found = 1;
+            }
+            cum += (i < per) ? h[i] : 0;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i)
+        if (i < per) hist[nbins - 1 - (threadIdx.x * per + i)] = 0;
+    if (threadIdx.x != 0) return;
+    if (!s_found) {  // fewer items than needed: cannot happen for a consistent table
+        report(a.status, DGC_EINVAL);
+        d.sel_x = 0;
+        d.state = kIdle;
+        atomicSub(&a.ctl->active, 1u);
+        return;
+    }
+    const uint64_t prefix = (d.prefix << bits) | s_bin;
+    const uint32_t need2 = need - s_above;
+    if (kKind == 0) {
+        if (level == 2) {
+            d.thresh = (uint32_t)prefix;
+            d.state = kIdle;
+            atomicSub(&a.ctl->active, 1u);
+        } else {
+            d.prefix = prefix;
+            d.need = need2;
+        }
+    } else {
+        if (s_cnt == need2 || level == 5) {
+            d.sel_x = prefix << shift;
+            d.state = kIdle;
+            atomicSub(&a.ctl->active, 1u);
+        } else {
+            d.prefix = prefix;
+            d.need = need2;
+        }
+    }
+}
+
+// --------------------------------------------------------------------- streaming pass
+// kMode 0: exact-mode pass (accumulate, compact candidates). kMode 1: sampled-mode pass
+// (accumulate, compact candidates and clear their v and, with masking, u). kMode 2: exact-mode
+// re-compaction from v alone (a segment whose bound was too tight takes threshold 0).
+// Thread t of a tile handles float4 q = r*256 + t for rows r, so every load is a coalesced
+// 16-byte access; candidate order inside the tile comes from a bitmap of the tile.
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 2) k_stream(Args a) {
+    __shared__ uint32_t s_bitmap[kTile / 32];
+    __shared__ uint32_t s_wordpre[kTile / 32];
+    __shared__ uint32_t s_scan[33];
+    __shared__ uint32_t s_tile;
+    __shared__ uint64_t s_base;
+    __shared__ int s_seg0, s_uniform;
+    __shared__ float s_scale;
+    __shared__ uint32_t s_thresh;
+    __shared__ int s_skip;
+    const uint64_t n = a.n;
+    uint32_t* ticket = kMode == 2 ? &a.ctl->ticket_compact : &a.ctl->ticket_fused;
+    uint64_t* st = kMode == 2 ? a.st_compact : a.st_fused;
+    // one thread reads the flags and takes the tile, so the whole block agrees
+    if (threadIdx.x == 0) {
+        s_skip = (kMode == 2 && !a.ctl->any_failed) || ld_relaxed_u32((const uint32_t*)&a.ctl->abort);
+        if (!s_skip) s_tile = atomicAdd(ticket, 1u);
+    }
+    for (int w = threadIdx.x; w < kTile / 32; w += kThreads) s_bitmap[w] = 0;
+    __syncthreads();
+    if (s_skip) return;
+    const uint32_t tile = s_tile;
+    const uint64_t base = (uint64_t)tile * kTile;
+    const uint64_t tile_end = umin64(a.n, base + kTile);
+    if (threadIdx.x == 0) {
+        const int s0 = upper_bound_minus1(a.seg_start, a.nseg, (uint32_t)base);
+        s_seg0 = s0;
+        const SegInfo& d = a.segs[s0];
+        s_uniform = (d.end >= tile_end) ? 1 : 0;
+        s_scale = d.scale;
+        s_thresh = (kMode == 2 && d.failed) ? 0u : d.thresh;
+    }
+    __syncthreads();
+    const bool uniform = s_uniform;
+    const float m = a.hp.momentum;
+    const bool full = (base + kTile <= a.n);
+
+    float4 vv[kRows], uu[kRows];
+    uint32_t flags = 0;  // bit r*4+e: entry e of row r is a candidate
+    if (kMode == 2) {
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const uint64_t e0 = base + 4u * (r * kThreads + threadIdx.x);
+            if (full) {
+                vv[r] = *reinterpret_cast<const float4*>(a.v + e0);
+            } else {
+                float t[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) t[e] = (e0 + e < n) ? a.v[e0 + e] : 0.0f;
+                vv[r] = make_float4(t[0], t[1], t[2], t[3]);
+            }
+            uu[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    } else {
+        float4 gg[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const uint64_t e0 = base + 4u * (r * kThreads + threadIdx.x);
+            if (full) {
+                gg[r] = __ldcs(reinterpret_cast<const float4*>(a.g + e0));
+                uu[r] = *reinterpret_cast<const float4*>(a.u + e0);
+                vv[r] = *reinterpret_cast<const float4*>(a.v + e0);
+            } else {
+                float tg[4], tu[4], tv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool in = e0 + e < n;
+                    tg[e] = in ? a.g[e0 + e] : 0.f;
+                    tu[e] = in ? a.u[e0 + e] : 0.f;
+                    tv[e] = in ? a.v[e0 + e] : 0.f;
+                }
+                gg[r] = make_float4(tg[0], tg[1], tg[2], tg[3]);
+                uu[r] = make_float4(tu[0], tu[1], tu[2], tu[3]);
+                vv[r] = make_float4(tv[0], tv[1], tv[2], tv[3]);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const uint64_t e0 = base + 4u * (r * kThreads + threadIdx.x);
+            float* g4 = reinterpret_cast<float*>(&gg[r]);
+            float* u4 = reinterpret_cast<float*>(&uu[r]);
+            float* v4 = reinterpret_cast<float*>(&vv[r]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float scale = s_scale;
+                if (!uniform && e0 + e < n)
+                    scale = a.segs[upper_bound_minus1(a.seg_start, a.nseg, (uint32_t)(e0 + e))].scale;
+                accumulate(g4[e], u4[e], v4[e], m, scale);
+            }
+        }
+    }
+    // candidates
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+        const uint64_t e0 = base + 4u * (r * kThreads + threadIdx.x);
+        const float* v4 = reinterpret_cast<const float*>(&vv[r]);
+        uint32_t f4 = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (e0 + e >= n) continue;
+            uint32_t t = s_thresh;
+            if (!uniform) {
+                const SegInfo& d = a.segs[upper_bound_minus1(a.seg_start, a.nseg, (uint32_t)(e0 + e))];
+                t = (kMode == 2 && d.failed) ? 0u : d.thresh;
+            }
+            if (key_of(v4[e]) >= t) f4 |= 1u << e;
+        }
+        if (f4) {
+            const uint32_t off = (uint32_t)(e0 - base);
+            atomicOr(&s_bitmap[off >> 5], f4 << (off & 31));
+        }
+        flags |= f4 << (4 * r);
+    }
+    // stores of the updated state (sampled mode clears candidates optimistically)
+    if (kMode != 2) {
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const uint64_t e0 = base + 4u * (r * kThreads + threadIdx.x);
+            float4 vs = vv[r], us = uu[r];
+            if (kMode == 1) {
+                float* v4 = reinterpret_cast<float*>(&vs);
+                float* u4 = reinterpret_cast<float*>(&us);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (flags & (1u << (4 * r + e))) {
+                        v4[e] = 0.0f;
+                        if (a.hp.mask) u4[e] = 0.0f;
+                    }
+            }
+            if (full) {
+                *reinterpret_cast<float4*>(a.u + e0) = us;
+                *reinterpret_cast<float4*>(a.v + e0) = vs;
+            } else {
+                const float* u4 = reinterpret_cast<const float*>(&us);
+                const float* v4 = reinterpret_cast<const float*>(&vs);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (e0 + e < n) {
+                        a.u[e0 + e] = u4[e];
+                        a.v[e0 + e] = v4[e];
+                    }
+            }
+        }
+    }
+    __syncthreads();
+    // tile-local ranks from the bitmap, then the global base from the look-back
+    uint32_t cnt = 0;
+    for (int w = threadIdx.x; w < kTile / 32; w += kThreads) cnt += __popc(s_bitmap[w]);
+    static_assert(kTile / 32 == kThreads, "one bitmap word per thread");
+    uint32_t tile_total;
+    const uint32_t ex = block_excl_scan<kThreads>(cnt, s_scan, &tile_total);
+    s_wordpre[threadIdx.x] = ex;
+    if (threadIdx.x < 32) {
+        const uint64_t excl = lookback_exclusive(st, tile, tile_total, a.spin_limit, a.status,
+                                                 &a.ctl->abort);
+        if (threadIdx.x == 0) s_base = excl;
+    }
+    __syncthreads();
+    const uint64_t gbase = s_base;
+    if (flags) {
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const uint64_t e0 = base + 4u * (r * kThreads + threadIdx.x);
+            const float* v4 = reinterpret_cast<const float*>(&vv[r]);
+            const float* u4 = reinterpret_cast<const float*>(&uu[r]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (!(flags & (1u << (4 * r + e)))) continue;
+                const uint32_t off = (uint32_t)(e0 + e - base);
+                const uint32_t w = off >> 5;
+                const uint32_t rank = s_wordpre[w] + __popc(s_bitmap[w] & ((1u << (off & 31)) - 1u));
+                const uint64_t pos = gbase + rank;
+                if (pos < n) {
+                    a.cidx[pos] = (uint32_t)(e0 + e);
+                    a.cval[pos] = v4[e];
+                    if (kMode == 1) a.cu[pos] = u4[e];
+                }
+            }
+        }
+    }
+    if (tile == a.fused_tiles - 1 && threadIdx.x == 0)
+        a.ctl->total_cand = (uint32_t)umin64(gbase + tile_total, n);
+}
+
+// ------------------------------------------------------------------- candidate ranges
+// One block: per-segment candidate ranges by binary search of the ascending candidate
+// indices, then who selects among them. pass 1 only runs after an exact-mode re-compaction.
+__global__ void __launch_bounds__(1024) k_candoff(Args a, int pass) {
+    __shared__ uint32_t s_active;
+    __shared__ int s_skip;
+    if (threadIdx.x == 0) s_skip = a.ctl->abort || (pass == 1 && !a.ctl->any_failed);
+    __syncthreads();
+    if (s_skip) return;
+    if (threadIdx.x == 0) {
+        a.ctl->active = 0;
+        s_active = 0;
+    }
+    const uint32_t total = a.ctl->total_cand;
+    for (int s = threadIdx.x; s <= a.nseg; s += blockDim.x) {
+        const uint32_t x = a.seg_start[s];
+        uint32_t lo = 0, hi = total;  // first candidate index >= x
+        while (lo < hi) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (a.cidx[mid] < x) lo = mid + 1; else hi = mid;
+        }
+        a.cand_off[s] = (s == a.nseg) ? total : lo;
+    }
+    __syncthreads();
+    uint32_t any_failed = 0, active = 0;
+    for (int s = threadIdx.x; s < a.nseg; s += blockDim.x) {
+        SegInfo& d = a.segs[s];
+        const uint32_t cnt = a.cand_off[s + 1] - a.cand_off[s];
+        d.cand_cnt = cnt;
+        d.prefix = 0;
+        d.state = kIdle;
+        d.sel_x = 0;
+        if (d.k == 0) continue;
+        if (a.hp.mode == DGC_SELECT_EXACT) {
+            if (cnt < d.k) {
+                d.failed = 1;
+                any_failed = 1;
+            } else if (cnt > d.k) {
+                d.state = kActive;
+                d.need = d.k;
+                ++active;
+            }
+        } else if ((unsigned __int128)cnt * kBillion > (unsigned __int128)a.hp.q_ppb * d.k) {
+            d.resel = 1;
+            d.state = kActive;
+            d.need = d.k;
+            ++active;
+        }
+    }
+    if (active) atomicAdd(&s_active, active);
+    if (any_failed) a.ctl->any_failed = 1;
+    __syncthreads();
+    if (threadIdx.x == 0) a.ctl->active = s_active;
+}
+
+// ---------------------------------------------------------------------------------- emit
+// Candidates in index order; selected <=> X >= sel_x of their segment. Positions of the
+// selected ones come from a second decoupled look-back. Exact mode clears v (and u) of what
+// is sent; sampled mode put back v (and u) of candidates that re-selection dropped. The last
+// block to finish writes out_count and the statistics.
+template <int kMode>
+__global__ void __launch_bounds__(kThreads) k_emit(Args a) {
+    __shared__ uint32_t s_bitmap[kEmitTile / 32];
+    __shared__ uint32_t s_wordpre[kEmitTile / 32];
+    __shared__ uint32_t s_scan[33];
+    __shared__ uint32_t s_tile;
+    __shared__ uint64_t s_base;
+    __shared__ int s_last, s_ok;
+    if (threadIdx.x == 0) s_ok = !ld_relaxed_u32((const uint32_t*)&a.ctl->abort);
+    __syncthreads();
+    const bool ok = s_ok;
+    const uint32_t total = a.ctl->total_cand;
+    const uint32_t ntiles = (total + kEmitTile - 1) / kEmitTile;
+    while (ok) {
+        if (threadIdx.x == 0) s_tile = atomicAdd(&a.ctl->ticket_emit, 1u);
+        for (int w = threadIdx.x; w < kEmitTile / 32; w += kThreads) s_bitmap[w] = 0;
+        __syncthreads();
+        const uint32_t tile = s_tile;
+        if (tile >= ntiles) break;
+        const uint64_t base = (uint64_t)tile * kEmitTile;
+        uint32_t sel = 0;
+        uint32_t idx[kEmitRows * 4];
+        float val[kEmitRows * 4];
+        int seg[kEmitRows * 4];
+#pragma unroll
+        for (int r = 0; r < kEmitRows; ++r) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint64_t i = base + 4u * (r * kThreads + threadIdx.x) + e;
+                const int q = r * 4 + e;
+                seg[q] = -1;
+                if (i < total) {
+                    idx[q] = a.cidx[i];
+                    val[q] = a.cval[i];
+                    const int s = upper_bound_minus1(a.cand_off, a.nseg, (uint32_t)i);
+                    seg[q] = s;
+                    const uint64_t x = ((uint64_t)key_of(val[q]) << 32) | (uint64_t)(~idx[q]);
+                    if (x >= a.segs[s].sel_x) sel |= 1u << q;
+                }
+            }
+            const uint32_t f4 = (sel >> (4 * r)) & 0xFu;
+            if (f4) {
+                const uint32_t off = 4u * (r * kThreads + threadIdx.x);
+                atomicOr(&s_bitmap[off >> 5], f4 << (off & 31));
+            }
+        }
+        __syncthreads();
+        uint32_t cnt = 0;
+        for (int w = threadIdx.x; w < kEmitTile / 32; w += kThreads) cnt += __popc(s_bitmap[w]);
+        uint32_t tile_total;
+        const uint32_t ex = block_excl_scan<kThreads>(cnt, s_scan, &tile_total);
+        if (threadIdx.x < kEmitTile / 32) s_wordpre[threadIdx.x] = ex;
+        if (threadIdx.x < 32) {
+            const uint64_t excl = lookback_exclusive(a.st_emit, tile, tile_total, a.spin_limit,
+                                                     a.status, &a.ctl->abort);
+            if (threadIdx.x == 0) s_base = excl;
+        }
+        __syncthreads();
+        const uint64_t gbase = s_base;
+#pragma unroll
+        for (int q = 0; q < kEmitRows * 4; ++q) {
+            if (seg[q] < 0) continue;
+            const uint64_t i = base + 4u * ((q >> 2) * kThreads + threadIdx.x) + (q & 3);
+            if (sel & (1u << q)) {
+                const uint32_t off = (uint32_t)(i - base);
+                const uint32_t w = off >> 5;
+                const uint64_t pos =
+                    gbase + s_wordpre[w] + __popc(s_bitmap[w] & ((1u << (off & 31)) - 1u));
+                if (pos < a.out_cap) {
+                    a.out_idx[pos] = idx[q];
+                    a.out_val[pos] = val[q];
+                }
+                if (kMode == 0) {
+                    a.v[idx[q]] = 0.0f;
+                    if (a.hp.mask) a.u[idx[q]] = 0.0f;
+                }
+                atomicMin(&a.segs[seg[q]].min_key, key_of(val[q]));
+            } else if (kMode == 1) {
+                a.v[idx[q]] = val[q];
+                if (a.hp.mask) a.u[idx[q]] = a.cu[i];
+            }
+        }
+        if (tile == ntiles - 1 && threadIdx.x == 0) a.ctl->total_sent = (uint32_t)(gbase + tile_total);
+        __syncthreads();
+    }
+    // the last block out writes the results
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(&a.ctl->emit_done, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (threadIdx.x == 0 && ok) *a.out_count = (int64_t)ld_relaxed_u32(&a.ctl->total_sent);
+    if (!a.stats) return;
+    for (int s = threadIdx.x; s < a.nseg; s += kThreads) {
+        const SegInfo& d = a.segs[s];
+        dgc_seg_stats o;
+        o.k = d.k;
+        uint64_t sent = 0;
+        if (ok && d.k > 0) {
+            if (a.hp.mode == DGC_SELECT_EXACT) sent = d.k;
+            else sent = d.resel ? d.k : d.cand_cnt;
+        }
+        o.sent = sent;
+        o.candidates = (a.hp.mode == DGC_SELECT_EXACT) ? sent : (ok ? d.cand_cnt : 0);
+        o.thresh_key = ld_relaxed_u32(&d.min_key);
+        o.sample_key = (a.hp.mode == DGC_SELECT_SAMPLED && d.k > 0) ? d.thresh : 0u;
+        o.reselected = d.resel;
+        o.clip_scale = d.scale;
+        a.stats[s] = o;
+    }
+}
+
+}  // namespace
+}  // namespace dgc
+
+using namespace dgc;
+
+static cudaEvent_t g_prof_begin = nullptr, g_prof_end = nullptr;
+
+extern "C" void dgc_profile_stream_pass(dgc_event_t begin, dgc_event_t end) {
+    g_prof_begin = reinterpret_cast<cudaEvent_t>(begin);
+    g_prof_end = reinterpret_cast<cudaEvent_t>(end);
+}
+
+extern "C" int dgc_compress_workspace(int64_t n, int32_t nseg, const dgc_params* params,
+                                      size_t* bytes) {
+    HostParams hp;
+    if (!bytes || nseg < 1 || n < 0) return DGC_EINVAL;
+    if (n > 0xFFFFFFFFll || nseg > (1 << 28)) return DGC_EUNSUPPORTED;
+    const int rc = check_params(params, &hp);
+    if (rc) return rc;
+    *bytes = make_layout(n, nseg, hp).total;
+    return DGC_OK;
+}
+
+extern "C" int dgc_compress_max_out(int64_t n, int32_t nseg, const dgc_params* params,
+                                    int64_t* max_out) {
+    HostParams hp;
+    if (!max_out || nseg < 1 || n < 0) return DGC_EINVAL;
+    if (n > 0xFFFFFFFFll || nseg > (1 << 28)) return DGC_EUNSUPPORTED;
+    const int rc = check_params(params, &hp);
+    if (rc) return rc;
+    *max_out = (int64_t)max_out_for(n, nseg, hp);
+    return DGC_OK;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* seg_off,
+                            int32_t nseg, const dgc_params* params, uint32_t* out_idx,
+                            float* out_val, int64_t out_cap, int64_t* out_count,
+                            dgc_seg_stats* stats, int32_t* status, void* ws, size_t ws_bytes,
+                            dgc_stream_t stream) {
+    HostParams hp;
+    if (n < 0 || nseg < 1) return DGC_EINVAL;
+    if (n > 0xFFFFFFFFll || nseg > (1 << 28)) return DGC_EUNSUPPORTED;
+    int rc = check_params(params, &hp);
+    if (rc) return rc;
+    if (!seg_off || !out_count || !status || !ws) return DGC_EINVAL;
+    if (n > 0 && (!g || !u || !v || !aligned16(g) || !aligned16(u) || !aligned16(v)))
+        return DGC_EINVAL;
+    if (((uintptr_t)ws & 255u) != 0) return DGC_EINVAL;
+    const Layout L = make_layout(n, nseg, hp);
+    if (ws_bytes < L.total) return DGC_EINVAL;
+    const uint64_t mo = max_out_for(n, nseg, hp);
+    if (out_cap < 0 || (uint64_t)out_cap < mo) return DGC_ECAPACITY;
+    if (mo > 0 && (!out_idx || !out_val)) return DGC_EINVAL;
+
+    char* w = static_cast<char*>(ws);
+    Args a{};
+    a.g = g;
+    a.u = u;
+    a.v = v;
+    a.n = (uint32_t)n;
+    a.nseg = nseg;
+    a.seg_off = seg_off;
+    a.hp = hp;
+    a.out_idx = out_idx;
+    a.out_val = out_val;
+    a.out_cap = (uint64_t)out_cap;
+    a.out_count = out_count;
+    a.stats = stats;
+    a.status = status;
+    a.ctl = reinterpret_cast<Ctl*>(w + L.ctl);
+    a.segs = reinterpret_cast<SegInfo*>(w + L.segs);
+    a.seg_start = reinterpret_cast<uint32_t*>(w + L.seg_start);
+    a.samp_off = reinterpret_cast<uint32_t*>(w + L.samp_off);
+    a.clip_off = reinterpret_cast<uint32_t*>(w + L.clip_off);
+    a.cand_off = reinterpret_cast<uint32_t*>(w + L.cand_off);
+    a.clip_part = reinterpret_cast<double*>(w + L.clip_part);
+    a.skeys = reinterpret_cast<uint32_t*>(w + L.skeys);
+    a.histA = reinterpret_cast<uint32_t*>(w + L.histA);
+    a.histB = reinterpret_cast<uint32_t*>(w + L.histB);
+    a.st_fused = reinterpret_cast<uint64_t*>(w + L.st_fused);
+    a.st_compact = reinterpret_cast<uint64_t*>(w + L.st_compact);
+    a.st_emit = reinterpret_cast<uint64_t*>(w + L.st_emit);
+    a.cidx = reinterpret_cast<uint32_t*>(w + L.cidx);
+    a.cval = reinterpret_cast<float*>(w + L.cval);
+    a.cu = reinterpret_cast<float*>(w + L.cu);
+    a.max_samples = L.max_samples;
+    a.fused_tiles = L.fused_tiles;
+    a.emit_tiles = L.emit_tiles;
+    a.max_clip_tiles = L.max_clip_tiles;
+    a.spin_limit = kDefaultSpinLimit;
+
+    const int sms = dgc_internal_sm_count();
+    if (sms <= 0) return DGC_ECUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint64_t launches = 0;
+    auto L1 = [&](auto kernel, unsigned grid, unsigned block, auto... args) {
+        if (grid == 0) return;
+        kernel<<<grid, block, 0, s>>>(args...);
+        ++launches;
+    };
+    const size_t zero_work = (size_t)nseg * kHistBins + L.fused_tiles + L.emit_tiles + 2;
+    const unsigned plan_grid = (unsigned)std::min<size_t>((zero_work + 1023) / 1024 + 1,
+                                                          (size_t)sms * 2);
+    L1(k_plan, plan_grid, 1024, a);
+    if (hp.clip_on) {
+        L1(k_clip_tiles, (unsigned)L.max_clip_tiles, kThreads, a);
+        L1(k_clip_scale, (unsigned)((nseg + 255) / 256), 256, a);
+    }
+    const uint64_t sgrid = (L.max_samples + kThreads * kSamplePerThread - 1) /
+                           (kThreads * kSamplePerThread);
+    L1(k_sample, (unsigned)sgrid, kThreads, a);
+    const unsigned hist_grid = (unsigned)sms * 2;
+    L1(k_find<0>, (unsigned)nseg, kThreads, a, 0);
+    L1(k_hist<0>, hist_grid, kThreads, a, 1);
+    L1(k_find<0>, (unsigned)nseg, kThreads, a, 1);
+    L1(k_hist<0>, hist_grid, kThreads, a, 2);
+    L1(k_find<0>, (unsigned)nseg, kThreads, a, 2);
+    const cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
+    if (pb && pe) cudaEventRecord(pb, s);
+    if (hp.mode == DGC_SELECT_SAMPLED) L1(k_stream<1>, (unsigned)L.fused_tiles, kThreads, a);
+    else L1(k_stream<0>, (unsigned)L.fused_tiles, kThreads, a);
+    if (pb && pe) cudaEventRecord(pe, s);
+    L1(k_candoff, 1, 1024, a, 0);
+    if (hp.mode == DGC_SELECT_EXACT) {
+        L1(k_stream<2>, (unsigned)L.fused_tiles, kThreads, a);
+        L1(k_candoff, 1, 1024, a, 1);
+    }
+    for (int level = 0; level < 6; ++level) {
+        L1(k_hist<1>, hist_grid, kThreads, a, level);
+        L1(k_find<1>, (unsigned)nseg, kThreads, a, level);
+    }
+    const unsigned emit_grid = (unsigned)std::max<uint64_t>(
+        1, std::min<uint64_t>((uint64_t)sms * 4, L.emit_tiles));
+    if (hp.mode == DGC_SELECT_SAMPLED) L1(k_emit<1>, emit_grid, kThreads, a);
+    else L1(k_emit<0>, emit_grid, kThreads, a);
+    dgc_internal_count_launches(launches);
+    if (cudaPeekAtLastError() != cudaSuccess) {
+        cudaGetLastError();
+        return DGC_ECUDA;
+    }
+    return DGC_OK;
+}

@@ -1,0 +1,437 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle, element by element.
+
+Integer and index results (selected sets, encoded bytes, counts, keys) must be bit-identical.
+The floating-point results are too: the kernels perform the same binary32/binary64 operations
+in the same order as the oracle (fma for u, one rounding per add, the fixed clipping sum), so
+u, v, the sent values and the decoded sums are compared bitwise -- tighter than the 1e-6 /
+1-ulp / 1e-5 tolerances the workloads allow.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparsified_gradient_compression_gb300 as dgc
+import workloads
+from conftest import read_golden
+from gpu_helpers import Compressor, Encoder, decode, dev_f32, host_f32
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU-only machines, never run there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    dgc.build()
+    dgc.lib()
+    oracle.lib()
+
+
+def bits(a):
+    return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+
+
+def same_bits(a, b):
+    return np.array_equal(bits(a), bits(b))
+
+
+def params_pair(**kw):
+    return dgc.make_params(**kw), oracle.make_params(**kw)
+
+
+def run_steps(grads, seg_off, steps, check_state=True, u0=None, v0=None, **kw):
+    """Run `steps` compressor steps on both sides; compare outputs, state and stats each step."""
+    n = int(seg_off[-1])
+    pd, po = params_pair(**kw)
+    comp = Compressor(n, seg_off, pd)
+    u_h = np.zeros(n, np.float32) if u0 is None else u0.copy()
+    v_h = np.zeros(n, np.float32) if v0 is None else v0.copy()
+    u_d, v_d = dev_f32(u_h), dev_f32(v_h)
+    outs = []
+    for t in range(steps):
+        g = grads(t)
+        comp(dev_f32(g), u_d, v_d)
+        assert comp.status_code() == 0
+        idx, val, st = comp.results()
+        oidx, oval, ost = oracle.compress(g, u_h, v_h, seg_off, po)
+        assert idx.size == oidx.size, f"step {t}: |S| {idx.size} vs {oidx.size}"
+        assert np.array_equal(idx, oidx), f"step {t}: index sets differ"
+        assert same_bits(val, oval), f"step {t}: sent values differ"
+        if check_state:
+            assert same_bits(host_f32(v_d), v_h), f"step {t}: residual v differs"
+            assert same_bits(host_f32(u_d), u_h), f"step {t}: momentum u differs"
+        for s, o in enumerate(ost):
+            got = st[s]
+            assert got["k"] == o["k"] and got["sent"] == o["sent"], (t, s)
+            assert got["candidates"] == o["candidates"], (t, s)
+            assert got["thresh_key"] == o["thresh_key"], (t, s)
+            assert got["sample_key"] == o["sample_key"], (t, s)
+            assert got["reselected"] == o["reselected"], (t, s)
+            assert bits(np.float32(got["clip_scale"])) == bits(o["clip_scale"]), (t, s)
+        outs.append((idx, val))
+    return outs, u_d, v_d
+
+
+# ------------------------------------------------------------------- the five workloads
+def test_single_tensor_1m_exact_three_steps_and_codec():
+    n = 1_048_576
+    off = np.array([0, n])
+    outs, _, _ = run_steps(lambda t: workloads.gradient("single", t), off, 3,
+                           mode=dgc.SELECT_EXACT, sparsity=0.999, momentum=0.9)
+    for idx, val in outs:
+        assert idx.size == 1049
+        enc = Encoder(idx.size, n)
+        cnt = torch.tensor([idx.size], dtype=torch.int64, device="cuda")
+        enc(torch.from_numpy(idx.view(np.int32)).cuda(), dev_f32(val), cnt)
+        msg = enc.message()
+        assert msg == oracle.encode(idx, val, n)
+        rc, dense = decode([msg], n)
+        orc_rc, odense = oracle.decode_accumulate([msg], n)
+        assert rc == 0 and orc_rc == 0
+        assert same_bits(host_f32(dense), odense)
+
+
+@pytest.mark.slow
+def test_resnet50_161_tensors_clip_exact_ten_steps():
+    off = workloads.resnet50_segments()
+    run_steps(lambda t: workloads.gradient("resnet50", t), off, 10, mode=dgc.SELECT_EXACT,
+              sparsity=0.999, momentum=0.9, clip_norm=1.0)
+
+
+@pytest.mark.slow
+def test_deepspeech_sampled_six_segments():
+    off = workloads.deepspeech_segments()
+    outs, _, _ = run_steps(lambda t: workloads.gradient("deepspeech", t), off, 4,
+                           mode=dgc.SELECT_SAMPLED, sparsity=0.999, momentum=0.9,
+                           sample_ratio=0.01, reselect_factor=1.3, seed=1234)
+    # the message size the DGC review prints for DeepSpeech: 0.74 MB
+    idx, val = outs[-1]
+    assert abs(len(oracle.encode(idx, val, int(off[-1]))) / 1e6 - 0.74) / 0.74 < 0.1
+
+
+@pytest.mark.slow
+def test_bucket_1g_sampled_warmup_schedule():
+    n = 1 << 30
+    off = np.array([0, n])
+    pd, po = params_pair(mode=dgc.SELECT_SAMPLED, sparsity=0.75, momentum=0.9, sample_ratio=0.01,
+                         reselect_factor=1.3, seed=99)
+    u_h = np.zeros(n, np.float32)
+    v_h = np.zeros(n, np.float32)
+    u_d = torch.zeros(n, dtype=torch.float32, device="cuda")
+    v_d = torch.zeros(n, dtype=torch.float32, device="cuda")
+    for t, s in enumerate(workloads.WARMUP_SPARSITY):
+        pd.sparsity = po.sparsity = s
+        comp = Compressor(n, off, pd)
+        g = workloads.gradient("bucket1g", t)
+        comp(dev_f32(g), u_d, v_d)
+        assert comp.status_code() == 0
+        idx, val, st = comp.results()
+        oidx, oval, ost = oracle.compress(g, u_h, v_h, off, po)
+        assert np.array_equal(idx, oidx) and same_bits(val, oval), f"step {t}"
+        assert st[0]["sample_key"] == ost[0]["sample_key"]
+        assert st[0]["candidates"] == ost[0]["candidates"]
+        assert same_bits(host_f32(v_d), v_h) and same_bits(host_f32(u_d), u_h), f"step {t}"
+        del comp
+        torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+def test_aggregation_64_learners():
+    n, W, k = 25_557_032, 64, 25_558
+    for step in range(5):
+        msgs_gpu, msgs_orc = [], []
+        for w in range(W):
+            rng = np.random.Generator(np.random.PCG64([5, step, w]))
+            idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+            val = (rng.standard_normal(k) * 0.01).astype(np.float32)
+            enc = Encoder(k, n)
+            enc(torch.from_numpy(idx.view(np.int32)).cuda(), dev_f32(val),
+                torch.tensor([k], dtype=torch.int64, device="cuda"))
+            msgs_gpu.append(enc.message())
+            msgs_orc.append(oracle.encode(idx, val, n))
+            assert msgs_gpu[-1] == msgs_orc[-1]
+        rc, dense = decode(msgs_gpu, n)
+        orc_rc, odense = oracle.decode_accumulate(msgs_orc, n)
+        assert rc == 0 and orc_rc == 0
+        assert same_bits(host_f32(dense), odense)
+
+
+@pytest.mark.slow
+def test_learner_compress_full_size():
+    # two of the aggregation workload's learners through the whole compressor at full size
+    n = 25_557_032
+    off = np.array([0, n])
+    for learner in (0, 63):
+        run_steps(lambda t: workloads.gradient("learners", t, learner=learner), off, 2,
+                  mode=dgc.SELECT_EXACT, sparsity=0.999, momentum=0.9)
+
+
+# --------------------------------------------------------------------- shapes and edges
+EDGE_N = [1, 3, 15, 17, 4095, 8191, 8192, 8193, 40_000, 100_003]
+
+
+def _segments(rng, n):
+    kind = rng.integers(0, 4)
+    if kind == 0:
+        return np.array([0, n])
+    cuts = np.sort(rng.integers(0, n + 1, int(rng.integers(1, 12))))
+    off = np.concatenate([[0], cuts, [n]])
+    if kind == 2:  # force empty and length-1 segments
+        off = np.concatenate([[0, 0, min(1, n)], cuts, [n, n]])
+        off.sort()
+    return off.astype(np.int64)
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_exact_edges(case):
+    rng = np.random.default_rng(9000 + case)
+    n = EDGE_N[case % len(EDGE_N)]
+    off = _segments(rng, n)
+    sparsity = float(rng.choice([0.0, 0.5, 0.9, 0.99, 0.999, 1.0]))
+    kind = case % 3
+    scale = float(10.0 ** rng.integers(-4, 1))
+
+    def grads(t):
+        r = np.random.default_rng([case, t])
+        if kind == 1:  # many ties and zeros
+            return r.integers(-2, 3, n).astype(np.float32)
+        return (r.standard_normal(n) * scale).astype(np.float32)
+
+    run_steps(grads, off, 3, mode=dgc.SELECT_EXACT, sparsity=sparsity,
+              momentum=float(rng.choice([0.0, 0.9])), clip_norm=float(rng.choice([0.0, 0.5])),
+              mask_momentum=bool(case % 2))
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_sampled_edges(case):
+    rng = np.random.default_rng(7000 + case)
+    n = EDGE_N[case % len(EDGE_N)] * (1 + case % 3)
+    off = _segments(rng, n)
+    sparsity = float(rng.choice([0.0, 0.5, 0.9, 0.99, 0.999, 1.0]))
+    kind = case % 3
+
+    def grads(t):
+        r = np.random.default_rng([case, t, 1])
+        if kind == 1:  # ties: C much larger than k, so the exact re-selection runs
+            return r.integers(-2, 3, n).astype(np.float32)
+        return (r.standard_t(3, n) * 1e-3).astype(np.float32)
+
+    run_steps(grads, off, 3, mode=dgc.SELECT_SAMPLED, sparsity=sparsity, momentum=0.9,
+              sample_ratio=float(rng.choice([0.01, 0.1, 1.0])), reselect_factor=1.3,
+              seed=int(rng.integers(0, 2**63)), mask_momentum=bool(case % 2),
+              clip_norm=float(rng.choice([0.0, 1.0])))
+
+
+def test_exact_tight_sample_bound_falls_back():
+    # White-box: exact mode bounds the threshold from below with a 1% sample drawn from the same
+    # SplitMix64 positions (seed from the params). Putting the only large values exactly at the
+    # sampled positions makes that bound admit fewer than k candidates (the draws repeat a few
+    # positions), which forces the re-compaction from v. The result must still be exact.
+    n, seed = 400_000, 77
+    ms = -(-n // 100)
+    pos = np.unique([oracle.sample_position(seed, 0, j, n) for j in range(ms)])
+    k = -(-n // 100)  # sparsity 0.99
+    assert pos.size < k
+    g = np.full(n, 1e-6, np.float32)
+    g[pos] = 1.0
+    run_steps(lambda t: g * np.float32(1 + t), np.array([0, n]), 2, mode=dgc.SELECT_EXACT,
+              sparsity=0.99, momentum=0.9, seed=seed)
+
+
+def test_all_equal_magnitudes_ties_to_lower_index():
+    n = 50_000
+    g = np.where(np.arange(n) % 2 == 0, np.float32(0.5), np.float32(-0.5)).astype(np.float32)
+    for mode in (dgc.SELECT_EXACT, dgc.SELECT_SAMPLED):
+        outs, _, _ = run_steps(lambda t: g, np.array([0, n]), 2, mode=mode, sparsity=0.999,
+                               momentum=0.0)
+        assert outs[0][0].tolist() == list(range(50))
+
+
+def test_empty_gradient():
+    outs, _, _ = run_steps(lambda t: np.zeros(0, np.float32), np.array([0, 0, 0]), 1,
+                           mode=dgc.SELECT_EXACT)
+    assert outs[0][0].size == 0
+
+
+# ------------------------------------------------------------------------------- codec
+def golden_message(name):
+    import struct
+
+    n, entries, tokens = None, [], []
+    for tag, vals in read_golden(name):
+        if tag == "n":
+            n = vals[0]
+        elif tag == "entry":
+            entries.append(vals)
+        elif tag == "token":
+            tokens.append(vals)
+    T = len(tokens)
+    msg = struct.pack("<4sHHQQQ", b"DGC1", 1, 0, n, T, len(entries))
+    msg += b"".join(struct.pack("<I", t[1]) for t in tokens)
+    msg += b"".join(struct.pack("<H", t[0]) for t in tokens)
+    msg += b"\0" * ((-len(msg)) % 4)
+    idx = np.array([e[0] for e in entries], np.uint32)
+    val = np.array([e[1] for e in entries], np.uint32).view(np.float32)
+    return n, idx, val, msg
+
+
+@pytest.mark.parametrize("name", ["codec_gaps.txt", "codec_single.txt", "codec_odd.txt",
+                                  "codec_empty.txt"])
+def test_codec_golden_on_gpu(name):
+    n, idx, val, msg = golden_message(name)
+    enc = Encoder(max(idx.size, 1), n)
+    enc(torch.from_numpy(np.append(idx, 0).view(np.int32)).cuda(),
+        dev_f32(np.append(val, 0)), torch.tensor([idx.size], dtype=torch.int64, device="cuda"))
+    assert dgc.dgc_read_status(enc.status) == 0
+    assert enc.message() == msg
+    rc, dense = decode([msg], n)
+    assert rc == 0
+    exp = np.zeros(n, np.float32)
+    exp[idx] = exp[idx] + val
+    assert same_bits(host_f32(dense)[:n], exp)
+
+
+def test_decode_order_golden_on_gpu():
+    rows = read_golden("decode_order.txt")
+    n = rows[0][1][0]
+    msgs = [oracle.encode(np.array([v[0]], np.uint32), np.array([v[1]], np.uint32).view(np.float32), n)
+            for t, v in rows if t == "learner"]
+    rc, dense = decode(msgs, n)
+    assert rc == 0
+    d = host_f32(dense)
+    for t, (pos, b) in ((t, v) for t, v in rows if t == "expect"):
+        assert int(bits(d[pos:pos + 1])[0]) == b
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_decode_many_learners_and_accumulate(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 3_000_000))
+    W = int(rng.integers(1, 300))
+    msgs = []
+    for w in range(W):
+        k = int(rng.integers(0, min(n, 20_000) + 1))
+        idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+        msgs.append(oracle.encode(idx, (rng.standard_normal(k) * 10.0 ** rng.integers(-3, 3, k))
+                                  .astype(np.float32), n))
+    base = rng.standard_normal(n).astype(np.float32)
+    for acc in (False, True):
+        rc, dense = decode(msgs, n, dense=dev_f32(base), accumulate=acc)
+        orc_rc, odense = oracle.decode_accumulate(msgs, n, dense=base, accumulate=acc)
+        assert rc == 0 and orc_rc == 0
+        assert same_bits(host_f32(dense), odense)
+
+
+def test_decode_zero_learners():
+    rc, dense = decode([], 1000)
+    assert rc == 0 and not host_f32(dense).any()
+
+
+def test_encode_random_matches_oracle():
+    rng = np.random.default_rng(4)
+    for _ in range(10):
+        n = int(rng.integers(1, 5_000_000))
+        k = int(rng.integers(0, min(n, 300_000) + 1))
+        idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+        val = rng.standard_normal(k).astype(np.float32)
+        enc = Encoder(max(k, 1), n)
+        enc(torch.from_numpy(np.append(idx, 0).view(np.int32)).cuda(), dev_f32(np.append(val, 0)),
+            torch.tensor([k], dtype=torch.int64, device="cuda"))
+        assert enc.message() == oracle.encode(idx, val, n)
+
+
+# ------------------------------------------------------------------ errors and recovery
+def test_decode_rejects_malformed_and_leaves_dense():
+    import struct
+
+    n = 1000
+    good = oracle.encode(np.array([5, 999], np.uint32), np.array([1.0, 2.0], np.float32), n)
+    bad = [b"XGC1" + good[4:], good[:4] + struct.pack("<H", 2) + good[6:],
+           good[:8] + struct.pack("<Q", n + 1) + good[16:],
+           good[:32 + 8] + struct.pack("<H", 999) + good[32 + 10:]]
+    for b in bad:
+        base = dev_f32(np.full(n, 7.0, np.float32))
+        rc, dense = decode([good, b], n, dense=base, accumulate=True)
+        assert rc == dgc.ECORRUPT
+        assert np.all(host_f32(dense) == 7.0)
+
+
+def test_encode_rejects_unsorted_and_small_buffer():
+    n = 100
+    enc = Encoder(3, n)
+    enc(torch.tensor([5, 3, 9], dtype=torch.int32, device="cuda"),
+        dev_f32(np.ones(3, np.float32)), torch.tensor([3], dtype=torch.int64, device="cuda"))
+    assert dgc.dgc_read_status(enc.status) == dgc.EINVAL
+    enc = Encoder(3, n)
+    enc.cap = 40  # 3 tokens need 32 + 18 + 2 = 52 bytes
+    enc(torch.tensor([1, 2, 3], dtype=torch.int32, device="cuda"),
+        dev_f32(np.ones(3, np.float32)), torch.tensor([3], dtype=torch.int64, device="cuda"))
+    assert dgc.dgc_read_status(enc.status) == dgc.ECAPACITY
+    assert int(enc.out_bytes.item()) == 52
+
+
+def test_bad_segment_table_is_reported_and_state_untouched():
+    n = 10_000
+    pd = dgc.make_params(sparsity=0.99)
+    comp = Compressor(n, np.array([0, 6000, n]), pd)
+    comp.seg_off.copy_(torch.tensor([0, 7000, 5000], dtype=torch.int64))  # ends short of n
+    u = dev_f32(np.ones(n, np.float32))
+    v = dev_f32(np.ones(n, np.float32))
+    comp(dev_f32(np.ones(n, np.float32)), u, v)
+    assert comp.status_code() == dgc.EINVAL
+    assert np.all(host_f32(u) == 1.0) and np.all(host_f32(v) == 1.0)
+    assert int(comp.out_count.item()) == 0
+
+
+def test_bounded_wait_times_out():
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dgc.dgc_selftest_wait_timeout(status, 1000)
+    assert dgc.dgc_read_status(status) == dgc.ETIMEOUT
+    # the context is still usable afterwards
+    x = torch.ones(10, device="cuda")
+    assert float(x.sum()) == 10.0
+
+
+def test_checkpoint_resume_is_bitwise():
+    # The compressor state is exactly (u, v): restoring a copy reproduces the next step.
+    n = 300_000
+    off = np.array([0, 100_000, n])
+    pd = dgc.make_params(mode=dgc.SELECT_SAMPLED, sparsity=0.99, seed=5)
+    comp = Compressor(n, off, pd)
+    u = torch.zeros(n, device="cuda")
+    v = torch.zeros(n, device="cuda")
+    gs = [dev_f32(workloads.misc([t], n, 0.01)) for t in range(4)]
+    for t in range(3):
+        comp(gs[t], u, v)
+    ck = (u.clone(), v.clone())
+    comp(gs[3], u, v)
+    first = comp.results()
+    u.copy_(ck[0])
+    v.copy_(ck[1])
+    comp(gs[3], u, v)
+    second = comp.results()
+    assert np.array_equal(first[0], second[0]) and same_bits(first[1], second[1])
+
+
+def test_runs_are_deterministic():
+    n = 2_000_003
+    off = np.array([0, 1_000_000, n])
+    res = []
+    for _ in range(2):
+        for mode in (dgc.SELECT_EXACT, dgc.SELECT_SAMPLED):
+            comp = Compressor(n, off, dgc.make_params(mode=mode, sparsity=0.999, seed=3))
+            u = torch.zeros(n, device="cuda")
+            v = torch.zeros(n, device="cuda")
+            for t in range(3):
+                comp(dev_f32(workloads.misc([t, 1], n, 0.01)), u, v)
+            idx, val, _ = comp.results()
+            res.append((idx.tobytes(), val.tobytes(), host_f32(u).tobytes(), host_f32(v).tobytes()))
+    assert res[0] == res[2] and res[1] == res[3]
+
+
+def test_launch_counter_counts_kernels():
+    before = dgc.dgc_launch_count()
+    run_steps(lambda t: workloads.misc([t], 10_000, 1.0), np.array([0, 10_000]), 1)
+    assert dgc.dgc_launch_count() > before
