@@ -235,9 +235,15 @@ def dgc_launch_count() -> int:
 
 def dgc_profile_stream_pass(begin, end) -> None:
     """begin/end: torch.cuda.Event objects (created with enable_timing=True), or None."""
-    b = None if begin is None else begin.cuda_event
-    e = None if end is None else end.cuda_event
-    lib().dgc_profile_stream_pass(b, e)
+    handles = []
+    for ev in (begin, end):
+        if ev is None:
+            handles.append(None)
+            continue
+        if not ev.cuda_event:  # torch creates the CUDA event on its first record
+            ev.record()
+        handles.append(ev.cuda_event)
+    lib().dgc_profile_stream_pass(*handles)
 
 
 def dgc_selftest_wait_timeout(status, spin_limit: int, stream=None) -> int:

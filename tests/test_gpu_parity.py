@@ -29,6 +29,13 @@ def _built():
     oracle.lib()
 
 
+def dev_idx(idx):
+    """uint32 indices plus one spare entry, as a device int32 tensor."""
+    a = np.zeros(idx.size + 1, np.uint32)
+    a[: idx.size] = idx
+    return torch.from_numpy(a.view(np.int32)).cuda()
+
+
 def bits(a):
     return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
 
@@ -282,8 +289,8 @@ def golden_message(name):
 def test_codec_golden_on_gpu(name):
     n, idx, val, msg = golden_message(name)
     enc = Encoder(max(idx.size, 1), n)
-    enc(torch.from_numpy(np.append(idx, 0).view(np.int32)).cuda(),
-        dev_f32(np.append(val, 0)), torch.tensor([idx.size], dtype=torch.int64, device="cuda"))
+    enc(dev_idx(idx), dev_f32(np.append(val, np.float32(0))),
+        torch.tensor([idx.size], dtype=torch.int64, device="cuda"))
     assert dgc.dgc_read_status(enc.status) == 0
     assert enc.message() == msg
     rc, dense = decode([msg], n)
@@ -337,7 +344,7 @@ def test_encode_random_matches_oracle():
         idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
         val = rng.standard_normal(k).astype(np.float32)
         enc = Encoder(max(k, 1), n)
-        enc(torch.from_numpy(np.append(idx, 0).view(np.int32)).cuda(), dev_f32(np.append(val, 0)),
+        enc(dev_idx(idx), dev_f32(np.append(val, np.float32(0))),
             torch.tensor([k], dtype=torch.int64, device="cuda"))
         assert enc.message() == oracle.encode(idx, val, n)
 
