@@ -118,6 +118,29 @@ int dgc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* s
                  int64_t out_cap, int64_t* out_count, dgc_seg_stats* stats, int32_t* status,
                  void* ws, size_t ws_bytes, dgc_stream_t stream);
 
+/* dgc_compress for callers that cannot allocate device memory. The DGC and AdaComp pages have
+ * no counterpart to this entry point: it exists for integration, not for the method.
+ * Some callers cannot give the library a workspace at the point where they compress: their
+ * framework's allocator owns all device memory and hands none out for a library's private use;
+ * or they run while a CUDA graph is being captured, or in a loop where cudaMalloc (which may
+ * synchronize the device) is not allowed; or they must not grow the process's device-memory
+ * footprint once running. This variant takes dgc_compress's arguments without ws/ws_bytes and
+ * works in a 16 MiB scratch array that the library holds on every GPU it is loaded on (created
+ * when the library's device code loads on that GPU, kept until the process exits). It calls no
+ * allocation routine.
+ * Limit: the problem must fit the scratch, dgc_compress_workspace(n, nseg, params) <= 16 MiB --
+ * about 1.3 million entries in one segment. A larger problem returns DGC_EUNSUPPORTED before
+ * anything is enqueued; use dgc_compress with your own workspace instead.
+ * The first call on each device looks the scratch address up with cudaGetSymbolAddress (which
+ * may load the library's device code on that device); make that first call before any stream
+ * capture. All later calls on the device reuse the same array; each call re-initialises every
+ * part of it that it reads. Calls whose GPU work can overlap (streams without ordering between
+ * them, several host threads) race on the shared array: the caller must serialize them. */
+int dgc_compress_noalloc(const float* g, float* u, float* v, int64_t n, const int64_t* seg_off,
+                         int32_t nseg, const dgc_params* params, uint32_t* out_idx,
+                         float* out_val, int64_t out_cap, int64_t* out_count,
+                         dgc_seg_stats* stats, int32_t* status, dgc_stream_t stream);
+
 /* ------------------------------------------------------------------------------ codec */
 
 /* Message format, [DGC] Proposed method, bullet 2 (each sent value a 32-bit word, each run of

@@ -15,7 +15,7 @@ from ._build import LIB, build
 
 __all__ = [
     "DGCError", "build", "lib", "dgc_params", "dgc_seg_stats", "make_params",
-    "dgc_compress_workspace", "dgc_compress_max_out", "dgc_compress",
+    "dgc_compress_workspace", "dgc_compress_max_out", "dgc_compress", "dgc_compress_noalloc",
     "dgc_encode_max_bytes", "dgc_encode_workspace", "dgc_encode",
     "dgc_decode_workspace", "dgc_decode_accumulate",
     "dgc_read_status", "dgc_status_string", "dgc_launch_count", "dgc_selftest_wait_timeout",
@@ -80,6 +80,8 @@ def lib():
         L.dgc_compress_max_out.argtypes = [i64, i32, P(dgc_params), P(i64)]
         L.dgc_compress.argtypes = [vp, vp, vp, i64, vp, i32, P(dgc_params), vp, vp, i64, vp, vp,
                                    vp, vp, sz, vp]
+        L.dgc_compress_noalloc.argtypes = [vp, vp, vp, i64, vp, i32, P(dgc_params), vp, vp, i64,
+                                           vp, vp, vp, vp]
         L.dgc_encode_max_bytes.argtypes = [i64, i64, P(u64)]
         L.dgc_encode_workspace.argtypes = [i64, P(sz)]
         L.dgc_encode.argtypes = [vp, vp, vp, i64, i64, vp, u64, vp, vp, vp, sz, vp]
@@ -94,6 +96,7 @@ def lib():
         L.dgc_profile_stream_pass.argtypes = [vp, vp]
         L.dgc_profile_stream_pass.restype = None
         for f in ("dgc_compress_workspace", "dgc_compress_max_out", "dgc_compress",
+                  "dgc_compress_noalloc",
                   "dgc_encode_max_bytes", "dgc_encode_workspace", "dgc_encode",
                   "dgc_decode_workspace", "dgc_decode_accumulate", "dgc_read_status",
                   "dgc_selftest_wait_timeout"):
@@ -171,6 +174,21 @@ def dgc_compress(g, u, v, seg_off, params: dgc_params, out_idx, out_val, out_cou
                                      ctypes.byref(params), _ptr(out_idx), _ptr(out_val),
                                      int(out_cap), _ptr(out_count), _ptr(stats), _ptr(status),
                                      _ptr(ws), int(ws_bytes), _stream(stream)), "dgc_compress")
+
+
+def dgc_compress_noalloc(g, u, v, seg_off, params: dgc_params, out_idx, out_val, out_count,
+                         stats, status, n: int | None = None, out_cap: int | None = None,
+                         stream=None) -> int:
+    """dgc_compress without a caller workspace, for callers that cannot allocate device memory
+    (the library's own 16 MiB scratch per GPU; see include/dgc.h for the limit and rules)."""
+    n = g.numel() if n is None else n
+    nseg = seg_off.numel() - 1
+    out_cap = out_idx.numel() if out_cap is None else out_cap
+    return _check(lib().dgc_compress_noalloc(_ptr(g), _ptr(u), _ptr(v), int(n), _ptr(seg_off),
+                                             int(nseg), ctypes.byref(params), _ptr(out_idx),
+                                             _ptr(out_val), int(out_cap), _ptr(out_count),
+                                             _ptr(stats), _ptr(status), _stream(stream)),
+                  "dgc_compress_noalloc")
 
 
 # -------------------------------------------------------------------------------- codec
