@@ -129,7 +129,7 @@ int dgc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* s
  * when the library's device code loads on that GPU, kept until the process exits). It calls no
  * allocation routine.
  * Limit: the problem must fit the scratch, dgc_compress_workspace(n, nseg, params) <= 16 MiB --
- * about 1.3 million entries in one segment. A larger problem returns DGC_EUNSUPPORTED before
+ * about 2 million entries in one segment. A larger problem returns DGC_EUNSUPPORTED before
  * anything is enqueued; use dgc_compress with your own workspace instead.
  * The first call on each device looks the scratch address up with cudaGetSymbolAddress (which
  * may load the library's device code on that device); make that first call before any stream

@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) k_dec_pos(DecArgs a) {
 }
 
 __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
-    __shared__ float s_acc[kDecTile];
+    __shared__ __align__(16) float s_acc[kDecTile];
     __shared__ uint32_t s_pos[kDecCap];
     __shared__ float s_val[kDecCap];
     __shared__ uint32_t s_off[kThreads + 1];
@@ -299,8 +299,17 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
     const uint64_t t = blockIdx.x;
     const uint64_t p0 = t * kDecTile;
     const uint32_t len = (uint32_t)umin64(kDecTile, a.n - p0);
-    for (uint32_t i = threadIdx.x; i < kDecTile; i += kThreads)
-        s_acc[i] = (a.accumulate && i < len) ? a.dense[p0 + i] : 0.0f;
+    const bool vec = (len == kDecTile) && ((reinterpret_cast<uintptr_t>(a.dense) & 15u) == 0);
+    if (vec && a.accumulate) {
+        for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
+            reinterpret_cast<float4*>(s_acc)[i] = reinterpret_cast<const float4*>(a.dense + p0)[i];
+    } else if (vec) {
+        for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
+            reinterpret_cast<float4*>(s_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+        for (uint32_t i = threadIdx.x; i < kDecTile; i += kThreads)
+            s_acc[i] = (a.accumulate && i < len) ? a.dense[p0 + i] : 0.0f;
+    }
     for (int wb = 0; wb < a.W; wb += kThreads) {
         const int w = wb + threadIdx.x;
         uint32_t cnt = 0, first = 0;
@@ -344,7 +353,45 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
             __syncthreads();
         }
     }
-    for (uint32_t i = threadIdx.x; i < len; i += kThreads) a.dense[p0 + i] = s_acc[i];
+    __syncthreads();
+    if (vec) {
+        for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
+            reinterpret_cast<float4*>(a.dense + p0)[i] = reinterpret_cast<const float4*>(s_acc)[i];
+    } else {
+        for (uint32_t i = threadIdx.x; i < len; i += kThreads) a.dense[p0 + i] = s_acc[i];
+    }
+}
+
+// One message (W = 1): its positions are distinct, so its values can be added in parallel. The
+// dense output is first cleared by a streaming store pass (unless accumulating), then each value
+// token adds itself to its position: the same single binary32 addition per value as the tile
+// kernel performs, onto the same starting value.
+__global__ void __launch_bounds__(kThreads) k_dec_zero(DecArgs a) {
+    if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
+    float* dense = a.dense;
+    const uint64_t n = a.n;
+    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    if ((reinterpret_cast<uintptr_t>(dense) & 15u) == 0) {
+        float4* d4 = reinterpret_cast<float4*>(dense);
+        const uint64_t n4 = n / 4;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (uint64_t i = tid; i < n4; i += stride) __stcs(d4 + i, z);
+        for (uint64_t i = n4 * 4 + tid; i < n; i += stride) dense[i] = 0.0f;
+    } else {
+        for (uint64_t i = tid; i < n; i += stride) dense[i] = 0.0f;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) k_dec_scatter1(DecArgs a) {
+    if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
+    const DecStream d = a.tab[0];
+    const uint64_t j = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= d.T) return;
+    const uint32_t p = a.pos[d.tok_base + j];
+    if (p == kEscPos || p >= a.n) return;
+    const float x = reinterpret_cast<const float*>(d.ptr + 32)[j];
+    a.dense[p] = __fadd_rn(a.dense[p], x);
 }
 
 struct DecLayout {
@@ -505,7 +552,18 @@ extern "C" int dgc_decode_accumulate(const uint8_t* const* streams, const uint64
         k_dec_pos<<<(unsigned)L.nchunks, kThreads, 0, s>>>(a);
         ++launches;
     }
-    if (L.ntiles > 0) {
+    if (W == 1) {  // runs after the positions are checked: a malformed message changes nothing
+        if (!accumulate && n > 0) {
+            const int sms = dgc_internal_sm_count();
+            if (sms <= 0) return DGC_ECUDA;
+            k_dec_zero<<<(unsigned)sms * 8, kThreads, 0, s>>>(a);
+            ++launches;
+        }
+        if (L.sum_T > 0) {
+            k_dec_scatter1<<<(unsigned)((L.sum_T + kThreads - 1) / kThreads), kThreads, 0, s>>>(a);
+            ++launches;
+        }
+    } else if (L.ntiles > 0) {
         k_dec_tiles<<<(unsigned)L.ntiles, kThreads, 0, s>>>(a);
         ++launches;
     }

@@ -37,6 +37,27 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRows = 8;                          // float4 rows per thread in the streaming pass
 constexpr int kTile = kThreads * kRows * 4;       // 8192 entries per streaming tile
+// streaming pass shape: entries per tile, tiles in flight per block, blocks per SM
+// (2048 entries x 4 stages x 2 blocks per SM: the fastest of the shapes measured on GB300)
+#ifndef DGC_STREAM_TILE
+#define DGC_STREAM_TILE 2048
+#endif
+#ifndef DGC_STREAM_STAGES
+#define DGC_STREAM_STAGES 4
+#endif
+#ifndef DGC_STREAM_BLOCKS_PER_SM
+#define DGC_STREAM_BLOCKS_PER_SM 2
+#endif
+constexpr int kPTile = DGC_STREAM_TILE;
+constexpr int kPStages = DGC_STREAM_STAGES;
+constexpr int kPBlocksPerSM = DGC_STREAM_BLOCKS_PER_SM;
+constexpr int kPRows = kPTile / (4 * kThreads);   // float4 rows per thread
+constexpr int kWarps = kThreads / 32;
+static_assert(kPRows >= 1 && kPRows * 4 * kThreads == kPTile, "tile = rows x 1024 entries");
+static_assert(kPRows * kWarps <= 32, "one warp scans the per-(row, warp) counts");
+constexpr uint32_t kPStageFloats = 3u * kPTile;   // g, u, v
+constexpr size_t kPSmemBytes = sizeof(float) * kPStageFloats * kPStages;  // 192 KiB
+constexpr uint32_t kMbarSpinLimit = 1u << 22;
 constexpr int kEmitRows = 4;
 constexpr int kEmitTile = kThreads * kEmitRows * 4;  // 4096 candidates per emit tile
 constexpr int kClipTile = 4096;
@@ -75,7 +96,7 @@ struct Ctl {
     int32_t abort;
     uint32_t active;
     uint32_t any_failed;
-    uint32_t ticket_fused, ticket_compact, ticket_emit;
+    uint32_t ticket_fused, ticket_compact, ticket_emit, ticket_collect;
     uint32_t total_samples, total_clip_tiles, total_cand, total_sent;
     uint32_t emit_done;
     uint32_t pad;
@@ -84,8 +105,8 @@ struct Ctl {
 // Workspace layout (host computes it; every piece 256-byte aligned).
 struct Layout {
     size_t ctl, segs, seg_start, samp_off, clip_off, cand_off, clip_part, skeys, histA, histB;
-    size_t st_fused, st_compact, st_emit, cidx, cval, cu, total;
-    uint64_t max_samples, max_clip_tiles, fused_tiles, emit_tiles;
+    size_t st_collect, st_compact, st_emit, cidx, sidx, tcount, total;
+    uint64_t max_samples, max_clip_tiles, fused_tiles, emit_tiles, ptiles, cgroups;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -129,6 +150,8 @@ Layout make_layout(int64_t n, int32_t nseg, const HostParams& hp) {
     L.max_samples = count_ppb(un, hp.r_ppb) + (uint64_t)nseg;
     L.max_clip_tiles = hp.clip_on ? (un + kClipTile - 1) / kClipTile + (uint64_t)nseg : 0;
     L.fused_tiles = (un + kTile - 1) / kTile;
+    L.ptiles = (un + kPTile - 1) / kPTile;
+    L.cgroups = (L.ptiles + kThreads - 1) / kThreads;
     L.emit_tiles = (un + kEmitTile - 1) / kEmitTile;
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
@@ -142,12 +165,12 @@ Layout make_layout(int64_t n, int32_t nseg, const HostParams& hp) {
     L.skeys = take(sizeof(uint32_t) * (size_t)L.max_samples);
     L.histA = take(sizeof(uint32_t) * (size_t)nseg * kHistBins);
     L.histB = take(sizeof(uint32_t) * (size_t)nseg * kHistBins);
-    L.st_fused = take(sizeof(uint64_t) * (size_t)(L.fused_tiles + 1));
+    L.st_collect = take(sizeof(uint64_t) * (size_t)(L.cgroups + 1));
     L.st_compact = take(sizeof(uint64_t) * (size_t)(L.fused_tiles + 1));
     L.st_emit = take(sizeof(uint64_t) * (size_t)(L.emit_tiles + 1));
     L.cidx = take(sizeof(uint32_t) * (size_t)un);
-    L.cval = take(sizeof(float) * (size_t)un);
-    L.cu = take(sizeof(float) * (size_t)un);
+    L.sidx = take(sizeof(uint32_t) * (size_t)un);
+    L.tcount = take(sizeof(uint32_t) * (size_t)(L.ptiles + 1));
     L.total = o;
     return L;
 }
@@ -190,13 +213,13 @@ struct Args {
     uint32_t* skeys;
     uint32_t* histA;
     uint32_t* histB;
-    uint64_t* st_fused;
+    uint64_t* st_collect;
     uint64_t* st_compact;
     uint64_t* st_emit;
-    uint32_t* cidx;
-    float* cval;
-    float* cu;
-    uint64_t max_samples, fused_tiles, emit_tiles, max_clip_tiles;
+    uint32_t* cidx;   // candidates, ascending index
+    uint32_t* sidx;   // per-tile candidate slots of the streaming pass
+    uint32_t* tcount; // per-tile candidate counts
+    uint64_t max_samples, fused_tiles, emit_tiles, max_clip_tiles, ptiles, cgroups;
     uint32_t spin_limit;
 };
 
@@ -294,10 +317,8 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
         a.histA[i] = 0;
         a.histB[i] = 0;
     }
-    for (size_t i = tid; i <= a.fused_tiles; i += stride) {
-        a.st_fused[i] = 0;
-        a.st_compact[i] = 0;
-    }
+    for (size_t i = tid; i <= a.fused_tiles; i += stride) a.st_compact[i] = 0;
+    for (size_t i = tid; i <= a.cgroups; i += stride) a.st_collect[i] = 0;
     for (size_t i = tid; i <= a.emit_tiles; i += stride) a.st_emit[i] = 0;
 }
 
@@ -442,7 +463,8 @@ __global__ void __launch_bounds__(kThreads) k_sample(Args a) {
 template <int kKind>
 __device__ __forceinline__ uint64_t item_x(const Args& a, uint32_t i) {
     if (kKind == 0) return (uint64_t)a.skeys[i] << 32;
-    return ((uint64_t)key_of(a.cval[i]) << 32) | (uint64_t)(~a.cidx[i]);
+    const uint32_t idx = a.cidx[i];
+    return ((uint64_t)key_of(a.v[idx]) << 32) | (uint64_t)(~idx);
 }
 
 template <int kKind>
@@ -474,9 +496,17 @@ __global__ void __launch_bounds__(kThreads) k_hist(Args a, int level) {
                 h.cur = s0;
             }
             const uint64_t prefix = a.segs[s0].prefix;
-            for (uint32_t i = (uint32_t)c0 + threadIdx.x; i < c1; i += kThreads) {
-                const uint64_t x = item_x<kKind>(a, i);
-                if ((x >> (shift + bits)) == prefix) atomicAdd(&s_hist[(x >> shift) & mask], 1u);
+            uint64_t xs[kPer];
+#pragma unroll
+            for (int r = 0; r < kPer; ++r) {  // all loads first, then the counting
+                const uint32_t i = (uint32_t)c0 + r * kThreads + threadIdx.x;
+                xs[r] = (i < c1) ? item_x<kKind>(a, i) : ~0ull;
+            }
+#pragma unroll
+            for (int r = 0; r < kPer; ++r) {
+                const uint32_t i = (uint32_t)c0 + r * kThreads + threadIdx.x;
+                if (i < c1 && (xs[r] >> (shift + bits)) == prefix)
+                    atomicAdd(&s_hist[(xs[r] >> shift) & mask], 1u);
             }
         } else {
             for (uint32_t i = (uint32_t)c0 + threadIdx.x; i < c1; i += kThreads) {
@@ -576,119 +606,51 @@ __global__ void __launch_bounds__(kThreads) k_find(Args a, int level) {
     }
 }
 
-// --------------------------------------------------------------------- streaming pass
-// kMode 0: exact-mode pass (accumulate, compact candidates). kMode 1: sampled-mode pass
-// (accumulate, compact candidates and clear their v and, with masking, u). kMode 2: exact-mode
-// re-compaction from v alone (a segment whose bound was too tight takes threshold 0).
-// Thread t of a tile handles float4 q = r*256 + t for rows r, so every load is a coalesced
-// 16-byte access; candidate order inside the tile comes from a bitmap of the tile.
-template <int kMode>
-__global__ void __launch_bounds__(kThreads, 2) k_stream(Args a) {
+// ------------------------------------------------------------- exact-mode re-compaction
+// Runs only when, in exact mode, a segment's sampled lower bound admitted fewer than k
+// candidates: it rebuilds the whole index-ordered candidate list from v (already updated),
+// with threshold 0 for those segments. One tile per block, offsets by decoupled look-back.
+__global__ void __launch_bounds__(kThreads, 2) k_recompact(Args a) {
     __shared__ uint32_t s_bitmap[kTile / 32];
     __shared__ uint32_t s_wordpre[kTile / 32];
     __shared__ uint32_t s_scan[33];
     __shared__ uint32_t s_tile;
     __shared__ uint64_t s_base;
-    __shared__ int s_seg0, s_uniform;
-    __shared__ float s_scale;
+    __shared__ int s_uniform, s_skip;
     __shared__ uint32_t s_thresh;
-    __shared__ int s_skip;
     const uint64_t n = a.n;
-    uint32_t* ticket = kMode == 2 ? &a.ctl->ticket_compact : &a.ctl->ticket_fused;
-    uint64_t* st = kMode == 2 ? a.st_compact : a.st_fused;
     // one thread reads the flags and takes the tile, so the whole block agrees
     if (threadIdx.x == 0) {
-        s_skip = (kMode == 2 && !a.ctl->any_failed) || ld_relaxed_u32((const uint32_t*)&a.ctl->abort);
-        if (!s_skip) s_tile = atomicAdd(ticket, 1u);
+        s_skip = !a.ctl->any_failed || ld_relaxed_u32((const uint32_t*)&a.ctl->abort);
+        if (!s_skip) s_tile = atomicAdd(&a.ctl->ticket_compact, 1u);
     }
     for (int w = threadIdx.x; w < kTile / 32; w += kThreads) s_bitmap[w] = 0;
     __syncthreads();
     if (s_skip) return;
     const uint32_t tile = s_tile;
     const uint64_t base = (uint64_t)tile * kTile;
-    const uint64_t tile_end = umin64(a.n, base + kTile);
+    const uint64_t tile_end = umin64(n, base + kTile);
     if (threadIdx.x == 0) {
-        const int s0 = upper_bound_minus1(a.seg_start, a.nseg, (uint32_t)base);
-        s_seg0 = s0;
-        const SegInfo& d = a.segs[s0];
+        const SegInfo& d = a.segs[upper_bound_minus1(a.seg_start, a.nseg, (uint32_t)base)];
         s_uniform = (d.end >= tile_end) ? 1 : 0;
-        s_scale = d.scale;
-        s_thresh = (kMode == 2 && d.failed) ? 0u : d.thresh;
+        s_thresh = d.failed ? 0u : d.thresh;
     }
     __syncthreads();
-    const bool uniform = s_uniform;
-    const float m = a.hp.momentum;
-    const bool full = (base + kTile <= a.n);
-
-    float4 vv[kRows], uu[kRows];
     uint32_t flags = 0;  // bit r*4+e: entry e of row r is a candidate
-    if (kMode == 2) {
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-            const uint64_t e0 = base + 4u * (r * kThreads + threadIdx.x);
-            if (full) {
-                vv[r] = *reinterpret_cast<const float4*>(a.v + e0);
-            } else {
-                float t[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) t[e] = (e0 + e < n) ? a.v[e0 + e] : 0.0f;
-                vv[r] = make_float4(t[0], t[1], t[2], t[3]);
-            }
-            uu[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    } else {
-        float4 gg[kRows];
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-            const uint64_t e0 = base + 4u * (r * kThreads + threadIdx.x);
-            if (full) {
-                gg[r] = __ldcs(reinterpret_cast<const float4*>(a.g + e0));
-                uu[r] = *reinterpret_cast<const float4*>(a.u + e0);
-                vv[r] = *reinterpret_cast<const float4*>(a.v + e0);
-            } else {
-                float tg[4], tu[4], tv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const bool in = e0 + e < n;
-                    tg[e] = in ? a.g[e0 + e] : 0.f;
-                    tu[e] = in ? a.u[e0 + e] : 0.f;
-                    tv[e] = in ? a.v[e0 + e] : 0.f;
-                }
-                gg[r] = make_float4(tg[0], tg[1], tg[2], tg[3]);
-                uu[r] = make_float4(tu[0], tu[1], tu[2], tu[3]);
-                vv[r] = make_float4(tv[0], tv[1], tv[2], tv[3]);
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-            const uint64_t e0 = base + 4u * (r * kThreads + threadIdx.x);
-            float* g4 = reinterpret_cast<float*>(&gg[r]);
-            float* u4 = reinterpret_cast<float*>(&uu[r]);
-            float* v4 = reinterpret_cast<float*>(&vv[r]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float scale = s_scale;
-                if (!uniform && e0 + e < n)
-                    scale = a.segs[upper_bound_minus1(a.seg_start, a.nseg, (uint32_t)(e0 + e))].scale;
-                accumulate(g4[e], u4[e], v4[e], m, scale);
-            }
-        }
-    }
-    // candidates
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
         const uint64_t e0 = base + 4u * (r * kThreads + threadIdx.x);
-        const float* v4 = reinterpret_cast<const float*>(&vv[r]);
         uint32_t f4 = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             if (e0 + e >= n) continue;
             uint32_t t = s_thresh;
-            if (!uniform) {
-                const SegInfo& d = a.segs[upper_bound_minus1(a.seg_start, a.nseg, (uint32_t)(e0 + e))];
-                t = (kMode == 2 && d.failed) ? 0u : d.thresh;
+            if (!s_uniform) {
+                const SegInfo& d =
+                    a.segs[upper_bound_minus1(a.seg_start, a.nseg, (uint32_t)(e0 + e))];
+                t = d.failed ? 0u : d.thresh;
             }
-            if (key_of(v4[e]) >= t) f4 |= 1u << e;
+            if (key_of(a.v[e0 + e]) >= t) f4 |= 1u << e;
         }
         if (f4) {
             const uint32_t off = (uint32_t)(e0 - base);
@@ -696,75 +658,272 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(Args a) {
         }
         flags |= f4 << (4 * r);
     }
-    // stores of the updated state (sampled mode clears candidates optimistically)
-    if (kMode != 2) {
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-            const uint64_t e0 = base + 4u * (r * kThreads + threadIdx.x);
-            float4 vs = vv[r], us = uu[r];
-            if (kMode == 1) {
-                float* v4 = reinterpret_cast<float*>(&vs);
-                float* u4 = reinterpret_cast<float*>(&us);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (flags & (1u << (4 * r + e))) {
-                        v4[e] = 0.0f;
-                        if (a.hp.mask) u4[e] = 0.0f;
-                    }
-            }
-            if (full) {
-                *reinterpret_cast<float4*>(a.u + e0) = us;
-                *reinterpret_cast<float4*>(a.v + e0) = vs;
-            } else {
-                const float* u4 = reinterpret_cast<const float*>(&us);
-                const float* v4 = reinterpret_cast<const float*>(&vs);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (e0 + e < n) {
-                        a.u[e0 + e] = u4[e];
-                        a.v[e0 + e] = v4[e];
-                    }
-            }
-        }
-    }
     __syncthreads();
-    // tile-local ranks from the bitmap, then the global base from the look-back
-    uint32_t cnt = 0;
-    for (int w = threadIdx.x; w < kTile / 32; w += kThreads) cnt += __popc(s_bitmap[w]);
     static_assert(kTile / 32 == kThreads, "one bitmap word per thread");
+    const uint32_t cnt = __popc(s_bitmap[threadIdx.x]);
     uint32_t tile_total;
-    const uint32_t ex = block_excl_scan<kThreads>(cnt, s_scan, &tile_total);
-    s_wordpre[threadIdx.x] = ex;
+    s_wordpre[threadIdx.x] = block_excl_scan<kThreads>(cnt, s_scan, &tile_total);
     if (threadIdx.x < 32) {
-        const uint64_t excl = lookback_exclusive(st, tile, tile_total, a.spin_limit, a.status,
-                                                 &a.ctl->abort);
+        const uint64_t excl = lookback_exclusive(a.st_compact, tile, tile_total, a.spin_limit,
+                                                 a.status, &a.ctl->abort);
         if (threadIdx.x == 0) s_base = excl;
     }
     __syncthreads();
     const uint64_t gbase = s_base;
-    if (flags) {
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-            const uint64_t e0 = base + 4u * (r * kThreads + threadIdx.x);
-            const float* v4 = reinterpret_cast<const float*>(&vv[r]);
-            const float* u4 = reinterpret_cast<const float*>(&uu[r]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (!(flags & (1u << (4 * r + e)))) continue;
-                const uint32_t off = (uint32_t)(e0 + e - base);
-                const uint32_t w = off >> 5;
-                const uint32_t rank = s_wordpre[w] + __popc(s_bitmap[w] & ((1u << (off & 31)) - 1u));
-                const uint64_t pos = gbase + rank;
-                if (pos < n) {
-                    a.cidx[pos] = (uint32_t)(e0 + e);
-                    a.cval[pos] = v4[e];
-                    if (kMode == 1) a.cu[pos] = u4[e];
-                }
-            }
-        }
+    for (int q = 0; q < kRows * 4; ++q) {
+        if (!(flags & (1u << q))) continue;
+        const uint32_t off = 4u * ((q >> 2) * kThreads + threadIdx.x) + (q & 3);
+        const uint32_t w = off >> 5;
+        const uint64_t pos = gbase + s_wordpre[w] + __popc(s_bitmap[w] & ((1u << (off & 31)) - 1u));
+        if (pos < n) a.cidx[pos] = (uint32_t)(base + off);
     }
     if (tile == a.fused_tiles - 1 && threadIdx.x == 0)
         a.ctl->total_cand = (uint32_t)umin64(gbase + tile_total, n);
+}
+
+// ------------------------------------------------- streaming pass, bulk-copy pipeline
+// The pass every entry goes through: u = fma(m, u, g*scale); v += u; candidates are the
+// entries with key(v) >= the segment's threshold. Persistent blocks (one per SM) take 4096-entry
+// tiles from an atomic ticket and keep kPStages tiles of g, u and v in flight as bulk copies
+// (TMA, cp.async.bulk) into shared memory, so HBM streams without pause. Updated u and v go back
+// with coalesced 16-byte stores. A tile's candidates are compacted, in index order, into the
+// tile's own slot range sidx[base, base + count) and its count into tcount[tile]: no block
+// ever waits on another, and k_collect turns the counts into global offsets afterwards.
+template <bool kKeepU>
+__device__ __forceinline__ void stream_compute(const Args& a, const float* sg, uint64_t base,
+                                               uint32_t len, bool uniform, float scale0,
+                                               uint32_t thresh0, float4 (&uu)[kPRows],
+                                               float4 (&vv)[kPRows], uint32_t& flags) {
+    const int tid = threadIdx.x;
+    const uint32_t bulk = len & ~3u;
+    flags = 0;
+#pragma unroll
+    for (int r = 0; r < kPRows; ++r) {
+        const uint32_t off = 4u * (r * kThreads + tid);
+        float4 g4, u4, v4;
+        if (off + 4 <= bulk) {
+            g4 = reinterpret_cast<const float4*>(sg)[r * kThreads + tid];
+            u4 = reinterpret_cast<const float4*>(sg + kPTile)[r * kThreads + tid];
+            v4 = reinterpret_cast<const float4*>(sg + 2 * kPTile)[r * kThreads + tid];
+        } else {  // the last, ragged tile: at most 3 entries past the bulk copy
+            float tg[4], tu[4], tv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool in = off + e < len;
+                tg[e] = in ? a.g[base + off + e] : 0.f;
+                tu[e] = in ? a.u[base + off + e] : 0.f;
+                tv[e] = in ? a.v[base + off + e] : 0.f;
+            }
+            g4 = make_float4(tg[0], tg[1], tg[2], tg[3]);
+            u4 = make_float4(tu[0], tu[1], tu[2], tu[3]);
+            v4 = make_float4(tv[0], tv[1], tv[2], tv[3]);
+        }
+        float* gp = reinterpret_cast<float*>(&g4);
+        float* up = reinterpret_cast<float*>(&u4);
+        float* vp = reinterpret_cast<float*>(&v4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (off + e >= len) continue;
+            float scale = scale0;
+            uint32_t t = thresh0;
+            if (!uniform) {
+                const SegInfo& d = a.segs[upper_bound_minus1(a.seg_start, a.nseg,
+                                                             (uint32_t)(base + off + e))];
+                scale = d.scale;
+                t = d.thresh;
+            }
+            accumulate(gp[e], up[e], vp[e], a.hp.momentum, scale);
+            if (key_of(vp[e]) >= t) flags |= 1u << (4 * r + e);
+        }
+        if (kKeepU) uu[r] = u4;
+        vv[r] = v4;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) {
+    extern __shared__ __align__(128) float s_stage[];  // [kPStages][3][kPTile]
+    __shared__ __align__(8) uint64_t s_bar[kPStages];
+    __shared__ uint32_t s_tile[kPStages];
+    __shared__ int s_uniform[kPStages];
+    __shared__ float s_scale[kPStages];
+    __shared__ uint32_t s_thresh[kPStages];
+    __shared__ uint32_t s_rc[2][kPRows * kWarps];  // candidates per (row, warp), by parity
+    __shared__ int s_skip;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint64_t n = a.n;
+    const uint32_t ntiles = (uint32_t)((n + kPTile - 1) / kPTile);
+
+    // thread 0 owns the pipeline: it takes a ticket, notes the tile's segment, and starts the
+    // tile's three bulk copies; the mbarrier phase publishes all of it to the block
+    auto issue = [&](int st) {
+        const uint32_t t = atomicAdd(&a.ctl->ticket_fused, 1u);
+        s_tile[st] = t;
+        if (t < ntiles) {
+            const uint64_t base = (uint64_t)t * kPTile;
+            const uint32_t len = (uint32_t)umin64(kPTile, n - base);
+            const SegInfo& d = a.segs[upper_bound_minus1(a.seg_start, a.nseg, (uint32_t)base)];
+            s_uniform[st] = (d.end >= base + len) ? 1 : 0;
+            s_scale[st] = d.scale;
+            s_thresh[st] = d.thresh;
+            const uint32_t bytes = (len & ~3u) * 4u;  // whole 16-byte units; the rest by hand
+            mbar_arrive_expect_tx(&s_bar[st], 3u * bytes);
+            if (bytes) {
+                float* dst = s_stage + (size_t)st * kPStageFloats;
+                bulk_g2s(dst, a.g + base, bytes, &s_bar[st]);
+                bulk_g2s(dst + kPTile, a.u + base, bytes, &s_bar[st]);
+                bulk_g2s(dst + 2 * kPTile, a.v + base, bytes, &s_bar[st]);
+            }
+        } else {
+            mbar_arrive_expect_tx(&s_bar[st], 0u);  // an empty phase marks the end
+        }
+    };
+
+    if (tid == 0) {
+        s_skip = ld_relaxed_u32((const uint32_t*)&a.ctl->abort);
+        if (!s_skip) {
+            for (int st = 0; st < kPStages; ++st) mbar_init(&s_bar[st], 1);
+            mbar_init_fence();
+            for (int st = 0; st < kPStages; ++st) issue(st);
+        }
+    }
+    __syncthreads();
+    if (s_skip) return;
+
+    for (uint32_t it = 0;; ++it) {
+        const int st = (int)(it % kPStages);
+        const uint32_t parity = (it / kPStages) & 1u;
+        uint32_t spins = 0;
+        while (!mbar_try_wait(&s_bar[st], parity)) {
+            if (++spins > kMbarSpinLimit) {  // a bulk copy that never lands: report, give the
+                if (tid == 0) {              // copy one more bounded wait, then leave
+                    report(a.status, DGC_ETIMEOUT);
+                    atomicExch(&a.ctl->abort, 1);
+                }
+                for (uint32_t k = 0; k < kMbarSpinLimit && !mbar_try_wait(&s_bar[st], parity); ++k) {
+                }
+                return;
+            }
+        }
+        const uint32_t tile = s_tile[st];
+        if (tile >= ntiles) break;  // every later stage holds an empty phase too
+        const uint64_t base = (uint64_t)tile * kPTile;
+        const uint32_t len = (uint32_t)(umin64(n, base + kPTile) - base);
+        float4 uu[kPRows], vv[kPRows];
+        uint32_t flags;
+        stream_compute<true>(a, s_stage + (size_t)st * kPStageFloats, base, len, s_uniform[st],
+                             s_scale[st], s_thresh[st], uu, vv, flags);
+        // candidate words: the 8 lanes of a lane-group cover 32 consecutive entries of a row
+        uint32_t word[kPRows];
+#pragma unroll
+        for (int r = 0; r < kPRows; ++r) {
+            const uint32_t off = 4u * (r * kThreads + tid);
+            uint32_t x = ((flags >> (4 * r)) & 0xFu) << (4 * (lane & 7));
+            x |= __shfl_xor_sync(kFull, x, 1);
+            x |= __shfl_xor_sync(kFull, x, 2);
+            x |= __shfl_xor_sync(kFull, x, 4);
+            word[r] = x;
+            const uint32_t pc = __popc(x);
+            const uint32_t rc = __shfl_sync(kFull, pc, 0) + __shfl_sync(kFull, pc, 8) +
+                                __shfl_sync(kFull, pc, 16) + __shfl_sync(kFull, pc, 24);
+            if (lane == 0) s_rc[it & 1][r * kWarps + warp] = rc;
+            if (off + 4 <= len) {
+                *reinterpret_cast<float4*>(a.u + base + off) = uu[r];
+                *reinterpret_cast<float4*>(a.v + base + off) = vv[r];
+            } else {
+                const float* u2 = reinterpret_cast<const float*>(&uu[r]);
+                const float* v2 = reinterpret_cast<const float*>(&vv[r]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (off + e < len) {
+                        a.u[base + off + e] = u2[e];
+                        a.v[base + off + e] = v2[e];
+                    }
+            }
+        }
+        __syncthreads();  // the stage's data is in registers, the per-(row, warp) counts in place
+        if (tid == 0) {
+            fence_proxy_async_smem();
+            issue(st);  // the next tile for this stage starts loading now
+        }
+        // every warp scans the kPRows x kWarps counts itself (row-major = index order)
+        const uint32_t cv = (lane < kPRows * kWarps) ? s_rc[it & 1][lane] : 0u;
+        const uint32_t cinc = warp_incl_scan(cv);
+        const uint32_t tile_total = __shfl_sync(kFull, cinc, 31);
+#pragma unroll
+        for (int r = 0; r < kPRows; ++r) {  // every lane joins the shuffles, candidates or not
+            const uint32_t f4 = (flags >> (4 * r)) & 0xFu;
+            // entries before this lane's: earlier (row, warp) chunks, earlier lane-groups of this
+            // chunk, earlier lanes of this lane-group
+            const int ci = r * kWarps + warp;
+            uint32_t before = __shfl_sync(kFull, cinc, ci) - __shfl_sync(kFull, cv, ci);
+            const uint32_t p0 = __popc(__shfl_sync(kFull, word[r], 0));
+            const uint32_t p1 = __popc(__shfl_sync(kFull, word[r], 8));
+            const uint32_t p2 = __popc(__shfl_sync(kFull, word[r], 16));
+            const int grp = lane >> 3;
+            before += (grp > 0 ? p0 : 0) + (grp > 1 ? p1 : 0) + (grp > 2 ? p2 : 0);
+            const uint32_t sh = 4u * (lane & 7);
+            if (f4) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (f4 & (1u << e)) {
+                        const uint32_t rank = before + __popc(word[r] & ((1u << (sh + e)) - 1u));
+                        a.sidx[base + rank] = (uint32_t)(base + 4u * (r * kThreads + tid) + e);
+                    }
+            }
+        }
+        if (tid == 0) a.tcount[tile] = tile_total;
+    }
+}
+
+// ------------------------------------------------------------------------- collect
+// Turns the streaming pass's per-tile slots into one index-ordered candidate list. Block b owns
+// kCGroup consecutive tiles: it scans their counts, gets the group's global offset from a
+// decoupled look-back over groups, and copies the slots to cidx[offset + rank].
+constexpr int kCGroup = kThreads;  // tiles per collect block
+
+__global__ void __launch_bounds__(kThreads) k_collect(Args a) {
+    __shared__ uint32_t s_ex[kCGroup + 1];
+    __shared__ uint32_t s_scan[33];
+    __shared__ uint32_t s_group;
+    __shared__ uint64_t s_base;
+    __shared__ int s_skip;
+    const int tid = threadIdx.x;
+    const uint32_t ntiles = (uint32_t)a.ptiles;
+    const uint32_t ngroups = (ntiles + kCGroup - 1) / kCGroup;
+    if (tid == 0) {
+        s_skip = ld_relaxed_u32((const uint32_t*)&a.ctl->abort);
+        if (!s_skip) s_group = atomicAdd(&a.ctl->ticket_collect, 1u);
+    }
+    __syncthreads();
+    if (s_skip) return;
+    const uint32_t grp = s_group;
+    if (grp >= ngroups) return;
+    const uint32_t t = grp * kCGroup + tid;
+    const uint32_t c = (t < ntiles) ? a.tcount[t] : 0u;
+    uint32_t total;
+    const uint32_t ex = block_excl_scan<kThreads>(c, s_scan, &total);
+    s_ex[tid] = ex;
+    if (tid == 0) s_ex[kCGroup] = total;
+    if (tid < 32) {
+        const uint64_t b = lookback_exclusive(a.st_collect, grp, total, a.spin_limit, a.status,
+                                              &a.ctl->abort);
+        if (tid == 0) s_base = b;
+    }
+    __syncthreads();
+    const uint64_t gbase = s_base;
+    for (uint32_t f = tid; f < total; f += kThreads) {
+        int lo = 0, hi = kCGroup;  // the tile of flattened entry f
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_ex[mid] <= f) lo = mid; else hi = mid;
+        }
+        const uint64_t tb = (uint64_t)(grp * kCGroup + lo) * kPTile;
+        const uint64_t pos = gbase + f;
+        if (pos < a.n) a.cidx[pos] = a.sidx[tb + (f - s_ex[lo])];
+    }
+    if (grp == ngroups - 1 && tid == 0)
+        a.ctl->total_cand = (uint32_t)umin64(gbase + total, a.n);
 }
 
 // ------------------------------------------------------------------- candidate ranges
@@ -824,10 +983,9 @@ __global__ void __launch_bounds__(1024) k_candoff(Args a, int pass) {
 
 // ---------------------------------------------------------------------------------- emit
 // Candidates in index order; selected <=> X >= sel_x of their segment. Positions of the
-// selected ones come from a second decoupled look-back. Exact mode clears v (and u) of what
-// is sent; sampled mode put back v (and u) of candidates that re-selection dropped. The last
-// block to finish writes out_count and the statistics.
-template <int kMode>
+// selected ones come from a decoupled look-back. Each sent entry leaves the accumulator
+// (v <- 0) and, with masking, its momentum (u <- 0). The last block to finish writes out_count
+// and the statistics.
 __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
     __shared__ uint32_t s_bitmap[kEmitTile / 32];
     __shared__ uint32_t s_wordpre[kEmitTile / 32];
@@ -860,7 +1018,7 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
                 seg[q] = -1;
                 if (i < total) {
                     idx[q] = a.cidx[i];
-                    val[q] = a.cval[i];
+                    val[q] = a.v[idx[q]];
                     const int s = upper_bound_minus1(a.cand_off, a.nseg, (uint32_t)i);
                     seg[q] = s;
                     const uint64_t x = ((uint64_t)key_of(val[q]) << 32) | (uint64_t)(~idx[q]);
@@ -886,11 +1044,17 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
         }
         __syncthreads();
         const uint64_t gbase = s_base;
+        int my_seg = -1;             // the smallest key sent, per segment: one atomic per warp
+        uint32_t my_min = 0xFFFFFFFFu;
 #pragma unroll
         for (int q = 0; q < kEmitRows * 4; ++q) {
             if (seg[q] < 0) continue;
             const uint64_t i = base + 4u * ((q >> 2) * kThreads + threadIdx.x) + (q & 3);
             if (sel & (1u << q)) {
+                const uint32_t key = key_of(val[q]);
+                if (my_seg < 0) my_seg = seg[q];
+                if (seg[q] == my_seg) my_min = min(my_min, key);
+                else atomicMin(&a.segs[seg[q]].min_key, key);
                 const uint32_t off = (uint32_t)(i - base);
                 const uint32_t w = off >> 5;
                 const uint64_t pos =
@@ -899,15 +1063,15 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
                     a.out_idx[pos] = idx[q];
                     a.out_val[pos] = val[q];
                 }
-                if (kMode == 0) {
-                    a.v[idx[q]] = 0.0f;
-                    if (a.hp.mask) a.u[idx[q]] = 0.0f;
-                }
-                atomicMin(&a.segs[seg[q]].min_key, key_of(val[q]));
-            } else if (kMode == 1) {
-                a.v[idx[q]] = val[q];
-                if (a.hp.mask) a.u[idx[q]] = a.cu[i];
+                a.v[idx[q]] = 0.0f;
+                if (a.hp.mask) a.u[idx[q]] = 0.0f;
             }
+        }
+        {
+            const unsigned group = __match_any_sync(kFull, my_seg);
+            const uint32_t gmin = __reduce_min_sync(group, my_min);
+            if (my_seg >= 0 && (threadIdx.x & 31) == __ffs(group) - 1)
+                atomicMin(&a.segs[my_seg].min_key, gmin);
         }
         if (tile == ntiles - 1 && threadIdx.x == 0) a.ctl->total_sent = (uint32_t)(gbase + tile_total);
         __syncthreads();
@@ -1021,14 +1185,16 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     a.skeys = reinterpret_cast<uint32_t*>(w + L.skeys);
     a.histA = reinterpret_cast<uint32_t*>(w + L.histA);
     a.histB = reinterpret_cast<uint32_t*>(w + L.histB);
-    a.st_fused = reinterpret_cast<uint64_t*>(w + L.st_fused);
+    a.st_collect = reinterpret_cast<uint64_t*>(w + L.st_collect);
     a.st_compact = reinterpret_cast<uint64_t*>(w + L.st_compact);
     a.st_emit = reinterpret_cast<uint64_t*>(w + L.st_emit);
     a.cidx = reinterpret_cast<uint32_t*>(w + L.cidx);
-    a.cval = reinterpret_cast<float*>(w + L.cval);
-    a.cu = reinterpret_cast<float*>(w + L.cu);
+    a.sidx = reinterpret_cast<uint32_t*>(w + L.sidx);
+    a.tcount = reinterpret_cast<uint32_t*>(w + L.tcount);
     a.max_samples = L.max_samples;
     a.fused_tiles = L.fused_tiles;
+    a.ptiles = L.ptiles;
+    a.cgroups = L.cgroups;
     a.emit_tiles = L.emit_tiles;
     a.max_clip_tiles = L.max_clip_tiles;
     a.spin_limit = kDefaultSpinLimit;
@@ -1061,12 +1227,25 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     L1(k_find<0>, (unsigned)nseg, kThreads, a, 2);
     const cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
     if (pb && pe) cudaEventRecord(pb, s);
-    if (hp.mode == DGC_SELECT_SAMPLED) L1(k_stream<1>, (unsigned)L.fused_tiles, kThreads, a);
-    else L1(k_stream<0>, (unsigned)L.fused_tiles, kThreads, a);
+    if (n > 0) {
+        static bool attr_set[128] = {false};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev >= 0 && dev < 128 && !attr_set[dev]) {
+            cudaFuncSetAttribute(k_stream_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kPSmemBytes);
+            attr_set[dev] = true;
+        }
+        const unsigned pgrid =
+            (unsigned)std::min<uint64_t>((uint64_t)sms * kPBlocksPerSM, L.ptiles);
+        k_stream_tma<<<pgrid, kThreads, kPSmemBytes, s>>>(a);
+        ++launches;
+    }
     if (pb && pe) cudaEventRecord(pe, s);
+    L1(k_collect, (unsigned)L.cgroups, kThreads, a);
     L1(k_candoff, 1, 1024, a, 0);
     if (hp.mode == DGC_SELECT_EXACT) {
-        L1(k_stream<2>, (unsigned)L.fused_tiles, kThreads, a);
+        L1(k_recompact, (unsigned)L.fused_tiles, kThreads, a);
         L1(k_candoff, 1, 1024, a, 1);
     }
     for (int level = 0; level < 6; ++level) {
@@ -1075,8 +1254,7 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     }
     const unsigned emit_grid = (unsigned)std::max<uint64_t>(
         1, std::min<uint64_t>((uint64_t)sms * 4, L.emit_tiles));
-    if (hp.mode == DGC_SELECT_SAMPLED) L1(k_emit<1>, emit_grid, kThreads, a);
-    else L1(k_emit<0>, emit_grid, kThreads, a);
+    L1(k_emit, emit_grid, kThreads, a);
     dgc_internal_count_launches(launches);
     if (cudaPeekAtLastError() != cudaSuccess) {
         cudaGetLastError();

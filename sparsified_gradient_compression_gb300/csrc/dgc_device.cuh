@@ -152,6 +152,114 @@ __device__ __forceinline__ uint64_t lookback_exclusive(uint64_t* st, uint32_t ti
     return excl;
 }
 
+// Decoupled look-back walked by a whole block (kThreads predecessors per round trip), for
+// kernels whose other warps would otherwise idle during the walk. Same status words, limits
+// and timeout behaviour as lookback_exclusive. Every thread of the block must call it; `sm`
+// is shared scratch of at least 2 uint32 + 33 uint64.
+// With publish_agg false the caller has already published the tile's aggregate (or, for tile
+// 0, its inclusive prefix).
+template <int kThreads>
+__device__ __forceinline__ uint64_t block_lookback(uint64_t* st, uint32_t tile, uint64_t agg,
+                                                   uint32_t spin_limit, int32_t* status,
+                                                   int32_t* abort_flag, uint32_t* sm_u32,
+                                                   uint64_t* sm_u64, bool publish_agg = true) {
+    const int tid = threadIdx.x;
+    if (tid == 0 && publish_agg)
+        st_relaxed(&st[tile], (tile == 0 ? kFlagInc : kFlagAgg) | (agg & kValMask));
+    if (tile == 0) return 0;
+    uint64_t excl = 0;
+    int64_t pred = (int64_t)tile - 1;
+    while (true) {
+        const int64_t i = pred - tid;
+        uint64_t w = (i >= 0) ? ld_relaxed(&st[i]) : kFlagInc;  // before tile 0: prefix 0
+        uint32_t spins = 0;
+        uint32_t nearest;  // 0xFFFFFFFF: no inclusive prefix among these predecessors
+        while (true) {
+            if (tid == 0) sm_u32[0] = 0xFFFFFFFFu;
+            __syncthreads();
+            if ((w >> 62) == 2) atomicMin(&sm_u32[0], (uint32_t)tid);
+            __syncthreads();
+            nearest = sm_u32[0];  // nearest predecessor with an inclusive prefix
+            const bool need = ((w >> 62) == 0) && (uint32_t)tid < nearest;
+            if (!__syncthreads_or(need)) break;
+            if (++spins > spin_limit) {
+                if (tid == 0) {
+                    report(status, DGC_ETIMEOUT);
+                    if (abort_flag) atomicExch(abort_flag, 1);
+                }
+                if ((w >> 62) == 0) w = kFlagInc;
+                continue;
+            }
+            if (need) {
+                __nanosleep(64);
+                w = ld_relaxed(&st[i]);
+            }
+        }
+        uint64_t val = ((uint32_t)tid <= nearest) ? (w & kValMask) : 0;
+        uint64_t sum;
+        block_excl_scan<kThreads>(val, sm_u64, &sum);
+        excl += sum;
+        if (nearest != 0xFFFFFFFFu) break;
+        pred -= kThreads;
+    }
+    if (tid == 0) st_relaxed(&st[tile], kFlagInc | ((excl + agg) & kValMask));
+    return excl;
+}
+
+// ------------------------------------------------- bulk copies (TMA) and mbarriers, sm_90+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+// Non-blocking probe of a phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Order this thread's earlier generic-proxy accesses to shared memory before later
+// async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to this
+// block's shared memory; completion is counted on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // Largest s in [0, n) with a[s] <= x, for a non-decreasing a with a[0] <= x (n >= 1).
 template <typename T>
 __device__ __forceinline__ int upper_bound_minus1(const T* a, int n, T x) {

@@ -331,6 +331,36 @@ def test_decode_many_learners_and_accumulate(seed):
         assert same_bits(host_f32(dense), odense)
 
 
+@pytest.mark.parametrize("acc", [False, True])
+def test_decode_single_message_both_modes(acc):
+    # one message: the decoder clears dense (unless accumulating) and adds each value once
+    rng = np.random.default_rng(77)
+    n = 3_000_001
+    idx = np.sort(rng.choice(n, size=5000, replace=False)).astype(np.uint32)
+    idx[-1] = n - 1
+    val = rng.standard_normal(5000).astype(np.float32)
+    val[::7] = np.float32(-0.0)
+    msg = oracle.encode(idx, val, n)
+    base = rng.standard_normal(n).astype(np.float32)
+    rc, dense = decode([msg], n, dense=dev_f32(base), accumulate=acc)
+    orc_rc, odense = oracle.decode_accumulate([msg], n, dense=base, accumulate=acc)
+    assert rc == 0 and orc_rc == 0
+    assert same_bits(host_f32(dense), odense)
+
+
+def test_decode_single_malformed_message_leaves_dense():
+    import struct
+
+    n = 1000
+    good = oracle.encode(np.array([5, 999], np.uint32), np.array([1.0, 2.0], np.float32), n)
+    for bad in (good[:32 + 8] + struct.pack("<H", 999) + good[32 + 10:], b"XGC1" + good[4:]):
+        for acc in (False, True):
+            rc, dense = decode([bad], n, dense=dev_f32(np.full(n, 7.0, np.float32)),
+                               accumulate=acc)
+            assert rc == dgc.ECORRUPT
+            assert np.all(host_f32(dense) == 7.0)
+
+
 def test_decode_zero_learners():
     rc, dense = decode([], 1000)
     assert rc == 0 and not host_f32(dense).any()

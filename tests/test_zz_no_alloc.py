@@ -62,7 +62,7 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(mode):
 
 
 def test_noalloc_rejects_problems_larger_than_its_scratch():
-    n = 4_000_000  # needs ~48 MiB of scratch, more than the 16 MiB the library holds
+    n = 4_000_000  # needs ~32 MiB of scratch, more than the 16 MiB the library holds
     p = dgc.make_params()
     g = torch.zeros(n, device="cuda")
     u, v = _state(n)
