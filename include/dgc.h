@@ -23,7 +23,11 @@
  *     sequence of calls and read it with dgc_read_status.
  *   - Scratch memory is the caller's `ws` buffer of at least the bytes the matching
  *     *_workspace query returns (256-byte aligned). A call may overwrite all of it; calls that
- *     share one workspace must be ordered (same stream, or synchronized).
+ *     share one workspace must be ordered (same stream, or synchronized). dgc_compress also
+ *     keeps its sample positions there from one call to the next (they depend only on the seed
+ *     and the segment layout); every call checks them against a tag and a checksum and
+ *     rebuilds them when either differs, so using the workspace for anything else in between
+ *     is safe and only costs that rebuild.
  *   - Indices are uint32: n must be below 2^32.
  */
 #ifndef DGC_H

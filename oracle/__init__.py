@@ -21,7 +21,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-EXACT, SAMPLED = 0, 1
+EXACT, SAMPLED, ADACOMP = 0, 1, 2
 MASK_MOMENTUM = 1
 OK, EINVAL, ECAPACITY, ECORRUPT, ENOMEM = 0, -1, -2, -5, -7
 
@@ -36,6 +36,8 @@ class Params(ctypes.Structure):
         ("sample_ratio", ctypes.c_double),
         ("reselect_factor", ctypes.c_double),
         ("seed", ctypes.c_uint64),
+        ("bin_size", ctypes.c_uint32),
+        ("pad", ctypes.c_uint32),
     ]
 
 
@@ -91,6 +93,8 @@ def lib():
             ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
         L.orc_topk.restype = ctypes.c_int
         L.orc_topk.argtypes = [vp, vp, i64, i64, vp]
+        L.orc_bin_select.restype = None
+        L.orc_bin_select.argtypes = [vp, i64, u32, vp]
         L.orc_compress.restype = ctypes.c_int
         L.orc_compress.argtypes = [vp, vp, vp, i64, vp, i32, ctypes.POINTER(Params),
                                    vp, vp, i64, ctypes.POINTER(i64), vp]
@@ -109,10 +113,10 @@ def _ptr(a: np.ndarray):
 
 
 def make_params(mode=EXACT, sparsity=0.999, momentum=0.9, clip_norm=0.0, mask_momentum=True,
-                sample_ratio=0.01, reselect_factor=1.3, seed=0) -> Params:
+                sample_ratio=0.01, reselect_factor=1.3, seed=0, bin_size=1000) -> Params:
     return Params(mode, MASK_MOMENTUM if mask_momentum else 0, float(sparsity),
                   float(momentum), float(clip_norm), float(sample_ratio),
-                  float(reselect_factor), int(seed) & (2**64 - 1))
+                  float(reselect_factor), int(seed) & (2**64 - 1), int(bin_size), 0)
 
 
 def ppb(fraction: float) -> int:
@@ -158,6 +162,13 @@ def topk(v: np.ndarray, cand: np.ndarray, k: int) -> np.ndarray:
     if rc != OK:
         raise RuntimeError(f"orc_topk failed: {rc}")
     return sel
+
+
+def bin_select(v: np.ndarray, bin_size: int) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    sel = np.zeros(max(v.size, 1), dtype=np.uint8)
+    lib().orc_bin_select(_ptr(v), v.size, int(bin_size), _ptr(sel))
+    return sel[: v.size]
 
 
 def max_out(n: int) -> int:

@@ -154,6 +154,24 @@ int orc_topk(const float* v, const uint32_t* cand, int64_t ncand, int64_t k, uin
     return ORC_OK;
 }
 
+/* AdaComp selection, [ADA] abstract (residues are selected locally, so the compression rate
+ * follows local activity) and citation snippet (each layer's residual is cut into fixed-size
+ * bins; a bin's largest |residual| is its threshold). Reading: bins are runs of bin_size
+ * consecutive entries from the start of the segment (the last one may be shorter); the entries
+ * whose |v| reaches the bin's largest |v| are selected, ties included; a bin whose largest |v|
+ * is 0 selects nothing. */
+void orc_bin_select(const float* v, int64_t n, uint32_t bin_size, uint8_t* selected) {
+    for (int64_t b = 0; b < n; b += bin_size) {
+        const int64_t e = (b + (int64_t)bin_size < n) ? b + (int64_t)bin_size : n;
+        uint32_t mx = 0;
+        for (int64_t i = b; i < e; ++i)
+            if (orc_key(v[i]) > mx) mx = orc_key(v[i]);
+        if (mx == 0) continue;
+        for (int64_t i = b; i < e; ++i)
+            if (orc_key(v[i]) == mx) selected[i] = 1;
+    }
+}
+
 static int orc_u32_desc(const void* a, const void* b) {
     uint32_t x = *(const uint32_t*)a, y = *(const uint32_t*)b;
     return x > y ? -1 : (x < y ? 1 : 0);
@@ -165,6 +183,7 @@ static int orc_u32_desc(const void* a, const void* b) {
  *   3. u <- m*u + g; v <- v + u, [DGC] Proposed method, bullets 3 and 1.
  *   4. selection S of the largest |v|:
  *      exact   -- the k largest under (|v| desc, index asc);
+ *      AdaComp -- per fixed-size bin, the entries at the bin's largest |v| (orc_bin_select);
  *      sampled -- [DGC] RQ4: t = the k_s-th largest |v| among m_s = ceil(n_s * ratio) sampled
  *                 entries, k_s = ceil(m_s * (1 - sparsity)); C = {i : |v_i| >= t}; reading of
  *                 "hierarchical": when |C| > factor * k, S = the exact top-k of C, else S = C.
@@ -176,7 +195,8 @@ int orc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* s
                  int64_t out_cap, int64_t* out_count, orc_seg_stats* stats) {
     if (!p || !seg_off || nseg < 1 || n < 0 || n > 0xFFFFFFFFll) return ORC_EINVAL;
     if (!(p->sparsity >= 0.0 && p->sparsity <= 1.0)) return ORC_EINVAL;
-    if (p->mode != ORC_EXACT && p->mode != ORC_SAMPLED) return ORC_EINVAL;
+    if (p->mode != ORC_EXACT && p->mode != ORC_SAMPLED && p->mode != ORC_ADACOMP) return ORC_EINVAL;
+    if (p->mode == ORC_ADACOMP && p->bin_size == 0) return ORC_EINVAL;
     if (seg_off[0] != 0 || seg_off[nseg] != n) return ORC_EINVAL;
     for (int32_t s = 0; s < nseg; ++s)
         if (seg_off[s + 1] < seg_off[s]) return ORC_EINVAL;
@@ -195,7 +215,9 @@ int orc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* s
         orc_seg_stats st;
         memset(&st, 0, sizeof st);
         st.thresh_key = 0xFFFFFFFFu;
-        const uint64_t k = orc_count((uint64_t)ns, d_ppb);
+        const uint64_t k = (p->mode == ORC_ADACOMP)
+                               ? ((uint64_t)ns + p->bin_size - 1) / p->bin_size
+                               : orc_count((uint64_t)ns, d_ppb);
         st.k = k;
 
         int clipped = 0;
@@ -214,7 +236,9 @@ int orc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* s
         }
         const float* vs = v + a; /* segment-local view: indices below are segment-relative */
 
-        if (k > 0 && p->mode == ORC_EXACT) {
+        if (p->mode == ORC_ADACOMP) {
+            orc_bin_select(vs, ns, p->bin_size, sel);
+        } else if (k > 0 && p->mode == ORC_EXACT) {
             for (int64_t i = 0; i < ns; ++i) cand[i] = (uint32_t)i;
             if (orc_topk(vs, cand, ns, (int64_t)k, sel) != ORC_OK) goto nomem;
         } else if (k > 0) {
@@ -257,7 +281,7 @@ int orc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* s
             v[a + i] = 0.0f;
             if (mask_momentum) u[a + i] = 0.0f;
         }
-        if (p->mode == ORC_EXACT) st.candidates = st.sent;
+        if (p->mode != ORC_SAMPLED) st.candidates = st.sent;
         if (stats) stats[s] = st;
         free(sel);
         free(cand);

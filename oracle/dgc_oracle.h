@@ -21,11 +21,11 @@ extern "C" {
 #endif
 
 enum { ORC_OK = 0, ORC_EINVAL = -1, ORC_ECAPACITY = -2, ORC_ECORRUPT = -5, ORC_ENOMEM = -7 };
-enum { ORC_EXACT = 0, ORC_SAMPLED = 1 };
+enum { ORC_EXACT = 0, ORC_SAMPLED = 1, ORC_ADACOMP = 2 };
 enum { ORC_MASK_MOMENTUM = 1u };
 
 typedef struct {
-    uint32_t mode;          /* ORC_EXACT or ORC_SAMPLED */
+    uint32_t mode;          /* ORC_EXACT, ORC_SAMPLED or ORC_ADACOMP */
     uint32_t flags;         /* ORC_MASK_MOMENTUM: zero u where a value was sent */
     double sparsity;        /* fraction NOT sent, in [0,1] */
     float momentum;         /* m in u <- m*u + g */
@@ -33,11 +33,13 @@ typedef struct {
     double sample_ratio;    /* sampled mode: fraction of a segment sampled */
     double reselect_factor; /* sampled mode: re-select exactly when |C| > factor * k */
     uint64_t seed;          /* sampled mode: seed of the sample positions */
+    uint32_t bin_size;      /* AdaComp mode: entries per bin (>= 1) */
+    uint32_t pad;
 } orc_params;
 
 typedef struct {
-    uint64_t k;          /* target count for the segment */
-    uint64_t candidates; /* sampled: |C|; exact: |S| */
+    uint64_t k;          /* target count for the segment (AdaComp: number of bins) */
+    uint64_t candidates; /* sampled: |C|; exact and AdaComp: |S| */
     uint64_t sent;       /* |S| */
     uint32_t thresh_key; /* smallest |v| key among sent entries; 0xFFFFFFFF if none */
     uint32_t sample_key; /* sampled: the sampled threshold t; exact: 0 */
@@ -55,6 +57,7 @@ float orc_clip_scale(const float* g, int64_t n, float clip_norm, int* clipped);
 void orc_accumulate_one(float g, float u, float v, float momentum, float scale, int clipped,
                         float* u_out, float* v_out);
 int orc_topk(const float* v, const uint32_t* cand, int64_t ncand, int64_t k, uint8_t* selected);
+void orc_bin_select(const float* v, int64_t n, uint32_t bin_size, uint8_t* selected);
 
 int orc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* seg_off,
                  int32_t nseg, const orc_params* p, uint32_t* out_idx, float* out_val,

@@ -89,7 +89,7 @@ struct SegInfo {
     uint32_t resel;     // sampled mode: re-selection ran
     uint32_t min_key;
     float scale;
-    uint32_t pad;
+    uint32_t bbase;     // first position bucket of the segment
 };
 
 struct Ctl {
@@ -99,14 +99,27 @@ struct Ctl {
     uint32_t ticket_fused, ticket_compact, ticket_emit, ticket_collect;
     uint32_t total_samples, total_clip_tiles, total_cand, total_sent;
     uint32_t emit_done;
+    uint32_t rebuild;       // the cached sample positions must be rebuilt this call
+    uint64_t tag;           // what the sample positions depend on, for this call
+    uint64_t csum;          // checksum of the cached positions as found
+    uint64_t newsum;        // checksum of the rebuilt positions
+    uint32_t sum_done;
     uint32_t pad;
 };
 
+// Header of the sample-position cache kept in the workspace between calls.
+struct SampleCache {
+    uint64_t magic, tag, checksum, pad;
+};
+constexpr uint64_t kCacheMagic = 0x53504F5343414348ull;
+constexpr int kBucketShift = 10;  // cache order: 1024-entry buckets, segment by segment
+
 // Workspace layout (host computes it; every piece 256-byte aligned).
 struct Layout {
-    size_t ctl, segs, seg_start, samp_off, clip_off, cand_off, clip_part, skeys, histA, histB;
+    size_t ctl, scache, segs, seg_start, samp_off, clip_off, cand_off, clip_part, skeys, spos,
+        bcount, histA, histB;
     size_t st_collect, st_compact, st_emit, cidx, sidx, tcount, total;
-    uint64_t max_samples, max_clip_tiles, fused_tiles, emit_tiles, ptiles, cgroups;
+    uint64_t max_samples, max_clip_tiles, fused_tiles, emit_tiles, ptiles, cgroups, nbuckets;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -152,10 +165,12 @@ Layout make_layout(int64_t n, int32_t nseg, const HostParams& hp) {
     L.fused_tiles = (un + kTile - 1) / kTile;
     L.ptiles = (un + kPTile - 1) / kPTile;
     L.cgroups = (L.ptiles + kThreads - 1) / kThreads;
+    L.nbuckets = (un >> kBucketShift) + 2 * (uint64_t)nseg + 1;  // >= sum of per-segment buckets
     L.emit_tiles = (un + kEmitTile - 1) / kEmitTile;
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
     L.ctl = take(sizeof(Ctl));
+    L.scache = take(sizeof(SampleCache));
     L.segs = take(sizeof(SegInfo) * (size_t)nseg);
     L.seg_start = take(sizeof(uint32_t) * (size_t)(nseg + 1));
     L.samp_off = take(sizeof(uint32_t) * (size_t)(nseg + 1));
@@ -163,6 +178,8 @@ Layout make_layout(int64_t n, int32_t nseg, const HostParams& hp) {
     L.cand_off = take(sizeof(uint32_t) * (size_t)(nseg + 1));
     L.clip_part = take(sizeof(double) * (size_t)L.max_clip_tiles);
     L.skeys = take(sizeof(uint32_t) * (size_t)L.max_samples);
+    L.spos = take(sizeof(uint32_t) * (size_t)L.max_samples);
+    L.bcount = take(sizeof(uint32_t) * (size_t)L.nbuckets);
     L.histA = take(sizeof(uint32_t) * (size_t)nseg * kHistBins);
     L.histB = take(sizeof(uint32_t) * (size_t)nseg * kHistBins);
     L.st_collect = take(sizeof(uint64_t) * (size_t)(L.cgroups + 1));
@@ -204,6 +221,7 @@ struct Args {
     dgc_seg_stats* stats;
     int32_t* status;
     Ctl* ctl;
+    SampleCache* scache;
     SegInfo* segs;
     uint32_t* seg_start;
     uint32_t* samp_off;
@@ -211,6 +229,8 @@ struct Args {
     uint32_t* cand_off;
     double* clip_part;
     uint32_t* skeys;
+    uint32_t* spos;    // sample positions in bucket order (cached between calls)
+    uint32_t* bcount;  // per-bucket counts, then cursors, while the cache is rebuilt
     uint32_t* histA;
     uint32_t* histB;
     uint64_t* st_collect;
@@ -219,7 +239,7 @@ struct Args {
     uint32_t* cidx;   // candidates, ascending index
     uint32_t* sidx;   // per-tile candidate slots of the streaming pass
     uint32_t* tcount; // per-tile candidate counts
-    uint64_t max_samples, fused_tiles, emit_tiles, max_clip_tiles, ptiles, cgroups;
+    uint64_t max_samples, fused_tiles, emit_tiles, max_clip_tiles, ptiles, cgroups, nbuckets;
     uint32_t spin_limit;
 };
 
@@ -228,12 +248,13 @@ struct Args {
 // look-back words.
 __global__ void __launch_bounds__(1024) k_plan(Args a) {
     __shared__ uint32_t s_scan[33];
-    __shared__ uint32_t s_carry_samp, s_carry_clip;
+    __shared__ uint32_t s_carry_samp, s_carry_clip, s_carry_bkt;
     __shared__ int s_bad;
     if (blockIdx.x == 0) {
         if (threadIdx.x == 0) {
             s_carry_samp = 0;
             s_carry_clip = 0;
+            s_carry_bkt = 0;
             s_bad = (a.seg_off[0] != 0 || a.seg_off[a.nseg] != (int64_t)a.n) ? 1 : 0;
             Ctl c{};
             *a.ctl = c;
@@ -241,9 +262,10 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
         }
         __syncthreads();
         uint32_t active = 0;
+        uint64_t tag = 0;  // what the sample positions depend on: seeds, ranges, counts
         for (int base = 0; base < a.nseg; base += 1024) {
             const int s = base + threadIdx.x;
-            uint32_t ms = 0, clip_tiles = 0;
+            uint32_t ms = 0, clip_tiles = 0, buckets = 0;
             if (s < a.nseg) {
                 const int64_t lo = a.seg_off[s], hi = a.seg_off[s + 1];
                 if (hi < lo || lo < 0 || hi > (int64_t)a.n) atomicExch(&s_bad, 1);
@@ -279,9 +301,11 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
                     }
                 }
                 ms = d.ms;
+                if (ms) buckets = (ns >> kBucketShift) + 1;
                 if (a.hp.clip_on) clip_tiles = (ns + kClipTile - 1) / kClipTile;
                 a.segs[s] = d;
                 a.seg_start[s] = st;
+                tag ^= mix64(d.seed ^ mix64(((uint64_t)st << 32) | en) ^ mix64(ms + kGolden));
             }
             uint32_t tot;
             const uint32_t ex = block_excl_scan<1024>(ms, s_scan, &tot);
@@ -292,8 +316,15 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
             if (s < a.nseg) a.clip_off[s] = s_carry_clip + exc;
             __syncthreads();
             if (threadIdx.x == 0) s_carry_clip += tot;
+            const uint32_t exb = block_excl_scan<1024>(buckets, s_scan, &tot);
+            if (s < a.nseg) a.segs[s].bbase = s_carry_bkt + exb;
+            __syncthreads();
+            if (threadIdx.x == 0) s_carry_bkt += tot;
             __syncthreads();
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tag ^= __shfl_xor_sync(kFull, tag, o);
+        if ((threadIdx.x & 31) == 0) atomicXor((unsigned long long*)&a.ctl->tag, tag);
         active = warp_sum(active);
         if ((threadIdx.x & 31) == 0 && active) atomicAdd(&a.ctl->active, active);
         __syncthreads();
@@ -303,6 +334,8 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
             a.seg_start[a.nseg] = a.n;
             a.ctl->total_samples = s_carry_samp;
             a.ctl->total_clip_tiles = s_carry_clip;
+            atomicXor((unsigned long long*)&a.ctl->tag,
+                      mix64((uint64_t)a.n ^ mix64((uint64_t)a.nseg + kCacheMagic)));
             if (s_bad) {
                 a.ctl->abort = 1;
                 report(a.status, DGC_EINVAL);
@@ -320,6 +353,7 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
     for (size_t i = tid; i <= a.fused_tiles; i += stride) a.st_compact[i] = 0;
     for (size_t i = tid; i <= a.cgroups; i += stride) a.st_collect[i] = 0;
     for (size_t i = tid; i <= a.emit_tiles; i += stride) a.st_emit[i] = 0;
+    for (size_t i = tid; i < a.nbuckets; i += stride) a.bcount[i] = 0;
 }
 
 // ----------------------------------------------------------------------------- clipping
@@ -399,6 +433,123 @@ struct BlockHist {
     }
 };
 
+// ------------------------------------------------------------- sample-position cache
+// The sample positions depend only on the seed and the segment layout, and gathering g, u, v in
+// position order is much kinder to HBM than in draw order. So the workspace keeps the positions
+// sorted by 1024-entry bucket (segment by segment, so each segment's samples stay together), with
+// a tag of what they depend on and a checksum of the array. Every call re-checks both (one read
+// of the array) and rebuilds the cache when either differs -- a workspace that was reused for
+// something else, or a new seed or layout, costs one counting sort. The order of positions inside
+// a bucket depends on atomics, but the threshold only depends on the multiset of sampled keys.
+__device__ __forceinline__ uint32_t sample_position(const SegInfo& d, uint64_t j) {
+    const uint64_t x = mix64(d.seed + kGolden * (j + 1));
+    return d.start + (uint32_t)__umul64hi(x, (uint64_t)(d.end - d.start));
+}
+
+__device__ __forceinline__ uint64_t cache_term(uint32_t pos, uint64_t i) {
+    return mix64((uint64_t)pos ^ (i * kGolden));
+}
+
+__device__ __forceinline__ uint64_t block_sum64(uint64_t x, uint64_t* sm) {
+    uint64_t total;
+    block_excl_scan<kThreads>(x, sm, &total);
+    return total;
+}
+
+// checksum of the cached positions, when the header matches this call's tag
+__global__ void __launch_bounds__(kThreads) k_cache_check(Args a) {
+    __shared__ uint64_t s_scan[33];
+    const SampleCache c = *a.scache;
+    if (a.ctl->abort || c.magic != kCacheMagic || c.tag != a.ctl->tag) return;
+    const uint32_t total = a.ctl->total_samples;
+    uint64_t part = 0;
+    for (uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < total;
+         i += (uint64_t)gridDim.x * kThreads)
+        part += cache_term(a.spos[i], i);
+    const uint64_t sum = block_sum64(part, s_scan);
+    if (threadIdx.x == 0 && sum) atomicAdd((unsigned long long*)&a.ctl->csum, sum);
+}
+
+__device__ __forceinline__ bool cache_valid(const Args& a) {
+    const SampleCache c = *a.scache;
+    return c.magic == kCacheMagic && c.tag == a.ctl->tag && c.checksum == a.ctl->csum;
+}
+
+// rebuild, step 1: bucket counts (every block takes the same decision from the same inputs)
+__global__ void __launch_bounds__(kThreads) k_cache_count(Args a) {
+    const bool rebuild = !a.ctl->abort && !cache_valid(a);
+    if (blockIdx.x == 0 && threadIdx.x == 0) a.ctl->rebuild = rebuild ? 1u : 0u;
+    if (!rebuild) return;
+    const uint32_t total = a.ctl->total_samples;
+    for (uint64_t jg = (uint64_t)blockIdx.x * kThreads + threadIdx.x; jg < total;
+         jg += (uint64_t)gridDim.x * kThreads) {
+        const int s = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)jg);
+        const SegInfo& d = a.segs[s];
+        const uint32_t pos = sample_position(d, jg - a.samp_off[s]);
+        atomicAdd(&a.bcount[d.bbase + ((pos - d.start) >> kBucketShift)], 1u);
+    }
+}
+
+// rebuild, step 2: counts -> first slot of each bucket (one block)
+__global__ void __launch_bounds__(1024) k_cache_scan(Args a) {
+    __shared__ uint32_t s_scan[33];
+    if (!a.ctl->rebuild) return;
+    const uint64_t nb = a.nbuckets;
+    const uint64_t per = (nb + 1023) / 1024;
+    const uint64_t lo = umin64(nb, threadIdx.x * per), hi = umin64(nb, lo + per);
+    uint32_t mine = 0;
+    for (uint64_t b = lo; b < hi; ++b) mine += a.bcount[b];
+    uint32_t total;
+    uint32_t run = block_excl_scan<1024>(mine, s_scan, &total);
+    for (uint64_t b = lo; b < hi; ++b) {
+        const uint32_t c = a.bcount[b];
+        a.bcount[b] = run;
+        run += c;
+    }
+}
+
+// rebuild, step 3: every position into its bucket
+__global__ void __launch_bounds__(kThreads) k_cache_scatter(Args a) {
+    if (!a.ctl->rebuild) return;
+    const uint32_t total = a.ctl->total_samples;
+    for (uint64_t jg = (uint64_t)blockIdx.x * kThreads + threadIdx.x; jg < total;
+         jg += (uint64_t)gridDim.x * kThreads) {
+        const int s = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)jg);
+        const SegInfo& d = a.segs[s];
+        const uint32_t pos = sample_position(d, jg - a.samp_off[s]);
+        const uint32_t slot = atomicAdd(&a.bcount[d.bbase + ((pos - d.start) >> kBucketShift)], 1u);
+        a.spos[slot] = pos;
+    }
+}
+
+// rebuild, step 4: checksum of the new array; the last block writes the header
+__global__ void __launch_bounds__(kThreads) k_cache_commit(Args a) {
+    __shared__ uint64_t s_scan[33];
+    __shared__ int s_last;
+    if (!a.ctl->rebuild) return;
+    const uint32_t total = a.ctl->total_samples;
+    uint64_t part = 0;
+    for (uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < total;
+         i += (uint64_t)gridDim.x * kThreads)
+        part += cache_term(a.spos[i], i);
+    const uint64_t sum = block_sum64(part, s_scan);
+    if (threadIdx.x == 0) {
+        if (sum) atomicAdd((unsigned long long*)&a.ctl->newsum, sum);
+        __threadfence();
+        s_last = (atomicAdd(&a.ctl->sum_done, 1u) == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (s_last && threadIdx.x == 0) {
+        __threadfence();
+        SampleCache c;
+        c.magic = kCacheMagic;
+        c.tag = a.ctl->tag;
+        c.checksum = atomicAdd((unsigned long long*)&a.ctl->newsum, 0ull);
+        c.pad = 0;
+        *a.scache = c;
+    }
+}
+
 // --------------------------------------------------------------------------- sampling
 // Sample draw j of segment s sits at start + floor(mix(seed_s + (j+1)g) * n_s / 2^64). The
 // post-accumulate value there is recomputed from the pre-step g, u, v with the same
@@ -428,10 +579,7 @@ __global__ void __launch_bounds__(kThreads) k_sample(Args a) {
         sg[r] = -1;
         if (jg < chunk_end) {
             const int s = uniform ? s_seg0 : upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)jg);
-            const SegInfo& d = a.segs[s];
-            const uint64_t j = jg - a.samp_off[s];
-            const uint64_t x = mix64(d.seed + kGolden * (j + 1));
-            const uint32_t pos = d.start + (uint32_t)__umul64hi(x, (uint64_t)(d.end - d.start));
+            const uint32_t pos = a.spos[jg];  // the sample positions in bucket order
             gv[r] = __ldg(a.g + pos);
             uv[r] = a.u[pos];
             vv[r] = a.v[pos];
@@ -1176,6 +1324,7 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     a.stats = stats;
     a.status = status;
     a.ctl = reinterpret_cast<Ctl*>(w + L.ctl);
+    a.scache = reinterpret_cast<SampleCache*>(w + L.scache);
     a.segs = reinterpret_cast<SegInfo*>(w + L.segs);
     a.seg_start = reinterpret_cast<uint32_t*>(w + L.seg_start);
     a.samp_off = reinterpret_cast<uint32_t*>(w + L.samp_off);
@@ -1183,6 +1332,8 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     a.cand_off = reinterpret_cast<uint32_t*>(w + L.cand_off);
     a.clip_part = reinterpret_cast<double*>(w + L.clip_part);
     a.skeys = reinterpret_cast<uint32_t*>(w + L.skeys);
+    a.spos = reinterpret_cast<uint32_t*>(w + L.spos);
+    a.bcount = reinterpret_cast<uint32_t*>(w + L.bcount);
     a.histA = reinterpret_cast<uint32_t*>(w + L.histA);
     a.histB = reinterpret_cast<uint32_t*>(w + L.histB);
     a.st_collect = reinterpret_cast<uint64_t*>(w + L.st_collect);
@@ -1195,6 +1346,7 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     a.fused_tiles = L.fused_tiles;
     a.ptiles = L.ptiles;
     a.cgroups = L.cgroups;
+    a.nbuckets = L.nbuckets;
     a.emit_tiles = L.emit_tiles;
     a.max_clip_tiles = L.max_clip_tiles;
     a.spin_limit = kDefaultSpinLimit;
@@ -1208,7 +1360,8 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
         kernel<<<grid, block, 0, s>>>(args...);
         ++launches;
     };
-    const size_t zero_work = (size_t)nseg * kHistBins + L.fused_tiles + L.emit_tiles + 2;
+    const size_t zero_work =
+        (size_t)nseg * kHistBins + L.fused_tiles + L.emit_tiles + L.nbuckets + 2;
     const unsigned plan_grid = (unsigned)std::min<size_t>((zero_work + 1023) / 1024 + 1,
                                                           (size_t)sms * 2);
     L1(k_plan, plan_grid, 1024, a);
@@ -1216,6 +1369,13 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
         L1(k_clip_tiles, (unsigned)L.max_clip_tiles, kThreads, a);
         L1(k_clip_scale, (unsigned)((nseg + 255) / 256), 256, a);
     }
+    const unsigned cgrid = (unsigned)std::max<uint64_t>(
+        1, std::min<uint64_t>((uint64_t)sms * 4, (L.max_samples + kThreads - 1) / kThreads));
+    L1(k_cache_check, cgrid, kThreads, a);
+    L1(k_cache_count, cgrid, kThreads, a);
+    L1(k_cache_scan, 1, 1024, a);
+    L1(k_cache_scatter, cgrid, kThreads, a);
+    L1(k_cache_commit, cgrid, kThreads, a);
     const uint64_t sgrid = (L.max_samples + kThreads * kSamplePerThread - 1) /
                            (kThreads * kSamplePerThread);
     L1(k_sample, (unsigned)sgrid, kThreads, a);

@@ -452,6 +452,37 @@ def test_checkpoint_resume_is_bitwise():
     assert np.array_equal(first[0], second[0]) and same_bits(first[1], second[1])
 
 
+@pytest.mark.parametrize("damage", ["whole", "past_header", "new_seed"])
+def test_workspace_reuse_is_safe(damage):
+    # The workspace carries the sample positions from one call to the next, validated by a tag
+    # and a checksum. Whatever happens to the workspace between calls, results stay exact.
+    n = 1_000_003
+    off = np.array([0, 400_000, n])
+    kw = dict(mode=dgc.SELECT_SAMPLED, sparsity=0.999, momentum=0.9, sample_ratio=0.05, seed=21)
+    pd, po = params_pair(**kw)
+    comp = Compressor(n, off, pd)
+    u_h = np.zeros(n, np.float32)
+    v_h = np.zeros(n, np.float32)
+    u_d, v_d = dev_f32(u_h), dev_f32(v_h)
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    for t in range(4):
+        if t == 2:
+            if damage == "whole":
+                comp.ws.random_(0, 256, generator=gen)
+            elif damage == "past_header":  # control words and cache header survive
+                comp.ws[4096:].random_(0, 256, generator=gen)
+            else:
+                pd.seed = po.seed = 22
+        g = workloads.misc([t, 3], n, 0.01)
+        comp(dev_f32(g), u_d, v_d)
+        assert comp.status_code() == 0
+        idx, val, st = comp.results()
+        oidx, oval, ost = oracle.compress(g, u_h, v_h, off, po)
+        assert np.array_equal(idx, oidx) and same_bits(val, oval), f"step {t}"
+        assert same_bits(host_f32(v_d), v_h) and same_bits(host_f32(u_d), u_h), f"step {t}"
+        assert [s_["sample_key"] for s_ in st] == [o["sample_key"] for o in ost]
+
+
 def test_runs_are_deterministic():
     n = 2_000_003
     off = np.array([0, 1_000_000, n])

@@ -548,3 +548,64 @@ def test_reselect_not_taken_at_exactly_factor_times_k(orc):
                                                              sample_ratio=1.0, seed=seed))
     assert idx.tolist() == exp_idx
     assert st[0]["candidates"] == 13 and st[0]["reselected"] == 0
+
+
+# ---------------------------------------------------------------------- AdaComp bins
+def brute_bins(v, L):
+    """Per run of L entries: the indices whose |v| equals the run's largest |v|, if above 0."""
+    keys = [X.key(x) for x in v]
+    out = []
+    for b in range(0, len(v), L):
+        mx = max(keys[b:b + L])
+        if mx > 0:
+            out += [i for i in range(b, min(b + L, len(v))) if keys[i] == mx]
+    return out
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_bin_select_matches_bruteforce(orc, seed):
+    rng = np.random.default_rng(4000 + seed)
+    n = int(rng.integers(1, 400))
+    v = _tricky(rng, n, seed % 5)
+    L = int(rng.choice([1, 2, 3, 7, 16, 50, 1000]))
+    sel = orc.bin_select(v, L)
+    assert np.nonzero(sel)[0].tolist() == brute_bins(v, L)
+
+
+def test_bin_select_closed_forms(orc):
+    rng = np.random.default_rng(1)
+    v = rng.standard_normal(1000).astype(np.float32)
+    v[::10] = 0.0
+    # one entry per bin: every nonzero entry is its own bin's largest
+    assert np.nonzero(orc.bin_select(v, 1))[0].tolist() == np.nonzero(v)[0].tolist()
+    # one bin larger than everything: the entries at the largest |v|
+    assert np.nonzero(orc.bin_select(v, 5000))[0].tolist() == [int(np.argmax(np.abs(v)))]
+    assert not orc.bin_select(np.zeros(100, np.float32), 10).any()
+    w = np.array([1, -3, 3, 2, -3, 0, 0, 0, 5, -5], np.float32)
+    assert np.nonzero(orc.bin_select(w, 5))[0].tolist() == [1, 2, 4, 8, 9]
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_adacomp_compress_matches_definition(orc, seed):
+    rng = np.random.default_rng(5000 + seed)
+    n = int(rng.integers(1, 500))
+    off = _random_segments(rng, n)
+    kind = seed % 4
+    g, u, v = (_tricky(rng, n, kind) for _ in range(3))
+    m = np.float32(rng.choice([0.0, 0.9]))
+    L = int(rng.choice([1, 4, 10, 64]))
+    mask = bool(seed % 2)
+    un, vn = _exact_accumulate(g, u, v, m)
+    exp_idx = []
+    for a, b in zip(off[:-1], off[1:]):
+        exp_idx += [int(a) + i for i in brute_bins(vn[a:b], L)]
+    p = orc.make_params(orc.ADACOMP, 0.999, float(m), mask_momentum=mask, bin_size=L)
+    uu, vv = u.copy(), v.copy()
+    idx, val, st = orc.compress(g, uu, vv, off, p)
+    assert idx.tolist() == exp_idx
+    assert [X.bits(x) for x in val] == [X.bits(vn[i]) for i in exp_idx]
+    v_exp = vn.copy()
+    v_exp[exp_idx] = 0.0
+    assert vv.view(np.uint32).tolist() == v_exp.view(np.uint32).tolist()
+    for s_, (a, b) in zip(st, zip(off[:-1], off[1:])):
+        assert s_["k"] == -(-(int(b) - int(a)) // L)
