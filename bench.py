@@ -35,6 +35,9 @@ UNIT = "GB/s"
 WORKLOAD = ("flat bucket of 2^30 fp32 entries (4 GiB), g ~ N(0, 1e-4) with 0.01% fixed "
             "outliers x100; sampled 1% threshold, re-select if |C| > 1.3k; 99.9% sparsity; "
             "compress + encode + decode per step")
+WORKLOAD_ADACOMP = ("flat bucket of 2^30 fp32 entries (4 GiB), g ~ N(0, 1e-4) with 0.01% fixed "
+                    "outliers x100; AdaComp bins of {} entries; compress + encode + decode per "
+                    "step")
 SEED = 20240
 
 
@@ -50,6 +53,9 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-n", type=int, default=1 << 26)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--select", choices=["sampled", "adacomp"], default="sampled",
+                    help="DGC sampled threshold (the headline) or AdaComp bins of --bin-size")
+    ap.add_argument("--bin-size", type=int, default=1000)
     return ap.parse_args(argv)
 
 
@@ -255,8 +261,9 @@ def run_ours(args, world, rank, local):
     dgc.build()
     n = args.n
     sched = list(workloads.WARMUP_SPARSITY[:4])
-    params = [dgc.make_params(mode=dgc.SELECT_SAMPLED, sparsity=s, momentum=0.9,
-                              sample_ratio=0.01, reselect_factor=1.3, seed=SEED + rank)
+    mode = dgc.SELECT_ADACOMP if args.select == "adacomp" else dgc.SELECT_SAMPLED
+    params = [dgc.make_params(mode=mode, sparsity=s, momentum=0.9, sample_ratio=0.01,
+                              reselect_factor=1.3, seed=SEED + rank, bin_size=args.bin_size)
               for s in sched + [0.999]]
     p_main = params[-1]
     pipe = Pipeline(n, params, dev)
@@ -320,18 +327,20 @@ def run_ours(args, world, rank, local):
     e2e = None if args.no_e2e else run_e2e(args, pipe, pool, p_main, K)
     cpu = None
     if not args.no_cpu and rank == 0 and world == 1:
-        cpu = run_cpu_baseline(args.cpu_n, steps=3)
+        cpu = run_cpu_baseline(args.cpu_n, steps=3, select=args.select, bin_size=args.bin_size)
+    workload = WORKLOAD if args.select == "sampled" else WORKLOAD_ADACOMP.format(args.bin_size)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(sec_max * 1e3 / K, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; see workloads/)",
-        "config": {"workload": WORKLOAD, "n": n, "sparsity": 0.999, "k": int(st["k"]),
+        "config": {"workload": workload, "n": n, "sparsity": 0.999, "k": int(st["k"]),
+                   "selection": args.select,
                    "momentum": 0.9, "sample_ratio": 0.01, "reselect_factor": 1.3,
                    "segments": 1, "l2": f"inputs larger than L2 ({4 * n >> 20} MiB per array; "
                    f"{len(pool)} distinct gradients cycled)",
                    "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "k_stream_tma (accumulate + per-tile compaction)",
+        "roofline": {"bound": "hbm", "kernel": "k_stream_tma<%d> (accumulate + per-tile compaction)" % (args.select == "adacomp"),
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None if traffic is None else round(traffic),
@@ -415,7 +424,7 @@ def run_e2e(args, pipe, pool, p, K_dev):
 
 
 # ------------------------------------------------------------------ CPU baseline / reference
-def run_cpu_baseline(n_cpu: int, steps: int):
+def run_cpu_baseline(n_cpu: int, steps: int, select: str = "sampled", bin_size: int = 1000):
     """The oracle, single-threaded on one host core, on a bounded sample of the workload:
     an n_cpu-entry bucket with the same recipe (one untimed step, then `steps` timed steps of
     compress + encode + decode at 99.9%)."""
@@ -424,8 +433,9 @@ def run_cpu_baseline(n_cpu: int, steps: int):
     import oracle
     import workloads
 
-    p = oracle.make_params(oracle.SAMPLED, 0.999, 0.9, sample_ratio=0.01, reselect_factor=1.3,
-                           seed=SEED)
+    mode = oracle.ADACOMP if select == "adacomp" else oracle.SAMPLED
+    p = oracle.make_params(mode, 0.999, 0.9, sample_ratio=0.01, reselect_factor=1.3, seed=SEED,
+                           bin_size=bin_size)
     off = np.array([0, n_cpu], np.int64)
     u = np.zeros(n_cpu, np.float32)
     v = np.zeros(n_cpu, np.float32)
@@ -451,13 +461,15 @@ def run_reference(args, world, rank):
     n_ref = 1 << 26
     while n_ref > (1 << 16) and steps * n_ref * 40e-9 > 120:
         n_ref >>= 1
-    cpu = run_cpu_baseline(n_ref, steps)
+    cpu = run_cpu_baseline(n_ref, steps, select=args.select, bin_size=args.bin_size)
     out = {"impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": UNIT,
            "n_gpus": world, "steps": steps, "warmup": args.warmup,
            "ms_per_step": round(cpu["seconds"] * 1e3 / steps, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
            "data": "synthetic (seeded; see workloads/)",
-           "config": {"workload": WORKLOAD, "n": n_ref, "sample_of_n": args.n},
+           "config": {"workload": WORKLOAD if args.select == "sampled"
+                      else WORKLOAD_ADACOMP.format(args.bin_size), "n": n_ref,
+                      "sample_of_n": args.n, "selection": args.select},
            "cpu_baseline": cpu,
            "e2e": {"value": cpu["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}

@@ -52,14 +52,15 @@ enum {
     DGC_EUNSUPPORTED = -6  /* a size the library does not handle (n >= 2^32) */
 };
 
-enum { DGC_SELECT_EXACT = 0, DGC_SELECT_SAMPLED = 1 };
+enum { DGC_SELECT_EXACT = 0, DGC_SELECT_SAMPLED = 1, DGC_SELECT_ADACOMP = 2 };
 enum { DGC_FLAG_MASK_MOMENTUM = 1u };
 
 /* Compressor settings. [DGC] Proposed method: momentum correction (momentum), local gradient
  * clipping (clip_norm), momentum factor masking (DGC_FLAG_MASK_MOMENTUM); [DGC] Abstract:
- * 99.9% sparsity; [DGC] RQ4: hierarchical thresholding (sample_ratio, reselect_factor). */
+ * 99.9% sparsity; [DGC] RQ4: hierarchical thresholding (sample_ratio, reselect_factor);
+ * [ADA] bin-local selection (bin_size). */
 typedef struct {
-    uint32_t mode;          /* DGC_SELECT_EXACT or DGC_SELECT_SAMPLED */
+    uint32_t mode;          /* DGC_SELECT_EXACT, DGC_SELECT_SAMPLED or DGC_SELECT_ADACOMP */
     uint32_t flags;         /* DGC_FLAG_MASK_MOMENTUM: clear u where a value is sent */
     double sparsity;        /* fraction of each segment NOT sent, in [0, 1] */
     float momentum;         /* m in u <- m*u + g (finite) */
@@ -67,12 +68,14 @@ typedef struct {
     double sample_ratio;    /* sampled mode: fraction of each segment sampled, in (0, 1] */
     double reselect_factor; /* sampled mode: exact re-selection when |C| > factor*k, in [1,16] */
     uint64_t seed;          /* sampled mode: seed of the sample positions */
+    uint32_t bin_size;      /* AdaComp mode: entries per bin, >= 1 (sparsity is not used) */
+    uint32_t reserved;      /* 0 */
 } dgc_params;
 
 /* Per-segment statistics of one dgc_compress call. */
 typedef struct {
-    uint64_t k;          /* ceil(n_s * (1 - sparsity)) */
-    uint64_t candidates; /* sampled: |C| = #{i : |v_i| >= t}; exact: |S| */
+    uint64_t k;          /* ceil(n_s * (1 - sparsity)); AdaComp: the number of bins */
+    uint64_t candidates; /* sampled: |C| = #{i : |v_i| >= t}; exact and AdaComp: |S| */
     uint64_t sent;       /* |S| */
     uint32_t thresh_key; /* smallest |v| key (bits & 0x7FFFFFFF) among sent entries, or
                             0xFFFFFFFF when nothing was sent */
@@ -88,7 +91,7 @@ int dgc_compress_workspace(int64_t n, int32_t nseg, const dgc_params* params, si
 
 /* Upper bound on the number of (index, value) pairs one dgc_compress call can emit; out_cap
  * must be at least this. Exact mode: sum of k; sampled mode: the re-selection rule bounds
- * |S| by reselect_factor * k per segment. */
+ * |S| by reselect_factor * k per segment; AdaComp mode: n (ties can select a whole bin). */
 int dgc_compress_max_out(int64_t n, int32_t nseg, const dgc_params* params, int64_t* max_out);
 
 /* One compressor step over a flat buffer holding nseg segments (tensors), each compressed on
@@ -101,7 +104,10 @@ int dgc_compress_max_out(int64_t n, int32_t nseg, const dgc_params* params, int6
  *   4. S = the k_s largest |v| (ties to the lower index) in exact mode; in sampled mode
  *      t = the k_s'-th largest |v| among m_s = ceil(n_s * sample_ratio) positions drawn with
  *      SplitMix64 (seed), C = {|v| >= t}, and S = exact top-k_s of C when
- *      |C| > reselect_factor * k_s, else S = C.
+ *      |C| > reselect_factor * k_s, else S = C. In AdaComp mode ([ADA] abstract and citation
+ *      snippet) each segment is cut into bins of bin_size entries from its start (the last one
+ *      shorter) and S = the entries whose |v| equals their bin's largest |v| (ties included;
+ *      a bin whose largest |v| is 0 sends nothing).
  *   5. out_idx/out_val receive (i, v_i) for i in S in ascending i (segments in order), then
  *      v_i <- 0 and, with DGC_FLAG_MASK_MOMENTUM, u_i <- 0.
  * Arguments:

@@ -20,11 +20,11 @@ __all__ = [
     "dgc_decode_workspace", "dgc_decode_accumulate",
     "dgc_read_status", "dgc_status_string", "dgc_launch_count", "dgc_selftest_wait_timeout",
     "dgc_profile_stream_pass",
-    "SELECT_EXACT", "SELECT_SAMPLED", "FLAG_MASK_MOMENTUM",
+    "SELECT_EXACT", "SELECT_SAMPLED", "SELECT_ADACOMP", "FLAG_MASK_MOMENTUM",
 ]
 
 OK, EINVAL, ECAPACITY, ECUDA, ETIMEOUT, ECORRUPT, EUNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
-SELECT_EXACT, SELECT_SAMPLED = 0, 1
+SELECT_EXACT, SELECT_SAMPLED, SELECT_ADACOMP = 0, 1, 2
 FLAG_MASK_MOMENTUM = 1
 
 
@@ -38,6 +38,8 @@ class dgc_params(ctypes.Structure):
         ("sample_ratio", ctypes.c_double),
         ("reselect_factor", ctypes.c_double),
         ("seed", ctypes.c_uint64),
+        ("bin_size", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32),
     ]
 
 
@@ -138,10 +140,11 @@ def _stream(stream) -> int | None:
 
 
 def make_params(mode=SELECT_EXACT, sparsity=0.999, momentum=0.9, clip_norm=0.0,
-                mask_momentum=True, sample_ratio=0.01, reselect_factor=1.3, seed=0) -> dgc_params:
+                mask_momentum=True, sample_ratio=0.01, reselect_factor=1.3, seed=0,
+                bin_size=1000) -> dgc_params:
     return dgc_params(int(mode), FLAG_MASK_MOMENTUM if mask_momentum else 0, float(sparsity),
                       float(momentum), float(clip_norm), float(sample_ratio),
-                      float(reselect_factor), int(seed) & (2**64 - 1))
+                      float(reselect_factor), int(seed) & (2**64 - 1), int(bin_size), 0)
 
 
 # --------------------------------------------------------------------------- compressor

@@ -90,6 +90,8 @@ struct SegInfo {
     uint32_t min_key;
     float scale;
     uint32_t bbase;     // first position bucket of the segment
+    uint32_t binbase;   // AdaComp: first bin of the segment
+    uint32_t nsent;     // AdaComp: entries sent
 };
 
 struct Ctl {
@@ -118,14 +120,15 @@ constexpr int kBucketShift = 10;  // cache order: 1024-entry buckets, segment by
 struct Layout {
     size_t ctl, scache, segs, seg_start, samp_off, clip_off, cand_off, clip_part, skeys, spos,
         bcount, histA, histB;
-    size_t st_collect, st_compact, st_emit, cidx, sidx, tcount, total;
-    uint64_t max_samples, max_clip_tiles, fused_tiles, emit_tiles, ptiles, cgroups, nbuckets;
+    size_t st_collect, st_compact, st_emit, cidx, sidx, tcount, binmax, total;
+    uint64_t max_samples, max_clip_tiles, fused_tiles, emit_tiles, ptiles, cgroups, nbuckets,
+        max_bins;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct HostParams {
-    uint32_t mode, mask, clip_on;
+    uint32_t mode, mask, clip_on, bin;
     uint64_t d_ppb, r_ppb, q_ppb;
     float momentum, clip_norm;
     uint64_t seed;
@@ -133,7 +136,11 @@ struct HostParams {
 
 int check_params(const dgc_params* p, HostParams* hp) {
     if (!p) return DGC_EINVAL;
-    if (p->mode != DGC_SELECT_EXACT && p->mode != DGC_SELECT_SAMPLED) return DGC_EINVAL;
+    if (p->mode != DGC_SELECT_EXACT && p->mode != DGC_SELECT_SAMPLED &&
+        p->mode != DGC_SELECT_ADACOMP)
+        return DGC_EINVAL;
+    if (p->mode == DGC_SELECT_ADACOMP && p->bin_size == 0) return DGC_EINVAL;
+    hp->bin = p->mode == DGC_SELECT_ADACOMP ? p->bin_size : 0;
     if (!(p->sparsity >= 0.0 && p->sparsity <= 1.0)) return DGC_EINVAL;
     if (!std::isfinite(p->momentum)) return DGC_EINVAL;
     if (std::isnan(p->clip_norm)) return DGC_EINVAL;
@@ -150,8 +157,11 @@ int check_params(const dgc_params* p, HostParams* hp) {
         if (hp->r_ppb == 0) return DGC_EINVAL;
         if (!(p->reselect_factor >= 1.0 && p->reselect_factor <= 16.0)) return DGC_EINVAL;
         hp->q_ppb = (uint64_t)llround(p->reselect_factor * 1e9);
-    } else {
+    } else if (p->mode == DGC_SELECT_EXACT) {
         hp->r_ppb = kExactSamplePpb;
+        hp->q_ppb = 0;
+    } else {  // AdaComp: no sample, no re-selection
+        hp->r_ppb = 0;
         hp->q_ppb = 0;
     }
     return DGC_OK;
@@ -166,6 +176,7 @@ Layout make_layout(int64_t n, int32_t nseg, const HostParams& hp) {
     L.ptiles = (un + kPTile - 1) / kPTile;
     L.cgroups = (L.ptiles + kThreads - 1) / kThreads;
     L.nbuckets = (un >> kBucketShift) + 2 * (uint64_t)nseg + 1;  // >= sum of per-segment buckets
+    L.max_bins = hp.bin ? un / hp.bin + (uint64_t)nseg + 1 : 0;  // >= sum of per-segment bins
     L.emit_tiles = (un + kEmitTile - 1) / kEmitTile;
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
@@ -188,12 +199,14 @@ Layout make_layout(int64_t n, int32_t nseg, const HostParams& hp) {
     L.cidx = take(sizeof(uint32_t) * (size_t)un);
     L.sidx = take(sizeof(uint32_t) * (size_t)un);
     L.tcount = take(sizeof(uint32_t) * (size_t)(L.ptiles + 1));
+    L.binmax = take(sizeof(uint32_t) * (size_t)L.max_bins);
     L.total = o;
     return L;
 }
 
 uint64_t max_out_for(int64_t n, int32_t nseg, const HostParams& hp) {
     const uint64_t un = (uint64_t)n;
+    if (hp.mode == DGC_SELECT_ADACOMP) return un;
     uint64_t ksum = count_ppb(un, hp.d_ppb) + (uint64_t)nseg;  // >= sum of per-segment ceils
     if (hp.d_ppb == 0) ksum = 0;
     uint64_t bound = ksum;
@@ -239,7 +252,9 @@ struct Args {
     uint32_t* cidx;   // candidates, ascending index
     uint32_t* sidx;   // per-tile candidate slots of the streaming pass
     uint32_t* tcount; // per-tile candidate counts
-    uint64_t max_samples, fused_tiles, emit_tiles, max_clip_tiles, ptiles, cgroups, nbuckets;
+    uint32_t* binmax; // AdaComp: largest |v| key of every bin
+    uint64_t max_samples, fused_tiles, emit_tiles, max_clip_tiles, ptiles, cgroups, nbuckets,
+        max_bins;
     uint32_t spin_limit;
 };
 
@@ -248,13 +263,14 @@ struct Args {
 // look-back words.
 __global__ void __launch_bounds__(1024) k_plan(Args a) {
     __shared__ uint32_t s_scan[33];
-    __shared__ uint32_t s_carry_samp, s_carry_clip, s_carry_bkt;
+    __shared__ uint32_t s_carry_samp, s_carry_clip, s_carry_bkt, s_carry_bin;
     __shared__ int s_bad;
     if (blockIdx.x == 0) {
         if (threadIdx.x == 0) {
             s_carry_samp = 0;
             s_carry_clip = 0;
             s_carry_bkt = 0;
+            s_carry_bin = 0;
             s_bad = (a.seg_off[0] != 0 || a.seg_off[a.nseg] != (int64_t)a.n) ? 1 : 0;
             Ctl c{};
             *a.ctl = c;
@@ -265,7 +281,7 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
         uint64_t tag = 0;  // what the sample positions depend on: seeds, ranges, counts
         for (int base = 0; base < a.nseg; base += 1024) {
             const int s = base + threadIdx.x;
-            uint32_t ms = 0, clip_tiles = 0, buckets = 0;
+            uint32_t ms = 0, clip_tiles = 0, buckets = 0, bins = 0;
             if (s < a.nseg) {
                 const int64_t lo = a.seg_off[s], hi = a.seg_off[s + 1];
                 if (hi < lo || lo < 0 || hi > (int64_t)a.n) atomicExch(&s_bad, 1);
@@ -275,12 +291,13 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
                 SegInfo d{};
                 d.start = st;
                 d.end = en;
-                d.k = (uint32_t)count_ppb(ns, a.hp.d_ppb);
+                d.k = a.hp.bin ? (ns + a.hp.bin - 1) / a.hp.bin  // AdaComp: bins
+                               : (uint32_t)count_ppb(ns, a.hp.d_ppb);
                 d.seed = mix64(a.hp.seed + kGolden * ((uint64_t)s + 1));
                 d.scale = 1.0f;
                 d.min_key = 0xFFFFFFFFu;
                 d.thresh = kNoKey;
-                if (d.k > 0) {
+                if (d.k > 0 && a.hp.mode != DGC_SELECT_ADACOMP) {
                     if (a.hp.mode == DGC_SELECT_SAMPLED) {
                         d.ms = (uint32_t)count_ppb(ns, a.hp.r_ppb);
                         d.rank = (uint32_t)count_ppb(d.ms, a.hp.d_ppb);
@@ -302,6 +319,7 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
                 }
                 ms = d.ms;
                 if (ms) buckets = (ns >> kBucketShift) + 1;
+                if (a.hp.bin) bins = d.k;
                 if (a.hp.clip_on) clip_tiles = (ns + kClipTile - 1) / kClipTile;
                 a.segs[s] = d;
                 a.seg_start[s] = st;
@@ -320,6 +338,10 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
             if (s < a.nseg) a.segs[s].bbase = s_carry_bkt + exb;
             __syncthreads();
             if (threadIdx.x == 0) s_carry_bkt += tot;
+            const uint32_t exn = block_excl_scan<1024>(bins, s_scan, &tot);
+            if (s < a.nseg) a.segs[s].binbase = s_carry_bin + exn;
+            __syncthreads();
+            if (threadIdx.x == 0) s_carry_bin += tot;
             __syncthreads();
         }
 #pragma unroll
@@ -354,6 +376,7 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
     for (size_t i = tid; i <= a.cgroups; i += stride) a.st_collect[i] = 0;
     for (size_t i = tid; i <= a.emit_tiles; i += stride) a.st_emit[i] = 0;
     for (size_t i = tid; i < a.nbuckets; i += stride) a.bcount[i] = 0;
+    for (size_t i = tid; i < a.max_bins; i += stride) a.binmax[i] = 0;
 }
 
 // ----------------------------------------------------------------------------- clipping
@@ -889,6 +912,11 @@ __device__ __forceinline__ void stream_compute(const Args& a, const float* sg, u
     }
 }
 
+// kSel 0: candidates are the entries at or above the segment's threshold key (DGC). kSel 1
+// (AdaComp): candidates are the entries at the largest key of their bin within the tile; the
+// tile also raises each bin's global maximum, and the emit step keeps the candidates that
+// reach it.
+template <int kSel>
 __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) {
     extern __shared__ __align__(128) float s_stage[];  // [kPStages][3][kPTile]
     __shared__ __align__(8) uint64_t s_bar[kPStages];
@@ -896,6 +924,9 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
     __shared__ int s_uniform[kPStages];
     __shared__ float s_scale[kPStages];
     __shared__ uint32_t s_thresh[kPStages];
+    __shared__ uint32_t s_start[kPStages], s_binbase[kPStages];  // first segment of the tile
+    __shared__ uint32_t s_binA[kPStages], s_nloc[kPStages];      // AdaComp: bins in the tile
+    __shared__ uint32_t s_bmax[kSel == 1 ? kPTile : 1];           // AdaComp: largest key per bin
     __shared__ uint32_t s_rc[2][kPRows * kWarps];  // candidates per (row, warp), by parity
     __shared__ int s_skip;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -914,6 +945,15 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
             s_uniform[st] = (d.end >= base + len) ? 1 : 0;
             s_scale[st] = d.scale;
             s_thresh[st] = d.thresh;
+            if (kSel == 1) {
+                const uint32_t last = (uint32_t)(base + len - 1);
+                const SegInfo& z = a.segs[upper_bound_minus1(a.seg_start, a.nseg, last)];
+                const uint32_t binA = d.binbase + ((uint32_t)base - d.start) / a.hp.bin;
+                s_start[st] = d.start;
+                s_binbase[st] = d.binbase;
+                s_binA[st] = binA;
+                s_nloc[st] = z.binbase + (last - z.start) / a.hp.bin - binA + 1;
+            }
             const uint32_t bytes = (len & ~3u) * 4u;  // whole 16-byte units; the rest by hand
             mbar_arrive_expect_tx(&s_bar[st], 3u * bytes);
             if (bytes) {
@@ -935,6 +975,8 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
             for (int st = 0; st < kPStages; ++st) issue(st);
         }
     }
+    if (kSel == 1)
+        for (int b = tid; b < kPTile; b += kThreads) s_bmax[b] = 0;
     __syncthreads();
     if (s_skip) return;
 
@@ -957,10 +999,52 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
         if (tile >= ntiles) break;  // every later stage holds an empty phase too
         const uint64_t base = (uint64_t)tile * kPTile;
         const uint32_t len = (uint32_t)(umin64(n, base + kPTile) - base);
+        const uint32_t nloc = (kSel == 1) ? s_nloc[st] : 0u;  // read before the stage is reissued
         float4 uu[kPRows], vv[kPRows];
         uint32_t flags;
         stream_compute<true>(a, s_stage + (size_t)st * kPStageFloats, base, len, s_uniform[st],
                              s_scale[st], s_thresh[st], uu, vv, flags);
+        if constexpr (kSel == 1) {  // bin-local maxima of this tile, then the candidates that reach them
+            const uint32_t binA = s_binA[st], L = a.hp.bin;
+            uint32_t lb[kPRows * 4];
+#pragma unroll
+            for (int r = 0; r < kPRows; ++r)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t off = 4u * (r * kThreads + tid) + e;
+                    uint32_t b = 0xFFFFFFFFu, key = 0;
+                    if (off < len) {
+                        const uint32_t i = (uint32_t)(base + off);
+                        uint32_t start = s_start[st], bb = s_binbase[st];
+                        if (!s_uniform[st]) {
+                            const SegInfo& d =
+                                a.segs[upper_bound_minus1(a.seg_start, a.nseg, i)];
+                            start = d.start;
+                            bb = d.binbase;
+                        }
+                        b = bb + (i - start) / L - binA;
+                        key = key_of(reinterpret_cast<const float*>(&vv[r])[e]);
+                    }
+                    lb[r * 4 + e] = b;
+                    const unsigned grp = __match_any_sync(kFull, b);
+                    const uint32_t mx = __reduce_max_sync(grp, key);
+                    if (b != 0xFFFFFFFFu && mx > 0 && lane == __ffs(grp) - 1)
+                        atomicMax(&s_bmax[b], mx);
+                }
+            __syncthreads();
+            flags = 0;
+#pragma unroll
+            for (int r = 0; r < kPRows; ++r)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t b = lb[r * 4 + e];
+                    if (b == 0xFFFFFFFFu) continue;
+                    const uint32_t key = key_of(reinterpret_cast<const float*>(&vv[r])[e]);
+                    if (key > 0 && key == s_bmax[b]) flags |= 1u << (4 * r + e);
+                }
+            for (uint32_t b = tid; b < nloc; b += kThreads)
+                if (s_bmax[b]) atomicMax(&a.binmax[binA + b], s_bmax[b]);
+        }
         // candidate words: the 8 lanes of a lane-group cover 32 consecutive entries of a row
         uint32_t word[kPRows];
 #pragma unroll
@@ -994,6 +1078,8 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
             fence_proxy_async_smem();
             issue(st);  // the next tile for this stage starts loading now
         }
+        if constexpr (kSel == 1)
+            for (uint32_t b = tid; b < nloc; b += kThreads) s_bmax[b] = 0;
         // every warp scans the kPRows x kWarps counts itself (row-major = index order)
         const uint32_t cv = (lane < kPRows * kWarps) ? s_rc[it & 1][lane] : 0u;
         const uint32_t cinc = warp_incl_scan(cv);
@@ -1021,6 +1107,7 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
             }
         }
         if (tid == 0) a.tcount[tile] = tile_total;
+        if (kSel == 1) __syncthreads();  // the bin maxima are cleared before the next tile
     }
 }
 
@@ -1116,7 +1203,8 @@ __global__ void __launch_bounds__(1024) k_candoff(Args a, int pass) {
                 d.need = d.k;
                 ++active;
             }
-        } else if ((unsigned __int128)cnt * kBillion > (unsigned __int128)a.hp.q_ppb * d.k) {
+        } else if (a.hp.mode == DGC_SELECT_SAMPLED &&
+                   (unsigned __int128)cnt * kBillion > (unsigned __int128)a.hp.q_ppb * d.k) {
             d.resel = 1;
             d.state = kActive;
             d.need = d.k;
@@ -1169,8 +1257,15 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
                     val[q] = a.v[idx[q]];
                     const int s = upper_bound_minus1(a.cand_off, a.nseg, (uint32_t)i);
                     seg[q] = s;
-                    const uint64_t x = ((uint64_t)key_of(val[q]) << 32) | (uint64_t)(~idx[q]);
-                    if (x >= a.segs[s].sel_x) sel |= 1u << q;
+                    const SegInfo& d = a.segs[s];
+                    if (a.hp.bin) {  // AdaComp: the candidate reaches its bin's largest key
+                        const uint32_t key = key_of(val[q]);
+                        if (key > 0 && key == a.binmax[d.binbase + (idx[q] - d.start) / a.hp.bin])
+                            sel |= 1u << q;
+                    } else {
+                        const uint64_t x = ((uint64_t)key_of(val[q]) << 32) | (uint64_t)(~idx[q]);
+                        if (x >= d.sel_x) sel |= 1u << q;
+                    }
                 }
             }
             const uint32_t f4 = (sel >> (4 * r)) & 0xFu;
@@ -1192,8 +1287,9 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
         }
         __syncthreads();
         const uint64_t gbase = s_base;
-        int my_seg = -1;             // the smallest key sent, per segment: one atomic per warp
-        uint32_t my_min = 0xFFFFFFFFu;
+        int my_seg = -1;             // the smallest key sent and the number sent, per segment:
+        uint32_t my_min = 0xFFFFFFFFu;  // one atomic per warp
+        uint32_t my_cnt = 0;
 #pragma unroll
         for (int q = 0; q < kEmitRows * 4; ++q) {
             if (seg[q] < 0) continue;
@@ -1201,8 +1297,13 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
             if (sel & (1u << q)) {
                 const uint32_t key = key_of(val[q]);
                 if (my_seg < 0) my_seg = seg[q];
-                if (seg[q] == my_seg) my_min = min(my_min, key);
-                else atomicMin(&a.segs[seg[q]].min_key, key);
+                if (seg[q] == my_seg) {
+                    my_min = min(my_min, key);
+                    ++my_cnt;
+                } else {
+                    atomicMin(&a.segs[seg[q]].min_key, key);
+                    atomicAdd(&a.segs[seg[q]].nsent, 1u);
+                }
                 const uint32_t off = (uint32_t)(i - base);
                 const uint32_t w = off >> 5;
                 const uint64_t pos =
@@ -1218,8 +1319,11 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
         {
             const unsigned group = __match_any_sync(kFull, my_seg);
             const uint32_t gmin = __reduce_min_sync(group, my_min);
-            if (my_seg >= 0 && (threadIdx.x & 31) == __ffs(group) - 1)
+            const uint32_t gcnt = __reduce_add_sync(group, my_cnt);
+            if (my_seg >= 0 && (threadIdx.x & 31) == __ffs(group) - 1) {
                 atomicMin(&a.segs[my_seg].min_key, gmin);
+                atomicAdd(&a.segs[my_seg].nsent, gcnt);
+            }
         }
         if (tile == ntiles - 1 && threadIdx.x == 0) a.ctl->total_sent = (uint32_t)(gbase + tile_total);
         __syncthreads();
@@ -1240,10 +1344,11 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
         uint64_t sent = 0;
         if (ok && d.k > 0) {
             if (a.hp.mode == DGC_SELECT_EXACT) sent = d.k;
+            else if (a.hp.mode == DGC_SELECT_ADACOMP) sent = ld_relaxed_u32(&d.nsent);
             else sent = d.resel ? d.k : d.cand_cnt;
         }
         o.sent = sent;
-        o.candidates = (a.hp.mode == DGC_SELECT_EXACT) ? sent : (ok ? d.cand_cnt : 0);
+        o.candidates = (a.hp.mode != DGC_SELECT_SAMPLED) ? sent : (ok ? d.cand_cnt : 0);
         o.thresh_key = ld_relaxed_u32(&d.min_key);
         o.sample_key = (a.hp.mode == DGC_SELECT_SAMPLED && d.k > 0) ? d.thresh : 0u;
         o.reselected = d.resel;
@@ -1342,11 +1447,13 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     a.cidx = reinterpret_cast<uint32_t*>(w + L.cidx);
     a.sidx = reinterpret_cast<uint32_t*>(w + L.sidx);
     a.tcount = reinterpret_cast<uint32_t*>(w + L.tcount);
+    a.binmax = reinterpret_cast<uint32_t*>(w + L.binmax);
     a.max_samples = L.max_samples;
     a.fused_tiles = L.fused_tiles;
     a.ptiles = L.ptiles;
     a.cgroups = L.cgroups;
     a.nbuckets = L.nbuckets;
+    a.max_bins = L.max_bins;
     a.emit_tiles = L.emit_tiles;
     a.max_clip_tiles = L.max_clip_tiles;
     a.spin_limit = kDefaultSpinLimit;
@@ -1360,8 +1467,8 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
         kernel<<<grid, block, 0, s>>>(args...);
         ++launches;
     };
-    const size_t zero_work =
-        (size_t)nseg * kHistBins + L.fused_tiles + L.emit_tiles + L.nbuckets + 2;
+    const size_t zero_work = (size_t)nseg * kHistBins + L.fused_tiles + L.emit_tiles +
+                             L.nbuckets + L.max_bins + 2;
     const unsigned plan_grid = (unsigned)std::min<size_t>((zero_work + 1023) / 1024 + 1,
                                                           (size_t)sms * 2);
     L1(k_plan, plan_grid, 1024, a);
@@ -1392,13 +1499,18 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
         int dev = 0;
         cudaGetDevice(&dev);
         if (dev >= 0 && dev < 128 && !attr_set[dev]) {
-            cudaFuncSetAttribute(k_stream_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(k_stream_tma<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kPSmemBytes);
+            cudaFuncSetAttribute(k_stream_tma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kPSmemBytes);
             attr_set[dev] = true;
         }
         const unsigned pgrid =
             (unsigned)std::min<uint64_t>((uint64_t)sms * kPBlocksPerSM, L.ptiles);
-        k_stream_tma<<<pgrid, kThreads, kPSmemBytes, s>>>(a);
+        if (hp.mode == DGC_SELECT_ADACOMP)
+            k_stream_tma<1><<<pgrid, kThreads, kPSmemBytes, s>>>(a);
+        else
+            k_stream_tma<0><<<pgrid, kThreads, kPSmemBytes, s>>>(a);
         ++launches;
     }
     if (pb && pe) cudaEventRecord(pe, s);

@@ -48,6 +48,7 @@ def test_workspace_and_bounds_queries(L):
     assert dgc.dgc_compress_max_out(1_048_576, 1, p) == 1049 + 1  # sum of ceilings + slack
     assert dgc.dgc_compress_max_out(1000, 1, P(sparsity=0.0)) == 1000
     assert dgc.dgc_compress_max_out(1000, 1, P(sparsity=1.0)) == 0
+    assert dgc.dgc_compress_max_out(1000, 3, P(mode=dgc.SELECT_ADACOMP, bin_size=7)) == 1000
     ps = P(mode=dgc.SELECT_SAMPLED, sparsity=0.999, reselect_factor=1.3)
     assert dgc.dgc_compress_max_out(1 << 30, 1, ps) >= int(1.3 * 1073742)
     w1 = dgc.dgc_compress_workspace(1 << 20, 1, p)
@@ -95,6 +96,7 @@ def _compress(L, n=1024, nseg=1, params=None, g=FAKE, u=FAKE, v=FAKE, seg=FAKE, 
     (dict(params=P(mode=dgc.SELECT_SAMPLED, sample_ratio=0.0)), dgc.EINVAL),
     (dict(params=P(mode=dgc.SELECT_SAMPLED, sample_ratio=1e-12)), dgc.EINVAL),
     (dict(params=P(mode=dgc.SELECT_SAMPLED, reselect_factor=0.5)), dgc.EINVAL),
+    (dict(params=P(mode=dgc.SELECT_ADACOMP, bin_size=0)), dgc.EINVAL),
     (dict(g=None), dgc.EINVAL),
     (dict(g=FAKE + 4), dgc.EINVAL),
     (dict(u=FAKE + 8), dgc.EINVAL),

@@ -231,6 +231,38 @@ def test_sampled_edges(case):
               clip_norm=float(rng.choice([0.0, 1.0])))
 
 
+@pytest.mark.parametrize("case", range(30))
+def test_adacomp_edges(case):
+    # AdaComp bin-local selection against the oracle: bins of bin_size entries per segment, the
+    # entries at each bin's largest |v| sent (ties included, all-zero bins send nothing)
+    rng = np.random.default_rng(11000 + case)
+    n = EDGE_N[case % len(EDGE_N)] * (1 + case % 2)
+    off = _segments(rng, n)
+    L = int(rng.choice([1, 3, 17, 50, 1000, 2048, 5000]))
+    kind = case % 3
+
+    def grads(t):
+        r = np.random.default_rng([case, t, 2])
+        if kind == 1:
+            return r.integers(-2, 3, n).astype(np.float32)
+        if kind == 2:
+            x = (r.standard_normal(n) * 0.01).astype(np.float32)
+            x[r.random(n) < 0.5] = 0.0
+            return x
+        return (r.standard_normal(n) * 0.01).astype(np.float32)
+
+    run_steps(grads, off, 3, mode=dgc.SELECT_ADACOMP, bin_size=L,
+              momentum=float(rng.choice([0.0, 0.9])), mask_momentum=bool(case % 2),
+              clip_norm=float(rng.choice([0.0, 1.0])))
+
+
+@pytest.mark.slow
+def test_adacomp_resnet50_layout():
+    off = workloads.resnet50_segments()
+    run_steps(lambda t: workloads.gradient("resnet50", t), off, 3, mode=dgc.SELECT_ADACOMP,
+              bin_size=1000, momentum=0.9, clip_norm=1.0)
+
+
 def test_exact_tight_sample_bound_falls_back():
     # White-box: exact mode bounds the threshold from below with a 1% sample drawn from the same
     # SplitMix64 positions (seed from the params). Putting the only large values exactly at the
