@@ -104,6 +104,8 @@ def lib():
         L.orc_encode.argtypes = [vp, vp, i64, i64, vp, u64, ctypes.POINTER(u64)]
         L.orc_decode_accumulate.restype = ctypes.c_int
         L.orc_decode_accumulate.argtypes = [vp, vp, i32, vp, i64, ctypes.c_int]
+        L.orc_decode_apply.restype = ctypes.c_int
+        L.orc_decode_apply.argtypes = [vp, vp, i32, vp, i64, ctypes.c_float]
         _lib = L
     return _lib
 
@@ -230,3 +232,17 @@ def decode_accumulate(streams, n: int, dense=None, accumulate=False):
                                      ctypes.cast(sizes, ctypes.c_void_p), W,
                                      _ptr(dense) if n else None, int(n), int(bool(accumulate)))
     return rc, dense
+
+
+def decode_apply(streams, n: int, w, lr: float):
+    """Decode and sum the messages in order, then w <- fmaf(-lr, sum, w). Returns (rc, w)."""
+    bufs = [np.frombuffer(s, dtype=np.uint8) if len(s) else np.zeros(1, np.uint8)
+            for s in streams]
+    W = len(bufs)
+    ptrs = (ctypes.c_void_p * max(W, 1))(*[b.ctypes.data for b in bufs])
+    sizes = (ctypes.c_uint64 * max(W, 1))(*[len(s) for s in streams])
+    w = np.ascontiguousarray(w, dtype=np.float32).copy()
+    rc = lib().orc_decode_apply(ctypes.cast(ptrs, ctypes.c_void_p),
+                                ctypes.cast(sizes, ctypes.c_void_p), W,
+                                _ptr(w) if n else None, int(n), float(lr))
+    return rc, w

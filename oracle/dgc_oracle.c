@@ -431,3 +431,23 @@ int orc_decode_accumulate(const uint8_t* const* streams, const uint64_t* stream_
     }
     return ORC_OK;
 }
+
+/* Decode, sum and apply as one plain SGD step: s = the ordered sum of the W messages (exactly
+ * as orc_decode_accumulate builds it from +0), then w_i <- fmaf(-lr, s_i, w_i) for every i.
+ * [DGC] Abstract: the setting is distributed SGD; "Proposed method", momentum-correction
+ * bullet: the velocity is accumulated locally, so what the learners send is already the
+ * momentum-corrected update. Reading: the receiver therefore takes a plain SGD step
+ * w <- w - lr * s with the summed message, one rounding (fmaf); the caller folds any 1/W
+ * average into lr. lr must be finite with its sign bit clear (+0 allowed): then entries that no
+ * message touches (s_i = +0) keep their bits, -0 included. On any error w is left unchanged. */
+int orc_decode_apply(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
+                     float* w, int64_t n, float lr) {
+    if (W < 0 || n < 0 || !isfinite(lr) || signbit(lr)) return ORC_EINVAL;
+    float* s = (float*)calloc(n > 0 ? (size_t)n : 1, sizeof(float));
+    if (!s) return ORC_ENOMEM;
+    const int rc = orc_decode_accumulate(streams, stream_bytes, W, s, n, 0);
+    if (rc == ORC_OK)
+        for (int64_t i = 0; i < n; ++i) w[i] = fmaf(-lr, s[i], w[i]);
+    free(s);
+    return rc;
+}

@@ -68,6 +68,8 @@ int orc_encode(const uint32_t* idx, const float* val, int64_t count, int64_t n, 
                uint64_t out_cap, uint64_t* out_bytes);
 int orc_decode_accumulate(const uint8_t* const* streams, const uint64_t* stream_bytes,
                           int32_t W, float* dense, int64_t n, int accumulate);
+int orc_decode_apply(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
+                     float* w, int64_t n, float lr);
 
 #ifdef __cplusplus
 }

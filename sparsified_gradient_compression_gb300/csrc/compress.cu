@@ -56,7 +56,7 @@ constexpr int kWarps = kThreads / 32;
 static_assert(kPRows >= 1 && kPRows * 4 * kThreads == kPTile, "tile = rows x 1024 entries");
 static_assert(kPRows * kWarps <= 32, "one warp scans the per-(row, warp) counts");
 constexpr uint32_t kPStageFloats = 3u * kPTile;   // g, u, v
-constexpr size_t kPSmemBytes = sizeof(float) * kPStageFloats * kPStages;  // 192 KiB
+constexpr size_t kPSmemBytes = sizeof(float) * kPStageFloats * kPStages;  // 96 KiB
 constexpr uint32_t kMbarSpinLimit = 1u << 22;
 constexpr int kEmitRows = 4;
 constexpr int kEmitTile = kThreads * kEmitRows * 4;  // 4096 candidates per emit tile
@@ -855,8 +855,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_recompact(Args a) {
 
 // ------------------------------------------------- streaming pass, bulk-copy pipeline
 // The pass every entry goes through: u = fma(m, u, g*scale); v += u; candidates are the
-// entries with key(v) >= the segment's threshold. Persistent blocks (one per SM) take 4096-entry
-// tiles from an atomic ticket and keep kPStages tiles of g, u and v in flight as bulk copies
+// entries with key(v) >= the segment's threshold. Persistent blocks (kPBlocksPerSM per SM) take
+// kPTile-entry tiles from an atomic ticket and keep kPStages tiles of g, u and v in flight as bulk copies
 // (TMA, cp.async.bulk) into shared memory, so HBM streams without pause. Updated u and v go back
 // with coalesced 16-byte stores. A tile's candidates are compacted, in index order, into the
 // tile's own slot range sidx[base, base + count) and its count into tcount[tile]: no block
@@ -924,9 +924,11 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
     __shared__ int s_uniform[kPStages];
     __shared__ float s_scale[kPStages];
     __shared__ uint32_t s_thresh[kPStages];
-    __shared__ uint32_t s_start[kPStages], s_binbase[kPStages];  // first segment of the tile
     __shared__ uint32_t s_binA[kPStages], s_nloc[kPStages];      // AdaComp: bins in the tile
-    __shared__ uint32_t s_bmax[kSel == 1 ? kPTile : 1];           // AdaComp: largest key per bin
+    __shared__ uint32_t s_rem[kPStages];  // AdaComp: offset of the tile start in bin s_binA
+    // AdaComp: per local bin, (tile tag << 32) | largest key; a slot whose tag is not the current
+    // tile's counts as 0, so the slots never need clearing
+    __shared__ unsigned long long s_bmax[kSel == 1 ? kPTile : 1];
     __shared__ uint32_t s_rc[2][kPRows * kWarps];  // candidates per (row, warp), by parity
     __shared__ int s_skip;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -949,9 +951,8 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
                 const uint32_t last = (uint32_t)(base + len - 1);
                 const SegInfo& z = a.segs[upper_bound_minus1(a.seg_start, a.nseg, last)];
                 const uint32_t binA = d.binbase + ((uint32_t)base - d.start) / a.hp.bin;
-                s_start[st] = d.start;
-                s_binbase[st] = d.binbase;
                 s_binA[st] = binA;
+                s_rem[st] = ((uint32_t)base - d.start) - (binA - d.binbase) * a.hp.bin;
                 s_nloc[st] = z.binbase + (last - z.start) / a.hp.bin - binA + 1;
             }
             const uint32_t bytes = (len & ~3u) * 4u;  // whole 16-byte units; the rest by hand
@@ -1006,44 +1007,83 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
                              s_scale[st], s_thresh[st], uu, vv, flags);
         if constexpr (kSel == 1) {  // bin-local maxima of this tile, then the candidates that reach them
             const uint32_t binA = s_binA[st], L = a.hp.bin;
+            const uint64_t tag = (uint64_t)(it + 1) << 32;  // slots of earlier tiles hold smaller tags
             uint32_t lb[kPRows * 4];
+            if (s_uniform[st]) {
+                // one segment: the tile's entry o lies in local bin (rem + o) / L, rem being the
+                // tile start's offset within bin binA; bins rise with o, so a warp row holds
+                // contiguous runs of equal bins
+                const uint32_t rem = s_rem[st];
 #pragma unroll
-            for (int r = 0; r < kPRows; ++r)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint32_t off = 4u * (r * kThreads + tid) + e;
-                    uint32_t b = 0xFFFFFFFFu, key = 0;
-                    if (off < len) {
-                        const uint32_t i = (uint32_t)(base + off);
-                        uint32_t start = s_start[st], bb = s_binbase[st];
-                        if (!s_uniform[st]) {
-                            const SegInfo& d =
-                                a.segs[upper_bound_minus1(a.seg_start, a.nseg, i)];
-                            start = d.start;
-                            bb = d.binbase;
-                        }
-                        b = bb + (i - start) / L - binA;
-                        key = key_of(reinterpret_cast<const float*>(&vv[r])[e]);
+                for (int r = 0; r < kPRows; ++r) {
+                    const uint32_t o0 = 4u * (r * kThreads + tid);
+                    uint32_t q, d0;  // local bin of entry o0, and entries from o0 to the next bin
+                    if (L >= (uint32_t)kPTile) {
+                        q = (o0 >= L - rem) ? 1u : 0u;
+                        d0 = q ? L - (o0 - (L - rem)) : L - rem - o0;
+                    } else {
+                        q = (rem + o0) / L;
+                        d0 = L - (rem + o0 - q * L);
                     }
-                    lb[r * 4 + e] = b;
-                    const unsigned grp = __match_any_sync(kFull, b);
-                    const uint32_t mx = __reduce_max_sync(grp, key);
-                    if (b != 0xFFFFFFFFu && mx > 0 && lane == __ffs(grp) - 1)
-                        atomicMax(&s_bmax[b], mx);
+                    const float* vr = reinterpret_cast<const float*>(&vv[r]);
+                    uint32_t b = q, nxt = d0, mx = 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if ((uint32_t)e == nxt) {  // a bin starts at this entry
+                            if (mx) atomicMax(&s_bmax[b], tag | mx);
+                            ++b;
+                            nxt += L < 4u ? L : 4u;
+                            mx = 0;
+                        }
+                        lb[r * 4 + e] = b;
+                        const uint32_t key = (o0 + e < len) ? key_of(vr[e]) : 0u;
+                        mx = key > mx ? key : mx;
+                    }
+                    // the lane's last bin: a max over the run of lanes that share it, kept by
+                    // the run's first lane
+#pragma unroll
+                    for (int dl = 1; dl < 32; dl <<= 1) {
+                        const uint32_t om = __shfl_down_sync(kFull, mx, dl);
+                        const uint32_t ob = __shfl_down_sync(kFull, b, dl);
+                        if (lane + dl < 32 && ob == b && om > mx) mx = om;
+                    }
+                    const uint32_t pb = __shfl_up_sync(kFull, b, 1);
+                    if (mx && (lane == 0 || pb != b)) atomicMax(&s_bmax[b], tag | mx);
                 }
+            } else {  // a segment boundary inside the tile (rare): every entry on its own
+#pragma unroll
+                for (int r = 0; r < kPRows; ++r)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t off = 4u * (r * kThreads + tid) + e;
+                        uint32_t b = 0;
+                        if (off < len) {
+                            const uint32_t i = (uint32_t)(base + off);
+                            const SegInfo& d = a.segs[upper_bound_minus1(a.seg_start, a.nseg, i)];
+                            b = d.binbase + (i - d.start) / L - binA;
+                            const uint32_t key = key_of(reinterpret_cast<const float*>(&vv[r])[e]);
+                            if (key) atomicMax(&s_bmax[b], tag | key);
+                        }
+                        lb[r * 4 + e] = b;
+                    }
+            }
             __syncthreads();
             flags = 0;
 #pragma unroll
             for (int r = 0; r < kPRows; ++r)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const uint32_t b = lb[r * 4 + e];
-                    if (b == 0xFFFFFFFFu) continue;
+                    if (4u * (r * kThreads + tid) + e >= len) continue;
                     const uint32_t key = key_of(reinterpret_cast<const float*>(&vv[r])[e]);
-                    if (key > 0 && key == s_bmax[b]) flags |= 1u << (4 * r + e);
+                    const unsigned long long m = s_bmax[lb[r * 4 + e]];
+                    if (key > 0 && m == (tag | key)) flags |= 1u << (4 * r + e);
                 }
-            for (uint32_t b = tid; b < nloc; b += kThreads)
-                if (s_bmax[b]) atomicMax(&a.binmax[binA + b], s_bmax[b]);
+            // this tile's maxima into the global ones; before the next block barrier, since
+            // the next tile's (larger) tags may overwrite the slots right after it
+            for (uint32_t b = tid; b < nloc; b += kThreads) {
+                const unsigned long long m = s_bmax[b];
+                if ((m & ~0xFFFFFFFFull) == tag) atomicMax(&a.binmax[binA + b], (uint32_t)m);
+            }
         }
         // candidate words: the 8 lanes of a lane-group cover 32 consecutive entries of a row
         uint32_t word[kPRows];
@@ -1078,8 +1118,6 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
             fence_proxy_async_smem();
             issue(st);  // the next tile for this stage starts loading now
         }
-        if constexpr (kSel == 1)
-            for (uint32_t b = tid; b < nloc; b += kThreads) s_bmax[b] = 0;
         // every warp scans the kPRows x kWarps counts itself (row-major = index order)
         const uint32_t cv = (lane < kPRows * kWarps) ? s_rc[it & 1][lane] : 0u;
         const uint32_t cinc = warp_incl_scan(cv);
@@ -1107,7 +1145,6 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
             }
         }
         if (tid == 0) a.tcount[tile] = tile_total;
-        if (kSel == 1) __syncthreads();  // the bin maxima are cleared before the next tile
     }
 }
 
@@ -1503,6 +1540,11 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
                                  (int)kPSmemBytes);
             cudaFuncSetAttribute(k_stream_tma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kPSmemBytes);
+            // the AdaComp variant needs nearly all of the SM's shared memory for two blocks
+            cudaFuncSetAttribute(k_stream_tma<0>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+            cudaFuncSetAttribute(k_stream_tma<1>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
             attr_set[dev] = true;
         }
         const unsigned pgrid =

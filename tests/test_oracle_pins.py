@@ -609,3 +609,99 @@ def test_adacomp_compress_matches_definition(orc, seed):
     assert vv.view(np.uint32).tolist() == v_exp.view(np.uint32).tolist()
     for s_, (a, b) in zip(st, zip(off[:-1], off[1:])):
         assert s_["k"] == -(-(int(b) - int(a)) // L)
+
+
+# ------------------------------------------------------------------ decode -> plain SGD step
+# Reading of "[Paper Review] Deep Gradient Compression ...", Abstract (distributed SGD) and
+# "Proposed method" (momentum correction keeps the velocity on the learner): the receiver adds
+# the messages in learner order from +0 and takes w <- fmaf(-lr, sum, w), one rounding. The
+# expected values below come from exact rational arithmetic, not from the oracle.
+def _apply_expected(w, parts, lr):
+    s = {}
+    for idx, val in parts:
+        for i, x in zip(idx.tolist(), val):
+            s[i] = X.add_f32(s.get(i, np.float32(0.0)), x)
+    exp = w.copy()
+    for i, t in s.items():
+        exp[i] = X.fma_f32(np.float32(-lr), t, w[i])
+    return exp, s
+
+
+@pytest.mark.parametrize("name", ["codec_gaps.txt", "codec_single.txt", "codec_odd.txt",
+                                  "codec_empty.txt"])
+def test_decode_apply_golden_streams(orc, name):
+    n, idx, val, msg, _ = golden_message(name)
+    rng = np.random.default_rng(17)
+    w = _tricky(rng, n, 0)
+    exp, _ = _apply_expected(w, [(idx, val)], 0.75)
+    rc, out = orc.decode_apply([msg], n, w, 0.75)
+    assert rc == 0
+    assert out.view(np.uint32).tolist() == exp.view(np.uint32).tolist()
+
+
+def test_decode_apply_learner_order_golden(orc):
+    # the ordered sum at index 2 is exactly 0 (see decode_order.txt), so w[2] keeps its bits;
+    # any other order would leave 1 or -1e8 + ... and move w[2]
+    rows = read_golden("decode_order.txt")
+    n = rows[0][1][0]
+    msgs = [orc.encode(np.array([r[1][0]], np.uint32),
+                       np.array([r[1][1]], np.uint32).view(np.float32), n)
+            for r in rows if r[0] == "learner"]
+    w = np.array([1.5, -2.5, 3.25, -0.0], np.float32)
+    rc, out = orc.decode_apply(msgs, n, w, 0.5)
+    assert rc == 0 and out.view(np.uint32).tolist() == w.view(np.uint32).tolist()
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_decode_apply_random_learners(orc, seed):
+    rng = np.random.default_rng(900 + seed)
+    n, W = int(rng.integers(1, 3000)), int(rng.integers(1, 6))
+    lr = float(np.float32(rng.choice([0.1, 0.37, 1.0, 3.0]))) if seed else float(np.float32(0.37))
+    msgs, parts = [], []
+    for _ in range(W):
+        k = int(rng.integers(0, min(n, 300) + 1))
+        idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+        val = (rng.standard_normal(k) * 10.0 ** rng.integers(-3, 3, k)).astype(np.float32)
+        msgs.append(orc.encode(idx, val, n))
+        parts.append((idx, val))
+    w = (rng.standard_normal(n) * 10.0 ** rng.integers(-3, 3, n)).astype(np.float32)
+    w[rng.random(n) < 0.05] = -0.0
+    exp, s = _apply_expected(w, parts, lr)
+    rc, out = orc.decode_apply(msgs, n, w, lr)
+    assert rc == 0
+    assert out.view(np.uint32).tolist() == exp.view(np.uint32).tolist()
+    # the single rounding matters on these inputs: a separate multiply and subtract differs
+    if seed == 0:
+        two = [X.add_f32(w[i], -X.mul_f32(lr, t)) for i, t in s.items()]
+        assert any(X.bits(a) != X.bits(exp[i]) for a, i in zip(two, s.keys()))
+
+
+def test_decode_apply_closed_forms(orc):
+    rng = np.random.default_rng(5)
+    n = 2000
+    idx = np.sort(rng.choice(n, 100, replace=False)).astype(np.uint32)
+    val = rng.standard_normal(100).astype(np.float32)
+    msg = orc.encode(idx, val, n)
+    w = rng.standard_normal(n).astype(np.float32)
+    w[::7] = -0.0
+    untouched = np.setdiff1d(np.arange(n), idx)
+    rc, out = orc.decode_apply([msg], n, w, 0.0)  # lr = +0: no value moves (a touched -0 may
+    assert rc == 0 and np.array_equal(out, w)     # become +0: -0*t + -0 is +0 for t < 0)
+    assert out[untouched].view(np.uint32).tolist() == w[untouched].view(np.uint32).tolist()
+    rc, out = orc.decode_apply([msg], n, np.zeros(n, np.float32), 1.0)  # from 0, lr 1: -sum
+    exp = np.zeros(n, np.float32)
+    exp[idx] = -val
+    assert rc == 0 and out.view(np.uint32).tolist() == exp.view(np.uint32).tolist()
+    rc, out = orc.decode_apply([msg], n, w, 2.0)  # untouched entries keep their bits, -0 too
+    assert out[untouched].view(np.uint32).tolist() == w[untouched].view(np.uint32).tolist()
+
+
+def test_decode_apply_rejects(orc):
+    n = 100
+    msg = orc.encode(np.array([3], np.uint32), np.array([1.0], np.float32), n)
+    w = np.full(n, 2.0, np.float32)
+    for lr in (-0.0, -1.0, math.inf, math.nan):
+        rc, out = orc.decode_apply([msg], n, w, lr)
+        assert rc == orc.EINVAL and np.all(out == 2.0)
+    rc, out = orc.decode_apply([msg, b"XGC1" + msg[4:]], n, w, 1.0)
+    assert rc == orc.ECORRUPT and np.all(out == 2.0)
