@@ -247,6 +247,25 @@ class Pipeline:
             ev[3].record()
         return nb
 
+    def time_decode_apply(self, nb, reps=20):
+        """The receiving side's alternative to the dense decode: the last message applied as one
+        SGD step to a weight vector (dgc_decode_apply), timed alone with CUDA events."""
+        import torch
+
+        w = torch.zeros(self.n, dtype=torch.float32, device=self.dev)
+        E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        ms = []
+        for _ in range(reps + 3):
+            a, b = E(), E()
+            a.record()
+            self.dgc.dgc_decode_apply([self.msg], [nb], w, self.n, 0.01, self.status, self.dws,
+                                      ws_bytes=self.dws_bytes)
+            b.record()
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        del w
+        return sorted(ms[3:])[reps // 2]
+
 
 def run_ours(args, world, rank, local):
     import numpy as np
@@ -323,6 +342,9 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peak_hbm()
     achieved = alg_bytes / (t_kernel / 1e3) / 1e9
     traffic = recorded_traffic(n)
+    t_apply = pipe.time_decode_apply(nbytes[-1])
+    if dgc.dgc_read_status(pipe.status) != 0:
+        raise RuntimeError("decode-apply reported an error")
 
     e2e = None if args.no_e2e else run_e2e(args, pipe, pool, p_main, K)
     cpu = None
@@ -347,6 +369,7 @@ def run_ours(args, world, rank, local):
                      "alg_bytes": alg_bytes, "kernel_ms": round(t_kernel, 4)},
         "stages_ms": {"compress": round(t_compress, 4), "encode": round(t_encode, 4),
                       "decode": round(t_decode, 4)},
+        "decode_apply_ms": round(t_apply, 4),  # outside the step: message -> SGD step on w
         "compress_gbs": round(4.0 * n / (t_compress / 1e3) / 1e9, 2),
         "message_bytes": int(statistics.median(nbytes)),
         "candidates": cand, "sent": int(st["sent"]),
@@ -411,11 +434,13 @@ def run_e2e(args, pipe, pool, p, K_dev):
     b.record(main)
     torch.cuda.synchronize()
     sec = a.elapsed_time(b) / 1e3
-    copy_ms = sorted(began[i].elapsed_time(landed[i]) for i in range(K))
+    copy_each = [round(began[i].elapsed_time(landed[i]), 2) for i in range(K)]
+    copy_ms = sorted(copy_each)
     return {"value": round(4.0 * n * K / sec / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": int(d2h / K), "steps": K,
             "h2d_ms_median": round(copy_ms[len(copy_ms) // 2], 3),
             "h2d_gbs_median": round(4.0 * n / (copy_ms[len(copy_ms) // 2] / 1e3) / 1e9, 1),
+            "h2d_ms_each": copy_each,
             "note": "gradient copied from pinned host memory each step on a second stream, "
                     "overlapped with the previous step's kernels; message copied back"}
 

@@ -178,7 +178,8 @@ int dgc_encode(const uint32_t* idx, const float* val, const int64_t* count, int6
 
 /* ---------------------------------------------------------------------------- decoder */
 
-/* Bytes of workspace dgc_decode_accumulate needs for W messages of the given sizes (host). */
+/* Bytes of workspace dgc_decode_accumulate or dgc_decode_apply needs for W messages of the
+ * given sizes (host). */
 int dgc_decode_workspace(int32_t W, const uint64_t* stream_bytes, int64_t n, size_t* bytes);
 
 /* Decode W messages and sum them into dense (device, n binary32): synchronous SGD adds up
@@ -188,10 +189,27 @@ int dgc_decode_workspace(int32_t W, const uint64_t* stream_bytes, int64_t n, siz
  *   streams       host array of W device pointers (16-byte aligned)
  *   stream_bytes  host array of W sizes; a size that no message can have returns DGC_ECORRUPT
  * A message whose header (magic, version, n, T) or runs (a position at or past n) are wrong
- * sets *status = DGC_ECORRUPT and is skipped; nothing is written outside dense[0, n). */
+ * sets *status = DGC_ECORRUPT and dense is left as it was; nothing is written outside
+ * dense[0, n). */
 int dgc_decode_accumulate(const uint8_t* const* streams, const uint64_t* stream_bytes,
                           int32_t W, float* dense, int64_t n, int32_t accumulate,
                           int32_t* status, void* ws, size_t ws_bytes, dgc_stream_t stream);
+
+/* Decode W messages, sum them and take one plain SGD step on the weights w (device, n
+ * binary32): s = the sum dgc_decode_accumulate would produce from +0 (learner order 0..W-1),
+ * then w_i <- fma(-lr, s_i, w_i) with one rounding. [DGC] Abstract (distributed SGD) and
+ * Proposed method (momentum correction keeps the velocity on each learner, so the messages
+ * already carry the momentum-corrected update): the receiver's step is plain SGD. Fold any
+ * 1/W average into lr.
+ *   lr  finite, sign bit clear (+0 allowed); anything else returns DGC_EINVAL. Under that rule
+ *       the update is the identity wherever no message lands, and those entries are not
+ *       touched at all: no dense sum is written, w is read and written only at received
+ *       positions.
+ * Workspace: dgc_decode_workspace. Arguments and errors as for dgc_decode_accumulate; on
+ * DGC_ECORRUPT w is left as it was. */
+int dgc_decode_apply(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
+                     float* w, int64_t n, float lr, int32_t* status, void* ws, size_t ws_bytes,
+                     dgc_stream_t stream);
 
 /* -------------------------------------------------------------------------- utilities */
 

@@ -17,7 +17,7 @@ __all__ = [
     "DGCError", "build", "lib", "dgc_params", "dgc_seg_stats", "make_params",
     "dgc_compress_workspace", "dgc_compress_max_out", "dgc_compress", "dgc_compress_noalloc",
     "dgc_encode_max_bytes", "dgc_encode_workspace", "dgc_encode",
-    "dgc_decode_workspace", "dgc_decode_accumulate",
+    "dgc_decode_workspace", "dgc_decode_accumulate", "dgc_decode_apply",
     "dgc_read_status", "dgc_status_string", "dgc_launch_count", "dgc_selftest_wait_timeout",
     "dgc_profile_stream_pass",
     "SELECT_EXACT", "SELECT_SAMPLED", "SELECT_ADACOMP", "FLAG_MASK_MOMENTUM",
@@ -89,6 +89,7 @@ def lib():
         L.dgc_encode.argtypes = [vp, vp, vp, i64, i64, vp, u64, vp, vp, vp, sz, vp]
         L.dgc_decode_workspace.argtypes = [i32, vp, i64, P(sz)]
         L.dgc_decode_accumulate.argtypes = [vp, vp, i32, vp, i64, i32, vp, vp, sz, vp]
+        L.dgc_decode_apply.argtypes = [vp, vp, i32, vp, i64, ctypes.c_float, vp, vp, sz, vp]
         L.dgc_read_status.argtypes = [vp, vp]
         L.dgc_status_string.argtypes = [ctypes.c_int]
         L.dgc_status_string.restype = ctypes.c_char_p
@@ -100,7 +101,8 @@ def lib():
         for f in ("dgc_compress_workspace", "dgc_compress_max_out", "dgc_compress",
                   "dgc_compress_noalloc",
                   "dgc_encode_max_bytes", "dgc_encode_workspace", "dgc_encode",
-                  "dgc_decode_workspace", "dgc_decode_accumulate", "dgc_read_status",
+                  "dgc_decode_workspace", "dgc_decode_accumulate", "dgc_decode_apply",
+                  "dgc_read_status",
                   "dgc_selftest_wait_timeout"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
@@ -239,6 +241,19 @@ def dgc_decode_accumulate(streams, stream_bytes, dense, n: int, accumulate: bool
                                               _ptr(dense), int(n), int(bool(accumulate)),
                                               _ptr(status), _ptr(ws), int(ws_bytes),
                                               _stream(stream)), "dgc_decode_accumulate")
+
+
+def dgc_decode_apply(streams, stream_bytes, w, n: int, lr: float, status, ws,
+                     ws_bytes: int | None = None, stream=None) -> int:
+    """w <- fma(-lr, ordered sum of the decoded messages, w); streams as for decode."""
+    W = len(stream_bytes)
+    ptrs = (ctypes.c_void_p * max(W, 1))(*[_ptr(s) for s in streams])
+    sizes = (ctypes.c_uint64 * max(W, 1))(*[int(b) for b in stream_bytes])
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    return _check(lib().dgc_decode_apply(ctypes.cast(ptrs, ctypes.c_void_p),
+                                         ctypes.cast(sizes, ctypes.c_void_p), W, _ptr(w), int(n),
+                                         float(lr), _ptr(status), _ptr(ws), int(ws_bytes),
+                                         _stream(stream)), "dgc_decode_apply")
 
 
 # ----------------------------------------------------------------------------- utilities

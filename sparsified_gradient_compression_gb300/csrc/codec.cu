@@ -1,4 +1,4 @@
-// codec.cu -- dgc_encode and dgc_decode_accumulate on sm_103a.
+// codec.cu -- dgc_encode, dgc_decode_accumulate and dgc_decode_apply on sm_103a.
 //
 // Source: "[Paper Review] Deep Gradient Compression: Reducing the Communication Bandwidth for
 // Distributed Training", Proposed method, bullet 2 (each sent value as a 32-bit word and the
@@ -17,6 +17,12 @@
 // tile to one block: it gathers the tile's tokens of all messages into shared memory, adds them
 // in message order 0..W-1 into a shared-memory copy of the tile, and writes the tile once. Each
 // dense entry is therefore written exactly once and summed in a fixed order.
+//
+// Decode-apply (dgc_decode_apply) runs the same passes but never materialises the dense sum:
+// each tile's sum, built from +0 in the same order, updates the weights w <- fma(-lr, sum, w)
+// only where a message landed (elsewhere the update is the identity), so w is read and written
+// at the touched positions instead of streaming a dense array through HBM.
+#include <cmath>
 #include <vector>
 
 #include "dgc_device.cuh"
@@ -187,8 +193,10 @@ struct DecArgs {
     const DecStream* tab;  // W + 1 entries (the last holds the totals)
     int32_t W;
     uint64_t n;
-    float* dense;
+    float* dense;      // the dense sum, or the weights w when apply is set
     int32_t accumulate;
+    int32_t apply;     // w <- fma(neg_lr, sum, w) at every position a message touches
+    float neg_lr;
     int32_t* status;
     DecCtl* ctl;
     uint32_t* bad;
@@ -300,7 +308,8 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
     const uint64_t p0 = t * kDecTile;
     const uint32_t len = (uint32_t)umin64(kDecTile, a.n - p0);
     const bool vec = (len == kDecTile) && ((reinterpret_cast<uintptr_t>(a.dense) & 15u) == 0);
-    if (vec && a.accumulate) {
+    const bool load = a.accumulate && !a.apply;  // apply mode sums from +0
+    if (vec && load) {
         for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
             reinterpret_cast<float4*>(s_acc)[i] = reinterpret_cast<const float4*>(a.dense + p0)[i];
     } else if (vec) {
@@ -308,7 +317,7 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
             reinterpret_cast<float4*>(s_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     } else {
         for (uint32_t i = threadIdx.x; i < kDecTile; i += kThreads)
-            s_acc[i] = (a.accumulate && i < len) ? a.dense[p0 + i] : 0.0f;
+            s_acc[i] = (load && i < len) ? a.dense[p0 + i] : 0.0f;
     }
     for (int wb = 0; wb < a.W; wb += kThreads) {
         const int w = wb + threadIdx.x;
@@ -354,7 +363,15 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
         }
     }
     __syncthreads();
-    if (vec) {
+    if (a.apply) {
+        // a sum that starts at +0 is +0 wherever no message lands (x + y is -0 only for two -0
+        // addends), and fma(neg_lr, +0, w) == w for a finite neg_lr with its sign bit set: those
+        // entries are left alone, the others take the step
+        for (uint32_t i = threadIdx.x; i < len; i += kThreads) {
+            const float t = s_acc[i];
+            if (__float_as_uint(t) != 0u) a.dense[p0 + i] = __fmaf_rn(a.neg_lr, t, a.dense[p0 + i]);
+        }
+    } else if (vec) {
         for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
             reinterpret_cast<float4*>(a.dense + p0)[i] = reinterpret_cast<const float4*>(s_acc)[i];
     } else {
@@ -391,7 +408,10 @@ __global__ void __launch_bounds__(kThreads) k_dec_scatter1(DecArgs a) {
     const uint32_t p = a.pos[d.tok_base + j];
     if (p == kEscPos || p >= a.n) return;
     const float x = reinterpret_cast<const float*>(d.ptr + 32)[j];
-    a.dense[p] = __fadd_rn(a.dense[p], x);
+    if (a.apply)  // the one-message sum at p is +0 + x; then the step
+        a.dense[p] = __fmaf_rn(a.neg_lr, __fadd_rn(0.0f, x), a.dense[p]);
+    else
+        a.dense[p] = __fadd_rn(a.dense[p], x);
 }
 
 struct DecLayout {
@@ -503,10 +523,10 @@ extern "C" int dgc_decode_workspace(int32_t W, const uint64_t* stream_bytes, int
     return DGC_OK;
 }
 
-extern "C" int dgc_decode_accumulate(const uint8_t* const* streams, const uint64_t* stream_bytes,
-                                     int32_t W, float* dense, int64_t n, int32_t accumulate,
-                                     int32_t* status, void* ws, size_t ws_bytes,
-                                     dgc_stream_t stream) {
+namespace {
+int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
+                float* dense, int64_t n, int32_t accumulate, int32_t apply, float lr,
+                int32_t* status, void* ws, size_t ws_bytes, dgc_stream_t stream) {
     if (W < 0 || n < 0) return DGC_EINVAL;
     if (n > 0xFFFFFFFFll) return DGC_EUNSUPPORTED;
     if (W > 0 && (!streams || !stream_bytes)) return DGC_EINVAL;
@@ -528,6 +548,8 @@ extern "C" int dgc_decode_accumulate(const uint8_t* const* streams, const uint64
     a.n = (uint64_t)n;
     a.dense = dense;
     a.accumulate = accumulate ? 1 : 0;
+    a.apply = apply ? 1 : 0;
+    a.neg_lr = -lr;
     a.status = status;
     a.ctl = reinterpret_cast<DecCtl*>(p + L.ctl);
     a.bad = reinterpret_cast<uint32_t*>(p + L.bad);
@@ -553,7 +575,7 @@ extern "C" int dgc_decode_accumulate(const uint8_t* const* streams, const uint64
         ++launches;
     }
     if (W == 1) {  // runs after the positions are checked: a malformed message changes nothing
-        if (!accumulate && n > 0) {
+        if (!accumulate && !apply && n > 0) {
             const int sms = dgc_internal_sm_count();
             if (sms <= 0) return DGC_ECUDA;
             k_dec_zero<<<(unsigned)sms * 8, kThreads, 0, s>>>(a);
@@ -573,4 +595,20 @@ extern "C" int dgc_decode_accumulate(const uint8_t* const* streams, const uint64
         return DGC_ECUDA;
     }
     return DGC_OK;
+}
+}  // namespace
+
+extern "C" int dgc_decode_accumulate(const uint8_t* const* streams, const uint64_t* stream_bytes,
+                                     int32_t W, float* dense, int64_t n, int32_t accumulate,
+                                     int32_t* status, void* ws, size_t ws_bytes,
+                                     dgc_stream_t stream) {
+    return decode_impl(streams, stream_bytes, W, dense, n, accumulate, 0, 0.0f, status, ws,
+                       ws_bytes, stream);
+}
+
+extern "C" int dgc_decode_apply(const uint8_t* const* streams, const uint64_t* stream_bytes,
+                                int32_t W, float* w, int64_t n, float lr, int32_t* status,
+                                void* ws, size_t ws_bytes, dgc_stream_t stream) {
+    if (!std::isfinite(lr) || std::signbit(lr)) return DGC_EINVAL;
+    return decode_impl(streams, stream_bytes, W, w, n, 0, 1, lr, status, ws, ws_bytes, stream);
 }

@@ -926,9 +926,9 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
     __shared__ uint32_t s_thresh[kPStages];
     __shared__ uint32_t s_binA[kPStages], s_nloc[kPStages];      // AdaComp: bins in the tile
     __shared__ uint32_t s_rem[kPStages];  // AdaComp: offset of the tile start in bin s_binA
-    // AdaComp: per local bin, (tile tag << 32) | largest key; a slot whose tag is not the current
-    // tile's counts as 0, so the slots never need clearing
-    __shared__ unsigned long long s_bmax[kSel == 1 ? kPTile : 1];
+    // AdaComp: largest key per local bin, two buffers by tile parity: a tile's buffer is cleared
+    // after the block barrier that ends its use, and the next use is two tiles later
+    __shared__ uint32_t s_bmax[kSel == 1 ? 2 : 1][kSel == 1 ? kPTile : 1];
     __shared__ uint32_t s_rc[2][kPRows * kWarps];  // candidates per (row, warp), by parity
     __shared__ int s_skip;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -977,7 +977,7 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
         }
     }
     if (kSel == 1)
-        for (int b = tid; b < kPTile; b += kThreads) s_bmax[b] = 0;
+        for (int b = tid; b < kPTile; b += kThreads) s_bmax[0][b] = s_bmax[kSel == 1][b] = 0;
     __syncthreads();
     if (s_skip) return;
 
@@ -1007,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
                              s_scale[st], s_thresh[st], uu, vv, flags);
         if constexpr (kSel == 1) {  // bin-local maxima of this tile, then the candidates that reach them
             const uint32_t binA = s_binA[st], L = a.hp.bin;
-            const uint64_t tag = (uint64_t)(it + 1) << 32;  // slots of earlier tiles hold smaller tags
+            uint32_t* bmax = s_bmax[it & 1];
             uint32_t lb[kPRows * 4];
             if (s_uniform[st]) {
                 // one segment: the tile's entry o lies in local bin (rem + o) / L, rem being the
@@ -1030,7 +1030,7 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         if ((uint32_t)e == nxt) {  // a bin starts at this entry
-                            if (mx) atomicMax(&s_bmax[b], tag | mx);
+                            if (mx) atomicMax(&bmax[b], mx);
                             ++b;
                             nxt += L < 4u ? L : 4u;
                             mx = 0;
@@ -1039,16 +1039,23 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
                         const uint32_t key = (o0 + e < len) ? key_of(vr[e]) : 0u;
                         mx = key > mx ? key : mx;
                     }
-                    // the lane's last bin: a max over the run of lanes that share it, kept by
-                    // the run's first lane
+                    // the lane's last bin: one max per run of lanes that share it
+                    if (L >= 128u) {  // at most two bins in the row's 128 entries
+                        const uint32_t b0 = __shfl_sync(kFull, b, 0), b1 = __shfl_sync(kFull, b, 31);
+                        const uint32_t m0 = __reduce_max_sync(kFull, b == b0 ? mx : 0u);
+                        const uint32_t m1 = __reduce_max_sync(kFull, b == b1 ? mx : 0u);
+                        if (lane == 0 && m0) atomicMax(&bmax[b0], m0);
+                        if (lane == 31 && b1 != b0 && m1) atomicMax(&bmax[b1], m1);
+                    } else {  // segmented max by shuffles; the run's first lane keeps it
 #pragma unroll
-                    for (int dl = 1; dl < 32; dl <<= 1) {
-                        const uint32_t om = __shfl_down_sync(kFull, mx, dl);
-                        const uint32_t ob = __shfl_down_sync(kFull, b, dl);
-                        if (lane + dl < 32 && ob == b && om > mx) mx = om;
+                        for (int dl = 1; dl < 32; dl <<= 1) {
+                            const uint32_t om = __shfl_down_sync(kFull, mx, dl);
+                            const uint32_t ob = __shfl_down_sync(kFull, b, dl);
+                            if (lane + dl < 32 && ob == b && om > mx) mx = om;
+                        }
+                        const uint32_t pb = __shfl_up_sync(kFull, b, 1);
+                        if (mx && (lane == 0 || pb != b)) atomicMax(&bmax[b], mx);
                     }
-                    const uint32_t pb = __shfl_up_sync(kFull, b, 1);
-                    if (mx && (lane == 0 || pb != b)) atomicMax(&s_bmax[b], tag | mx);
                 }
             } else {  // a segment boundary inside the tile (rare): every entry on its own
 #pragma unroll
@@ -1062,7 +1069,7 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
                             const SegInfo& d = a.segs[upper_bound_minus1(a.seg_start, a.nseg, i)];
                             b = d.binbase + (i - d.start) / L - binA;
                             const uint32_t key = key_of(reinterpret_cast<const float*>(&vv[r])[e]);
-                            if (key) atomicMax(&s_bmax[b], tag | key);
+                            if (key) atomicMax(&bmax[b], key);
                         }
                         lb[r * 4 + e] = b;
                     }
@@ -1075,15 +1082,10 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
                 for (int e = 0; e < 4; ++e) {
                     if (4u * (r * kThreads + tid) + e >= len) continue;
                     const uint32_t key = key_of(reinterpret_cast<const float*>(&vv[r])[e]);
-                    const unsigned long long m = s_bmax[lb[r * 4 + e]];
-                    if (key > 0 && m == (tag | key)) flags |= 1u << (4 * r + e);
+                    if (key > 0 && key == bmax[lb[r * 4 + e]]) flags |= 1u << (4 * r + e);
                 }
-            // this tile's maxima into the global ones; before the next block barrier, since
-            // the next tile's (larger) tags may overwrite the slots right after it
-            for (uint32_t b = tid; b < nloc; b += kThreads) {
-                const unsigned long long m = s_bmax[b];
-                if ((m & ~0xFFFFFFFFull) == tag) atomicMax(&a.binmax[binA + b], (uint32_t)m);
-            }
+            for (uint32_t b = tid; b < nloc; b += kThreads)  // this tile's maxima into the global ones
+                if (bmax[b]) atomicMax(&a.binmax[binA + b], bmax[b]);
         }
         // candidate words: the 8 lanes of a lane-group cover 32 consecutive entries of a row
         uint32_t word[kPRows];
@@ -1118,6 +1120,8 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
             fence_proxy_async_smem();
             issue(st);  // the next tile for this stage starts loading now
         }
+        if constexpr (kSel == 1)  // every read of this tile's bin maxima is behind the barrier
+            for (uint32_t b = tid; b < nloc; b += kThreads) s_bmax[it & 1][b] = 0;
         // every warp scans the kPRows x kWarps counts itself (row-major = index order)
         const uint32_t cv = (lane < kPRows * kWarps) ? s_rc[it & 1][lane] : 0u;
         const uint32_t cinc = warp_incl_scan(cv);

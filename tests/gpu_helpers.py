@@ -91,3 +91,20 @@ def decode(messages, n: int, dense: torch.Tensor | None = None, accumulate=False
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     dgc.dgc_decode_accumulate(bufs, sizes, dense, n, accumulate, status, ws, ws_bytes=ws_bytes)
     return dgc.dgc_read_status(status), dense
+
+
+def decode_apply(messages, n: int, w: np.ndarray, lr: float):
+    """w <- fma(-lr, ordered sum of the messages, w) on the GPU; returns (status, w on host)."""
+    bufs = []
+    for m in messages:
+        t = torch.zeros(max(len(m), 16) + 16, dtype=torch.uint8, device="cuda")
+        if len(m):
+            t[: len(m)] = torch.frombuffer(bytearray(m), dtype=torch.uint8).cuda()
+        bufs.append(t)
+    sizes = [len(m) for m in messages]
+    ws_bytes = dgc.dgc_decode_workspace(sizes, n)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    wd = dev_f32(w) if n else torch.zeros(1, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dgc.dgc_decode_apply(bufs, sizes, wd, n, lr, status, ws, ws_bytes=ws_bytes)
+    return dgc.dgc_read_status(status), host_f32(wd)[:n]

@@ -5,6 +5,7 @@ Every rejected call below breaks at least one host-side rule, so nothing reaches
 where a GPU is present.
 """
 import ctypes
+import math
 import os
 import re
 
@@ -134,3 +135,18 @@ def test_encode_and_decode_reject_on_host(L):
     ptrs_mis = (ctypes.c_void_p * 1)(FAKE + 4)
     assert d(cast(ptrs_mis), cast(good), 1, FAKE, 100, 0, FAKE, FAKE, wsb, None) == dgc.EINVAL
     assert d(cast(ptrs), cast(good), -1, FAKE, 100, 0, FAKE, FAKE, wsb, None) == dgc.EINVAL
+
+
+def test_decode_apply_rejects_on_host(L):
+    d = L.dgc_decode_apply
+    ptrs = (ctypes.c_void_p * 1)(FAKE)
+    good = (ctypes.c_uint64 * 1)(40)
+    bad = (ctypes.c_uint64 * 1)(37)
+    cast = lambda a: ctypes.cast(a, ctypes.c_void_p)  # noqa: E731
+    wsb = dgc.dgc_decode_workspace([40], 100)
+    for lr in (-0.0, -1.0, math.inf, -math.inf, math.nan):  # lr must be finite, sign bit clear
+        assert d(cast(ptrs), cast(good), 1, FAKE, 100, lr, FAKE, FAKE, wsb, None) == dgc.EINVAL
+    assert d(cast(ptrs), cast(bad), 1, FAKE, 100, 0.5, FAKE, FAKE, wsb, None) == dgc.ECORRUPT
+    assert d(cast(ptrs), cast(good), 1, FAKE, 100, 0.5, FAKE, FAKE, wsb - 1, None) == dgc.EINVAL
+    assert d(cast(ptrs), cast(good), 1, None, 100, 0.5, FAKE, FAKE, wsb, None) == dgc.EINVAL
+    assert d(cast(ptrs), cast(good), 1, FAKE, 2**32, 0.5, FAKE, FAKE, wsb, None) == dgc.EUNSUPPORTED

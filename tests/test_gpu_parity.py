@@ -14,7 +14,7 @@ import oracle
 import sparsified_gradient_compression_gb300 as dgc
 import workloads
 from conftest import read_golden
-from gpu_helpers import Compressor, Encoder, decode, dev_f32, host_f32
+from gpu_helpers import Compressor, Encoder, decode, decode_apply, dev_f32, host_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -163,6 +163,12 @@ def test_aggregation_64_learners():
         orc_rc, odense = oracle.decode_accumulate(msgs_orc, n)
         assert rc == 0 and orc_rc == 0
         assert same_bits(host_f32(dense), odense)
+        # the same messages as one SGD step on weights (1/W folded into lr)
+        w0 = np.random.Generator(np.random.PCG64([6, step])).standard_normal(n).astype(np.float32)
+        rc, w_gpu = decode_apply(msgs_gpu, n, w0, 0.1 / W)
+        orc_rc, w_orc = oracle.decode_apply(msgs_orc, n, w0, np.float32(0.1 / W))
+        assert rc == 0 and orc_rc == 0
+        assert same_bits(w_gpu, w_orc)
 
 
 @pytest.mark.slow
@@ -535,3 +541,85 @@ def test_launch_counter_counts_kernels():
     before = dgc.dgc_launch_count()
     run_steps(lambda t: workloads.misc([t], 10_000, 1.0), np.array([0, 10_000]), 1)
     assert dgc.dgc_launch_count() > before
+
+
+# --------------------------------------------------------------- decode -> plain SGD step
+def _weights(rng, n):
+    w = (rng.standard_normal(n) * 10.0 ** rng.integers(-3, 3, n)).astype(np.float32)
+    w[rng.random(n) < 0.05] = np.float32(-0.0)
+    return w
+
+
+@pytest.mark.parametrize("name", ["codec_gaps.txt", "codec_single.txt", "codec_odd.txt",
+                                  "codec_empty.txt", "decode_order.txt"])
+def test_decode_apply_goldens(name):
+    if name == "decode_order.txt":
+        rows = read_golden(name)
+        n = rows[0][1][0]
+        msgs = [oracle.encode(np.array([v[0]], np.uint32),
+                              np.array([v[1]], np.uint32).view(np.float32), n)
+                for t, v in rows if t == "learner"]
+    else:
+        from test_oracle_pins import golden_message
+        n, _, _, msg, _ = golden_message(name)
+        msgs = [msg]
+    w = _weights(np.random.default_rng(3), n)
+    rc, got = decode_apply(msgs, n, w, 0.75)
+    orc_rc, exp = oracle.decode_apply(msgs, n, w, 0.75)
+    assert rc == 0 and orc_rc == 0
+    assert same_bits(got, exp)
+
+
+def test_decode_apply_single_message():
+    # one message: no dense sum at all, one fma per received value
+    rng = np.random.default_rng(78)
+    n = 3_000_001
+    idx = np.sort(rng.choice(n, size=5000, replace=False)).astype(np.uint32)
+    idx[-1] = n - 1
+    val = rng.standard_normal(5000).astype(np.float32)
+    val[::7] = np.float32(-0.0)
+    msg = oracle.encode(idx, val, n)
+    w = _weights(rng, n)
+    for lr in (0.37, 0.0, 1.0):
+        rc, got = decode_apply([msg], n, w, lr)
+        orc_rc, exp = oracle.decode_apply([msg], n, w, np.float32(lr))
+        assert rc == 0 and orc_rc == 0
+        assert same_bits(got, exp), lr
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_decode_apply_many_learners(seed):
+    rng = np.random.default_rng(300 + seed)
+    n = int(rng.integers(1, 3_000_000))
+    W = int(rng.integers(2, 200))
+    msgs = []
+    for _ in range(W):
+        k = int(rng.integers(0, min(n, 20_000) + 1))
+        idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+        val = (rng.standard_normal(k) * 10.0 ** rng.integers(-3, 3, k)).astype(np.float32)
+        val[rng.random(k) < 0.02] = np.float32(-0.0)
+        msgs.append(oracle.encode(idx, val, n))
+    w = _weights(rng, n)
+    lr = float(np.float32(rng.choice([0.01, 0.37, 2.0])))
+    rc, got = decode_apply(msgs, n, w, lr)
+    orc_rc, exp = oracle.decode_apply(msgs, n, w, lr)
+    assert rc == 0 and orc_rc == 0
+    assert same_bits(got, exp)
+
+
+def test_decode_apply_malformed_and_empty():
+    import struct
+
+    n = 1000
+    good = oracle.encode(np.array([5, 999], np.uint32), np.array([1.0, 2.0], np.float32), n)
+    bad = good[:32 + 8] + struct.pack("<H", 999) + good[32 + 10:]  # second position past n
+    w = np.full(n, 7.0, np.float32)
+    for msgs in ([bad], [good, bad], [bad, good]):
+        rc, got = decode_apply(msgs, n, w, 0.5)
+        assert rc == dgc.ECORRUPT
+        assert np.all(got == 7.0)
+    rc, got = decode_apply([], n, w, 0.5)  # no learners: the step is the identity
+    assert rc == 0 and same_bits(got, w)
+    with pytest.raises(dgc.DGCError) as e:
+        decode_apply([good], n, w, -0.0)
+    assert e.value.code == dgc.EINVAL
