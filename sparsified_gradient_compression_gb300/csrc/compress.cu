@@ -55,6 +55,9 @@ constexpr int kPRows = kPTile / (4 * kThreads);   // float4 rows per thread
 constexpr int kWarps = kThreads / 32;
 static_assert(kPRows >= 1 && kPRows * 4 * kThreads == kPTile, "tile = rows x 1024 entries");
 static_assert(kPRows * kWarps <= 32, "one warp scans the per-(row, warp) counts");
+// the AdaComp pass finds bins with (x + 0.5) * fl(1/L) for x < 2 * kPTile, L < kPTile: checked
+// exhaustively against integer division for tiles of 2048 and 4096
+static_assert(kPTile <= 4096, "bin index by reciprocal is only checked up to 4096-entry tiles");
 constexpr uint32_t kPStageFloats = 3u * kPTile;   // g, u, v
 constexpr size_t kPSmemBytes = sizeof(float) * kPStageFloats * kPStages;  // 96 KiB
 constexpr uint32_t kMbarSpinLimit = 1u << 22;
@@ -132,6 +135,7 @@ struct HostParams {
     uint64_t d_ppb, r_ppb, q_ppb;
     float momentum, clip_norm;
     uint64_t seed;
+    float bin_inv;  // AdaComp: 1/bin rounded to binary32 (used while bin < the tile length)
 };
 
 int check_params(const dgc_params* p, HostParams* hp) {
@@ -141,6 +145,7 @@ int check_params(const dgc_params* p, HostParams* hp) {
         return DGC_EINVAL;
     if (p->mode == DGC_SELECT_ADACOMP && p->bin_size == 0) return DGC_EINVAL;
     hp->bin = p->mode == DGC_SELECT_ADACOMP ? p->bin_size : 0;
+    hp->bin_inv = hp->bin ? 1.0f / (float)hp->bin : 0.0f;
     if (!(p->sparsity >= 0.0 && p->sparsity <= 1.0)) return DGC_EINVAL;
     if (!std::isfinite(p->momentum)) return DGC_EINVAL;
     if (std::isnan(p->clip_norm)) return DGC_EINVAL;
@@ -1006,39 +1011,43 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
         stream_compute<true>(a, s_stage + (size_t)st * kPStageFloats, base, len, s_uniform[st],
                              s_scale[st], s_thresh[st], uu, vv, flags);
         if constexpr (kSel == 1) {  // bin-local maxima of this tile, then the candidates that reach them
+            // entries past len hold v = 0 (key 0): they raise no maximum and are never candidates
             const uint32_t binA = s_binA[st], L = a.hp.bin;
             uint32_t* bmax = s_bmax[it & 1];
-            uint32_t lb[kPRows * 4];
-            if (s_uniform[st]) {
-                // one segment: the tile's entry o lies in local bin (rem + o) / L, rem being the
-                // tile start's offset within bin binA; bins rise with o, so a warp row holds
-                // contiguous runs of equal bins
+            const bool fast = s_uniform[st] && L >= 4u;
+            uint32_t qr[kPRows], dr[kPRows];  // fast path: a lane's first local bin, and the
+                                              // entries before the next one (>= 4: none)
+            uint32_t lb[kPRows * 4];          // other tiles: every entry's local bin
+            if (fast) {
+                // one segment: tile entry o lies in local bin (rem + o) / L, rem being the tile
+                // start's offset within bin binA. A lane's 4 entries span at most two bins, and
+                // bins rise with o, so a warp row holds contiguous runs of equal bins.
                 const uint32_t rem = s_rem[st];
 #pragma unroll
                 for (int r = 0; r < kPRows; ++r) {
                     const uint32_t o0 = 4u * (r * kThreads + tid);
-                    uint32_t q, d0;  // local bin of entry o0, and entries from o0 to the next bin
+                    uint32_t q, d0;
                     if (L >= (uint32_t)kPTile) {
                         q = (o0 >= L - rem) ? 1u : 0u;
                         d0 = q ? L - (o0 - (L - rem)) : L - rem - o0;
-                    } else {
-                        q = (rem + o0) / L;
-                        d0 = L - (rem + o0 - q * L);
+                    } else {  // (x + 0.5) * fl(1/L) rounds down to x / L here (x < 2 kPTile)
+                        const uint32_t x = rem + o0;
+                        q = __float2uint_rd(__fmul_rn(__fadd_rn((float)x, 0.5f), a.hp.bin_inv));
+                        d0 = L - (x - q * L);
                     }
+                    qr[r] = q;
+                    dr[r] = d0;
                     const float* vr = reinterpret_cast<const float*>(&vv[r]);
-                    uint32_t b = q, nxt = d0, mx = 0;
+                    uint32_t mlo = 0, mhi = 0;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        if ((uint32_t)e == nxt) {  // a bin starts at this entry
-                            if (mx) atomicMax(&bmax[b], mx);
-                            ++b;
-                            nxt += L < 4u ? L : 4u;
-                            mx = 0;
-                        }
-                        lb[r * 4 + e] = b;
-                        const uint32_t key = (o0 + e < len) ? key_of(vr[e]) : 0u;
-                        mx = key > mx ? key : mx;
+                        const uint32_t key = key_of(vr[e]);
+                        if ((uint32_t)e < d0) mlo = max(mlo, key); else mhi = max(mhi, key);
                     }
+                    const bool split = d0 < 4u;  // the first bin ends inside this lane
+                    if (split && mlo) atomicMax(&bmax[q], mlo);
+                    const uint32_t b = q + (split ? 1u : 0u);
+                    uint32_t mx = split ? mhi : mlo;
                     // the lane's last bin: one max per run of lanes that share it
                     if (L >= 128u) {  // at most two bins in the row's 128 entries
                         const uint32_t b0 = __shfl_sync(kFull, b, 0), b1 = __shfl_sync(kFull, b, 31);
@@ -1057,7 +1066,7 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
                         if (mx && (lane == 0 || pb != b)) atomicMax(&bmax[b], mx);
                     }
                 }
-            } else {  // a segment boundary inside the tile (rare): every entry on its own
+            } else {  // a segment boundary inside the tile, or bins under 4 entries: per entry
 #pragma unroll
                 for (int r = 0; r < kPRows; ++r)
 #pragma unroll
@@ -1076,14 +1085,27 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
             }
             __syncthreads();
             flags = 0;
+            if (fast) {
 #pragma unroll
-            for (int r = 0; r < kPRows; ++r)
+                for (int r = 0; r < kPRows; ++r) {
+                    const float* vr = reinterpret_cast<const float*>(&vv[r]);
+                    const uint32_t d0 = dr[r], lo = bmax[qr[r]];
+                    const uint32_t hi = (d0 < 4u) ? bmax[qr[r] + 1] : 0u;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if (4u * (r * kThreads + tid) + e >= len) continue;
-                    const uint32_t key = key_of(reinterpret_cast<const float*>(&vv[r])[e]);
-                    if (key > 0 && key == bmax[lb[r * 4 + e]]) flags |= 1u << (4 * r + e);
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t key = key_of(vr[e]);
+                        if (key > 0 && key == ((uint32_t)e < d0 ? lo : hi)) flags |= 1u << (4 * r + e);
+                    }
                 }
+            } else {
+#pragma unroll
+                for (int r = 0; r < kPRows; ++r)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t key = key_of(reinterpret_cast<const float*>(&vv[r])[e]);
+                        if (key > 0 && key == bmax[lb[r * 4 + e]]) flags |= 1u << (4 * r + e);
+                    }
+            }
             for (uint32_t b = tid; b < nloc; b += kThreads)  // this tile's maxima into the global ones
                 if (bmax[b]) atomicMax(&a.binmax[binA + b], bmax[b]);
         }

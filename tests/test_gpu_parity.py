@@ -262,6 +262,16 @@ def test_adacomp_edges(case):
               clip_norm=float(rng.choice([0.0, 1.0])))
 
 
+@pytest.mark.parametrize("L", [1, 2, 3, 4, 5, 7, 127, 128, 129, 1000, 2047, 2048, 2049, 4096])
+def test_adacomp_bin_sizes_one_segment(L):
+    # one segment, so every tile but the ragged last one takes the per-lane bin arithmetic; the
+    # sizes straddle its branches (under 4, under 128, under the 2048-entry tile)
+    n = 3 * 2048 * 5 + 1234
+    off = np.array([0, n])
+    run_steps(lambda t: (np.random.default_rng([L, t]).standard_normal(n) * 0.01)
+              .astype(np.float32), off, 2, mode=dgc.SELECT_ADACOMP, bin_size=L, momentum=0.9)
+
+
 @pytest.mark.slow
 def test_adacomp_resnet50_layout():
     off = workloads.resnet50_segments()
