@@ -23,7 +23,7 @@ _lib = None
 
 EXACT, SAMPLED, ADACOMP = 0, 1, 2
 MASK_MOMENTUM = 1
-OK, EINVAL, ECAPACITY, ECORRUPT, ENOMEM = 0, -1, -2, -5, -7
+OK, EINVAL, ECAPACITY, ECORRUPT, EUNSUPPORTED, ENOMEM = 0, -1, -2, -5, -6, -7
 
 
 class Params(ctypes.Structure):
@@ -106,6 +106,14 @@ def lib():
         L.orc_decode_accumulate.argtypes = [vp, vp, i32, vp, i64, ctypes.c_int]
         L.orc_decode_apply.restype = ctypes.c_int
         L.orc_decode_apply.argtypes = [vp, vp, i32, vp, i64, ctypes.c_float]
+        f32 = ctypes.c_float
+        L.orc_encode_quant.restype = ctypes.c_int
+        L.orc_encode_quant.argtypes = [vp, vp, i64, i64, f32, ctypes.c_int, vp, vp,
+                                       ctypes.c_uint64, vp]
+        L.orc_decode_accumulate_quant.restype = ctypes.c_int
+        L.orc_decode_accumulate_quant.argtypes = [vp, vp, i32, f32, vp, i64, ctypes.c_int]
+        L.orc_decode_apply_quant.restype = ctypes.c_int
+        L.orc_decode_apply_quant.argtypes = [vp, vp, i32, f32, vp, i64, f32]
         _lib = L
     return _lib
 
@@ -245,4 +253,48 @@ def decode_apply(streams, n: int, w, lr: float):
     rc = lib().orc_decode_apply(ctypes.cast(ptrs, ctypes.c_void_p),
                                 ctypes.cast(sizes, ctypes.c_void_p), W,
                                 _ptr(w) if n else None, int(n), float(lr))
+    return rc, w
+
+
+def encode_quant(idx, val, n: int, alpha: float, bits: int, v=None):
+    """Integer-valued message (version 2). Returns (rc, message bytes, residual v after the
+    quantizer put each sent entry's remainder back), v being a copy of the given array."""
+    idx = np.ascontiguousarray(idx, dtype=np.uint32)
+    val = np.ascontiguousarray(val, dtype=np.float32)
+    vv = None if v is None else np.ascontiguousarray(v, dtype=np.float32).copy()
+    cap = 40 + 6 * (idx.size + int(n) // 65535 + 1)
+    out = np.zeros(cap, np.uint8)
+    nb = ctypes.c_uint64(0)
+    rc = lib().orc_encode_quant(_ptr(idx), _ptr(val), idx.size, int(n), float(alpha), int(bits),
+                                None if vv is None else _ptr(vv), _ptr(out), out.size,
+                                ctypes.byref(nb))
+    return rc, (out[: nb.value].tobytes() if rc == OK else b""), vv
+
+
+def _streams(streams):
+    bufs = [np.frombuffer(s, dtype=np.uint8) if len(s) else np.zeros(1, np.uint8)
+            for s in streams]
+    W = len(bufs)
+    ptrs = (ctypes.c_void_p * max(W, 1))(*[b.ctypes.data for b in bufs])
+    sizes = (ctypes.c_uint64 * max(W, 1))(*[len(s) for s in streams])
+    return bufs, W, ctypes.cast(ptrs, ctypes.c_void_p), ctypes.cast(sizes, ctypes.c_void_p)
+
+
+def decode_accumulate_quant(streams, n: int, alpha: float, dense=None, accumulate=False):
+    """Sum version-2 messages exactly in integers, divide by alpha once. Returns (rc, dense)."""
+    bufs, W, ptrs, sizes = _streams(streams)
+    dense = (np.zeros(n, np.float32) if dense is None
+             else np.ascontiguousarray(dense, dtype=np.float32).copy())
+    rc = lib().orc_decode_accumulate_quant(ptrs, sizes, W, float(alpha),
+                                           _ptr(dense) if n else None, int(n),
+                                           int(bool(accumulate)))
+    return rc, dense
+
+
+def decode_apply_quant(streams, n: int, alpha: float, w, lr: float):
+    """w <- fmaf(-lr, (float)S / alpha, w) for version-2 messages. Returns (rc, w)."""
+    bufs, W, ptrs, sizes = _streams(streams)
+    w = np.ascontiguousarray(w, dtype=np.float32).copy()
+    rc = lib().orc_decode_apply_quant(ptrs, sizes, W, float(alpha), _ptr(w) if n else None,
+                                      int(n), float(lr))
     return rc, w

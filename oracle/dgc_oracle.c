@@ -451,3 +451,175 @@ int orc_decode_apply(const uint8_t* const* streams, const uint64_t* stream_bytes
     free(s);
     return rc;
 }
+
+/* ---- integer values: [ADA] abstract (AdaComp sends the selected residues both sparse and
+ * quantized); the IntSGD page, abstract (each learner multiplies its vector by a number every
+ * learner knows and rounds to integers, so no float is sent). Reading of the quantizer (the pages
+ * give no bit format):
+ *   q_j = clamp(rint(alpha * val_j), -Q, Q), Q = 2^(b-1) - 1, b in {8, 16}; the product is one
+ *         binary32 multiply, rint rounds half to even, NaN gives 0;
+ *   deq(q) = (float)q / alpha (one binary32 divide); the residual keeps what the integer did
+ *         not carry: v[idx_j] <- val_j - deq(q_j) (one binary32 subtract; [DGC] Proposed method,
+ *         bullet 1: what is not sent stays in the local accumulator).
+ * Message, version 2: header "DGC1", u16 version 2, u16 b, u64 n, u64 T, binary32 alpha, u32
+ * nnz; then T two's-complement integers of b bits (escape tokens carry 0), zero bytes up to an
+ * even offset, T u16 runs, zero bytes up to a multiple of 4. Receivers sum the integers exactly
+ * (order does not matter) and divide once: dense_i = (float)S_i / alpha. ---- */
+static int32_t orc_quantize(float val, float alpha, int bits) {
+    const float x = rintf(alpha * val);
+    const float Q = (float)((1 << (bits - 1)) - 1);
+    if (isnan(x)) return 0;
+    if (x > Q) return (int32_t)Q;
+    if (x < -Q) return -(int32_t)Q;
+    return (int32_t)x;
+}
+
+static uint64_t orc_runs_offset(uint64_t T, int bits) {
+    const uint64_t at = 32 + T * (uint64_t)(bits / 8);
+    return at + (at & 1); /* runs start at an even offset */
+}
+
+static uint64_t orc_size_quant(uint64_t T, int bits) {
+    const uint64_t at = orc_runs_offset(T, bits) + 2 * T;
+    return at + ((4 - (at & 3)) & 3); /* whole message a multiple of 4 */
+}
+
+int orc_encode_quant(const uint32_t* idx, const float* val, int64_t count, int64_t n, float alpha,
+                     int bits, float* v, uint8_t* out, uint64_t out_cap, uint64_t* out_bytes) {
+    if (count < 0 || n < 0 || (bits != 8 && bits != 16) || !isfinite(alpha) || !(alpha > 0.0f))
+        return ORC_EINVAL;
+    int64_t prev = -1;
+    for (int64_t j = 0; j < count; ++j) {
+        if ((int64_t)idx[j] <= prev || (int64_t)idx[j] >= n) return ORC_EINVAL;
+        prev = idx[j];
+    }
+    const uint64_t T = orc_tokens(idx, count);
+    const uint64_t size = orc_size_quant(T, bits);
+    *out_bytes = size;
+    if (size > out_cap) return ORC_ECAPACITY;
+    memset(out, 0, (size_t)size);
+    orc_put32(out, ORC_MAGIC);
+    orc_put16(out + 4, 2);
+    orc_put16(out + 6, (uint16_t)bits);
+    orc_put64(out + 8, (uint64_t)n);
+    orc_put64(out + 16, T);
+    uint32_t abits;
+    memcpy(&abits, &alpha, 4);
+    orc_put32(out + 24, abits);
+    orc_put32(out + 28, (uint32_t)count);
+    const int vb = bits / 8;
+    uint8_t* vals = out + 32;
+    uint8_t* runs = out + orc_runs_offset(T, bits);
+    uint64_t tok = 0;
+    prev = -1;
+    for (int64_t j = 0; j < count; ++j) {
+        uint64_t r = (uint64_t)((int64_t)idx[j] - prev - 1);
+        while (r >= ORC_RUN_ESCAPE) { /* value bytes stay 0 */
+            orc_put16(runs + 2 * tok, ORC_RUN_ESCAPE);
+            ++tok;
+            r -= ORC_RUN_ESCAPE;
+        }
+        const int32_t q = orc_quantize(val[j], alpha, bits);
+        if (vb == 1)
+            vals[tok] = (uint8_t)(q & 0xFF);
+        else
+            orc_put16(vals + 2 * tok, (uint16_t)(q & 0xFFFF));
+        orc_put16(runs + 2 * tok, (uint16_t)r);
+        ++tok;
+        if (v) v[idx[j]] = val[j] - (float)q / alpha;
+        prev = idx[j];
+    }
+    return ORC_OK;
+}
+
+/* The integer sums of W version-2 messages: S (int64) and which positions a value token reached.
+ * Every message must carry the caller's alpha (bitwise) and a width of 8 or 16 bits. */
+static int orc_sum_quant(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
+                         int64_t n, float alpha, int64_t* S, uint8_t* touched) {
+    uint32_t abits;
+    memcpy(&abits, &alpha, 4);
+    for (int32_t w = 0; w < W; ++w) {
+        const uint8_t* s = streams[w];
+        const uint64_t bytes = stream_bytes[w];
+        if (bytes < 32) return ORC_ECORRUPT;
+        const int bits = orc_get16(s + 6);
+        if (orc_get32(s) != ORC_MAGIC || orc_get16(s + 4) != 2 || (bits != 8 && bits != 16) ||
+            orc_get64(s + 8) != (uint64_t)n || orc_get32(s + 24) != abits)
+            return ORC_ECORRUPT;
+        const uint64_t T = orc_get64(s + 16);
+        if (T > bytes || orc_size_quant(T, bits) != bytes) return ORC_ECORRUPT;
+        const uint8_t* runs = s + orc_runs_offset(T, bits);
+        int64_t pos = -1;
+        for (uint64_t t = 0; t < T; ++t) {
+            const uint16_t r = orc_get16(runs + 2 * t);
+            pos += (r == ORC_RUN_ESCAPE) ? (int64_t)ORC_RUN_ESCAPE : (int64_t)r + 1;
+            if (pos >= n) return ORC_ECORRUPT;
+        }
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        S[i] = 0;
+        touched[i] = 0;
+    }
+    for (int32_t w = 0; w < W; ++w) {
+        const uint8_t* s = streams[w];
+        const int bits = orc_get16(s + 6);
+        const uint64_t T = orc_get64(s + 16);
+        const uint8_t* runs = s + orc_runs_offset(T, bits);
+        int64_t pos = -1;
+        for (uint64_t t = 0; t < T; ++t) {
+            const uint16_t r = orc_get16(runs + 2 * t);
+            if (r == ORC_RUN_ESCAPE) {
+                pos += ORC_RUN_ESCAPE;
+                continue;
+            }
+            pos += (int64_t)r + 1;
+            const int32_t q = (bits == 8) ? (int32_t)(int8_t)s[32 + t]
+                                          : (int32_t)(int16_t)orc_get16(s + 32 + 2 * t);
+            S[pos] += q;
+            touched[pos] = 1;
+        }
+    }
+    return ORC_OK;
+}
+
+/* Decode and sum version-2 messages: dense_i = (float)S_i / alpha at every position some message
+ * reaches, added onto dense_i when accumulate is set (one binary32 addition); +0 elsewhere
+ * unless accumulating. W is at most 65536, so |S_i| < 2^31. */
+int orc_decode_accumulate_quant(const uint8_t* const* streams, const uint64_t* stream_bytes,
+                                int32_t W, float alpha, float* dense, int64_t n, int accumulate) {
+    if (W < 0 || n < 0 || !isfinite(alpha) || !(alpha > 0.0f)) return ORC_EINVAL;
+    if (W > 65536) return ORC_EUNSUPPORTED;
+    int64_t* S = (int64_t*)malloc((n > 0 ? (size_t)n : 1) * sizeof(int64_t));
+    uint8_t* touched = (uint8_t*)malloc(n > 0 ? (size_t)n : 1);
+    if (!S || !touched) {
+        free(S);
+        free(touched);
+        return ORC_ENOMEM;
+    }
+    const int rc = orc_sum_quant(streams, stream_bytes, W, n, alpha, S, touched);
+    if (rc == ORC_OK)
+        for (int64_t i = 0; i < n; ++i) {
+            const float x = (float)S[i] / alpha;
+            if (!accumulate)
+                dense[i] = x;
+            else if (touched[i])
+                dense[i] = dense[i] + x;
+        }
+    free(S);
+    free(touched);
+    return rc;
+}
+
+/* The SGD step of orc_decode_apply with version-2 messages: w_i <- fmaf(-lr, (float)S_i / alpha,
+ * w_i); lr as there. */
+int orc_decode_apply_quant(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
+                           float alpha, float* w, int64_t n, float lr) {
+    if (!isfinite(lr) || signbit(lr)) return ORC_EINVAL;
+    float* s = (float*)malloc((n > 0 ? (size_t)n : 1) * sizeof(float));
+    if (!s) return ORC_ENOMEM;
+    const int rc = orc_decode_accumulate_quant(streams, stream_bytes, W, alpha, s, n, 0);
+    if (rc == ORC_OK)
+        for (int64_t i = 0; i < n; ++i) w[i] = fmaf(-lr, s[i], w[i]);
+    free(s);
+    return rc;
+}

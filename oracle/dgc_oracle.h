@@ -20,7 +20,8 @@
 extern "C" {
 #endif
 
-enum { ORC_OK = 0, ORC_EINVAL = -1, ORC_ECAPACITY = -2, ORC_ECORRUPT = -5, ORC_ENOMEM = -7 };
+enum { ORC_OK = 0, ORC_EINVAL = -1, ORC_ECAPACITY = -2, ORC_ECORRUPT = -5, ORC_EUNSUPPORTED = -6,
+       ORC_ENOMEM = -7 };
 enum { ORC_EXACT = 0, ORC_SAMPLED = 1, ORC_ADACOMP = 2 };
 enum { ORC_MASK_MOMENTUM = 1u };
 
@@ -70,6 +71,14 @@ int orc_decode_accumulate(const uint8_t* const* streams, const uint64_t* stream_
                           int32_t W, float* dense, int64_t n, int accumulate);
 int orc_decode_apply(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
                      float* w, int64_t n, float lr);
+
+/* integer-valued messages (version 2) */
+int orc_encode_quant(const uint32_t* idx, const float* val, int64_t count, int64_t n, float alpha,
+                     int bits, float* v, uint8_t* out, uint64_t out_cap, uint64_t* out_bytes);
+int orc_decode_accumulate_quant(const uint8_t* const* streams, const uint64_t* stream_bytes,
+                                int32_t W, float alpha, float* dense, int64_t n, int accumulate);
+int orc_decode_apply_quant(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
+                           float alpha, float* w, int64_t n, float lr);
 
 #ifdef __cplusplus
 }

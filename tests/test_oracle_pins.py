@@ -705,3 +705,153 @@ def test_decode_apply_rejects(orc):
         assert rc == orc.EINVAL and np.all(out == 2.0)
     rc, out = orc.decode_apply([msg, b"XGC1" + msg[4:]], n, w, 1.0)
     assert rc == orc.ECORRUPT and np.all(out == 2.0)
+
+
+# --------------------------------------------------------------- integer-valued messages
+# Reading of "AdaComp ..." (abstract: sparse and quantized residues) and of the IntSGD page
+# (abstract: scale by a shared number, round to integers): see tests/golden/codec_quant8.txt.
+def golden_quant(name):
+    rows = read_golden(name)
+    kv = {t: v for t, v in rows if t in ("n", "alpha", "bits", "size")}
+    n, bits, size = kv["n"][0], kv["bits"][0], kv["size"][0]
+    alpha = X.from_bits(kv["alpha"][0])
+    ent = [v for t, v in rows if t == "entry"]
+    tok = [v for t, v in rows if t == "token"]
+    T = len(tok)
+    msg = struct.pack("<4sHHQQII", b"DGC1", 2, bits, n, T, kv["alpha"][0], len(ent))
+    fmt = "<b" if bits == 8 else "<h"
+    msg += b"".join(struct.pack(fmt, t[1]) for t in tok)
+    msg += b"\0" * (len(msg) % 2)
+    msg += b"".join(struct.pack("<H", t[0]) for t in tok)
+    msg += b"\0" * ((-len(msg)) % 4)
+    return n, bits, alpha, ent, msg, size
+
+
+@pytest.mark.parametrize("name", ["codec_quant8.txt", "codec_quant16.txt"])
+def test_quant_golden(orc, name):
+    n, bits, alpha, ent, msg, size = golden_quant(name)
+    assert len(msg) == size
+    idx = np.array([e[0] for e in ent], np.uint32)
+    val = np.array([e[1] for e in ent], np.uint32).view(np.float32)
+    v = np.full(n, 9.0, np.float32)
+    rc, out, v2 = orc.encode_quant(idx, val, n, alpha, bits, v)
+    assert rc == 0 and out == msg
+    assert [X.bits(v2[e[0]]) for e in ent] == [e[3] for e in ent]
+    rest = np.setdiff1d(np.arange(n), idx)
+    assert np.all(v2[rest] == 9.0)  # only sent entries take their remainder back
+    rc, dense = orc.decode_accumulate_quant([msg], n, alpha)
+    assert rc == 0
+    exp = np.zeros(n, np.float32)
+    exp[idx] = np.array([e[4] for e in ent], np.uint32).view(np.float32)
+    assert dense.view(np.uint32).tolist() == exp.view(np.uint32).tolist()
+
+
+def _quant_expected(val, alpha, bits):
+    """q and residual from the definition, in exact rational arithmetic."""
+    Q = 2 ** (bits - 1) - 1
+    p = X.mul_f32(alpha, val)
+    if math.isnan(float(p)):
+        q = 0
+    else:
+        q = int(np.rint(np.float64(p)))  # p is a binary32 value: rint in binary64 is exact
+        q = max(-Q, min(Q, q))
+    deq = X.round_f32(Fraction(q) / Fraction(float(alpha))) if q else np.float32(0.0)
+    return q, X.add_f32(val, -deq)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_quant_random_against_definition(orc, seed):
+    rng = np.random.default_rng(1200 + seed)
+    n = int(rng.integers(1, 200_000))
+    k = int(rng.integers(0, min(n, 400) + 1))
+    bits = 8 if seed % 2 else 16
+    alpha = np.float32(rng.choice([1.0, 3.0, 1000.0, 0.37, 2.0 ** 20]))
+    idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+    val = (rng.standard_normal(k) * 10.0 ** rng.integers(-6, 3, k)).astype(np.float32)
+    val[rng.random(k) < 0.05] = np.float32(-0.0)
+    rc, msg, v = orc.encode_quant(idx, val, n, alpha, bits, np.zeros(n, np.float32))
+    assert rc == 0
+    Q = 2 ** (bits - 1) - 1
+    qs = []
+    for j, x in enumerate(val):
+        q, r = _quant_expected(x, alpha, bits)
+        qs.append(q)
+        assert X.bits(v[idx[j]]) == X.bits(r)
+        if abs(q) < Q:  # not clamped: the remainder is exact, q/alpha + r == v
+            deq = Fraction(float(X.round_f32(Fraction(q) / Fraction(float(alpha))))) if q else 0
+            assert deq + Fraction(float(r)) == Fraction(float(x))
+    # the message's integers, read back by walking the layout
+    T = struct.unpack_from("<Q", msg, 16)[0]
+    vals = struct.unpack_from(f"<{T}{'b' if bits == 8 else 'h'}", msg, 32)
+    at = 32 + T * bits // 8
+    at += at % 2
+    runs = struct.unpack_from(f"<{T}H", msg, at)
+    got = [q for q, r in zip(vals, runs) if r != 0xFFFF]
+    assert got == qs
+
+
+def test_quant_nan_and_infinities(orc):
+    n = 10
+    idx = np.array([1, 2, 3], np.uint32)
+    val = np.array([np.nan, np.inf, -np.inf], np.float32)
+    rc, msg, v = orc.encode_quant(idx, val, n, 2.0, 8, np.zeros(n, np.float32))
+    assert rc == 0
+    assert struct.unpack_from("<3b", msg, 32) == (0, 127, -127)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_quant_decode_sums_integers_in_any_order(orc, seed):
+    rng = np.random.default_rng(1300 + seed)
+    n, W, bits = 5000, int(rng.integers(2, 700)), 16
+    alpha = np.float32(rng.choice([0.5, 3.0, 1000.0]))
+    msgs, S, touched = [], {}, set()
+    for _ in range(W):
+        k = int(rng.integers(0, 50))
+        idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+        val = (rng.choice([-1, 1], k) * rng.integers(0, 40000, k) / float(alpha)).astype(np.float32)
+        rc, m, _ = orc.encode_quant(idx, val, n, alpha, bits)
+        assert rc == 0
+        msgs.append(m)
+        for j, x in enumerate(val):
+            q, _ = _quant_expected(x, alpha, bits)
+            S[int(idx[j])] = S.get(int(idx[j]), 0) + q
+            touched.add(int(idx[j]))
+    base = rng.standard_normal(n).astype(np.float32)
+    base[::5] = np.float32(-0.0)
+    for acc in (False, True):
+        exp = base.copy() if acc else np.zeros(n, np.float32)
+        for i in touched:
+            x = X.round_f32(Fraction(float(X.round_f32(Fraction(S[i])))) / Fraction(float(alpha)))
+            exp[i] = X.add_f32(exp[i], x) if acc else x
+        rc, dense = orc.decode_accumulate_quant(msgs, n, alpha, dense=base, accumulate=acc)
+        assert rc == 0 and dense.view(np.uint32).tolist() == exp.view(np.uint32).tolist()
+        perm = [msgs[i] for i in rng.permutation(W)]  # integer sums: the order cannot matter
+        rc, dense2 = orc.decode_accumulate_quant(perm, n, alpha, dense=base, accumulate=acc)
+        assert rc == 0 and dense2.view(np.uint32).tolist() == exp.view(np.uint32).tolist()
+    lr = 0.37
+    rc, w = orc.decode_apply_quant(msgs, n, alpha, base, lr)
+    exp = base.copy()
+    for i in touched:
+        t = X.round_f32(Fraction(float(X.round_f32(Fraction(S[i])))) / Fraction(float(alpha)))
+        exp[i] = X.fma_f32(np.float32(-lr), t, base[i])
+    assert rc == 0 and w.view(np.uint32).tolist() == exp.view(np.uint32).tolist()
+
+
+def test_quant_rejects(orc):
+    n = 100
+    idx, val = np.array([3, 7], np.uint32), np.array([1.0, -2.0], np.float32)
+    for alpha, bits in ((0.0, 8), (-1.0, 8), (math.inf, 8), (math.nan, 16), (1.0, 4), (1.0, 32)):
+        assert orc.encode_quant(idx, val, n, alpha, bits)[0] == orc.EINVAL
+    rc, m, _ = orc.encode_quant(idx, val, n, 2.0, 8)
+    assert orc.decode_accumulate_quant([m], n, 2.0)[0] == 0
+    assert orc.decode_accumulate_quant([m], n, 4.0)[0] == orc.ECORRUPT   # another alpha
+    v1 = orc.encode(idx, val, n)
+    assert orc.decode_accumulate_quant([m, v1], n, 2.0)[0] == orc.ECORRUPT  # a float message
+    assert orc.decode_accumulate([m], n)[0] == orc.ECORRUPT                  # and the reverse
+    assert orc.decode_accumulate_quant([m + b"\0\0\0\0"], n, 2.0)[0] == orc.ECORRUPT
+    assert orc.decode_accumulate_quant([m], n, -2.0)[0] == orc.EINVAL
+    assert orc.decode_apply_quant([m], n, 2.0, np.zeros(n, np.float32), -1.0)[0] == orc.EINVAL
+    base = np.full(n, 5.0, np.float32)
+    rc, d = orc.decode_accumulate_quant([m, m[:-4]], n, 2.0, dense=base, accumulate=True)
+    assert rc == orc.ECORRUPT and np.all(d == 5.0)
+    assert orc.decode_accumulate_quant([m] * 65537, n, 2.0)[0] == orc.EUNSUPPORTED
