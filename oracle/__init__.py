@@ -111,9 +111,10 @@ def lib():
         L.orc_encode_quant.argtypes = [vp, vp, i64, i64, f32, ctypes.c_int, vp, vp,
                                        ctypes.c_uint64, vp]
         L.orc_decode_accumulate_quant.restype = ctypes.c_int
-        L.orc_decode_accumulate_quant.argtypes = [vp, vp, i32, f32, vp, i64, ctypes.c_int]
+        L.orc_decode_accumulate_quant.argtypes = [vp, vp, i32, ctypes.c_int, f32, vp, i64,
+                                                  ctypes.c_int]
         L.orc_decode_apply_quant.restype = ctypes.c_int
-        L.orc_decode_apply_quant.argtypes = [vp, vp, i32, f32, vp, i64, f32]
+        L.orc_decode_apply_quant.argtypes = [vp, vp, i32, ctypes.c_int, f32, vp, i64, f32]
         _lib = L
     return _lib
 
@@ -280,21 +281,24 @@ def _streams(streams):
     return bufs, W, ctypes.cast(ptrs, ctypes.c_void_p), ctypes.cast(sizes, ctypes.c_void_p)
 
 
-def decode_accumulate_quant(streams, n: int, alpha: float, dense=None, accumulate=False):
-    """Sum version-2 messages exactly in integers, divide by alpha once. Returns (rc, dense)."""
+def decode_accumulate_quant(streams, n: int, bits: int, alpha: float, dense=None,
+                            accumulate=False):
+    """Sum version-2 messages of `bits`-bit values exactly in integers, divide by alpha once.
+    Returns (rc, dense)."""
     bufs, W, ptrs, sizes = _streams(streams)
     dense = (np.zeros(n, np.float32) if dense is None
              else np.ascontiguousarray(dense, dtype=np.float32).copy())
-    rc = lib().orc_decode_accumulate_quant(ptrs, sizes, W, float(alpha),
+    rc = lib().orc_decode_accumulate_quant(ptrs, sizes, W, int(bits), float(alpha),
                                            _ptr(dense) if n else None, int(n),
                                            int(bool(accumulate)))
     return rc, dense
 
 
-def decode_apply_quant(streams, n: int, alpha: float, w, lr: float):
+def decode_apply_quant(streams, n: int, bits: int, alpha: float, w, lr: float):
     """w <- fmaf(-lr, (float)S / alpha, w) for version-2 messages. Returns (rc, w)."""
     bufs, W, ptrs, sizes = _streams(streams)
     w = np.ascontiguousarray(w, dtype=np.float32).copy()
-    rc = lib().orc_decode_apply_quant(ptrs, sizes, W, float(alpha), _ptr(w) if n else None,
+    rc = lib().orc_decode_apply_quant(ptrs, sizes, W, int(bits), float(alpha),
+                                      _ptr(w) if n else None,
                                       int(n), float(lr))
     return rc, w

@@ -533,9 +533,10 @@ int orc_encode_quant(const uint32_t* idx, const float* val, int64_t count, int64
 }
 
 /* The integer sums of W version-2 messages: S (int64) and which positions a value token reached.
- * Every message must carry the caller's alpha (bitwise) and a width of 8 or 16 bits. */
+ * Every message must carry the caller's width and alpha (bitwise): like alpha, the width is
+ * fixed for all learners, and the receiver needs it to find each message's runs. */
 static int orc_sum_quant(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
-                         int64_t n, float alpha, int64_t* S, uint8_t* touched) {
+                         int64_t n, int qbits, float alpha, int64_t* S, uint8_t* touched) {
     uint32_t abits;
     memcpy(&abits, &alpha, 4);
     for (int32_t w = 0; w < W; ++w) {
@@ -543,7 +544,7 @@ static int orc_sum_quant(const uint8_t* const* streams, const uint64_t* stream_b
         const uint64_t bytes = stream_bytes[w];
         if (bytes < 32) return ORC_ECORRUPT;
         const int bits = orc_get16(s + 6);
-        if (orc_get32(s) != ORC_MAGIC || orc_get16(s + 4) != 2 || (bits != 8 && bits != 16) ||
+        if (orc_get32(s) != ORC_MAGIC || orc_get16(s + 4) != 2 || bits != qbits ||
             orc_get64(s + 8) != (uint64_t)n || orc_get32(s + 24) != abits)
             return ORC_ECORRUPT;
         const uint64_t T = orc_get64(s + 16);
@@ -586,8 +587,10 @@ static int orc_sum_quant(const uint8_t* const* streams, const uint64_t* stream_b
  * reaches, added onto dense_i when accumulate is set (one binary32 addition); +0 elsewhere
  * unless accumulating. W is at most 65536, so |S_i| < 2^31. */
 int orc_decode_accumulate_quant(const uint8_t* const* streams, const uint64_t* stream_bytes,
-                                int32_t W, float alpha, float* dense, int64_t n, int accumulate) {
-    if (W < 0 || n < 0 || !isfinite(alpha) || !(alpha > 0.0f)) return ORC_EINVAL;
+                                int32_t W, int bits, float alpha, float* dense, int64_t n,
+                                int accumulate) {
+    if (W < 0 || n < 0 || (bits != 8 && bits != 16) || !isfinite(alpha) || !(alpha > 0.0f))
+        return ORC_EINVAL;
     if (W > 65536) return ORC_EUNSUPPORTED;
     int64_t* S = (int64_t*)malloc((n > 0 ? (size_t)n : 1) * sizeof(int64_t));
     uint8_t* touched = (uint8_t*)malloc(n > 0 ? (size_t)n : 1);
@@ -596,7 +599,7 @@ int orc_decode_accumulate_quant(const uint8_t* const* streams, const uint64_t* s
         free(touched);
         return ORC_ENOMEM;
     }
-    const int rc = orc_sum_quant(streams, stream_bytes, W, n, alpha, S, touched);
+    const int rc = orc_sum_quant(streams, stream_bytes, W, n, bits, alpha, S, touched);
     if (rc == ORC_OK)
         for (int64_t i = 0; i < n; ++i) {
             const float x = (float)S[i] / alpha;
@@ -613,11 +616,11 @@ int orc_decode_accumulate_quant(const uint8_t* const* streams, const uint64_t* s
 /* The SGD step of orc_decode_apply with version-2 messages: w_i <- fmaf(-lr, (float)S_i / alpha,
  * w_i); lr as there. */
 int orc_decode_apply_quant(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
-                           float alpha, float* w, int64_t n, float lr) {
+                           int bits, float alpha, float* w, int64_t n, float lr) {
     if (!isfinite(lr) || signbit(lr)) return ORC_EINVAL;
     float* s = (float*)malloc((n > 0 ? (size_t)n : 1) * sizeof(float));
     if (!s) return ORC_ENOMEM;
-    const int rc = orc_decode_accumulate_quant(streams, stream_bytes, W, alpha, s, n, 0);
+    const int rc = orc_decode_accumulate_quant(streams, stream_bytes, W, bits, alpha, s, n, 0);
     if (rc == ORC_OK)
         for (int64_t i = 0; i < n; ++i) w[i] = fmaf(-lr, s[i], w[i]);
     free(s);

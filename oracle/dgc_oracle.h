@@ -76,9 +76,10 @@ int orc_decode_apply(const uint8_t* const* streams, const uint64_t* stream_bytes
 int orc_encode_quant(const uint32_t* idx, const float* val, int64_t count, int64_t n, float alpha,
                      int bits, float* v, uint8_t* out, uint64_t out_cap, uint64_t* out_bytes);
 int orc_decode_accumulate_quant(const uint8_t* const* streams, const uint64_t* stream_bytes,
-                                int32_t W, float alpha, float* dense, int64_t n, int accumulate);
+                                int32_t W, int bits, float alpha, float* dense, int64_t n,
+                                int accumulate);
 int orc_decode_apply_quant(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
-                           float alpha, float* w, int64_t n, float lr);
+                           int bits, float alpha, float* w, int64_t n, float lr);
 
 #ifdef __cplusplus
 }

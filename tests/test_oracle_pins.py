@@ -739,7 +739,7 @@ def test_quant_golden(orc, name):
     assert [X.bits(v2[e[0]]) for e in ent] == [e[3] for e in ent]
     rest = np.setdiff1d(np.arange(n), idx)
     assert np.all(v2[rest] == 9.0)  # only sent entries take their remainder back
-    rc, dense = orc.decode_accumulate_quant([msg], n, alpha)
+    rc, dense = orc.decode_accumulate_quant([msg], n, bits, alpha)
     assert rc == 0
     exp = np.zeros(n, np.float32)
     exp[idx] = np.array([e[4] for e in ent], np.uint32).view(np.float32)
@@ -823,13 +823,13 @@ def test_quant_decode_sums_integers_in_any_order(orc, seed):
         for i in touched:
             x = X.round_f32(Fraction(float(X.round_f32(Fraction(S[i])))) / Fraction(float(alpha)))
             exp[i] = X.add_f32(exp[i], x) if acc else x
-        rc, dense = orc.decode_accumulate_quant(msgs, n, alpha, dense=base, accumulate=acc)
+        rc, dense = orc.decode_accumulate_quant(msgs, n, bits, alpha, dense=base, accumulate=acc)
         assert rc == 0 and dense.view(np.uint32).tolist() == exp.view(np.uint32).tolist()
         perm = [msgs[i] for i in rng.permutation(W)]  # integer sums: the order cannot matter
-        rc, dense2 = orc.decode_accumulate_quant(perm, n, alpha, dense=base, accumulate=acc)
+        rc, dense2 = orc.decode_accumulate_quant(perm, n, bits, alpha, dense=base, accumulate=acc)
         assert rc == 0 and dense2.view(np.uint32).tolist() == exp.view(np.uint32).tolist()
     lr = 0.37
-    rc, w = orc.decode_apply_quant(msgs, n, alpha, base, lr)
+    rc, w = orc.decode_apply_quant(msgs, n, bits, alpha, base, lr)
     exp = base.copy()
     for i in touched:
         t = X.round_f32(Fraction(float(X.round_f32(Fraction(S[i])))) / Fraction(float(alpha)))
@@ -843,15 +843,17 @@ def test_quant_rejects(orc):
     for alpha, bits in ((0.0, 8), (-1.0, 8), (math.inf, 8), (math.nan, 16), (1.0, 4), (1.0, 32)):
         assert orc.encode_quant(idx, val, n, alpha, bits)[0] == orc.EINVAL
     rc, m, _ = orc.encode_quant(idx, val, n, 2.0, 8)
-    assert orc.decode_accumulate_quant([m], n, 2.0)[0] == 0
-    assert orc.decode_accumulate_quant([m], n, 4.0)[0] == orc.ECORRUPT   # another alpha
+    assert orc.decode_accumulate_quant([m], n, 8, 2.0)[0] == 0
+    assert orc.decode_accumulate_quant([m], n, 8, 4.0)[0] == orc.ECORRUPT   # another alpha
+    assert orc.decode_accumulate_quant([m], n, 16, 2.0)[0] == orc.ECORRUPT  # another width
     v1 = orc.encode(idx, val, n)
-    assert orc.decode_accumulate_quant([m, v1], n, 2.0)[0] == orc.ECORRUPT  # a float message
-    assert orc.decode_accumulate([m], n)[0] == orc.ECORRUPT                  # and the reverse
-    assert orc.decode_accumulate_quant([m + b"\0\0\0\0"], n, 2.0)[0] == orc.ECORRUPT
-    assert orc.decode_accumulate_quant([m], n, -2.0)[0] == orc.EINVAL
-    assert orc.decode_apply_quant([m], n, 2.0, np.zeros(n, np.float32), -1.0)[0] == orc.EINVAL
+    assert orc.decode_accumulate_quant([m, v1], n, 8, 2.0)[0] == orc.ECORRUPT  # a float message
+    assert orc.decode_accumulate([m], n)[0] == orc.ECORRUPT                     # and the reverse
+    assert orc.decode_accumulate_quant([m + b"\0\0\0\0"], n, 8, 2.0)[0] == orc.ECORRUPT
+    assert orc.decode_accumulate_quant([m], n, 8, -2.0)[0] == orc.EINVAL
+    assert orc.decode_accumulate_quant([m], n, 12, 2.0)[0] == orc.EINVAL
+    assert orc.decode_apply_quant([m], n, 8, 2.0, np.zeros(n, np.float32), -1.0)[0] == orc.EINVAL
     base = np.full(n, 5.0, np.float32)
-    rc, d = orc.decode_accumulate_quant([m, m[:-4]], n, 2.0, dense=base, accumulate=True)
+    rc, d = orc.decode_accumulate_quant([m, m[:-4]], n, 8, 2.0, dense=base, accumulate=True)
     assert rc == orc.ECORRUPT and np.all(d == 5.0)
-    assert orc.decode_accumulate_quant([m] * 65537, n, 2.0)[0] == orc.EUNSUPPORTED
+    assert orc.decode_accumulate_quant([m] * 65537, n, 8, 2.0)[0] == orc.EUNSUPPORTED
