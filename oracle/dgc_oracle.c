@@ -463,7 +463,7 @@ int orc_decode_apply(const uint8_t* const* streams, const uint64_t* stream_bytes
  *         bullet 1: what is not sent stays in the local accumulator).
  * Message, version 2: header "DGC1", u16 version 2, u16 b, u64 n, u64 T, binary32 alpha, u32
  * nnz; then T two's-complement integers of b bits (escape tokens carry 0), zero bytes up to an
- * even offset, T u16 runs, zero bytes up to a multiple of 4. Receivers sum the integers exactly
+ * even offset, T u16 runs (no padding after them). Receivers sum the integers exactly
  * (order does not matter) and divide once: dense_i = (float)S_i / alpha. ---- */
 static int32_t orc_quantize(float val, float alpha, int bits) {
     const float x = rintf(alpha * val);
@@ -479,10 +479,10 @@ static uint64_t orc_runs_offset(uint64_t T, int bits) {
     return at + (at & 1); /* runs start at an even offset */
 }
 
-static uint64_t orc_size_quant(uint64_t T, int bits) {
-    const uint64_t at = orc_runs_offset(T, bits) + 2 * T;
-    return at + ((4 - (at & 3)) & 3); /* whole message a multiple of 4 */
-}
+/* no padding after the runs: the size then fixes T, so a receiver that knows b can lay out the
+ * messages from their sizes alone (a pad to 4 bytes would make 8-bit messages of 3 and 4 tokens
+ * the same size) */
+static uint64_t orc_size_quant(uint64_t T, int bits) { return orc_runs_offset(T, bits) + 2 * T; }
 
 int orc_encode_quant(const uint32_t* idx, const float* val, int64_t count, int64_t n, float alpha,
                      int bits, float* v, uint8_t* out, uint64_t out_cap, uint64_t* out_bytes) {

@@ -723,7 +723,6 @@ def golden_quant(name):
     msg += b"".join(struct.pack(fmt, t[1]) for t in tok)
     msg += b"\0" * (len(msg) % 2)
     msg += b"".join(struct.pack("<H", t[0]) for t in tok)
-    msg += b"\0" * ((-len(msg)) % 4)
     return n, bits, alpha, ent, msg, size
 
 
@@ -771,6 +770,8 @@ def test_quant_random_against_definition(orc, seed):
     val[rng.random(k) < 0.05] = np.float32(-0.0)
     rc, msg, v = orc.encode_quant(idx, val, n, alpha, bits, np.zeros(n, np.float32))
     assert rc == 0
+    T = struct.unpack_from("<Q", msg, 16)[0]  # the size follows from T and b
+    assert len(msg) == 32 + T * bits // 8 + (T * bits // 8) % 2 + 2 * T
     Q = 2 ** (bits - 1) - 1
     qs = []
     for j, x in enumerate(val):
