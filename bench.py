@@ -266,6 +266,45 @@ class Pipeline:
         del w
         return sorted(ms[3:])[reps // 2]
 
+    def time_quant(self, bits=8, alpha=1000.0, reps=20):
+        """The integer-valued variant of the last step's message, outside the step: encode with
+        the remainders put back into v (idempotent: the same values again), then decode it to a
+        dense array and apply it to a weight vector. Median CUDA-event times of each call."""
+        import torch
+
+        dgc = self.dgc
+        qmsg = torch.empty(self.msg_cap, dtype=torch.uint8, device=self.dev)
+        E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+        def timed(fn):
+            ms = []
+            for _ in range(reps + 3):
+                a, b = E(), E()
+                a.record()
+                fn()
+                b.record()
+                b.synchronize()
+                ms.append(a.elapsed_time(b))
+            return sorted(ms[3:])[reps // 2]
+
+        t_enc = timed(lambda: dgc.dgc_encode_quant(
+            self.out_idx, self.out_val, self.out_count, self.n, alpha, bits, self.v, qmsg,
+            self.msg_bytes, self.status, self.ews, max_count=self.cap, out_cap=self.msg_cap,
+            ws_bytes=self.ews_bytes))
+        self.nb_host.copy_(self.msg_bytes)
+        nb = int(self.nb_host.item())
+        ws_bytes = dgc.dgc_decode_workspace_quant([nb], self.n, bits)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=self.dev)
+        t_dec = timed(lambda: dgc.dgc_decode_accumulate_quant(
+            [qmsg], [nb], bits, alpha, self.dense, self.n, False, self.status, ws,
+            ws_bytes=ws_bytes))
+        w = torch.zeros(self.n, dtype=torch.float32, device=self.dev)
+        t_app = timed(lambda: dgc.dgc_decode_apply_quant(
+            [qmsg], [nb], bits, alpha, w, self.n, 0.01, self.status, ws, ws_bytes=ws_bytes))
+        del w, ws, qmsg
+        return {"bits": bits, "alpha": alpha, "message_bytes": nb, "encode_ms": round(t_enc, 4),
+                "decode_ms": round(t_dec, 4), "decode_apply_ms": round(t_app, 4)}
+
 
 def run_ours(args, world, rank, local):
     import numpy as np
@@ -343,6 +382,9 @@ def run_ours(args, world, rank, local):
     achieved = alg_bytes / (t_kernel / 1e3) / 1e9
     traffic = recorded_traffic(n)
     t_apply = pipe.time_decode_apply(nbytes[-1])
+    quant = pipe.time_quant()
+    if dgc.dgc_read_status(pipe.status) != 0:
+        raise RuntimeError("integer-message calls reported an error")
     if dgc.dgc_read_status(pipe.status) != 0:
         raise RuntimeError("decode-apply reported an error")
 
@@ -370,6 +412,7 @@ def run_ours(args, world, rank, local):
         "stages_ms": {"compress": round(t_compress, 4), "encode": round(t_encode, 4),
                       "decode": round(t_decode, 4)},
         "decode_apply_ms": round(t_apply, 4),  # outside the step: message -> SGD step on w
+        "quant": quant,  # outside the step: the same message as 8-bit integers
         "compress_gbs": round(4.0 * n / (t_compress / 1e3) / 1e9, 2),
         "message_bytes": int(statistics.median(nbytes)),
         "candidates": cand, "sent": int(st["sent"]),

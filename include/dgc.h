@@ -176,6 +176,30 @@ int dgc_encode(const uint32_t* idx, const float* val, const int64_t* count, int6
                int64_t n, uint8_t* out, uint64_t out_cap, uint64_t* out_bytes, int32_t* status,
                void* ws, size_t ws_bytes, dgc_stream_t stream);
 
+/* Integer-valued messages (version 2). [ADA] abstract: AdaComp sends the selected residues
+ * sparse and quantized; the IntSGD page, abstract: each learner scales its vector by a number
+ * every learner knows and rounds to integers, so no float crosses the wire. The pages give no
+ * bit format; this library's reading:
+ *   q_j = clamp(rint(alpha * val_j), -Q, Q), Q = 2^(bits-1) - 1, bits 8 or 16: one binary32
+ *         multiply, rounding half to even, NaN to 0;
+ *   the residual takes back what q_j does not carry: v[idx_j] = val_j - (float)q_j / alpha
+ *         (one binary32 divide, one subtract);
+ *   layout: "DGC1", u16 version 2, u16 bits, u64 n, u64 T, binary32 alpha, u32 nnz; T integers
+ *         of `bits` bits (escape tokens carry 0); one zero byte when that ends on an odd offset;
+ *         T u16 runs as in version 1; nothing after them, so a message's size fixes its T.
+ * Receivers add the integers exactly (the order cannot change the sum) and divide once:
+ * value_i = (float)S_i / alpha. alpha and bits are settings every learner and receiver share. */
+
+/* Encode count (device int64, at most max_count) ascending indices idx with values val as a
+ * version-2 message, as dgc_encode does for version 1 (same workspace, same errors; the message
+ * is never larger than dgc_encode_max_bytes). v (device, n binary32, or NULL) is the residual:
+ * v[idx_j] is overwritten with val_j - (float)q_j / alpha, the compressor having left 0 there.
+ * alpha must be finite and > 0, bits 8 or 16, else DGC_EINVAL. */
+int dgc_encode_quant(const uint32_t* idx, const float* val, const int64_t* count,
+                     int64_t max_count, int64_t n, float alpha, int32_t bits, float* v,
+                     uint8_t* out, uint64_t out_cap, uint64_t* out_bytes, int32_t* status,
+                     void* ws, size_t ws_bytes, dgc_stream_t stream);
+
 /* ---------------------------------------------------------------------------- decoder */
 
 /* Bytes of workspace dgc_decode_accumulate or dgc_decode_apply needs for W messages of the
@@ -210,6 +234,29 @@ int dgc_decode_accumulate(const uint8_t* const* streams, const uint64_t* stream_
 int dgc_decode_apply(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
                      float* w, int64_t n, float lr, int32_t* status, void* ws, size_t ws_bytes,
                      dgc_stream_t stream);
+
+/* Workspace for the version-2 decoders: W messages of `bits`-bit values with the given sizes. */
+int dgc_decode_workspace_quant(int32_t W, const uint64_t* stream_bytes, int64_t n, int32_t bits,
+                               size_t* bytes);
+
+/* Decode W version-2 messages whose values are `bits`-bit integers scaled by alpha. S_i = the
+ * exact integer sum over the messages; dense_i = (float)S_i / alpha (accumulate = 0: every
+ * entry, +0 where nothing landed), or dense_i + (float)S_i / alpha at the positions some message
+ * reaches (accumulate = 1; one binary32 addition, other entries untouched). A message whose
+ * version, width, alpha (bitwise), n or T differ from the call's sets *status = DGC_ECORRUPT and
+ * leaves dense as it was. bits other than 8 or 16, or alpha not finite and > 0: DGC_EINVAL;
+ * W > 65536: DGC_EUNSUPPORTED (so |S_i| < 2^31). Other arguments as dgc_decode_accumulate. */
+int dgc_decode_accumulate_quant(const uint8_t* const* streams, const uint64_t* stream_bytes,
+                                int32_t W, int32_t bits, float alpha, float* dense, int64_t n,
+                                int32_t accumulate, int32_t* status, void* ws, size_t ws_bytes,
+                                dgc_stream_t stream);
+
+/* The SGD step of dgc_decode_apply with version-2 messages: w_i <- fma(-lr, (float)S_i / alpha,
+ * w_i) where S_i != 0, w untouched elsewhere (where the step is the identity). Arguments and
+ * errors as dgc_decode_apply and dgc_decode_accumulate_quant. */
+int dgc_decode_apply_quant(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
+                           int32_t bits, float alpha, float* w, int64_t n, float lr,
+                           int32_t* status, void* ws, size_t ws_bytes, dgc_stream_t stream);
 
 /* -------------------------------------------------------------------------- utilities */
 

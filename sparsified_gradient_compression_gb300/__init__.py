@@ -18,6 +18,8 @@ __all__ = [
     "dgc_compress_workspace", "dgc_compress_max_out", "dgc_compress", "dgc_compress_noalloc",
     "dgc_encode_max_bytes", "dgc_encode_workspace", "dgc_encode",
     "dgc_decode_workspace", "dgc_decode_accumulate", "dgc_decode_apply",
+    "dgc_encode_quant", "dgc_decode_workspace_quant", "dgc_decode_accumulate_quant",
+    "dgc_decode_apply_quant",
     "dgc_read_status", "dgc_status_string", "dgc_launch_count", "dgc_selftest_wait_timeout",
     "dgc_profile_stream_pass",
     "SELECT_EXACT", "SELECT_SAMPLED", "SELECT_ADACOMP", "FLAG_MASK_MOMENTUM",
@@ -90,6 +92,13 @@ def lib():
         L.dgc_decode_workspace.argtypes = [i32, vp, i64, P(sz)]
         L.dgc_decode_accumulate.argtypes = [vp, vp, i32, vp, i64, i32, vp, vp, sz, vp]
         L.dgc_decode_apply.argtypes = [vp, vp, i32, vp, i64, ctypes.c_float, vp, vp, sz, vp]
+        f32 = ctypes.c_float
+        L.dgc_encode_quant.argtypes = [vp, vp, vp, i64, i64, f32, i32, vp, vp, u64, vp, vp, vp,
+                                       sz, vp]
+        L.dgc_decode_workspace_quant.argtypes = [i32, vp, i64, i32, P(sz)]
+        L.dgc_decode_accumulate_quant.argtypes = [vp, vp, i32, i32, f32, vp, i64, i32, vp, vp, sz,
+                                                  vp]
+        L.dgc_decode_apply_quant.argtypes = [vp, vp, i32, i32, f32, vp, i64, f32, vp, vp, sz, vp]
         L.dgc_read_status.argtypes = [vp, vp]
         L.dgc_status_string.argtypes = [ctypes.c_int]
         L.dgc_status_string.restype = ctypes.c_char_p
@@ -102,6 +111,8 @@ def lib():
                   "dgc_compress_noalloc",
                   "dgc_encode_max_bytes", "dgc_encode_workspace", "dgc_encode",
                   "dgc_decode_workspace", "dgc_decode_accumulate", "dgc_decode_apply",
+                  "dgc_encode_quant", "dgc_decode_workspace_quant",
+                  "dgc_decode_accumulate_quant", "dgc_decode_apply_quant",
                   "dgc_read_status",
                   "dgc_selftest_wait_timeout"):
             getattr(L, f).restype = ctypes.c_int
@@ -254,6 +265,55 @@ def dgc_decode_apply(streams, stream_bytes, w, n: int, lr: float, status, ws,
                                          ctypes.cast(sizes, ctypes.c_void_p), W, _ptr(w), int(n),
                                          float(lr), _ptr(status), _ptr(ws), int(ws_bytes),
                                          _stream(stream)), "dgc_decode_apply")
+
+
+def dgc_encode_quant(idx, val, count, n: int, alpha: float, bits: int, v, out, out_bytes, status,
+                     ws, max_count: int | None = None, out_cap: int | None = None,
+                     ws_bytes: int | None = None, stream=None) -> int:
+    """Version-2 message of `bits`-bit integers; v (or None) takes back each remainder."""
+    max_count = idx.numel() if max_count is None else max_count
+    out_cap = out.numel() * out.element_size() if out_cap is None else out_cap
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    return _check(lib().dgc_encode_quant(_ptr(idx), _ptr(val), _ptr(count), int(max_count),
+                                         int(n), float(alpha), int(bits),
+                                         None if v is None else _ptr(v), _ptr(out), int(out_cap),
+                                         _ptr(out_bytes), _ptr(status), _ptr(ws), int(ws_bytes),
+                                         _stream(stream)), "dgc_encode_quant")
+
+
+def dgc_decode_workspace_quant(stream_bytes, n: int, bits: int) -> int:
+    W = len(stream_bytes)
+    arr = (ctypes.c_uint64 * max(W, 1))(*[int(b) for b in stream_bytes])
+    out = ctypes.c_size_t(0)
+    _check(lib().dgc_decode_workspace_quant(W, ctypes.cast(arr, ctypes.c_void_p), int(n),
+                                            int(bits), ctypes.byref(out)),
+           "dgc_decode_workspace_quant")
+    return out.value
+
+
+def dgc_decode_accumulate_quant(streams, stream_bytes, bits: int, alpha: float, dense, n: int,
+                                accumulate: bool, status, ws, ws_bytes: int | None = None,
+                                stream=None) -> int:
+    W = len(stream_bytes)
+    ptrs = (ctypes.c_void_p * max(W, 1))(*[_ptr(s) for s in streams])
+    sizes = (ctypes.c_uint64 * max(W, 1))(*[int(b) for b in stream_bytes])
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    return _check(lib().dgc_decode_accumulate_quant(
+        ctypes.cast(ptrs, ctypes.c_void_p), ctypes.cast(sizes, ctypes.c_void_p), W, int(bits),
+        float(alpha), _ptr(dense), int(n), int(bool(accumulate)), _ptr(status), _ptr(ws),
+        int(ws_bytes), _stream(stream)), "dgc_decode_accumulate_quant")
+
+
+def dgc_decode_apply_quant(streams, stream_bytes, bits: int, alpha: float, w, n: int, lr: float,
+                           status, ws, ws_bytes: int | None = None, stream=None) -> int:
+    W = len(stream_bytes)
+    ptrs = (ctypes.c_void_p * max(W, 1))(*[_ptr(s) for s in streams])
+    sizes = (ctypes.c_uint64 * max(W, 1))(*[int(b) for b in stream_bytes])
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    return _check(lib().dgc_decode_apply_quant(
+        ctypes.cast(ptrs, ctypes.c_void_p), ctypes.cast(sizes, ctypes.c_void_p), W, int(bits),
+        float(alpha), _ptr(w), int(n), float(lr), _ptr(status), _ptr(ws), int(ws_bytes),
+        _stream(stream)), "dgc_decode_apply_quant")
 
 
 # ----------------------------------------------------------------------------- utilities

@@ -59,7 +59,27 @@ struct EncArgs {
     int32_t* status;
     EncCtl* ctl;
     uint64_t* tot;  // per-block token counts, then exclusive offsets
+    int32_t qbits;  // 0: binary32 values (version 1); 8 or 16: integers (version 2)
+    float alpha;    // version 2: the shared scale
+    float* v;       // version 2: residual that takes back what the integers do not carry
 };
+
+// version 2 layout: values of qbits/8 bytes, runs from the next even offset, nothing after them
+// (so the size fixes T: the receiver lays the messages out from their sizes)
+__host__ __device__ __forceinline__ uint64_t q_runs_offset(uint64_t T, int qbits) {
+    const uint64_t at = 32 + T * (uint64_t)(qbits / 8);
+    return at + (at & 1);
+}
+__host__ __device__ __forceinline__ uint64_t q_size(uint64_t T, int qbits) {
+    return q_runs_offset(T, qbits) + 2 * T;
+}
+
+// q = clamp(rint(alpha * x), -Q, Q); the conversion rounds half to even and takes NaN to 0
+__device__ __forceinline__ int32_t quantize(float x, float alpha, int qbits) {
+    const int32_t Q = (1 << (qbits - 1)) - 1;
+    const int32_t q = __float2int_rn(__fmul_rn(alpha, x));
+    return q > Q ? Q : (q < -Q ? -Q : q);
+}
 
 __device__ __forceinline__ bool enc_range(const EncArgs& a, uint64_t* lo, uint64_t* hi,
                                           uint64_t* cnt) {
@@ -121,7 +141,7 @@ __global__ void __launch_bounds__(1024) k_enc_scan(EncArgs a, int nblocks) {
     const uint64_t ex = block_excl_scan<1024>(x, s_scan, &T);
     if (threadIdx.x < nblocks) a.tot[threadIdx.x] = ex;
     if (threadIdx.x != 0) return;
-    const uint64_t bytes = 32 + 6 * T + ((T & 1) ? 2 : 0);
+    const uint64_t bytes = a.qbits ? q_size(T, a.qbits) : 32 + 6 * T + ((T & 1) ? 2 : 0);
     *a.out_bytes = bytes;
     if (bytes > a.out_cap) {
         report(a.status, DGC_ECAPACITY);
@@ -130,11 +150,18 @@ __global__ void __launch_bounds__(1024) k_enc_scan(EncArgs a, int nblocks) {
     }
     a.ctl->T = T;
     uint64_t* h = reinterpret_cast<uint64_t*>(a.out);
-    h[0] = (uint64_t)kMagic | (1ull << 32);  // magic, version 1, flags 0
     h[1] = a.n;
     h[2] = T;
-    h[3] = (uint64_t)*a.count;
-    if (T & 1) *reinterpret_cast<uint16_t*>(a.out + 32 + 6 * T) = 0;
+    if (a.qbits) {  // magic, version 2, width; alpha and the entry count share the last word
+        h[0] = (uint64_t)kMagic | (2ull << 32) | ((uint64_t)a.qbits << 48);
+        h[3] = (uint64_t)__float_as_uint(a.alpha) | ((uint64_t)*a.count << 32);
+        const uint64_t vend = 32 + T * (uint64_t)(a.qbits / 8);
+        if (vend & 1) a.out[vend] = 0;  // the pad byte before the runs
+    } else {
+        h[0] = (uint64_t)kMagic | (1ull << 32);  // magic, version 1, flags 0
+        h[3] = (uint64_t)*a.count;
+        if (T & 1) *reinterpret_cast<uint16_t*>(a.out + 32 + 6 * T) = 0;
+    }
 }
 
 __global__ void __launch_bounds__(kThreads) k_enc_write(EncArgs a) {
@@ -144,7 +171,10 @@ __global__ void __launch_bounds__(kThreads) k_enc_write(EncArgs a) {
     if (!enc_range(a, &lo, &hi, &cnt)) return;
     const uint64_t T = a.ctl->T;
     uint32_t* vals = reinterpret_cast<uint32_t*>(a.out + 32);
-    uint16_t* runs = reinterpret_cast<uint16_t*>(a.out + 32 + 4 * T);
+    int8_t* vals8 = reinterpret_cast<int8_t*>(a.out + 32);
+    int16_t* vals16 = reinterpret_cast<int16_t*>(a.out + 32);
+    uint16_t* runs = reinterpret_cast<uint16_t*>(
+        a.out + (a.qbits ? q_runs_offset(T, a.qbits) : 32 + 4 * T));
     uint64_t carry = a.tot[blockIdx.x];
     for (uint64_t c = lo; c < hi; c += (uint64_t)kThreads * kEncPer) {
         uint64_t tk[kEncPer];
@@ -165,10 +195,21 @@ __global__ void __launch_bounds__(kThreads) k_enc_write(EncArgs a) {
             const int64_t prev = j ? (int64_t)a.idx[j - 1] : -1;
             const uint64_t gap = (uint64_t)((int64_t)a.idx[j] - prev - 1);
             for (uint64_t x = 1; x < tk[e]; ++x, ++p) {
-                vals[p] = 0u;
+                if (a.qbits == 8) vals8[p] = 0;
+                else if (a.qbits == 16) vals16[p] = 0;
+                else vals[p] = 0u;
                 runs[p] = (uint16_t)kRunEscape;
             }
-            vals[p] = __float_as_uint(a.val[j]);
+            const float x = a.val[j];
+            if (a.qbits) {
+                const int32_t q = quantize(x, a.alpha, a.qbits);
+                if (a.qbits == 8) vals8[p] = (int8_t)q;
+                else vals16[p] = (int16_t)q;
+                if (a.v)  // the residual keeps x - q / alpha
+                    a.v[a.idx[j]] = __fsub_rn(x, __fdiv_rn(__int2float_rn(q), a.alpha));
+            } else {
+                vals[p] = __float_as_uint(x);
+            }
             runs[p] = (uint16_t)(gap % kRunEscape);
             ++p;
         }
@@ -182,6 +223,7 @@ struct DecStream {
     uint64_t T;
     uint64_t tok_base;
     uint64_t chunk_base;
+    uint64_t runs_off;  // byte offset of the runs block
 };
 
 struct DecCtl {
@@ -197,6 +239,8 @@ struct DecArgs {
     int32_t accumulate;
     int32_t apply;     // w <- fma(neg_lr, sum, w) at every position a message touches
     float neg_lr;
+    int32_t qbits;     // 0: binary32 messages; 8 or 16: integer messages (version 2)
+    float alpha;       // version 2: the shared scale every message must carry
     int32_t* status;
     DecCtl* ctl;
     uint32_t* bad;
@@ -224,8 +268,13 @@ __global__ void k_dec_init(DecArgs a) {
         const uint64_t* h = reinterpret_cast<const uint64_t*>(d.ptr);
         const uint64_t h0 = h[0];
         a.bad[w] = 0;
-        if ((uint32_t)h0 != kMagic || ((h0 >> 32) & 0xFFFFu) != 1u || h[1] != a.n || h[2] != d.T)
-            mark_bad(a, (int)w);
+        bool ok = (uint32_t)h0 == kMagic && h[1] == a.n && h[2] == d.T;
+        if (a.qbits)  // version 2: the receiver's width and alpha, bit for bit
+            ok = ok && ((h0 >> 32) & 0xFFFFu) == 2u && (h0 >> 48) == (uint64_t)a.qbits &&
+                 (uint32_t)h[3] == __float_as_uint(a.alpha);
+        else
+            ok = ok && ((h0 >> 32) & 0xFFFFu) == 1u;
+        if (!ok) mark_bad(a, (int)w);
     }
 }
 
@@ -247,7 +296,7 @@ __global__ void __launch_bounds__(kThreads) k_dec_pos(DecArgs a) {
     const uint64_t lc = c - d.chunk_base;
     const uint64_t tok0 = lc * kDecChunk;
     const uint64_t tok1 = umin64(d.T, tok0 + kDecChunk);
-    const uint16_t* runs = reinterpret_cast<const uint16_t*>(d.ptr + 32 + 4 * d.T);
+    const uint16_t* runs = reinterpret_cast<const uint16_t*>(d.ptr + d.runs_off);
     constexpr int kPer = kDecChunk / kThreads;
     uint32_t adv[kPer];
     uint64_t mine = 0;
@@ -296,20 +345,43 @@ __global__ void __launch_bounds__(kThreads) k_dec_pos(DecArgs a) {
     if (bad) mark_bad(a, w);
 }
 
+// token j's value: binary32 bits (version 1) or the integer, sign-extended (version 2)
+__device__ __forceinline__ uint32_t dec_value(const DecArgs& a, const DecStream& d, uint64_t j) {
+    if (a.qbits == 8) return (uint32_t)(int32_t)reinterpret_cast<const int8_t*>(d.ptr + 32)[j];
+    if (a.qbits == 16) return (uint32_t)(int32_t)reinterpret_cast<const int16_t*>(d.ptr + 32)[j];
+    return reinterpret_cast<const uint32_t*>(d.ptr + 32)[j];
+}
+
+// an integer sum back to a value: one conversion, one division by the shared alpha
+__device__ __forceinline__ float dequant(int32_t S, float alpha) {
+    return __fdiv_rn(__int2float_rn(S), alpha);
+}
+
+// kInt: version-2 messages. Their integers are summed exactly (any order gives the same sum) and
+// turned into a value once per position; a flag per entry records whether any message landed.
+template <bool kInt>
 __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
-    __shared__ __align__(16) float s_acc[kDecTile];
+    __shared__ __align__(16) uint32_t s_accw[kDecTile];  // binary32 sums, or int32 sums
+    __shared__ uint8_t s_touch[kInt ? kDecTile : 1];
     __shared__ uint32_t s_pos[kDecCap];
-    __shared__ float s_val[kDecCap];
+    __shared__ uint32_t s_val[kDecCap];
     __shared__ uint32_t s_off[kThreads + 1];
     __shared__ uint32_t s_first[kThreads];
     __shared__ uint64_t s_scan[33];
+    float* s_acc = reinterpret_cast<float*>(s_accw);
+    int32_t* s_acci = reinterpret_cast<int32_t*>(s_accw);
     if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
     const uint64_t t = blockIdx.x;
     const uint64_t p0 = t * kDecTile;
     const uint32_t len = (uint32_t)umin64(kDecTile, a.n - p0);
     const bool vec = (len == kDecTile) && ((reinterpret_cast<uintptr_t>(a.dense) & 15u) == 0);
-    const bool load = a.accumulate && !a.apply;  // apply mode sums from +0
-    if (vec && load) {
+    const bool load = !kInt && a.accumulate && !a.apply;  // apply mode sums from +0
+    if (kInt) {
+        for (uint32_t i = threadIdx.x; i < kDecTile; i += kThreads) {
+            s_acci[i] = 0;
+            s_touch[i] = 0;
+        }
+    } else if (vec && load) {
         for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
             reinterpret_cast<float4*>(s_acc)[i] = reinterpret_cast<const float4*>(a.dense + p0)[i];
     } else if (vec) {
@@ -345,7 +417,7 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
                 const DecStream& d = a.tab[wb + l];
                 const uint64_t j = s_first[l] + (f - s_off[l]);
                 s_pos[i] = a.pos[d.tok_base + j];
-                s_val[i] = reinterpret_cast<const float*>(d.ptr + 32)[j];
+                s_val[i] = dec_value(a, d, j);
             }
             __syncthreads();
             if (threadIdx.x < 32) {
@@ -353,8 +425,14 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
                     const uint32_t lo = max(s_off[l], r0), hi = min(s_off[l + 1], r0 + m);
                     for (uint32_t i = lo + threadIdx.x; i < hi; i += 32) {
                         const uint32_t p = s_pos[i - r0];
-                        if (p != kEscPos && p >= p0 && p < p0 + len)
-                            s_acc[p - p0] = __fadd_rn(s_acc[p - p0], s_val[i - r0]);
+                        if (p != kEscPos && p >= p0 && p < p0 + len) {
+                            if (kInt) {
+                                s_acci[p - p0] += (int32_t)s_val[i - r0];
+                                s_touch[p - p0] = 1;
+                            } else {
+                                s_acc[p - p0] = __fadd_rn(s_acc[p - p0], __uint_as_float(s_val[i - r0]));
+                            }
+                        }
                     }
                     __syncwarp();
                 }
@@ -363,7 +441,19 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
         }
     }
     __syncthreads();
-    if (a.apply) {
+    if (kInt) {
+        for (uint32_t i = threadIdx.x; i < len; i += kThreads) {
+            const int32_t S = s_acci[i];
+            float* o = a.dense + p0 + i;
+            if (a.apply) {  // S == 0: the step is the identity
+                if (S) *o = __fmaf_rn(a.neg_lr, dequant(S, a.alpha), *o);
+            } else if (a.accumulate) {  // one addition where a message landed
+                if (s_touch[i]) *o = __fadd_rn(*o, dequant(S, a.alpha));
+            } else {
+                *o = dequant(S, a.alpha);
+            }
+        }
+    } else if (a.apply) {
         // a sum that starts at +0 is +0 wherever no message lands (x + y is -0 only for two -0
         // addends), and fma(neg_lr, +0, w) == w for a finite neg_lr with its sign bit set: those
         // entries are left alone, the others take the step
@@ -407,7 +497,8 @@ __global__ void __launch_bounds__(kThreads) k_dec_scatter1(DecArgs a) {
     if (j >= d.T) return;
     const uint32_t p = a.pos[d.tok_base + j];
     if (p == kEscPos || p >= a.n) return;
-    const float x = reinterpret_cast<const float*>(d.ptr + 32)[j];
+    const uint32_t raw = dec_value(a, d, j);
+    const float x = a.qbits ? dequant((int32_t)raw, a.alpha) : __uint_as_float(raw);
     if (a.apply)  // the one-message sum at p is +0 + x; then the step
         a.dense[p] = __fmaf_rn(a.neg_lr, __fadd_rn(0.0f, x), a.dense[p]);
     else
@@ -419,26 +510,38 @@ struct DecLayout {
     uint64_t sum_T, nchunks, ntiles;
 };
 
-bool stream_tokens(uint64_t bytes, uint64_t* T) {
+// tokens of a message of `bytes` bytes; false when no message of that kind has that size
+bool stream_tokens(uint64_t bytes, int qbits, uint64_t* T) {
     if (bytes < 32) return false;
-    const uint64_t t = (bytes - 32) / 6;
-    if (32 + 6 * t + ((t & 1) ? 2 : 0) != bytes) return false;
-    *T = t;
-    return true;
+    if (!qbits) {
+        const uint64_t t = (bytes - 32) / 6;
+        if (32 + 6 * t + ((t & 1) ? 2 : 0) != bytes) return false;
+        *T = t;
+        return true;
+    }
+    const uint64_t per = (uint64_t)qbits / 8 + 2;  // bytes per token; padding adds at most 4
+    const uint64_t t0 = (bytes - 32) / per;
+    for (uint64_t t = t0 > 2 ? t0 - 2 : 0; t <= t0; ++t)
+        if (q_size(t, qbits) == bytes) {
+            *T = t;
+            return true;
+        }
+    return false;
 }
 
-int dec_layout(int32_t W, const uint64_t* stream_bytes, int64_t n, DecLayout* L,
+int dec_layout(int32_t W, const uint64_t* stream_bytes, int64_t n, int qbits, DecLayout* L,
                std::vector<DecStream>* tab) {
     L->sum_T = 0;
     L->nchunks = 0;
     for (int w = 0; w < W; ++w) {
         uint64_t T;
-        if (!stream_tokens(stream_bytes[w], &T)) return DGC_ECORRUPT;
-        if (tab) (*tab)[w] = DecStream{nullptr, T, L->sum_T, L->nchunks};
+        if (!stream_tokens(stream_bytes[w], qbits, &T)) return DGC_ECORRUPT;
+        const uint64_t ro = qbits ? q_runs_offset(T, qbits) : 32 + 4 * T;
+        if (tab) (*tab)[w] = DecStream{nullptr, T, L->sum_T, L->nchunks, ro};
         L->sum_T += T;
         L->nchunks += (T + kDecChunk - 1) / kDecChunk;
     }
-    if (tab) (*tab)[W] = DecStream{nullptr, 0, L->sum_T, L->nchunks};
+    if (tab) (*tab)[W] = DecStream{nullptr, 0, L->sum_T, L->nchunks, 0};
     L->ntiles = ((uint64_t)n + kDecTile - 1) / kDecTile;
     size_t o = 0;
     auto take = [&](size_t b) { size_t at = o; o = align256(o + b); return at; };
@@ -471,10 +574,11 @@ extern "C" int dgc_encode_workspace(int64_t max_count, size_t* bytes) {
     return DGC_OK;
 }
 
-extern "C" int dgc_encode(const uint32_t* idx, const float* val, const int64_t* count,
-                          int64_t max_count, int64_t n, uint8_t* out, uint64_t out_cap,
-                          uint64_t* out_bytes, int32_t* status, void* ws, size_t ws_bytes,
-                          dgc_stream_t stream) {
+namespace {
+int encode_impl(const uint32_t* idx, const float* val, const int64_t* count, int64_t max_count,
+                int64_t n, int32_t qbits, float alpha, float* v, uint8_t* out, uint64_t out_cap,
+                uint64_t* out_bytes, int32_t* status, void* ws, size_t ws_bytes,
+                dgc_stream_t stream) {
     if (max_count < 0 || n < 0) return DGC_EINVAL;
     if (n > 0xFFFFFFFFll || max_count > 0xFFFFFFFFll) return DGC_EUNSUPPORTED;
     if (!count || !out || !out_bytes || !status || !ws) return DGC_EINVAL;
@@ -493,6 +597,9 @@ extern "C" int dgc_encode(const uint32_t* idx, const float* val, const int64_t* 
     a.out_cap = out_cap;
     a.out_bytes = out_bytes;
     a.status = status;
+    a.qbits = qbits;
+    a.alpha = alpha;
+    a.v = v;
     char* w = static_cast<char*>(ws);
     a.ctl = reinterpret_cast<EncCtl*>(w);
     a.tot = reinterpret_cast<uint64_t*>(w + align256(sizeof(EncCtl)));
@@ -511,22 +618,54 @@ extern "C" int dgc_encode(const uint32_t* idx, const float* val, const int64_t* 
     }
     return DGC_OK;
 }
+}  // namespace
 
-extern "C" int dgc_decode_workspace(int32_t W, const uint64_t* stream_bytes, int64_t n,
-                                    size_t* bytes) {
+extern "C" int dgc_encode(const uint32_t* idx, const float* val, const int64_t* count,
+                          int64_t max_count, int64_t n, uint8_t* out, uint64_t out_cap,
+                          uint64_t* out_bytes, int32_t* status, void* ws, size_t ws_bytes,
+                          dgc_stream_t stream) {
+    return encode_impl(idx, val, count, max_count, n, 0, 0.0f, nullptr, out, out_cap, out_bytes,
+                       status, ws, ws_bytes, stream);
+}
+
+extern "C" int dgc_encode_quant(const uint32_t* idx, const float* val, const int64_t* count,
+                                int64_t max_count, int64_t n, float alpha, int32_t bits,
+                                float* v, uint8_t* out, uint64_t out_cap, uint64_t* out_bytes,
+                                int32_t* status, void* ws, size_t ws_bytes, dgc_stream_t stream) {
+    if ((bits != 8 && bits != 16) || !std::isfinite(alpha) || !(alpha > 0.0f)) return DGC_EINVAL;
+    return encode_impl(idx, val, count, max_count, n, bits, alpha, v, out, out_cap, out_bytes,
+                       status, ws, ws_bytes, stream);
+}
+
+namespace {
+int decode_workspace_impl(int32_t W, const uint64_t* stream_bytes, int64_t n, int32_t qbits,
+                          size_t* bytes) {
     if (!bytes || W < 0 || n < 0 || (W > 0 && !stream_bytes)) return DGC_EINVAL;
     if (n > 0xFFFFFFFFll) return DGC_EUNSUPPORTED;
     DecLayout L;
-    const int rc = dec_layout(W, stream_bytes, n, &L, nullptr);
+    const int rc = dec_layout(W, stream_bytes, n, qbits, &L, nullptr);
     if (rc) return rc;
     *bytes = L.total;
     return DGC_OK;
+}
+}  // namespace
+
+extern "C" int dgc_decode_workspace(int32_t W, const uint64_t* stream_bytes, int64_t n,
+                                    size_t* bytes) {
+    return decode_workspace_impl(W, stream_bytes, n, 0, bytes);
+}
+
+extern "C" int dgc_decode_workspace_quant(int32_t W, const uint64_t* stream_bytes, int64_t n,
+                                          int32_t bits, size_t* bytes) {
+    if (bits != 8 && bits != 16) return DGC_EINVAL;
+    return decode_workspace_impl(W, stream_bytes, n, bits, bytes);
 }
 
 namespace {
 int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
                 float* dense, int64_t n, int32_t accumulate, int32_t apply, float lr,
-                int32_t* status, void* ws, size_t ws_bytes, dgc_stream_t stream) {
+                int32_t qbits, float alpha, int32_t* status, void* ws, size_t ws_bytes,
+                dgc_stream_t stream) {
     if (W < 0 || n < 0) return DGC_EINVAL;
     if (n > 0xFFFFFFFFll) return DGC_EUNSUPPORTED;
     if (W > 0 && (!streams || !stream_bytes)) return DGC_EINVAL;
@@ -536,7 +675,7 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
         if (!streams[w] || ((uintptr_t)streams[w] & 15u) != 0) return DGC_EINVAL;
     std::vector<DecStream> tab((size_t)W + 1);
     DecLayout L;
-    int rc = dec_layout(W, stream_bytes, n, &L, &tab);
+    int rc = dec_layout(W, stream_bytes, n, qbits, &L, &tab);
     if (rc) return rc;
     if (L.sum_T > 0xFFFFFFFFull) return DGC_EUNSUPPORTED;
     if (ws_bytes < L.total) return DGC_EINVAL;
@@ -550,6 +689,8 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
     a.accumulate = accumulate ? 1 : 0;
     a.apply = apply ? 1 : 0;
     a.neg_lr = -lr;
+    a.qbits = qbits;
+    a.alpha = alpha;
     a.status = status;
     a.ctl = reinterpret_cast<DecCtl*>(p + L.ctl);
     a.bad = reinterpret_cast<uint32_t*>(p + L.bad);
@@ -586,7 +727,10 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
             ++launches;
         }
     } else if (L.ntiles > 0) {
-        k_dec_tiles<<<(unsigned)L.ntiles, kThreads, 0, s>>>(a);
+        if (qbits)
+            k_dec_tiles<true><<<(unsigned)L.ntiles, kThreads, 0, s>>>(a);
+        else
+            k_dec_tiles<false><<<(unsigned)L.ntiles, kThreads, 0, s>>>(a);
         ++launches;
     }
     dgc_internal_count_launches(launches);
@@ -602,13 +746,45 @@ extern "C" int dgc_decode_accumulate(const uint8_t* const* streams, const uint64
                                      int32_t W, float* dense, int64_t n, int32_t accumulate,
                                      int32_t* status, void* ws, size_t ws_bytes,
                                      dgc_stream_t stream) {
-    return decode_impl(streams, stream_bytes, W, dense, n, accumulate, 0, 0.0f, status, ws,
-                       ws_bytes, stream);
+    return decode_impl(streams, stream_bytes, W, dense, n, accumulate, 0, 0.0f, 0, 0.0f, status,
+                       ws, ws_bytes, stream);
 }
 
 extern "C" int dgc_decode_apply(const uint8_t* const* streams, const uint64_t* stream_bytes,
                                 int32_t W, float* w, int64_t n, float lr, int32_t* status,
                                 void* ws, size_t ws_bytes, dgc_stream_t stream) {
     if (!std::isfinite(lr) || std::signbit(lr)) return DGC_EINVAL;
-    return decode_impl(streams, stream_bytes, W, w, n, 0, 1, lr, status, ws, ws_bytes, stream);
+    return decode_impl(streams, stream_bytes, W, w, n, 0, 1, lr, 0, 0.0f, status, ws, ws_bytes,
+                       stream);
+}
+
+namespace {
+int check_quant(int32_t W, int32_t bits, float alpha) {
+    if ((bits != 8 && bits != 16) || !std::isfinite(alpha) || !(alpha > 0.0f)) return DGC_EINVAL;
+    if (W > 65536) return DGC_EUNSUPPORTED;  // keeps every integer sum below 2^31
+    return DGC_OK;
+}
+}  // namespace
+
+extern "C" int dgc_decode_accumulate_quant(const uint8_t* const* streams,
+                                           const uint64_t* stream_bytes, int32_t W, int32_t bits,
+                                           float alpha, float* dense, int64_t n,
+                                           int32_t accumulate, int32_t* status, void* ws,
+                                           size_t ws_bytes, dgc_stream_t stream) {
+    if (W < 0) return DGC_EINVAL;
+    const int rc = check_quant(W, bits, alpha);
+    if (rc) return rc;
+    return decode_impl(streams, stream_bytes, W, dense, n, accumulate, 0, 0.0f, bits, alpha,
+                       status, ws, ws_bytes, stream);
+}
+
+extern "C" int dgc_decode_apply_quant(const uint8_t* const* streams, const uint64_t* stream_bytes,
+                                      int32_t W, int32_t bits, float alpha, float* w, int64_t n,
+                                      float lr, int32_t* status, void* ws, size_t ws_bytes,
+                                      dgc_stream_t stream) {
+    if (W < 0 || !std::isfinite(lr) || std::signbit(lr)) return DGC_EINVAL;
+    const int rc = check_quant(W, bits, alpha);
+    if (rc) return rc;
+    return decode_impl(streams, stream_bytes, W, w, n, 0, 1, lr, bits, alpha, status, ws,
+                       ws_bytes, stream);
 }

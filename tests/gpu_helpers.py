@@ -108,3 +108,52 @@ def decode_apply(messages, n: int, w: np.ndarray, lr: float):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     dgc.dgc_decode_apply(bufs, sizes, wd, n, lr, status, ws, ws_bytes=ws_bytes)
     return dgc.dgc_read_status(status), host_f32(wd)[:n]
+
+
+def encode_quant(idx: np.ndarray, val: np.ndarray, n: int, alpha: float, bits: int,
+                 v: np.ndarray | None = None):
+    """Version-2 message on the GPU; returns (status, message bytes, residual v on host or None)."""
+    k = idx.size
+    enc = Encoder(max(k, 1), n)
+    d_idx = torch.from_numpy(np.append(idx, np.uint32(0)).astype(np.uint32).view(np.int32)).cuda()
+    d_val = dev_f32(np.append(val, np.float32(0)))
+    d_v = None if v is None else dev_f32(v)
+    dgc.dgc_encode_quant(d_idx, d_val, torch.tensor([k], dtype=torch.int64, device="cuda"), n,
+                         alpha, bits, d_v, enc.out, enc.out_bytes, enc.status, enc.ws,
+                         max_count=enc.max_count, out_cap=enc.cap, ws_bytes=enc.ws_bytes)
+    rc = dgc.dgc_read_status(enc.status)
+    return rc, (enc.message() if rc == 0 else b""), (None if d_v is None else host_f32(d_v))
+
+
+def _device_messages(messages):
+    bufs = []
+    for m in messages:
+        t = torch.zeros(max(len(m), 16) + 16, dtype=torch.uint8, device="cuda")
+        if len(m):
+            t[: len(m)] = torch.frombuffer(bytearray(m), dtype=torch.uint8).cuda()
+        bufs.append(t)
+    return bufs, [len(m) for m in messages]
+
+
+def decode_quant(messages, n: int, bits: int, alpha: float, dense: np.ndarray | None = None,
+                 accumulate=False):
+    """Version-2 decode on the GPU; returns (status, dense on host)."""
+    bufs, sizes = _device_messages(messages)
+    ws_bytes = dgc.dgc_decode_workspace_quant(sizes, n, bits)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    d = (torch.full((max(n, 1),), float("nan"), dtype=torch.float32, device="cuda")
+         if dense is None else dev_f32(dense))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dgc.dgc_decode_accumulate_quant(bufs, sizes, bits, alpha, d, n, accumulate, status, ws,
+                                    ws_bytes=ws_bytes)
+    return dgc.dgc_read_status(status), host_f32(d)[:n]
+
+
+def decode_apply_quant(messages, n: int, bits: int, alpha: float, w: np.ndarray, lr: float):
+    bufs, sizes = _device_messages(messages)
+    ws_bytes = dgc.dgc_decode_workspace_quant(sizes, n, bits)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    wd = dev_f32(w) if n else torch.zeros(1, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dgc.dgc_decode_apply_quant(bufs, sizes, bits, alpha, wd, n, lr, status, ws, ws_bytes=ws_bytes)
+    return dgc.dgc_read_status(status), host_f32(wd)[:n]

@@ -150,3 +150,35 @@ def test_decode_apply_rejects_on_host(L):
     assert d(cast(ptrs), cast(good), 1, FAKE, 100, 0.5, FAKE, FAKE, wsb - 1, None) == dgc.EINVAL
     assert d(cast(ptrs), cast(good), 1, None, 100, 0.5, FAKE, FAKE, wsb, None) == dgc.EINVAL
     assert d(cast(ptrs), cast(good), 1, FAKE, 2**32, 0.5, FAKE, FAKE, wsb, None) == dgc.EUNSUPPORTED
+
+
+def test_quant_entry_points_reject_on_host(L):
+    cast = lambda a: ctypes.cast(a, ctypes.c_void_p)  # noqa: E731
+    ews = dgc.dgc_encode_workspace(10)
+    e = L.dgc_encode_quant
+    for alpha, bits in ((0.0, 8), (-1.0, 16), (math.inf, 8), (math.nan, 8), (1.0, 4), (1.0, 32)):
+        assert e(FAKE, FAKE, FAKE, 10, 100, alpha, bits, None, FAKE, 100, FAKE, FAKE, FAKE, ews,
+                 None) == dgc.EINVAL
+    # the size fixes T for a known width: 16-bit messages are 32 + 4T bytes
+    sizes = (ctypes.c_uint64 * 1)(33)
+    out = ctypes.c_size_t(0)
+    w = L.dgc_decode_workspace_quant
+    assert w(1, cast(sizes), 100, 16, ctypes.byref(out)) == dgc.ECORRUPT
+    assert w(1, cast(sizes), 100, 12, ctypes.byref(out)) == dgc.EINVAL
+    assert dgc.dgc_decode_workspace_quant([40], 100, 16) > 0   # T = 2
+    assert dgc.dgc_decode_workspace_quant([42], 100, 8) > 0    # T = 3: 35 -> 36, + 6
+    ptrs = (ctypes.c_void_p * 1)(FAKE)
+    good = (ctypes.c_uint64 * 1)(40)
+    wsb = dgc.dgc_decode_workspace_quant([40], 100, 16)
+    d, a = L.dgc_decode_accumulate_quant, L.dgc_decode_apply_quant
+    for bits, alpha in ((12, 1.0), (16, 0.0), (16, math.nan)):
+        assert d(cast(ptrs), cast(good), 1, bits, alpha, FAKE, 100, 0, FAKE, FAKE, wsb,
+                 None) == dgc.EINVAL
+        assert a(cast(ptrs), cast(good), 1, bits, alpha, FAKE, 100, 0.5, FAKE, FAKE, wsb,
+                 None) == dgc.EINVAL
+    assert a(cast(ptrs), cast(good), 1, 16, 1.0, FAKE, 100, -0.0, FAKE, FAKE, wsb,
+             None) == dgc.EINVAL
+    many = (ctypes.c_void_p * 65537)(*([FAKE] * 65537))
+    many_sizes = (ctypes.c_uint64 * 65537)(*([40] * 65537))
+    assert d(cast(many), cast(many_sizes), 65537, 16, 1.0, FAKE, 100, 0, FAKE, FAKE, 1 << 30,
+             None) == dgc.EUNSUPPORTED

@@ -633,3 +633,135 @@ def test_decode_apply_malformed_and_empty():
     with pytest.raises(dgc.DGCError) as e:
         decode_apply([good], n, w, -0.0)
     assert e.value.code == dgc.EINVAL
+
+
+# ------------------------------------------------------------------- integer-valued messages
+from gpu_helpers import decode_apply_quant, decode_quant, encode_quant  # noqa: E402
+
+
+@pytest.mark.parametrize("name", ["codec_quant8.txt", "codec_quant16.txt"])
+def test_quant_goldens_on_gpu(name):
+    from test_oracle_pins import golden_quant
+    n, bits, alpha, ent, msg, _ = golden_quant(name)
+    idx = np.array([e[0] for e in ent], np.uint32)
+    val = np.array([e[1] for e in ent], np.uint32).view(np.float32)
+    rc, got, v = encode_quant(idx, val, n, float(alpha), bits, np.full(n, 9.0, np.float32))
+    assert rc == 0 and got == msg
+    assert [int(bits_of) for bits_of in v[idx].view(np.uint32)] == [e[3] for e in ent]
+    assert np.all(np.delete(v, idx) == 9.0)
+    rc, dense = decode_quant([msg], n, bits, float(alpha))
+    orc_rc, odense = oracle.decode_accumulate_quant([msg], n, bits, alpha)
+    assert rc == 0 and orc_rc == 0 and same_bits(dense, odense)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_quant_encode_random(seed):
+    rng = np.random.default_rng(2100 + seed)
+    n = int(rng.integers(1, 5_000_000))
+    k = int(rng.integers(0, min(n, 300_000) + 1))
+    bits = 8 if seed % 2 else 16
+    alpha = float(np.float32(rng.choice([1.0, 3.0, 1000.0, 0.37, 2.0 ** 20])))
+    idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+    val = (rng.standard_normal(k) * 10.0 ** rng.integers(-6, 3, k)).astype(np.float32)
+    val[rng.random(k) < 0.02] = np.float32(-0.0)
+    val[rng.random(k) < 0.01] = np.float32(np.inf)
+    v0 = rng.standard_normal(n).astype(np.float32)
+    rc, msg, v = encode_quant(idx, val, n, alpha, bits, v0)
+    orc_rc, omsg, ov = oracle.encode_quant(idx, val, n, alpha, bits, v0)
+    assert rc == 0 and orc_rc == 0
+    assert msg == omsg
+    assert same_bits(v, ov)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_quant_decode_learners(seed):
+    rng = np.random.default_rng(2200 + seed)
+    n = int(rng.integers(1, 3_000_000))
+    W = int(rng.integers(1, 300))
+    bits = 16 if seed % 2 else 8
+    alpha = float(np.float32(rng.choice([0.5, 3.0, 1000.0])))
+    msgs = []
+    for _ in range(W):
+        k = int(rng.integers(0, min(n, 20_000) + 1))
+        idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+        val = (rng.standard_normal(k) * 10.0 ** rng.integers(-3, 2, k)).astype(np.float32)
+        rc, m, _ = oracle.encode_quant(idx, val, n, alpha, bits)
+        assert rc == 0
+        msgs.append(m)
+    base = rng.standard_normal(n).astype(np.float32)
+    base[::9] = np.float32(-0.0)
+    for acc in (False, True):
+        rc, dense = decode_quant(msgs, n, bits, alpha, dense=base, accumulate=acc)
+        orc_rc, odense = oracle.decode_accumulate_quant(msgs, n, bits, alpha, dense=base,
+                                                        accumulate=acc)
+        assert rc == 0 and orc_rc == 0 and same_bits(dense, odense), acc
+    rc, w = decode_apply_quant(msgs, n, bits, alpha, base, 0.37)
+    orc_rc, ow = oracle.decode_apply_quant(msgs, n, bits, alpha, base, np.float32(0.37))
+    assert rc == 0 and orc_rc == 0 and same_bits(w, ow)
+
+
+def test_quant_nan_and_infinities_on_gpu():
+    n = 10
+    idx = np.array([1, 2, 3], np.uint32)
+    val = np.array([np.nan, np.inf, -np.inf], np.float32)
+    rc, msg, v = encode_quant(idx, val, n, 2.0, 8, np.zeros(n, np.float32))
+    orc_rc, omsg, ov = oracle.encode_quant(idx, val, n, 2.0, 8, np.zeros(n, np.float32))
+    assert rc == 0 and orc_rc == 0 and msg == omsg  # NaN -> 0, +-inf -> +-127
+    assert np.isnan(v[1]) and np.isnan(ov[1])       # NaN - 0 is a NaN (payloads may differ)
+    assert same_bits(v[2:4], ov[2:4])
+
+
+def test_quant_decode_rejects_and_leaves_dense():
+    n = 1000
+    idx, val = np.array([5, 999], np.uint32), np.array([1.0, -2.0], np.float32)
+    _, m8, _ = oracle.encode_quant(idx, val, n, 2.0, 8)
+    _, m8b, _ = oracle.encode_quant(idx, val, n, 4.0, 8)   # another alpha
+    v1 = oracle.encode(idx, val, n)                          # a binary32 message, 6 B per token
+    base = np.full(n, 7.0, np.float32)
+    for msgs in ([m8b], [m8, m8b], [m8b, m8]):
+        rc, d = decode_quant(msgs, n, 8, 2.0, dense=base, accumulate=True)
+        assert rc == dgc.ECORRUPT and np.all(d == 7.0)
+        rc, w = decode_apply_quant(msgs, n, 8, 2.0, base, 0.5)
+        assert rc == dgc.ECORRUPT and np.all(w == 7.0)
+    # its 44 bytes fit both widths (8 bits: T = 4, 16 bits: T = 3): the header tells it apart
+    for bits in (8, 16):
+        rc, d = decode_quant([v1], n, bits, 2.0, dense=base, accumulate=True)
+        assert rc == dgc.ECORRUPT and np.all(d == 7.0)
+    with pytest.raises(dgc.DGCError) as e:  # 45 bytes: no message of this library
+        decode_quant([v1 + b"\0"], n, 16, 2.0, dense=base)
+    assert e.value.code == dgc.ECORRUPT
+    with pytest.raises(dgc.DGCError) as e:  # 38 bytes: an 8-bit message, no 16-bit size
+        decode_quant([m8], n, 16, 2.0, dense=base)
+    assert e.value.code == dgc.ECORRUPT
+    _, m16, _ = oracle.encode_quant(np.array([5, 6, 999], np.uint32), np.ones(3, np.float32), n,
+                                    2.0, 16)  # 44 bytes, also an 8-bit size: the width differs
+    rc, d = decode_quant([m16], n, 8, 2.0, dense=base, accumulate=True)
+    assert rc == dgc.ECORRUPT and np.all(d == 7.0)
+
+
+def test_quant_after_compress_matches_oracle():
+    # the path a learner runs: compress (sampled, 99.9%), then 8-bit integers with the
+    # remainders put back into the residual
+    n = 4_000_003
+    off = np.array([0, 1_000_000, n])
+    pd, po = params_pair(mode=dgc.SELECT_SAMPLED, sparsity=0.999, momentum=0.9, seed=5)
+    comp = Compressor(n, off, pd)
+    u_h, v_h = np.zeros(n, np.float32), np.zeros(n, np.float32)
+    u_d, v_d = dev_f32(u_h), dev_f32(v_h)
+    for t in range(3):
+        g = (np.random.default_rng([7, t]).standard_normal(n) * 0.01).astype(np.float32)
+        comp(dev_f32(g), u_d, v_d)
+        assert comp.status_code() == 0
+        idx, val, _ = comp.results()
+        oidx, oval, _ = oracle.compress(g, u_h, v_h, off, po)
+        assert np.array_equal(idx, oidx) and same_bits(val, oval)
+        alpha = 1000.0
+        enc = Encoder(comp.cap, n)
+        dgc.dgc_encode_quant(comp.out_idx, comp.out_val, comp.out_count, n, alpha, 8, v_d,
+                             enc.out, enc.out_bytes, enc.status, enc.ws, max_count=comp.cap,
+                             out_cap=enc.cap, ws_bytes=enc.ws_bytes)
+        assert dgc.dgc_read_status(enc.status) == 0
+        rc, omsg, v_h = oracle.encode_quant(oidx, oval, n, alpha, 8, v_h)
+        assert rc == 0 and enc.message() == omsg
+        assert same_bits(host_f32(v_d), v_h), f"step {t}"
+        assert same_bits(host_f32(u_d), u_h)
