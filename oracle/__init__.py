@@ -37,7 +37,7 @@ class Params(ctypes.Structure):
         ("reselect_factor", ctypes.c_double),
         ("seed", ctypes.c_uint64),
         ("bin_size", ctypes.c_uint32),
-        ("pad", ctypes.c_uint32),
+        ("leak", ctypes.c_float),
     ]
 
 
@@ -91,6 +91,15 @@ def lib():
         L.orc_accumulate_one.restype = None
         L.orc_accumulate_one.argtypes = [ctypes.c_float] * 5 + [
             ctypes.c_int, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
+        L.orc_accumulate_leak.restype = None
+        L.orc_accumulate_leak.argtypes = [ctypes.c_float] * 5 + [
+            ctypes.c_int, ctypes.c_float, ctypes.POINTER(ctypes.c_float),
+            ctypes.POINTER(ctypes.c_float)]
+        L.orc_compress_shared.restype = ctypes.c_int
+        L.orc_compress_shared.argtypes = [vp, vp, vp, i64, vp, i32, ctypes.POINTER(Params), vp,
+                                          i64, vp]
+        L.orc_sum_shared.restype = ctypes.c_int
+        L.orc_sum_shared.argtypes = [vp, i32, i64, vp]
         L.orc_topk.restype = ctypes.c_int
         L.orc_topk.argtypes = [vp, vp, i64, i64, vp]
         L.orc_bin_select.restype = None
@@ -124,10 +133,11 @@ def _ptr(a: np.ndarray):
 
 
 def make_params(mode=EXACT, sparsity=0.999, momentum=0.9, clip_norm=0.0, mask_momentum=True,
-                sample_ratio=0.01, reselect_factor=1.3, seed=0, bin_size=1000) -> Params:
+                sample_ratio=0.01, reselect_factor=1.3, seed=0, bin_size=1000,
+                leak=0.0) -> Params:
     return Params(mode, MASK_MOMENTUM if mask_momentum else 0, float(sparsity),
                   float(momentum), float(clip_norm), float(sample_ratio),
-                  float(reselect_factor), int(seed) & (2**64 - 1), int(bin_size), 0)
+                  float(reselect_factor), int(seed) & (2**64 - 1), int(bin_size), float(leak))
 
 
 def ppb(fraction: float) -> int:
@@ -162,6 +172,13 @@ def accumulate_one(g, u, v, momentum, scale=1.0, clipped=False):
     uo, vo = ctypes.c_float(), ctypes.c_float()
     lib().orc_accumulate_one(float(g), float(u), float(v), float(momentum), float(scale),
                              int(bool(clipped)), ctypes.byref(uo), ctypes.byref(vo))
+    return np.float32(uo.value), np.float32(vo.value)
+
+
+def accumulate_leak(g, u, v, momentum, leak, scale=1.0, clipped=False):
+    uo, vo = ctypes.c_float(), ctypes.c_float()
+    lib().orc_accumulate_leak(float(g), float(u), float(v), float(momentum), float(scale),
+                              int(bool(clipped)), float(leak), ctypes.byref(uo), ctypes.byref(vo))
     return np.float32(uo.value), np.float32(vo.value)
 
 
@@ -302,3 +319,26 @@ def decode_apply_quant(streams, n: int, bits: int, alpha: float, w, lr: float):
                                       _ptr(w) if n else None,
                                       int(n), float(lr))
     return rc, w
+
+
+def compress_shared(g, u, v, seg_off, params: Params, idx):
+    """One step at the shared index set idx; u and v are updated in place. Returns (rc, values)."""
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    assert u.dtype == np.float32 and v.dtype == np.float32
+    seg_off = np.ascontiguousarray(seg_off, dtype=np.int64)
+    idx = np.ascontiguousarray(idx, dtype=np.uint32)
+    out = np.zeros(max(idx.size, 1), np.float32)
+    rc = lib().orc_compress_shared(_ptr(g), _ptr(u), _ptr(v), g.size, _ptr(seg_off),
+                                   seg_off.size - 1, ctypes.byref(params), _ptr(idx), idx.size,
+                                   _ptr(out))
+    return rc, out[: idx.size].copy()
+
+
+def sum_shared(vals):
+    """Learner-ordered binary32 sum of equal-length value vectors. Returns (rc, sum)."""
+    arrs = [np.ascontiguousarray(a, dtype=np.float32) for a in vals]
+    count = arrs[0].size if arrs else 0
+    ptrs = (ctypes.c_void_p * max(len(arrs), 1))(*[a.ctypes.data for a in arrs])
+    out = np.zeros(max(count, 1), np.float32)
+    rc = lib().orc_sum_shared(ctypes.cast(ptrs, ctypes.c_void_p), len(arrs), count, _ptr(out))
+    return rc, out[:count].copy()

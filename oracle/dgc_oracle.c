@@ -16,6 +16,10 @@
  *   [ADA] "AdaComp : Adaptive Residual Gradient Compression for Data-Parallel Distributed
  *         Training" -- abstract (residues selected locally), citation snippets (entries ranked
  *         by magnitude, e.g. the largest 1%).
+ *   [SC]  the ScaleComp abstract (Scalable Sparsified Gradient Compression) on the first page,
+ *         a taxoreview.com listing -- a commutative compressor that uses how alike the
+ *         learners' gradients are, keeps the traffic independent of the number of learners and
+ *         works with all-reduce; a low-pass filter in the local gradient accumulation.
  * The pages give bullets, not formulas. Each step below names the reading it takes where the
  * pages leave a detail open.
  *
@@ -122,6 +126,17 @@ void orc_accumulate_one(float g, float u, float v, float momentum, float scale, 
     *v_out = v + un;
 }
 
+/* The accumulation with [SC]'s low-pass filter. Reading: the accumulator becomes a first-order
+ * (leaky) low-pass filter, v <- leak*v + u in one fused multiply-add, 0 < leak <= 1; leak = 1 is
+ * DGC's plain accumulation (fmaf(1, v, u) rounds v + u once, exactly as the addition does). */
+void orc_accumulate_leak(float g, float u, float v, float momentum, float scale, int clipped,
+                         float leak, float* u_out, float* v_out) {
+    float gp = clipped ? g * scale : g;
+    float un = fmaf(momentum, u, gp);
+    *u_out = un;
+    *v_out = fmaf(leak, v, un);
+}
+
 typedef struct {
     uint32_t key;
     uint32_t idx;
@@ -197,6 +212,7 @@ int orc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* s
     if (!(p->sparsity >= 0.0 && p->sparsity <= 1.0)) return ORC_EINVAL;
     if (p->mode != ORC_EXACT && p->mode != ORC_SAMPLED && p->mode != ORC_ADACOMP) return ORC_EINVAL;
     if (p->mode == ORC_ADACOMP && p->bin_size == 0) return ORC_EINVAL;
+    if (!(p->leak >= 0.0f && p->leak <= 1.0f)) return ORC_EINVAL; /* 0: no filter (leak 1) */
     if (seg_off[0] != 0 || seg_off[nseg] != n) return ORC_EINVAL;
     for (int32_t s = 0; s < nseg; ++s)
         if (seg_off[s + 1] < seg_off[s]) return ORC_EINVAL;
@@ -224,8 +240,9 @@ int orc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* s
         const float scale = orc_clip_scale(g + a, ns, p->clip_norm, &clipped);
         st.clip_scale = scale;
 
+        const float leak = p->leak == 0.0f ? 1.0f : p->leak;
         for (int64_t i = a; i < b; ++i)
-            orc_accumulate_one(g[i], u[i], v[i], p->momentum, scale, clipped, &u[i], &v[i]);
+            orc_accumulate_leak(g[i], u[i], v[i], p->momentum, scale, clipped, leak, &u[i], &v[i]);
 
         uint8_t* sel = (uint8_t*)calloc((size_t)(ns > 0 ? ns : 1), 1);
         uint32_t* cand = (uint32_t*)malloc((size_t)(ns > 0 ? ns : 1) * sizeof(uint32_t));
@@ -625,4 +642,56 @@ int orc_decode_apply_quant(const uint8_t* const* streams, const uint64_t* stream
         for (int64_t i = 0; i < n; ++i) w[i] = fmaf(-lr, s[i], w[i]);
     free(s);
     return rc;
+}
+
+/* ---- [SC]'s commutative compressor. Reading: every learner sends its accumulator at one
+ * shared index set S (the same positions for all), so the learners' messages are vectors of
+ * the same |S| entries that add up position by position -- what an all-reduce computes -- and
+ * each learner's traffic is |S| values whatever the number of learners. Which learner chooses S
+ * is the caller's choice (for instance one learner in turn, with orc_compress); the others then
+ * call orc_compress_shared with that S. ---- */
+
+/* One step of a learner that sends at the given S: clipping and accumulation exactly as in
+ * orc_compress (same parameters; the selection mode and sparsity are not used), then for each
+ * j < count: out_val[j] = v[idx[j]], and the sent entry leaves the accumulator (v <- 0, u <- 0
+ * with masking). idx must be strictly ascending and below n. */
+int orc_compress_shared(const float* g, float* u, float* v, int64_t n, const int64_t* seg_off,
+                        int32_t nseg, const orc_params* p, const uint32_t* idx, int64_t count,
+                        float* out_val) {
+    if (!p || !seg_off || nseg < 1 || n < 0 || n > 0xFFFFFFFFll || count < 0) return ORC_EINVAL;
+    if (!(p->leak >= 0.0f && p->leak <= 1.0f)) return ORC_EINVAL;
+    if (seg_off[0] != 0 || seg_off[nseg] != n) return ORC_EINVAL;
+    for (int32_t s = 0; s < nseg; ++s)
+        if (seg_off[s + 1] < seg_off[s]) return ORC_EINVAL;
+    int64_t prev = -1;
+    for (int64_t j = 0; j < count; ++j) {
+        if ((int64_t)idx[j] <= prev || (int64_t)idx[j] >= n) return ORC_EINVAL;
+        prev = idx[j];
+    }
+    const float leak = p->leak == 0.0f ? 1.0f : p->leak;
+    for (int32_t s = 0; s < nseg; ++s) {
+        const int64_t a = seg_off[s], b = seg_off[s + 1];
+        int clipped = 0;
+        const float scale = orc_clip_scale(g + a, b - a, p->clip_norm, &clipped);
+        for (int64_t i = a; i < b; ++i)
+            orc_accumulate_leak(g[i], u[i], v[i], p->momentum, scale, clipped, leak, &u[i], &v[i]);
+    }
+    for (int64_t j = 0; j < count; ++j) {
+        out_val[j] = v[idx[j]];
+        v[idx[j]] = 0.0f;
+        if (p->flags & ORC_MASK_MOMENTUM) u[idx[j]] = 0.0f;
+    }
+    return ORC_OK;
+}
+
+/* The sum of W learners' value vectors over one shared S: out[j] = the learner-ordered sum
+ * from +0 of vals[w][j], one binary32 addition each (the order the decoder uses). */
+int orc_sum_shared(const float* const* vals, int32_t W, int64_t count, float* out) {
+    if (W < 0 || count < 0) return ORC_EINVAL;
+    for (int64_t j = 0; j < count; ++j) {
+        float acc = 0.0f;
+        for (int32_t w = 0; w < W; ++w) acc = acc + vals[w][j];
+        out[j] = acc;
+    }
+    return ORC_OK;
 }

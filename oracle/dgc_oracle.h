@@ -35,7 +35,7 @@ typedef struct {
     double reselect_factor; /* sampled mode: re-select exactly when |C| > factor * k */
     uint64_t seed;          /* sampled mode: seed of the sample positions */
     uint32_t bin_size;      /* AdaComp mode: entries per bin (>= 1) */
-    uint32_t pad;
+    float leak;             /* v <- leak*v + u, in [0, 1]; 0 means 1 (no filter) */
 } orc_params;
 
 typedef struct {
@@ -57,6 +57,8 @@ double orc_sumsq(const float* g, int64_t n);
 float orc_clip_scale(const float* g, int64_t n, float clip_norm, int* clipped);
 void orc_accumulate_one(float g, float u, float v, float momentum, float scale, int clipped,
                         float* u_out, float* v_out);
+void orc_accumulate_leak(float g, float u, float v, float momentum, float scale, int clipped,
+                         float leak, float* u_out, float* v_out);
 int orc_topk(const float* v, const uint32_t* cand, int64_t ncand, int64_t k, uint8_t* selected);
 void orc_bin_select(const float* v, int64_t n, uint32_t bin_size, uint8_t* selected);
 
@@ -71,6 +73,12 @@ int orc_decode_accumulate(const uint8_t* const* streams, const uint64_t* stream_
                           int32_t W, float* dense, int64_t n, int accumulate);
 int orc_decode_apply(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
                      float* w, int64_t n, float lr);
+
+/* one index set shared by all learners */
+int orc_compress_shared(const float* g, float* u, float* v, int64_t n, const int64_t* seg_off,
+                        int32_t nseg, const orc_params* p, const uint32_t* idx, int64_t count,
+                        float* out_val);
+int orc_sum_shared(const float* const* vals, int32_t W, int64_t count, float* out);
 
 /* integer-valued messages (version 2) */
 int orc_encode_quant(const uint32_t* idx, const float* val, int64_t count, int64_t n, float alpha,

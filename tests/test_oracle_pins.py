@@ -858,3 +858,137 @@ def test_quant_rejects(orc):
     rc, d = orc.decode_accumulate_quant([m, m[:-4]], n, 8, 2.0, dense=base, accumulate=True)
     assert rc == orc.ECORRUPT and np.all(d == 5.0)
     assert orc.decode_accumulate_quant([m] * 65537, n, 8, 2.0)[0] == orc.EUNSUPPORTED
+
+
+# ------------------------------------------------------------- ScaleComp: leak and shared set
+# Readings of the ScaleComp abstract (first page): the low-pass filter in the local accumulation
+# is a leaky accumulator v <- fma(leak, v, u); the commutative compressor sends every learner's
+# accumulator at one shared index set, so the messages add up position by position.
+def _exact_accumulate_leak(g, u, v, m, leak):
+    un = np.empty_like(u)
+    vn = np.empty_like(v)
+    for i in range(g.size):
+        un[i] = X.fma_f32(m, u[i], g[i])
+        vn[i] = X.fma_f32(leak, v[i], un[i])
+    return un, vn
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_accumulate_leak_is_single_rounding_fma(orc, seed):
+    rng = np.random.default_rng(3000 + seed)
+    for _ in range(200):
+        g, u, v = (np.float32(x) for x in rng.standard_normal(3) * 10.0 ** rng.integers(-6, 6, 3))
+        m = np.float32(rng.choice([0.9, 0.0]))
+        leak = np.float32(rng.choice([0.5, 0.9, 0.999, 1.0, 0.1]))
+        uo, vo = orc.accumulate_leak(g, u, v, m, leak)
+        ue = X.fma_f32(m, u, g)
+        assert X.bits(uo) == X.bits(ue) and X.bits(vo) == X.bits(X.fma_f32(leak, v, ue))
+        if leak == 1.0:  # fma(1, v, u) is the plain sum: DGC's accumulation
+            assert X.bits(vo) == X.bits(orc.accumulate_one(g, u, v, m)[1])
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_leak_in_compress(orc, seed):
+    rng = np.random.default_rng(3100 + seed)
+    n = int(rng.integers(1, 3000))
+    off = _random_segments(rng, n)
+    g, u, v = (rng.standard_normal(n).astype(np.float32) for _ in range(3))
+    mode = [orc.EXACT, orc.SAMPLED, orc.ADACOMP][seed % 3]
+    # leak 0 (off) and leak 1 give the same step, bit for bit
+    outs = []
+    for leak in (0.0, 1.0):
+        uu, vv = u.copy(), v.copy()
+        idx, val, _ = orc.compress(g, uu, vv, off, orc.make_params(mode, 0.99, 0.9, seed=3,
+                                                                   bin_size=16, leak=leak))
+        outs.append((idx, val, uu, vv))
+    assert all(np.array_equal(a.view(np.uint32), b.view(np.uint32))
+               for a, b in zip(outs[0][1:], outs[1][1:])) and np.array_equal(outs[0][0], outs[1][0])
+    # a real leak: the accumulator follows the definition, the selection runs on it
+    leak = np.float32(0.75)
+    un, vn = _exact_accumulate_leak(g, u, v, np.float32(0.9), leak)
+    uu, vv = u.copy(), v.copy()
+    idx, val, _ = orc.compress(g, uu, vv, off, orc.make_params(orc.EXACT, 0.99, 0.9,
+                                                               mask_momentum=False, leak=leak))
+    exp_idx = []
+    for a, b in zip(off[:-1], off[1:]):
+        k = orc.count(int(b - a), orc.ppb(1 - 0.99))
+        exp_idx += [int(a) + i for i in brute_topk(vn[a:b], k)]
+    assert sorted(exp_idx) == idx.tolist()
+    assert [X.bits(x) for x in val] == [X.bits(vn[i]) for i in idx]
+    vn[idx] = 0.0
+    assert vv.view(np.uint32).tolist() == vn.view(np.uint32).tolist()
+    assert uu.view(np.uint32).tolist() == un.view(np.uint32).tolist()
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_compress_shared_matches_definition(orc, seed):
+    rng = np.random.default_rng(3200 + seed)
+    n = int(rng.integers(1, 2000))
+    off = _random_segments(rng, n)
+    g, u, v = (_tricky(rng, n, seed % 4) for _ in range(3))
+    k = int(rng.integers(0, n + 1))
+    idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+    leak = np.float32(rng.choice([1.0, 0.9]))
+    mask = bool(seed % 2)
+    p = orc.make_params(orc.SAMPLED, 0.999, 0.9, mask_momentum=mask, leak=leak)
+    un, vn = _exact_accumulate_leak(g, u, v, np.float32(0.9), leak)
+    uu, vv = u.copy(), v.copy()
+    rc, val = orc.compress_shared(g, uu, vv, off, p, idx)
+    assert rc == 0
+    assert [X.bits(x) for x in val] == [X.bits(vn[i]) for i in idx]
+    vn[idx] = 0.0
+    if mask:
+        un[idx] = 0.0
+    assert vv.view(np.uint32).tolist() == vn.view(np.uint32).tolist()
+    assert uu.view(np.uint32).tolist() == un.view(np.uint32).tolist()
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_compress_shared_at_own_selection_is_compress(orc, seed):
+    # the learner that chose S, sending at S, takes exactly the step dgc_compress takes
+    rng = np.random.default_rng(3300 + seed)
+    n = int(rng.integers(100, 5000))
+    off = _random_segments(rng, n)
+    p = orc.make_params([orc.EXACT, orc.SAMPLED, orc.ADACOMP][seed % 3], 0.99, 0.9, clip_norm=1.0,
+                        seed=seed, bin_size=50, leak=0.9)
+    g, u, v = (rng.standard_normal(n).astype(np.float32) for _ in range(3))
+    ua, va, ub, vb = u.copy(), v.copy(), u.copy(), v.copy()
+    idx, val, _ = orc.compress(g, ua, va, off, p)
+    rc, val2 = orc.compress_shared(g, ub, vb, off, p, idx)
+    assert rc == 0 and val.view(np.uint32).tolist() == val2.view(np.uint32).tolist()
+    assert np.array_equal(ua.view(np.uint32), ub.view(np.uint32))
+    assert np.array_equal(va.view(np.uint32), vb.view(np.uint32))
+
+
+def test_sum_shared_order_and_definition(orc):
+    rows = read_golden("decode_order.txt")  # 1e8, 1, -1e8 at one position: ordered sum 0
+    vals = [np.array([np.uint32(r[1][1])], np.uint32).view(np.float32) for r in rows
+            if r[0] == "learner"]
+    rc, out = orc.sum_shared(vals)
+    assert rc == 0 and X.bits(out[0]) == 0
+    rng = np.random.default_rng(7)
+    vals = [(rng.standard_normal(500) * 10.0 ** rng.integers(-3, 3, 500)).astype(np.float32)
+            for _ in range(9)]
+    exp = np.zeros(500, np.float32)
+    for a in vals:
+        exp = np.array([X.add_f32(x, y) for x, y in zip(exp, a)], np.float32)
+    rc, out = orc.sum_shared(vals)
+    assert rc == 0 and out.view(np.uint32).tolist() == exp.view(np.uint32).tolist()
+
+
+def test_shared_rejects(orc):
+    n = 50
+    g = np.ones(n, np.float32)
+    off = np.array([0, n])
+    for leak in (-0.5, 1.5, math.nan):
+        p = orc.make_params(orc.EXACT, 0.9, 0.9, leak=leak)
+        assert orc.compress_shared(g, np.zeros(n, np.float32), np.zeros(n, np.float32), off, p,
+                                   np.array([1], np.uint32))[0] == orc.EINVAL
+    p = orc.make_params(orc.EXACT, 0.9, 0.9)
+    for bad in ([3, 3], [4, 2], [n]):
+        u, v = np.zeros(n, np.float32), np.ones(n, np.float32)
+        assert orc.compress_shared(g, u, v, off, p, np.array(bad, np.uint32))[0] == orc.EINVAL
+        assert np.all(v == 1.0)  # nothing changes on a rejected call
+    with pytest.raises(RuntimeError):
+        orc.compress(g, np.zeros(n, np.float32), np.zeros(n, np.float32), off,
+                     orc.make_params(orc.EXACT, 0.9, 0.9, leak=1.5))
