@@ -306,6 +306,45 @@ class Pipeline:
                 "decode_ms": round(t_dec, 4), "decode_apply_ms": round(t_app, 4)}
 
 
+    def time_shared(self, p, g, learners=8, reps=20):
+        """One index set for all learners, outside the step: a learner's step at the last
+        step's set (dgc_compress_shared: the accumulate-only streaming pass, then the gather),
+        and the learner-ordered sum of `learners` value vectors (dgc_sum_shared)."""
+        import torch
+
+        dgc = self.dgc
+        E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        vals = [torch.empty(self.cap, dtype=torch.float32, device=self.dev)
+                for _ in range(learners)]
+
+        def timed(fn):
+            ms = []
+            for _ in range(reps + 3):
+                a, b = E(), E()
+                a.record()
+                fn()
+                b.record()
+                b.synchronize()
+                ms.append(a.elapsed_time(b))
+            return sorted(ms[3:])[reps // 2]
+
+        kev = (E(), E())
+        dgc.dgc_profile_stream_pass(*kev)  # the shared call marks its streaming pass too
+        t_step = timed(lambda: dgc.dgc_compress_shared(
+            g, self.u, self.v, self.seg, p, self.out_idx, self.out_count, vals[0], self.status,
+            self.ws, n=self.n, max_count=self.cap, ws_bytes=self.ws_bytes))
+        dgc.dgc_profile_stream_pass(None, None)
+        t_pass = kev[0].elapsed_time(kev[1])
+        ws = torch.empty(dgc.dgc_sum_shared_workspace(learners), dtype=torch.uint8,
+                         device=self.dev)
+        out = torch.empty(self.cap, dtype=torch.float32, device=self.dev)
+        t_sum = timed(lambda: dgc.dgc_sum_shared(vals, self.out_count, self.cap, out,
+                                                 self.status, ws))
+        del vals, out, ws
+        return {"compress_shared_ms": round(t_step, 4), "stream_pass_ms": round(t_pass, 4),
+                "sum_shared_ms": round(t_sum, 4), "learners": learners}
+
+
 def run_ours(args, world, rank, local):
     import numpy as np
     import torch
@@ -385,6 +424,10 @@ def run_ours(args, world, rank, local):
     quant = pipe.time_quant()
     if dgc.dgc_read_status(pipe.status) != 0:
         raise RuntimeError("integer-message calls reported an error")
+    shared = pipe.time_shared(p_main, pool[0])
+    if dgc.dgc_read_status(pipe.status) != 0:
+        raise RuntimeError("shared-set calls reported an error")
+    shared["stream_pass_frac"] = round(20.0 * n / (shared["stream_pass_ms"] / 1e3) / 1e9 / peak, 4)
     if dgc.dgc_read_status(pipe.status) != 0:
         raise RuntimeError("decode-apply reported an error")
 
@@ -413,6 +456,7 @@ def run_ours(args, world, rank, local):
                       "decode": round(t_decode, 4)},
         "decode_apply_ms": round(t_apply, 4),  # outside the step: message -> SGD step on w
         "quant": quant,  # outside the step: the same message as 8-bit integers
+        "shared": shared,  # outside the step: one index set for all learners
         "compress_gbs": round(4.0 * n / (t_compress / 1e3) / 1e9, 2),
         "message_bytes": int(statistics.median(nbytes)),
         "candidates": cand, "sent": int(st["sent"]),

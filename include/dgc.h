@@ -9,6 +9,9 @@
  *         bullets), Research questions (RQ4), Key findings.
  *   [ADA] "AdaComp : Adaptive Residual Gradient Compression for Data-Parallel Distributed
  *         Training": abstract and citation snippets.
+ *   [SC]  the ScaleComp abstract (Scalable Sparsified Gradient Compression) on the first page
+ *         of the sources, a taxoreview.com listing.
+ *   [INT] "IntSGD: Adaptive Floatless Compression of Stochastic Gradients": abstract.
  *
  * Conventions for every call:
  *   - All array arguments are DEVICE pointers unless marked "host". The caller owns every
@@ -58,7 +61,8 @@ enum { DGC_FLAG_MASK_MOMENTUM = 1u };
 /* Compressor settings. [DGC] Proposed method: momentum correction (momentum), local gradient
  * clipping (clip_norm), momentum factor masking (DGC_FLAG_MASK_MOMENTUM); [DGC] Abstract:
  * 99.9% sparsity; [DGC] RQ4: hierarchical thresholding (sample_ratio, reselect_factor);
- * [ADA] bin-local selection (bin_size). */
+ * [ADA] bin-local selection (bin_size); [SC] the low-pass filter in the local accumulation
+ * (leak). */
 typedef struct {
     uint32_t mode;          /* DGC_SELECT_EXACT, DGC_SELECT_SAMPLED or DGC_SELECT_ADACOMP */
     uint32_t flags;         /* DGC_FLAG_MASK_MOMENTUM: clear u where a value is sent */
@@ -69,7 +73,7 @@ typedef struct {
     double reselect_factor; /* sampled mode: exact re-selection when |C| > factor*k, in [1,16] */
     uint64_t seed;          /* sampled mode: seed of the sample positions */
     uint32_t bin_size;      /* AdaComp mode: entries per bin, >= 1 (sparsity is not used) */
-    uint32_t reserved;      /* 0 */
+    float leak;             /* v <- fma(leak, v, u), in [0, 1]; 0 means 1: DGC's plain sum */
 } dgc_params;
 
 /* Per-segment statistics of one dgc_compress call. */
@@ -151,6 +155,26 @@ int dgc_compress_noalloc(const float* g, float* u, float* v, int64_t n, const in
                          float* out_val, int64_t out_cap, int64_t* out_count,
                          dgc_seg_stats* stats, int32_t* status, dgc_stream_t stream);
 
+/* One index set for all learners. [SC] (the ScaleComp abstract, first page): a commutative
+ * compressor keeps each learner's traffic independent of the number of learners and works with
+ * all-reduce. This library's reading: every learner sends its accumulator at the same index set
+ * S, so the learners' value vectors add up position by position. Which learner chooses S is the
+ * caller's choice (for instance one learner in turn, with dgc_compress); the others then call
+ * dgc_compress_shared with that S, and dgc_sum_shared adds the value vectors.
+ *
+ * One step at the given S: clipping and accumulation exactly as dgc_compress (same params; mode,
+ * sparsity and the sample settings are not used), then out_val[j] = v[idx[j]] for j < *count,
+ * and each sent entry leaves the accumulator (v <- 0, u <- 0 with masking).
+ *   idx, count  device; idx strictly ascending and below n, 0 <= *count <= max_count, else
+ *               *status = DGC_EINVAL and u, v and out_val are left as they were
+ *   out_val     device, max_count binary32
+ *   ws          dgc_compress_workspace(n, nseg, params) bytes suffice
+ * Other arguments and errors as dgc_compress. */
+int dgc_compress_shared(const float* g, float* u, float* v, int64_t n, const int64_t* seg_off,
+                        int32_t nseg, const dgc_params* params, const uint32_t* idx,
+                        const int64_t* count, int64_t max_count, float* out_val, int32_t* status,
+                        void* ws, size_t ws_bytes, dgc_stream_t stream);
+
 /* ------------------------------------------------------------------------------ codec */
 
 /* Message format, [DGC] Proposed method, bullet 2 (each sent value a 32-bit word, each run of
@@ -179,7 +203,7 @@ int dgc_encode(const uint32_t* idx, const float* val, const int64_t* count, int6
 /* Integer-valued messages (version 2). [ADA] abstract: AdaComp sends the selected residues
  * sparse and quantized; the IntSGD page, abstract: each learner scales its vector by a number
  * every learner knows and rounds to integers, so no float crosses the wire. The pages give no
- * bit format; this library's reading:
+ * bit format ([INT] is the IntSGD abstract); this library's reading:
  *   q_j = clamp(rint(alpha * val_j), -Q, Q), Q = 2^(bits-1) - 1, bits 8 or 16: one binary32
  *         multiply, rounding half to even, NaN to 0;
  *   the residual takes back what q_j does not carry: v[idx_j] = val_j - (float)q_j / alpha
@@ -258,6 +282,18 @@ int dgc_decode_apply_quant(const uint8_t* const* streams, const uint64_t* stream
                            int32_t bits, float alpha, float* w, int64_t n, float lr,
                            int32_t* status, void* ws, size_t ws_bytes, dgc_stream_t stream);
 
+/* Workspace for dgc_sum_shared: the table of W pointers. */
+int dgc_sum_shared_workspace(int32_t W, size_t* bytes);
+
+/* The sum of W learners' value vectors over one shared index set, the step an all-reduce would
+ * take: out[j] = the learner-ordered sum from +0 of vals[w][j] (w = 0..W-1, one binary32 addition
+ * each, the order the decoders use), for j < *count (device int64, 0 <= *count <= max_count,
+ * else *status = DGC_EINVAL and out is not written).
+ *   vals  host array of W device pointers (4-byte aligned), each to *count binary32
+ *   out   device, max_count binary32; it may be one of vals only if that is vals[0] */
+int dgc_sum_shared(const float* const* vals, int32_t W, const int64_t* count, int64_t max_count,
+                   float* out, int32_t* status, void* ws, size_t ws_bytes, dgc_stream_t stream);
+
 /* -------------------------------------------------------------------------- utilities */
 
 /* Synchronize `stream`, then return the int32 at status_dev (or DGC_ECUDA). */
@@ -269,8 +305,8 @@ const char* dgc_status_string(int code);
 /* Number of kernels this library has launched in this process (all calls, all threads). */
 uint64_t dgc_launch_count(void);
 
-/* Profiling hook for benchmarks: while begin and end are non-NULL, every dgc_compress call
- * records `begin` on its stream right before its streaming pass (the accumulate-and-compact
+/* Profiling hook for benchmarks: while begin and end are non-NULL, every dgc_compress and
+ * dgc_compress_shared call records `begin` on its stream right before its streaming pass (the
  * kernel that touches all n entries) and `end` right after it. dgc_profile_stream_pass(NULL,
  * NULL) turns it off. The setting is process-wide and not synchronized between threads. */
 typedef struct CUevent_st* dgc_event_t; /* the same type as cudaEvent_t */

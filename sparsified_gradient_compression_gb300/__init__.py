@@ -19,7 +19,8 @@ __all__ = [
     "dgc_encode_max_bytes", "dgc_encode_workspace", "dgc_encode",
     "dgc_decode_workspace", "dgc_decode_accumulate", "dgc_decode_apply",
     "dgc_encode_quant", "dgc_decode_workspace_quant", "dgc_decode_accumulate_quant",
-    "dgc_decode_apply_quant",
+    "dgc_decode_apply_quant", "dgc_compress_shared", "dgc_sum_shared_workspace",
+    "dgc_sum_shared",
     "dgc_read_status", "dgc_status_string", "dgc_launch_count", "dgc_selftest_wait_timeout",
     "dgc_profile_stream_pass",
     "SELECT_EXACT", "SELECT_SAMPLED", "SELECT_ADACOMP", "FLAG_MASK_MOMENTUM",
@@ -41,7 +42,7 @@ class dgc_params(ctypes.Structure):
         ("reselect_factor", ctypes.c_double),
         ("seed", ctypes.c_uint64),
         ("bin_size", ctypes.c_uint32),
-        ("reserved", ctypes.c_uint32),
+        ("leak", ctypes.c_float),
     ]
 
 
@@ -99,6 +100,10 @@ def lib():
         L.dgc_decode_accumulate_quant.argtypes = [vp, vp, i32, i32, f32, vp, i64, i32, vp, vp, sz,
                                                   vp]
         L.dgc_decode_apply_quant.argtypes = [vp, vp, i32, i32, f32, vp, i64, f32, vp, vp, sz, vp]
+        L.dgc_compress_shared.argtypes = [vp, vp, vp, i64, vp, i32, P(dgc_params), vp, vp, i64,
+                                          vp, vp, vp, sz, vp]
+        L.dgc_sum_shared_workspace.argtypes = [i32, P(sz)]
+        L.dgc_sum_shared.argtypes = [vp, i32, vp, i64, vp, vp, vp, sz, vp]
         L.dgc_read_status.argtypes = [vp, vp]
         L.dgc_status_string.argtypes = [ctypes.c_int]
         L.dgc_status_string.restype = ctypes.c_char_p
@@ -113,6 +118,7 @@ def lib():
                   "dgc_decode_workspace", "dgc_decode_accumulate", "dgc_decode_apply",
                   "dgc_encode_quant", "dgc_decode_workspace_quant",
                   "dgc_decode_accumulate_quant", "dgc_decode_apply_quant",
+                  "dgc_compress_shared", "dgc_sum_shared_workspace", "dgc_sum_shared",
                   "dgc_read_status",
                   "dgc_selftest_wait_timeout"):
             getattr(L, f).restype = ctypes.c_int
@@ -154,10 +160,11 @@ def _stream(stream) -> int | None:
 
 def make_params(mode=SELECT_EXACT, sparsity=0.999, momentum=0.9, clip_norm=0.0,
                 mask_momentum=True, sample_ratio=0.01, reselect_factor=1.3, seed=0,
-                bin_size=1000) -> dgc_params:
+                bin_size=1000, leak=0.0) -> dgc_params:
     return dgc_params(int(mode), FLAG_MASK_MOMENTUM if mask_momentum else 0, float(sparsity),
                       float(momentum), float(clip_norm), float(sample_ratio),
-                      float(reselect_factor), int(seed) & (2**64 - 1), int(bin_size), 0)
+                      float(reselect_factor), int(seed) & (2**64 - 1), int(bin_size),
+                      float(leak))
 
 
 # --------------------------------------------------------------------------- compressor
@@ -314,6 +321,38 @@ def dgc_decode_apply_quant(streams, stream_bytes, bits: int, alpha: float, w, n:
         ctypes.cast(ptrs, ctypes.c_void_p), ctypes.cast(sizes, ctypes.c_void_p), W, int(bits),
         float(alpha), _ptr(w), int(n), float(lr), _ptr(status), _ptr(ws), int(ws_bytes),
         _stream(stream)), "dgc_decode_apply_quant")
+
+
+def dgc_compress_shared(g, u, v, seg_off, params: dgc_params, idx, count, out_val, status, ws,
+                        n: int | None = None, max_count: int | None = None,
+                        ws_bytes: int | None = None, stream=None) -> int:
+    """One learner's step at a shared index set idx (device, ascending), count device int64."""
+    n = g.numel() if n is None else n
+    nseg = seg_off.numel() - 1
+    max_count = idx.numel() if max_count is None else max_count
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    return _check(lib().dgc_compress_shared(_ptr(g), _ptr(u), _ptr(v), int(n), _ptr(seg_off),
+                                            int(nseg), ctypes.byref(params), _ptr(idx),
+                                            _ptr(count), int(max_count), _ptr(out_val),
+                                            _ptr(status), _ptr(ws), int(ws_bytes),
+                                            _stream(stream)), "dgc_compress_shared")
+
+
+def dgc_sum_shared_workspace(W: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().dgc_sum_shared_workspace(int(W), ctypes.byref(out)), "dgc_sum_shared_workspace")
+    return out.value
+
+
+def dgc_sum_shared(vals, count, max_count: int, out, status, ws, ws_bytes: int | None = None,
+                   stream=None) -> int:
+    """vals: list of device addresses or float32 CUDA tensors (the learners, in order)."""
+    W = len(vals)
+    ptrs = (ctypes.c_void_p * max(W, 1))(*[_ptr(x) for x in vals])
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    return _check(lib().dgc_sum_shared(ctypes.cast(ptrs, ctypes.c_void_p), W, _ptr(count),
+                                       int(max_count), _ptr(out), _ptr(status), _ptr(ws),
+                                       int(ws_bytes), _stream(stream)), "dgc_sum_shared")
 
 
 # ----------------------------------------------------------------------------- utilities

@@ -505,6 +505,25 @@ __global__ void __launch_bounds__(kThreads) k_dec_scatter1(DecArgs a) {
         a.dense[p] = __fadd_rn(a.dense[p], x);
 }
 
+// ---------------------------------------------------------------- shared-set sums
+// out[j] = ((+0 + vals[0][j]) + vals[1][j]) + ... : the learners in order, as the decoders add
+// them. Consecutive threads read consecutive entries of each learner's vector.
+__global__ void __launch_bounds__(kThreads) k_sum_shared(const float* const* vals, int32_t W,
+                                                        const int64_t* count, uint64_t max_count,
+                                                        float* out, int32_t* status) {
+    const int64_t c = *count;
+    if (c < 0 || (uint64_t)c > max_count) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) report(status, DGC_EINVAL);
+        return;
+    }
+    for (uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x; j < (uint64_t)c;
+         j += (uint64_t)gridDim.x * kThreads) {
+        float acc = 0.0f;
+        for (int32_t w = 0; w < W; ++w) acc = __fadd_rn(acc, vals[w][j]);
+        out[j] = acc;
+    }
+}
+
 struct DecLayout {
     size_t ctl, tab, bad, pos, st, ts, total;
     uint64_t sum_T, nchunks, ntiles;
@@ -787,4 +806,42 @@ extern "C" int dgc_decode_apply_quant(const uint8_t* const* streams, const uint6
     if (rc) return rc;
     return decode_impl(streams, stream_bytes, W, w, n, 0, 1, lr, bits, alpha, status, ws,
                        ws_bytes, stream);
+}
+
+extern "C" int dgc_sum_shared_workspace(int32_t W, size_t* bytes) {
+    if (!bytes || W < 0) return DGC_EINVAL;
+    *bytes = align256(sizeof(float*) * (size_t)(W > 0 ? W : 1));
+    return DGC_OK;
+}
+
+extern "C" int dgc_sum_shared(const float* const* vals, int32_t W, const int64_t* count,
+                              int64_t max_count, float* out, int32_t* status, void* ws,
+                              size_t ws_bytes, dgc_stream_t stream) {
+    if (W < 0 || max_count < 0 || !count || !status || !ws) return DGC_EINVAL;
+    if (max_count > 0 && !out) return DGC_EINVAL;
+    if (W > 0 && !vals) return DGC_EINVAL;
+    for (int w = 0; w < W; ++w)
+        if (!vals[w] || ((uintptr_t)vals[w] & 3u) != 0) return DGC_EINVAL;
+    if (((uintptr_t)ws & 255u) != 0) return DGC_EINVAL;
+    size_t need;
+    dgc_sum_shared_workspace(W, &need);
+    if (ws_bytes < need) return DGC_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the pointer table goes to the device with the call (a pageable copy: staged before this
+    // function returns, so the host array may go away)
+    if (W > 0 && cudaMemcpyAsync(ws, vals, sizeof(float*) * (size_t)W, cudaMemcpyHostToDevice,
+                                 s) != cudaSuccess)
+        return DGC_ECUDA;
+    const int sms = dgc_internal_sm_count();
+    if (sms <= 0) return DGC_ECUDA;
+    const unsigned grid = (unsigned)std::max<uint64_t>(
+        1, std::min<uint64_t>((uint64_t)sms * 8, ((uint64_t)max_count + kThreads - 1) / kThreads));
+    k_sum_shared<<<grid, kThreads, 0, s>>>(static_cast<const float* const*>(ws), W, count,
+                                           (uint64_t)max_count, out, status);
+    dgc_internal_count_launches(1);
+    if (cudaPeekAtLastError() != cudaSuccess) {
+        cudaGetLastError();
+        return DGC_ECUDA;
+    }
+    return DGC_OK;
 }

@@ -136,6 +136,7 @@ struct HostParams {
     float momentum, clip_norm;
     uint64_t seed;
     float bin_inv;  // AdaComp: 1/bin rounded to binary32 (used while bin < the tile length)
+    float leak;     // v <- fma(leak, v, u); 1 is the plain sum
 };
 
 int check_params(const dgc_params* p, HostParams* hp) {
@@ -149,6 +150,8 @@ int check_params(const dgc_params* p, HostParams* hp) {
     if (!(p->sparsity >= 0.0 && p->sparsity <= 1.0)) return DGC_EINVAL;
     if (!std::isfinite(p->momentum)) return DGC_EINVAL;
     if (std::isnan(p->clip_norm)) return DGC_EINVAL;
+    if (!(p->leak >= 0.0f && p->leak <= 1.0f)) return DGC_EINVAL;
+    hp->leak = p->leak == 0.0f ? 1.0f : p->leak;  // 0: no filter
     hp->mode = p->mode;
     hp->mask = (p->flags & DGC_FLAG_MASK_MOMENTUM) ? 1u : 0u;
     hp->clip_on = (p->clip_norm > 0.0f && !std::isinf(p->clip_norm)) ? 1u : 0u;
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
             s_bad = (a.seg_off[0] != 0 || a.seg_off[a.nseg] != (int64_t)a.n) ? 1 : 0;
             Ctl c{};
             *a.ctl = c;
-            *a.out_count = 0;
+            if (a.out_count) *a.out_count = 0;
         }
         __syncthreads();
         uint32_t active = 0;
@@ -435,10 +438,12 @@ __global__ void k_clip_scale(Args a) {
     d.scale = (norm > c) ? (float)(c / norm) : 1.0f;
 }
 
-__device__ __forceinline__ void accumulate(float g, float& u, float& v, float m, float scale) {
+// v <- fma(leak, v, u): with leak = 1 this is the plain sum v + u, rounded once
+__device__ __forceinline__ void accumulate(float g, float& u, float& v, float m, float scale,
+                                           float leak) {
     const float gp = (scale != 1.0f) ? __fmul_rn(g, scale) : g;
     u = __fmaf_rn(m, u, gp);
-    v = __fadd_rn(v, u);
+    v = __fmaf_rn(leak, v, u);
 }
 
 // ----------------------------------------------------------------------- histograms
@@ -619,7 +624,7 @@ __global__ void __launch_bounds__(kThreads) k_sample(Args a) {
         if (sg[r] < 0) continue;
         const uint64_t jg = chunk0 + r * kThreads + threadIdx.x;
         float uu = uv[r], vn = vv[r];
-        accumulate(gv[r], uu, vn, a.hp.momentum, a.segs[sg[r]].scale);
+        accumulate(gv[r], uu, vn, a.hp.momentum, a.segs[sg[r]].scale, a.hp.leak);
         const uint32_t key = key_of(vn);
         a.skeys[jg] = key;
         const uint32_t bin = key >> 20;
@@ -909,7 +914,7 @@ __device__ __forceinline__ void stream_compute(const Args& a, const float* sg, u
                 scale = d.scale;
                 t = d.thresh;
             }
-            accumulate(gp[e], up[e], vp[e], a.hp.momentum, scale);
+            accumulate(gp[e], up[e], vp[e], a.hp.momentum, scale, a.hp.leak);
             if (key_of(vp[e]) >= t) flags |= 1u << (4 * r + e);
         }
         if (kKeepU) uu[r] = u4;
@@ -920,7 +925,7 @@ __device__ __forceinline__ void stream_compute(const Args& a, const float* sg, u
 // kSel 0: candidates are the entries at or above the segment's threshold key (DGC). kSel 1
 // (AdaComp): candidates are the entries at the largest key of their bin within the tile; the
 // tile also raises each bin's global maximum, and the emit step keeps the candidates that
-// reach it.
+// reach it. kSel 2 (a shared index set given by the caller): the pass only accumulates.
 template <int kSel>
 __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) {
     extern __shared__ __align__(128) float s_stage[];  // [kPStages][3][kPTile]
@@ -1010,6 +1015,7 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
         uint32_t flags;
         stream_compute<true>(a, s_stage + (size_t)st * kPStageFloats, base, len, s_uniform[st],
                              s_scale[st], s_thresh[st], uu, vv, flags);
+        if constexpr (kSel == 2) flags = 0;  // the shared set is given: no candidates
         if constexpr (kSel == 1) {  // bin-local maxima of this tile, then the candidates that reach them
             // entries past len hold v = 0 (key 0): they raise no maximum and are never candidates
             const uint32_t binA = s_binA[st], L = a.hp.bin;
@@ -1420,6 +1426,47 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
     }
 }
 
+// ------------------------------------------------------------------ shared index set
+// A learner that sends at an index set chosen elsewhere (one set for all learners, so their
+// messages add up position by position). The set is checked before anything changes: strictly
+// ascending, below n, and count within [0, max_count]; otherwise the call reports DGC_EINVAL and
+// the abort flag stops every later kernel of the call.
+__global__ void __launch_bounds__(kThreads) k_shared_check(Args a, const uint32_t* idx,
+                                                          const int64_t* count,
+                                                          uint64_t max_count) {
+    const int64_t c = *count;
+    if (c < 0 || (uint64_t)c > max_count) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            report(a.status, DGC_EINVAL);
+            atomicExch(&a.ctl->abort, 1);
+        }
+        return;
+    }
+    bool bad = false;
+    for (uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x; j < (uint64_t)c;
+         j += (uint64_t)gridDim.x * kThreads)
+        if (idx[j] >= a.n || (j > 0 && idx[j - 1] >= idx[j])) bad = true;
+    if (__syncthreads_or(bad) && threadIdx.x == 0) {
+        report(a.status, DGC_EINVAL);
+        atomicExch(&a.ctl->abort, 1);
+    }
+}
+
+// After the accumulate-only pass: out_val[j] = v[idx[j]], then the entry leaves the accumulator
+// (v <- 0; u <- 0 with momentum factor masking).
+__global__ void __launch_bounds__(kThreads) k_shared_gather(Args a, const uint32_t* idx,
+                                                           const int64_t* count, float* out_val) {
+    if (ld_relaxed_u32((const uint32_t*)&a.ctl->abort)) return;
+    const uint64_t c = (uint64_t)*count;
+    for (uint64_t j = (uint64_t)blockIdx.x * kThreads + threadIdx.x; j < c;
+         j += (uint64_t)gridDim.x * kThreads) {
+        const uint32_t i = idx[j];
+        out_val[j] = a.v[i];
+        a.v[i] = 0.0f;
+        if (a.hp.mask) a.u[i] = 0.0f;
+    }
+}
+
 }  // namespace
 }  // namespace dgc
 
@@ -1456,26 +1503,11 @@ extern "C" int dgc_compress_max_out(int64_t n, int32_t nseg, const dgc_params* p
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* seg_off,
-                            int32_t nseg, const dgc_params* params, uint32_t* out_idx,
-                            float* out_val, int64_t out_cap, int64_t* out_count,
-                            dgc_seg_stats* stats, int32_t* status, void* ws, size_t ws_bytes,
-                            dgc_stream_t stream) {
-    HostParams hp;
-    if (n < 0 || nseg < 1) return DGC_EINVAL;
-    if (n > 0xFFFFFFFFll || nseg > (1 << 28)) return DGC_EUNSUPPORTED;
-    int rc = check_params(params, &hp);
-    if (rc) return rc;
-    if (!seg_off || !out_count || !status || !ws) return DGC_EINVAL;
-    if (n > 0 && (!g || !u || !v || !aligned16(g) || !aligned16(u) || !aligned16(v)))
-        return DGC_EINVAL;
-    if (((uintptr_t)ws & 255u) != 0) return DGC_EINVAL;
-    const Layout L = make_layout(n, nseg, hp);
-    if (ws_bytes < L.total) return DGC_EINVAL;
-    const uint64_t mo = max_out_for(n, nseg, hp);
-    if (out_cap < 0 || (uint64_t)out_cap < mo) return DGC_ECAPACITY;
-    if (mo > 0 && (!out_idx || !out_val)) return DGC_EINVAL;
-
+namespace dgc {
+namespace {
+// The kernels' view of one call: caller buffers and the workspace carved by the layout L.
+Args make_args(const float* g, float* u, float* v, int64_t n, const int64_t* seg_off,
+               int32_t nseg, const HostParams& hp, const Layout& L, void* ws, int32_t* status) {
     char* w = static_cast<char*>(ws);
     Args a{};
     a.g = g;
@@ -1485,11 +1517,6 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     a.nseg = nseg;
     a.seg_off = seg_off;
     a.hp = hp;
-    a.out_idx = out_idx;
-    a.out_val = out_val;
-    a.out_cap = (uint64_t)out_cap;
-    a.out_count = out_count;
-    a.stats = stats;
     a.status = status;
     a.ctl = reinterpret_cast<Ctl*>(w + L.ctl);
     a.scache = reinterpret_cast<SampleCache*>(w + L.scache);
@@ -1520,6 +1547,66 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     a.emit_tiles = L.emit_tiles;
     a.max_clip_tiles = L.max_clip_tiles;
     a.spin_limit = kDefaultSpinLimit;
+    return a;
+}
+
+template <int kSel>
+void stream_attributes() {
+    cudaFuncSetAttribute(k_stream_tma<kSel>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kPSmemBytes);
+    // the AdaComp variant needs nearly all of the SM's shared memory for two blocks
+    cudaFuncSetAttribute(k_stream_tma<kSel>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         (int)cudaSharedmemCarveoutMaxShared);
+}
+
+// The streaming pass: persistent blocks, kPBlocksPerSM per SM (at most one per tile).
+void launch_stream_pass(int sel, const Args& a, uint64_t ptiles, int sms, cudaStream_t s) {
+    static bool attr_set[128] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 128 && !attr_set[dev]) {
+        stream_attributes<0>();
+        stream_attributes<1>();
+        stream_attributes<2>();
+        attr_set[dev] = true;
+    }
+    const unsigned pgrid = (unsigned)std::min<uint64_t>((uint64_t)sms * kPBlocksPerSM, ptiles);
+    if (sel == 1)
+        k_stream_tma<1><<<pgrid, kThreads, kPSmemBytes, s>>>(a);
+    else if (sel == 2)
+        k_stream_tma<2><<<pgrid, kThreads, kPSmemBytes, s>>>(a);
+    else
+        k_stream_tma<0><<<pgrid, kThreads, kPSmemBytes, s>>>(a);
+}
+}  // namespace
+}  // namespace dgc
+
+extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* seg_off,
+                            int32_t nseg, const dgc_params* params, uint32_t* out_idx,
+                            float* out_val, int64_t out_cap, int64_t* out_count,
+                            dgc_seg_stats* stats, int32_t* status, void* ws, size_t ws_bytes,
+                            dgc_stream_t stream) {
+    HostParams hp;
+    if (n < 0 || nseg < 1) return DGC_EINVAL;
+    if (n > 0xFFFFFFFFll || nseg > (1 << 28)) return DGC_EUNSUPPORTED;
+    int rc = check_params(params, &hp);
+    if (rc) return rc;
+    if (!seg_off || !out_count || !status || !ws) return DGC_EINVAL;
+    if (n > 0 && (!g || !u || !v || !aligned16(g) || !aligned16(u) || !aligned16(v)))
+        return DGC_EINVAL;
+    if (((uintptr_t)ws & 255u) != 0) return DGC_EINVAL;
+    const Layout L = make_layout(n, nseg, hp);
+    if (ws_bytes < L.total) return DGC_EINVAL;
+    const uint64_t mo = max_out_for(n, nseg, hp);
+    if (out_cap < 0 || (uint64_t)out_cap < mo) return DGC_ECAPACITY;
+    if (mo > 0 && (!out_idx || !out_val)) return DGC_EINVAL;
+
+    Args a = make_args(g, u, v, n, seg_off, nseg, hp, L, ws, status);
+    a.out_idx = out_idx;
+    a.out_val = out_val;
+    a.out_cap = (uint64_t)out_cap;
+    a.out_count = out_count;
+    a.stats = stats;
 
     const int sms = dgc_internal_sm_count();
     if (sms <= 0) return DGC_ECUDA;
@@ -1558,27 +1645,7 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     const cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
     if (pb && pe) cudaEventRecord(pb, s);
     if (n > 0) {
-        static bool attr_set[128] = {false};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev >= 0 && dev < 128 && !attr_set[dev]) {
-            cudaFuncSetAttribute(k_stream_tma<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kPSmemBytes);
-            cudaFuncSetAttribute(k_stream_tma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kPSmemBytes);
-            // the AdaComp variant needs nearly all of the SM's shared memory for two blocks
-            cudaFuncSetAttribute(k_stream_tma<0>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxShared);
-            cudaFuncSetAttribute(k_stream_tma<1>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxShared);
-            attr_set[dev] = true;
-        }
-        const unsigned pgrid =
-            (unsigned)std::min<uint64_t>((uint64_t)sms * kPBlocksPerSM, L.ptiles);
-        if (hp.mode == DGC_SELECT_ADACOMP)
-            k_stream_tma<1><<<pgrid, kThreads, kPSmemBytes, s>>>(a);
-        else
-            k_stream_tma<0><<<pgrid, kThreads, kPSmemBytes, s>>>(a);
+        launch_stream_pass(hp.mode == DGC_SELECT_ADACOMP ? 1 : 0, a, L.ptiles, sms, s);
         ++launches;
     }
     if (pb && pe) cudaEventRecord(pe, s);
@@ -1595,6 +1662,67 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     const unsigned emit_grid = (unsigned)std::max<uint64_t>(
         1, std::min<uint64_t>((uint64_t)sms * 4, L.emit_tiles));
     L1(k_emit, emit_grid, kThreads, a);
+    dgc_internal_count_launches(launches);
+    if (cudaPeekAtLastError() != cudaSuccess) {
+        cudaGetLastError();
+        return DGC_ECUDA;
+    }
+    return DGC_OK;
+}
+
+extern "C" int dgc_compress_shared(const float* g, float* u, float* v, int64_t n,
+                                   const int64_t* seg_off, int32_t nseg, const dgc_params* params,
+                                   const uint32_t* idx, const int64_t* count, int64_t max_count,
+                                   float* out_val, int32_t* status, void* ws, size_t ws_bytes,
+                                   dgc_stream_t stream) {
+    HostParams hp;
+    if (n < 0 || nseg < 1 || max_count < 0) return DGC_EINVAL;
+    if (n > 0xFFFFFFFFll || nseg > (1 << 28)) return DGC_EUNSUPPORTED;
+    int rc = check_params(params, &hp);
+    if (rc) return rc;
+    // no selection: every segment's k is 0, so the plan draws no sample and counts no bin
+    hp.mode = DGC_SELECT_EXACT;
+    hp.d_ppb = 0;
+    hp.bin = 0;
+    if (!seg_off || !count || !status || !ws) return DGC_EINVAL;
+    if (max_count > 0 && (!idx || !out_val)) return DGC_EINVAL;
+    if (n > 0 && (!g || !u || !v || !aligned16(g) || !aligned16(u) || !aligned16(v)))
+        return DGC_EINVAL;
+    if (((uintptr_t)ws & 255u) != 0) return DGC_EINVAL;
+    const Layout L = make_layout(n, nseg, hp);
+    if (ws_bytes < L.total) return DGC_EINVAL;
+    Args a = make_args(g, u, v, n, seg_off, nseg, hp, L, ws, status);
+    a.out_count = nullptr;  // the count is the caller's input here
+
+    const int sms = dgc_internal_sm_count();
+    if (sms <= 0) return DGC_ECUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint64_t launches = 0;
+    auto L1 = [&](auto kernel, unsigned grid, unsigned block, auto... args) {
+        if (grid == 0) return;
+        kernel<<<grid, block, 0, s>>>(args...);
+        ++launches;
+    };
+    const size_t zero_work = (size_t)nseg * kHistBins + L.fused_tiles + L.emit_tiles +
+                             L.nbuckets + L.max_bins + 2;
+    const unsigned plan_grid = (unsigned)std::min<size_t>((zero_work + 1023) / 1024 + 1,
+                                                          (size_t)sms * 2);
+    const unsigned jgrid = (unsigned)std::max<uint64_t>(
+        1, std::min<uint64_t>((uint64_t)sms * 4, ((uint64_t)max_count + kThreads - 1) / kThreads));
+    L1(k_plan, plan_grid, 1024, a);
+    L1(k_shared_check, jgrid, kThreads, a, idx, count, (uint64_t)max_count);
+    if (hp.clip_on) {
+        L1(k_clip_tiles, (unsigned)L.max_clip_tiles, kThreads, a);
+        L1(k_clip_scale, (unsigned)((nseg + 255) / 256), 256, a);
+    }
+    const cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
+    if (pb && pe) cudaEventRecord(pb, s);
+    if (n > 0) {
+        launch_stream_pass(2, a, L.ptiles, sms, s);
+        ++launches;
+    }
+    if (pb && pe) cudaEventRecord(pe, s);
+    L1(k_shared_gather, jgrid, kThreads, a, idx, count, out_val);
     dgc_internal_count_launches(launches);
     if (cudaPeekAtLastError() != cudaSuccess) {
         cudaGetLastError();

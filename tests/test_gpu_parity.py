@@ -765,3 +765,144 @@ def test_quant_after_compress_matches_oracle():
         assert rc == 0 and enc.message() == omsg
         assert same_bits(host_f32(v_d), v_h), f"step {t}"
         assert same_bits(host_f32(u_d), u_h)
+
+
+# ---------------------------------------------------- ScaleComp: leak and one shared index set
+@pytest.mark.parametrize("case", range(9))
+def test_leak_all_modes(case):
+    rng = np.random.default_rng(4000 + case)
+    n = EDGE_N[case % len(EDGE_N)] * 3
+    off = _segments(rng, n)
+    mode = [dgc.SELECT_EXACT, dgc.SELECT_SAMPLED, dgc.SELECT_ADACOMP][case % 3]
+    leak = float(np.float32(rng.choice([0.5, 0.9, 0.999])))
+    run_steps(lambda t: (np.random.default_rng([case, t]).standard_normal(n) * 0.01)
+              .astype(np.float32), off, 3, mode=mode, sparsity=0.99, momentum=0.9, bin_size=64,
+              clip_norm=float(rng.choice([0.0, 1.0])), leak=leak)
+
+
+class Shared:
+    """dgc_compress_shared for one (n, segments, params) shape."""
+
+    def __init__(self, n, seg_off, params, max_count):
+        self.n, self.params, self.max_count = n, params, max(int(max_count), 1)
+        self.seg = torch.from_numpy(np.asarray(seg_off, np.int64)).cuda()
+        self.ws = torch.empty(max(dgc.dgc_compress_workspace(n, self.seg.numel() - 1, params), 256),
+                              dtype=torch.uint8, device="cuda")
+        self.out = torch.zeros(self.max_count, dtype=torch.float32, device="cuda")
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def __call__(self, g, u, v, idx, count):
+        dgc.dgc_compress_shared(g, u, v, self.seg, self.params, idx, count, self.out,
+                                self.status, self.ws, n=self.n, max_count=self.max_count)
+        return dgc.dgc_read_status(self.status)
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_compress_shared_random_sets(case):
+    rng = np.random.default_rng(4100 + case)
+    n = EDGE_N[case % len(EDGE_N)] * (1 + case % 3)
+    off = _segments(rng, n)
+    kw = dict(mode=dgc.SELECT_SAMPLED, momentum=0.9, mask_momentum=bool(case % 2),
+              clip_norm=float(rng.choice([0.0, 1.0])), leak=float(np.float32(rng.choice([0, 0.9]))))
+    pd, po = params_pair(**kw)
+    u_h, v_h = (rng.standard_normal(n).astype(np.float32) for _ in range(2))
+    u_d, v_d = dev_f32(u_h), dev_f32(v_h)
+    sh = Shared(n, off, pd, n)
+    for t in range(3):
+        g = (rng.standard_normal(n) * 0.01).astype(np.float32)
+        k = int(rng.integers(0, n + 1))
+        idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+        rc = sh(dev_f32(g), u_d, v_d, dev_idx(idx), torch.tensor([k], dtype=torch.int64,
+                                                                device="cuda"))
+        assert rc == 0
+        orc_rc, oval = oracle.compress_shared(g, u_h, v_h, off, po, idx)
+        assert orc_rc == 0
+        assert same_bits(host_f32(sh.out)[:k], oval)
+        assert same_bits(host_f32(v_d), v_h) and same_bits(host_f32(u_d), u_h), t
+
+
+def test_compress_shared_rejects_bad_sets():
+    n = 5000
+    off = np.array([0, n])
+    pd = dgc.make_params(mode=dgc.SELECT_EXACT)
+    sh = Shared(n, off, pd, 8)
+    for idx, count in (([3, 3, 9], 3), ([9, 3], 2), ([1, n], 2), ([1, 2], 9), ([1, 2], -1)):
+        u = dev_f32(np.ones(n, np.float32))
+        v = dev_f32(np.ones(n, np.float32))
+        sh.out.fill_(7.0)
+        rc = sh(dev_f32(np.ones(n, np.float32)), u, v, dev_idx(np.array(idx + [0] * 8, np.uint32)),
+                torch.tensor([count], dtype=torch.int64, device="cuda"))
+        assert rc == dgc.EINVAL
+        assert torch.all(u == 1.0) and torch.all(v == 1.0) and torch.all(sh.out == 7.0)
+
+
+def _sum_shared(vals, count=None, max_count=None):
+    k = vals[0].size if vals else 0
+    d = [dev_f32(np.append(x, np.float32(0))) for x in vals]
+    out = torch.full((max(k, 1),), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(dgc.dgc_sum_shared_workspace(len(vals)), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    c = torch.tensor([k if count is None else count], dtype=torch.int64, device="cuda")
+    dgc.dgc_sum_shared(d, c, k if max_count is None else max_count, out, status, ws)
+    return dgc.dgc_read_status(status), host_f32(out)[:k]
+
+
+def test_sum_shared_matches_oracle():
+    rows = read_golden("decode_order.txt")  # 1e8 + 1 - 1e8 in learner order is exactly 0
+    vals = [np.array([v[1]], np.uint32).view(np.float32) for t, v in rows if t == "learner"]
+    rc, out = _sum_shared(vals)
+    assert rc == 0 and int(out.view(np.uint32)[0]) == 0
+    rng = np.random.default_rng(8)
+    for W, k in ((1, 1000), (7, 123_457), (64, 25_558)):
+        vals = [(rng.standard_normal(k) * 10.0 ** rng.integers(-3, 3, k)).astype(np.float32)
+                for _ in range(W)]
+        rc, out = _sum_shared(vals)
+        orc_rc, oout = oracle.sum_shared(vals)
+        assert rc == 0 and orc_rc == 0 and same_bits(out, oout)
+    rc, out = _sum_shared([np.ones(10, np.float32)], count=11, max_count=10)
+    assert rc == dgc.EINVAL and np.all(np.isnan(out))
+
+
+def test_scalecomp_learners_rotating_chooser():
+    _scalecomp_learners(4, 1_000_003, np.array([0, 300_000, 1_000_003]), 4)
+
+
+@pytest.mark.slow
+def test_scalecomp_learners_full_size():
+    # eight learners of the aggregation workload's size (25,557,032 entries), two steps
+    _scalecomp_learners(8, 25_557_032, np.array([0, 25_557_032]), 2)
+
+
+def _scalecomp_learners(W, n, off, steps):
+    # W learners, one shared set per step chosen by learner t mod W with the sampled compressor,
+    # the others sending at that set, the value vectors summed: against the oracle run alike
+    kw = dict(mode=dgc.SELECT_SAMPLED, sparsity=0.999, momentum=0.9, seed=11, leak=0.9)
+    pd, po = params_pair(**kw)
+    comp = Compressor(n, off, pd)
+    sh = Shared(n, off, pd, comp.cap)
+    state_h = [[np.zeros(n, np.float32), np.zeros(n, np.float32)] for _ in range(W)]
+    state_d = [[dev_f32(a), dev_f32(b)] for a, b in state_h]
+    for t in range(steps):
+        grads = [(np.random.default_rng([9, t, w]).standard_normal(n) * 0.01).astype(np.float32)
+                 for w in range(W)]
+        lead = t % W
+        comp(dev_f32(grads[lead]), *state_d[lead])
+        assert comp.status_code() == 0
+        idx, val, _ = comp.results()
+        oidx, oval, _ = oracle.compress(grads[lead], *state_h[lead], off, po)
+        assert np.array_equal(idx, oidx) and same_bits(val, oval)
+        vals_d, vals_o = [None] * W, [None] * W
+        vals_d[lead], vals_o[lead] = val, oval
+        for w in range(W):
+            if w == lead:
+                continue
+            assert sh(dev_f32(grads[w]), *state_d[w], comp.out_idx, comp.out_count) == 0
+            vals_d[w] = host_f32(sh.out)[: idx.size].copy()
+            rc, vals_o[w] = oracle.compress_shared(grads[w], *state_h[w], off, po, oidx)
+            assert rc == 0 and same_bits(vals_d[w], vals_o[w])
+        rc, total = _sum_shared(vals_d)
+        orc_rc, ototal = oracle.sum_shared(vals_o)
+        assert rc == 0 and orc_rc == 0 and same_bits(total, ototal)
+        for w in range(W):
+            assert same_bits(host_f32(state_d[w][1]), state_h[w][1]), (t, w)
+            assert same_bits(host_f32(state_d[w][0]), state_h[w][0]), (t, w)
