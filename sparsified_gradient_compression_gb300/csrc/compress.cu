@@ -472,8 +472,9 @@ struct BlockHist {
 // sorted by 1024-entry bucket (segment by segment, so each segment's samples stay together), with
 // a tag of what they depend on and a checksum of the array. Every call re-checks both (one read
 // of the array) and rebuilds the cache when either differs -- a workspace that was reused for
-// something else, or a new seed or layout, costs one counting sort. The order of positions inside
-// a bucket depends on atomics, but the threshold only depends on the multiset of sampled keys.
+// something else, or a new seed or layout, costs one counting sort by bucket and a sort inside
+// each bucket, so the cached array is the sample positions in ascending order, segment by
+// segment. (The threshold only depends on the multiset of sampled keys in any case.)
 __device__ __forceinline__ uint32_t sample_position(const SegInfo& d, uint64_t j) {
     const uint64_t x = mix64(d.seed + kGolden * (j + 1));
     return d.start + (uint32_t)__umul64hi(x, (uint64_t)(d.end - d.start));
@@ -555,7 +556,27 @@ __global__ void __launch_bounds__(kThreads) k_cache_scatter(Args a) {
     }
 }
 
-// rebuild, step 4: checksum of the new array; the last block writes the header
+// rebuild, step 4: each bucket's positions in ascending order (about ten per bucket), so that
+// the gather walks every array upward; bcount[b] now holds the end of bucket b
+__global__ void __launch_bounds__(kThreads) k_cache_sort(Args a) {
+    if (!a.ctl->rebuild) return;
+    const uint64_t nb = a.nbuckets;
+    for (uint64_t b = (uint64_t)blockIdx.x * kThreads + threadIdx.x; b < nb;
+         b += (uint64_t)gridDim.x * kThreads) {
+        const uint32_t lo = b ? a.bcount[b - 1] : 0u, hi = a.bcount[b];
+        for (uint32_t i = lo + 1; i < hi; ++i) {  // insertion sort
+            const uint32_t x = a.spos[i];
+            uint32_t j = i;
+            while (j > lo && a.spos[j - 1] > x) {
+                a.spos[j] = a.spos[j - 1];
+                --j;
+            }
+            a.spos[j] = x;
+        }
+    }
+}
+
+// rebuild, step 5: checksum of the new array; the last block writes the header
 __global__ void __launch_bounds__(kThreads) k_cache_commit(Args a) {
     __shared__ uint64_t s_scan[33];
     __shared__ int s_last;
@@ -934,11 +955,8 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
     __shared__ int s_uniform[kPStages];
     __shared__ float s_scale[kPStages];
     __shared__ uint32_t s_thresh[kPStages];
-    __shared__ uint32_t s_binA[kPStages], s_nloc[kPStages];      // AdaComp: bins in the tile
-    __shared__ uint32_t s_rem[kPStages];  // AdaComp: offset of the tile start in bin s_binA
-    // AdaComp: largest key per local bin, two buffers by tile parity: a tile's buffer is cleared
-    // after the block barrier that ends its use, and the next use is two tiles later
-    __shared__ uint32_t s_bmax[kSel == 1 ? 2 : 1][kSel == 1 ? kPTile : 1];
+    __shared__ uint32_t s_binA[kPStages];  // AdaComp: global index of the tile's first bin
+    __shared__ uint32_t s_rem[kPStages];   // AdaComp: offset of the tile start in bin s_binA
     __shared__ uint32_t s_rc[2][kPRows * kWarps];  // candidates per (row, warp), by parity
     __shared__ int s_skip;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -958,12 +976,9 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
             s_scale[st] = d.scale;
             s_thresh[st] = d.thresh;
             if (kSel == 1) {
-                const uint32_t last = (uint32_t)(base + len - 1);
-                const SegInfo& z = a.segs[upper_bound_minus1(a.seg_start, a.nseg, last)];
                 const uint32_t binA = d.binbase + ((uint32_t)base - d.start) / a.hp.bin;
                 s_binA[st] = binA;
                 s_rem[st] = ((uint32_t)base - d.start) - (binA - d.binbase) * a.hp.bin;
-                s_nloc[st] = z.binbase + (last - z.start) / a.hp.bin - binA + 1;
             }
             const uint32_t bytes = (len & ~3u) * 4u;  // whole 16-byte units; the rest by hand
             mbar_arrive_expect_tx(&s_bar[st], 3u * bytes);
@@ -986,8 +1001,6 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
             for (int st = 0; st < kPStages; ++st) issue(st);
         }
     }
-    if (kSel == 1)
-        for (int b = tid; b < kPTile; b += kThreads) s_bmax[0][b] = s_bmax[kSel == 1][b] = 0;
     __syncthreads();
     if (s_skip) return;
 
@@ -1010,21 +1023,22 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
         if (tile >= ntiles) break;  // every later stage holds an empty phase too
         const uint64_t base = (uint64_t)tile * kPTile;
         const uint32_t len = (uint32_t)(umin64(n, base + kPTile) - base);
-        const uint32_t nloc = (kSel == 1) ? s_nloc[st] : 0u;  // read before the stage is reissued
         float4 uu[kPRows], vv[kPRows];
         uint32_t flags;
         stream_compute<true>(a, s_stage + (size_t)st * kPStageFloats, base, len, s_uniform[st],
                              s_scale[st], s_thresh[st], uu, vv, flags);
         if constexpr (kSel == 2) flags = 0;  // the shared set is given: no candidates
-        if constexpr (kSel == 1) {  // bin-local maxima of this tile, then the candidates that reach them
-            // entries past len hold v = 0 (key 0): they raise no maximum and are never candidates
+        if constexpr (kSel == 1) {
+            // AdaComp without a block barrier: each warp row (128 consecutive entries) finds the
+            // largest key of every run of one bin inside it, raises the bin's global maximum with
+            // it, and makes the entries that reach their run's maximum candidates. A bin's
+            // global maximum is the largest of its runs' maxima, so every entry the emit step
+            // keeps (key == the bin's global maximum) is a candidate. Entries past len hold
+            // v = 0 (key 0): they raise nothing and are never candidates.
             const uint32_t binA = s_binA[st], L = a.hp.bin;
-            uint32_t* bmax = s_bmax[it & 1];
-            const bool fast = s_uniform[st] && L >= 4u;
-            uint32_t qr[kPRows], dr[kPRows];  // fast path: a lane's first local bin, and the
-                                              // entries before the next one (>= 4: none)
-            uint32_t lb[kPRows * 4];          // other tiles: every entry's local bin
-            if (fast) {
+            uint32_t* gmax = a.binmax + binA;  // global maxima, indexed by local bin
+            flags = 0;
+            if (s_uniform[st] && L >= 4u) {
                 // one segment: tile entry o lies in local bin (rem + o) / L, rem being the tile
                 // start's offset within bin binA. A lane's 4 entries span at most two bins, and
                 // bins rise with o, so a warp row holds contiguous runs of equal bins.
@@ -1032,7 +1046,7 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
 #pragma unroll
                 for (int r = 0; r < kPRows; ++r) {
                     const uint32_t o0 = 4u * (r * kThreads + tid);
-                    uint32_t q, d0;
+                    uint32_t q, d0;  // the lane's first local bin; entries before the next one
                     if (L >= (uint32_t)kPTile) {
                         q = (o0 >= L - rem) ? 1u : 0u;
                         d0 = q ? L - (o0 - (L - rem)) : L - rem - o0;
@@ -1041,79 +1055,91 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
                         q = __float2uint_rd(__fmul_rn(__fadd_rn((float)x, 0.5f), a.hp.bin_inv));
                         d0 = L - (x - q * L);
                     }
-                    qr[r] = q;
-                    dr[r] = d0;
                     const float* vr = reinterpret_cast<const float*>(&vv[r]);
-                    uint32_t mlo = 0, mhi = 0;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t key = key_of(vr[e]);
-                        if ((uint32_t)e < d0) mlo = max(mlo, key); else mhi = max(mhi, key);
+                    const uint32_t kk[4] = {key_of(vr[0]), key_of(vr[1]), key_of(vr[2]),
+                                            key_of(vr[3])};
+                    const bool split = d0 < 4u;  // the first bin ends inside this lane (rare)
+                    uint32_t mlo, mhi = 0;
+                    if (!split) {
+                        mlo = max(max(kk[0], kk[1]), max(kk[2], kk[3]));
+                    } else {
+                        mlo = kk[0];  // d0 >= 1: entry 0 is always in the first bin
+                        mhi = d0 <= 1u ? kk[1] : 0u;
+                        mlo = d0 > 1u ? max(mlo, kk[1]) : mlo;
+                        mhi = d0 <= 2u ? max(mhi, kk[2]) : mhi;
+                        mlo = d0 > 2u ? max(mlo, kk[2]) : mlo;
+                        mhi = max(mhi, kk[3]);  // d0 <= 3
                     }
-                    const bool split = d0 < 4u;  // the first bin ends inside this lane
-                    if (split && mlo) atomicMax(&bmax[q], mlo);
-                    const uint32_t b = q + (split ? 1u : 0u);
-                    uint32_t mx = split ? mhi : mlo;
-                    // the lane's last bin: one max per run of lanes that share it
+                    const uint32_t b = q + (split ? 1u : 0u);  // the lane's last bin
+                    uint32_t run;  // the maximum of the lane's last bin over the row
                     if (L >= 128u) {  // at most two bins in the row's 128 entries
                         const uint32_t b0 = __shfl_sync(kFull, b, 0), b1 = __shfl_sync(kFull, b, 31);
-                        const uint32_t m0 = __reduce_max_sync(kFull, b == b0 ? mx : 0u);
-                        const uint32_t m1 = __reduce_max_sync(kFull, b == b1 ? mx : 0u);
-                        if (lane == 0 && m0) atomicMax(&bmax[b0], m0);
-                        if (lane == 31 && b1 != b0 && m1) atomicMax(&bmax[b1], m1);
-                    } else {  // segmented max by shuffles; the run's first lane keeps it
+                        const uint32_t mx = split ? mhi : mlo;
+                        if (b0 == b1) {  // the whole row in one bin (the common case)
+                            run = __reduce_max_sync(kFull, mx);
+                            if (lane == 0 && run) atomicMax(gmax + b0, run);
+                        } else {
+                            const uint32_t m0 = __reduce_max_sync(kFull, b == b0 ? mx : 0u);
+                            const uint32_t m1 = __reduce_max_sync(kFull, b == b1 ? mx : 0u);
+                            if (lane == 0 && m0) atomicMax(gmax + b0, m0);
+                            if (lane == 31 && m1) atomicMax(gmax + b1, m1);
+                            run = (b == b0) ? m0 : m1;
+                        }
+                    } else {  // segmented max by shuffles, suffix then prefix over each run
+                        run = split ? mhi : mlo;
 #pragma unroll
                         for (int dl = 1; dl < 32; dl <<= 1) {
-                            const uint32_t om = __shfl_down_sync(kFull, mx, dl);
+                            const uint32_t om = __shfl_down_sync(kFull, run, dl);
                             const uint32_t ob = __shfl_down_sync(kFull, b, dl);
-                            if (lane + dl < 32 && ob == b && om > mx) mx = om;
+                            if (lane + dl < 32 && ob == b && om > run) run = om;
                         }
                         const uint32_t pb = __shfl_up_sync(kFull, b, 1);
-                        if (mx && (lane == 0 || pb != b)) atomicMax(&bmax[b], mx);
+                        if (run && (lane == 0 || pb != b)) atomicMax(gmax + b, run);
+#pragma unroll
+                        for (int dl = 1; dl < 32; dl <<= 1) {
+                            const uint32_t om = __shfl_up_sync(kFull, run, dl);
+                            const uint32_t ob = __shfl_up_sync(kFull, b, dl);
+                            if (lane >= dl && ob == b && om > run) run = om;
+                        }
+                    }
+                    // the first bin of a split lane: its run ends here, and the lane before
+                    // holds the row's maximum of it when that lane's last bin is the same
+                    const uint32_t prun = __shfl_up_sync(kFull, run, 1);
+                    const uint32_t pbin = __shfl_up_sync(kFull, b, 1);
+                    if (split) {
+                        const uint32_t rq = (lane > 0 && pbin == q) ? max(prun, mlo) : mlo;
+                        if (lane == 0 || pbin != q) {  // this lane holds the whole run
+                            if (mlo) atomicMax(gmax + q, mlo);
+                        } else if (rq > prun) {  // the lane before did not see this part
+                            atomicMax(gmax + q, rq);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint32_t m = ((uint32_t)e < d0) ? rq : run;
+                            if (kk[e] && kk[e] == m) flags |= 1u << (4 * r + e);
+                        }
+                    } else if (run && mlo == run) {  // this lane reaches its run's maximum
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (kk[e] == run) flags |= 1u << (4 * r + e);
                     }
                 }
-            } else {  // a segment boundary inside the tile, or bins under 4 entries: per entry
+            } else {  // a segment boundary inside the tile, or bins under 4 entries: every
+                      // non-zero entry is a candidate and raises its bin's maximum itself
 #pragma unroll
                 for (int r = 0; r < kPRows; ++r)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const uint32_t off = 4u * (r * kThreads + tid) + e;
-                        uint32_t b = 0;
-                        if (off < len) {
+                        const uint32_t key = key_of(reinterpret_cast<const float*>(&vv[r])[e]);
+                        if (off < len && key) {
                             const uint32_t i = (uint32_t)(base + off);
                             const SegInfo& d = a.segs[upper_bound_minus1(a.seg_start, a.nseg, i)];
-                            b = d.binbase + (i - d.start) / L - binA;
-                            const uint32_t key = key_of(reinterpret_cast<const float*>(&vv[r])[e]);
-                            if (key) atomicMax(&bmax[b], key);
+                            atomicMax(a.binmax + d.binbase + (i - d.start) / L, key);
+                            flags |= 1u << (4 * r + e);
                         }
-                        lb[r * 4 + e] = b;
                     }
             }
-            __syncthreads();
-            flags = 0;
-            if (fast) {
-#pragma unroll
-                for (int r = 0; r < kPRows; ++r) {
-                    const float* vr = reinterpret_cast<const float*>(&vv[r]);
-                    const uint32_t d0 = dr[r], lo = bmax[qr[r]];
-                    const uint32_t hi = (d0 < 4u) ? bmax[qr[r] + 1] : 0u;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t key = key_of(vr[e]);
-                        if (key > 0 && key == ((uint32_t)e < d0 ? lo : hi)) flags |= 1u << (4 * r + e);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < kPRows; ++r)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t key = key_of(reinterpret_cast<const float*>(&vv[r])[e]);
-                        if (key > 0 && key == bmax[lb[r * 4 + e]]) flags |= 1u << (4 * r + e);
-                    }
-            }
-            for (uint32_t b = tid; b < nloc; b += kThreads)  // this tile's maxima into the global ones
-                if (bmax[b]) atomicMax(&a.binmax[binA + b], bmax[b]);
         }
         // candidate words: the 8 lanes of a lane-group cover 32 consecutive entries of a row
         uint32_t word[kPRows];
@@ -1148,8 +1174,6 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
             fence_proxy_async_smem();
             issue(st);  // the next tile for this stage starts loading now
         }
-        if constexpr (kSel == 1)  // every read of this tile's bin maxima is behind the barrier
-            for (uint32_t b = tid; b < nloc; b += kThreads) s_bmax[it & 1][b] = 0;
         // every warp scans the kPRows x kWarps counts itself (row-major = index order)
         const uint32_t cv = (lane < kPRows * kWarps) ? s_rc[it & 1][lane] : 0u;
         const uint32_t cinc = warp_incl_scan(cv);
@@ -1632,6 +1656,7 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     L1(k_cache_count, cgrid, kThreads, a);
     L1(k_cache_scan, 1, 1024, a);
     L1(k_cache_scatter, cgrid, kThreads, a);
+    L1(k_cache_sort, cgrid, kThreads, a);
     L1(k_cache_commit, cgrid, kThreads, a);
     const uint64_t sgrid = (L.max_samples + kThreads * kSamplePerThread - 1) /
                            (kThreads * kSamplePerThread);
