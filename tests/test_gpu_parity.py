@@ -906,3 +906,35 @@ def _scalecomp_learners(W, n, off, steps):
         for w in range(W):
             assert same_bits(host_f32(state_d[w][1]), state_h[w][1]), (t, w)
             assert same_bits(host_f32(state_d[w][0]), state_h[w][0]), (t, w)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_sampled_calls_with_changing_sparsity(seed):
+    # one workspace across calls whose sparsity jumps both ways (the cached sample positions
+    # stay valid, the threshold moves a long way), a zero-length segment, and one call with a
+    # gradient ten times larger: every call bitwise equal to the oracle
+    rng = np.random.default_rng(4700 + seed)
+    n = 2_000_003
+    off = np.array([0, 700_000, 700_000, 1_500_000, n])
+    schedule = [0.999, 0.9, 0.999, 0.99, 0.5, 0.999, 0.999]
+    u_h, v_h = np.zeros(n, np.float32), np.zeros(n, np.float32)
+    u_d, v_d = dev_f32(u_h), dev_f32(v_h)
+    comp = None
+    for t, sp in enumerate(schedule):
+        kw = dict(mode=dgc.SELECT_SAMPLED, sparsity=sp, momentum=0.9, seed=seed,
+                  clip_norm=float(rng.choice([0.0, 1.0])))
+        pd, po = params_pair(**kw)
+        if comp is None:  # outputs sized for the densest call
+            comp = Compressor(n, off, dgc.make_params(**dict(kw, sparsity=min(schedule))))
+        comp.params = pd  # the same workspace across calls, as a training loop keeps it
+        g = (rng.standard_normal(n) * 0.01 * (10.0 if t == 4 else 1.0)).astype(np.float32)
+        comp(dev_f32(g), u_d, v_d)
+        assert comp.status_code() == 0
+        idx, val, st = comp.results()
+        oidx, oval, ost = oracle.compress(g, u_h, v_h, off, po)
+        assert np.array_equal(idx, oidx), f"call {t}"
+        assert same_bits(val, oval)
+        assert same_bits(host_f32(v_d), v_h) and same_bits(host_f32(u_d), u_h)
+        for s, o in enumerate(ost):
+            assert st[s]["candidates"] == o["candidates"] and st[s]["reselected"] == o["reselected"]
+            assert st[s]["sample_key"] == o["sample_key"], (t, s)
