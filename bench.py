@@ -56,6 +56,8 @@ def parse_args(argv=None):
     ap.add_argument("--select", choices=["sampled", "adacomp"], default="sampled",
                     help="DGC sampled threshold (the headline) or AdaComp bins of --bin-size")
     ap.add_argument("--bin-size", type=int, default=1000)
+    ap.add_argument("--l2-fetch", type=int, default=64,
+                    help="this process's L2 fetch granularity limit in bytes (0: leave it)")
     return ap.parse_args(argv)
 
 
@@ -356,6 +358,9 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     dist_init(world, "nccl")
     dgc.build()
+    torch.zeros(1, device=dev)  # the context exists before its limit is set
+    if args.l2_fetch > 0:  # a context limit of this process (see dgc_set_l2_fetch_granularity)
+        dgc.dgc_set_l2_fetch_granularity(args.l2_fetch)
     n = args.n
     sched = list(workloads.WARMUP_SPARSITY[:4])
     mode = dgc.SELECT_ADACOMP if args.select == "adacomp" else dgc.SELECT_SAMPLED
@@ -446,7 +451,8 @@ def run_ours(args, world, rank, local):
                    "momentum": 0.9, "sample_ratio": 0.01, "reselect_factor": 1.3,
                    "segments": 1, "l2": f"inputs larger than L2 ({4 * n >> 20} MiB per array; "
                    f"{len(pool)} distinct gradients cycled)",
-                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
+                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
+                   "l2_fetch_granularity_bytes": args.l2_fetch or "driver default"},
         "roofline": {"bound": "hbm", "kernel": "k_stream_tma<%d> (accumulate + per-tile compaction)" % (args.select == "adacomp"),
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),

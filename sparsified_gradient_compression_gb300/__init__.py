@@ -22,6 +22,7 @@ __all__ = [
     "dgc_decode_apply_quant", "dgc_compress_shared", "dgc_sum_shared_workspace",
     "dgc_sum_shared",
     "dgc_read_status", "dgc_status_string", "dgc_launch_count", "dgc_selftest_wait_timeout",
+    "dgc_set_l2_fetch_granularity",
     "dgc_profile_stream_pass",
     "SELECT_EXACT", "SELECT_SAMPLED", "SELECT_ADACOMP", "FLAG_MASK_MOMENTUM",
 ]
@@ -109,6 +110,8 @@ def lib():
         L.dgc_status_string.restype = ctypes.c_char_p
         L.dgc_launch_count.argtypes = []
         L.dgc_launch_count.restype = u64
+        L.dgc_set_l2_fetch_granularity.argtypes = [i32]
+        L.dgc_set_l2_fetch_granularity.restype = ctypes.c_int
         L.dgc_selftest_wait_timeout.argtypes = [vp, u32, vp]
         L.dgc_profile_stream_pass.argtypes = [vp, vp]
         L.dgc_profile_stream_pass.restype = None
@@ -366,6 +369,11 @@ def dgc_status_string(code: int) -> str:
 
 def dgc_launch_count() -> int:
     return int(lib().dgc_launch_count())
+
+
+def dgc_set_l2_fetch_granularity(nbytes: int) -> int:
+    """Context limit cudaLimitMaxL2FetchGranularity for the current device (0..128 bytes)."""
+    return _check(lib().dgc_set_l2_fetch_granularity(int(nbytes)), "dgc_set_l2_fetch_granularity")
 
 
 def dgc_profile_stream_pass(begin, end) -> None:

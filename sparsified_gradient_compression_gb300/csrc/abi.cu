@@ -31,6 +31,15 @@ int dgc_internal_sm_count() {
 
 extern "C" uint64_t dgc_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+extern "C" int dgc_set_l2_fetch_granularity(int32_t bytes) {
+    if (bytes < 0 || bytes > 128) return DGC_EINVAL;
+    if (cudaDeviceSetLimit(cudaLimitMaxL2FetchGranularity, (size_t)bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return DGC_ECUDA;
+    }
+    return DGC_OK;
+}
+
 extern "C" const char* dgc_status_string(int code) {
     switch (code) {
         case DGC_OK: return "ok";

@@ -182,3 +182,8 @@ def test_quant_entry_points_reject_on_host(L):
     many_sizes = (ctypes.c_uint64 * 65537)(*([40] * 65537))
     assert d(cast(many), cast(many_sizes), 65537, 16, 1.0, FAKE, 100, 0, FAKE, FAKE, 1 << 30,
              None) == dgc.EUNSUPPORTED
+
+
+def test_l2_fetch_granularity_rejects_out_of_range(L):
+    assert L.dgc_set_l2_fetch_granularity(-1) == dgc.EINVAL
+    assert L.dgc_set_l2_fetch_granularity(129) == dgc.EINVAL

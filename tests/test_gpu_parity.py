@@ -938,3 +938,12 @@ def test_sampled_calls_with_changing_sparsity(seed):
         for s, o in enumerate(ost):
             assert st[s]["candidates"] == o["candidates"] and st[s]["reselected"] == o["reselected"]
             assert st[s]["sample_key"] == o["sample_key"], (t, s)
+
+
+def test_l2_fetch_granularity_hint_keeps_results():
+    # the context limit is a fetch-size hint: the sampled step stays bitwise equal to the oracle
+    assert dgc.dgc_set_l2_fetch_granularity(64) == 0
+    n = 1_000_003
+    off = np.array([0, 400_000, n])
+    run_steps(lambda t: (np.random.default_rng([31, t]).standard_normal(n) * 0.01)
+              .astype(np.float32), off, 3, mode=dgc.SELECT_SAMPLED, sparsity=0.999, momentum=0.9)
