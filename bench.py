@@ -170,10 +170,15 @@ def measured_peak_hbm():
 
 
 def stream_pass_source_hash() -> str:
+    """Hash of the streaming kernel's code (compress.cu and dgc_device.cuh without // comments and
+    blank lines, so that a comment edit does not orphan the recorded counters)."""
     h = hashlib.sha256()
     for f in ("compress.cu", "dgc_device.cuh"):
-        with open(os.path.join(ROOT, "sparsified_gradient_compression_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "sparsified_gradient_compression_gb300", "csrc", f)) as fh:
+            for line in fh:
+                code = line.split("//")[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

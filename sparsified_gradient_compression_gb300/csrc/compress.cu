@@ -1,31 +1,39 @@
-// compress.cu -- dgc_compress: the DGC per-worker compressor on sm_103a.
+// compress.cu -- dgc_compress, dgc_compress_shared: the DGC per-worker compressor on sm_103a.
 //
 // Sources: "[Paper Review] Deep Gradient Compression: Reducing the Communication Bandwidth for
-// Distributed Training" (Abstract; Proposed method bullets 1, 3, 4, 5; Research questions RQ4)
-// and "AdaComp : Adaptive Residual Gradient Compression for Data-Parallel Distributed
-// Training" (abstract; citation snippets on magnitude selection).
+// Distributed Training" (Abstract; Proposed method bullets 1, 3, 4, 5; Research questions RQ4),
+// "AdaComp : Adaptive Residual Gradient Compression for Data-Parallel Distributed Training"
+// (abstract; citation snippets on magnitude and bin-local selection) and the ScaleComp abstract
+// (low-pass filter in the local accumulation; one index set for all learners).
 //
-// One call enqueues this pipeline on the caller's stream (every kernel reads the segment table
-// and counters the previous ones left in the workspace, so no host round trip is needed):
+// One dgc_compress call enqueues this pipeline on the caller's stream (every kernel reads the
+// segment table and counters the previous ones left in the workspace, so no host round trip):
 //
-//   plan          segment table: k, sample counts, seeds; validates seg_off; zeroes counters
-//   clip_tiles    [clipping] binary64 pairwise sum of g^2 per 4096-entry tile
+//   plan          segment table: k, sample counts, seeds, bins; validates seg_off; zeroes counters
+//   clip_tiles    [clipping] binary64 pairwise sum of g^2 per 4096-entry clip tile
 //   clip_scale    [clipping] tile sums left to right -> per-segment scale
+//   cache_*       [sampled, exact] the sample positions, kept sorted in the workspace; checked
+//                 every call (tag + checksum), rebuilt only when they no longer match
 //   sample        gathers g,u,v at the SplitMix64 sample positions, recomputes v' there,
 //                 writes the sample keys and the first radix-select histogram
 //   find/hist x3  radix select of the sampled threshold t (11 + 10 + 10 key bits)
-//   fused         THE STREAMING PASS: u = fma(m,u,g*scale); v += u; candidates key(v) >= t
-//                 are compacted in index order through a decoupled look-back (sampled mode
-//                 also clears v,u of every candidate in the same store)
+//   stream_tma    THE STREAMING PASS: persistent blocks, bulk-copy pipeline of g,u,v tiles;
+//                 u = fma(m,u,g*scale); v = fma(leak,v,u); candidates (key(v) >= t, or for
+//                 AdaComp the entries at their bin run's maximum, which also raise the bin's
+//                 global maximum) are compacted into each tile's own slots
+//   collect       tile slots -> one index-ordered candidate list (decoupled look-back)
 //   candoff       per-segment candidate ranges; decides who re-selects
-//   compact_v     [exact mode, only if the sampled bound was too tight] re-compacts from v
+//   recompact     [exact mode, only if the sampled bound was too tight] re-compacts from v
 //   hist/find x6  radix select of the exact k-th (|v|, index) pair among candidates
-//   emit          writes S in index order (second look-back), clears v,u of sent entries
-//                 (exact) or restores those of unsent candidates (sampled); statistics
+//   emit          writes S in index order (second look-back), clears v (and u with masking)
+//                 of the sent entries; statistics
 //
 // Exact mode uses the sampled threshold only as a safe lower bound: a margin above the sample
-// rank makes |C| >= k overwhelmingly likely, and when it is not, compact_v re-reads v with a
+// rank makes |C| >= k overwhelmingly likely, and when it is not, recompact re-reads v with a
 // zero threshold for that segment. Either way S is the exact top-k.
+//
+// dgc_compress_shared (one index set given by the caller) runs plan, a check of the set,
+// clipping, the streaming pass without candidates, and a gather of v at the set.
 #include <cmath>
 #include <cstring>
 
@@ -35,8 +43,8 @@ namespace dgc {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRows = 8;                          // float4 rows per thread in the streaming pass
-constexpr int kTile = kThreads * kRows * 4;       // 8192 entries per streaming tile
+constexpr int kRows = 8;                          // float4 rows per thread in re-compaction
+constexpr int kTile = kThreads * kRows * 4;       // 8192 entries per re-compaction tile
 // streaming pass shape: entries per tile, tiles in flight per block, blocks per SM
 // (2048 entries x 4 stages x 2 blocks per SM: the fastest of the shapes measured on GB300)
 #ifndef DGC_STREAM_TILE
@@ -250,7 +258,7 @@ struct Args {
     uint32_t* cand_off;
     double* clip_part;
     uint32_t* skeys;
-    uint32_t* spos;    // sample positions in bucket order (cached between calls)
+    uint32_t* spos;    // sample positions in ascending order (cached between calls)
     uint32_t* bcount;  // per-bucket counts, then cursors, while the cache is rebuilt
     uint32_t* histA;
     uint32_t* histB;
@@ -633,7 +641,7 @@ __global__ void __launch_bounds__(kThreads) k_sample(Args a) {
         sg[r] = -1;
         if (jg < chunk_end) {
             const int s = uniform ? s_seg0 : upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)jg);
-            const uint32_t pos = a.spos[jg];  // the sample positions in bucket order
+            const uint32_t pos = a.spos[jg];  // the sample positions in ascending order
             gv[r] = __ldg(a.g + pos);
             uv[r] = a.u[pos];
             vv[r] = a.v[pos];
