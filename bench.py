@@ -469,6 +469,10 @@ def run_ours(args, world, rank, local):
         "quant": quant,  # outside the step: the same message as 8-bit integers
         "shared": shared,  # outside the step: one index set for all learners
         "compress_gbs": round(4.0 * n / (t_compress / 1e3) / 1e9, 2),
+        # the whole compress call against the same peak: 20 B per entry streamed, 0.12 B per
+        # entry of sample (12 B per sample at 1%), 24 B per sent entry (index, value, v, u)
+        "compress_roofline_frac": round((20.12 * n + 24.0 * int(st["sent"])) /
+                                        (t_compress / 1e3) / 1e9 / peak, 4),
         "message_bytes": int(statistics.median(nbytes)),
         "candidates": cand, "sent": int(st["sent"]),
         "gpu_launches": int(launches), "clocks": clk,

@@ -14,7 +14,8 @@ import oracle
 import sparsified_gradient_compression_gb300 as dgc
 import workloads
 from conftest import read_golden
-from gpu_helpers import Compressor, Encoder, decode, decode_apply, dev_f32, host_f32
+from gpu_helpers import (Compressor, Encoder, decode, decode_apply, decode_apply_quant,
+                         decode_quant, dev_f32, encode_quant, host_f32)
 
 pytestmark = pytest.mark.gpu
 
@@ -169,6 +170,21 @@ def test_aggregation_64_learners():
         orc_rc, w_orc = oracle.decode_apply(msgs_orc, n, w0, np.float32(0.1 / W))
         assert rc == 0 and orc_rc == 0
         assert same_bits(w_gpu, w_orc)
+        if step < 2:  # the same learners' entries as 16-bit integer messages
+            qmsgs = []
+            for w in range(W):
+                rng = np.random.Generator(np.random.PCG64([5, step, w]))
+                idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+                val = (rng.standard_normal(k) * 0.01).astype(np.float32)
+                rc, m, _ = oracle.encode_quant(idx, val, n, 1e5, 16)
+                assert rc == 0
+                qmsgs.append(m)
+            rc, dq = decode_quant(qmsgs, n, 16, 1e5)
+            orc_rc, odq = oracle.decode_accumulate_quant(qmsgs, n, 16, 1e5)
+            assert rc == 0 and orc_rc == 0 and same_bits(dq, odq)
+            rc, wq = decode_apply_quant(qmsgs, n, 16, 1e5, w0, 0.1 / W)
+            orc_rc, owq = oracle.decode_apply_quant(qmsgs, n, 16, 1e5, w0, np.float32(0.1 / W))
+            assert rc == 0 and orc_rc == 0 and same_bits(wq, owq)
 
 
 @pytest.mark.slow
@@ -636,7 +652,6 @@ def test_decode_apply_malformed_and_empty():
 
 
 # ------------------------------------------------------------------- integer-valued messages
-from gpu_helpers import decode_apply_quant, decode_quant, encode_quant  # noqa: E402
 
 
 @pytest.mark.parametrize("name", ["codec_quant8.txt", "codec_quant16.txt"])
