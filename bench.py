@@ -56,6 +56,8 @@ def parse_args(argv=None):
     ap.add_argument("--select", choices=["sampled", "adacomp"], default="sampled",
                     help="DGC sampled threshold (the headline) or AdaComp bins of --bin-size")
     ap.add_argument("--bin-size", type=int, default=1000)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch compress and encode call by call instead of replaying graphs")
     ap.add_argument("--l2-fetch", type=int, default=64,
                     help="this process's L2 fetch granularity limit in bytes (0: leave it)")
     return ap.parse_args(argv)
@@ -232,18 +234,48 @@ class Pipeline:
         self.dense = torch.empty(n, dtype=torch.float32, device=dev)
         self.nb_host = torch.zeros(1, dtype=torch.int64, pin_memory=True)
 
-    def step(self, g, p, ev=None):
+    def compress(self, g, p):
+        self.dgc.dgc_compress(g, self.u, self.v, self.seg, p, self.out_idx, self.out_val,
+                              self.out_count, self.stats, self.status, self.ws, n=self.n,
+                              out_cap=self.cap, ws_bytes=self.ws_bytes)
+
+    def encode(self):
+        self.dgc.dgc_encode(self.out_idx, self.out_val, self.out_count, self.n, self.msg,
+                            self.msg_bytes, self.status, self.ews, max_count=self.cap,
+                            out_cap=self.msg_cap, ws_bytes=self.ews_bytes)
+
+    def capture(self, g, p):
+        """CUDA graphs of this pipeline's compress call on g and of its encode call: both
+        enqueue kernels (and a memset) only, so they replay as they were captured."""
+        import torch
+
+        side = torch.cuda.Stream(self.dev)
+        side.wait_stream(torch.cuda.current_stream(self.dev))
+        graphs = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graphs[0], stream=side):
+                self.compress(g, p)
+            with torch.cuda.graph(graphs[1], stream=side):
+                self.encode()
+        torch.cuda.current_stream(self.dev).wait_stream(side)
+        return graphs
+
+    def step(self, g, p, ev=None, graphs=None):
+        """One step; with `graphs` (from capture() on the same g and p) compress and encode are
+        graph replays."""
         dgc = self.dgc
         if ev:
             ev[0].record()
-        dgc.dgc_compress(g, self.u, self.v, self.seg, p, self.out_idx, self.out_val,
-                         self.out_count, self.stats, self.status, self.ws, n=self.n,
-                         out_cap=self.cap, ws_bytes=self.ws_bytes)
+        if graphs:
+            graphs[0].replay()
+        else:
+            self.compress(g, p)
         if ev:
             ev[1].record()
-        dgc.dgc_encode(self.out_idx, self.out_val, self.out_count, self.n, self.msg,
-                       self.msg_bytes, self.status, self.ews, max_count=self.cap,
-                       out_cap=self.msg_cap, ws_bytes=self.ews_bytes)
+        if graphs:
+            graphs[1].replay()
+        else:
+            self.encode()
         if ev:
             ev[2].record()
         self.nb_host.copy_(self.msg_bytes)  # the decoder takes message sizes on the host
@@ -389,6 +421,15 @@ def run_ours(args, world, rank, local):
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     evs = [(E(), E(), E(), E()) for _ in range(K)]
     kev = [(E(), E()) for _ in range(K)]
+    graphs, graph_kernels, gkev = None, 0, (E(), E())
+    if not args.no_graph:  # one compress graph per pool buffer (p_main), one encode graph each
+        torch.cuda.synchronize()
+        l0 = dgc.dgc_launch_count()
+        dgc.dgc_profile_stream_pass(*gkev)  # becomes an event-record node pair in each graph
+        graphs = [pipe.capture(g, p_main) for g in pool]
+        dgc.dgc_profile_stream_pass(None, None)
+        graph_kernels = (dgc.dgc_launch_count() - l0) // len(pool)  # kernels per replay pair
+        torch.cuda.synchronize()
     gpu_id = None
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -403,13 +444,19 @@ def run_ours(args, world, rank, local):
     t_begin, t_end = E(), E()
     t_begin.record()
     nbytes = []
+    t_graph_kernel = []
     for i in range(K):
-        dgc.dgc_profile_stream_pass(kev[i][0], kev[i][1])
-        nbytes.append(pipe.step(pool[(args.warmup + i) % len(pool)], p_main, evs[i]))
+        j = (args.warmup + i) % len(pool)
+        if graphs:
+            nbytes.append(pipe.step(pool[j], p_main, evs[i], graphs[j]))
+            t_graph_kernel.append(gkev[0].elapsed_time(gkev[1]))  # the step read nb: done
+        else:
+            dgc.dgc_profile_stream_pass(kev[i][0], kev[i][1])
+            nbytes.append(pipe.step(pool[j], p_main, evs[i]))
     t_end.record()
     torch.cuda.synchronize()
     dgc.dgc_profile_stream_pass(None, None)
-    launches = dgc.dgc_launch_count() - launches0
+    launches = dgc.dgc_launch_count() - launches0 + (K * graph_kernels if graphs else 0)
     clk = clocks.stop()
     barrier()
     if dgc.dgc_read_status(pipe.status) != 0:
@@ -420,7 +467,8 @@ def run_ours(args, world, rank, local):
     t_compress = sum(e[0].elapsed_time(e[1]) for e in evs) / K
     t_encode = sum(e[1].elapsed_time(e[2]) for e in evs) / K
     t_decode = sum(e[2].elapsed_time(e[3]) for e in evs) / K
-    t_kernel = sum(a.elapsed_time(b) for a, b in kev) / K
+    t_kernel = (sum(t_graph_kernel) / K if graphs else
+                sum(a.elapsed_time(b) for a, b in kev) / K)
     st = np.frombuffer(pipe.stats.cpu().numpy().tobytes(), dtype=[
         ("k", "<u8"), ("candidates", "<u8"), ("sent", "<u8"), ("thresh_key", "<u4"),
         ("sample_key", "<u4"), ("reselected", "<u4"), ("clip_scale", "<f4")])[0]
@@ -457,7 +505,10 @@ def run_ours(args, world, rank, local):
                    "segments": 1, "l2": f"inputs larger than L2 ({4 * n >> 20} MiB per array; "
                    f"{len(pool)} distinct gradients cycled)",
                    "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
-                   "l2_fetch_granularity_bytes": args.l2_fetch or "driver default"},
+                   "l2_fetch_granularity_bytes": args.l2_fetch or "driver default",
+                   "launch": "compress and encode as CUDA graph replays (captured once per "
+                             "gradient buffer), decode call by call" if graphs else
+                             "call by call"},
         "roofline": {"bound": "hbm", "kernel": "k_stream_tma<%d> (accumulate + per-tile compaction)" % (args.select == "adacomp"),
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),

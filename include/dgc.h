@@ -32,6 +32,12 @@
  *     rebuilds them when either differs, so using the workspace for anything else in between
  *     is safe and only costs that rebuild.
  *   - Indices are uint32: n must be below 2^32.
+ *   - CUDA graphs: dgc_compress, dgc_compress_shared and dgc_encode enqueue kernels and at most
+ *     a memset, so a stream capture of them replays as captured. Make one ordinary
+ *     dgc_compress or dgc_compress_shared call on the device first (it sets the streaming
+ *     kernels' shared-memory attributes once per device). The decoders copy their table of
+ *     messages from host memory on every call and are not meant for capture. (This note does
+ *     not cover dgc_compress_noalloc.)
  */
 #ifndef DGC_H
 #define DGC_H

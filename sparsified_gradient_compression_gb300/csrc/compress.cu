@@ -1506,6 +1506,16 @@ using namespace dgc;
 
 static cudaEvent_t g_prof_begin = nullptr, g_prof_end = nullptr;
 
+// A profiling marker on the call's stream. Under stream capture it becomes an event-record node
+// of the graph, so every launch of the graph records it.
+static void record_marker(cudaEvent_t ev, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(ev, s);
+}
+
 extern "C" void dgc_profile_stream_pass(dgc_event_t begin, dgc_event_t end) {
     g_prof_begin = reinterpret_cast<cudaEvent_t>(begin);
     g_prof_end = reinterpret_cast<cudaEvent_t>(end);
@@ -1676,12 +1686,12 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     L1(k_hist<0>, hist_grid, kThreads, a, 2);
     L1(k_find<0>, (unsigned)nseg, kThreads, a, 2);
     const cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
-    if (pb && pe) cudaEventRecord(pb, s);
+    if (pb && pe) record_marker(pb, s);
     if (n > 0) {
         launch_stream_pass(hp.mode == DGC_SELECT_ADACOMP ? 1 : 0, a, L.ptiles, sms, s);
         ++launches;
     }
-    if (pb && pe) cudaEventRecord(pe, s);
+    if (pb && pe) record_marker(pe, s);
     L1(k_collect, (unsigned)L.cgroups, kThreads, a);
     L1(k_candoff, 1, 1024, a, 0);
     if (hp.mode == DGC_SELECT_EXACT) {
@@ -1749,12 +1759,12 @@ extern "C" int dgc_compress_shared(const float* g, float* u, float* v, int64_t n
         L1(k_clip_scale, (unsigned)((nseg + 255) / 256), 256, a);
     }
     const cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
-    if (pb && pe) cudaEventRecord(pb, s);
+    if (pb && pe) record_marker(pb, s);
     if (n > 0) {
         launch_stream_pass(2, a, L.ptiles, sms, s);
         ++launches;
     }
-    if (pb && pe) cudaEventRecord(pe, s);
+    if (pb && pe) record_marker(pe, s);
     L1(k_shared_gather, jgrid, kThreads, a, idx, count, out_val);
     dgc_internal_count_launches(launches);
     if (cudaPeekAtLastError() != cudaSuccess) {

@@ -962,3 +962,50 @@ def test_l2_fetch_granularity_hint_keeps_results():
     off = np.array([0, 400_000, n])
     run_steps(lambda t: (np.random.default_rng([31, t]).standard_normal(n) * 0.01)
               .astype(np.float32), off, 3, mode=dgc.SELECT_SAMPLED, sparsity=0.999, momentum=0.9)
+
+
+def test_compress_encode_in_cuda_graph():
+    # dgc_compress and dgc_encode enqueue kernels and a memset only, so a training loop can
+    # capture them once (after one ordinary call on the device) and replay the graph every step;
+    # the replays must give the oracle's results step after step
+    n = 3_000_017
+    off = np.array([0, 1_000_000, n])
+    kw = dict(mode=dgc.SELECT_SAMPLED, sparsity=0.999, momentum=0.9, seed=4, clip_norm=1.0)
+    pd, po = params_pair(**kw)
+    comp = Compressor(n, off, pd)
+    enc = Encoder(comp.cap, n)
+    g_static = torch.zeros(n, dtype=torch.float32, device="cuda")
+    u_d, v_d = torch.zeros(n, device="cuda"), torch.zeros(n, device="cuda")
+    u_h, v_h = np.zeros(n, np.float32), np.zeros(n, np.float32)
+
+    def step():
+        comp(g_static, u_d, v_d)
+        dgc.dgc_encode(comp.out_idx, comp.out_val, comp.out_count, n, enc.out, enc.out_bytes,
+                       enc.status, enc.ws, max_count=comp.cap, out_cap=enc.cap,
+                       ws_bytes=enc.ws_bytes)
+
+    grads = [(np.random.default_rng([61, t]).standard_normal(n) * 0.01).astype(np.float32)
+             for t in range(4)]
+    g_static.copy_(torch.from_numpy(grads[0]))
+    step()  # the ordinary first call (sets the streaming kernels' attributes on this device)
+    torch.cuda.synchronize()
+    oracle.compress(grads[0], u_h, v_h, off, po)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            step()
+    torch.cuda.synchronize()
+    # capture enqueues nothing: the state is still after step 0
+    assert same_bits(host_f32(v_d), v_h)
+    for t in range(1, 4):
+        g_static.copy_(torch.from_numpy(grads[t]))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert comp.status_code() == 0 and dgc.dgc_read_status(enc.status) == 0
+        idx, val, _ = comp.results()
+        oidx, oval, _ = oracle.compress(grads[t], u_h, v_h, off, po)
+        assert np.array_equal(idx, oidx) and same_bits(val, oval), t
+        assert same_bits(host_f32(v_d), v_h) and same_bits(host_f32(u_d), u_h), t
+        assert enc.message() == oracle.encode(oidx, oval, n)
