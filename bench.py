@@ -41,6 +41,37 @@ WORKLOAD_ADACOMP = ("flat bucket of 2^30 fp32 entries (4 GiB), g ~ N(0, 1e-4) wi
 SEED = 20240
 
 
+def _one_segment(n):
+    import numpy as np
+
+    return lambda: np.array([0, n], np.int64)
+
+
+def _workload_segments(name):
+    def f():
+        import workloads
+
+        return getattr(workloads, name)()
+    return f
+
+
+# the other workloads: segment table, settings beyond sparsity 0.999 and momentum 0.9, name
+OTHER_WORKLOADS = {
+    "single": (_one_segment(1_048_576), dict(mode=0),
+               "single tensor of 1,048,576 fp32 entries ~ N(0, 0.01^2); exact top-k (k = 1049)"),
+    "resnet50": (_workload_segments("resnet50_segments"), dict(mode=0, clip_norm=1.0),
+                 "ResNet-50-shaped set: 161 tensors, 25,557,032 fp32 entries, per-tensor "
+                 "sigma log-uniform in [1e-4, 1e-1]; exact top-k per tensor, clip 1.0 per tensor"),
+    "deepspeech": (_workload_segments("deepspeech_segments"),
+                   dict(mode=1, sample_ratio=0.01, reselect_factor=1.3),
+                   "DeepSpeech-scale bucket: 122,000,000 fp32 entries, Student-t(3) x 1e-3, "
+                   "5 x 24M + 2M segments; sampled 1% threshold, re-select if |C| > 1.3k"),
+    "learners": (_one_segment(25_557_032), dict(mode=0),
+                 "one learner of the aggregation workload: 25,557,032 fp32 entries ~ "
+                 "N(0, 0.01^2); exact top-k (k = 25,558)"),
+}
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -53,6 +84,9 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-n", type=int, default=1 << 26)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--workload", choices=["bucket1g", "single", "resnet50", "deepspeech",
+                                           "learners"], default="bucket1g",
+                    help="bucket1g is the headline; the others time the other workloads' steps")
     ap.add_argument("--select", choices=["sampled", "adacomp"], default="sampled",
                     help="DGC sampled threshold (the headline) or AdaComp bins of --bin-size")
     ap.add_argument("--bin-size", type=int, default=1000)
@@ -206,22 +240,25 @@ def recorded_traffic(n: int):
 class Pipeline:
     """Buffers for one worker's step on one GPU, and the step itself (public API calls only)."""
 
-    def __init__(self, n, params, dev):
+    def __init__(self, n, params, dev, seg_off=None):
+        import numpy as np
         import torch
 
         import sparsified_gradient_compression_gb300 as dgc
 
         self.dgc, self.n, self.dev = dgc, n, dev
-        self.seg = torch.tensor([0, n], dtype=torch.int64, device=dev)
-        self.cap = max(dgc.dgc_compress_max_out(n, 1, p) for p in params)
-        self.ws_bytes = max(dgc.dgc_compress_workspace(n, 1, p) for p in params)
+        off = np.array([0, n], np.int64) if seg_off is None else np.asarray(seg_off, np.int64)
+        self.nseg = off.size - 1
+        self.seg = torch.from_numpy(off).to(dev)
+        self.cap = max(dgc.dgc_compress_max_out(n, self.nseg, p) for p in params)
+        self.ws_bytes = max(dgc.dgc_compress_workspace(n, self.nseg, p) for p in params)
         self.u = torch.zeros(n, dtype=torch.float32, device=dev)
         self.v = torch.zeros(n, dtype=torch.float32, device=dev)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.out_idx = torch.empty(self.cap, dtype=torch.int32, device=dev)
         self.out_val = torch.empty(self.cap, dtype=torch.float32, device=dev)
         self.out_count = torch.zeros(1, dtype=torch.int64, device=dev)
-        self.stats = torch.zeros(dgc.STATS_BYTES, dtype=torch.uint8, device=dev)
+        self.stats = torch.zeros(self.nseg * dgc.STATS_BYTES, dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.msg_cap = dgc.dgc_encode_max_bytes(self.cap, n)
         self.msg = torch.empty(self.msg_cap, dtype=torch.uint8, device=dev)
@@ -398,18 +435,27 @@ def run_ours(args, world, rank, local):
     torch.zeros(1, device=dev)  # the context exists before its limit is set
     if args.l2_fetch > 0:  # a context limit of this process (see dgc_set_l2_fetch_granularity)
         dgc.dgc_set_l2_fetch_granularity(args.l2_fetch)
-    n = args.n
-    sched = list(workloads.WARMUP_SPARSITY[:4])
+    wl = args.workload
     mode = dgc.SELECT_ADACOMP if args.select == "adacomp" else dgc.SELECT_SAMPLED
-    params = [dgc.make_params(mode=mode, sparsity=s, momentum=0.9, sample_ratio=0.01,
-                              reselect_factor=1.3, seed=SEED + rank, bin_size=args.bin_size)
-              for s in sched + [0.999]]
+    if wl == "bucket1g":  # the headline: one segment, the warm-up schedule, then 99.9%
+        n, off = args.n, None
+        params = [dgc.make_params(mode=mode, sparsity=s, momentum=0.9, sample_ratio=0.01,
+                                  reselect_factor=1.3, seed=SEED + rank, bin_size=args.bin_size)
+                  for s in list(workloads.WARMUP_SPARSITY[:4]) + [0.999]]
+    else:  # the other workloads at their own settings, 99.9% from the first step
+        off = OTHER_WORKLOADS[wl][0]()
+        n = int(off[-1])
+        kw = OTHER_WORKLOADS[wl][1]
+        if args.select == "adacomp":
+            kw = dict(kw, mode=dgc.SELECT_ADACOMP)
+        params = [dgc.make_params(sparsity=0.999, momentum=0.9, seed=SEED + rank,
+                                  bin_size=args.bin_size, **kw)]
     p_main = params[-1]
-    pipe = Pipeline(n, params, dev)
+    pipe = Pipeline(n, params, dev, off)
     # inputs resident in HBM: a pool of distinct gradients, one per step in turn
     pool = []
     for i in range(args.pool):
-        pool.append(torch.from_numpy(workloads.gradient("bucket1g", step=i, seed=rank, n=n)).to(dev))
+        pool.append(torch.from_numpy(workloads.gradient(wl, step=i, seed=rank, n=n)).to(dev))
 
     for i in range(args.warmup):  # the warm-up schedule, then 99.9%
         pipe.step(pool[i % len(pool)], params[min(i, len(params) - 1)])
@@ -469,9 +515,10 @@ def run_ours(args, world, rank, local):
     t_decode = sum(e[2].elapsed_time(e[3]) for e in evs) / K
     t_kernel = (sum(t_graph_kernel) / K if graphs else
                 sum(a.elapsed_time(b) for a, b in kev) / K)
-    st = np.frombuffer(pipe.stats.cpu().numpy().tobytes(), dtype=[
+    segst = np.frombuffer(pipe.stats.cpu().numpy().tobytes(), dtype=[
         ("k", "<u8"), ("candidates", "<u8"), ("sent", "<u8"), ("thresh_key", "<u4"),
-        ("sample_key", "<u4"), ("reselected", "<u4"), ("clip_scale", "<f4")])[0]
+        ("sample_key", "<u4"), ("reselected", "<u4"), ("clip_scale", "<f4")])
+    st = {f: int(segst[f].sum()) for f in ("k", "candidates", "sent")}  # over the segments
     cand = int(st["candidates"])
     # read g, u, v and write u, v; one 4-byte slot per candidate and one count per 2048-entry tile
     alg_bytes = 20.0 * n + 4.0 * cand + 4.0 * ((n + 2047) // 2048)
@@ -491,9 +538,13 @@ def run_ours(args, world, rank, local):
 
     e2e = None if args.no_e2e else run_e2e(args, pipe, pool, p_main, K)
     cpu = None
-    if not args.no_cpu and rank == 0 and world == 1:
+    if not args.no_cpu and rank == 0 and world == 1 and wl == "bucket1g":
         cpu = run_cpu_baseline(args.cpu_n, steps=3, select=args.select, bin_size=args.bin_size)
-    workload = WORKLOAD if args.select == "sampled" else WORKLOAD_ADACOMP.format(args.bin_size)
+    if wl != "bucket1g":
+        workload = OTHER_WORKLOADS[wl][2] + ("" if args.select == "sampled" else
+                                             f"; AdaComp bins of {args.bin_size} entries")
+    else:
+        workload = WORKLOAD if args.select == "sampled" else WORKLOAD_ADACOMP.format(args.bin_size)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(sec_max * 1e3 / K, 4),
@@ -502,8 +553,9 @@ def run_ours(args, world, rank, local):
         "config": {"workload": workload, "n": n, "sparsity": 0.999, "k": int(st["k"]),
                    "selection": args.select,
                    "momentum": 0.9, "sample_ratio": 0.01, "reselect_factor": 1.3,
-                   "segments": 1, "l2": f"inputs larger than L2 ({4 * n >> 20} MiB per array; "
-                   f"{len(pool)} distinct gradients cycled)",
+                   "segments": pipe.nseg, "l2": f"{4 * n >> 20} MiB per array "
+                   f"({'larger' if 4 * n > 129 * 2**20 else 'smaller'} than L2); "
+                   f"{len(pool)} distinct gradients cycled",
                    "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
                    "l2_fetch_granularity_bytes": args.l2_fetch or "driver default",
                    "launch": "compress and encode as CUDA graph replays (captured once per "

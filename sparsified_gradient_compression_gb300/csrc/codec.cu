@@ -501,8 +501,10 @@ __global__ void __launch_bounds__(kThreads) k_dec_scatter1(DecArgs a) {
     const float x = a.qbits ? dequant((int32_t)raw, a.alpha) : __uint_as_float(raw);
     if (a.apply)  // the one-message sum at p is +0 + x; then the step
         a.dense[p] = __fmaf_rn(a.neg_lr, __fadd_rn(0.0f, x), a.dense[p]);
-    else
+    else if (a.accumulate)
         a.dense[p] = __fadd_rn(a.dense[p], x);
+    else  // dense[p] was just cleared to +0: the sum is +0 + x, with no read
+        a.dense[p] = __fadd_rn(0.0f, x);
 }
 
 // ---------------------------------------------------------------- shared-set sums

@@ -1679,7 +1679,7 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     const uint64_t sgrid = (L.max_samples + kThreads * kSamplePerThread - 1) /
                            (kThreads * kSamplePerThread);
     L1(k_sample, (unsigned)sgrid, kThreads, a);
-    const unsigned hist_grid = (unsigned)sms * 2;
+    const unsigned hist_grid = (unsigned)sms * 8;  // more loads in flight over the sample keys
     L1(k_find<0>, (unsigned)nseg, kThreads, a, 0);
     L1(k_hist<0>, hist_grid, kThreads, a, 1);
     L1(k_find<0>, (unsigned)nseg, kThreads, a, 1);
