@@ -551,7 +551,7 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; see workloads/)",
         "config": {"workload": workload, "n": n, "sparsity": 0.999, "k": int(st["k"]),
-                   "selection": args.select,
+                   "selection": ("exact", "sampled", "adacomp")[int(p_main.mode)],
                    "momentum": 0.9, "sample_ratio": 0.01, "reselect_factor": 1.3,
                    "segments": pipe.nseg, "l2": f"{4 * n >> 20} MiB per array "
                    f"({'larger' if 4 * n > 129 * 2**20 else 'smaller'} than L2); "

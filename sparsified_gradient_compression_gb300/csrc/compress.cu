@@ -267,7 +267,7 @@ struct Args {
     uint64_t* st_emit;
     uint32_t* cidx;   // candidates, ascending index
     uint32_t* sidx;   // per-tile candidate slots of the streaming pass
-    uint32_t* tcount; // per-tile candidate counts
+    uint32_t* tcount; // per-tile candidate counts, then (k_collect) each tile's first position
     uint32_t* binmax; // AdaComp: largest |v| key of every bin
     uint64_t max_samples, fused_tiles, emit_tiles, max_clip_tiles, ptiles, cgroups, nbuckets,
         max_bins;
@@ -411,11 +411,23 @@ __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
     const uint64_t base = (uint64_t)d.start + (uint64_t)(c - a.clip_off[s]) * kClipTile +
                           16u * threadIdx.x;
     double q[16];
+    if ((base & 3u) == 0 && base + 16 <= d.end) {  // 16-byte aligned and whole: four float4
+        const float4* g4 = reinterpret_cast<const float4*>(a.g + base);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const uint64_t e = base + i;
-        const double x = (e < d.end) ? (double)a.g[e] : 0.0;
-        q[i] = x * x;
+        for (int j = 0; j < 4; ++j) {
+            const float4 x = g4[j];
+            q[4 * j] = (double)x.x * (double)x.x;
+            q[4 * j + 1] = (double)x.y * (double)x.y;
+            q[4 * j + 2] = (double)x.z * (double)x.z;
+            q[4 * j + 3] = (double)x.w * (double)x.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint64_t e = base + i;
+            const double x = (e < d.end) ? (double)a.g[e] : 0.0;
+            q[i] = x * x;
+        }
     }
 #pragma unroll
     for (int w = 1; w < 16; w <<= 1)
@@ -440,7 +452,16 @@ __global__ void k_clip_scale(Args a) {
     if (a.ctl->abort || s >= a.nseg) return;
     SegInfo& d = a.segs[s];
     double S = 0.0;
-    for (uint32_t t = a.clip_off[s]; t < a.clip_off[s + 1]; ++t) S = S + a.clip_part[t];
+    const uint32_t t0 = a.clip_off[s], t1 = a.clip_off[s + 1];
+    uint32_t t = t0;
+    for (; t + 8 <= t1; t += 8) {  // eight loads in flight, then the adds in order
+        double p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p[i] = a.clip_part[t + i];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) S = S + p[i];
+    }
+    for (; t < t1; ++t) S = S + a.clip_part[t];
     const double norm = sqrt(S);
     const double c = (double)a.hp.clip_norm;
     d.scale = (norm > c) ? (float)(c / norm) : 1.0f;
@@ -1214,8 +1235,9 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
 
 // ------------------------------------------------------------------------- collect
 // Turns the streaming pass's per-tile slots into one index-ordered candidate list. Block b owns
-// kCGroup consecutive tiles: it scans their counts, gets the group's global offset from a
-// decoupled look-back over groups, and copies the slots to cidx[offset + rank].
+// kCGroup consecutive tiles: it scans their counts and gets the group's global offset from a
+// decoupled look-back over groups; each tile's count is replaced by its first list position,
+// and k_collect_copy then moves the slots to cidx.
 constexpr int kCGroup = kThreads;  // tiles per collect block
 
 __global__ void __launch_bounds__(kThreads) k_collect(Args a) {
@@ -1248,18 +1270,27 @@ __global__ void __launch_bounds__(kThreads) k_collect(Args a) {
     }
     __syncthreads();
     const uint64_t gbase = s_base;
-    for (uint32_t f = tid; f < total; f += kThreads) {
-        int lo = 0, hi = kCGroup;  // the tile of flattened entry f
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (s_ex[mid] <= f) lo = mid; else hi = mid;
-        }
-        const uint64_t tb = (uint64_t)(grp * kCGroup + lo) * kPTile;
-        const uint64_t pos = gbase + f;
-        if (pos < a.n) a.cidx[pos] = a.sidx[tb + (f - s_ex[lo])];
-    }
+    // the tile's count becomes its first position in the list; k_collect_copy moves the slots
+    if (t < ntiles) a.tcount[t] = (uint32_t)umin64(gbase + ex, a.n);
     if (grp == ngroups - 1 && tid == 0)
         a.ctl->total_cand = (uint32_t)umin64(gbase + total, a.n);
+}
+
+// Every list position f finds its tile (the last one whose first position is <= f) by binary
+// search and copies its slot. Spread over the whole grid, so that a tile range dense with
+// candidates (a run of small, all-candidate segments) is not copied by one block alone.
+__global__ void __launch_bounds__(kThreads) k_collect_copy(Args a) {
+    if (ld_relaxed_u32((const uint32_t*)&a.ctl->abort)) return;
+    const uint32_t total = a.ctl->total_cand;
+    const uint32_t nt = (uint32_t)a.ptiles;
+    for (uint32_t f = blockIdx.x * kThreads + threadIdx.x; f < total; f += gridDim.x * kThreads) {
+        uint32_t lo = 0, hi = nt;
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (a.tcount[mid] <= f) lo = mid; else hi = mid;
+        }
+        a.cidx[f] = a.sidx[(uint64_t)lo * kPTile + (f - a.tcount[lo])];
+    }
 }
 
 // ------------------------------------------------------------------- candidate ranges
@@ -1693,6 +1724,7 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     }
     if (pb && pe) record_marker(pe, s);
     L1(k_collect, (unsigned)L.cgroups, kThreads, a);
+    L1(k_collect_copy, (unsigned)sms * 8, kThreads, a);
     L1(k_candoff, 1, 1024, a, 0);
     if (hp.mode == DGC_SELECT_EXACT) {
         L1(k_recompact, (unsigned)L.fused_tiles, kThreads, a);
