@@ -16,15 +16,18 @@
 //                 every call (tag + checksum), rebuilt only when they no longer match
 //   sample        gathers g,u,v at the SplitMix64 sample positions, recomputes v' there,
 //                 writes the sample keys and the first radix-select histogram
-//   find/hist x3  radix select of the sampled threshold t (11 + 10 + 10 key bits)
+//   select x2     radix select of the sampled threshold t (11 + 10 + 10 key bits): segments
+//                 whose sample fits on chip in one block each, the rest by the cooperative
+//                 global-memory select (one launch, grid barriers between levels)
 //   stream_tma    THE STREAMING PASS: persistent blocks, bulk-copy pipeline of g,u,v tiles;
 //                 u = fma(m,u,g*scale); v = fma(leak,v,u); candidates (key(v) >= t, or for
 //                 AdaComp the entries at their bin run's maximum, which also raise the bin's
 //                 global maximum) are compacted into each tile's own slots
-//   collect       tile slots -> one index-ordered candidate list (decoupled look-back)
+//   collect(+copy) tile slots -> one index-ordered candidate list (decoupled look-back)
 //   candoff       per-segment candidate ranges; decides who re-selects
 //   recompact     [exact mode, only if the sampled bound was too tight] re-compacts from v
-//   hist/find x6  radix select of the exact k-th (|v|, index) pair among candidates
+//   select x2     radix select of the exact k-th (|v|, index) pair among candidates (on chip,
+//                 then the global-memory levels for larger candidate sets)
 //   emit          writes S in index order (second look-back), clears v (and u with masking)
 //                 of the sent entries; statistics
 //
@@ -36,6 +39,7 @@
 // clipping, the streaming pass without candidates, and a gather of v at the set.
 #include <cmath>
 #include <cstring>
+#include <type_traits>
 
 #include "dgc_device.cuh"
 
@@ -75,7 +79,7 @@ constexpr int kClipTile = 4096;
 constexpr int kHistBins = 2048;
 constexpr int kSamplePerThread = 4;
 constexpr uint64_t kExactSamplePpb = 10000000;    // exact mode samples 1% to bound t from below
-constexpr uint32_t kExactWholeBelow = 32768;      // smaller segments: every entry is a candidate
+constexpr uint32_t kExactWholeBelow = 8192;       // smaller segments: every entry is a candidate
 
 // composite selection key X = (|v| key << 32) | ~index, selected from the top 11+10+10 key
 // bits then 11+11+10 index bits
@@ -117,6 +121,8 @@ struct Ctl {
     uint64_t csum;          // checksum of the cached positions as found
     uint64_t newsum;        // checksum of the rebuilt positions
     uint32_t sum_done;
+    uint32_t bar_count;     // grid barrier of the cooperative select: arrivals, generation
+    uint32_t bar_gen;
     uint32_t pad;
 };
 
@@ -131,7 +137,7 @@ constexpr int kBucketShift = 10;  // cache order: 1024-entry buckets, segment by
 struct Layout {
     size_t ctl, scache, segs, seg_start, samp_off, clip_off, cand_off, clip_part, skeys, spos,
         bcount, histA, histB;
-    size_t st_collect, st_compact, st_emit, cidx, sidx, tcount, binmax, total;
+    size_t st_collect, st_compact, st_emit, cidx, sidx, tcount, tseg, eseg, binmax, total;
     uint64_t max_samples, max_clip_tiles, fused_tiles, emit_tiles, ptiles, cgroups, nbuckets,
         max_bins;
 };
@@ -215,6 +221,8 @@ Layout make_layout(int64_t n, int32_t nseg, const HostParams& hp) {
     L.cidx = take(sizeof(uint32_t) * (size_t)un);
     L.sidx = take(sizeof(uint32_t) * (size_t)un);
     L.tcount = take(sizeof(uint32_t) * (size_t)(L.ptiles + 1));
+    L.tseg = take(sizeof(uint32_t) * (size_t)(L.ptiles + 1));
+    L.eseg = take(sizeof(uint32_t) * 2 * (size_t)(L.emit_tiles + 1));
     L.binmax = take(sizeof(uint32_t) * (size_t)L.max_bins);
     L.total = o;
     return L;
@@ -268,6 +276,8 @@ struct Args {
     uint32_t* cidx;   // candidates, ascending index
     uint32_t* sidx;   // per-tile candidate slots of the streaming pass
     uint32_t* tcount; // per-tile candidate counts, then (k_collect) each tile's first position
+    uint32_t* tseg;   // streaming tile t starts in segment tseg[t]; tseg[ptiles] = nseg - 1
+    uint32_t* eseg;   // emit tile t's candidates lie in segments [eseg[2t], eseg[2t + 1]]
     uint32_t* binmax; // AdaComp: largest |v| key of every bin
     uint64_t max_samples, fused_tiles, emit_tiles, max_clip_tiles, ptiles, cgroups, nbuckets,
         max_bins;
@@ -393,14 +403,40 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
     for (size_t i = tid; i <= a.emit_tiles; i += stride) a.st_emit[i] = 0;
     for (size_t i = tid; i < a.nbuckets; i += stride) a.bcount[i] = 0;
     for (size_t i = tid; i < a.max_bins; i += stride) a.binmax[i] = 0;
+    // the segment of every streaming tile's first entry, searched in the caller's offsets (when
+    // they are invalid, block 0 raises abort and no later kernel reads this)
+    for (size_t t = tid; t <= a.ptiles; t += stride)
+        a.tseg[t] = (t == a.ptiles) ? (uint32_t)(a.nseg - 1)
+                                    : (uint32_t)upper_bound_minus1(a.seg_off, a.nseg,
+                                                                   (int64_t)(t * kPTile));
 }
 
 // ----------------------------------------------------------------------------- clipping
-// Sum of squares of one 4096-entry tile in binary64, split in halves recursively: thread t
-// sums entries [16t, 16t+16) as a 4-level tree, lanes combine with xor-shuffles (pairs of
-// neighbouring 16-entry blocks first), then the 8 warp sums combine pairwise.
+// The sum of squares of a segment: 4096-entry tiles from the segment start (the last padded
+// with zeros), each a complete binary tree, then the tile sums added left to right, all in
+// binary64. binary64 is slow on this part, so the squares (exact in binary64) are built with
+// integer operations and only the additions use the binary64 unit.
+
+// x * x in binary64, exactly, from the bits of x: |x| = m 2^(e' - 150) with e' = max(e, 1), so
+// x^2 = M 2^(2e' - 300), M = m^2 < 2^48, and with p the top bit of M the binary64 exponent is
+// p + 2e' - 300 (never below -298 nor above 208: always a normal binary64).
+__device__ __forceinline__ double exact_square(float x) {
+    const uint32_t a = __float_as_uint(x) & 0x7FFFFFFFu;
+    const uint32_t e = a >> 23;
+    const uint32_t m = e ? ((a & 0x7FFFFFu) | 0x800000u) : a;
+    const uint64_t M = (uint64_t)m * m;
+    const int p = 63 - __clzll((long long)M);
+    const uint64_t ex = (uint64_t)(p + 2 * (int)max(e, 1u) - 300 + 1023);
+    uint64_t bits = (ex << 52) | ((M << ((52 - p) & 63)) & 0xFFFFFFFFFFFFFull);
+    if (a == 0) bits = 0;
+    if (a >= 0x7F800000u) bits = (a == 0x7F800000u) ? 0x7FF0000000000000ull : 0x7FF8000000000000ull;
+    return __longlong_as_double((long long)bits);
+}
+
+// One 4096-entry tile per block: thread t sums entries [16t, 16t+16) as a 4-level tree, then
+// the 256 thread sums combine pairwise in shared memory.
 __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
-    __shared__ double s_w[8];
+    __shared__ double s_t[kThreads];
     __shared__ int s_skip;
     const uint32_t c = blockIdx.x;
     if (threadIdx.x == 0) s_skip = a.ctl->abort || c >= a.ctl->total_clip_tiles;
@@ -416,55 +452,72 @@ __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const float4 x = g4[j];
-            q[4 * j] = (double)x.x * (double)x.x;
-            q[4 * j + 1] = (double)x.y * (double)x.y;
-            q[4 * j + 2] = (double)x.z * (double)x.z;
-            q[4 * j + 3] = (double)x.w * (double)x.w;
+            q[4 * j] = exact_square(x.x);
+            q[4 * j + 1] = exact_square(x.y);
+            q[4 * j + 2] = exact_square(x.z);
+            q[4 * j + 3] = exact_square(x.w);
         }
     } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const uint64_t e = base + i;
-            const double x = (e < d.end) ? (double)a.g[e] : 0.0;
-            q[i] = x * x;
+            q[i] = (e < d.end) ? exact_square(a.g[e]) : 0.0;
         }
     }
 #pragma unroll
     for (int w = 1; w < 16; w <<= 1)
 #pragma unroll
         for (int i = 0; i < 16; i += 2 * w) q[i] = q[i] + q[i + w];
-    double t = q[0];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) t = t + __shfl_xor_sync(kFull, t, o);
-    if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = t;
+    s_t[threadIdx.x] = q[0];
     __syncthreads();
-    if (threadIdx.x == 0) {
-        const double a01 = s_w[0] + s_w[1], a23 = s_w[2] + s_w[3];
-        const double a45 = s_w[4] + s_w[5], a67 = s_w[6] + s_w[7];
-        a.clip_part[c] = (a01 + a23) + (a45 + a67);
+#pragma unroll
+    for (int w = 1; w < kThreads; w <<= 1) {
+        const int i = 2 * w * threadIdx.x;
+        if (i < kThreads) s_t[i] = s_t[i] + s_t[i + w];
+        __syncthreads();
     }
+    if (threadIdx.x == 0) a.clip_part[c] = s_t[0];
 }
 
-// Tile sums left to right; scale = c / sqrt(S) when sqrt(S) > c (binary64, correctly rounded
-// sqrt and division, rounded once to binary32).
-__global__ void k_clip_scale(Args a) {
-    const int s = blockIdx.x * blockDim.x + threadIdx.x;
+// One warp per segment: the tile sums left to right, then scale = c / sqrt(S) when
+// sqrt(S) > c (binary64, correctly rounded sqrt and division, rounded once to binary32). The
+// sum is a chain of dependent additions on lane 0; the other lanes keep the next chunk of tile
+// sums in flight and stage each chunk in shared memory.
+constexpr int kClipScaleWarps = 4;
+constexpr int kClipChunk = 512;
+__global__ void __launch_bounds__(32 * kClipScaleWarps) k_clip_scale(Args a) {
+    __shared__ double s_buf[kClipScaleWarps][kClipChunk];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int s = blockIdx.x * kClipScaleWarps + warp;
     if (a.ctl->abort || s >= a.nseg) return;
-    SegInfo& d = a.segs[s];
-    double S = 0.0;
     const uint32_t t0 = a.clip_off[s], t1 = a.clip_off[s + 1];
-    uint32_t t = t0;
-    for (; t + 8 <= t1; t += 8) {  // eight loads in flight, then the adds in order
-        double p[8];
+    double* buf = s_buf[warp];
+    double r[kClipChunk / 32];
+    auto fetch = [&](uint32_t c0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) p[i] = a.clip_part[t + i];
+        for (int i = 0; i < kClipChunk / 32; ++i) {
+            const uint32_t t = c0 + 32 * i + lane;
+            r[i] = (t < t1) ? a.clip_part[t] : 0.0;
+        }
+    };
+    double S = 0.0;
+    fetch(t0);
+    for (uint32_t c0 = t0; c0 < t1; c0 += kClipChunk) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) S = S + p[i];
+        for (int i = 0; i < kClipChunk / 32; ++i) buf[32 * i + lane] = r[i];
+        __syncwarp();
+        if (c0 + kClipChunk < t1) fetch(c0 + kClipChunk);
+        if (lane == 0) {
+            const uint32_t len = min(t1 - c0, (uint32_t)kClipChunk);
+            for (uint32_t i = 0; i < len; ++i) S = S + buf[i];
+        }
+        __syncwarp();
     }
-    for (; t < t1; ++t) S = S + a.clip_part[t];
-    const double norm = sqrt(S);
-    const double c = (double)a.hp.clip_norm;
-    d.scale = (norm > c) ? (float)(c / norm) : 1.0f;
+    if (lane == 0) {
+        const double norm = sqrt(S);
+        const double c = (double)a.hp.clip_norm;
+        a.segs[s].scale = (norm > c) ? (float)(c / norm) : 1.0f;
+    }
 }
 
 // v <- fma(leak, v, u): with leak = 1 this is the plain sum v + u, rounded once
@@ -698,13 +751,10 @@ __device__ __forceinline__ uint64_t item_x(const Args& a, uint32_t i) {
     return ((uint64_t)key_of(a.v[idx]) << 32) | (uint64_t)(~idx);
 }
 
+// Runs inside the cooperative select, where other blocks change the segment words between
+// levels: those are read past L1 (ld.global.cg).
 template <int kKind>
-__global__ void __launch_bounds__(kThreads) k_hist(Args a, int level) {
-    __shared__ uint32_t s_hist[kHistBins];
-    __shared__ int s_skip;
-    if (threadIdx.x == 0) s_skip = a.ctl->abort || a.ctl->active == 0;
-    __syncthreads();
-    if (s_skip) return;
+__device__ void hist_level(const Args& a, int level, uint32_t* s_hist) {
     const uint32_t* off = kKind == 0 ? a.samp_off : a.cand_off;
     const uint32_t total = off[a.nseg];
     uint32_t* ghist = (level & 1) ? a.histB : a.histA;
@@ -721,12 +771,12 @@ __global__ void __launch_bounds__(kThreads) k_hist(Args a, int level) {
         const int s0 = upper_bound_minus1(off, a.nseg, (uint32_t)c0);
         const int s1 = upper_bound_minus1(off, a.nseg, c1 - 1);
         if (s0 == s1) {
-            if (a.segs[s0].state != kActive) continue;
+            if (__ldcg(&a.segs[s0].state) != kActive) continue;
             if (h.cur != s0) {
                 h.flush(ghist, nbins);
                 h.cur = s0;
             }
-            const uint64_t prefix = a.segs[s0].prefix;
+            const uint64_t prefix = __ldcg(&a.segs[s0].prefix);
             uint64_t xs[kPer];
 #pragma unroll
             for (int r = 0; r < kPer; ++r) {  // all loads first, then the counting
@@ -743,9 +793,9 @@ __global__ void __launch_bounds__(kThreads) k_hist(Args a, int level) {
             for (uint32_t i = (uint32_t)c0 + threadIdx.x; i < c1; i += kThreads) {
                 const int s = upper_bound_minus1(off, a.nseg, i);
                 const SegInfo& d = a.segs[s];
-                if (d.state != kActive) continue;
+                if (__ldcg(&d.state) != kActive) continue;
                 const uint64_t x = item_x<kKind>(a, i);
-                if ((x >> (shift + bits)) == d.prefix)
+                if ((x >> (shift + bits)) == __ldcg(&d.prefix))
                     atomicAdd(&ghist[(size_t)s * kHistBins + ((x >> shift) & mask)], 1u);
             }
         }
@@ -754,50 +804,44 @@ __global__ void __launch_bounds__(kThreads) k_hist(Args a, int level) {
 }
 
 // ----------------------------------------------------------------- radix select: find
-// One block per segment: walk the level's bins from the top until `need` items are covered.
-// That bin extends the prefix. For the sample select the prefix after three levels is the
-// threshold key t. For the candidate select, once the bin holds exactly the items still
-// needed, everything at or above the prefix is selected (sel_x = prefix << shift).
-template <int kKind>
-__global__ void __launch_bounds__(kThreads) k_find(Args a, int level) {
-    __shared__ uint32_t s_scan[33];
-    __shared__ uint32_t s_bin, s_above, s_cnt;
-    __shared__ int s_found;
-    __shared__ int s_skip;
-    const int s = blockIdx.x;
-    SegInfo& d = a.segs[s];
-    if (threadIdx.x == 0) s_skip = a.ctl->abort || d.state != kActive;
-    __syncthreads();
-    if (s_skip) return;
-    const int bits = c_bits[level], shift = c_shift[level];
-    const int nbins = 1 << bits;
-    constexpr int kMaxPer = kHistBins / kThreads;  // 8
-    const int per = nbins / kThreads;              // 4 or 8
-    uint32_t* hist = ((level & 1) ? a.histB : a.histA) + (size_t)s * kHistBins;
+// Walk the bins of `hist` from the top until `need` items are covered (block-wide, kBlock
+// threads; thread t owns the positions [t*per, t*per + per) counted from the top bin down).
+// After the call's barrier r->found says whether the walk ended inside the histogram, r->bin
+// is that bin, r->above the items in higher bins and r->cnt the bin's own count. The bins read
+// are set to zero afterwards (visible after the caller's next barrier).
+struct FindRes {
+    uint32_t bin, above, cnt;
+    int found;
+};
+
+template <int kBlock, bool kCG = false>
+__device__ void find_from_top(uint32_t* hist, int nbins, uint32_t need, uint32_t* s_scan,
+                              FindRes* r) {
+    constexpr int kMaxPer = kHistBins / kBlock;
+    const int per = nbins / kBlock;
     uint32_t h[kMaxPer];
     uint32_t local = 0;
-    // thread t owns positions [t*per, t*per + per) counted from the top bin down
 #pragma unroll
     for (int i = 0; i < kMaxPer; ++i) {
         h[i] = 0;
         if (i < per) {
-            h[i] = hist[nbins - 1 - (threadIdx.x * per + i)];
+            const uint32_t* p = hist + (nbins - 1 - (threadIdx.x * per + i));
+            h[i] = kCG ? __ldcg(p) : *p;
             local += h[i];
         }
     }
-    if (threadIdx.x == 0) s_found = 0;
+    if (threadIdx.x == 0) r->found = 0;
     uint32_t tot;
-    const uint32_t ex = block_excl_scan<kThreads>(local, s_scan, &tot);
-    const uint32_t need = d.need;
+    const uint32_t ex = block_excl_scan<kBlock>(local, s_scan, &tot);
     if (ex < need && need <= ex + local) {
         uint32_t cum = ex;
 #pragma unroll
         for (int i = 0; i < kMaxPer; ++i) {
             if (i < per && cum < need && need <= cum + h[i]) {
-                s_bin = (uint32_t)(nbins - 1 - (threadIdx.x * per + i));
-                s_above = cum;
-                s_cnt = h[i];
-                s_found = 1;
+                r->bin = (uint32_t)(nbins - 1 - (threadIdx.x * per + i));
+                r->above = cum;
+                r->cnt = h[i];
+                r->found = 1;
             }
             cum += (i < per) ? h[i] : 0;
         }
@@ -806,35 +850,257 @@ __global__ void __launch_bounds__(kThreads) k_find(Args a, int level) {
 #pragma unroll
     for (int i = 0; i < kMaxPer; ++i)
         if (i < per) hist[nbins - 1 - (threadIdx.x * per + i)] = 0;
-    if (threadIdx.x != 0) return;
-    if (!s_found) {  // fewer items than needed: cannot happen for a consistent table
+}
+
+// One level's outcome: the bin extends the prefix. True when the selection is complete: for
+// the sample select the prefix after three levels is the threshold key t; for the candidate
+// select, once the bin holds exactly the items still needed (or at the last level), everything
+// at or above prefix << shift is selected.
+template <int kKind>
+__device__ __forceinline__ bool select_step(int level, int bits, const FindRes& r,
+                                            uint64_t& prefix, uint32_t& need) {
+    prefix = (prefix << bits) | r.bin;
+    const uint32_t need2 = need - r.above;
+    need = need2;
+    return kKind == 0 ? level == 2 : (r.cnt == need2 || level == 5);
+}
+
+// The end of a segment's select: the threshold key (kind 0) or sel_x (kind 1).
+template <int kKind>
+__device__ __forceinline__ void select_done(const Args& a, SegInfo& d, bool found, int level,
+                                            uint64_t prefix) {
+    if (!found) {  // fewer items than needed: cannot happen for a consistent table
         report(a.status, DGC_EINVAL);
         d.sel_x = 0;
-        d.state = kIdle;
-        atomicSub(&a.ctl->active, 1u);
-        return;
+    } else if (kKind == 0) {
+        d.thresh = (uint32_t)prefix;
+    } else {
+        d.sel_x = prefix << c_shift[level];
     }
-    const uint64_t prefix = (d.prefix << bits) | s_bin;
-    const uint32_t need2 = need - s_above;
-    if (kKind == 0) {
-        if (level == 2) {
-            d.thresh = (uint32_t)prefix;
-            d.state = kIdle;
-            atomicSub(&a.ctl->active, 1u);
+    d.state = kIdle;
+    atomicSub(&a.ctl->active, 1u);
+}
+
+// Grid-wide barrier of a cooperative launch (every block resident). Thread 0 of each block
+// arrives on a counter; the last arrival resets it and bumps the generation the others poll.
+// The poll is bounded: past spin_limit the block reports DGC_ETIMEOUT, raises abort and
+// returns false (so does every block that then sees abort).
+__device__ bool grid_barrier(const Args& a, int* s_ok) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t g = ld_relaxed_u32(&a.ctl->bar_gen);
+        __threadfence();
+        int ok = 1;
+        if (atomicAdd(&a.ctl->bar_count, 1u) == gridDim.x - 1) {
+            a.ctl->bar_count = 0;
+            __threadfence();
+            atomicExch(&a.ctl->bar_gen, g + 1);
         } else {
-            d.prefix = prefix;
-            d.need = need2;
+            uint32_t spins = 0;
+            while (ld_relaxed_u32(&a.ctl->bar_gen) == g) {
+                if (++spins > a.spin_limit) {
+                    report(a.status, DGC_ETIMEOUT);
+                    atomicExch(&a.ctl->abort, 1);
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        __threadfence();
+        *s_ok = ok && !ld_relaxed_u32((const uint32_t*)&a.ctl->abort);
+    }
+    __syncthreads();
+    return *s_ok != 0;
+}
+
+// The global-memory radix select for the segments the on-chip select left active, every level
+// in one cooperative launch: a level counts (all blocks, grid-stride over the items), then
+// after a grid barrier blocks take the active segments and walk their histograms from the top,
+// then a grid barrier. The sample select's first level was counted by the sampling
+// kernel. The kernel ends as soon as no segment is active, at once when none was to begin
+// with. Segment words and histograms change between levels, so they are read past L1.
+template <int kKind>
+__global__ void __launch_bounds__(kThreads) k_select_global(Args a) {
+    __shared__ uint32_t s_hist[kHistBins];
+    __shared__ uint32_t s_scan[33];
+    __shared__ FindRes s_r;
+    __shared__ int s_go, s_bar;
+    constexpr int kLevels = kKind == 0 ? 3 : 6;
+    if (threadIdx.x == 0)
+        s_go = !ld_relaxed_u32((const uint32_t*)&a.ctl->abort) &&
+               ld_relaxed_u32(&a.ctl->active) != 0;
+    __syncthreads();
+    if (!s_go) return;  // the same words for every block: no block reaches a barrier alone
+    for (int level = 0; level < kLevels; ++level) {
+        const int bits = c_bits[level];
+        if (kKind == 1 || level > 0) {
+            hist_level<kKind>(a, level, s_hist);
+            if (!grid_barrier(a, &s_bar)) return;
+        }
+        uint32_t* hbase = (level & 1) ? a.histB : a.histA;
+        for (int s = blockIdx.x; s < a.nseg; s += gridDim.x) {
+            SegInfo& d = a.segs[s];
+            if (__ldcg(&d.state) != kActive) continue;  // only this block changes it, below
+            const uint32_t need0 = __ldcg(&d.need);
+            find_from_top<kThreads, true>(hbase + (size_t)s * kHistBins, 1 << bits, need0,
+                                          s_scan, &s_r);
+            if (threadIdx.x == 0) {
+                uint64_t prefix = __ldcg(&d.prefix);
+                uint32_t need = need0;
+                if (!s_r.found || select_step<kKind>(level, bits, s_r, prefix, need)) {
+                    select_done<kKind>(a, d, s_r.found, level, prefix);
+                } else {
+                    d.prefix = prefix;
+                    d.need = need;
+                }
+            }
+        }
+        if (!grid_barrier(a, &s_bar)) return;
+        if (threadIdx.x == 0) s_go = ld_relaxed_u32(&a.ctl->active) != 0;
+        __syncthreads();
+        if (!s_go) return;
+    }
+}
+
+// ------------------------------------------------------ radix select: whole segment on chip
+// One block per active segment whose items fit in shared memory: every level runs on chip, and
+// each level keeps only the items that still match the prefix (each warp compacts its own share
+// in place). Segments with more items stay active for the global-memory levels
+// (k_select_global). The segment's contiguous items (sample keys, or candidate indices) arrive
+// in one bulk copy; for candidates the keys of v at those indices are then gathered with every
+// load in flight at once, and counted for the first level as they arrive. For the sample select
+// the first level's counts come from the sampling kernel's histogram, cleared here as the global
+// walk would. Two blocks fit on an SM, so up to 2 x 152 segments run in one wave.
+constexpr int kSmallThreads = 512;
+constexpr size_t kSmallBytes = 100u * 1024u;
+template <int kKind>
+__global__ void __launch_bounds__(kSmallThreads, 2) k_select_small(Args a) {
+    constexpr uint32_t kArrays = kKind == 0 ? 1 : 2;  // sample keys | candidate indices, keys
+    // the copy starts at the 16-byte boundary at or before the first item: 3 words of slack
+    constexpr uint32_t kCap = (uint32_t)(kSmallBytes / (4 * kArrays)) - 4;
+    constexpr int kW = kSmallThreads / 32;
+    constexpr int kLevels = kKind == 0 ? 3 : 6;
+    constexpr int kBatch = 16;
+    extern __shared__ __align__(16) unsigned char s_dyn[];
+    __shared__ uint32_t s_hist[kHistBins];
+    __shared__ uint32_t s_scan[33];
+    __shared__ FindRes s_r;
+    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ int s_fail;
+    const int s = blockIdx.x;
+    SegInfo& d = a.segs[s];
+    if (a.ctl->abort || d.state != kActive) return;  // every thread reads the same words
+    const uint32_t* off = kKind == 0 ? a.samp_off : a.cand_off;
+    const uint32_t i0 = off[s], C = off[s + 1] - i0;
+    if (C > kCap) return;
+    uint32_t* sraw = reinterpret_cast<uint32_t*>(s_dyn);
+    uint32_t* s_a = sraw + (i0 & 3u);  // item i: key (kind 0) or candidate index (kind 1)
+    uint32_t* s_k = sraw + kCap + 4;   // kind 1: key of item i
+    if (threadIdx.x == 0) {
+        s_fail = 0;
+        mbar_init(&s_bar, 1);
+        mbar_init_fence();
+        // whole 16-byte units from the boundary at or before item 0; the workspace regions are
+        // padded to 256 bytes, so the last unit stays inside the array's region
+        const uint32_t bytes = (((i0 & 3u) + C + 3u) & ~3u) * 4u;
+        mbar_arrive_expect_tx(&s_bar, bytes);
+        if (bytes) bulk_g2s(sraw, (kKind == 0 ? a.skeys : a.cidx) + (i0 & ~3u), bytes, &s_bar);
+    }
+    if (kKind == 0) {
+        uint32_t* gh = a.histA + (size_t)s * kHistBins;
+        for (int b = threadIdx.x; b < kHistBins; b += kSmallThreads) {
+            s_hist[b] = gh[b];
+            gh[b] = 0;
         }
     } else {
-        if (s_cnt == need2 || level == 5) {
-            d.sel_x = prefix << shift;
-            d.state = kIdle;
-            atomicSub(&a.ctl->active, 1u);
-        } else {
-            d.prefix = prefix;
-            d.need = need2;
+        for (int b = threadIdx.x; b < kHistBins; b += kSmallThreads) s_hist[b] = 0;
+    }
+    __syncthreads();  // the mbarrier is initialised before anyone polls it
+    {
+        uint32_t spins = 0;
+        while (!mbar_try_wait(&s_bar, 0)) {
+            if (++spins > kMbarSpinLimit) {
+                s_fail = 1;
+                break;
+            }
         }
     }
+    __syncthreads();
+    if (s_fail) {  // the copy never landed: report, give it one more bounded wait, leave
+        if (threadIdx.x == 0) {
+            report(a.status, DGC_ETIMEOUT);
+            atomicExch(&a.ctl->abort, 1);
+        }
+        for (uint32_t k = 0; k < kMbarSpinLimit && !mbar_try_wait(&s_bar, 0); ++k) {
+        }
+        return;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t R = (C + kW - 1) / kW;
+    const uint32_t wb = min(C, (uint32_t)warp * R), we = min(C, wb + R);
+    uint32_t wn = we - wb;  // items this warp still holds, at the front of its share
+    if (kKind == 1) {
+        for (uint32_t j0 = wb; j0 < we; j0 += 32 * kBatch) {
+            float vr[kBatch];
+#pragma unroll
+            for (int r = 0; r < kBatch; ++r) {
+                const uint32_t i = j0 + 32 * r + lane;
+                vr[r] = (i < we) ? a.v[s_a[i]] : 0.f;
+            }
+#pragma unroll
+            for (int r = 0; r < kBatch; ++r) {
+                const uint32_t i = j0 + 32 * r + lane;
+                if (i < we) {
+                    const uint32_t key = key_of(vr[r]);
+                    s_k[i] = key;
+                    atomicAdd(&s_hist[key >> 20], 1u);  // X >> 52: the first level's digit
+                }
+            }
+        }
+        __syncthreads();
+    }
+    uint64_t prefix = 0;
+    uint32_t need = d.need;
+    bool done = false, found = true;
+    int level = 0;
+    for (; level < kLevels; ++level) {
+        const int shift = c_shift[level], bits = c_bits[level];
+        const uint32_t mask = (1u << bits) - 1u;
+        if (level > 0) {
+            uint32_t keep = 0;
+            for (uint32_t j = 0; j < wn; j += 32) {
+                const bool in = j + lane < wn;
+                const uint32_t ia = in ? s_a[wb + j + lane] : 0u;
+                const uint32_t ik = (kKind == 1 && in) ? s_k[wb + j + lane] : 0u;
+                const uint64_t x = kKind == 0 ? ((uint64_t)ia << 32)
+                                              : (((uint64_t)ik << 32) | (uint64_t)(~ia));
+                const bool match = in && (x >> (shift + bits)) == prefix;
+                const unsigned mm = __ballot_sync(kFull, match);
+                if (match) {
+                    atomicAdd(&s_hist[(uint32_t)(x >> shift) & mask], 1u);
+                    // write position <= every position read in this round: in place is safe
+                    const uint32_t w = wb + keep + __popc(mm & ((1u << lane) - 1u));
+                    s_a[w] = ia;
+                    if (kKind == 1) s_k[w] = ik;
+                }
+                keep += __popc(mm);
+            }
+            wn = keep;
+            __syncthreads();
+        }
+        find_from_top<kSmallThreads>(s_hist, 1 << bits, need, s_scan, &s_r);
+        __syncthreads();
+        if (!s_r.found) {
+            found = false;
+            break;
+        }
+        if (select_step<kKind>(level, bits, s_r, prefix, need)) {
+            done = true;
+            break;
+        }
+    }
+    if (threadIdx.x == 0) select_done<kKind>(a, d, found && done, min(level, kLevels - 1), prefix);
 }
 
 // ------------------------------------------------------------- exact-mode re-compaction
@@ -921,11 +1187,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_recompact(Args a) {
 // with coalesced 16-byte stores. A tile's candidates are compacted, in index order, into the
 // tile's own slot range sidx[base, base + count) and its count into tcount[tile]: no block
 // ever waits on another, and k_collect turns the counts into global offsets afterwards.
+// In a tile that crosses a segment boundary, entry i lies in one of the segments
+// [s0, s0 + ns) (from the tile table), found by a short search.
+__device__ __forceinline__ const SegInfo& tile_segment(const Args& a, int s0, int ns, uint32_t i) {
+    return a.segs[s0 + upper_bound_minus1(a.seg_start + s0, ns, i)];
+}
+
 template <bool kKeepU>
 __device__ __forceinline__ void stream_compute(const Args& a, const float* sg, uint64_t base,
-                                               uint32_t len, bool uniform, float scale0,
-                                               uint32_t thresh0, float4 (&uu)[kPRows],
-                                               float4 (&vv)[kPRows], uint32_t& flags) {
+                                               uint32_t len, bool uniform, int s0, int ns,
+                                               float scale0, uint32_t thresh0,
+                                               float4 (&uu)[kPRows], float4 (&vv)[kPRows],
+                                               uint32_t& flags) {
     const int tid = threadIdx.x;
     const uint32_t bulk = len & ~3u;
     flags = 0;
@@ -959,8 +1232,7 @@ __device__ __forceinline__ void stream_compute(const Args& a, const float* sg, u
             float scale = scale0;
             uint32_t t = thresh0;
             if (!uniform) {
-                const SegInfo& d = a.segs[upper_bound_minus1(a.seg_start, a.nseg,
-                                                             (uint32_t)(base + off + e))];
+                const SegInfo& d = tile_segment(a, s0, ns, (uint32_t)(base + off + e));
                 scale = d.scale;
                 t = d.thresh;
             }
@@ -982,6 +1254,7 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
     __shared__ __align__(8) uint64_t s_bar[kPStages];
     __shared__ uint32_t s_tile[kPStages];
     __shared__ int s_uniform[kPStages];
+    __shared__ int s_seg0[kPStages], s_nseg[kPStages];  // the tile's segments [s0, s0 + ns)
     __shared__ float s_scale[kPStages];
     __shared__ uint32_t s_thresh[kPStages];
     __shared__ uint32_t s_binA[kPStages];  // AdaComp: global index of the tile's first bin
@@ -992,15 +1265,30 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
     const uint64_t n = a.n;
     const uint32_t ntiles = (uint32_t)((n + kPTile - 1) / kPTile);
 
-    // thread 0 owns the pipeline: it takes a ticket, notes the tile's segment, and starts the
-    // tile's three bulk copies; the mbarrier phase publishes all of it to the block
+    // thread 0 owns the pipeline: it takes a ticket, notes the tile's segments, and starts the
+    // tile's three bulk copies; the mbarrier phase publishes all of it to the block. Tickets are
+    // taken two issues ahead and their tile-table entries read one issue ahead, so neither the
+    // atomic's round trip nor the table read (a miss while HBM streams) waits in line with the
+    // copies. Tickets rise within a block, so the block stops at its first tile past the end
+    // having handled every tile it took before; the tickets it still holds are past the end.
+    uint32_t t_next = 0, t_next2 = 0;  // the next two tickets
+    uint32_t s0_next = 0, s1_next = 0;  // tile-table entries of t_next (read when t_next < ntiles)
     auto issue = [&](int st) {
-        const uint32_t t = atomicAdd(&a.ctl->ticket_fused, 1u);
+        const uint32_t t = t_next;
+        const int s0 = (int)s0_next, s1 = (int)s1_next;
+        t_next = t_next2;
+        if (t_next < ntiles) {
+            s0_next = a.tseg[t_next];
+            s1_next = a.tseg[t_next + 1];
+        }
+        t_next2 = atomicAdd(&a.ctl->ticket_fused, 1u);
         s_tile[st] = t;
         if (t < ntiles) {
             const uint64_t base = (uint64_t)t * kPTile;
             const uint32_t len = (uint32_t)umin64(kPTile, n - base);
-            const SegInfo& d = a.segs[upper_bound_minus1(a.seg_start, a.nseg, (uint32_t)base)];
+            const SegInfo& d = a.segs[s0];
+            s_seg0[st] = s0;
+            s_nseg[st] = s1 - s0 + 1;
             s_uniform[st] = (d.end >= base + len) ? 1 : 0;
             s_scale[st] = d.scale;
             s_thresh[st] = d.thresh;
@@ -1027,6 +1315,12 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
         if (!s_skip) {
             for (int st = 0; st < kPStages; ++st) mbar_init(&s_bar[st], 1);
             mbar_init_fence();
+            t_next = atomicAdd(&a.ctl->ticket_fused, 1u);
+            t_next2 = atomicAdd(&a.ctl->ticket_fused, 1u);
+            if (t_next < ntiles) {
+                s0_next = a.tseg[t_next];
+                s1_next = a.tseg[t_next + 1];
+            }
             for (int st = 0; st < kPStages; ++st) issue(st);
         }
     }
@@ -1055,7 +1349,7 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
         float4 uu[kPRows], vv[kPRows];
         uint32_t flags;
         stream_compute<true>(a, s_stage + (size_t)st * kPStageFloats, base, len, s_uniform[st],
-                             s_scale[st], s_thresh[st], uu, vv, flags);
+                             s_seg0[st], s_nseg[st], s_scale[st], s_thresh[st], uu, vv, flags);
         if constexpr (kSel == 2) flags = 0;  // the shared set is given: no candidates
         if constexpr (kSel == 1) {
             // AdaComp without a block barrier: each warp row (128 consecutive entries) finds the
@@ -1163,7 +1457,7 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
                         const uint32_t key = key_of(reinterpret_cast<const float*>(&vv[r])[e]);
                         if (off < len && key) {
                             const uint32_t i = (uint32_t)(base + off);
-                            const SegInfo& d = a.segs[upper_bound_minus1(a.seg_start, a.nseg, i)];
+                            const SegInfo& d = tile_segment(a, s_seg0[st], s_nseg[st], i);
                             atomicMax(a.binmax + d.binbase + (i - d.start) / L, key);
                             flags |= 1u << (4 * r + e);
                         }
@@ -1296,6 +1590,8 @@ __global__ void __launch_bounds__(kThreads) k_collect_copy(Args a) {
 // ------------------------------------------------------------------- candidate ranges
 // One block: per-segment candidate ranges by binary search of the ascending candidate
 // indices, then who selects among them. pass 1 only runs after an exact-mode re-compaction.
+// In pass 0 the list is still laid out by streaming tile (k_collect left each tile's first
+// position in tcount), so the first candidate at or past x lies in x's tile's own range.
 __global__ void __launch_bounds__(1024) k_candoff(Args a, int pass) {
     __shared__ uint32_t s_active;
     __shared__ int s_skip;
@@ -1307,9 +1603,15 @@ __global__ void __launch_bounds__(1024) k_candoff(Args a, int pass) {
         s_active = 0;
     }
     const uint32_t total = a.ctl->total_cand;
+    const uint32_t ntiles = (uint32_t)a.ptiles;
     for (int s = threadIdx.x; s <= a.nseg; s += blockDim.x) {
         const uint32_t x = a.seg_start[s];
         uint32_t lo = 0, hi = total;  // first candidate index >= x
+        const uint32_t t = x / kPTile;
+        if (pass == 0 && t < ntiles) {
+            lo = a.tcount[t];
+            hi = (t + 1 < ntiles) ? a.tcount[t + 1] : total;
+        }
         while (lo < hi) {
             const uint32_t mid = (lo + hi) >> 1;
             if (a.cidx[mid] < x) lo = mid + 1; else hi = mid;
@@ -1317,6 +1619,13 @@ __global__ void __launch_bounds__(1024) k_candoff(Args a, int pass) {
         a.cand_off[s] = (s == a.nseg) ? total : lo;
     }
     __syncthreads();
+    // the segments of every emit tile's first and last candidate
+    const uint32_t etiles = (total + kEmitTile - 1) / kEmitTile;
+    for (uint32_t t = threadIdx.x; t < etiles; t += blockDim.x) {
+        const uint32_t f0 = t * kEmitTile, f1 = (uint32_t)umin64(total, (uint64_t)f0 + kEmitTile) - 1u;
+        a.eseg[2 * t] = (uint32_t)upper_bound_minus1(a.cand_off, a.nseg, f0);
+        a.eseg[2 * t + 1] = (uint32_t)upper_bound_minus1(a.cand_off, a.nseg, f1);
+    }
     uint32_t any_failed = 0, active = 0;
     for (int s = threadIdx.x; s < a.nseg; s += blockDim.x) {
         SegInfo& d = a.segs[s];
@@ -1373,6 +1682,8 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
         const uint32_t tile = s_tile;
         if (tile >= ntiles) break;
         const uint64_t base = (uint64_t)tile * kEmitTile;
+        // the tile's candidates lie in segments [es0, es0 + ens) (from k_candoff): short searches
+        const int es0 = (int)a.eseg[2 * tile], ens = (int)a.eseg[2 * tile + 1] - es0 + 1;
         uint32_t sel = 0;
         uint32_t idx[kEmitRows * 4];
         float val[kEmitRows * 4];
@@ -1387,7 +1698,7 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
                 if (i < total) {
                     idx[q] = a.cidx[i];
                     val[q] = a.v[idx[q]];
-                    const int s = upper_bound_minus1(a.cand_off, a.nseg, (uint32_t)i);
+                    const int s = es0 + upper_bound_minus1(a.cand_off + es0, ens, (uint32_t)i);
                     seg[q] = s;
                     const SegInfo& d = a.segs[s];
                     if (a.hp.bin) {  // AdaComp: the candidate reaches its bin's largest key
@@ -1610,6 +1921,8 @@ Args make_args(const float* g, float* u, float* v, int64_t n, const int64_t* seg
     a.cidx = reinterpret_cast<uint32_t*>(w + L.cidx);
     a.sidx = reinterpret_cast<uint32_t*>(w + L.sidx);
     a.tcount = reinterpret_cast<uint32_t*>(w + L.tcount);
+    a.tseg = reinterpret_cast<uint32_t*>(w + L.tseg);
+    a.eseg = reinterpret_cast<uint32_t*>(w + L.eseg);
     a.binmax = reinterpret_cast<uint32_t*>(w + L.binmax);
     a.max_samples = L.max_samples;
     a.fused_tiles = L.fused_tiles;
@@ -1632,8 +1945,8 @@ void stream_attributes() {
                          (int)cudaSharedmemCarveoutMaxShared);
 }
 
-// The streaming pass: persistent blocks, kPBlocksPerSM per SM (at most one per tile).
-void launch_stream_pass(int sel, const Args& a, uint64_t ptiles, int sms, cudaStream_t s) {
+// Shared-memory limits of the kernels that need more than 48 KiB, once per device.
+void set_kernel_attributes() {
     static bool attr_set[128] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1641,8 +1954,34 @@ void launch_stream_pass(int sel, const Args& a, uint64_t ptiles, int sms, cudaSt
         stream_attributes<0>();
         stream_attributes<1>();
         stream_attributes<2>();
+        cudaFuncSetAttribute(k_select_small<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmallBytes);
+        cudaFuncSetAttribute(k_select_small<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmallBytes);
         attr_set[dev] = true;
     }
+}
+
+// Blocks of the cooperative select: all resident at once, up to 4 per SM (more loads in flight
+// over the items), once per device.
+unsigned cooperative_select_grid(int sms) {
+    static int per_sm[128] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int b = (dev >= 0 && dev < 128) ? per_sm[dev] : 0;
+    if (b == 0) {
+        int b0 = 0, b1 = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, k_select_global<0>, kThreads, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k_select_global<1>, kThreads, 0);
+        b = std::max(1, std::min(4, std::min(b0, b1)));
+        if (dev >= 0 && dev < 128) per_sm[dev] = b;
+    }
+    return (unsigned)(b * sms);
+}
+
+// The streaming pass: persistent blocks, kPBlocksPerSM per SM (at most one per tile).
+void launch_stream_pass(int sel, const Args& a, uint64_t ptiles, int sms, cudaStream_t s) {
+    set_kernel_attributes();
     const unsigned pgrid = (unsigned)std::min<uint64_t>((uint64_t)sms * kPBlocksPerSM, ptiles);
     if (sel == 1)
         k_stream_tma<1><<<pgrid, kThreads, kPSmemBytes, s>>>(a);
@@ -1691,13 +2030,14 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
         ++launches;
     };
     const size_t zero_work = (size_t)nseg * kHistBins + L.fused_tiles + L.emit_tiles +
-                             L.nbuckets + L.max_bins + 2;
+                             L.nbuckets + L.max_bins + L.ptiles + 3;
     const unsigned plan_grid = (unsigned)std::min<size_t>((zero_work + 1023) / 1024 + 1,
                                                           (size_t)sms * 2);
     L1(k_plan, plan_grid, 1024, a);
     if (hp.clip_on) {
         L1(k_clip_tiles, (unsigned)L.max_clip_tiles, kThreads, a);
-        L1(k_clip_scale, (unsigned)((nseg + 255) / 256), 256, a);
+        L1(k_clip_scale, (unsigned)((nseg + kClipScaleWarps - 1) / kClipScaleWarps),
+           32 * kClipScaleWarps, a);
     }
     const unsigned cgrid = (unsigned)std::max<uint64_t>(
         1, std::min<uint64_t>((uint64_t)sms * 4, (L.max_samples + kThreads - 1) / kThreads));
@@ -1710,12 +2050,29 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     const uint64_t sgrid = (L.max_samples + kThreads * kSamplePerThread - 1) /
                            (kThreads * kSamplePerThread);
     L1(k_sample, (unsigned)sgrid, kThreads, a);
-    const unsigned hist_grid = (unsigned)sms * 8;  // more loads in flight over the sample keys
-    L1(k_find<0>, (unsigned)nseg, kThreads, a, 0);
-    L1(k_hist<0>, hist_grid, kThreads, a, 1);
-    L1(k_find<0>, (unsigned)nseg, kThreads, a, 1);
-    L1(k_hist<0>, hist_grid, kThreads, a, 2);
-    L1(k_find<0>, (unsigned)nseg, kThreads, a, 2);
+    const bool selects = hp.mode != DGC_SELECT_ADACOMP;  // AdaComp keeps every segment idle
+    set_kernel_attributes();
+    const unsigned sel_grid = cooperative_select_grid(sms);
+    bool launch_failed = false;
+    auto global_select = [&](int kind) {
+        void* args[] = {&a};
+        const void* k = kind == 0 ? (const void*)k_select_global<0> : (const void*)k_select_global<1>;
+        if (cudaLaunchCooperativeKernel(k, dim3(sel_grid), dim3(kThreads), args, 0, s) !=
+            cudaSuccess)
+            launch_failed = true;
+        ++launches;
+    };
+    auto small_select = [&](int kind) {
+        if (kind == 0)
+            k_select_small<0><<<(unsigned)nseg, kSmallThreads, kSmallBytes, s>>>(a);
+        else
+            k_select_small<1><<<(unsigned)nseg, kSmallThreads, kSmallBytes, s>>>(a);
+        ++launches;
+    };
+    if (selects) {
+        small_select(0);
+        global_select(0);
+    }
     const cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
     if (pb && pe) record_marker(pb, s);
     if (n > 0) {
@@ -1730,15 +2087,15 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
         L1(k_recompact, (unsigned)L.fused_tiles, kThreads, a);
         L1(k_candoff, 1, 1024, a, 1);
     }
-    for (int level = 0; level < 6; ++level) {
-        L1(k_hist<1>, hist_grid, kThreads, a, level);
-        L1(k_find<1>, (unsigned)nseg, kThreads, a, level);
+    if (selects) {
+        small_select(1);
+        global_select(1);
     }
     const unsigned emit_grid = (unsigned)std::max<uint64_t>(
         1, std::min<uint64_t>((uint64_t)sms * 4, L.emit_tiles));
     L1(k_emit, emit_grid, kThreads, a);
     dgc_internal_count_launches(launches);
-    if (cudaPeekAtLastError() != cudaSuccess) {
+    if (launch_failed || cudaPeekAtLastError() != cudaSuccess) {
         cudaGetLastError();
         return DGC_ECUDA;
     }
@@ -1779,7 +2136,7 @@ extern "C" int dgc_compress_shared(const float* g, float* u, float* v, int64_t n
         ++launches;
     };
     const size_t zero_work = (size_t)nseg * kHistBins + L.fused_tiles + L.emit_tiles +
-                             L.nbuckets + L.max_bins + 2;
+                             L.nbuckets + L.max_bins + L.ptiles + 3;
     const unsigned plan_grid = (unsigned)std::min<size_t>((zero_work + 1023) / 1024 + 1,
                                                           (size_t)sms * 2);
     const unsigned jgrid = (unsigned)std::max<uint64_t>(
@@ -1788,7 +2145,8 @@ extern "C" int dgc_compress_shared(const float* g, float* u, float* v, int64_t n
     L1(k_shared_check, jgrid, kThreads, a, idx, count, (uint64_t)max_count);
     if (hp.clip_on) {
         L1(k_clip_tiles, (unsigned)L.max_clip_tiles, kThreads, a);
-        L1(k_clip_scale, (unsigned)((nseg + 255) / 256), 256, a);
+        L1(k_clip_scale, (unsigned)((nseg + kClipScaleWarps - 1) / kClipScaleWarps),
+           32 * kClipScaleWarps, a);
     }
     const cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
     if (pb && pe) record_marker(pb, s);
