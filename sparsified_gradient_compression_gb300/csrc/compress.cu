@@ -10,10 +10,11 @@
 // segment table and counters the previous ones left in the workspace, so no host round trip):
 //
 //   plan          segment table: k, sample counts, seeds, bins; validates seg_off; zeroes counters
-//   clip_tiles    [clipping] binary64 pairwise sum of g^2 per 4096-entry clip tile
-//   clip_scale    [clipping] tile sums left to right -> per-segment scale
-//   cache_*       [sampled, exact] the sample positions, kept sorted in the workspace; checked
-//                 every call (tag + checksum), rebuilt only when they no longer match
+//   clip_tiles    [clipping] binary64 pairwise sum of g^2 per 4096-entry clip tile; the block
+//                 finishing a segment's last tile adds its tile sums left to right -> scale
+//   cache         [sampled, exact] the sample positions, kept sorted in the workspace; checked
+//                 every call (tag + checksum), rebuilt only when they no longer match (one
+//                 cooperative launch)
 //   sample        gathers g,u,v at the SplitMix64 sample positions, recomputes v' there,
 //                 writes the sample keys and the first radix-select histogram
 //   select x2     radix select of the sampled threshold t (11 + 10 + 10 key bits): segments
@@ -116,11 +117,9 @@ struct Ctl {
     uint32_t ticket_fused, ticket_compact, ticket_emit, ticket_collect;
     uint32_t total_samples, total_clip_tiles, total_cand, total_sent;
     uint32_t emit_done;
-    uint32_t rebuild;       // the cached sample positions must be rebuilt this call
     uint64_t tag;           // what the sample positions depend on, for this call
     uint64_t csum;          // checksum of the cached positions as found
     uint64_t newsum;        // checksum of the rebuilt positions
-    uint32_t sum_done;
     uint32_t bar_count;     // grid barrier of the cooperative select: arrivals, generation
     uint32_t bar_gen;
     uint32_t pad;
@@ -137,7 +136,8 @@ constexpr int kBucketShift = 10;  // cache order: 1024-entry buckets, segment by
 struct Layout {
     size_t ctl, scache, segs, seg_start, samp_off, clip_off, cand_off, clip_part, skeys, spos,
         bcount, histA, histB;
-    size_t st_collect, st_compact, st_emit, cidx, sidx, tcount, tseg, eseg, binmax, total;
+    size_t st_collect, st_compact, st_emit, cidx, sidx, tcount, tseg, eseg, clip_cnt, binmax,
+        total;
     uint64_t max_samples, max_clip_tiles, fused_tiles, emit_tiles, ptiles, cgroups, nbuckets,
         max_bins;
 };
@@ -223,6 +223,7 @@ Layout make_layout(int64_t n, int32_t nseg, const HostParams& hp) {
     L.tcount = take(sizeof(uint32_t) * (size_t)(L.ptiles + 1));
     L.tseg = take(sizeof(uint32_t) * (size_t)(L.ptiles + 1));
     L.eseg = take(sizeof(uint32_t) * 2 * (size_t)(L.emit_tiles + 1));
+    L.clip_cnt = take(sizeof(uint32_t) * (size_t)nseg);
     L.binmax = take(sizeof(uint32_t) * (size_t)L.max_bins);
     L.total = o;
     return L;
@@ -278,6 +279,7 @@ struct Args {
     uint32_t* tcount; // per-tile candidate counts, then (k_collect) each tile's first position
     uint32_t* tseg;   // streaming tile t starts in segment tseg[t]; tseg[ptiles] = nseg - 1
     uint32_t* eseg;   // emit tile t's candidates lie in segments [eseg[2t], eseg[2t + 1]]
+    uint32_t* clip_cnt;  // clip tiles of each segment summed so far
     uint32_t* binmax; // AdaComp: largest |v| key of every bin
     uint64_t max_samples, fused_tiles, emit_tiles, max_clip_tiles, ptiles, cgroups, nbuckets,
         max_bins;
@@ -403,6 +405,7 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
     for (size_t i = tid; i <= a.emit_tiles; i += stride) a.st_emit[i] = 0;
     for (size_t i = tid; i < a.nbuckets; i += stride) a.bcount[i] = 0;
     for (size_t i = tid; i < a.max_bins; i += stride) a.binmax[i] = 0;
+    for (size_t i = tid; i < (size_t)a.nseg; i += stride) a.clip_cnt[i] = 0;
     // the segment of every streaming tile's first entry, searched in the caller's offsets (when
     // they are invalid, block 0 raises abort and no later kernel reads this)
     for (size_t t = tid; t <= a.ptiles; t += stride)
@@ -419,8 +422,8 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
 
 // x * x in binary64, exactly, from the bits of x: |x| = m 2^(e' - 150) with e' = max(e, 1), so
 // x^2 = M 2^(2e' - 300), M = m^2 < 2^48, and with p the top bit of M the binary64 exponent is
-// p + 2e' - 300 (never below -298 nor above 208: always a normal binary64).
-__device__ __forceinline__ double exact_square(float x) {
+// p + 2e' - 300 (never below -298 nor above 208: always a normal binary64). Returns the bits.
+__device__ __forceinline__ uint64_t exact_square_bits(float x) {
     const uint32_t a = __float_as_uint(x) & 0x7FFFFFFFu;
     const uint32_t e = a >> 23;
     const uint32_t m = e ? ((a & 0x7FFFFFu) | 0x800000u) : a;
@@ -430,40 +433,57 @@ __device__ __forceinline__ double exact_square(float x) {
     uint64_t bits = (ex << 52) | ((M << ((52 - p) & 63)) & 0xFFFFFFFFFFFFFull);
     if (a == 0) bits = 0;
     if (a >= 0x7F800000u) bits = (a == 0x7F800000u) ? 0x7FF0000000000000ull : 0x7FF8000000000000ull;
-    return __longlong_as_double((long long)bits);
+    return bits;
 }
 
+
+
 // One 4096-entry tile per block: thread t sums entries [16t, 16t+16) as a 4-level tree, then
-// the 256 thread sums combine pairwise in shared memory.
+// the 256 thread sums combine pairwise in shared memory. The block that sums a segment's last
+// tile then adds the segment's tile sums left to right -- a chain of dependent binary64
+// additions on one lane while the other lanes keep the next chunk of tile sums in flight -- and
+// sets scale = c / sqrt(S) when sqrt(S) > c (binary64, correctly rounded sqrt and division,
+// rounded once to binary32). Tiles are taken from the last one backwards, so the long chains
+// of large segments late in the buffer run while the other tiles are still being summed.
+constexpr int kClipChunk = 512;
 __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
     __shared__ double s_t[kThreads];
-    __shared__ int s_skip;
-    const uint32_t c = blockIdx.x;
-    if (threadIdx.x == 0) s_skip = a.ctl->abort || c >= a.ctl->total_clip_tiles;
+    __shared__ double s_buf[kClipChunk];
+    __shared__ int s_skip, s_last;
+    __shared__ uint32_t s_c;
+    if (threadIdx.x == 0) {
+        const uint32_t total = a.ctl->total_clip_tiles;
+        s_skip = a.ctl->abort || blockIdx.x >= total;
+        s_c = total - 1u - blockIdx.x;
+    }
     __syncthreads();
     if (s_skip) return;
+    const uint32_t c = s_c;
     const int s = upper_bound_minus1(a.clip_off, a.nseg, c);
     const SegInfo& d = a.segs[s];
     const uint64_t base = (uint64_t)d.start + (uint64_t)(c - a.clip_off[s]) * kClipTile +
                           16u * threadIdx.x;
-    double q[16];
+    uint64_t qb[16];
     if ((base & 3u) == 0 && base + 16 <= d.end) {  // 16-byte aligned and whole: four float4
         const float4* g4 = reinterpret_cast<const float4*>(a.g + base);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const float4 x = g4[j];
-            q[4 * j] = exact_square(x.x);
-            q[4 * j + 1] = exact_square(x.y);
-            q[4 * j + 2] = exact_square(x.z);
-            q[4 * j + 3] = exact_square(x.w);
+            qb[4 * j] = exact_square_bits(x.x);
+            qb[4 * j + 1] = exact_square_bits(x.y);
+            qb[4 * j + 2] = exact_square_bits(x.z);
+            qb[4 * j + 3] = exact_square_bits(x.w);
         }
     } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const uint64_t e = base + i;
-            q[i] = (e < d.end) ? exact_square(a.g[e]) : 0.0;
+            qb[i] = (e < d.end) ? exact_square_bits(a.g[e]) : 0ull;
         }
     }
+    double q[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = __longlong_as_double((long long)qb[i]);
 #pragma unroll
     for (int w = 1; w < 16; w <<= 1)
 #pragma unroll
@@ -476,47 +496,41 @@ __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
         if (i < kThreads) s_t[i] = s_t[i] + s_t[i + w];
         __syncthreads();
     }
-    if (threadIdx.x == 0) a.clip_part[c] = s_t[0];
-}
-
-// One warp per segment: the tile sums left to right, then scale = c / sqrt(S) when
-// sqrt(S) > c (binary64, correctly rounded sqrt and division, rounded once to binary32). The
-// sum is a chain of dependent additions on lane 0; the other lanes keep the next chunk of tile
-// sums in flight and stage each chunk in shared memory.
-constexpr int kClipScaleWarps = 4;
-constexpr int kClipChunk = 512;
-__global__ void __launch_bounds__(32 * kClipScaleWarps) k_clip_scale(Args a) {
-    __shared__ double s_buf[kClipScaleWarps][kClipChunk];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int s = blockIdx.x * kClipScaleWarps + warp;
-    if (a.ctl->abort || s >= a.nseg) return;
     const uint32_t t0 = a.clip_off[s], t1 = a.clip_off[s + 1];
-    double* buf = s_buf[warp];
+    if (threadIdx.x == 0) {
+        a.clip_part[c] = s_t[0];
+        __threadfence();
+        s_last = (atomicAdd(&a.clip_cnt[s], 1u) == t1 - t0 - 1u);
+    }
+    __syncthreads();
+    if (!s_last || threadIdx.x >= 32) return;
+    __threadfence();  // every tile sum of the segment is in place: read them past L1
+    const int lane = threadIdx.x;
     double r[kClipChunk / 32];
     auto fetch = [&](uint32_t c0) {
 #pragma unroll
         for (int i = 0; i < kClipChunk / 32; ++i) {
             const uint32_t t = c0 + 32 * i + lane;
-            r[i] = (t < t1) ? a.clip_part[t] : 0.0;
+            r[i] = (t < t1) ? __ldcg(a.clip_part + t) : 0.0;
         }
     };
     double S = 0.0;
     fetch(t0);
     for (uint32_t c0 = t0; c0 < t1; c0 += kClipChunk) {
 #pragma unroll
-        for (int i = 0; i < kClipChunk / 32; ++i) buf[32 * i + lane] = r[i];
+        for (int i = 0; i < kClipChunk / 32; ++i) s_buf[32 * i + lane] = r[i];
         __syncwarp();
         if (c0 + kClipChunk < t1) fetch(c0 + kClipChunk);
         if (lane == 0) {
             const uint32_t len = min(t1 - c0, (uint32_t)kClipChunk);
-            for (uint32_t i = 0; i < len; ++i) S = S + buf[i];
+            for (uint32_t i = 0; i < len; ++i) S = S + s_buf[i];
         }
         __syncwarp();
     }
     if (lane == 0) {
         const double norm = sqrt(S);
-        const double c = (double)a.hp.clip_norm;
-        a.segs[s].scale = (norm > c) ? (float)(c / norm) : 1.0f;
+        const double cn = (double)a.hp.clip_norm;
+        a.segs[s].scale = (norm > cn) ? (float)(cn / norm) : 1.0f;
     }
 }
 
@@ -572,117 +586,97 @@ __device__ __forceinline__ uint64_t block_sum64(uint64_t x, uint64_t* sm) {
     return total;
 }
 
-// checksum of the cached positions, when the header matches this call's tag
-__global__ void __launch_bounds__(kThreads) k_cache_check(Args a) {
-    __shared__ uint64_t s_scan[33];
-    const SampleCache c = *a.scache;
-    if (a.ctl->abort || c.magic != kCacheMagic || c.tag != a.ctl->tag) return;
-    const uint32_t total = a.ctl->total_samples;
-    uint64_t part = 0;
-    for (uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < total;
-         i += (uint64_t)gridDim.x * kThreads)
-        part += cache_term(a.spos[i], i);
-    const uint64_t sum = block_sum64(part, s_scan);
-    if (threadIdx.x == 0 && sum) atomicAdd((unsigned long long*)&a.ctl->csum, sum);
-}
+__device__ bool grid_barrier(const Args& a, int* s_ok);
 
-__device__ __forceinline__ bool cache_valid(const Args& a) {
+// One cooperative launch: the checksum of the cached positions (when the header matches this
+// call's tag), a grid barrier, and -- only when the cache does not match -- the rebuild: bucket
+// counts, their scan (one block), every position into its bucket, each bucket sorted, and the
+// checksum of the new array, with grid barriers between the steps. Words written by other
+// blocks in an earlier step are read past L1.
+__global__ void __launch_bounds__(kThreads) k_cache(Args a) {
+    __shared__ uint64_t s_scan64[33];
+    __shared__ uint32_t s_scan[33];
+    __shared__ int s_bar, s_go;
+    if (ld_relaxed_u32((const uint32_t*)&a.ctl->abort)) return;  // the same word for every block
     const SampleCache c = *a.scache;
-    return c.magic == kCacheMagic && c.tag == a.ctl->tag && c.checksum == a.ctl->csum;
-}
-
-// rebuild, step 1: bucket counts (every block takes the same decision from the same inputs)
-__global__ void __launch_bounds__(kThreads) k_cache_count(Args a) {
-    const bool rebuild = !a.ctl->abort && !cache_valid(a);
-    if (blockIdx.x == 0 && threadIdx.x == 0) a.ctl->rebuild = rebuild ? 1u : 0u;
-    if (!rebuild) return;
+    const uint64_t tag = a.ctl->tag;
+    const bool tag_ok = c.magic == kCacheMagic && c.tag == tag;
     const uint32_t total = a.ctl->total_samples;
-    for (uint64_t jg = (uint64_t)blockIdx.x * kThreads + threadIdx.x; jg < total;
-         jg += (uint64_t)gridDim.x * kThreads) {
+    const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
+    const uint64_t stride = (uint64_t)gridDim.x * kThreads;
+    if (tag_ok) {
+        uint64_t part = 0;
+        for (uint64_t i = tid; i < total; i += stride) part += cache_term(a.spos[i], i);
+        const uint64_t sum = block_sum64(part, s_scan64);
+        if (threadIdx.x == 0 && sum) atomicAdd((unsigned long long*)&a.ctl->csum, sum);
+    }
+    if (!grid_barrier(a, &s_bar)) return;
+    if (threadIdx.x == 0) s_go = !(tag_ok && c.checksum == ld_relaxed(&a.ctl->csum));
+    __syncthreads();
+    if (!s_go) return;  // the cache matches: the same decision in every block
+    // bucket counts
+    for (uint64_t jg = tid; jg < total; jg += stride) {
         const int s = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)jg);
         const SegInfo& d = a.segs[s];
         const uint32_t pos = sample_position(d, jg - a.samp_off[s]);
         atomicAdd(&a.bcount[d.bbase + ((pos - d.start) >> kBucketShift)], 1u);
     }
-}
-
-// rebuild, step 2: counts -> first slot of each bucket (one block)
-__global__ void __launch_bounds__(1024) k_cache_scan(Args a) {
-    __shared__ uint32_t s_scan[33];
-    if (!a.ctl->rebuild) return;
-    const uint64_t nb = a.nbuckets;
-    const uint64_t per = (nb + 1023) / 1024;
-    const uint64_t lo = umin64(nb, threadIdx.x * per), hi = umin64(nb, lo + per);
-    uint32_t mine = 0;
-    for (uint64_t b = lo; b < hi; ++b) mine += a.bcount[b];
-    uint32_t total;
-    uint32_t run = block_excl_scan<1024>(mine, s_scan, &total);
-    for (uint64_t b = lo; b < hi; ++b) {
-        const uint32_t c = a.bcount[b];
-        a.bcount[b] = run;
-        run += c;
+    if (!grid_barrier(a, &s_bar)) return;
+    // counts -> first slot of each bucket (block 0)
+    if (blockIdx.x == 0) {
+        const uint64_t nb = a.nbuckets;
+        const uint64_t per = (nb + kThreads - 1) / kThreads;
+        const uint64_t lo = umin64(nb, threadIdx.x * per), hi = umin64(nb, lo + per);
+        uint32_t mine = 0;
+        for (uint64_t b = lo; b < hi; ++b) mine += __ldcg(a.bcount + b);
+        uint32_t sum;
+        uint32_t run = block_excl_scan<kThreads>(mine, s_scan, &sum);
+        for (uint64_t b = lo; b < hi; ++b) {
+            const uint32_t n_b = __ldcg(a.bcount + b);
+            a.bcount[b] = run;
+            run += n_b;
+        }
     }
-}
-
-// rebuild, step 3: every position into its bucket
-__global__ void __launch_bounds__(kThreads) k_cache_scatter(Args a) {
-    if (!a.ctl->rebuild) return;
-    const uint32_t total = a.ctl->total_samples;
-    for (uint64_t jg = (uint64_t)blockIdx.x * kThreads + threadIdx.x; jg < total;
-         jg += (uint64_t)gridDim.x * kThreads) {
+    if (!grid_barrier(a, &s_bar)) return;
+    // every position into its bucket; bcount[b] ends as the end of bucket b
+    for (uint64_t jg = tid; jg < total; jg += stride) {
         const int s = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)jg);
         const SegInfo& d = a.segs[s];
         const uint32_t pos = sample_position(d, jg - a.samp_off[s]);
         const uint32_t slot = atomicAdd(&a.bcount[d.bbase + ((pos - d.start) >> kBucketShift)], 1u);
         a.spos[slot] = pos;
     }
-}
-
-// rebuild, step 4: each bucket's positions in ascending order (about ten per bucket), so that
-// the gather walks every array upward; bcount[b] now holds the end of bucket b
-__global__ void __launch_bounds__(kThreads) k_cache_sort(Args a) {
-    if (!a.ctl->rebuild) return;
-    const uint64_t nb = a.nbuckets;
-    for (uint64_t b = (uint64_t)blockIdx.x * kThreads + threadIdx.x; b < nb;
-         b += (uint64_t)gridDim.x * kThreads) {
-        const uint32_t lo = b ? a.bcount[b - 1] : 0u, hi = a.bcount[b];
+    if (!grid_barrier(a, &s_bar)) return;
+    // each bucket's positions in ascending order (about ten per bucket), so that the gather
+    // walks every array upward
+    for (uint64_t b = tid; b < a.nbuckets; b += stride) {
+        const uint32_t lo = b ? __ldcg(a.bcount + b - 1) : 0u, hi = __ldcg(a.bcount + b);
         for (uint32_t i = lo + 1; i < hi; ++i) {  // insertion sort
-            const uint32_t x = a.spos[i];
+            const uint32_t x = __ldcg(a.spos + i);
             uint32_t j = i;
-            while (j > lo && a.spos[j - 1] > x) {
-                a.spos[j] = a.spos[j - 1];
+            while (j > lo) {
+                const uint32_t y = __ldcg(a.spos + j - 1);
+                if (y <= x) break;
+                a.spos[j] = y;
                 --j;
             }
             a.spos[j] = x;
         }
     }
-}
-
-// rebuild, step 5: checksum of the new array; the last block writes the header
-__global__ void __launch_bounds__(kThreads) k_cache_commit(Args a) {
-    __shared__ uint64_t s_scan[33];
-    __shared__ int s_last;
-    if (!a.ctl->rebuild) return;
-    const uint32_t total = a.ctl->total_samples;
+    if (!grid_barrier(a, &s_bar)) return;
+    // checksum of the new array; block 0 writes the header once every block has added its part
     uint64_t part = 0;
-    for (uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < total;
-         i += (uint64_t)gridDim.x * kThreads)
-        part += cache_term(a.spos[i], i);
-    const uint64_t sum = block_sum64(part, s_scan);
-    if (threadIdx.x == 0) {
-        if (sum) atomicAdd((unsigned long long*)&a.ctl->newsum, sum);
-        __threadfence();
-        s_last = (atomicAdd(&a.ctl->sum_done, 1u) == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (s_last && threadIdx.x == 0) {
-        __threadfence();
-        SampleCache c;
-        c.magic = kCacheMagic;
-        c.tag = a.ctl->tag;
-        c.checksum = atomicAdd((unsigned long long*)&a.ctl->newsum, 0ull);
-        c.pad = 0;
-        *a.scache = c;
+    for (uint64_t i = tid; i < total; i += stride) part += cache_term(__ldcg(a.spos + i), i);
+    const uint64_t sum = block_sum64(part, s_scan64);
+    if (threadIdx.x == 0 && sum) atomicAdd((unsigned long long*)&a.ctl->newsum, sum);
+    if (!grid_barrier(a, &s_bar)) return;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        SampleCache h;
+        h.magic = kCacheMagic;
+        h.tag = tag;
+        h.checksum = ld_relaxed(&a.ctl->newsum);
+        h.pad = 0;
+        *a.scache = h;
     }
 }
 
@@ -1923,6 +1917,7 @@ Args make_args(const float* g, float* u, float* v, int64_t n, const int64_t* seg
     a.tcount = reinterpret_cast<uint32_t*>(w + L.tcount);
     a.tseg = reinterpret_cast<uint32_t*>(w + L.tseg);
     a.eseg = reinterpret_cast<uint32_t*>(w + L.eseg);
+    a.clip_cnt = reinterpret_cast<uint32_t*>(w + L.clip_cnt);
     a.binmax = reinterpret_cast<uint32_t*>(w + L.binmax);
     a.max_samples = L.max_samples;
     a.fused_tiles = L.fused_tiles;
@@ -1962,19 +1957,23 @@ void set_kernel_attributes() {
     }
 }
 
-// Blocks of the cooperative select: all resident at once, up to 4 per SM (more loads in flight
-// over the items), once per device.
-unsigned cooperative_select_grid(int sms) {
-    static int per_sm[128] = {0};
+// Blocks of a cooperative launch (0, 1: the global select of sample keys / candidates; 2: the
+// sample-position cache): all resident at once, up to 4 per SM (more loads in flight over the
+// items); the occupancy is asked once per device.
+unsigned cooperative_grid(int which, int sms) {
+    static int per_sm[3][128] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    int b = (dev >= 0 && dev < 128) ? per_sm[dev] : 0;
+    int b = (dev >= 0 && dev < 128) ? per_sm[which][dev] : 0;
     if (b == 0) {
-        int b0 = 0, b1 = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, k_select_global<0>, kThreads, 0);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k_select_global<1>, kThreads, 0);
-        b = std::max(1, std::min(4, std::min(b0, b1)));
-        if (dev >= 0 && dev < 128) per_sm[dev] = b;
+        if (which == 0)
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_select_global<0>, kThreads, 0);
+        else if (which == 1)
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_select_global<1>, kThreads, 0);
+        else
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_cache, kThreads, 0);
+        b = std::max(1, std::min(4, b));
+        if (dev >= 0 && dev < 128) per_sm[which][dev] = b;
     }
     return (unsigned)(b * sms);
 }
@@ -2036,31 +2035,24 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     L1(k_plan, plan_grid, 1024, a);
     if (hp.clip_on) {
         L1(k_clip_tiles, (unsigned)L.max_clip_tiles, kThreads, a);
-        L1(k_clip_scale, (unsigned)((nseg + kClipScaleWarps - 1) / kClipScaleWarps),
-           32 * kClipScaleWarps, a);
     }
-    const unsigned cgrid = (unsigned)std::max<uint64_t>(
-        1, std::min<uint64_t>((uint64_t)sms * 4, (L.max_samples + kThreads - 1) / kThreads));
-    L1(k_cache_check, cgrid, kThreads, a);
-    L1(k_cache_count, cgrid, kThreads, a);
-    L1(k_cache_scan, 1, 1024, a);
-    L1(k_cache_scatter, cgrid, kThreads, a);
-    L1(k_cache_sort, cgrid, kThreads, a);
-    L1(k_cache_commit, cgrid, kThreads, a);
+    bool launch_failed = false;
+    auto coop = [&](const void* kernel, unsigned grid) {
+        void* args[] = {&a};
+        if (cudaLaunchCooperativeKernel(kernel, dim3(grid), dim3(kThreads), args, 0, s) !=
+            cudaSuccess)
+            launch_failed = true;
+        ++launches;
+    };
+    coop((const void*)k_cache, cooperative_grid(2, sms));
     const uint64_t sgrid = (L.max_samples + kThreads * kSamplePerThread - 1) /
                            (kThreads * kSamplePerThread);
     L1(k_sample, (unsigned)sgrid, kThreads, a);
     const bool selects = hp.mode != DGC_SELECT_ADACOMP;  // AdaComp keeps every segment idle
     set_kernel_attributes();
-    const unsigned sel_grid = cooperative_select_grid(sms);
-    bool launch_failed = false;
     auto global_select = [&](int kind) {
-        void* args[] = {&a};
-        const void* k = kind == 0 ? (const void*)k_select_global<0> : (const void*)k_select_global<1>;
-        if (cudaLaunchCooperativeKernel(k, dim3(sel_grid), dim3(kThreads), args, 0, s) !=
-            cudaSuccess)
-            launch_failed = true;
-        ++launches;
+        coop(kind == 0 ? (const void*)k_select_global<0> : (const void*)k_select_global<1>,
+             cooperative_grid(kind, sms));
     };
     auto small_select = [&](int kind) {
         if (kind == 0)
@@ -2145,8 +2137,6 @@ extern "C" int dgc_compress_shared(const float* g, float* u, float* v, int64_t n
     L1(k_shared_check, jgrid, kThreads, a, idx, count, (uint64_t)max_count);
     if (hp.clip_on) {
         L1(k_clip_tiles, (unsigned)L.max_clip_tiles, kThreads, a);
-        L1(k_clip_scale, (unsigned)((nseg + kClipScaleWarps - 1) / kClipScaleWarps),
-           32 * kClipScaleWarps, a);
     }
     const cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
     if (pb && pe) record_marker(pb, s);

@@ -233,6 +233,40 @@ def test_exact_edges(case):
               mask_momentum=bool(case % 2))
 
 
+def _extreme_segment(r, kind, size):
+    """Finite binary32 values at the ends of the range, for the clipping sum of squares."""
+    if kind == 0:  # subnormals: |x| < 2^-126
+        bits_ = r.integers(1, 1 << 23, size).astype(np.uint32)
+    elif kind == 1:  # huge: squares far beyond binary32, well inside binary64
+        bits_ = r.integers(0x71000000, 0x7F7FFFFF, size, endpoint=True).astype(np.uint32)
+    elif kind == 2:  # every exponent, subnormal to the largest finite
+        bits_ = r.integers(1, 0x7F7FFFFF, size, endpoint=True).astype(np.uint32)
+    else:  # mostly zeros
+        bits_ = np.where(r.random(size) < 0.01, r.integers(0x30000000, 0x40000000, size),
+                         0).astype(np.uint32)
+    bits_ |= (r.integers(0, 2, size).astype(np.uint32) << 31)
+    return bits_.view(np.float32)
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_clip_extreme_magnitudes(case):
+    # the clip norm's binary64 squares and sums at the edges of the binary32 range: subnormal
+    # gradients (no clipping), gradients whose norm overflows binary32, every exponent mixed
+    rng = np.random.default_rng(12000 + case)
+    sizes = [int(rng.integers(1, 20_000)) for _ in range(5)] + [4096, 12289]
+    kinds = [int(rng.integers(0, 4)) for _ in sizes]
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    n = int(off[-1])
+
+    def grads(t):
+        r = np.random.default_rng([case, t, 3])
+        return np.concatenate([_extreme_segment(r, k, z) for k, z in zip(kinds, sizes)])
+
+    run_steps(grads, off, 2, mode=[dgc.SELECT_EXACT, dgc.SELECT_SAMPLED][case % 2],
+              sparsity=0.99, momentum=0.9, clip_norm=float([1.0, 1e-3, 3.0][case % 3]),
+              sample_ratio=0.1, seed=case)
+
+
 @pytest.mark.parametrize("case", range(40))
 def test_sampled_edges(case):
     rng = np.random.default_rng(7000 + case)
