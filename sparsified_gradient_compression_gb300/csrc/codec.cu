@@ -473,21 +473,36 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
 // dense output is first cleared by a streaming store pass (unless accumulating), then each value
 // token adds itself to its position: the same single binary32 addition per value as the tile
 // kernel performs, onto the same starting value.
-__global__ void __launch_bounds__(kThreads) k_dec_zero(DecArgs a) {
+// The dense array to +0 before the one-message scatter: one zeroed 16 KiB shared buffer per
+// block, written out by bulk asynchronous stores (one thread issues them, chunk after chunk);
+// the few entries before the first 16-byte boundary and after the last whole chunk by plain
+// stores.
+constexpr uint32_t kZeroChunk = 4096;  // floats per bulk store
+constexpr int kZeroThreads = 128;
+__global__ void __launch_bounds__(kZeroThreads) k_dec_zero(DecArgs a) {
+    __shared__ __align__(128) float s_zero[kZeroChunk];
     if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
     float* dense = a.dense;
     const uint64_t n = a.n;
-    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-    if ((reinterpret_cast<uintptr_t>(dense) & 15u) == 0) {
-        float4* d4 = reinterpret_cast<float4*>(dense);
-        const uint64_t n4 = n / 4;
-        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (uint64_t i = tid; i < n4; i += stride) __stcs(d4 + i, z);
-        for (uint64_t i = n4 * 4 + tid; i < n; i += stride) dense[i] = 0.0f;
-    } else {
-        for (uint64_t i = tid; i < n; i += stride) dense[i] = 0.0f;
+    const uint64_t head = umin64(n, ((16u - ((uintptr_t)dense & 15u)) & 15u) / 4u);
+    const uint64_t nchunks = (n - head) / kZeroChunk;
+    const uint64_t body_end = head + nchunks * kZeroChunk;
+    if (nchunks > 0) {
+        for (uint32_t i = threadIdx.x; i < kZeroChunk; i += kZeroThreads) s_zero[i] = 0.0f;
+        fence_proxy_async_smem();  // the zeros, before the bulk copies read them
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (uint64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+                bulk_s2g(dense + head + c * kZeroChunk, s_zero, kZeroChunk * 4u);
+                bulk_commit();
+            }
+            bulk_wait_all();
+        }
     }
+    const uint64_t tid = (uint64_t)blockIdx.x * kZeroThreads + threadIdx.x;
+    const uint64_t stride = (uint64_t)gridDim.x * kZeroThreads;
+    for (uint64_t i = tid; i < head; i += stride) dense[i] = 0.0f;
+    for (uint64_t i = body_end + tid; i < n; i += stride) dense[i] = 0.0f;
 }
 
 __global__ void __launch_bounds__(kThreads) k_dec_scatter1(DecArgs a) {
@@ -740,7 +755,7 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
         if (!accumulate && !apply && n > 0) {
             const int sms = dgc_internal_sm_count();
             if (sms <= 0) return DGC_ECUDA;
-            k_dec_zero<<<(unsigned)sms * 8, kThreads, 0, s>>>(a);
+            k_dec_zero<<<(unsigned)sms * 4, kZeroThreads, 0, s>>>(a);
             ++launches;
         }
         if (L.sum_T > 0) {

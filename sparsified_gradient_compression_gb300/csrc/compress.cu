@@ -115,6 +115,7 @@ struct Ctl {
     uint32_t active;
     uint32_t any_failed;
     uint32_t ticket_fused, ticket_compact, ticket_emit, ticket_collect;
+    uint32_t ndense;        // tiles whose slots k_collect_copy moves
     uint32_t total_samples, total_clip_tiles, total_cand, total_sent;
     uint32_t emit_done;
     uint64_t tag;           // what the sample positions depend on, for this call
@@ -136,8 +137,8 @@ constexpr int kBucketShift = 10;  // cache order: 1024-entry buckets, segment by
 struct Layout {
     size_t ctl, scache, segs, seg_start, samp_off, clip_off, cand_off, clip_part, skeys, spos,
         bcount, histA, histB;
-    size_t st_collect, st_compact, st_emit, cidx, sidx, tcount, tseg, eseg, clip_cnt, binmax,
-        total;
+    size_t st_collect, st_compact, st_emit, cidx, sidx, tcount, tseg, eseg, clip_cnt, dlist,
+        binmax, total;
     uint64_t max_samples, max_clip_tiles, fused_tiles, emit_tiles, ptiles, cgroups, nbuckets,
         max_bins;
 };
@@ -224,6 +225,7 @@ Layout make_layout(int64_t n, int32_t nseg, const HostParams& hp) {
     L.tseg = take(sizeof(uint32_t) * (size_t)(L.ptiles + 1));
     L.eseg = take(sizeof(uint32_t) * 2 * (size_t)(L.emit_tiles + 1));
     L.clip_cnt = take(sizeof(uint32_t) * (size_t)nseg);
+    L.dlist = take(sizeof(uint32_t) * (size_t)(L.ptiles + 1));
     L.binmax = take(sizeof(uint32_t) * (size_t)L.max_bins);
     L.total = o;
     return L;
@@ -280,6 +282,7 @@ struct Args {
     uint32_t* tseg;   // streaming tile t starts in segment tseg[t]; tseg[ptiles] = nseg - 1
     uint32_t* eseg;   // emit tile t's candidates lie in segments [eseg[2t], eseg[2t + 1]]
     uint32_t* clip_cnt;  // clip tiles of each segment summed so far
+    uint32_t* dlist;     // the streaming tiles with many candidates (k_collect_copy's work)
     uint32_t* binmax; // AdaComp: largest |v| key of every bin
     uint64_t max_samples, fused_tiles, emit_tiles, max_clip_tiles, ptiles, cgroups, nbuckets,
         max_bins;
@@ -606,7 +609,15 @@ __global__ void __launch_bounds__(kThreads) k_cache(Args a) {
     const uint64_t stride = (uint64_t)gridDim.x * kThreads;
     if (tag_ok) {
         uint64_t part = 0;
-        for (uint64_t i = tid; i < total; i += stride) part += cache_term(a.spos[i], i);
+        constexpr int kB = 8;  // loads in flight per thread
+        for (uint64_t i0 = tid; i0 < total; i0 += kB * stride) {
+            uint32_t p[kB];
+#pragma unroll
+            for (int r = 0; r < kB; ++r) p[r] = (i0 + r * stride < total) ? a.spos[i0 + r * stride] : 0u;
+#pragma unroll
+            for (int r = 0; r < kB; ++r)
+                if (i0 + r * stride < total) part += cache_term(p[r], i0 + r * stride);
+        }
         const uint64_t sum = block_sum64(part, s_scan64);
         if (threadIdx.x == 0 && sum) atomicAdd((unsigned long long*)&a.ctl->csum, sum);
     }
@@ -1524,9 +1535,11 @@ __global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) 
 // ------------------------------------------------------------------------- collect
 // Turns the streaming pass's per-tile slots into one index-ordered candidate list. Block b owns
 // kCGroup consecutive tiles: it scans their counts and gets the group's global offset from a
-// decoupled look-back over groups; each tile's count is replaced by its first list position,
-// and k_collect_copy then moves the slots to cidx.
+// decoupled look-back over groups; each tile's count is replaced by its first list position. A
+// tile's few candidates are copied to cidx by its own thread; tiles with more are listed for
+// k_collect_copy.
 constexpr int kCGroup = kThreads;  // tiles per collect block
+constexpr uint32_t kCollectDirect = 16;  // a tile with at most this many candidates: copied in place
 
 __global__ void __launch_bounds__(kThreads) k_collect(Args a) {
     __shared__ uint32_t s_ex[kCGroup + 1];
@@ -1558,26 +1571,40 @@ __global__ void __launch_bounds__(kThreads) k_collect(Args a) {
     }
     __syncthreads();
     const uint64_t gbase = s_base;
-    // the tile's count becomes its first position in the list; k_collect_copy moves the slots
-    if (t < ntiles) a.tcount[t] = (uint32_t)umin64(gbase + ex, a.n);
+    // the tile's count becomes its first position in the list. A tile with few candidates (the
+    // common case) has its slots copied by its own thread; the others are listed for
+    // k_collect_copy, which spreads each over a whole block.
+    if (t < ntiles) {
+        const uint32_t p = (uint32_t)umin64(gbase + ex, a.n);
+        a.tcount[t] = p;
+        if (c <= kCollectDirect) {
+            uint32_t x[kCollectDirect];
+#pragma unroll
+            for (uint32_t j = 0; j < kCollectDirect; ++j)
+                if (j < c) x[j] = a.sidx[(uint64_t)t * kPTile + j];
+#pragma unroll
+            for (uint32_t j = 0; j < kCollectDirect; ++j)
+                if (j < c && (uint64_t)p + j < a.n) a.cidx[p + j] = x[j];
+        } else {
+            a.dlist[atomicAdd(&a.ctl->ndense, 1u)] = t;
+        }
+    }
     if (grp == ngroups - 1 && tid == 0)
         a.ctl->total_cand = (uint32_t)umin64(gbase + total, a.n);
 }
 
-// Every list position f finds its tile (the last one whose first position is <= f) by binary
-// search and copies its slot. Spread over the whole grid, so that a tile range dense with
-// candidates (a run of small, all-candidate segments) is not copied by one block alone.
+// The listed tiles' slots, one tile per block at a time (up to kPTile slots, coalesced).
 __global__ void __launch_bounds__(kThreads) k_collect_copy(Args a) {
     if (ld_relaxed_u32((const uint32_t*)&a.ctl->abort)) return;
     const uint32_t total = a.ctl->total_cand;
     const uint32_t nt = (uint32_t)a.ptiles;
-    for (uint32_t f = blockIdx.x * kThreads + threadIdx.x; f < total; f += gridDim.x * kThreads) {
-        uint32_t lo = 0, hi = nt;
-        while (hi - lo > 1) {
-            const uint32_t mid = (lo + hi) >> 1;
-            if (a.tcount[mid] <= f) lo = mid; else hi = mid;
-        }
-        a.cidx[f] = a.sidx[(uint64_t)lo * kPTile + (f - a.tcount[lo])];
+    const uint32_t nd = a.ctl->ndense;
+    for (uint32_t j = blockIdx.x; j < nd; j += gridDim.x) {
+        const uint32_t t = a.dlist[j];
+        const uint32_t p = a.tcount[t];
+        const uint32_t e = (t + 1 < nt) ? a.tcount[t + 1] : total;
+        for (uint32_t q = threadIdx.x; p + q < e; q += kThreads)
+            a.cidx[p + q] = a.sidx[(uint64_t)t * kPTile + q];
     }
 }
 
@@ -1918,6 +1945,7 @@ Args make_args(const float* g, float* u, float* v, int64_t n, const int64_t* seg
     a.tseg = reinterpret_cast<uint32_t*>(w + L.tseg);
     a.eseg = reinterpret_cast<uint32_t*>(w + L.eseg);
     a.clip_cnt = reinterpret_cast<uint32_t*>(w + L.clip_cnt);
+    a.dlist = reinterpret_cast<uint32_t*>(w + L.dlist);
     a.binmax = reinterpret_cast<uint32_t*>(w + L.binmax);
     a.max_samples = L.max_samples;
     a.fused_tiles = L.fused_tiles;

@@ -603,6 +603,24 @@ def test_launch_counter_counts_kernels():
     assert dgc.dgc_launch_count() > before
 
 
+@pytest.mark.parametrize("shift", [0, 1, 2, 3])
+@pytest.mark.parametrize("n", [5, 4096, 4099, 3 * 4096 + 7, 100_003])
+def test_decode_clear_any_alignment(shift, n):
+    # one message decoded into a dense view that starts 0-3 floats past a 16-byte boundary: the
+    # clear (bulk stores of whole 16 KiB chunks, plain stores around them) covers exactly [0, n)
+    rng = np.random.default_rng(n + shift)
+    k = max(1, n // 100)
+    idx = np.sort(rng.choice(n, k, replace=False)).astype(np.uint32)
+    val = rng.standard_normal(k).astype(np.float32)
+    msg = oracle.encode(idx, val, n)
+    buf = torch.full((n + 8,), float("nan"), dtype=torch.float32, device="cuda")
+    rc, _ = decode([msg], n, dense=buf[shift:shift + n])
+    _, odense = oracle.decode_accumulate([msg], n)
+    host = buf.cpu().numpy()
+    assert rc == 0 and same_bits(host[shift:shift + n], odense)
+    assert np.isnan(host[:shift]).all() and np.isnan(host[shift + n:]).all()
+
+
 # --------------------------------------------------------------- decode -> plain SGD step
 def _weights(rng, n):
     w = (rng.standard_normal(n) * 10.0 ** rng.integers(-3, 3, n)).astype(np.float32)
