@@ -19,8 +19,10 @@
  *   - Work is enqueued on `stream` (a cudaStream_t; 0 is the legacy default stream). No call
  *     synchronizes with the device except dgc_read_status.
  *   - The return value reports errors that can be seen on the host before anything is
- *     enqueued (DGC_EINVAL, DGC_EUNSUPPORTED, DGC_ECORRUPT for malformed sizes, DGC_ECUDA for a
- *     failed launch); on such an error nothing is enqueued and no buffer is touched.
+ *     enqueued (DGC_EINVAL, DGC_EUNSUPPORTED, DGC_ECORRUPT for malformed sizes); on such an
+ *     error nothing is enqueued and no buffer is touched. DGC_ECUDA reports a launch the
+ *     runtime refused; kernels of the call enqueued before it may have run, and the call's
+ *     outputs are then invalid.
  *   - Errors that only the device can see are written to `*status` (an int32 in device
  *     memory): the first error wins and the library never clears it, so zero it before a
  *     sequence of calls and read it with dgc_read_status.
@@ -32,10 +34,11 @@
  *     rebuilds them when either differs, so using the workspace for anything else in between
  *     is safe and only costs that rebuild.
  *   - Indices are uint32: n must be below 2^32.
- *   - CUDA graphs: dgc_compress, dgc_compress_shared and dgc_encode enqueue kernels and at most
- *     a memset, so a stream capture of them replays as captured. Make one ordinary
- *     dgc_compress or dgc_compress_shared call on the device first (it sets the streaming
- *     kernels' shared-memory attributes once per device). The decoders copy their table of
+ *   - CUDA graphs: dgc_compress, dgc_compress_shared and dgc_encode enqueue kernels (dgc_compress
+ *     some of them as cooperative launches) and at most a memset, so a stream capture of them
+ *     replays as captured. Make one ordinary dgc_compress or dgc_compress_shared call on the
+ *     device first (it sets the kernels' shared-memory attributes and reads the cooperative
+ *     kernels' occupancy once per device). The decoders copy their table of
  *     messages from host memory on every call and are not meant for capture. (This note does
  *     not cover dgc_compress_noalloc.)
  */

@@ -50,8 +50,10 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRows = 8;                          // float4 rows per thread in re-compaction
 constexpr int kTile = kThreads * kRows * 4;       // 8192 entries per re-compaction tile
-// streaming pass shape: entries per tile, tiles in flight per block, blocks per SM
-// (2048 entries x 4 stages x 2 blocks per SM: the fastest of the shapes measured on GB300)
+// streaming pass shape: entries per tile, tiles in flight per block, blocks per SM. The DGC
+// and shared-set passes run 2048 entries x 4 stages x 2 blocks per SM, the AdaComp pass (46%
+// more instructions per entry) 3 stages x 3 blocks, so that more warps hide its latency: the
+// fastest of the shapes measured on GB300 for each.
 #ifndef DGC_STREAM_TILE
 #define DGC_STREAM_TILE 2048
 #endif
@@ -61,9 +63,21 @@ constexpr int kTile = kThreads * kRows * 4;       // 8192 entries per re-compact
 #ifndef DGC_STREAM_BLOCKS_PER_SM
 #define DGC_STREAM_BLOCKS_PER_SM 2
 #endif
+#ifndef DGC_ADACOMP_STAGES
+#define DGC_ADACOMP_STAGES 3
+#endif
+#ifndef DGC_ADACOMP_BLOCKS_PER_SM
+#define DGC_ADACOMP_BLOCKS_PER_SM 3
+#endif
 constexpr int kPTile = DGC_STREAM_TILE;
-constexpr int kPStages = DGC_STREAM_STAGES;
-constexpr int kPBlocksPerSM = DGC_STREAM_BLOCKS_PER_SM;
+template <int kSel>
+__host__ __device__ constexpr int stream_stages() {
+    return kSel == 1 ? DGC_ADACOMP_STAGES : DGC_STREAM_STAGES;
+}
+template <int kSel>
+__host__ __device__ constexpr int stream_blocks_per_sm() {
+    return kSel == 1 ? DGC_ADACOMP_BLOCKS_PER_SM : DGC_STREAM_BLOCKS_PER_SM;
+}
 constexpr int kPRows = kPTile / (4 * kThreads);   // float4 rows per thread
 constexpr int kWarps = kThreads / 32;
 static_assert(kPRows >= 1 && kPRows * 4 * kThreads == kPTile, "tile = rows x 1024 entries");
@@ -72,7 +86,10 @@ static_assert(kPRows * kWarps <= 32, "one warp scans the per-(row, warp) counts"
 // exhaustively against integer division for tiles of 2048 and 4096
 static_assert(kPTile <= 4096, "bin index by reciprocal is only checked up to 4096-entry tiles");
 constexpr uint32_t kPStageFloats = 3u * kPTile;   // g, u, v
-constexpr size_t kPSmemBytes = sizeof(float) * kPStageFloats * kPStages;  // 96 KiB
+template <int kSel>
+constexpr size_t stream_smem_bytes() {  // 96 KiB (72 KiB for AdaComp)
+    return sizeof(float) * kPStageFloats * stream_stages<kSel>();
+}
 constexpr uint32_t kMbarSpinLimit = 1u << 22;
 constexpr int kEmitRows = 4;
 constexpr int kEmitTile = kThreads * kEmitRows * 4;  // 4096 candidates per emit tile
@@ -1186,8 +1203,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_recompact(Args a) {
 
 // ------------------------------------------------- streaming pass, bulk-copy pipeline
 // The pass every entry goes through: u = fma(m, u, g*scale); v += u; candidates are the
-// entries with key(v) >= the segment's threshold. Persistent blocks (kPBlocksPerSM per SM) take
-// kPTile-entry tiles from an atomic ticket and keep kPStages tiles of g, u and v in flight as bulk copies
+// entries with key(v) >= the segment's threshold. Persistent blocks (2 or 3 per SM) take
+// kPTile-entry tiles from an atomic ticket and keep 4 or 3 tiles of g, u and v in flight as bulk copies
 // (TMA, cp.async.bulk) into shared memory, so HBM streams without pause. Updated u and v go back
 // with coalesced 16-byte stores. A tile's candidates are compacted, in index order, into the
 // tile's own slot range sidx[base, base + count) and its count into tcount[tile]: no block
@@ -1254,7 +1271,8 @@ __device__ __forceinline__ void stream_compute(const Args& a, const float* sg, u
 // tile also raises each bin's global maximum, and the emit step keeps the candidates that
 // reach it. kSel 2 (a shared index set given by the caller): the pass only accumulates.
 template <int kSel>
-__global__ void __launch_bounds__(kThreads, kPBlocksPerSM) k_stream_tma(Args a) {
+__global__ void __launch_bounds__(kThreads, stream_blocks_per_sm<kSel>()) k_stream_tma(Args a) {
+    constexpr int kPStages = stream_stages<kSel>();
     extern __shared__ __align__(128) float s_stage[];  // [kPStages][3][kPTile]
     __shared__ __align__(8) uint64_t s_bar[kPStages];
     __shared__ uint32_t s_tile[kPStages];
@@ -1962,7 +1980,7 @@ Args make_args(const float* g, float* u, float* v, int64_t n, const int64_t* seg
 template <int kSel>
 void stream_attributes() {
     cudaFuncSetAttribute(k_stream_tma<kSel>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)kPSmemBytes);
+                         (int)stream_smem_bytes<kSel>());
     // the AdaComp variant needs nearly all of the SM's shared memory for two blocks
     cudaFuncSetAttribute(k_stream_tma<kSel>, cudaFuncAttributePreferredSharedMemoryCarveout,
                          (int)cudaSharedmemCarveoutMaxShared);
@@ -2006,16 +2024,18 @@ unsigned cooperative_grid(int which, int sms) {
     return (unsigned)(b * sms);
 }
 
-// The streaming pass: persistent blocks, kPBlocksPerSM per SM (at most one per tile).
+// The streaming pass: persistent blocks, 2 or 3 per SM (at most one per tile).
 void launch_stream_pass(int sel, const Args& a, uint64_t ptiles, int sms, cudaStream_t s) {
     set_kernel_attributes();
-    const unsigned pgrid = (unsigned)std::min<uint64_t>((uint64_t)sms * kPBlocksPerSM, ptiles);
+    auto grid = [&](int per_sm) {
+        return (unsigned)std::min<uint64_t>((uint64_t)sms * per_sm, ptiles);
+    };
     if (sel == 1)
-        k_stream_tma<1><<<pgrid, kThreads, kPSmemBytes, s>>>(a);
+        k_stream_tma<1><<<grid(stream_blocks_per_sm<1>()), kThreads, stream_smem_bytes<1>(), s>>>(a);
     else if (sel == 2)
-        k_stream_tma<2><<<pgrid, kThreads, kPSmemBytes, s>>>(a);
+        k_stream_tma<2><<<grid(stream_blocks_per_sm<2>()), kThreads, stream_smem_bytes<2>(), s>>>(a);
     else
-        k_stream_tma<0><<<pgrid, kThreads, kPSmemBytes, s>>>(a);
+        k_stream_tma<0><<<grid(stream_blocks_per_sm<0>()), kThreads, stream_smem_bytes<0>(), s>>>(a);
 }
 }  // namespace
 }  // namespace dgc
