@@ -626,15 +626,24 @@ __global__ void __launch_bounds__(kThreads) k_cache(Args a) {
     const uint64_t stride = (uint64_t)gridDim.x * kThreads;
     if (tag_ok) {
         uint64_t part = 0;
-        constexpr int kB = 8;  // loads in flight per thread
-        for (uint64_t i0 = tid; i0 < total; i0 += kB * stride) {
-            uint32_t p[kB];
-#pragma unroll
-            for (int r = 0; r < kB; ++r) p[r] = (i0 + r * stride < total) ? a.spos[i0 + r * stride] : 0u;
+        // 16-byte loads of 4 positions (the array is 256-byte aligned), 4 of them in flight
+        constexpr int kB = 4;
+        const uint64_t total4 = total / 4;
+        const uint4* sp4 = reinterpret_cast<const uint4*>(a.spos);
+        for (uint64_t q0 = tid; q0 < total4; q0 += kB * stride) {
+            uint4 p[kB];
 #pragma unroll
             for (int r = 0; r < kB; ++r)
-                if (i0 + r * stride < total) part += cache_term(p[r], i0 + r * stride);
+                p[r] = (q0 + r * stride < total4) ? sp4[q0 + r * stride] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int r = 0; r < kB; ++r) {
+                const uint64_t i = 4 * (q0 + r * stride);
+                if (q0 + r * stride < total4)
+                    part += cache_term(p[r].x, i) + cache_term(p[r].y, i + 1) +
+                            cache_term(p[r].z, i + 2) + cache_term(p[r].w, i + 3);
+            }
         }
+        for (uint64_t i = 4 * total4 + tid; i < total; i += stride) part += cache_term(a.spos[i], i);
         const uint64_t sum = block_sum64(part, s_scan64);
         if (threadIdx.x == 0 && sum) atomicAdd((unsigned long long*)&a.ctl->csum, sum);
     }
@@ -786,19 +795,29 @@ __device__ void hist_level(const Args& a, int level, uint32_t* s_hist) {
     for (int b = threadIdx.x; b < kHistBins; b += kThreads) s_hist[b] = 0;
     __syncthreads();
     BlockHist h{s_hist, -1};
-    constexpr int kPer = 8;
+    constexpr int kPer = 16;
     const uint32_t chunk = kThreads * kPer;
+    // the segment words do not change during a level: read them again only when the chunk's
+    // segment changes (every thread holds the same copy)
+    int seen = -1;
+    bool seen_active = false;
+    uint64_t seen_prefix = 0;
     for (uint64_t c0 = (uint64_t)blockIdx.x * chunk; c0 < total; c0 += (uint64_t)gridDim.x * chunk) {
         const uint32_t c1 = (uint32_t)umin64(total, c0 + chunk);
         const int s0 = upper_bound_minus1(off, a.nseg, (uint32_t)c0);
         const int s1 = upper_bound_minus1(off, a.nseg, c1 - 1);
         if (s0 == s1) {
-            if (__ldcg(&a.segs[s0].state) != kActive) continue;
+            if (s0 != seen) {
+                seen = s0;
+                seen_active = __ldcg(&a.segs[s0].state) == kActive;
+                seen_prefix = __ldcg(&a.segs[s0].prefix);
+            }
+            if (!seen_active) continue;
             if (h.cur != s0) {
                 h.flush(ghist, nbins);
                 h.cur = s0;
             }
-            const uint64_t prefix = __ldcg(&a.segs[s0].prefix);
+            const uint64_t prefix = seen_prefix;
             uint64_t xs[kPer];
 #pragma unroll
             for (int r = 0; r < kPer; ++r) {  // all loads first, then the counting
