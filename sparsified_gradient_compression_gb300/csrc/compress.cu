@@ -27,6 +27,7 @@
 //   collect(+copy) tile slots -> one index-ordered candidate list (decoupled look-back)
 //   candoff       per-segment candidate ranges; decides who re-selects
 //   recompact     [exact mode, only if the sampled bound was too tight] re-compacts from v
+//   cval          every candidate's value, gathered once by the whole grid
 //   select x2     radix select of the exact k-th (|v|, index) pair among candidates (on chip,
 //                 then the global-memory levels for larger candidate sets)
 //   emit          writes S in index order (second look-back), clears v (and u with masking)
@@ -295,6 +296,7 @@ struct Args {
     uint64_t* st_emit;
     uint32_t* cidx;   // candidates, ascending index
     uint32_t* sidx;   // per-tile candidate slots of the streaming pass
+    float* cval;      // candidate values v[cidx[f]] (in sidx's memory, once the slots are moved)
     uint32_t* tcount; // per-tile candidate counts, then (k_collect) each tile's first position
     uint32_t* tseg;   // streaming tile t starts in segment tseg[t]; tseg[ptiles] = nseg - 1
     uint32_t* eseg;   // emit tile t's candidates lie in segments [eseg[2t], eseg[2t + 1]]
@@ -778,8 +780,7 @@ __global__ void __launch_bounds__(kThreads) k_sample(Args a) {
 template <int kKind>
 __device__ __forceinline__ uint64_t item_x(const Args& a, uint32_t i) {
     if (kKind == 0) return (uint64_t)a.skeys[i] << 32;
-    const uint32_t idx = a.cidx[i];
-    return ((uint64_t)key_of(a.v[idx]) << 32) | (uint64_t)(~idx);
+    return ((uint64_t)key_of(a.cval[i]) << 32) | (uint64_t)(~a.cidx[i]);
 }
 
 // Runs inside the cooperative select, where other blocks change the segment words between
@@ -1008,9 +1009,9 @@ __global__ void __launch_bounds__(kThreads) k_select_global(Args a) {
 // One block per active segment whose items fit in shared memory: every level runs on chip, and
 // each level keeps only the items that still match the prefix (each warp compacts its own share
 // in place). Segments with more items stay active for the global-memory levels
-// (k_select_global). The segment's contiguous items (sample keys, or candidate indices) arrive
-// in one bulk copy; for candidates the keys of v at those indices are then gathered with every
-// load in flight at once, and counted for the first level as they arrive. For the sample select
+// (k_select_global). The segment's contiguous items (sample keys, or candidate indices and
+// values) arrive by bulk copy; candidate values become keys and are counted for the first
+// level on chip. For the sample select
 // the first level's counts come from the sampling kernel's histogram, cleared here as the global
 // walk would. Two blocks fit on an SM, so up to 2 x 152 segments run in one wave.
 constexpr int kSmallThreads = 512;
@@ -1022,7 +1023,6 @@ __global__ void __launch_bounds__(kSmallThreads, 2) k_select_small(Args a) {
     constexpr uint32_t kCap = (uint32_t)(kSmallBytes / (4 * kArrays)) - 4;
     constexpr int kW = kSmallThreads / 32;
     constexpr int kLevels = kKind == 0 ? 3 : 6;
-    constexpr int kBatch = 16;
     extern __shared__ __align__(16) unsigned char s_dyn[];
     __shared__ uint32_t s_hist[kHistBins];
     __shared__ uint32_t s_scan[33];
@@ -1037,7 +1037,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2) k_select_small(Args a) {
     if (C > kCap) return;
     uint32_t* sraw = reinterpret_cast<uint32_t*>(s_dyn);
     uint32_t* s_a = sraw + (i0 & 3u);  // item i: key (kind 0) or candidate index (kind 1)
-    uint32_t* s_k = sraw + kCap + 4;   // kind 1: key of item i
+    uint32_t* s_k = sraw + kCap + 4 + (i0 & 3u);  // kind 1: the value, then the key, of item i
     if (threadIdx.x == 0) {
         s_fail = 0;
         mbar_init(&s_bar, 1);
@@ -1045,14 +1045,21 @@ __global__ void __launch_bounds__(kSmallThreads, 2) k_select_small(Args a) {
         // whole 16-byte units from the boundary at or before item 0; the workspace regions are
         // padded to 256 bytes, so the last unit stays inside the array's region
         const uint32_t bytes = (((i0 & 3u) + C + 3u) & ~3u) * 4u;
-        mbar_arrive_expect_tx(&s_bar, bytes);
+        mbar_arrive_expect_tx(&s_bar, kKind == 0 ? bytes : 2u * bytes);
         if (bytes) bulk_g2s(sraw, (kKind == 0 ? a.skeys : a.cidx) + (i0 & ~3u), bytes, &s_bar);
+        if (kKind == 1 && bytes)
+            bulk_g2s(sraw + kCap + 4, a.cval + (i0 & ~3u), bytes, &s_bar);
     }
-    if (kKind == 0) {
+    constexpr int kBinsPer = kHistBins / kSmallThreads;
+    if (kKind == 0) {  // all of the thread's bins in flight at once, then cleared
         uint32_t* gh = a.histA + (size_t)s * kHistBins;
-        for (int b = threadIdx.x; b < kHistBins; b += kSmallThreads) {
-            s_hist[b] = gh[b];
-            gh[b] = 0;
+        uint32_t hv[kBinsPer];
+#pragma unroll
+        for (int r = 0; r < kBinsPer; ++r) hv[r] = gh[threadIdx.x + r * kSmallThreads];
+#pragma unroll
+        for (int r = 0; r < kBinsPer; ++r) {
+            s_hist[threadIdx.x + r * kSmallThreads] = hv[r];
+            gh[threadIdx.x + r * kSmallThreads] = 0;
         }
     } else {
         for (int b = threadIdx.x; b < kHistBins; b += kSmallThreads) s_hist[b] = 0;
@@ -1082,21 +1089,17 @@ __global__ void __launch_bounds__(kSmallThreads, 2) k_select_small(Args a) {
     const uint32_t wb = min(C, (uint32_t)warp * R), we = min(C, wb + R);
     uint32_t wn = we - wb;  // items this warp still holds, at the front of its share
     if (kKind == 1) {
-        for (uint32_t j0 = wb; j0 < we; j0 += 32 * kBatch) {
-            float vr[kBatch];
-#pragma unroll
-            for (int r = 0; r < kBatch; ++r) {
-                const uint32_t i = j0 + 32 * r + lane;
-                vr[r] = (i < we) ? a.v[s_a[i]] : 0.f;
-            }
-#pragma unroll
-            for (int r = 0; r < kBatch; ++r) {
-                const uint32_t i = j0 + 32 * r + lane;
-                if (i < we) {
-                    const uint32_t key = key_of(vr[r]);
-                    s_k[i] = key;
-                    atomicAdd(&s_hist[key >> 20], 1u);  // X >> 52: the first level's digit
-                }
+        // values to keys, counted for the first level; candidates crowd into a few first-level
+        // bins, so lanes with the same bin add once
+        for (uint32_t j = wb; j < we + 31u; j += 32) {
+            const uint32_t i = j + lane;
+            const bool in = i < we && j < we;
+            const uint32_t key = in ? (s_k[i] & 0x7FFFFFFFu) : 0u;
+            const uint32_t bin = in ? key >> 20 : 0xFFFFFFFFu;  // X >> 52
+            const unsigned peers = __match_any_sync(kFull, bin);
+            if (in) {
+                s_k[i] = key;
+                if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], (uint32_t)__popc(peers));
             }
         }
         __syncthreads();
@@ -1645,6 +1648,28 @@ __global__ void __launch_bounds__(kThreads) k_collect_copy(Args a) {
     }
 }
 
+// Every candidate's value v[cidx[f]], gathered once by the whole grid into cval (the slot
+// array's memory, free once k_collect / k_collect_copy have moved the slots): the selects and
+// the emit step then read values in list order, instead of each block gathering its segment's
+// share from one SM.
+__global__ void __launch_bounds__(kThreads) k_cval(Args a) {
+    if (ld_relaxed_u32((const uint32_t*)&a.ctl->abort)) return;
+    const uint64_t total = a.ctl->total_cand;
+    const uint64_t stride = (uint64_t)gridDim.x * kThreads;
+    constexpr int kB = 4;  // gathers in flight per thread
+    for (uint64_t f0 = (uint64_t)blockIdx.x * kThreads + threadIdx.x; f0 < total; f0 += kB * stride) {
+        uint32_t idx[kB];
+#pragma unroll
+        for (int r = 0; r < kB; ++r) idx[r] = (f0 + r * stride < total) ? a.cidx[f0 + r * stride] : 0u;
+        float x[kB];
+#pragma unroll
+        for (int r = 0; r < kB; ++r) x[r] = (f0 + r * stride < total) ? a.v[idx[r]] : 0.0f;
+#pragma unroll
+        for (int r = 0; r < kB; ++r)
+            if (f0 + r * stride < total) a.cval[f0 + r * stride] = x[r];
+    }
+}
+
 // ------------------------------------------------------------------- candidate ranges
 // One block: per-segment candidate ranges by binary search of the ascending candidate
 // indices, then who selects among them. pass 1 only runs after an exact-mode re-compaction.
@@ -1755,7 +1780,7 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
                 seg[q] = -1;
                 if (i < total) {
                     idx[q] = a.cidx[i];
-                    val[q] = a.v[idx[q]];
+                    val[q] = a.cval[i];
                     const int s = es0 + upper_bound_minus1(a.cand_off + es0, ens, (uint32_t)i);
                     seg[q] = s;
                     const SegInfo& d = a.segs[s];
@@ -1978,6 +2003,7 @@ Args make_args(const float* g, float* u, float* v, int64_t n, const int64_t* seg
     a.st_emit = reinterpret_cast<uint64_t*>(w + L.st_emit);
     a.cidx = reinterpret_cast<uint32_t*>(w + L.cidx);
     a.sidx = reinterpret_cast<uint32_t*>(w + L.sidx);
+    a.cval = reinterpret_cast<float*>(w + L.sidx);
     a.tcount = reinterpret_cast<uint32_t*>(w + L.tcount);
     a.tseg = reinterpret_cast<uint32_t*>(w + L.tseg);
     a.eseg = reinterpret_cast<uint32_t*>(w + L.eseg);
@@ -2146,6 +2172,7 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
         L1(k_recompact, (unsigned)L.fused_tiles, kThreads, a);
         L1(k_candoff, 1, 1024, a, 1);
     }
+    L1(k_cval, (unsigned)sms * 8, kThreads, a);
     if (selects) {
         small_select(1);
         global_select(1);
