@@ -747,7 +747,10 @@ __global__ void __launch_bounds__(kThreads) k_sample(Args a) {
         const uint64_t jg = chunk0 + r * kThreads + threadIdx.x;
         sg[r] = -1;
         if (jg < chunk_end) {
-            const int s = uniform ? s_seg0 : upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)jg);
+            // a chunk that crosses segments searches only its own segment range
+            const int s = uniform ? s_seg0
+                                  : s_seg0 + upper_bound_minus1(a.samp_off + s_seg0,
+                                                                s_seg1 - s_seg0 + 1, (uint32_t)jg);
             const uint32_t pos = a.spos[jg];  // the sample positions in ascending order
             gv[r] = __ldg(a.g + pos);
             uv[r] = a.u[pos];
@@ -833,7 +836,7 @@ __device__ void hist_level(const Args& a, int level, uint32_t* s_hist) {
             }
         } else {
             for (uint32_t i = (uint32_t)c0 + threadIdx.x; i < c1; i += kThreads) {
-                const int s = upper_bound_minus1(off, a.nseg, i);
+                const int s = s0 + upper_bound_minus1(off + s0, s1 - s0 + 1, i);
                 const SegInfo& d = a.segs[s];
                 if (__ldcg(&d.state) != kActive) continue;
                 const uint64_t x = item_x<kKind>(a, i);
@@ -1675,7 +1678,9 @@ __global__ void __launch_bounds__(kThreads) k_cval(Args a) {
 // indices, then who selects among them. pass 1 only runs after an exact-mode re-compaction.
 // In pass 0 the list is still laid out by streaming tile (k_collect left each tile's first
 // position in tcount), so the first candidate at or past x lies in x's tile's own range.
+constexpr int kCandoffStage = 4096;  // segment ranges staged in shared memory below this many
 __global__ void __launch_bounds__(1024) k_candoff(Args a, int pass) {
+    __shared__ uint32_t s_coff[kCandoffStage];
     __shared__ uint32_t s_active;
     __shared__ int s_skip;
     if (threadIdx.x == 0) s_skip = a.ctl->abort || (pass == 1 && !a.ctl->any_failed);
@@ -1702,12 +1707,18 @@ __global__ void __launch_bounds__(1024) k_candoff(Args a, int pass) {
         a.cand_off[s] = (s == a.nseg) ? total : lo;
     }
     __syncthreads();
-    // the segments of every emit tile's first and last candidate
+    // the segments of every emit tile's first and last candidate, searched in a shared-memory
+    // copy of the ranges when they fit
     const uint32_t etiles = (total + kEmitTile - 1) / kEmitTile;
+    const bool staged = a.nseg < kCandoffStage;
+    if (staged)
+        for (int s = threadIdx.x; s <= a.nseg; s += blockDim.x) s_coff[s] = a.cand_off[s];
+    __syncthreads();
+    const uint32_t* co = staged ? s_coff : a.cand_off;
     for (uint32_t t = threadIdx.x; t < etiles; t += blockDim.x) {
         const uint32_t f0 = t * kEmitTile, f1 = (uint32_t)umin64(total, (uint64_t)f0 + kEmitTile) - 1u;
-        a.eseg[2 * t] = (uint32_t)upper_bound_minus1(a.cand_off, a.nseg, f0);
-        a.eseg[2 * t + 1] = (uint32_t)upper_bound_minus1(a.cand_off, a.nseg, f1);
+        a.eseg[2 * t] = (uint32_t)upper_bound_minus1(co, a.nseg, f0);
+        a.eseg[2 * t + 1] = (uint32_t)upper_bound_minus1(co, a.nseg, f1);
     }
     uint32_t any_failed = 0, active = 0;
     for (int s = threadIdx.x; s < a.nseg; s += blockDim.x) {
