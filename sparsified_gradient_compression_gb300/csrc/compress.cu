@@ -1699,6 +1699,17 @@ __global__ void __launch_bounds__(1024) k_candoff(Args a, int pass) {
         if (pass == 0 && t < ntiles) {
             lo = a.tcount[t];
             hi = (t + 1 < ntiles) ? a.tcount[t + 1] : total;
+            // the tile's candidates ascend through [t kPTile, (t+1) kPTile): probe the position
+            // the tile's density predicts, and its left neighbour (exact when every entry of the
+            // tile is a candidate), before searching what is left
+            if (hi - lo > 2) {
+                const uint32_t g = lo + 1 + (uint32_t)((uint64_t)(x - t * kPTile) * (hi - lo - 1) /
+                                                       kPTile);
+                const uint32_t left = a.cidx[g - 1], here = a.cidx[g];
+                if (left >= x) hi = g - 1;
+                else if (here >= x) lo = hi = g;
+                else lo = g + 1;
+            }
         }
         while (lo < hi) {
             const uint32_t mid = (lo + hi) >> 1;

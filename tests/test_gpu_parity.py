@@ -267,6 +267,23 @@ def test_clip_extreme_magnitudes(case):
               sample_ratio=0.1, seed=case)
 
 
+@pytest.mark.parametrize("mode", ["exact", "sampled", "adacomp"])
+def test_many_segments(mode):
+    # ~6000 segments of 1-300 entries around a few large ones: more segments than one wave of
+    # on-chip selects, than the staged candidate ranges, and than the plan's 1024-segment passes;
+    # streaming, emit and clip tiles that cross dozens of segments
+    rng = np.random.default_rng({"exact": 1, "sampled": 2, "adacomp": 3}[mode])
+    sizes = list(rng.integers(1, 300, 6000))
+    for at, big in ((1000, 40_000), (3000, 120_000), (5999, 70_000)):
+        sizes[at] = big
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    n = int(off[-1])
+    m = {"exact": dgc.SELECT_EXACT, "sampled": dgc.SELECT_SAMPLED, "adacomp": dgc.SELECT_ADACOMP}
+    run_steps(lambda t: workloads.misc([t, 77], n, 0.01), off, 2, mode=m[mode], sparsity=0.99,
+              momentum=0.9, clip_norm=0.05, sample_ratio=0.1, seed=5, bin_size=64,
+              mask_momentum=True)
+
+
 @pytest.mark.parametrize("case", range(40))
 def test_sampled_edges(case):
     rng = np.random.default_rng(7000 + case)
