@@ -133,7 +133,8 @@ struct Ctl {
     uint32_t active;
     uint32_t any_failed;
     uint32_t ticket_fused, ticket_compact, ticket_emit, ticket_collect;
-    uint32_t ndense;        // tiles whose slots k_collect_copy moves
+    uint32_t ndense;        // tiles whose slots k_collect_copy moves: up to kCollectWarp ...
+    uint32_t nlarge;        // ... and more (listed from the end of dlist)
     uint32_t total_samples, total_clip_tiles, total_cand, total_sent;
     uint32_t emit_done;
     uint64_t tag;           // what the sample positions depend on, for this call
@@ -1583,6 +1584,7 @@ __global__ void __launch_bounds__(kThreads, stream_blocks_per_sm<kSel>()) k_stre
 // k_collect_copy.
 constexpr int kCGroup = kThreads;  // tiles per collect block
 constexpr uint32_t kCollectDirect = 16;  // a tile with at most this many candidates: copied in place
+constexpr uint32_t kCollectWarp = 256;   // up to this many: one warp; more: one block
 
 __global__ void __launch_bounds__(kThreads) k_collect(Args a) {
     __shared__ uint32_t s_ex[kCGroup + 1];
@@ -1628,26 +1630,50 @@ __global__ void __launch_bounds__(kThreads) k_collect(Args a) {
 #pragma unroll
             for (uint32_t j = 0; j < kCollectDirect; ++j)
                 if (j < c && (uint64_t)p + j < a.n) a.cidx[p + j] = x[j];
-        } else {
+        } else if (c <= kCollectWarp) {
             a.dlist[atomicAdd(&a.ctl->ndense, 1u)] = t;
+        } else {
+            a.dlist[ntiles - atomicAdd(&a.ctl->nlarge, 1u)] = t;
         }
     }
     if (grp == ngroups - 1 && tid == 0)
         a.ctl->total_cand = (uint32_t)umin64(gbase + total, a.n);
 }
 
-// The listed tiles' slots, one tile per block at a time (up to kPTile slots, coalesced).
+// The listed tiles' slots. A tile with more than kCollectWarp candidates (a run of small
+// all-candidate segments) is copied by a whole block. The others -- with AdaComp's bins nearly
+// every tile -- by a warp each: a warp reads the positions of 32 list entries at once (entries
+// spread over the warps) and then copies those tiles one after another.
 __global__ void __launch_bounds__(kThreads) k_collect_copy(Args a) {
     if (ld_relaxed_u32((const uint32_t*)&a.ctl->abort)) return;
     const uint32_t total = a.ctl->total_cand;
     const uint32_t nt = (uint32_t)a.ptiles;
-    const uint32_t nd = a.ctl->ndense;
-    for (uint32_t j = blockIdx.x; j < nd; j += gridDim.x) {
-        const uint32_t t = a.dlist[j];
+    const uint32_t nd = a.ctl->ndense, nl = a.ctl->nlarge;
+    for (uint32_t j = blockIdx.x; j < nl; j += gridDim.x) {
+        const uint32_t t = a.dlist[nt - j];
         const uint32_t p = a.tcount[t];
         const uint32_t e = (t + 1 < nt) ? a.tcount[t + 1] : total;
         for (uint32_t q = threadIdx.x; p + q < e; q += kThreads)
             a.cidx[p + q] = a.sidx[(uint64_t)t * kPTile + q];
+    }
+    const int lane = threadIdx.x & 31;
+    const uint64_t warps = (uint64_t)gridDim.x * kWarps;
+    for (uint64_t jb = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); jb < nd;
+         jb += 32 * warps) {
+        const uint64_t j = jb + lane * warps;
+        uint32_t t = 0, p = 0, e = 0;
+        if (j < nd) {
+            t = a.dlist[j];
+            p = a.tcount[t];
+            e = (t + 1 < nt) ? a.tcount[t + 1] : total;
+        }
+        const int m = (int)umin64(32, (nd - jb + warps - 1) / warps);  // entries jb + k warps < nd
+        for (int k = 0; k < m; ++k) {
+            const uint32_t tk = __shfl_sync(kFull, t, k), pk = __shfl_sync(kFull, p, k);
+            const uint32_t ek = __shfl_sync(kFull, e, k);
+            for (uint32_t q = lane; pk + q < ek; q += 32)
+                a.cidx[pk + q] = a.sidx[(uint64_t)tk * kPTile + q];
+        }
     }
 }
 
