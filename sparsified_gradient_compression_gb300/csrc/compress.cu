@@ -2185,11 +2185,14 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
             launch_failed = true;
         ++launches;
     };
-    coop((const void*)k_cache, cooperative_grid(2, sms));
-    const uint64_t sgrid = (L.max_samples + kThreads * kSamplePerThread - 1) /
-                           (kThreads * kSamplePerThread);
-    L1(k_sample, (unsigned)sgrid, kThreads, a);
-    const bool selects = hp.mode != DGC_SELECT_ADACOMP;  // AdaComp keeps every segment idle
+    // AdaComp draws no sample and keeps every segment idle: no cache, sample or select launches
+    const bool selects = hp.mode != DGC_SELECT_ADACOMP;
+    if (selects) {
+        coop((const void*)k_cache, cooperative_grid(2, sms));
+        const uint64_t sgrid = (L.max_samples + kThreads * kSamplePerThread - 1) /
+                               (kThreads * kSamplePerThread);
+        L1(k_sample, (unsigned)sgrid, kThreads, a);
+    }
     set_kernel_attributes();
     auto global_select = [&](int kind) {
         coop(kind == 0 ? (const void*)k_select_global<0> : (const void*)k_select_global<1>,
