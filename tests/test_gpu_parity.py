@@ -146,6 +146,30 @@ def test_bucket_1g_sampled_warmup_schedule():
 
 
 @pytest.mark.slow
+def test_bucket_1g_adacomp_bins_of_1000():
+    # the AdaComp bench configuration at full size: 2^30 entries, bins of 1000, two steps
+    n = 1 << 30
+    off = np.array([0, n])
+    pd, po = params_pair(mode=dgc.SELECT_ADACOMP, momentum=0.9, bin_size=1000)
+    u_h = np.zeros(n, np.float32)
+    v_h = np.zeros(n, np.float32)
+    u_d = torch.zeros(n, dtype=torch.float32, device="cuda")
+    v_d = torch.zeros(n, dtype=torch.float32, device="cuda")
+    comp = Compressor(n, off, pd)
+    for t in range(2):
+        g = workloads.gradient("bucket1g", t)
+        comp(dev_f32(g), u_d, v_d)
+        assert comp.status_code() == 0
+        idx, val, st = comp.results()
+        oidx, oval, ost = oracle.compress(g, u_h, v_h, off, po)
+        assert np.array_equal(idx, oidx) and same_bits(val, oval), f"step {t}"
+        assert st[0]["sent"] == ost[0]["sent"]
+        assert same_bits(host_f32(v_d), v_h) and same_bits(host_f32(u_d), u_h), f"step {t}"
+    del comp
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
 def test_aggregation_64_learners():
     n, W, k = 25_557_032, 64, 25_558
     for step in range(5):
