@@ -170,6 +170,53 @@ def test_bucket_1g_adacomp_bins_of_1000():
 
 
 @pytest.mark.slow
+def test_bench_pipeline_1g_in_cuda_graphs():
+    # the bench's own step on the 1B bucket in the configuration it times: the warm-up schedule
+    # call by call, then compress and encode as CUDA graph replays at 99.9% on gradient buffers
+    # resident in HBM; every step's selection, state, message and decoded dense array against
+    # the oracle
+    import bench
+
+    n = 1 << 30
+    off = np.array([0, n])
+    sched = list(workloads.WARMUP_SPARSITY[:4]) + [0.999]
+    kw = dict(mode=dgc.SELECT_SAMPLED, momentum=0.9, sample_ratio=0.01, reselect_factor=1.3,
+              seed=bench.SEED)
+    pd = [dgc.make_params(sparsity=s, **kw) for s in sched]
+    po = [oracle.make_params(sparsity=s, **kw) for s in sched]
+    pipe = bench.Pipeline(n, pd, torch.device("cuda", 0))
+    hosts = [workloads.gradient("bucket1g", step=i, seed=0, n=n) for i in range(2)]
+    pool = [torch.from_numpy(h).cuda() for h in hosts]
+    u_h = np.zeros(n, np.float32)
+    v_h = np.zeros(n, np.float32)
+
+    def check(t, g_h, p_o):
+        oidx, oval, _ = oracle.compress(g_h, u_h, v_h, off, p_o)
+        assert dgc.dgc_read_status(pipe.status) == 0
+        c = int(pipe.out_count.item())
+        assert np.array_equal(pipe.out_idx[:c].cpu().numpy().view(np.uint32), oidx), t
+        assert same_bits(pipe.out_val[:c].cpu().numpy(), oval), t
+        assert same_bits(host_f32(pipe.v), v_h) and same_bits(host_f32(pipe.u), u_h), t
+        msg = pipe.msg[: int(pipe.msg_bytes.item())].cpu().numpy().tobytes()
+        assert msg == oracle.encode(oidx, oval, n), t
+        _, odense = oracle.decode_accumulate([msg], n)
+        assert same_bits(host_f32(pipe.dense), odense), t
+
+    for i in range(4):  # the warm-up schedule, call by call
+        pipe.step(pool[i % 2], pd[i])
+        torch.cuda.synchronize()
+        check(i, hosts[i % 2], po[i])
+    graphs = [pipe.capture(g, pd[-1]) for g in pool]
+    torch.cuda.synchronize()
+    for i in range(4, 7):  # 99.9%, replayed
+        pipe.step(pool[i % 2], pd[-1], None, graphs[i % 2])
+        torch.cuda.synchronize()
+        check(i, hosts[i % 2], po[-1])
+    del pipe, pool, graphs
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
 def test_aggregation_64_learners():
     n, W, k = 25_557_032, 64, 25_558
     for step in range(5):
