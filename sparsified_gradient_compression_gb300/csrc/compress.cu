@@ -140,6 +140,7 @@ struct Ctl {
     uint64_t tag;           // what the sample positions depend on, for this call
     uint64_t csum;          // checksum of the cached positions as found
     uint64_t newsum;        // checksum of the rebuilt positions
+    uint32_t ncomp;         // sample keys kept by the sample select's second level
     uint32_t bar_count;     // grid barrier of the cooperative select: arrivals, generation
     uint32_t bar_gen;
     uint32_t pad;
@@ -789,8 +790,31 @@ __device__ __forceinline__ uint64_t item_x(const Args& a, uint32_t i) {
 
 // Runs inside the cooperative select, where other blocks change the segment words between
 // levels: those are read past L1 (ld.global.cg).
+// With `compact` (the sample select's second level) every item that matches its segment's
+// prefix is also appended to a compact list -- its key in the slot array's memory, its segment
+// in the candidate list's, both unused until the streaming pass -- so that the third level
+// counts only those (hist_compact).
+constexpr uint32_t kCompBuf = 1024;  // kept keys a block gathers before one global append
+__device__ __forceinline__ void compact_push(const Args& a, uint32_t* s_ck, uint32_t* s_cs,
+                                             uint32_t* s_cn, uint32_t key, uint32_t seg) {
+    const uint32_t q = atomicAdd(s_cn, 1u);
+    if (q < kCompBuf) {
+        s_ck[q] = key;
+        s_cs[q] = seg;
+    } else {  // the block's buffer is full: straight to the list
+        const uint32_t pos = atomicAdd(&a.ctl->ncomp, 1u);
+        if (pos < a.n) {
+            a.sidx[pos] = key;
+            a.cidx[pos] = seg;
+        }
+    }
+}
+
 template <int kKind>
-__device__ void hist_level(const Args& a, int level, uint32_t* s_hist) {
+__device__ void hist_level(const Args& a, int level, uint32_t* s_hist, bool compact) {
+    __shared__ uint32_t s_ck[kCompBuf], s_cs[kCompBuf];
+    __shared__ uint32_t s_cn, s_cbase;
+    if (threadIdx.x == 0) s_cn = 0;
     const uint32_t* off = kKind == 0 ? a.samp_off : a.cand_off;
     const uint32_t total = off[a.nseg];
     uint32_t* ghist = (level & 1) ? a.histB : a.histA;
@@ -832,8 +856,10 @@ __device__ void hist_level(const Args& a, int level, uint32_t* s_hist) {
 #pragma unroll
             for (int r = 0; r < kPer; ++r) {
                 const uint32_t i = (uint32_t)c0 + r * kThreads + threadIdx.x;
-                if (i < c1 && (xs[r] >> (shift + bits)) == prefix)
+                if (i < c1 && (xs[r] >> (shift + bits)) == prefix) {
                     atomicAdd(&s_hist[(xs[r] >> shift) & mask], 1u);
+                    if (compact) compact_push(a, s_ck, s_cs, &s_cn, (uint32_t)(xs[r] >> 32), s0);
+                }
             }
         } else {
             for (uint32_t i = (uint32_t)c0 + threadIdx.x; i < c1; i += kThreads) {
@@ -841,12 +867,43 @@ __device__ void hist_level(const Args& a, int level, uint32_t* s_hist) {
                 const SegInfo& d = a.segs[s];
                 if (__ldcg(&d.state) != kActive) continue;
                 const uint64_t x = item_x<kKind>(a, i);
-                if ((x >> (shift + bits)) == __ldcg(&d.prefix))
+                if ((x >> (shift + bits)) == __ldcg(&d.prefix)) {
                     atomicAdd(&ghist[(size_t)s * kHistBins + ((x >> shift) & mask)], 1u);
+                    if (compact) compact_push(a, s_ck, s_cs, &s_cn, (uint32_t)(x >> 32), (uint32_t)s);
+                }
             }
         }
     }
-    h.flush(ghist, nbins);
+    h.flush(ghist, nbins);  // ends with a barrier: the block's kept keys are all in s_ck
+    if (compact) {  // one global append for the block's kept keys
+        const uint32_t m = min(s_cn, kCompBuf);
+        if (threadIdx.x == 0) s_cbase = m ? atomicAdd(&a.ctl->ncomp, m) : 0u;
+        __syncthreads();
+        for (uint32_t q = threadIdx.x; q < m; q += kThreads) {
+            const uint32_t pos = s_cbase + q;
+            if (pos < a.n) {
+                a.sidx[pos] = s_ck[q];
+                a.cidx[pos] = s_cs[q];
+            }
+        }
+    }
+}
+
+// The sample select's third level over the compact list the second level left (key, segment),
+// written by other blocks before the grid barrier: read past L1.
+__device__ void hist_compact(const Args& a, int level) {
+    const uint32_t nc = (uint32_t)umin64(ld_relaxed_u32(&a.ctl->ncomp), a.n);
+    uint32_t* ghist = (level & 1) ? a.histB : a.histA;
+    const int shift = c_shift[level], bits = c_bits[level];
+    const uint32_t mask = (1u << bits) - 1u;
+    for (uint32_t i = blockIdx.x * kThreads + threadIdx.x; i < nc; i += gridDim.x * kThreads) {
+        const uint32_t s = __ldcg(a.cidx + i);
+        const uint64_t x = (uint64_t)__ldcg(a.sidx + i) << 32;
+        const SegInfo& d = a.segs[s];
+        if (__ldcg(&d.state) != kActive) continue;
+        if ((x >> (shift + bits)) == __ldcg(&d.prefix))
+            atomicAdd(&ghist[(size_t)s * kHistBins + ((x >> shift) & mask)], 1u);
+    }
 }
 
 // ----------------------------------------------------------------- radix select: find
@@ -961,7 +1018,8 @@ __device__ bool grid_barrier(const Args& a, int* s_ok) {
 }
 
 // The global-memory radix select for the segments the on-chip select left active, every level
-// in one cooperative launch: a level counts (all blocks, grid-stride over the items), then
+// in one cooperative launch: a level counts (all blocks, grid-stride over the items; the sample
+// select's third level only over the keys its second level kept), then
 // after a grid barrier blocks take the active segments and walk their histograms from the top,
 // then a grid barrier. The sample select's first level was counted by the sampling
 // kernel. The kernel ends as soon as no segment is active, at once when none was to begin
@@ -981,7 +1039,10 @@ __global__ void __launch_bounds__(kThreads) k_select_global(Args a) {
     for (int level = 0; level < kLevels; ++level) {
         const int bits = c_bits[level];
         if (kKind == 1 || level > 0) {
-            hist_level<kKind>(a, level, s_hist);
+            if (kKind == 0 && level == 2)
+                hist_compact(a, level);
+            else
+                hist_level<kKind>(a, level, s_hist, kKind == 0 && level == 1);
             if (!grid_barrier(a, &s_bar)) return;
         }
         uint32_t* hbase = (level & 1) ? a.histB : a.histA;
