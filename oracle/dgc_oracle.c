@@ -35,7 +35,6 @@
 
 #define ORC_BILLION 1000000000ull
 #define ORC_GOLDEN 0x9E3779B97F4A7C15ull /* SplitMix64 increment (Steele, Lea, Flood 2014) */
-#define ORC_CLIP_TILE 4096
 #define ORC_RUN_ESCAPE 0xFFFFu
 #define ORC_MAGIC 0x31434744u /* bytes 'D','G','C','1' read little-endian */
 
@@ -78,28 +77,79 @@ uint64_t orc_sample_position(uint64_t seed, uint32_t segment, uint64_t j, uint64
     return orc_mulhi64(orc_mix64(seg_seed + ORC_GOLDEN * (j + 1)), n_s);
 }
 
-/* Sum of squares of x[lo, lo+len) in binary64, split recursively in halves; entries at or
- * past `end` count as zero. Each square of a binary32 value is exact in binary64. */
-static double orc_pairwise_sq(const float* x, int64_t lo, int64_t len, int64_t end) {
-    if (len == 1) {
-        if (lo >= end) return 0.0;
-        double d = (double)x[lo];
-        return d * d;
+/* The sum of squares is kept exactly as a non-negative integer X in base-2^32 digits, least
+ * significant first. Entry x = m 2^(e'-150) (m its 24-bit significand with the hidden bit,
+ * e' = max(biased exponent, 1)) has x^2 = m^2 2^(2e'-300), and X collects m^2 2^(2e'-2), so
+ * that the sum of squares is X 2^-298. With m^2 < 2^48, 2e'-2 <= 506 and at most 2^32 entries,
+ * X < 2^586: twenty digits hold it. */
+#define ORC_SQ_DIGITS 20
+
+/* d += x 2^(32 i), carrying upward */
+static void orc_digits_add(uint32_t* d, int i, uint64_t x) {
+    uint64_t carry = x;
+    while (carry != 0 && i < ORC_SQ_DIGITS) {
+        const uint64_t t = (uint64_t)d[i] + (carry & 0xFFFFFFFFull);
+        d[i] = (uint32_t)t;
+        carry = (carry >> 32) + (t >> 32);
+        ++i;
     }
-    int64_t half = len / 2;
-    double left = orc_pairwise_sq(x, lo, half, end);
-    double right = orc_pairwise_sq(x, lo + half, half, end);
-    return left + right;
 }
 
-/* Squared L2 norm for local gradient clipping, [DGC] Proposed method, bullet 4. Reading: a
- * fixed order so that every implementation rounds alike -- tiles of 4096 entries from the
- * segment start (the last one padded with zeros), each summed pairwise, and the tile sums
- * added left to right in binary64. */
+static int orc_digits_bit(const uint32_t* d, int b) { return (int)((d[b / 32] >> (b % 32)) & 1u); }
+
+/* X 2^-298 rounded to the nearest binary64, ties to the even significand. The result is never
+ * below 2^-298 (unless X = 0) nor near the binary64 overflow, so the significand is kept whole
+ * and ldexp only moves the exponent. */
+static double orc_digits_round(const uint32_t* d) {
+    int top = -1;
+    for (int b = ORC_SQ_DIGITS * 32 - 1; b >= 0 && top < 0; --b)
+        if (orc_digits_bit(d, b)) top = b;
+    if (top < 0) return 0.0;
+    int low = top - 52;  /* the last bit kept */
+    if (low < 0) low = 0;
+    uint64_t mant = 0;
+    for (int b = top; b >= low; --b) mant = (mant << 1) | (uint64_t)orc_digits_bit(d, b);
+    if (low > 0) {
+        const int half = orc_digits_bit(d, low - 1);
+        int rest = 0;
+        for (int b = low - 2; b >= 0 && !rest; --b) rest = orc_digits_bit(d, b);
+        if (half && (rest || (mant & 1u))) {
+            mant += 1;
+            if (mant == (1ull << 53)) {
+                mant >>= 1;
+                low += 1;
+            }
+        }
+    }
+    return ldexp((double)mant, low - 298);
+}
+
+/* Squared L2 norm for local gradient clipping, [DGC] Proposed method, bullet 4. Reading: the
+ * pages fix no order for the sum, so S is the exact sum of the squares rounded once to the
+ * nearest binary64 (ties to even) -- the one value that every order of exact arithmetic
+ * reaches. A NaN entry makes S NaN; otherwise an infinite entry makes it +infinity. */
 double orc_sumsq(const float* g, int64_t n) {
-    double s = 0.0;
-    for (int64_t t = 0; t < n; t += ORC_CLIP_TILE) s += orc_pairwise_sq(g, t, ORC_CLIP_TILE, n);
-    return s;
+    uint32_t d[ORC_SQ_DIGITS];
+    memset(d, 0, sizeof d);
+    int has_inf = 0, has_nan = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t bits;
+        memcpy(&bits, &g[i], sizeof bits);
+        const uint32_t e = (bits >> 23) & 0xFFu;
+        const uint32_t f = bits & 0x7FFFFFu;
+        if (e == 0xFFu) {
+            if (f) has_nan = 1; else has_inf = 1;
+            continue;
+        }
+        const uint64_t m = e ? (f | 0x800000u) : f;
+        const uint64_t m2 = m * m;
+        const int at = 2 * (int)(e ? e : 1u) - 2;  /* the bit of X where m^2 starts */
+        orc_digits_add(d, at / 32, (m2 & 0xFFFFFFFFull) << (at % 32));
+        orc_digits_add(d, at / 32 + 1, (m2 >> 32) << (at % 32));
+    }
+    if (has_nan) return NAN;
+    if (has_inf) return INFINITY;
+    return orc_digits_round(d);
 }
 
 /* Local gradient clipping, [DGC] Proposed method, bullet 4. Reading: it bounds the L2 norm of

@@ -267,6 +267,23 @@ def test_accumulate_one_is_single_rounding_fma(orc, seed):
         assert X.bits(vo) == X.bits(X.add_f32(v, ue))
 
 
+@pytest.mark.parametrize("seed", range(2))
+def test_accumulate_one_clipped_scales_g_first(orc, seed):
+    # a clipped gradient enters as the binary32 product g * scale (one rounding), then the fma;
+    # an unclipped one enters bitwise, whatever scale is passed
+    rng = np.random.default_rng(70 + seed)
+    for _ in range(200):
+        g, u, v = (np.float32(x) for x in rng.standard_normal(3) * 10.0 ** rng.integers(-6, 6, 3))
+        scale = np.float32(rng.uniform(0.01, 0.99))
+        m = np.float32(rng.choice([0.9, 0.5, 0.0]))
+        uo, vo = orc.accumulate_one(g, u, v, m, scale=scale, clipped=True)
+        ue = X.fma_f32(m, u, X.mul_f32(g, scale))
+        assert X.bits(uo) == X.bits(ue)
+        assert X.bits(vo) == X.bits(X.add_f32(v, ue))
+        uo, _ = orc.accumulate_one(g, u, v, m, scale=scale, clipped=False)
+        assert X.bits(uo) == X.bits(X.fma_f32(m, u, g))
+
+
 # ---------------------------------------------------------------------------------- clipping
 def test_clip_scale_closed_form(orc):
     # DGC review, Proposed method, bullet 4: norm of (3, 4) is 5; bound 1 gives 1/5 in binary32.
@@ -276,13 +293,30 @@ def test_clip_scale_closed_form(orc):
     assert not clipped and s == 1.0
 
 
+def _is_nearest_binary64(S: float, exact: Fraction) -> bool:
+    """S is a binary64 nearest to `exact`; on a tie, the one whose significand is even."""
+    here = abs(Fraction(S) - exact)
+    for nb in (np.nextafter(S, -np.inf), np.nextafter(S, np.inf)):
+        there = abs(Fraction(float(nb)) - exact)
+        if there < here:
+            return False
+        if there == here and (struct.unpack("<Q", struct.pack("<d", S))[0] & 1):
+            return False
+    return True
+
+
 @pytest.mark.parametrize("n", [1, 2, 4095, 4096, 4097, 12289, 50_000])
-def test_sumsq_close_to_exact_sum(orc, n):
+def test_sumsq_is_the_exact_sum_rounded_once(orc, n):
+    # Entries over ~60 binades, subnormals included: S must be the binary64 nearest to the exact
+    # rational sum of squares (ties to even), and equal to Python's correctly rounded math.fsum
+    # of the (exact) binary64 squares.
     rng = np.random.default_rng(n)
-    g = (rng.standard_normal(n) * 10.0 ** rng.integers(-3, 3, n)).astype(np.float32)
+    g = (rng.standard_normal(n) * 2.0 ** rng.integers(-30, 30, n)).astype(np.float32)
+    g[rng.integers(0, n, max(1, n // 100))] = np.float32(1e-44)
     exact = sum(Fraction(float(x)) ** 2 for x in g)
     S = orc.sumsq(g)
-    assert abs(Fraction(S) - exact) <= exact * Fraction(n, 2**52)
+    assert _is_nearest_binary64(S, exact)
+    assert S == math.fsum(float(x) * float(x) for x in g)
 
 
 def test_sumsq_exact_on_integers(orc):
@@ -496,12 +530,11 @@ def test_decode_rejects_malformed(orc):
         assert np.all(dense == 7.0)
 
 
-# ------------------------------------------------------------- fixed summation order (clipping)
-# The reading fixes the order of the binary64 sum of squares: tiles of 4096 entries from the
-# segment start, each summed in halves recursively, then the tile sums left to right. The
-# inputs below are powers of two whose partial sums round differently under any other order;
-# the expected values are worked out by hand (2^54 has spacing 4 between binary64 neighbours,
-# so 2^54 + 2 is a tie that rounds to the even 2^54).
+# ------------------------------------------------------------- the clipping sum, rounded once
+# The reading makes the sum of squares exact and rounds it once to binary64 (ties to even), so no
+# order of summation shows. The inputs are powers of two worked out by hand: 2^54 has spacing 4
+# between binary64 neighbours, so 2^54 + 1 rounds down, 2^54 + 2 is a tie that goes to the even
+# 2^54, and 2^54 + 3 rounds up to 2^54 + 4.
 def _sparse(n, items):
     g = np.zeros(n, np.float32)
     for i, x in items:
@@ -509,24 +542,40 @@ def _sparse(n, items):
     return g
 
 
-def test_sumsq_pairwise_inside_a_tile(orc):
-    # halves: (2^54 + 0 + 0 + 0) + (1 + 1 + 1 + 1) = 2^54 + 4 exactly; a running sum would
-    # drop each 1 and return 2^54.
-    g = _sparse(8, [(0, 2.0**27), (4, 1.0), (5, 1.0), (6, 1.0), (7, 1.0)])
-    assert orc.sumsq(g) == 2.0**54 + 4
+@pytest.mark.parametrize("ones,expected", [(1, 2.0**54), (2, 2.0**54), (3, 2.0**54 + 4),
+                                           (4, 2.0**54 + 4), (6, 2.0**54 + 8)])
+def test_sumsq_rounds_once_to_nearest_even(orc, ones, expected):
+    g = _sparse(16384, [(0, 2.0**27)] + [(4096 * (i % 4) + i, 1.0) for i in range(1, ones + 1)])
+    assert orc.sumsq(g) == expected
+    # the same entries in any order give the same S: a running binary64 sum from the left
+    # would drop each 1 against 2^54 and return 2^54 for every count above
+    rng = np.random.default_rng(ones)
+    for _ in range(3):
+        assert orc.sumsq(g[rng.permutation(g.size)]) == expected
 
 
-def test_sumsq_tiles_are_4096_long(orc):
-    # tile 0 = 2^54, tile 1 = 1+1+1+1 = 4 (summed inside the tile) -> 2^54 + 4. Tiles of 2048
-    # would add 2 and 2 to the running total one at a time and return 2^54.
-    g = _sparse(8192, [(0, 2.0**27), (4096, 1.0), (4097, 1.0), (6144, 1.0), (6145, 1.0)])
-    assert orc.sumsq(g) == 2.0**54 + 4
+def test_sumsq_keeps_what_partial_sums_would_drop(orc):
+    # 2^-298 (the square of the least binary32 subnormal) is far below the spacing of 1.0, but
+    # 2^53 of them would add up to 2^-245; here 3 of them next to 1 vanish, alone they stay
+    tiny = np.float32(2.0**-149)
+    assert orc.sumsq(np.array([tiny], np.float32)) == 2.0**-298
+    assert orc.sumsq(np.array([tiny, tiny, tiny], np.float32)) == 3 * 2.0**-298
+    assert orc.sumsq(np.array([1.0, tiny, tiny, tiny], np.float32)) == 1.0
+    # the largest binary32 squared four times: exact, far from binary64 overflow
+    big = np.float32(np.finfo(np.float32).max)
+    assert orc.sumsq(np.full(4, big, np.float32)) == 4 * float(big) ** 2
+    # above 1 the spacing is 2^-52: two squares of 2^-27 (2^-54 each) make exactly half of it,
+    # a tie that stays at the even 1.0; a trace more (2^-298) tips it to 1 + 2^-52
+    h = 2.0**-27
+    assert orc.sumsq(np.array([1.0, h], np.float32)) == 1.0
+    assert orc.sumsq(np.array([1.0, h, h], np.float32)) == 1.0
+    assert orc.sumsq(np.array([h, 1.0, tiny, h], np.float32)) == 1.0 + 2.0**-52
 
 
-def test_sumsq_tile_sums_left_to_right(orc):
-    # tiles 2^54, 0, 2, 2 added left to right: 2^54 + 2 rounds to 2^54 twice -> 2^54.
-    g = _sparse(16384, [(0, 2.0**27), (8192, 1.0), (8193, 1.0), (12288, 1.0), (12289, 1.0)])
-    assert orc.sumsq(g) == 2.0**54
+def test_sumsq_non_finite(orc):
+    assert math.isnan(orc.sumsq(np.array([1.0, np.nan, np.inf], np.float32)))
+    assert orc.sumsq(np.array([1.0, -np.inf, 2.0], np.float32)) == math.inf
+    assert orc.sumsq(np.zeros(0, np.float32)) == 0.0
 
 
 def test_reselect_not_taken_at_exactly_factor_times_k(orc):
