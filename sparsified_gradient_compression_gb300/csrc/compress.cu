@@ -10,8 +10,9 @@
 // segment table and counters the previous ones left in the workspace, so no host round trip):
 //
 //   plan          segment table: k, sample counts, seeds, bins; validates seg_off; zeroes counters
-//   clip_tiles    [clipping] binary64 pairwise sum of g^2 per 4096-entry clip tile; the block
-//                 finishing a segment's last tile adds its tile sums left to right -> scale
+//   clip_tiles    [clipping] exact sum of g^2 per segment in integer arithmetic (a 128-bit
+//                 window per thread, 640-bit sums per segment); the block finishing a
+//                 segment's last tile rounds it once to binary64 -> scale
 //   cache         [sampled, exact] the sample positions, kept sorted in the workspace; checked
 //                 every call (tag + checksum), rebuilt only when they no longer match (one
 //                 cooperative launch)
@@ -95,6 +96,9 @@ constexpr uint32_t kMbarSpinLimit = 1u << 22;
 constexpr int kEmitRows = 4;
 constexpr int kEmitTile = kThreads * kEmitRows * 4;  // 4096 candidates per emit tile
 constexpr int kClipTile = 4096;
+constexpr int kSqLimbs = 10;   // 640-bit exact sum of squares, 64-bit limbs (when rounded)
+constexpr int kSqDigits = 20;  // the same sum as 32-bit digits, each in a 64-bit word
+constexpr int kSqWords = kSqDigits + 1;  // + one word of flags (2: +inf seen, 4: NaN seen)
 constexpr int kHistBins = 2048;
 constexpr int kSamplePerThread = 4;
 constexpr uint64_t kExactSamplePpb = 10000000;    // exact mode samples 1% to bound t from below
@@ -155,7 +159,7 @@ constexpr int kBucketShift = 10;  // cache order: 1024-entry buckets, segment by
 
 // Workspace layout (host computes it; every piece 256-byte aligned).
 struct Layout {
-    size_t ctl, scache, segs, seg_start, samp_off, clip_off, cand_off, clip_part, skeys, spos,
+    size_t ctl, scache, segs, seg_start, samp_off, clip_off, cand_off, clip_acc, skeys, spos,
         bcount, histA, histB;
     size_t st_collect, st_compact, st_emit, cidx, sidx, tcount, tseg, eseg, clip_cnt, dlist,
         binmax, total;
@@ -230,7 +234,7 @@ Layout make_layout(int64_t n, int32_t nseg, const HostParams& hp) {
     L.samp_off = take(sizeof(uint32_t) * (size_t)(nseg + 1));
     L.clip_off = take(sizeof(uint32_t) * (size_t)(nseg + 1));
     L.cand_off = take(sizeof(uint32_t) * (size_t)(nseg + 1));
-    L.clip_part = take(sizeof(double) * (size_t)L.max_clip_tiles);
+    L.clip_acc = take(sizeof(uint64_t) * kSqWords * (size_t)(hp.clip_on ? nseg : 0));
     L.skeys = take(sizeof(uint32_t) * (size_t)L.max_samples);
     L.spos = take(sizeof(uint32_t) * (size_t)L.max_samples);
     L.bcount = take(sizeof(uint32_t) * (size_t)L.nbuckets);
@@ -287,7 +291,7 @@ struct Args {
     uint32_t* samp_off;
     uint32_t* clip_off;
     uint32_t* cand_off;
-    double* clip_part;
+    unsigned long long* clip_acc;  // per segment: the exact sum of squares (kSqWords words)
     uint32_t* skeys;
     uint32_t* spos;    // sample positions in ascending order (cached between calls)
     uint32_t* bcount;  // per-bucket counts, then cursors, while the cache is rebuilt
@@ -430,6 +434,8 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
     for (size_t i = tid; i < a.nbuckets; i += stride) a.bcount[i] = 0;
     for (size_t i = tid; i < a.max_bins; i += stride) a.binmax[i] = 0;
     for (size_t i = tid; i < (size_t)a.nseg; i += stride) a.clip_cnt[i] = 0;
+    if (a.hp.clip_on)
+        for (size_t i = tid; i < (size_t)a.nseg * kSqWords; i += stride) a.clip_acc[i] = 0;
     // the segment of every streaming tile's first entry, searched in the caller's offsets (when
     // they are invalid, block 0 raises abort and no later kernel reads this)
     for (size_t t = tid; t <= a.ptiles; t += stride)
@@ -439,123 +445,203 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
 }
 
 // ----------------------------------------------------------------------------- clipping
-// The sum of squares of a segment: 4096-entry tiles from the segment start (the last padded
-// with zeros), each a complete binary tree, then the tile sums added left to right, all in
-// binary64. binary64 is slow on this part, so the squares (exact in binary64) are built with
-// integer operations and only the additions use the binary64 unit.
+// The sum of squares of a segment, exactly, rounded once to binary64 (ties to even). Entry
+// x = m 2^(e'-150) (m the 24-bit significand, e' = max(biased exponent, 1)) has the exact
+// square M 2^(2e'-300), M = m^2 < 2^48; the segment keeps X = sum M 2^(2e'-2) (2e'-2 <= 506, at
+// most 2^32 entries: X < 2^586) and S = X 2^-298. X lives in kSqDigits 64-bit words, word i
+// worth 2^(32 i): every addition puts less than 2^32 into a word, so the words take plain
+// atomic adds that nobody waits for, in any order, and never overflow (at most 2^21 additions
+// per word); the carries are propagated once, by k_clip_round.
 
-// x * x in binary64, exactly, from the bits of x: |x| = m 2^(e' - 150) with e' = max(e, 1), so
-// x^2 = M 2^(2e' - 300), M = m^2 < 2^48, and with p the top bit of M the binary64 exponent is
-// p + 2e' - 300 (never below -298 nor above 208: always a normal binary64). Returns the bits.
-__device__ __forceinline__ uint64_t exact_square_bits(float x) {
-    const uint32_t a = __float_as_uint(x) & 0x7FFFFFFFu;
-    const uint32_t e = a >> 23;
-    const uint32_t m = e ? ((a & 0x7FFFFFu) | 0x800000u) : a;
-    const uint64_t M = (uint64_t)m * m;
-    const int p = 63 - __clzll((long long)M);
-    const uint64_t ex = (uint64_t)(p + 2 * (int)max(e, 1u) - 300 + 1023);
-    uint64_t bits = (ex << 52) | ((M << ((52 - p) & 63)) & 0xFFFFFFFFFFFFFull);
-    if (a == 0) bits = 0;
-    if (a >= 0x7F800000u) bits = (a == 0x7F800000u) ? 0x7FF0000000000000ull : 0x7FF8000000000000ull;
-    return bits;
+// words[i..] += x 2^(32 i + sh) for x < 2^64, sh < 32: three 32-bit pieces
+__device__ __forceinline__ void digits_add(unsigned long long* words, int i, int sh,
+                                           unsigned long long x) {
+    const unsigned long long lo = (x & 0xFFFFFFFFull) << sh;  // < 2^63
+    const unsigned long long hi = (x >> 32) << sh;            // < 2^63
+    const unsigned long long d0 = lo & 0xFFFFFFFFull;
+    const unsigned long long d1 = (lo >> 32) + (hi & 0xFFFFFFFFull);
+    const unsigned long long d2 = hi >> 32;
+    if (d0) atomicAdd(words + i, d0);
+    if (d1) atomicAdd(words + i + 1, d1);  // < 2^33: two digits' worth, still far from overflow
+    if (d2) atomicAdd(words + i + 2, d2);
 }
 
-
-
-// One 4096-entry tile per block: thread t sums entries [16t, 16t+16) as a 4-level tree, then
-// the 256 thread sums combine pairwise in shared memory. The block that sums a segment's last
-// tile then adds the segment's tile sums left to right -- a chain of dependent binary64
-// additions on one lane while the other lanes keep the next chunk of tile sums in flight -- and
-// sets scale = c / sqrt(S) when sqrt(S) > c (binary64, correctly rounded sqrt and division,
-// rounded once to binary32). Tiles are taken from the last one backwards, so the long chains
-// of large segments late in the buffer run while the other tiles are still being summed.
-constexpr int kClipChunk = 512;
-__global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
-    __shared__ double s_t[kThreads];
-    __shared__ double s_buf[kClipChunk];
-    __shared__ int s_skip, s_last;
-    __shared__ uint32_t s_c;
-    if (threadIdx.x == 0) {
-        const uint32_t total = a.ctl->total_clip_tiles;
-        s_skip = a.ctl->abort || blockIdx.x >= total;
-        s_c = total - 1u - blockIdx.x;
-    }
-    __syncthreads();
-    if (s_skip) return;
-    const uint32_t c = s_c;
-    const int s = upper_bound_minus1(a.clip_off, a.nseg, c);
-    const SegInfo& d = a.segs[s];
-    const uint64_t base = (uint64_t)d.start + (uint64_t)(c - a.clip_off[s]) * kClipTile +
-                          16u * threadIdx.x;
-    uint64_t qb[16];
-    if ((base & 3u) == 0 && base + 16 <= d.end) {  // 16-byte aligned and whole: four float4
-        const float4* g4 = reinterpret_cast<const float4*>(a.g + base);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float4 x = g4[j];
-            qb[4 * j] = exact_square_bits(x.x);
-            qb[4 * j + 1] = exact_square_bits(x.y);
-            qb[4 * j + 2] = exact_square_bits(x.z);
-            qb[4 * j + 3] = exact_square_bits(x.w);
-        }
+// X 2^-298 to the nearest binary64, ties to even, from X in 64-bit limbs: the top 64 bits of
+// X, the bits below them folded into a sticky bit, then 53 of them kept. X < 2^586, so the
+// result is a normal number.
+__device__ double limbs_round(const unsigned long long* x) {
+    int h = kSqLimbs - 1;
+    while (h > 0 && x[h] == 0ull) --h;
+    if (x[h] == 0ull) return 0.0;
+    const int t = 64 * h + 63 - __clzll((long long)x[h]);  // the top set bit of X
+    unsigned long long top;  // bits t .. t-63 of X (zeros below bit 0)
+    bool sticky = false;
+    if (t < 64) {
+        top = x[0] << (63 - t);
     } else {
+        const int pos = t - 63, j = pos >> 6, sh = pos & 63;
+        top = sh ? ((x[j] >> sh) | (x[j + 1] << (64 - sh))) : x[j];
+        sticky = sh && (x[j] & ((1ull << sh) - 1ull)) != 0ull;
+        for (int i = 0; i < j; ++i) sticky = sticky || x[i] != 0ull;
+    }
+    unsigned long long mant = top >> 11;  // 53 bits, the leading one at bit 52
+    const bool half = (top >> 10) & 1ull;
+    sticky = sticky || (top & 0x3FFull) != 0ull;
+    int te = t;
+    if (half && (sticky || (mant & 1ull))) {
+        ++mant;
+        if (mant >> 53) {
+            mant >>= 1;
+            ++te;
+        }
+    }
+    // mant 2^(te - 52 - 298): biased exponent te - 298 + 1023
+    const unsigned long long bits =
+        ((unsigned long long)(te + 725) << 52) | (mant & 0xFFFFFFFFFFFFFull);
+    return __longlong_as_double((long long)bits);
+}
+
+// 4096-entry tiles of one segment each, the blocks looping over them. For a tile the block finds
+// the largest exponent e_max of its entries; each thread adds the squares of its 16 entries into
+// a 128-bit window whose lowest bit is bit lo = max(2 e_max - 68, 0) of X (a square there is
+// below 2^114, 4096 of them below 2^126). Squares that start below lo (entries more than 33
+// binades under the tile's largest) go to digit words in shared memory instead. The window's
+// block total, and the shared words when used (their carries propagated first, so each adds
+// less than 2^32 per word), then enter the segment's words in global memory.
+__global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
+    __shared__ unsigned long long s_low[kSqDigits];
+    __shared__ unsigned long long s_w[kThreads / 32][2];
+    __shared__ uint32_t s_emax[kThreads / 32];
+    __shared__ uint32_t s_flags;  // 1: an entry below the window; 2: +inf; 4: NaN
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) s_flags = 0;
+    if (threadIdx.x < kSqDigits) s_low[threadIdx.x] = 0ull;
+    if (a.ctl->abort) return;
+    const uint32_t total = a.ctl->total_clip_tiles;
+    for (uint32_t c = blockIdx.x; c < total; c += gridDim.x) {
+        const int s = upper_bound_minus1(a.clip_off, a.nseg, c);
+        const SegInfo& d = a.segs[s];
+        const uint64_t base = (uint64_t)d.start + (uint64_t)(c - a.clip_off[s]) * kClipTile +
+                              16u * threadIdx.x;
+        uint32_t xb[16];  // |x| bits
+        if ((base & 3u) == 0 && base + 16 <= d.end) {  // 16-byte aligned and whole: four float4
+            const uint4* g4 = reinterpret_cast<const uint4*>(a.g + base);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 x = g4[j];
+                xb[4 * j] = x.x & 0x7FFFFFFFu;
+                xb[4 * j + 1] = x.y & 0x7FFFFFFFu;
+                xb[4 * j + 2] = x.z & 0x7FFFFFFFu;
+                xb[4 * j + 3] = x.w & 0x7FFFFFFFu;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint64_t e = base + i;
+                xb[i] = (e < d.end) ? (__float_as_uint(a.g[e]) & 0x7FFFFFFFu) : 0u;
+            }
+        }
+        uint32_t em = 1;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const uint64_t e = base + i;
-            qb[i] = (e < d.end) ? exact_square_bits(a.g[e]) : 0ull;
+            const uint32_t e = xb[i] >> 23;
+            if (e != 0xFFu) em = max(em, e);
         }
-    }
-    double q[16];
+        em = __reduce_max_sync(0xFFFFFFFFu, em);
+        if (lane == 0) s_emax[warp] = em;
+        __syncthreads();  // (also orders the previous tile's use of s_w, s_low, s_flags)
 #pragma unroll
-    for (int i = 0; i < 16; ++i) q[i] = __longlong_as_double((long long)qb[i]);
+        for (int w = 0; w < kThreads / 32; ++w) em = max(em, s_emax[w]);
+        const int lo = max(2 * (int)em - 68, 0);
+        unsigned long long w0 = 0ull, w1 = 0ull;
+        uint32_t fl = 0;
 #pragma unroll
-    for (int w = 1; w < 16; w <<= 1)
-#pragma unroll
-        for (int i = 0; i < 16; i += 2 * w) q[i] = q[i] + q[i + w];
-    s_t[threadIdx.x] = q[0];
-    __syncthreads();
-#pragma unroll
-    for (int w = 1; w < kThreads; w <<= 1) {
-        const int i = 2 * w * threadIdx.x;
-        if (i < kThreads) s_t[i] = s_t[i] + s_t[i + w];
-        __syncthreads();
-    }
-    const uint32_t t0 = a.clip_off[s], t1 = a.clip_off[s + 1];
-    if (threadIdx.x == 0) {
-        a.clip_part[c] = s_t[0];
-        __threadfence();
-        s_last = (atomicAdd(&a.clip_cnt[s], 1u) == t1 - t0 - 1u);
-    }
-    __syncthreads();
-    if (!s_last || threadIdx.x >= 32) return;
-    __threadfence();  // every tile sum of the segment is in place: read them past L1
-    const int lane = threadIdx.x;
-    double r[kClipChunk / 32];
-    auto fetch = [&](uint32_t c0) {
-#pragma unroll
-        for (int i = 0; i < kClipChunk / 32; ++i) {
-            const uint32_t t = c0 + 32 * i + lane;
-            r[i] = (t < t1) ? __ldcg(a.clip_part + t) : 0.0;
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t ax = xb[i];
+            const uint32_t e = ax >> 23;
+            if (e == 0xFFu) {
+                fl |= (ax & 0x7FFFFFu) ? 4u : 2u;
+                continue;
+            }
+            const uint32_t m = e ? ((ax & 0x7FFFFFu) | 0x800000u) : ax;
+            const unsigned long long M = (unsigned long long)m * m;
+            const int at = 2 * (int)max(e, 1u) - 2;
+            const int r = at - lo;  // at most 66
+            if (r >= 0) {
+                const unsigned long long p0 = (r < 64) ? (M << r) : 0ull;
+                const unsigned long long p1 =
+                    (r == 0) ? 0ull : (r < 64) ? (M >> (64 - r)) : (M << (r - 64));
+                w0 += p0;
+                w1 += p1 + (w0 < p0 ? 1ull : 0ull);
+            } else if (M != 0ull) {
+                fl |= 1u;
+                digits_add(s_low, at >> 5, at & 31, M);
+            }
         }
-    };
-    double S = 0.0;
-    fetch(t0);
-    for (uint32_t c0 = t0; c0 < t1; c0 += kClipChunk) {
+        if (fl) atomicOr(&s_flags, fl);
 #pragma unroll
-        for (int i = 0; i < kClipChunk / 32; ++i) s_buf[32 * i + lane] = r[i];
-        __syncwarp();
-        if (c0 + kClipChunk < t1) fetch(c0 + kClipChunk);
+        for (int off = 16; off > 0; off >>= 1) {
+            const unsigned long long o0 = __shfl_down_sync(0xFFFFFFFFu, w0, off);
+            const unsigned long long o1 = __shfl_down_sync(0xFFFFFFFFu, w1, off);
+            w0 += o0;
+            w1 += o1 + (w0 < o0 ? 1ull : 0ull);
+        }
         if (lane == 0) {
-            const uint32_t len = min(t1 - c0, (uint32_t)kClipChunk);
-            for (uint32_t i = 0; i < len; ++i) S = S + s_buf[i];
+            s_w[warp][0] = w0;
+            s_w[warp][1] = w1;
         }
-        __syncwarp();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            unsigned long long* X = a.clip_acc + (size_t)s * kSqWords;
+            unsigned long long W0 = 0ull, W1 = 0ull;
+            for (int w = 0; w < kThreads / 32; ++w) {
+                W0 += s_w[w][0];
+                W1 += s_w[w][1] + (W0 < s_w[w][0] ? 1ull : 0ull);
+            }
+            // W 2^lo: W < 2^126 in five 32-bit pieces from word lo / 32
+            const int i = lo >> 5, sh = lo & 31;
+            digits_add(X, i, sh, W0);
+            digits_add(X, i + 2, sh, W1);
+            const uint32_t flags = s_flags;
+            if (flags & 1u) {
+                unsigned long long carry = 0ull;
+                for (int j = 0; j < kSqDigits; ++j) {
+                    const unsigned long long t = s_low[j] + carry;
+                    if (t & 0xFFFFFFFFull) atomicAdd(X + j, t & 0xFFFFFFFFull);
+                    carry = t >> 32;
+                    s_low[j] = 0ull;
+                }
+            }
+            if (flags & 6u) atomicOr(X + kSqDigits, (unsigned long long)(flags & 6u));
+            s_flags = 0;
+        }
     }
-    if (lane == 0) {
-        const double norm = sqrt(S);
-        const double cn = (double)a.hp.clip_norm;
-        a.segs[s].scale = (norm > cn) ? (float)(cn / norm) : 1.0f;
+}
+
+// One thread per segment, after every tile is summed: propagate the carries of the segment's
+// words into 32-bit digits, read them as 64-bit limbs, round once, and set scale = c / sqrt(S)
+// when sqrt(S) > c (correctly rounded binary64 sqrt and division, rounded once to binary32).
+// A segment without entries keeps S = 0 and scale 1.
+__global__ void __launch_bounds__(128) k_clip_round(Args a) {
+    const int s = blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= a.nseg || a.ctl->abort) return;
+    const unsigned long long* X = a.clip_acc + (size_t)s * kSqWords;
+    unsigned long long limb[kSqLimbs];
+    unsigned long long carry = 0ull;
+#pragma unroll
+    for (int j = 0; j < kSqLimbs; ++j) {
+        const unsigned long long t0 = X[2 * j] + carry;
+        const unsigned long long t1 = X[2 * j + 1] + (t0 >> 32);
+        limb[j] = (t0 & 0xFFFFFFFFull) | (t1 << 32);
+        carry = t1 >> 32;
     }
+    double S = limbs_round(limb);
+    const unsigned long long flags = X[kSqDigits];
+    if (flags & 4ull) S = __longlong_as_double(0x7FF8000000000000ll);
+    else if (flags & 2ull) S = __longlong_as_double(0x7FF0000000000000ll);
+    const double norm = sqrt(S);
+    const double cn = (double)a.hp.clip_norm;
+    a.segs[s].scale = (norm > cn) ? (float)(cn / norm) : 1.0f;
 }
 
 // v <- fma(leak, v, u): with leak = 1 this is the plain sum v + u, rounded once
@@ -2101,7 +2187,7 @@ Args make_args(const float* g, float* u, float* v, int64_t n, const int64_t* seg
     a.samp_off = reinterpret_cast<uint32_t*>(w + L.samp_off);
     a.clip_off = reinterpret_cast<uint32_t*>(w + L.clip_off);
     a.cand_off = reinterpret_cast<uint32_t*>(w + L.cand_off);
-    a.clip_part = reinterpret_cast<double*>(w + L.clip_part);
+    a.clip_acc = reinterpret_cast<unsigned long long*>(w + L.clip_acc);
     a.skeys = reinterpret_cast<uint32_t*>(w + L.skeys);
     a.spos = reinterpret_cast<uint32_t*>(w + L.spos);
     a.bcount = reinterpret_cast<uint32_t*>(w + L.bcount);
@@ -2236,7 +2322,10 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
                                                           (size_t)sms * 2);
     L1(k_plan, plan_grid, 1024, a);
     if (hp.clip_on) {
-        L1(k_clip_tiles, (unsigned)L.max_clip_tiles, kThreads, a);
+        L1(k_clip_tiles, (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(L.max_clip_tiles,
+                                                                            (uint64_t)sms * 4)),
+           kThreads, a);
+        L1(k_clip_round, (unsigned)((nseg + 127) / 128), 128, a);
     }
     bool launch_failed = false;
     auto coop = [&](const void* kernel, unsigned grid) {
@@ -2342,7 +2431,10 @@ extern "C" int dgc_compress_shared(const float* g, float* u, float* v, int64_t n
     L1(k_plan, plan_grid, 1024, a);
     L1(k_shared_check, jgrid, kThreads, a, idx, count, (uint64_t)max_count);
     if (hp.clip_on) {
-        L1(k_clip_tiles, (unsigned)L.max_clip_tiles, kThreads, a);
+        L1(k_clip_tiles, (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(L.max_clip_tiles,
+                                                                            (uint64_t)sms * 4)),
+           kThreads, a);
+        L1(k_clip_round, (unsigned)((nseg + 127) / 128), 128, a);
     }
     const cudaEvent_t pb = g_prof_begin, pe = g_prof_end;
     if (pb && pe) record_marker(pb, s);
