@@ -502,12 +502,14 @@ __device__ double limbs_round(const unsigned long long* x) {
 }
 
 // 4096-entry tiles of one segment each, the blocks looping over them. For a tile the block finds
-// the largest exponent e_max of its entries; each thread adds the squares of its 16 entries into
-// a 128-bit window whose lowest bit is bit lo = max(2 e_max - 68, 0) of X (a square there is
-// below 2^114, 4096 of them below 2^126). Squares that start below lo (entries more than 33
-// binades under the tile's largest) go to digit words in shared memory instead. The window's
-// block total, and the shared words when used (their carries propagated first, so each adds
-// less than 2^32 per word), then enter the segment's words in global memory.
+// the largest exponent e_max of its entries; the block sums into a 128-bit window whose lowest
+// bit is bit lo = max(2 e_max - 68, 0) of X. Each thread first sums its 16 squares in two 64-bit
+// bands below its own largest entry (a shift of at most 12 bits and one 64-bit add per entry),
+// then places the two band sums in the window (each below 2^118 there, 512 of them below
+// 2^127). What starts below lo, or lies more than 13 binades under the thread's largest entry,
+// goes to digit words in shared memory instead. The window's block total, and the shared words
+// when used (their carries propagated first, so each adds less than 2^32 per word), then enter
+// the segment's words in global memory.
 __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
     __shared__ unsigned long long s_low[kSqDigits];
     __shared__ unsigned long long s_w[kThreads / 32][2];
@@ -541,13 +543,14 @@ __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
                 xb[i] = (e < d.end) ? (__float_as_uint(a.g[e]) & 0x7FFFFFFFu) : 0u;
             }
         }
-        uint32_t em = 1;
+        uint32_t et = 1, nonfinite = 0;  // the thread's largest finite e', and any inf/NaN
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const uint32_t e = xb[i] >> 23;
-            if (e != 0xFFu) em = max(em, e);
+            nonfinite |= (e == 0xFFu);
+            if (e != 0xFFu) et = max(et, e);
         }
-        em = __reduce_max_sync(0xFFFFFFFFu, em);
+        uint32_t em = __reduce_max_sync(0xFFFFFFFFu, et);
         if (lane == 0) s_emax[warp] = em;
         __syncthreads();  // (also orders the previous tile's use of s_w, s_low, s_flags)
 #pragma unroll
@@ -555,27 +558,63 @@ __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
         const int lo = max(2 * (int)em - 68, 0);
         unsigned long long w0 = 0ull, w1 = 0ull;
         uint32_t fl = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t ax = xb[i];
-            const uint32_t e = ax >> 23;
-            if (e == 0xFFu) {
-                fl |= (ax & 0x7FFFFFu) ? 4u : 2u;
-                continue;
-            }
-            const uint32_t m = e ? ((ax & 0x7FFFFFu) | 0x800000u) : ax;
-            const unsigned long long M = (unsigned long long)m * m;
-            const int at = 2 * (int)max(e, 1u) - 2;
-            const int r = at - lo;  // at most 66
+        // v 2^bit into the window when bit >= lo, else into the shared words. In the window v 2^r
+        // stays below 2^118: a band sum (v < 2^64) has r <= 54, a single square (v < 2^48)
+        // r <= 66.
+        auto place = [&](unsigned long long v, int bit) {
+            if (v == 0ull) return;
+            const int r = bit - lo;
             if (r >= 0) {
-                const unsigned long long p0 = (r < 64) ? (M << r) : 0ull;
+                const unsigned long long p0 = (r < 64) ? (v << r) : 0ull;
                 const unsigned long long p1 =
-                    (r == 0) ? 0ull : (r < 64) ? (M >> (64 - r)) : (M << (r - 64));
+                    (r == 0) ? 0ull : (r < 64) ? (v >> (64 - r)) : (v << (r - 64));
                 w0 += p0;
                 w1 += p1 + (w0 < p0 ? 1ull : 0ull);
-            } else if (M != 0ull) {
+            } else {
                 fl |= 1u;
-                digits_add(s_low, at >> 5, at & 31, M);
+                digits_add(s_low, bit >> 5, bit & 31, v);
+            }
+        };
+        if (!nonfinite) {
+            // Two bands of 7 binades below the thread's largest entry, each summed in 64 bits:
+            // e' in [ea, ea + 6] as M 2^(2(e' - ea)) (below 2^60, 16 of them below 2^64), e' in
+            // [eb, ea - 1] likewise from eb; smaller entries go to the shared words one by one.
+            const uint32_t ea = max(et, 7u) - 6u;
+            const uint32_t eb = max(ea, 8u) - 7u;
+            unsigned long long A1 = 0ull, A2 = 0ull;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t ax = xb[i];
+                const uint32_t e = ax >> 23;
+                const uint32_t m = e ? ((ax & 0x7FFFFFu) | 0x800000u) : ax;
+                const uint32_t ep = max(e, 1u);
+                const unsigned long long M = (unsigned long long)m * m;
+                const bool in1 = ep >= ea, in2 = ep >= eb;
+                const uint32_t sft = in2 ? 2u * (ep - (in1 ? ea : eb)) : 0u;
+                const unsigned long long V = M << sft;
+                if (in1) {
+                    A1 += V;
+                } else if (in2) {
+                    A2 += V;
+                } else if (M != 0ull) {
+                    fl |= 1u;
+                    const int at = 2 * (int)ep - 2;
+                    digits_add(s_low, at >> 5, at & 31, M);
+                }
+            }
+            place(A1, 2 * (int)ea - 2);
+            place(A2, 2 * (int)eb - 2);
+        } else {  // a thread holding inf or NaN: entry by entry
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t ax = xb[i];
+                const uint32_t e = ax >> 23;
+                if (e == 0xFFu) {
+                    fl |= (ax & 0x7FFFFFu) ? 4u : 2u;
+                    continue;
+                }
+                const uint32_t m = e ? ((ax & 0x7FFFFFu) | 0x800000u) : ax;
+                place((unsigned long long)m * m, 2 * (int)max(e, 1u) - 2);
             }
         }
         if (fl) atomicOr(&s_flags, fl);
