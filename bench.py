@@ -517,7 +517,8 @@ def run_ours(args, world, rank, local):
                 sum(a.elapsed_time(b) for a, b in kev) / K)
     segst = np.frombuffer(pipe.stats.cpu().numpy().tobytes(), dtype=[
         ("k", "<u8"), ("candidates", "<u8"), ("sent", "<u8"), ("thresh_key", "<u4"),
-        ("sample_key", "<u4"), ("reselected", "<u4"), ("clip_scale", "<f4")])
+        ("sample_key", "<u4"), ("reselected", "<u4"), ("clip_scale", "<f4"),
+        ("clip_sumsq", "<f8")])
     st = {f: int(segst[f].sum()) for f in ("k", "candidates", "sent")}  # over the segments
     cand = int(st["candidates"])
     # read g, u, v and write u, v; one 4-byte slot per candidate and one count per 2048-entry tile

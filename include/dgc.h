@@ -95,6 +95,10 @@ typedef struct {
     uint32_t sample_key; /* sampled: the threshold key t; exact: 0 */
     uint32_t reselected; /* sampled: 1 if the exact re-selection ran */
     float clip_scale;    /* factor applied to g (1 when not clipped) */
+    double clip_sumsq;   /* with clipping on: S, the squared L2 norm of the segment's g -- the
+                            exact sum of the squares rounded once to binary64, ties to even
+                            (NaN if an entry is NaN, else +inf if one is infinite); 0 with
+                            clipping off */
 } dgc_seg_stats;
 
 /* ------------------------------------------------------------------------- compressor */

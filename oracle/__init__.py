@@ -50,6 +50,7 @@ class SegStats(ctypes.Structure):
         ("sample_key", ctypes.c_uint32),
         ("reselected", ctypes.c_uint32),
         ("clip_scale", ctypes.c_float),
+        ("clip_sumsq", ctypes.c_double),
     ]
 
 
@@ -226,7 +227,8 @@ def compress(g, u, v, seg_off, params: Params):
     c = cnt.value
     st = [dict(k=s.k, candidates=s.candidates, sent=s.sent, thresh_key=s.thresh_key,
                sample_key=s.sample_key, reselected=s.reselected,
-               clip_scale=np.float32(s.clip_scale)) for s in stats]
+               clip_scale=np.float32(s.clip_scale), clip_sumsq=float(s.clip_sumsq))
+          for s in stats]
     return out_idx[:c].copy(), out_val[:c].copy(), st
 
 

@@ -289,6 +289,7 @@ int orc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* s
         int clipped = 0;
         const float scale = orc_clip_scale(g + a, ns, p->clip_norm, &clipped);
         st.clip_scale = scale;
+        if (p->clip_norm > 0.0f && !isinf(p->clip_norm)) st.clip_sumsq = orc_sumsq(g + a, ns);
 
         const float leak = p->leak == 0.0f ? 1.0f : p->leak;
         for (int64_t i = a; i < b; ++i)

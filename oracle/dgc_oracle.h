@@ -46,6 +46,7 @@ typedef struct {
     uint32_t sample_key; /* sampled: the sampled threshold t; exact: 0 */
     uint32_t reselected; /* sampled: 1 if the exact re-selection ran */
     float clip_scale;    /* factor applied to g (1 when not clipped) */
+    double clip_sumsq;   /* with clipping on: S = orc_sumsq of the segment's g; else 0 */
 } orc_seg_stats;
 
 /* building blocks, exported so the tests can pin each one on its own */

@@ -56,6 +56,7 @@ class dgc_seg_stats(ctypes.Structure):
         ("sample_key", ctypes.c_uint32),
         ("reselected", ctypes.c_uint32),
         ("clip_scale", ctypes.c_float),
+        ("clip_sumsq", ctypes.c_double),
     ]
 
 

@@ -130,6 +130,7 @@ struct SegInfo {
     uint32_t bbase;     // first position bucket of the segment
     uint32_t binbase;   // AdaComp: first bin of the segment
     uint32_t nsent;     // AdaComp: entries sent
+    double sumsq;       // clipping: S, the squared norm (0 without clipping)
 };
 
 struct Ctl {
@@ -681,6 +682,7 @@ __global__ void __launch_bounds__(128) k_clip_round(Args a) {
     const double norm = sqrt(S);
     const double cn = (double)a.hp.clip_norm;
     a.segs[s].scale = (norm > cn) ? (float)(cn / norm) : 1.0f;
+    a.segs[s].sumsq = S;
 }
 
 // v <- fma(leak, v, u): with leak = 1 this is the plain sum v + u, rounded once
@@ -2113,6 +2115,7 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
         o.sample_key = (a.hp.mode == DGC_SELECT_SAMPLED && d.k > 0) ? d.thresh : 0u;
         o.reselected = d.resel;
         o.clip_scale = d.scale;
+        o.clip_sumsq = d.sumsq;
         a.stats[s] = o;
     }
 }

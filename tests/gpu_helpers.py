@@ -8,7 +8,7 @@ import sparsified_gradient_compression_gb300 as dgc
 
 STATS_DTYPE = np.dtype([("k", "<u8"), ("candidates", "<u8"), ("sent", "<u8"),
                         ("thresh_key", "<u4"), ("sample_key", "<u4"), ("reselected", "<u4"),
-                        ("clip_scale", "<f4")])
+                        ("clip_scale", "<f4"), ("clip_sumsq", "<f8")])
 assert STATS_DTYPE.itemsize == dgc.STATS_BYTES
 
 

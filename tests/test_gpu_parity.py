@@ -6,6 +6,8 @@ in the same order as the oracle (fma for u, one rounding per add, the fixed clip
 u, v, the sent values and the decoded sums are compared bitwise -- tighter than the 1e-6 /
 1-ulp / 1e-5 tolerances the workloads allow.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -78,6 +80,9 @@ def run_steps(grads, seg_off, steps, check_state=True, u0=None, v0=None, **kw):
             assert got["sample_key"] == o["sample_key"], (t, s)
             assert got["reselected"] == o["reselected"], (t, s)
             assert bits(np.float32(got["clip_scale"])) == bits(o["clip_scale"]), (t, s)
+            # the squared norm itself, bitwise (the binary32 scale hides most ulps of S)
+            gs, os_ = float(got["clip_sumsq"]), o["clip_sumsq"]
+            assert (gs == os_ or (math.isnan(gs) and math.isnan(os_))), (t, s, gs, os_)
         outs.append((idx, val))
     return outs, u_d, v_d
 

@@ -326,6 +326,22 @@ def test_sumsq_exact_on_integers(orc):
     assert orc.sumsq(g) == sum(int(x) ** 2 for x in range(-2000, 2001))
 
 
+def test_compress_reports_the_squared_norm(orc):
+    # the per-segment stat is S itself (math.fsum of the exact binary64 squares), 0 when
+    # clipping is off
+    rng = np.random.default_rng(23)
+    n = 9000
+    off = np.array([0, 0, 4097, 5000, n])
+    g = (rng.standard_normal(n) * 2.0 ** rng.integers(-20, 20, n)).astype(np.float32)
+    for c in (0.0, 1.0):
+        u = np.zeros(n, np.float32)
+        v = np.zeros(n, np.float32)
+        _, _, st = orc.compress(g, u, v, off, orc.make_params(orc.EXACT, 0.99, 0.9, clip_norm=c))
+        for s, (a, b) in enumerate(zip(off[:-1], off[1:])):
+            want = math.fsum(float(x) * float(x) for x in g[a:b]) if c else 0.0
+            assert st[s]["clip_sumsq"] == want
+
+
 def test_clip_within_bound_is_bitwise_noop(orc):
     rng = np.random.default_rng(21)
     n = 9000
