@@ -115,8 +115,9 @@ int dgc_compress_max_out(int64_t n, int32_t nseg, const dgc_params* params, int6
  * its own. [DGC] Proposed method, bullets 1 and 3-5; [DGC] RQ4; [ADA] abstract.
  *   1. k_s = ceil(n_s * (1 - sparsity)) per segment (integer arithmetic in parts per billion).
  *   2. If 0 < clip_norm < inf: scale_s = clip_norm / ||g_s|| when ||g_s|| > clip_norm (the
- *      squared norm summed in binary64 in a fixed order: 4096-entry tiles from the segment
- *      start, each summed in halves recursively, tile sums added left to right).
+ *      squared norm S is the exact sum of the squares rounded once to binary64, ties to even:
+ *      no order of summation shows; sqrt and the division correctly rounded in binary64, the
+ *      quotient rounded once to binary32).
  *   3. u <- fma(m, u, g * scale); v <- v + u (binary32, round to nearest).
  *   4. S = the k_s largest |v| (ties to the lower index) in exact mode; in sampled mode
  *      t = the k_s'-th largest |v| among m_s = ceil(n_s * sample_ratio) positions drawn with
