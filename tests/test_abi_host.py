@@ -187,3 +187,38 @@ def test_quant_entry_points_reject_on_host(L):
 def test_l2_fetch_granularity_rejects_out_of_range(L):
     assert L.dgc_set_l2_fetch_granularity(-1) == dgc.EINVAL
     assert L.dgc_set_l2_fetch_granularity(129) == dgc.EINVAL
+
+
+def _oracle_struct(name):
+    import oracle
+    return getattr(oracle, name)
+
+
+@pytest.mark.parametrize("cname,py,header", [
+    ("dgc_params", lambda: dgc.dgc_params, "include/dgc.h"),
+    ("dgc_seg_stats", lambda: dgc.dgc_seg_stats, "include/dgc.h"),
+    ("orc_params", lambda: _oracle_struct("Params"), "oracle/dgc_oracle.h"),
+    ("orc_seg_stats", lambda: _oracle_struct("SegStats"), "oracle/dgc_oracle.h")])
+def test_binding_structs_match_the_header(tmp_path, cname, py, header):
+    # the C compiler's layout of the header's struct against the ctypes copy in the library's
+    # binding (and in the oracle's test wrapper): the same size and every field at the same offset
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    py = py()
+    inc, hname = os.path.split(os.path.join(ROOT, header))
+    names = [f[0] for f in py._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text(
+        f'#include <stdio.h>\n#include <stddef.h>\n#include "{hname}"\nint main(void) {{\n'
+        f'    printf("%zu\\n", sizeof({cname}));\n'
+        + "".join(f'    printf("%zu\\n", offsetof({cname}, {n}));\n' for n in names)
+        + "    return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", inc, str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(py)
+    assert got[1:] == [getattr(py, n).offset for n in names]
