@@ -1,0 +1,161 @@
+"""A host model of the GPU clipping sum's integer steps (CPU only).
+
+The kernels `k_clip_tiles` and `k_clip_round` sum the squares of a segment exactly. Per
+4096-entry tile, each of 256 threads holds 16 entries and sums their squares in two 64-bit
+bands below its own largest entry. The block adds the band sums into a 128-bit window anchored
+68 bits below the tile's largest square. Anything lower goes to 32-bit digits held in 64-bit
+words, first per block, then per segment. One thread per segment then propagates the carries
+and rounds once to binary64.
+
+This model takes the same steps with Python integers and asserts the bounds the kernels rely
+on: a band sum below 2^64, a window term below 2^118 and the window below 2^127, and a word
+below 2^55. Its S must equal the oracle's, the exact sum rounded once (the DGC review's local
+gradient clipping; the pages fix no order of summation). It checks the scheme; the GPU parity
+tests check the kernels themselves against the oracle, S included.
+"""
+import math
+import struct
+
+import numpy as np
+import pytest
+
+TILE, THREADS, PER = 4096, 256, 16
+DIGITS = 20  # 32-bit digits of X = sum M 2^(2e'-2) < 2^586
+
+
+def _digits_add(words, i, sh, x):
+    """words[i..i+2] += x 2^(32 i + sh) in three pieces below 2^32, 2^33 and 2^31."""
+    assert 0 <= x < 2**64 and 0 <= sh < 32
+    lo, hi = (x & 0xFFFFFFFF) << sh, (x >> 32) << sh
+    words[i] += lo & 0xFFFFFFFF
+    words[i + 1] += (lo >> 32) + (hi & 0xFFFFFFFF)
+    words[i + 2] += hi >> 32
+
+
+def _tile(seg_words, bits):
+    """One block's work on one tile (|x| bits, zero-padded to 4096); returns its inf/NaN flags."""
+    bits = list(bits) + [0] * (TILE - len(bits))
+    threads = [bits[PER * t:PER * t + PER] for t in range(THREADS)]
+    et = [max([1] + [a >> 23 for a in th if (a >> 23) != 255]) for th in threads]
+    em = max(et)
+    lo = max(2 * em - 68, 0)  # the window's lowest bit of X
+    low = [0] * DIGITS
+    window, flags = 0, 0
+
+    def place(v, bit):
+        nonlocal window, flags
+        if v == 0:
+            return
+        if bit >= lo:
+            assert v << (bit - lo) < 2**118
+            window += v << (bit - lo)
+        else:
+            flags |= 1
+            _digits_add(low, bit >> 5, bit & 31, v)
+
+    for t, th in enumerate(threads):
+        if any((a >> 23) == 255 for a in th):  # a thread holding inf or NaN: entry by entry
+            for a in th:
+                e = a >> 23
+                if e == 255:
+                    flags |= 4 if a & 0x7FFFFF else 2
+                    continue
+                m = (a & 0x7FFFFF) | 0x800000 if e else a
+                place(m * m, 2 * max(e, 1) - 2)
+            continue
+        ea = max(et[t], 7) - 6  # band 1: e' in [ea, ea + 6]
+        eb = max(ea, 8) - 7     # band 2: e' in [eb, ea - 1]
+        A1 = A2 = 0
+        for a in th:
+            e = a >> 23
+            m = (a & 0x7FFFFF) | 0x800000 if e else a
+            ep, M = max(e, 1), m * m
+            if ep >= ea:
+                A1 += M << (2 * (ep - ea))
+            elif ep >= eb:
+                A2 += M << (2 * (ep - eb))
+            elif M:
+                flags |= 1
+                _digits_add(low, (2 * ep - 2) >> 5, (2 * ep - 2) & 31, M)
+        assert A1 < 2**64 and A2 < 2**64
+        place(A1, 2 * ea - 2)
+        place(A2, 2 * eb - 2)
+    assert window < 2**127
+    _digits_add(seg_words, lo >> 5, lo & 31, window & (2**64 - 1))
+    _digits_add(seg_words, (lo >> 5) + 2, lo & 31, window >> 64)
+    if flags & 1:  # the block's low words, carries propagated first
+        carry = 0
+        for j in range(DIGITS):
+            s = low[j] + carry
+            seg_words[j] += s & 0xFFFFFFFF
+            carry = s >> 32
+        assert carry == 0
+    return flags & 6
+
+
+def _round(words):
+    """Carries into 32-bit digits, then X 2^-298 rounded once to binary64 (ties to even)."""
+    X, carry = 0, 0
+    for j in range(DIGITS):
+        s = words[j] + carry
+        X |= (s & 0xFFFFFFFF) << (32 * j)
+        carry = s >> 32
+    assert carry == 0 and X < 2**586
+    if X == 0:
+        return 0.0
+    t = X.bit_length() - 1
+    if t <= 52:
+        mant, low = X, 0
+    else:
+        low = t - 52
+        mant, rest = X >> low, X & ((1 << low) - 1)
+        half = 1 << (low - 1)
+        if rest > half or (rest == half and mant & 1):
+            mant += 1
+            if mant == 1 << 53:
+                mant, low = mant >> 1, low + 1
+    return math.ldexp(mant, low - 298)
+
+
+def model_sumsq(g):
+    bits = (np.asarray(g, np.float32).view(np.uint32) & 0x7FFFFFFF).tolist()
+    words, flags = [0] * DIGITS, 0
+    for t0 in range(0, len(bits), TILE):
+        flags |= _tile(words, bits[t0:t0 + TILE])
+    assert max(words) < 2**55
+    if flags & 4:
+        return math.nan
+    if flags & 2:
+        return math.inf
+    return _round(words)
+
+
+def _cases():
+    rng = np.random.default_rng(31)
+    out = []
+    for n in (1, 17, 4096, 5000):
+        out.append(("normal", (rng.standard_normal(n) * 1e-3).astype(np.float32)))
+        out.append(("60 binades", (rng.standard_normal(n) * 2.0 ** rng.integers(-30, 30, n))
+                    .astype(np.float32)))
+        bits = rng.integers(0, 0x7F7FFFFF, n, endpoint=True).astype(np.uint32)
+        out.append(("every exponent", bits.view(np.float32)))
+        c = rng.standard_normal(n).astype(np.float32)
+        c[::7] = np.float32(1e-44)
+        out.append(("subnormals among normals", c))
+        out.append(("largest binary32", np.full(n, np.finfo(np.float32).max, np.float32)))
+        out.append(("least subnormal", np.full(n, np.float32(2.0**-149))))
+        c = rng.standard_normal(n).astype(np.float32)
+        c[::5] = np.inf
+        c[1::9] = np.nan
+        out.append(("inf and NaN", c))
+        c = rng.standard_normal(n).astype(np.float32)
+        c[::3] = -np.inf
+        out.append(("inf", c))
+    return out
+
+
+@pytest.mark.parametrize("name,g", _cases(), ids=lambda x: x if isinstance(x, str) else "")
+def test_kernel_scheme_reaches_the_oracle(orc, name, g):
+    want, got = orc.sumsq(g), model_sumsq(g)
+    assert (math.isnan(want) and math.isnan(got)) or \
+        struct.pack("<d", want) == struct.pack("<d", got), (name, want, got)
