@@ -652,6 +652,31 @@ def run_e2e(args, pipe, pool, p, K_dev):
 
 
 # ------------------------------------------------------------------ CPU baseline / reference
+def host_cpu() -> dict:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo) and the cores it reports."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu model")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    import platform
+
+    return {"cpu_model": model or platform.processor() or platform.machine(),
+            "nproc": os.cpu_count()}
+
+
 def run_cpu_baseline(n_cpu: int, steps: int, select: str = "sampled", bin_size: int = 1000):
     """The oracle, single-threaded on one host core, on a bounded sample of the workload:
     an n_cpu-entry bucket with the same recipe (one untimed step, then `steps` timed steps of
@@ -676,7 +701,7 @@ def run_cpu_baseline(n_cpu: int, steps: int, select: str = "sampled", bin_size: 
         oracle.decode_accumulate([m], n_cpu)
     sec = time.perf_counter() - t0
     return {"value": round(4.0 * n_cpu * steps / sec / 1e9, 4), "unit": UNIT, "cores": 1,
-            "kind": "oracle", "seconds": round(sec, 2),
+            "kind": "oracle", "seconds": round(sec, 2), **host_cpu(),
             "sample": f"{n_cpu}-entry bucket of the same recipe, {steps} timed steps of "
                       "compress+encode+decode at 99.9% after one untimed step"}
 

@@ -161,7 +161,10 @@ int dgc_compress(const float* g, float* u, float* v, int64_t n, const int64_t* s
  * anything is enqueued; use dgc_compress with your own workspace instead.
  * The first call on each device looks the scratch address up with cudaGetSymbolAddress (which
  * may load the library's device code on that device); make that first call before any stream
- * capture. All later calls on the device reuse the same array; each call re-initialises every
+ * capture. The address is kept with the identity of the CUDA context it was found in: after a
+ * device reset (or a primary context released and created again) the next call finds a new
+ * context and looks the address up again, so make that call outside stream capture too.
+ * All later calls on the device reuse the same array; each call re-initialises every
  * part of it that it reads. Calls whose GPU work can overlap (streams without ordering between
  * them, several host threads) race on the shared array: the caller must serialize them. */
 int dgc_compress_noalloc(const float* g, float* u, float* v, int64_t n, const int64_t* seg_off,

@@ -84,8 +84,9 @@ constexpr int kPRows = kPTile / (4 * kThreads);   // float4 rows per thread
 constexpr int kWarps = kThreads / 32;
 static_assert(kPRows >= 1 && kPRows * 4 * kThreads == kPTile, "tile = rows x 1024 entries");
 static_assert(kPRows * kWarps <= 32, "one warp scans the per-(row, warp) counts");
-// the AdaComp pass finds bins with (x + 0.5) * fl(1/L) for x < 2 * kPTile, L < kPTile: checked
-// exhaustively against integer division for tiles of 2048 and 4096
+// the AdaComp pass finds bins with (x + 0.5) * fl(1/L) for x < L + kPTile, L < kPTile: equal to
+// x / L for every L in [4, 4095] and x < L + 4096, checked exhaustively in binary32 on the host
+// by tests/test_adacomp_bin_index_host.py
 static_assert(kPTile <= 4096, "bin index by reciprocal is only checked up to 4096-entry tiles");
 constexpr uint32_t kPStageFloats = 3u * kPTile;   // g, u, v
 template <int kSel>
@@ -450,9 +451,12 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
 // x = m 2^(e'-150) (m the 24-bit significand, e' = max(biased exponent, 1)) has the exact
 // square M 2^(2e'-300), M = m^2 < 2^48; the segment keeps X = sum M 2^(2e'-2) (2e'-2 <= 506, at
 // most 2^32 entries: X < 2^586) and S = X 2^-298. X lives in kSqDigits 64-bit words, word i
-// worth 2^(32 i): every addition puts less than 2^32 into a word, so the words take plain
-// atomic adds that nobody waits for, in any order, and never overflow (at most 2^21 additions
-// per word); the carries are propagated once, by k_clip_round.
+// worth 2^(32 i), which take plain atomic adds that nobody waits for, in any order. Every such
+// add is below 2^33 (digits_add's middle piece holds two digits' worth), a tile adds to one
+// word at most three times (the window's two halves overlap in one word, and the shared low
+// words add once more), and a segment has fewer than 2^20 tiles, so every word stays below
+// 2^55 and never overflows; the carries are propagated once, by k_clip_round. A host model of
+// these integer steps, with the bounds asserted, is in tests/test_clip_scheme_host.py.
 
 // words[i..] += x 2^(32 i + sh) for x < 2^64, sh < 32: three 32-bit pieces
 __device__ __forceinline__ void digits_add(unsigned long long* words, int i, int sh,

@@ -12,11 +12,16 @@
 //
 // In host code the array's name is only a stand-in, not a device address, so the address is
 // looked up with cudaGetSymbolAddress once per device (on the first call with that device
-// current) and cached. Each call then runs the ordinary dgc_compress pipeline on that scratch;
+// current) and cached together with the identity of the CUDA context it belongs to. A device
+// reset, or a primary context torn down and created again, loads the device code anew and may
+// place the array elsewhere; the next call sees a different context and looks the address up
+// again. Each call then runs the ordinary dgc_compress pipeline on that scratch;
 // the pipeline's first kernel clears every counter, histogram and look-back word it later reads,
 // so the previous call's leftovers do not matter. All calls on a device share the one array:
 // calls whose GPU work can overlap (different streams without ordering, several host threads)
 // race on it and must be serialized by the caller.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "dgc_device.cuh"
@@ -28,24 +33,71 @@ constexpr int kMaxDevices = 128;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_scratch_mutex;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+// The driver calls that name the current context, fetched through the runtime so that the
+// library does not link the driver library itself.
+typedef CUresult (*ctx_get_current_fn)(CUcontext*);
+typedef CUresult (*ctx_get_id_fn)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device (looked up once per device).
+struct ScratchSlot {
+    void* addr = nullptr;
+    unsigned long long ctx_id = 0;  // the context the address was looked up in
+    bool have_id = false;
+};
+
+std::mutex g_scratch_mutex;
+ScratchSlot g_scratch[kMaxDevices];
+bool g_driver_looked_up = false;
+ctx_get_current_fn g_ctx_get_current = nullptr;
+ctx_get_id_fn g_ctx_get_id = nullptr;
+
+// The unique id of the current context (unique for the process's lifetime, unlike the handle,
+// which a new context may reuse); false when it cannot be had.
+bool current_context_id(unsigned long long* id) {
+    if (!g_driver_looked_up) {
+        g_driver_looked_up = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<ctx_get_current_fn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<ctx_get_id_fn>(f);
+        cudaGetLastError();
+    }
+    if (!g_ctx_get_current || !g_ctx_get_id) return false;
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current context: looked up once per device and
+// context. Without a context id (no current context yet, or a driver without the call) the
+// address is looked up on every call instead, which is correct, only slower.
 int scratch_address(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return DGC_ECUDA;
     if (dev < 0 || dev >= kMaxDevices) return DGC_EUNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-            cudaGetLastError();
-            return DGC_ECUDA;
-        }
-        g_scratch_addr[dev] = p;
+    ScratchSlot& slot = g_scratch[dev];
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
+    if (slot.addr && have_id && slot.have_id && slot.ctx_id == id) {
+        *out = slot.addr;
+        return DGC_OK;
     }
-    *out = g_scratch_addr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        slot = ScratchSlot();
+        return DGC_ECUDA;
+    }
+    // the lookup made the primary context current if none was: name it now
+    slot.addr = p;
+    slot.have_id = have_id || current_context_id(&id);
+    slot.ctx_id = id;
+    *out = p;
     return DGC_OK;
 }
 

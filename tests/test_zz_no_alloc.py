@@ -61,6 +61,69 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(mode):
         assert torch.equal(v_a.view(torch.int32), v_b.view(torch.int32))
 
 
+class _Problem:
+    """One compressor problem run twice side by side: through dgc_compress_noalloc (the shared
+    scratch) and through dgc_compress on a workspace of its own, allocated fresh for each call."""
+
+    def __init__(self, n, off, params, gen):
+        self.n, self.params, self.gen = n, params, gen
+        self.off = torch.tensor(off, dtype=torch.int64, device="cuda")
+        self.nseg = len(off) - 1
+        self.cap = dgc.dgc_compress_max_out(n, self.nseg, params)
+        self.ws_bytes = dgc.dgc_compress_workspace(n, self.nseg, params)
+        self.u_a, self.v_a = _state(n)
+        self.u_b, self.v_b = _state(n)
+        self.step = 0
+
+    def run_and_compare(self):
+        g = self.gen(self.step)
+        self.step += 1
+        oa, ob = _outputs(self.cap, self.nseg), _outputs(self.cap, self.nseg)
+        ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        dgc.dgc_compress(g, self.u_a, self.v_a, self.off, self.params, oa[0], oa[1], oa[2],
+                         oa[3], oa[4], ws)
+        dgc.dgc_compress_noalloc(g, self.u_b, self.v_b, self.off, self.params, ob[0], ob[1],
+                                 ob[2], ob[3], ob[4])
+        assert dgc.dgc_read_status(oa[4]) == 0
+        assert dgc.dgc_read_status(ob[4]) == 0
+        ca, cb = int(oa[2].item()), int(ob[2].item())
+        assert ca == cb and ca > 0
+        assert torch.equal(oa[0][:ca], ob[0][:cb])
+        assert torch.equal(oa[1][:ca].view(torch.int32), ob[1][:cb].view(torch.int32))
+        assert torch.equal(oa[3], ob[3])
+        assert torch.equal(self.u_a.view(torch.int32), self.u_b.view(torch.int32))
+        assert torch.equal(self.v_a.view(torch.int32), self.v_b.view(torch.int32))
+
+
+def test_noalloc_different_problems_in_turn_share_the_scratch_safely():
+    # Problems that leave different things in the shared array for each other: a sampled call
+    # (sample-position cache filled for its seed and layout), an exact call with clipping on
+    # another segment layout (which moves where the cache sits in the scratch), an AdaComp call
+    # (bin maxima), then the first problem again, whose cached positions must be rebuilt or
+    # recognised, never reused stale. Each call is compared bitwise with dgc_compress on a
+    # workspace of its own.
+    dgc.build()
+    n_a = 1_048_576
+
+    def grad_a(t):
+        return torch.from_numpy(workloads.gradient("single", t)).cuda()
+
+    a = _Problem(n_a, [0, 600_000, n_a],
+                 dgc.make_params(mode=dgc.SELECT_SAMPLED, sparsity=0.999, momentum=0.9,
+                                 sample_ratio=0.01, seed=3), grad_a)
+    n_b = 900_001
+    b = _Problem(n_b, [0, 1, 70_000, 70_000, 400_003, n_b],
+                 dgc.make_params(mode=dgc.SELECT_EXACT, sparsity=0.99, momentum=0.9,
+                                 clip_norm=0.05),
+                 lambda t: torch.from_numpy(workloads.misc([71, t], n_b, 0.01)).cuda())
+    n_c = 1_000_003
+    c = _Problem(n_c, [0, 333_333, n_c],
+                 dgc.make_params(mode=dgc.SELECT_ADACOMP, momentum=0.9, bin_size=1000),
+                 lambda t: torch.from_numpy(workloads.misc([72, t], n_c, 0.01)).cuda())
+    for prob in (a, b, c, a, b, c, a):
+        prob.run_and_compare()
+
+
 def test_noalloc_rejects_problems_larger_than_its_scratch():
     n = 4_000_000  # needs ~32 MiB of scratch, more than the 16 MiB the library holds
     p = dgc.make_params()
