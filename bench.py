@@ -92,6 +92,10 @@ def parse_args(argv=None):
     ap.add_argument("--bin-size", type=int, default=1000)
     ap.add_argument("--no-graph", action="store_true",
                     help="launch compress and encode call by call instead of replaying graphs")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the single-tensor, ResNet-50, DeepSpeech and aggregation timings "
+                         "that follow the headline bucket")
+    ap.add_argument("--workload-steps", type=int, default=30)
     ap.add_argument("--l2-fetch", type=int, default=64,
                     help="this process's L2 fetch granularity limit in bytes (0: leave it)")
     return ap.parse_args(argv)
@@ -566,6 +570,9 @@ def run_ours(args, world, rank, local):
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None if traffic is None else round(traffic),
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one "
+                                       "67,108,864-entry launch, scaled to n (an extrapolation "
+                                       "from that capture, not a measurement at n)",
                      "alg_bytes": alg_bytes, "kernel_ms": round(t_kernel, 4)},
         "stages_ms": {"compress": round(t_compress, 4), "encode": round(t_encode, 4),
                       "decode": round(t_decode, 4)},
@@ -582,6 +589,16 @@ def run_ours(args, world, rank, local):
         "gpu_launches": int(launches), "clocks": clk,
         "e2e": e2e, "cpu_baseline": cpu,
     }
+    if wl == "bucket1g" and world == 1 and not args.no_workloads:
+        # the other workloads and the aggregation, each at its own settings, after the headline
+        # bucket's buffers are released
+        del graphs, pool, pipe
+        torch.cuda.empty_cache()
+        flush = L2Flush(dev)
+        out["workloads"] = {name: run_workload(name, dev, peak, args.workload_steps, flush=flush)
+                            for name in ("single", "resnet50", "deepspeech")}
+        out["aggregation"] = run_aggregation(dev, peak, flush=flush)
+        del flush
     if rank == 0:
         print(json.dumps(out), flush=True)
 
@@ -649,6 +666,186 @@ def run_e2e(args, pipe, pool, p, K_dev):
             "h2d_ms_each": copy_each,
             "note": "gradient copied from pinned host memory each step on a second stream, "
                     "overlapped with the previous step's kernels; message copied back"}
+
+
+# -------------------------------------------------------- the other workloads, aggregation
+L2_BYTES = 129 * 2**20
+
+
+class L2Flush:
+    """Writes a buffer twice the size of L2 so that the next timed call starts cold."""
+
+    def __init__(self, dev):
+        import torch
+
+        self.buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def median_ms(fn, reps, flush=None, warm=3):
+    """Median CUDA-event time of fn() over `reps` calls after `warm` untimed ones; flush() (if
+    given) runs before every call, outside the events."""
+    import torch
+
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ms = []
+    for i in range(warm + reps):
+        if flush:
+            flush()
+        a, b = E(), E()
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        if i >= warm:
+            ms.append(a.elapsed_time(b))
+    return statistics.median(ms)
+
+
+def run_workload(name, dev, peak, steps, warmup=3, flush=None):
+    """One of the other workloads at its own settings: `warmup` untimed steps, then `steps`
+    timed steps (compress and encode as CUDA graph replays, decode call by call), each step
+    timed on its own with CUDA events, L2 flushed before each step when its arrays fit in L2."""
+    import numpy as np
+    import torch
+
+    import sparsified_gradient_compression_gb300 as dgc
+    import workloads
+
+    seg = OTHER_WORKLOADS[name][0]()
+    n = int(seg[-1])
+    p = dgc.make_params(sparsity=0.999, momentum=0.9, seed=SEED, **OTHER_WORKLOADS[name][1])
+    pipe = Pipeline(n, [p], dev, seg)
+    pool = [torch.from_numpy(workloads.gradient(name, step=i, seed=0, n=n)).to(dev)
+            for i in range(2)]
+    for i in range(warmup):
+        pipe.step(pool[i % 2], p)
+    torch.cuda.synchronize()
+    if dgc.dgc_read_status(pipe.status) != 0:
+        raise RuntimeError(f"{name}: warm-up steps reported an error")
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    gkev = (E(), E())
+    dgc.dgc_profile_stream_pass(*gkev)
+    graphs = [pipe.capture(g, p) for g in pool]
+    dgc.dgc_profile_stream_pass(None, None)
+    torch.cuda.synchronize()
+    small = 12 * n < L2_BYTES  # g, u and v together fit in L2
+    step_ms, st_ms, kern_ms = [], [], []
+    for i in range(steps):
+        if small and flush:
+            flush()
+        ev = (E(), E(), E(), E())
+        j = (warmup + i) % 2
+        pipe.step(pool[j], p, ev, graphs[j])
+        torch.cuda.synchronize()
+        step_ms.append(ev[0].elapsed_time(ev[3]))
+        st_ms.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]),
+                      ev[2].elapsed_time(ev[3])))
+        kern_ms.append(gkev[0].elapsed_time(gkev[1]))
+    if dgc.dgc_read_status(pipe.status) != 0:
+        raise RuntimeError(f"{name}: timed steps reported an error")
+    segst = np.frombuffer(pipe.stats.cpu().numpy().tobytes(), dtype=[
+        ("k", "<u8"), ("candidates", "<u8"), ("sent", "<u8"), ("thresh_key", "<u4"),
+        ("sample_key", "<u4"), ("reselected", "<u4"), ("clip_scale", "<f4"),
+        ("clip_sumsq", "<f8")])
+    cand, sent = int(segst["candidates"].sum()), int(segst["sent"].sum())
+    t_step = statistics.median(step_ms)
+    t_comp = statistics.median(x[0] for x in st_ms)
+    t_kern = statistics.median(kern_ms)
+    clip = p.clip_norm > 0
+    pass_bytes = 20.0 * n + 4.0 * cand + 4.0 * ((n + 2047) // 2048)
+    comp_bytes = 20.12 * n + (4.0 * n if clip else 0.0) + 24.0 * sent
+    out = {"workload": OTHER_WORKLOADS[name][2], "n": n, "segments": int(seg.size - 1),
+           "steps": steps, "warmup": warmup, "ms_per_step": round(t_step, 4),
+           "value": round(4.0 * n / (t_step / 1e3) / 1e9, 2), "unit": UNIT,
+           "stages_ms": {"compress": round(t_comp, 4),
+                         "encode": round(statistics.median(x[1] for x in st_ms), 4),
+                         "decode": round(statistics.median(x[2] for x in st_ms), 4)},
+           "stream_pass": {"kernel_ms": round(t_kern, 4), "alg_bytes": pass_bytes,
+                           "frac": round(pass_bytes / (t_kern / 1e3) / 1e9 / peak, 4)},
+           "compress_gbs": round(4.0 * n / (t_comp / 1e3) / 1e9, 2),
+           "compress_roofline_frac": round(comp_bytes / (t_comp / 1e3) / 1e9 / peak, 4),
+           "compress_alg_bytes": comp_bytes, "candidates": cand, "sent": sent,
+           "message_bytes": int(pipe.msg_bytes.item()),
+           "l2": ("L2 flushed before every step (g, u, v fit in L2)" if small else
+                  f"g, u, v together {12 * n >> 20} MiB, larger than L2"),
+           "launch": "compress and encode as CUDA graph replays, decode call by call"}
+    del pipe, pool, graphs
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_aggregation(dev, peak, W=64, n=25_557_032, reps=20, flush=None):
+    """The aggregation workload: W learners each compress their own seeded gradient (momentum
+    0.9, exact top-k at 99.9%, first step from zero state) and encode it; the W messages are
+    then decoded and summed in learner order into one dense array (dgc_decode_accumulate), and
+    applied as one SGD step (dgc_decode_apply). Median CUDA-event times of those two calls, L2
+    flushed before each."""
+    import numpy as np
+    import torch
+
+    import sparsified_gradient_compression_gb300 as dgc
+    import workloads
+
+    off = np.array([0, n], np.int64)
+    p = dgc.make_params(mode=dgc.SELECT_EXACT, sparsity=0.999, momentum=0.9, seed=SEED)
+    pipe = Pipeline(n, [p], dev, off)
+    msgs, sizes = [], []
+    for w in range(W):
+        g = torch.from_numpy(workloads.gradient("learners", 0, learner=w, n=n)).to(dev)
+        pipe.u.zero_()
+        pipe.v.zero_()
+        pipe.compress(g, p)
+        pipe.encode()
+        nb = int(pipe.msg_bytes.item())
+        msgs.append(pipe.msg[:nb].clone())
+        sizes.append(nb)
+    if dgc.dgc_read_status(pipe.status) != 0:
+        raise RuntimeError("aggregation: learners reported an error")
+    del pipe, g
+    torch.cuda.empty_cache()
+    ws_bytes = dgc.dgc_decode_workspace(sizes, n)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    dense = torch.empty(n, dtype=torch.float32, device=dev)
+    w_vec = torch.zeros(n, dtype=torch.float32, device=dev)
+    l0 = dgc.dgc_launch_count()
+    t_dec = median_ms(lambda: dgc.dgc_decode_accumulate(msgs, sizes, dense, n, False, status, ws,
+                                                        ws_bytes=ws_bytes), reps, flush)
+    launches_dec = (dgc.dgc_launch_count() - l0) // (reps + 3)
+    t_app = median_ms(lambda: dgc.dgc_decode_apply(msgs, sizes, w_vec, n, 0.01 / W, status, ws,
+                                                   ws_bytes=ws_bytes), reps, flush)
+    if dgc.dgc_read_status(status) != 0:
+        raise RuntimeError("aggregation: decode reported an error")
+    tokens = sum((s - 32) // 6 for s in sizes)  # values + escapes (the pad is under 6 bytes)
+    touched = int((dense != 0).sum().item())  # positions some message reached (sum not 0)
+    msg_bytes = float(sum(sizes))
+    dec_bytes = msg_bytes + 4.0 * n + 8.0 * tokens
+    app_bytes = msg_bytes + 8.0 * tokens + 8.0 * touched
+    out = {"workload": f"{W} learners x {n:,} fp32 entries, N(0, 0.01^2) each; messages from "
+                       "dgc_compress (exact top-k, 99.9%, momentum 0.9, first step) + dgc_encode;"
+                       " decode and sum in learner order 0..W-1",
+           "learners": W, "n": n, "message_bytes_total": int(msg_bytes), "tokens": tokens,
+           "decode_ms": round(t_dec, 4), "decode_apply_ms": round(t_app, 4),
+           "value": round(4.0 * n / (t_dec / 1e3) / 1e9, 2),
+           "unit": "GB/s of dense fp32 gradient produced",
+           "decode_roofline": {"bound": "hbm", "alg_bytes": dec_bytes,
+                               "achieved": round(dec_bytes / (t_dec / 1e3) / 1e9, 1),
+                               "frac": round(dec_bytes / (t_dec / 1e3) / 1e9 / peak, 4),
+                               "bytes_rule": "messages read + 4 B per dense entry written + "
+                                             "8 B per token (position written and read)"},
+           "decode_apply_roofline": {"bound": "hbm", "alg_bytes": app_bytes,
+                                     "achieved": round(app_bytes / (t_app / 1e3) / 1e9, 1),
+                                     "frac": round(app_bytes / (t_app / 1e3) / 1e9 / peak, 4),
+                                     "bytes_rule": "messages read + 8 B per token + 8 B per "
+                                                   "touched weight (read and write)"},
+           "touched": touched, "launches_per_decode": launches_dec,
+           "l2": "L2 flushed before every call (the 102 MB dense array fits in L2)"}
+    del msgs, ws, dense, w_vec
+    torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------ CPU baseline / reference

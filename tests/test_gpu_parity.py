@@ -116,7 +116,8 @@ def test_resnet50_161_tensors_clip_exact_ten_steps():
 @pytest.mark.slow
 def test_deepspeech_sampled_six_segments():
     off = workloads.deepspeech_segments()
-    outs, _, _ = run_steps(lambda t: workloads.gradient("deepspeech", t), off, 4,
+    # the workload's 10 steps, every step's selection, values, u, v and statistics bitwise
+    outs, _, _ = run_steps(lambda t: workloads.gradient("deepspeech", t), off, 10,
                            mode=dgc.SELECT_SAMPLED, sparsity=0.999, momentum=0.9,
                            sample_ratio=0.01, reselect_factor=1.3, seed=1234)
     # the message size the DGC review prints for DeepSpeech: 0.74 MB
@@ -261,6 +262,80 @@ def test_aggregation_64_learners():
             rc, wq = decode_apply_quant(qmsgs, n, 16, 1e5, w0, 0.1 / W)
             orc_rc, owq = oracle.decode_apply_quant(qmsgs, n, 16, 1e5, w0, np.float32(0.1 / W))
             assert rc == 0 and orc_rc == 0 and same_bits(wq, owq)
+
+
+@pytest.mark.slow
+def test_aggregation_64_learners_end_to_end():
+    # The aggregation workload as its recipe states it, 5 steps: each of the 64 learners runs
+    # the compressor (momentum 0.9, exact top-k at 99.9%, k = 25,558) and the encoder on its own
+    # seeded gradients; every step's 64 messages are decoded and summed in learner order
+    # (dgc_decode_accumulate) and applied as one SGD step (dgc_decode_apply). The oracle runs
+    # the same chain, its learners spread over a spawned process pool (its exact top-k sorts all
+    # 25.6M entries, ~5 s per learner and step on one core). Compared bitwise: every message,
+    # each learner's u and v after the last step (SHA-256 digests), every step's dense sum and
+    # updated weights.
+    import concurrent.futures as cf
+    import hashlib
+    import multiprocessing as mp
+    import os
+
+    import aggregation_oracle as agg
+
+    n, W, steps = agg.N_LEARNER, 64, 5
+    workers = max(1, min(16, os.cpu_count() or 1))
+    pool = cf.ProcessPoolExecutor(workers, mp_context=mp.get_context("spawn"))
+    try:
+        futs = [pool.submit(agg.learner_messages, w, steps, n) for w in range(W)]
+        off = np.array([0, n])
+        pd = dgc.make_params(mode=dgc.SELECT_EXACT, sparsity=0.999, momentum=0.9)
+        comp = Compressor(n, off, pd)
+        enc = Encoder(comp.cap, n)
+        gpu_msgs = [[None] * W for _ in range(steps)]  # device copies, [step][learner]
+        gpu_host = [[None] * W for _ in range(steps)]
+        digests = []
+        for w in range(W):
+            u_d = torch.zeros(n, dtype=torch.float32, device="cuda")
+            v_d = torch.zeros(n, dtype=torch.float32, device="cuda")
+            for t in range(steps):
+                comp(dev_f32(workloads.gradient("learners", t, learner=w, n=n)), u_d, v_d)
+                enc(comp.out_idx, comp.out_val, comp.out_count)
+                assert comp.status_code() == 0 and dgc.dgc_read_status(enc.status) == 0
+                nb = int(enc.out_bytes.item())
+                gpu_msgs[t][w] = enc.out[:nb].clone()
+                gpu_host[t][w] = gpu_msgs[t][w].cpu().numpy().tobytes()
+            digests.append((hashlib.sha256(host_f32(u_d).tobytes()).hexdigest(),
+                            hashlib.sha256(host_f32(v_d).tobytes()).hexdigest()))
+            del u_d, v_d
+        orc = [f.result() for f in futs]
+    finally:
+        pool.shutdown(cancel_futures=True)
+    for w in range(W):
+        omsgs, ou, ov = orc[w]
+        for t in range(steps):
+            assert gpu_host[t][w] == omsgs[t], f"learner {w}, step {t}: messages differ"
+        assert digests[w] == (ou, ov), f"learner {w}: u or v differs after {steps} steps"
+    ws_bytes = max(dgc.dgc_decode_workspace([len(m) for m in gpu_host[t]], n)
+                   for t in range(steps))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dense = torch.full((n,), float("nan"), dtype=torch.float32, device="cuda")
+    for t in range(steps):
+        sizes = [len(m) for m in gpu_host[t]]
+        dgc.dgc_decode_accumulate(gpu_msgs[t], sizes, dense, n, False, status, ws,
+                                  ws_bytes=ws_bytes)
+        assert dgc.dgc_read_status(status) == 0
+        orc_rc, odense = oracle.decode_accumulate([orc[w][0][t] for w in range(W)], n)
+        assert orc_rc == 0 and same_bits(host_f32(dense), odense), f"step {t}: dense sum"
+        w0 = np.random.Generator(np.random.PCG64([7, t])).standard_normal(n).astype(np.float32)
+        w_d = dev_f32(w0)
+        dgc.dgc_decode_apply(gpu_msgs[t], sizes, w_d, n, 0.1 / W, status, ws, ws_bytes=ws_bytes)
+        assert dgc.dgc_read_status(status) == 0
+        orc_rc, w_orc = oracle.decode_apply([orc[w][0][t] for w in range(W)], n, w0,
+                                            np.float32(0.1 / W))
+        assert orc_rc == 0 and same_bits(host_f32(w_d), w_orc), f"step {t}: SGD step"
+        del w_d
+    del comp, enc, gpu_msgs, dense, ws
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.slow
