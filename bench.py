@@ -85,8 +85,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--workload", choices=["bucket1g", "single", "resnet50", "deepspeech",
-                                           "learners"], default="bucket1g",
-                    help="bucket1g is the headline; the others time the other workloads' steps")
+                                           "learners", "aggregation"], default="bucket1g",
+                    help="bucket1g is the headline; the others time the other workloads' steps "
+                         "(aggregation: only the 64-learner decode and SGD step)")
     ap.add_argument("--select", choices=["sampled", "adacomp"], default="sampled",
                     help="DGC sampled threshold (the headline) or AdaComp bins of --bin-size")
     ap.add_argument("--bin-size", type=int, default=1000)
@@ -440,6 +441,12 @@ def run_ours(args, world, rank, local):
     if args.l2_fetch > 0:  # a context limit of this process (see dgc_set_l2_fetch_granularity)
         dgc.dgc_set_l2_fetch_granularity(args.l2_fetch)
     wl = args.workload
+    if wl == "aggregation":  # the 64-learner decode and SGD step alone
+        agg = run_aggregation(dev, measured_peak_hbm()[0], reps=args.steps, flush=L2Flush(dev))
+        if rank == 0:
+            print(json.dumps({"metric": "ms per 64-message decode", "aggregation": agg}),
+                  flush=True)
+        return
     mode = dgc.SELECT_ADACOMP if args.select == "adacomp" else dgc.SELECT_SAMPLED
     if wl == "bucket1g":  # the headline: one segment, the warm-up schedule, then 99.9%
         n, off = args.n, None

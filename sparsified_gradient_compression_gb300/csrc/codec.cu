@@ -359,12 +359,27 @@ __device__ __forceinline__ float dequant(int32_t S, float alpha) {
 
 // kInt: version-2 messages. Their integers are summed exactly (any order gives the same sum) and
 // turned into a value once per position; a flag per entry records whether any message landed.
+//
+// Binary32 sums keep the learners' order at every position. A message's positions are
+// distinct, so only tokens of different messages can meet at one position. The tile's tokens
+// are staged (message-major, up to kDecCap at a time) and added in rounds: each round, every
+// position still owed a value finds the smallest message index among its remaining tokens
+// (a shared atomicMin) and that token alone adds itself, then clears the position's minimum for
+// the next round. Positions that one message reaches finish in the first round; a round adds at
+// most one value per position, so the number of rounds is the most tokens that meet at one
+// position. Staged chunks follow each other in message order, so chunk boundaries keep the
+// order too.
+constexpr uint32_t kNoPos = 0xFFFFFFFFu;
 template <bool kInt>
 __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
+    constexpr int kPerThread = kDecCap / kThreads;  // staged tokens per thread
+    static_assert(kPerThread * kThreads == kDecCap && kPerThread <= 32, "staging layout");
     __shared__ __align__(16) uint32_t s_accw[kDecTile];  // binary32 sums, or int32 sums
     __shared__ uint8_t s_touch[kInt ? kDecTile : 1];
-    __shared__ uint32_t s_pos[kDecCap];
+    __shared__ __align__(16) uint32_t s_minw[kInt ? 1 : kDecTile];  // smallest message left
+    __shared__ uint32_t s_pos[kDecCap];  // tile-local position, or kNoPos
     __shared__ uint32_t s_val[kDecCap];
+    __shared__ uint32_t s_msg[kInt ? 1 : kDecCap];  // message index within the group
     __shared__ uint32_t s_off[kThreads + 1];
     __shared__ uint32_t s_first[kThreads];
     __shared__ uint64_t s_scan[33];
@@ -381,15 +396,19 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
             s_acci[i] = 0;
             s_touch[i] = 0;
         }
-    } else if (vec && load) {
-        for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
-            reinterpret_cast<float4*>(s_acc)[i] = reinterpret_cast<const float4*>(a.dense + p0)[i];
-    } else if (vec) {
-        for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
-            reinterpret_cast<float4*>(s_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     } else {
-        for (uint32_t i = threadIdx.x; i < kDecTile; i += kThreads)
-            s_acc[i] = (load && i < len) ? a.dense[p0 + i] : 0.0f;
+        for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
+            reinterpret_cast<uint4*>(s_minw)[i] = make_uint4(kNoPos, kNoPos, kNoPos, kNoPos);
+        if (vec && load) {
+            for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
+                reinterpret_cast<float4*>(s_acc)[i] = reinterpret_cast<const float4*>(a.dense + p0)[i];
+        } else if (vec) {
+            for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
+                reinterpret_cast<float4*>(s_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            for (uint32_t i = threadIdx.x; i < kDecTile; i += kThreads)
+                s_acc[i] = (load && i < len) ? a.dense[p0 + i] : 0.0f;
+        }
     }
     for (int wb = 0; wb < a.W; wb += kThreads) {
         const int w = wb + threadIdx.x;
@@ -407,7 +426,11 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
         const int nw = min(kThreads, a.W - wb);
         for (uint32_t r0 = 0; r0 < total; r0 += kDecCap) {
             const uint32_t m = (uint32_t)umin64(kDecCap, total - r0);
-            for (uint32_t i = threadIdx.x; i < m; i += kThreads) {
+            uint32_t act = 0;  // this thread's staged tokens that still owe an addition
+#pragma unroll
+            for (int k = 0; k < kPerThread; ++k) {
+                const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+                if (i >= m) break;
                 const uint32_t f = r0 + i;
                 int l = 0, h = nw;  // message of flattened token f
                 while (h - l > 1) {
@@ -416,28 +439,47 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
                 }
                 const DecStream& d = a.tab[wb + l];
                 const uint64_t j = s_first[l] + (f - s_off[l]);
-                s_pos[i] = a.pos[d.tok_base + j];
-                s_val[i] = dec_value(a, d, j);
-            }
-            __syncthreads();
-            if (threadIdx.x < 32) {
-                for (int l = 0; l < nw; ++l) {
-                    const uint32_t lo = max(s_off[l], r0), hi = min(s_off[l + 1], r0 + m);
-                    for (uint32_t i = lo + threadIdx.x; i < hi; i += 32) {
-                        const uint32_t p = s_pos[i - r0];
-                        if (p != kEscPos && p >= p0 && p < p0 + len) {
-                            if (kInt) {
-                                s_acci[p - p0] += (int32_t)s_val[i - r0];
-                                s_touch[p - p0] = 1;
-                            } else {
-                                s_acc[p - p0] = __fadd_rn(s_acc[p - p0], __uint_as_float(s_val[i - r0]));
-                            }
-                        }
+                const uint32_t p = a.pos[d.tok_base + j];
+                const uint32_t raw = dec_value(a, d, j);
+                const bool in = p != kEscPos && p >= p0 && p < p0 + len;
+                if (kInt) {
+                    if (in) {
+                        atomicAdd(&s_acci[p - p0], (int32_t)raw);
+                        s_touch[p - p0] = 1;
                     }
-                    __syncwarp();
+                } else {
+                    s_pos[i] = in ? (uint32_t)(p - p0) : kNoPos;
+                    s_val[i] = raw;
+                    s_msg[i] = (uint32_t)l;
+                    if (in) act |= 1u << k;
                 }
             }
-            __syncthreads();
+            if (!kInt) {
+                // rounds; s_minw holds kNoPos everywhere between rounds
+                while (__syncthreads_or(act != 0)) {
+#pragma unroll
+                    for (int k = 0; k < kPerThread; ++k) {
+                        const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+                        if (act & (1u << k)) atomicMin(&s_minw[s_pos[i]], s_msg[i]);
+                    }
+                    __syncthreads();
+#pragma unroll
+                    for (int k = 0; k < kPerThread; ++k) {
+                        const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+                        if (!(act & (1u << k))) continue;
+                        const uint32_t lp = s_pos[i];
+                        // the one token of the smallest message left at lp (another token there
+                        // may already see the cleared word: it never equals a message index)
+                        if (s_minw[lp] == s_msg[i]) {
+                            s_acc[lp] = __fadd_rn(s_acc[lp], __uint_as_float(s_val[i]));
+                            s_minw[lp] = kNoPos;
+                            act &= ~(1u << k);
+                        }
+                    }
+                }
+            } else {
+                __syncthreads();  // the staged chunk is consumed before the next one is staged
+            }
         }
     }
     __syncthreads();

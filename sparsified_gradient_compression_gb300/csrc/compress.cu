@@ -101,7 +101,6 @@ constexpr int kSqLimbs = 10;   // 640-bit exact sum of squares, 64-bit limbs (wh
 constexpr int kSqDigits = 20;  // the same sum as 32-bit digits, each in a 64-bit word
 constexpr int kSqWords = kSqDigits + 1;  // + one word of flags (2: +inf seen, 4: NaN seen)
 constexpr int kHistBins = 2048;
-constexpr int kSamplePerThread = 4;
 constexpr uint64_t kExactSamplePpb = 10000000;    // exact mode samples 1% to bound t from below
 constexpr uint32_t kExactWholeBelow = 8192;       // smaller segments: every entry is a candidate
 
@@ -506,26 +505,41 @@ __device__ double limbs_round(const unsigned long long* x) {
     return __longlong_as_double((long long)bits);
 }
 
+// (w1:w0) += (p1:p0), 128 bits
+__device__ __forceinline__ void add128(unsigned long long& w0, unsigned long long& w1,
+                                       unsigned long long p0, unsigned long long p1) {
+    asm("add.cc.u64 %0, %0, %2;\n\taddc.u64 %1, %1, %3;" : "+l"(w0), "+l"(w1) : "l"(p0), "l"(p1));
+}
+
 // 4096-entry tiles of one segment each, the blocks looping over them. For a tile the block finds
 // the largest exponent e_max of its entries; the block sums into a 128-bit window whose lowest
 // bit is bit lo = max(2 e_max - 68, 0) of X. Each thread first sums its 16 squares in two 64-bit
-// bands below its own largest entry (a shift of at most 12 bits and one 64-bit add per entry),
-// then places the two band sums in the window (each below 2^118 there, 512 of them below
-// 2^127). What starts below lo, or lies more than 13 binades under the thread's largest entry,
-// goes to digit words in shared memory instead. The window's block total, and the shared words
-// when used (their carries propagated first, so each adds less than 2^32 per word), then enter
-// the segment's words in global memory.
+// bands below its own largest entry, then places the two band sums in the window (each below
+// 2^118 there, 512 of them below 2^127). An entry of band b with e' = eb + d (d <= 6) adds
+// (m 2^d)^2 = M 4^d: a 32-bit shift of the significand (m 2^d < 2^30) and one 32 x 32 -> 64-bit
+// multiply, so the band sum stays below 16 x 2^60 = 2^64. What starts below lo, or lies more
+// than 13 binades under the thread's largest entry, goes to digit words in shared memory
+// instead. The window's block total, and the shared words when used (their carries propagated
+// first), then enter the segment's words in global memory. The tile's largest exponent comes
+// from the largest |x| bits of each warp (the exponent of the largest |x|), combined through
+// one shared word per tile (two, used in turn, so that one is cleared while the other is read).
 __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
     __shared__ unsigned long long s_low[kSqDigits];
     __shared__ unsigned long long s_w[kThreads / 32][2];
-    __shared__ uint32_t s_emax[kThreads / 32];
+    __shared__ uint32_t s_em[2];
     __shared__ uint32_t s_flags;  // 1: an entry below the window; 2: +inf; 4: NaN
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) s_flags = 0;
+    if (threadIdx.x == 0) {
+        s_flags = 0;
+        s_em[0] = 0;
+        s_em[1] = 0;
+    }
     if (threadIdx.x < kSqDigits) s_low[threadIdx.x] = 0ull;
     if (a.ctl->abort) return;
+    __syncthreads();
     const uint32_t total = a.ctl->total_clip_tiles;
-    for (uint32_t c = blockIdx.x; c < total; c += gridDim.x) {
+    uint32_t par = 0;
+    for (uint32_t c = blockIdx.x; c < total; c += gridDim.x, par ^= 1u) {
         const int s = upper_bound_minus1(a.clip_off, a.nseg, c);
         const SegInfo& d = a.segs[s];
         const uint64_t base = (uint64_t)d.start + (uint64_t)(c - a.clip_off[s]) * kClipTile +
@@ -548,18 +562,18 @@ __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
                 xb[i] = (e < d.end) ? (__float_as_uint(a.g[e]) & 0x7FFFFFFFu) : 0u;
             }
         }
-        uint32_t et = 1, nonfinite = 0;  // the thread's largest finite e', and any inf/NaN
+        uint32_t amax = 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t e = xb[i] >> 23;
-            nonfinite |= (e == 0xFFu);
-            if (e != 0xFFu) et = max(et, e);
-        }
-        uint32_t em = __reduce_max_sync(0xFFFFFFFFu, et);
-        if (lane == 0) s_emax[warp] = em;
+        for (int i = 0; i < 16; ++i) amax = max(amax, xb[i]);
+        const bool nonfinite = amax >= 0x7F800000u;
+        // the thread's largest e' (inf and NaN count as 254: the sum is then inf or NaN anyway,
+        // and every bound below still holds)
+        const uint32_t et = max(min(amax >> 23, 254u), 1u);
+        const uint32_t ew = __reduce_max_sync(kFull, et);
+        if (lane == 0) atomicMax(&s_em[par], ew);
         __syncthreads();  // (also orders the previous tile's use of s_w, s_low, s_flags)
-#pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) em = max(em, s_emax[w]);
+        const uint32_t em = s_em[par];
+        if (threadIdx.x == 0) s_em[par ^ 1u] = 0;  // for the next tile: read by nobody until then
         const int lo = max(2 * (int)em - 68, 0);
         unsigned long long w0 = 0ull, w1 = 0ull;
         uint32_t fl = 0;
@@ -573,44 +587,49 @@ __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
                 const unsigned long long p0 = (r < 64) ? (v << r) : 0ull;
                 const unsigned long long p1 =
                     (r == 0) ? 0ull : (r < 64) ? (v >> (64 - r)) : (v << (r - 64));
-                w0 += p0;
-                w1 += p1 + (w0 < p0 ? 1ull : 0ull);
+                add128(w0, w1, p0, p1);
             } else {
                 fl |= 1u;
                 digits_add(s_low, bit >> 5, bit & 31, v);
             }
         };
         if (!nonfinite) {
-            // Two bands of 7 binades below the thread's largest entry, each summed in 64 bits:
-            // e' in [ea, ea + 6] as M 2^(2(e' - ea)) (below 2^60, 16 of them below 2^64), e' in
-            // [eb, ea - 1] likewise from eb; smaller entries go to the shared words one by one.
+            // band 1: e' in [ea, ea + 6]; band 2: e' in [eb, ea - 1]; smaller entries (rare)
+            // go to the shared words one by one after the loop
             const uint32_t ea = max(et, 7u) - 6u;
             const uint32_t eb = max(ea, 8u) - 7u;
             unsigned long long A1 = 0ull, A2 = 0ull;
+            bool below = false;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const uint32_t ax = xb[i];
-                const uint32_t e = ax >> 23;
-                const uint32_t m = e ? ((ax & 0x7FFFFFu) | 0x800000u) : ax;
-                const uint32_t ep = max(e, 1u);
-                const unsigned long long M = (unsigned long long)m * m;
+                const uint32_t ep = max(ax >> 23, 1u);
+                const uint32_t m = ax - ((ep - 1u) << 23);  // significand (hidden bit if normal)
                 const bool in1 = ep >= ea, in2 = ep >= eb;
-                const uint32_t sft = in2 ? 2u * (ep - (in1 ? ea : eb)) : 0u;
-                const unsigned long long V = M << sft;
-                if (in1) {
-                    A1 += V;
-                } else if (in2) {
-                    A2 += V;
-                } else if (M != 0ull) {
-                    fl |= 1u;
-                    const int at = 2 * (int)ep - 2;
-                    digits_add(s_low, at >> 5, at & 31, M);
+                const uint32_t sh = ep - (in1 ? ea : eb);   // <= 6 whenever in2
+                const uint32_t mm = m << (sh & 7u);
+                const unsigned long long V = (unsigned long long)mm * mm;
+                if (in1) A1 += V;
+                else if (in2) A2 += V;
+                below |= !in2 && m != 0u;
+            }
+            if (below) {
+#pragma unroll 1
+                for (int i = 0; i < 16; ++i) {
+                    const uint32_t ax = xb[i];
+                    const uint32_t ep = max(ax >> 23, 1u);
+                    const uint32_t m = ax - ((ep - 1u) << 23);
+                    if (ep < eb && m != 0u) {
+                        fl |= 1u;
+                        const int at = 2 * (int)ep - 2;
+                        digits_add(s_low, at >> 5, at & 31, (unsigned long long)m * m);
+                    }
                 }
             }
             place(A1, 2 * (int)ea - 2);
             place(A2, 2 * (int)eb - 2);
         } else {  // a thread holding inf or NaN: entry by entry
-#pragma unroll
+#pragma unroll 1
             for (int i = 0; i < 16; ++i) {
                 const uint32_t ax = xb[i];
                 const uint32_t e = ax >> 23;
@@ -625,39 +644,43 @@ __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
         if (fl) atomicOr(&s_flags, fl);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-            const unsigned long long o0 = __shfl_down_sync(0xFFFFFFFFu, w0, off);
-            const unsigned long long o1 = __shfl_down_sync(0xFFFFFFFFu, w1, off);
-            w0 += o0;
-            w1 += o1 + (w0 < o0 ? 1ull : 0ull);
+            const unsigned long long o0 = __shfl_down_sync(kFull, w0, off);
+            const unsigned long long o1 = __shfl_down_sync(kFull, w1, off);
+            add128(w0, w1, o0, o1);
         }
         if (lane == 0) {
             s_w[warp][0] = w0;
             s_w[warp][1] = w1;
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
-            unsigned long long* X = a.clip_acc + (size_t)s * kSqWords;
-            unsigned long long W0 = 0ull, W1 = 0ull;
-            for (int w = 0; w < kThreads / 32; ++w) {
-                W0 += s_w[w][0];
-                W1 += s_w[w][1] + (W0 < s_w[w][0] ? 1ull : 0ull);
+        if (warp == 0) {  // the block's window total, then its 32-bit pieces into the segment
+            unsigned long long W0 = lane < kThreads / 32 ? s_w[lane][0] : 0ull;
+            unsigned long long W1 = lane < kThreads / 32 ? s_w[lane][1] : 0ull;
+#pragma unroll
+            for (int off = 4; off > 0; off >>= 1) {
+                const unsigned long long o0 = __shfl_down_sync(kFull, W0, off);
+                const unsigned long long o1 = __shfl_down_sync(kFull, W1, off);
+                add128(W0, W1, o0, o1);
             }
-            // W 2^lo: W < 2^126 in five 32-bit pieces from word lo / 32
-            const int i = lo >> 5, sh = lo & 31;
-            digits_add(X, i, sh, W0);
-            digits_add(X, i + 2, sh, W1);
-            const uint32_t flags = s_flags;
-            if (flags & 1u) {
-                unsigned long long carry = 0ull;
-                for (int j = 0; j < kSqDigits; ++j) {
-                    const unsigned long long t = s_low[j] + carry;
-                    if (t & 0xFFFFFFFFull) atomicAdd(X + j, t & 0xFFFFFFFFull);
-                    carry = t >> 32;
-                    s_low[j] = 0ull;
+            if (lane == 0) {
+                unsigned long long* X = a.clip_acc + (size_t)s * kSqWords;
+                // W 2^lo: W < 2^127 in five 32-bit pieces from word lo / 32
+                const int i = lo >> 5, sh = lo & 31;
+                digits_add(X, i, sh, W0);
+                digits_add(X, i + 2, sh, W1);
+                const uint32_t flags = s_flags;
+                if (flags & 1u) {
+                    unsigned long long carry = 0ull;
+                    for (int j = 0; j < kSqDigits; ++j) {
+                        const unsigned long long t = s_low[j] + carry;
+                        if (t & 0xFFFFFFFFull) atomicAdd(X + j, t & 0xFFFFFFFFull);
+                        carry = t >> 32;
+                        s_low[j] = 0ull;
+                    }
                 }
+                if (flags & 6u) atomicOr(X + kSqDigits, (unsigned long long)(flags & 6u));
+                s_flags = 0;
             }
-            if (flags & 6u) atomicOr(X + kSqDigits, (unsigned long long)(flags & 6u));
-            s_flags = 0;
         }
     }
 }
@@ -856,55 +879,88 @@ __global__ void __launch_bounds__(kThreads) k_cache(Args a) {
 // Sample draw j of segment s sits at start + floor(mix(seed_s + (j+1)g) * n_s / 2^64). The
 // post-accumulate value there is recomputed from the pre-step g, u, v with the same
 // operations the streaming pass uses, so it is bit-identical to what that pass will store.
-__global__ void __launch_bounds__(kThreads) k_sample(Args a) {
+//
+// A scattered 4-byte load costs a whole DRAM burst, so this gather is bound by the bursts it
+// can keep in flight. Persistent blocks (kSampleBlocksPerSm per SM) walk rounds of
+// kThreads x kSampleIter consecutive samples (positions ascending): each thread first loads its
+// kSampleIter positions, then issues all 3 x kSampleIter gathers before it uses any of them.
+// A round inside one segment counts into the block's shared histogram, one atomic per distinct
+// bin per warp (lanes with equal bins found by __match_any_sync); the block flushes it to the
+// segment's global histogram when it moves on to another segment and at its end. A round that
+// spans segments (rare: many small segments) adds straight to the global histograms.
+constexpr int kSampleIter = 8;
+constexpr int kSampleBlocksPerSm = 4;
+constexpr uint32_t kSampleRound = (uint32_t)kThreads * kSampleIter;
+
+__global__ void __launch_bounds__(kThreads, kSampleBlocksPerSm) k_sample(Args a) {
     __shared__ uint32_t s_hist[kHistBins];
-    __shared__ int s_seg0, s_seg1, s_skip;
-    if (threadIdx.x == 0) s_skip = a.ctl->abort;
-    __syncthreads();
-    if (s_skip) return;
+    // abort is only raised by earlier kernels of the call: every thread reads the same value
+    if (ld_relaxed_u32((const uint32_t*)&a.ctl->abort)) return;
     const uint32_t total = a.ctl->total_samples;
-    const uint64_t chunk0 = (uint64_t)blockIdx.x * kThreads * kSamplePerThread;
-    if (chunk0 >= total) return;
+    if ((uint64_t)blockIdx.x * kSampleRound >= total) return;
     for (int b = threadIdx.x; b < kHistBins; b += kThreads) s_hist[b] = 0;
-    const uint64_t chunk_end = umin64(total, chunk0 + kThreads * kSamplePerThread);
-    if (threadIdx.x == 0) {
-        s_seg0 = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)chunk0);
-        s_seg1 = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)(chunk_end - 1));
-    }
     __syncthreads();
-    const bool uniform = (s_seg0 == s_seg1);
-    float gv[kSamplePerThread], uv[kSamplePerThread], vv[kSamplePerThread];
-    int sg[kSamplePerThread];
+    const int lane = threadIdx.x & 31;
+    int cur = -1;  // the segment s_hist counts for (the same in every thread of the block)
+    for (uint64_t c0 = (uint64_t)blockIdx.x * kSampleRound; c0 < total;
+         c0 += (uint64_t)gridDim.x * kSampleRound) {
+        const uint64_t c1 = umin64(total, c0 + kSampleRound);
+        // the round's first and last segment: the same search in every thread (cached words)
+        const int s0 = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)c0);
+        const int s1 = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)(c1 - 1));
+        const bool uniform = (s0 == s1);
+        if (uniform && s0 != cur) {  // block-uniform: flush the previous segment's counts
+            if (cur >= 0) {
+                BlockHist h{s_hist, cur};
+                h.flush(a.histA, kHistBins);
+            }
+            cur = s0;
+        }
+        uint32_t pos[kSampleIter];
 #pragma unroll
-    for (int r = 0; r < kSamplePerThread; ++r) {
-        const uint64_t jg = chunk0 + r * kThreads + threadIdx.x;
-        sg[r] = -1;
-        if (jg < chunk_end) {
-            // a chunk that crosses segments searches only its own segment range
-            const int s = uniform ? s_seg0
-                                  : s_seg0 + upper_bound_minus1(a.samp_off + s_seg0,
-                                                                s_seg1 - s_seg0 + 1, (uint32_t)jg);
-            const uint32_t pos = a.spos[jg];  // the sample positions in ascending order
-            gv[r] = __ldg(a.g + pos);
-            uv[r] = a.u[pos];
-            vv[r] = a.v[pos];
-            sg[r] = s;
+        for (int r = 0; r < kSampleIter; ++r) {
+            const uint64_t j = c0 + (uint64_t)r * kThreads + threadIdx.x;
+            pos[r] = j < c1 ? __ldcs(a.spos + j) : 0u;  // the sample positions, ascending
+        }
+        float gv[kSampleIter], uv[kSampleIter], vv[kSampleIter];
+#pragma unroll
+        for (int r = 0; r < kSampleIter; ++r) {
+            const uint64_t j = c0 + (uint64_t)r * kThreads + threadIdx.x;
+            if (j < c1) {
+                gv[r] = __ldg(a.g + pos[r]);
+                uv[r] = __ldg(a.u + pos[r]);
+                vv[r] = __ldg(a.v + pos[r]);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kSampleIter; ++r) {
+            const uint64_t j = c0 + (uint64_t)r * kThreads + threadIdx.x;
+            const bool valid = j < c1;
+            uint32_t bin = 0;
+            int s = s0;
+            if (valid) {
+                // a round that crosses segments searches only its own segment range
+                if (!uniform)
+                    s = s0 + upper_bound_minus1(a.samp_off + s0, s1 - s0 + 1, (uint32_t)j);
+                float uu = uv[r], vn = vv[r];
+                accumulate(gv[r], uu, vn, a.hp.momentum, a.segs[s].scale, a.hp.leak);
+                const uint32_t key = key_of(vn);
+                a.skeys[j] = key;
+                bin = key >> 20;
+            }
+            if (uniform) {  // block-uniform branch: every lane of the warp is here
+                const unsigned m = __ballot_sync(kFull, valid);
+                if (valid) {
+                    const unsigned peers = __match_any_sync(m, bin);
+                    if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], (uint32_t)__popc(peers));
+                }
+            } else if (valid) {
+                atomicAdd(&a.histA[(size_t)s * kHistBins + bin], 1u);
+            }
         }
     }
-#pragma unroll
-    for (int r = 0; r < kSamplePerThread; ++r) {
-        if (sg[r] < 0) continue;
-        const uint64_t jg = chunk0 + r * kThreads + threadIdx.x;
-        float uu = uv[r], vn = vv[r];
-        accumulate(gv[r], uu, vn, a.hp.momentum, a.segs[sg[r]].scale, a.hp.leak);
-        const uint32_t key = key_of(vn);
-        a.skeys[jg] = key;
-        const uint32_t bin = key >> 20;
-        if (uniform) atomicAdd(&s_hist[bin], 1u);
-        else atomicAdd(&a.histA[(size_t)sg[r] * kHistBins + bin], 1u);
-    }
-    if (uniform) {
-        BlockHist h{s_hist, s_seg0};
+    if (cur >= 0) {
+        BlockHist h{s_hist, cur};
         h.flush(a.histA, kHistBins);
     }
 }
@@ -2385,8 +2441,8 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     const bool selects = hp.mode != DGC_SELECT_ADACOMP;
     if (selects) {
         coop((const void*)k_cache, cooperative_grid(2, sms));
-        const uint64_t sgrid = (L.max_samples + kThreads * kSamplePerThread - 1) /
-                               (kThreads * kSamplePerThread);
+        const uint64_t sgrid = std::min<uint64_t>((L.max_samples + kSampleRound - 1) / kSampleRound,
+                                                  (uint64_t)sms * kSampleBlocksPerSm);
         L1(k_sample, (unsigned)sgrid, kThreads, a);
     }
     set_kernel_attributes();

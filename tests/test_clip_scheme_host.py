@@ -2,16 +2,19 @@
 
 The kernels `k_clip_tiles` and `k_clip_round` sum the squares of a segment exactly. Per
 4096-entry tile, each of 256 threads holds 16 entries and sums their squares in two 64-bit
-bands below its own largest entry. The block adds the band sums into a 128-bit window anchored
+bands below its own largest entry: an entry with e' = e_band + d (d <= 6) adds the 64-bit
+product of its significand shifted left by d with itself, (m 2^d)^2 = m^2 4^d, which needs
+m 2^d to fit 32 bits. The thread's largest e' is read off its largest |x| bits (a thread that
+holds inf or NaN counts as 254). The block adds the band sums into a 128-bit window anchored
 68 bits below the tile's largest square. Anything lower goes to 32-bit digits held in 64-bit
 words, first per block, then per segment. One thread per segment then propagates the carries
 and rounds once to binary64.
 
 This model takes the same steps with Python integers and asserts the bounds the kernels rely
-on: a band sum below 2^64, a window term below 2^118 and the window below 2^127, and a word
-below 2^55. Its S must equal the oracle's, the exact sum rounded once (the DGC review's local
-gradient clipping; the pages fix no order of summation). It checks the scheme; the GPU parity
-tests check the kernels themselves against the oracle, S included.
+on: a shifted significand below 2^30, a band sum below 2^64, a window term below 2^118 and the
+window below 2^127, and a word below 2^55. Its S must equal the oracle's, the exact sum rounded
+once (the DGC review's local gradient clipping; the pages fix no order of summation). It checks
+the scheme; the GPU parity tests check the kernels themselves against the oracle, S included.
 """
 import math
 import struct
@@ -36,7 +39,8 @@ def _tile(seg_words, bits):
     """One block's work on one tile (|x| bits, zero-padded to 4096); returns its inf/NaN flags."""
     bits = list(bits) + [0] * (TILE - len(bits))
     threads = [bits[PER * t:PER * t + PER] for t in range(THREADS)]
-    et = [max([1] + [a >> 23 for a in th if (a >> 23) != 255]) for th in threads]
+    # the thread's largest e' from its largest |x| bits; inf or NaN counts as 254
+    et = [max(min(max(th) >> 23, 254), 1) for th in threads]
     em = max(et)
     lo = max(2 * em - 68, 0)  # the window's lowest bit of X
     low = [0] * DIGITS
@@ -67,16 +71,21 @@ def _tile(seg_words, bits):
         eb = max(ea, 8) - 7     # band 2: e' in [eb, ea - 1]
         A1 = A2 = 0
         for a in th:
-            e = a >> 23
-            m = (a & 0x7FFFFF) | 0x800000 if e else a
-            ep, M = max(e, 1), m * m
-            if ep >= ea:
-                A1 += M << (2 * (ep - ea))
-            elif ep >= eb:
-                A2 += M << (2 * (ep - eb))
-            elif M:
+            ep = max(a >> 23, 1)
+            m = a - ((ep - 1) << 23)  # the significand, hidden bit included when normal
+            assert m < 2**24
+            if ep >= eb:
+                sh = ep - (ea if ep >= ea else eb)
+                assert 0 <= sh <= 6
+                mm = m << sh
+                assert mm < 2**30
+                if ep >= ea:
+                    A1 += mm * mm
+                else:
+                    A2 += mm * mm
+            elif m:
                 flags |= 1
-                _digits_add(low, (2 * ep - 2) >> 5, (2 * ep - 2) & 31, M)
+                _digits_add(low, (2 * ep - 2) >> 5, (2 * ep - 2) & 31, m * m)
         assert A1 < 2**64 and A2 < 2**64
         place(A1, 2 * ea - 2)
         place(A2, 2 * eb - 2)

@@ -597,6 +597,48 @@ def test_decode_many_learners_and_accumulate(seed):
         assert same_bits(host_f32(dense), odense)
 
 
+@pytest.mark.parametrize("case", ["same set, 300 learners", "dense messages, 40 learners",
+                                  "half shared, 70 learners"])
+def test_decode_collisions_and_crowded_tiles(case):
+    # The worst cases of the ordered multi-message sum: every learner at the same positions (as
+    # many values meet at one position as there are learners, across the 256-message groups),
+    # messages that send every entry (tens of thousands of tokens per dense tile), and learners
+    # that share half of their positions. Dense sums, accumulation and the SGD step, bitwise.
+    rng = np.random.default_rng(len(case))
+    msgs = []
+    if case.startswith("same set"):
+        n, W = 20_003, 300
+        idx = np.sort(rng.choice(n, size=3000, replace=False)).astype(np.uint32)
+        for _ in range(W):
+            val = (rng.standard_normal(idx.size) * 10.0 ** rng.integers(-4, 4, idx.size))
+            msgs.append(oracle.encode(idx, val.astype(np.float32), n))
+    elif case.startswith("dense"):
+        n, W = 9_000, 40
+        idx = np.arange(n, dtype=np.uint32)
+        for _ in range(W):
+            val = (rng.standard_normal(n) * 10.0 ** rng.integers(-3, 3, n)).astype(np.float32)
+            val[rng.random(n) < 0.05] = np.float32(-0.0)
+            msgs.append(oracle.encode(idx, val, n))
+    else:
+        n, W = 100_000, 70
+        common = rng.choice(n, size=4000, replace=False)
+        for _ in range(W):
+            own = rng.choice(n, size=4000, replace=False)
+            idx = np.unique(np.concatenate([common, own])).astype(np.uint32)
+            val = (rng.standard_normal(idx.size) * 0.01).astype(np.float32)
+            msgs.append(oracle.encode(idx, val, n))
+    base = rng.standard_normal(n).astype(np.float32)
+    for acc in (False, True):
+        rc, dense = decode(msgs, n, dense=dev_f32(base), accumulate=acc)
+        orc_rc, odense = oracle.decode_accumulate(msgs, n, dense=base, accumulate=acc)
+        assert rc == 0 and orc_rc == 0
+        assert same_bits(host_f32(dense), odense), acc
+    rc, got = decode_apply(msgs, n, base, 0.37)
+    orc_rc, exp = oracle.decode_apply(msgs, n, base, np.float32(0.37))
+    assert rc == 0 and orc_rc == 0
+    assert same_bits(got, exp)
+
+
 @pytest.mark.parametrize("acc", [False, True])
 def test_decode_single_message_both_modes(acc):
     # one message: the decoder clears dense (unless accumulating) and adds each value once
