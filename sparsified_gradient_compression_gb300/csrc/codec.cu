@@ -424,9 +424,68 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
         if (threadIdx.x == 0) s_off[kThreads] = (uint32_t)total;
         __syncthreads();
         const int nw = min(kThreads, a.W - wb);
+        // the staged tokens this thread owns in the rounds: slots tid + k kThreads
+        auto rounds = [&](uint32_t m) {
+            uint32_t act = 0;
+#pragma unroll
+            for (int k = 0; k < kPerThread; ++k) {
+                const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+                if (i < m && s_pos[i] != kNoPos) act |= 1u << k;
+            }
+            // every position still owed a value takes the token of its smallest message; a
+            // barrier closes each round (s_minw is kNoPos everywhere between rounds)
+            do {
+#pragma unroll
+                for (int k = 0; k < kPerThread; ++k) {
+                    const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+                    if (act & (1u << k)) atomicMin(&s_minw[s_pos[i]], s_msg[i]);
+                }
+                __syncthreads();
+#pragma unroll
+                for (int k = 0; k < kPerThread; ++k) {
+                    const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+                    if (!(act & (1u << k))) continue;
+                    const uint32_t lp = s_pos[i];
+                    // the one token of the smallest message left at lp (another token there
+                    // may already see the cleared word: it never equals a message index)
+                    if (s_minw[lp] == s_msg[i]) {
+                        s_acc[lp] = __fadd_rn(s_acc[lp], __uint_as_float(s_val[i]));
+                        s_minw[lp] = kNoPos;
+                        act &= ~(1u << k);
+                    }
+                }
+            } while (__syncthreads_or(act != 0));
+        };
+        if (total <= kDecCap) {
+            // one chunk (the common case): each message's own thread stages its few tokens at
+            // the message's offset, so no token searches for its message
+            if (threadIdx.x < nw && cnt > 0) {
+                const DecStream& d = a.tab[wb + threadIdx.x];
+                const uint32_t at = (uint32_t)ex;
+#pragma unroll 4
+                for (uint32_t q = 0; q < cnt; ++q) {
+                    const uint64_t j = (uint64_t)first + q;
+                    const uint32_t p = a.pos[d.tok_base + j];
+                    const uint32_t raw = dec_value(a, d, j);
+                    const bool in = p != kEscPos && p >= p0 && p < p0 + len;
+                    if (kInt) {
+                        if (in) {
+                            atomicAdd(&s_acci[p - p0], (int32_t)raw);
+                            s_touch[p - p0] = 1;
+                        }
+                    } else {
+                        s_pos[at + q] = in ? (uint32_t)(p - p0) : kNoPos;
+                        s_val[at + q] = raw;
+                        s_msg[at + q] = (uint32_t)threadIdx.x;
+                    }
+                }
+            }
+            __syncthreads();
+            if (!kInt && total > 0) rounds((uint32_t)total);
+            continue;
+        }
         for (uint32_t r0 = 0; r0 < total; r0 += kDecCap) {
             const uint32_t m = (uint32_t)umin64(kDecCap, total - r0);
-            uint32_t act = 0;  // this thread's staged tokens that still owe an addition
 #pragma unroll
             for (int k = 0; k < kPerThread; ++k) {
                 const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
@@ -451,57 +510,57 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
                     s_pos[i] = in ? (uint32_t)(p - p0) : kNoPos;
                     s_val[i] = raw;
                     s_msg[i] = (uint32_t)l;
-                    if (in) act |= 1u << k;
                 }
             }
-            if (!kInt) {
-                // rounds; s_minw holds kNoPos everywhere between rounds
-                while (__syncthreads_or(act != 0)) {
-#pragma unroll
-                    for (int k = 0; k < kPerThread; ++k) {
-                        const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
-                        if (act & (1u << k)) atomicMin(&s_minw[s_pos[i]], s_msg[i]);
-                    }
-                    __syncthreads();
-#pragma unroll
-                    for (int k = 0; k < kPerThread; ++k) {
-                        const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
-                        if (!(act & (1u << k))) continue;
-                        const uint32_t lp = s_pos[i];
-                        // the one token of the smallest message left at lp (another token there
-                        // may already see the cleared word: it never equals a message index)
-                        if (s_minw[lp] == s_msg[i]) {
-                            s_acc[lp] = __fadd_rn(s_acc[lp], __uint_as_float(s_val[i]));
-                            s_minw[lp] = kNoPos;
-                            act &= ~(1u << k);
-                        }
-                    }
-                }
-            } else {
-                __syncthreads();  // the staged chunk is consumed before the next one is staged
-            }
+            if (!kInt) rounds(m);  // each thread reads back only slots it staged itself
+            else __syncthreads();  // the staged chunk is consumed before the next one is staged
         }
     }
     __syncthreads();
+    // Modes that read the output first (the SGD step, accumulation of integer sums) load every
+    // value this thread needs before any arithmetic, so a tile costs one round trip to memory
+    // instead of one per entry; only the entries that change are written.
+    constexpr int kOut = kDecTile / kThreads;
     if (kInt) {
-        for (uint32_t i = threadIdx.x; i < len; i += kThreads) {
-            const int32_t S = s_acci[i];
-            float* o = a.dense + p0 + i;
-            if (a.apply) {  // S == 0: the step is the identity
-                if (S) *o = __fmaf_rn(a.neg_lr, dequant(S, a.alpha), *o);
-            } else if (a.accumulate) {  // one addition where a message landed
-                if (s_touch[i]) *o = __fadd_rn(*o, dequant(S, a.alpha));
-            } else {
-                *o = dequant(S, a.alpha);
+        if (a.apply || a.accumulate) {
+            float o[kOut];
+#pragma unroll
+            for (int k = 0; k < kOut; ++k) {
+                const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+                const bool need = i < len && (a.apply ? s_acci[i] != 0 : s_touch[i] != 0);
+                o[k] = need ? a.dense[p0 + i] : 0.0f;
             }
+#pragma unroll
+            for (int k = 0; k < kOut; ++k) {
+                const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+                if (i >= len) break;
+                const int32_t S = s_acci[i];
+                if (a.apply) {  // S == 0: the step is the identity
+                    if (S) a.dense[p0 + i] = __fmaf_rn(a.neg_lr, dequant(S, a.alpha), o[k]);
+                } else if (s_touch[i]) {  // one addition where a message landed
+                    a.dense[p0 + i] = __fadd_rn(o[k], dequant(S, a.alpha));
+                }
+            }
+        } else {
+            for (uint32_t i = threadIdx.x; i < len; i += kThreads)
+                a.dense[p0 + i] = dequant(s_acci[i], a.alpha);
         }
     } else if (a.apply) {
         // a sum that starts at +0 is +0 wherever no message lands (x + y is -0 only for two -0
         // addends), and fma(neg_lr, +0, w) == w for a finite neg_lr with its sign bit set: those
         // entries are left alone, the others take the step
-        for (uint32_t i = threadIdx.x; i < len; i += kThreads) {
+        float o[kOut];
+#pragma unroll
+        for (int k = 0; k < kOut; ++k) {
+            const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+            o[k] = (i < len && __float_as_uint(s_acc[i]) != 0u) ? a.dense[p0 + i] : 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < kOut; ++k) {
+            const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+            if (i >= len) break;
             const float t = s_acc[i];
-            if (__float_as_uint(t) != 0u) a.dense[p0 + i] = __fmaf_rn(a.neg_lr, t, a.dense[p0 + i]);
+            if (__float_as_uint(t) != 0u) a.dense[p0 + i] = __fmaf_rn(a.neg_lr, t, o[k]);
         }
     } else if (vec) {
         for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)

@@ -450,12 +450,15 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
 // x = m 2^(e'-150) (m the 24-bit significand, e' = max(biased exponent, 1)) has the exact
 // square M 2^(2e'-300), M = m^2 < 2^48; the segment keeps X = sum M 2^(2e'-2) (2e'-2 <= 506, at
 // most 2^32 entries: X < 2^586) and S = X 2^-298. X lives in kSqDigits 64-bit words, word i
-// worth 2^(32 i), which take plain atomic adds that nobody waits for, in any order. Every such
-// add is below 2^33 (digits_add's middle piece holds two digits' worth), a tile adds to one
-// word at most three times (the window's two halves overlap in one word, and the shared low
-// words add once more), and a segment has fewer than 2^20 tiles, so every word stays below
-// 2^55 and never overflows; the carries are propagated once, by k_clip_round. A host model of
-// these integer steps, with the bounds asserted, is in tests/test_clip_scheme_host.py.
+// worth 2^(32 i), which take plain atomic adds that nobody waits for, in any order. A block
+// keeps its share of a segment in the same form in shared memory: every shared add is below
+// 2^33 (digits_add's middle piece holds two digits' worth), a tile makes at most 8 x 2 + 4096
+// of them to one word (two per warp window, one per entry below its window), and a block sums
+// at most ceil(2^20 / grid) + 1 tiles of a segment (under 1800 with the 608-block grid), so a
+// shared word stays below 2^56. The block then adds 32-bit digits to the segment's global words
+// (its carries propagated first), once per block and segment, so a global word stays below
+// 2^42; the carries are propagated once more, by k_clip_round. A host model of these integer
+// steps, with the bounds asserted, is in tests/test_clip_scheme_host.py.
 
 // words[i..] += x 2^(32 i + sh) for x < 2^64, sh < 32: three 32-bit pieces
 __device__ __forceinline__ void digits_add(unsigned long long* words, int i, int sh,
@@ -511,36 +514,55 @@ __device__ __forceinline__ void add128(unsigned long long& w0, unsigned long lon
     asm("add.cc.u64 %0, %0, %2;\n\taddc.u64 %1, %1, %3;" : "+l"(w0), "+l"(w1) : "l"(p0), "l"(p1));
 }
 
-// 4096-entry tiles of one segment each, the blocks looping over them. For a tile the block finds
-// the largest exponent e_max of its entries; the block sums into a 128-bit window whose lowest
-// bit is bit lo = max(2 e_max - 68, 0) of X. Each thread first sums its 16 squares in two 64-bit
-// bands below its own largest entry, then places the two band sums in the window (each below
-// 2^118 there, 512 of them below 2^127). An entry of band b with e' = eb + d (d <= 6) adds
+// 4096-entry tiles of one segment each. Block b takes a contiguous range of the tiles (so its
+// segment changes only at segment boundaries), and its warps work without block barriers: warp w
+// of a tile holds entries [512 w, 512 w + 512), 16 per thread. The warp finds the largest
+// exponent e_max of its entries (from the largest |x| bits) and sums into a 128-bit window whose
+// lowest bit is bit lo = max(2 e_max - 68, 0) of X. Each thread first sums its 16 squares in two
+// 64-bit bands below its own largest entry, then places the two band sums in the window (each
+// below 2^118 there, 64 of them below 2^124). An entry of band b with e' = eb + d (d <= 6) adds
 // (m 2^d)^2 = M 4^d: a 32-bit shift of the significand (m 2^d < 2^30) and one 32 x 32 -> 64-bit
-// multiply, so the band sum stays below 16 x 2^60 = 2^64. What starts below lo, or lies more
-// than 13 binades under the thread's largest entry, goes to digit words in shared memory
-// instead. The window's block total, and the shared words when used (their carries propagated
-// first), then enter the segment's words in global memory. The tile's largest exponent comes
-// from the largest |x| bits of each warp (the exponent of the largest |x|), combined through
-// one shared word per tile (two, used in turn, so that one is cleared while the other is read).
+// multiply, so a band sum stays below 16 x 2^60 = 2^64. What starts below lo, or lies more than
+// 13 binades under the thread's largest entry, is added to the block's digit words in shared
+// memory at once; lane 0 then adds the warp's window there too (shared atomic adds, each below
+// 2^33). When the block moves to another segment, and at its end, one thread propagates the
+// carries of the shared words into 32-bit digits and adds those to the segment's words in global
+// memory (each below 2^32, at most one add per block and segment).
 __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
-    __shared__ unsigned long long s_low[kSqDigits];
-    __shared__ unsigned long long s_w[kThreads / 32][2];
-    __shared__ uint32_t s_em[2];
-    __shared__ uint32_t s_flags;  // 1: an entry below the window; 2: +inf; 4: NaN
+    __shared__ unsigned long long s_dig[kSqDigits];  // the block's share of the current segment
+    __shared__ uint32_t s_flags;                     // 2: +inf seen; 4: NaN seen
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) {
-        s_flags = 0;
-        s_em[0] = 0;
-        s_em[1] = 0;
-    }
-    if (threadIdx.x < kSqDigits) s_low[threadIdx.x] = 0ull;
-    if (a.ctl->abort) return;
+    if (threadIdx.x == 0) s_flags = 0;
+    if (threadIdx.x < kSqDigits) s_dig[threadIdx.x] = 0ull;
+    if (a.ctl->abort) return;  // written only by earlier kernels: the same in every thread
     __syncthreads();
     const uint32_t total = a.ctl->total_clip_tiles;
-    uint32_t par = 0;
-    for (uint32_t c = blockIdx.x; c < total; c += gridDim.x, par ^= 1u) {
-        const int s = upper_bound_minus1(a.clip_off, a.nseg, c);
+    const uint32_t c0 = (uint32_t)((uint64_t)total * blockIdx.x / gridDim.x);
+    const uint32_t c1 = (uint32_t)((uint64_t)total * (blockIdx.x + 1) / gridDim.x);
+    if (c0 >= c1) return;
+    int s = upper_bound_minus1(a.clip_off, a.nseg, c0);
+    // the block's digits into segment s's words: carries first, then one add per digit
+    auto flush = [&](int seg) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            unsigned long long* X = a.clip_acc + (size_t)seg * kSqWords;
+            unsigned long long carry = 0ull;
+            for (int j = 0; j < kSqDigits; ++j) {
+                const unsigned long long t = s_dig[j] + carry;
+                if (t & 0xFFFFFFFFull) atomicAdd(X + j, t & 0xFFFFFFFFull);
+                carry = t >> 32;
+                s_dig[j] = 0ull;
+            }
+            if (s_flags) atomicOr(X + kSqDigits, (unsigned long long)s_flags);
+            s_flags = 0;
+        }
+        __syncthreads();
+    };
+    for (uint32_t c = c0; c < c1; ++c) {
+        if (s + 1 < a.nseg && a.clip_off[s + 1] <= c) {  // block-uniform: a new segment
+            flush(s);
+            while (s + 1 < a.nseg && a.clip_off[s + 1] <= c) ++s;
+        }
         const SegInfo& d = a.segs[s];
         const uint64_t base = (uint64_t)d.start + (uint64_t)(c - a.clip_off[s]) * kClipTile +
                               16u * threadIdx.x;
@@ -569,17 +591,13 @@ __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
         // the thread's largest e' (inf and NaN count as 254: the sum is then inf or NaN anyway,
         // and every bound below still holds)
         const uint32_t et = max(min(amax >> 23, 254u), 1u);
-        const uint32_t ew = __reduce_max_sync(kFull, et);
-        if (lane == 0) atomicMax(&s_em[par], ew);
-        __syncthreads();  // (also orders the previous tile's use of s_w, s_low, s_flags)
-        const uint32_t em = s_em[par];
-        if (threadIdx.x == 0) s_em[par ^ 1u] = 0;  // for the next tile: read by nobody until then
+        const uint32_t em = __reduce_max_sync(kFull, et);
         const int lo = max(2 * (int)em - 68, 0);
         unsigned long long w0 = 0ull, w1 = 0ull;
         uint32_t fl = 0;
-        // v 2^bit into the window when bit >= lo, else into the shared words. In the window v 2^r
-        // stays below 2^118: a band sum (v < 2^64) has r <= 54, a single square (v < 2^48)
-        // r <= 66.
+        // v 2^bit into the window when bit >= lo, else into the block's digits. In the window
+        // v 2^r stays below 2^118: a band sum (v < 2^64) has r <= 54, a single square
+        // (v < 2^48) r <= 66.
         auto place = [&](unsigned long long v, int bit) {
             if (v == 0ull) return;
             const int r = bit - lo;
@@ -589,13 +607,12 @@ __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
                     (r == 0) ? 0ull : (r < 64) ? (v >> (64 - r)) : (v << (r - 64));
                 add128(w0, w1, p0, p1);
             } else {
-                fl |= 1u;
-                digits_add(s_low, bit >> 5, bit & 31, v);
+                digits_add(s_dig, bit >> 5, bit & 31, v);
             }
         };
         if (!nonfinite) {
             // band 1: e' in [ea, ea + 6]; band 2: e' in [eb, ea - 1]; smaller entries (rare)
-            // go to the shared words one by one after the loop
+            // go to the shared digits one by one after the loop
             const uint32_t ea = max(et, 7u) - 6u;
             const uint32_t eb = max(ea, 8u) - 7u;
             unsigned long long A1 = 0ull, A2 = 0ull;
@@ -614,22 +631,21 @@ __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
                 below |= !in2 && m != 0u;
             }
             if (below) {
-#pragma unroll 1
+#pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const uint32_t ax = xb[i];
                     const uint32_t ep = max(ax >> 23, 1u);
                     const uint32_t m = ax - ((ep - 1u) << 23);
                     if (ep < eb && m != 0u) {
-                        fl |= 1u;
                         const int at = 2 * (int)ep - 2;
-                        digits_add(s_low, at >> 5, at & 31, (unsigned long long)m * m);
+                        digits_add(s_dig, at >> 5, at & 31, (unsigned long long)m * m);
                     }
                 }
             }
             place(A1, 2 * (int)ea - 2);
             place(A2, 2 * (int)eb - 2);
         } else {  // a thread holding inf or NaN: entry by entry
-#pragma unroll 1
+#pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const uint32_t ax = xb[i];
                 const uint32_t e = ax >> 23;
@@ -648,41 +664,14 @@ __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
             const unsigned long long o1 = __shfl_down_sync(kFull, w1, off);
             add128(w0, w1, o0, o1);
         }
-        if (lane == 0) {
-            s_w[warp][0] = w0;
-            s_w[warp][1] = w1;
+        if (lane == 0) {  // W 2^lo: W < 2^124 in five 32-bit pieces from word lo / 32
+            const int i = lo >> 5, sh = lo & 31;
+            digits_add(s_dig, i, sh, w0);
+            digits_add(s_dig, i + 2, sh, w1);
         }
-        __syncthreads();
-        if (warp == 0) {  // the block's window total, then its 32-bit pieces into the segment
-            unsigned long long W0 = lane < kThreads / 32 ? s_w[lane][0] : 0ull;
-            unsigned long long W1 = lane < kThreads / 32 ? s_w[lane][1] : 0ull;
-#pragma unroll
-            for (int off = 4; off > 0; off >>= 1) {
-                const unsigned long long o0 = __shfl_down_sync(kFull, W0, off);
-                const unsigned long long o1 = __shfl_down_sync(kFull, W1, off);
-                add128(W0, W1, o0, o1);
-            }
-            if (lane == 0) {
-                unsigned long long* X = a.clip_acc + (size_t)s * kSqWords;
-                // W 2^lo: W < 2^127 in five 32-bit pieces from word lo / 32
-                const int i = lo >> 5, sh = lo & 31;
-                digits_add(X, i, sh, W0);
-                digits_add(X, i + 2, sh, W1);
-                const uint32_t flags = s_flags;
-                if (flags & 1u) {
-                    unsigned long long carry = 0ull;
-                    for (int j = 0; j < kSqDigits; ++j) {
-                        const unsigned long long t = s_low[j] + carry;
-                        if (t & 0xFFFFFFFFull) atomicAdd(X + j, t & 0xFFFFFFFFull);
-                        carry = t >> 32;
-                        s_low[j] = 0ull;
-                    }
-                }
-                if (flags & 6u) atomicOr(X + kSqDigits, (unsigned long long)(flags & 6u));
-                s_flags = 0;
-            }
-        }
+        (void)warp;
     }
+    flush(s);
 }
 
 // One thread per segment, after every tile is summed: propagate the carries of the segment's
@@ -880,87 +869,75 @@ __global__ void __launch_bounds__(kThreads) k_cache(Args a) {
 // post-accumulate value there is recomputed from the pre-step g, u, v with the same
 // operations the streaming pass uses, so it is bit-identical to what that pass will store.
 //
-// A scattered 4-byte load costs a whole DRAM burst, so this gather is bound by the bursts it
-// can keep in flight. Persistent blocks (kSampleBlocksPerSm per SM) walk rounds of
-// kThreads x kSampleIter consecutive samples (positions ascending): each thread first loads its
-// kSampleIter positions, then issues all 3 x kSampleIter gathers before it uses any of them.
-// A round inside one segment counts into the block's shared histogram, one atomic per distinct
-// bin per warp (lanes with equal bins found by __match_any_sync); the block flushes it to the
-// segment's global histogram when it moves on to another segment and at its end. A round that
-// spans segments (rare: many small segments) adds straight to the global histograms.
-constexpr int kSampleIter = 8;
-constexpr int kSampleBlocksPerSm = 4;
-constexpr uint32_t kSampleRound = (uint32_t)kThreads * kSampleIter;
+// A scattered 4-byte load costs a whole DRAM burst, so this gather is bound by the bursts in
+// flight: every thread issues its kSamplePerThread x 3 gathers before it uses any of them, and
+// the grid holds one block per kThreads x kSamplePerThread samples, so that many blocks stay
+// resident. (Persistent blocks walking rounds of 8 samples per thread, 24 gathers in flight,
+// kept fewer warps resident and measured slower.) A block inside one segment counts into a
+// shared histogram, one atomic per distinct bin per warp (lanes with equal bins found by
+// __match_any_sync), and flushes it to the segment's global histogram at its end.
+constexpr int kSamplePerThread = 4;
 
-__global__ void __launch_bounds__(kThreads, kSampleBlocksPerSm) k_sample(Args a) {
+__global__ void __launch_bounds__(kThreads) k_sample(Args a) {
     __shared__ uint32_t s_hist[kHistBins];
-    // abort is only raised by earlier kernels of the call: every thread reads the same value
-    if (ld_relaxed_u32((const uint32_t*)&a.ctl->abort)) return;
-    const uint32_t total = a.ctl->total_samples;
-    if ((uint64_t)blockIdx.x * kSampleRound >= total) return;
-    for (int b = threadIdx.x; b < kHistBins; b += kThreads) s_hist[b] = 0;
+    __shared__ int s_seg0, s_seg1, s_skip;
+    if (threadIdx.x == 0) s_skip = a.ctl->abort;
     __syncthreads();
+    if (s_skip) return;
+    const uint32_t total = a.ctl->total_samples;
+    const uint64_t chunk0 = (uint64_t)blockIdx.x * kThreads * kSamplePerThread;
+    if (chunk0 >= total) return;
+    for (int b = threadIdx.x; b < kHistBins; b += kThreads) s_hist[b] = 0;
+    const uint64_t chunk_end = umin64(total, chunk0 + kThreads * kSamplePerThread);
+    if (threadIdx.x == 0) {
+        s_seg0 = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)chunk0);
+        s_seg1 = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)(chunk_end - 1));
+    }
+    __syncthreads();
+    const bool uniform = (s_seg0 == s_seg1);
     const int lane = threadIdx.x & 31;
-    int cur = -1;  // the segment s_hist counts for (the same in every thread of the block)
-    for (uint64_t c0 = (uint64_t)blockIdx.x * kSampleRound; c0 < total;
-         c0 += (uint64_t)gridDim.x * kSampleRound) {
-        const uint64_t c1 = umin64(total, c0 + kSampleRound);
-        // the round's first and last segment: the same search in every thread (cached words)
-        const int s0 = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)c0);
-        const int s1 = upper_bound_minus1(a.samp_off, a.nseg, (uint32_t)(c1 - 1));
-        const bool uniform = (s0 == s1);
-        if (uniform && s0 != cur) {  // block-uniform: flush the previous segment's counts
-            if (cur >= 0) {
-                BlockHist h{s_hist, cur};
-                h.flush(a.histA, kHistBins);
-            }
-            cur = s0;
-        }
-        uint32_t pos[kSampleIter];
+    float gv[kSamplePerThread], uv[kSamplePerThread], vv[kSamplePerThread];
+    int sg[kSamplePerThread];
 #pragma unroll
-        for (int r = 0; r < kSampleIter; ++r) {
-            const uint64_t j = c0 + (uint64_t)r * kThreads + threadIdx.x;
-            pos[r] = j < c1 ? __ldcs(a.spos + j) : 0u;  // the sample positions, ascending
-        }
-        float gv[kSampleIter], uv[kSampleIter], vv[kSampleIter];
-#pragma unroll
-        for (int r = 0; r < kSampleIter; ++r) {
-            const uint64_t j = c0 + (uint64_t)r * kThreads + threadIdx.x;
-            if (j < c1) {
-                gv[r] = __ldg(a.g + pos[r]);
-                uv[r] = __ldg(a.u + pos[r]);
-                vv[r] = __ldg(a.v + pos[r]);
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < kSampleIter; ++r) {
-            const uint64_t j = c0 + (uint64_t)r * kThreads + threadIdx.x;
-            const bool valid = j < c1;
-            uint32_t bin = 0;
-            int s = s0;
-            if (valid) {
-                // a round that crosses segments searches only its own segment range
-                if (!uniform)
-                    s = s0 + upper_bound_minus1(a.samp_off + s0, s1 - s0 + 1, (uint32_t)j);
-                float uu = uv[r], vn = vv[r];
-                accumulate(gv[r], uu, vn, a.hp.momentum, a.segs[s].scale, a.hp.leak);
-                const uint32_t key = key_of(vn);
-                a.skeys[j] = key;
-                bin = key >> 20;
-            }
-            if (uniform) {  // block-uniform branch: every lane of the warp is here
-                const unsigned m = __ballot_sync(kFull, valid);
-                if (valid) {
-                    const unsigned peers = __match_any_sync(m, bin);
-                    if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], (uint32_t)__popc(peers));
-                }
-            } else if (valid) {
-                atomicAdd(&a.histA[(size_t)s * kHistBins + bin], 1u);
-            }
+    for (int r = 0; r < kSamplePerThread; ++r) {
+        const uint64_t jg = chunk0 + r * kThreads + threadIdx.x;
+        sg[r] = -1;
+        if (jg < chunk_end) {
+            // a chunk that crosses segments searches only its own segment range
+            const int s = uniform ? s_seg0
+                                  : s_seg0 + upper_bound_minus1(a.samp_off + s_seg0,
+                                                                s_seg1 - s_seg0 + 1, (uint32_t)jg);
+            const uint32_t pos = a.spos[jg];  // the sample positions in ascending order
+            gv[r] = __ldg(a.g + pos);
+            uv[r] = a.u[pos];
+            vv[r] = a.v[pos];
+            sg[r] = s;
         }
     }
-    if (cur >= 0) {
-        BlockHist h{s_hist, cur};
+#pragma unroll
+    for (int r = 0; r < kSamplePerThread; ++r) {
+        const uint64_t jg = chunk0 + r * kThreads + threadIdx.x;
+        const bool valid = sg[r] >= 0;
+        uint32_t bin = 0;
+        if (valid) {
+            float uu = uv[r], vn = vv[r];
+            accumulate(gv[r], uu, vn, a.hp.momentum, a.segs[sg[r]].scale, a.hp.leak);
+            const uint32_t key = key_of(vn);
+            a.skeys[jg] = key;
+            bin = key >> 20;
+        }
+        if (uniform) {  // block-uniform branch: every lane of the warp is here
+            const unsigned m = __ballot_sync(kFull, valid);
+            if (valid) {
+                const unsigned peers = __match_any_sync(m, bin);
+                if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], (uint32_t)__popc(peers));
+            }
+        } else if (valid) {
+            atomicAdd(&a.histA[(size_t)sg[r] * kHistBins + bin], 1u);
+        }
+    }
+    if (uniform) {
+        BlockHist h{s_hist, s_seg0};
         h.flush(a.histA, kHistBins);
     }
 }
@@ -2441,8 +2418,8 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     const bool selects = hp.mode != DGC_SELECT_ADACOMP;
     if (selects) {
         coop((const void*)k_cache, cooperative_grid(2, sms));
-        const uint64_t sgrid = std::min<uint64_t>((L.max_samples + kSampleRound - 1) / kSampleRound,
-                                                  (uint64_t)sms * kSampleBlocksPerSm);
+        const uint64_t sgrid = (L.max_samples + kThreads * kSamplePerThread - 1) /
+                               (kThreads * kSamplePerThread);
         L1(k_sample, (unsigned)sgrid, kThreads, a);
     }
     set_kernel_attributes();

@@ -1,20 +1,24 @@
 """A host model of the GPU clipping sum's integer steps (CPU only).
 
-The kernels `k_clip_tiles` and `k_clip_round` sum the squares of a segment exactly. Per
-4096-entry tile, each of 256 threads holds 16 entries and sums their squares in two 64-bit
-bands below its own largest entry: an entry with e' = e_band + d (d <= 6) adds the 64-bit
-product of its significand shifted left by d with itself, (m 2^d)^2 = m^2 4^d, which needs
-m 2^d to fit 32 bits. The thread's largest e' is read off its largest |x| bits (a thread that
-holds inf or NaN counts as 254). The block adds the band sums into a 128-bit window anchored
-68 bits below the tile's largest square. Anything lower goes to 32-bit digits held in 64-bit
-words, first per block, then per segment. One thread per segment then propagates the carries
-and rounds once to binary64.
+The kernels `k_clip_tiles` and `k_clip_round` sum the squares of a segment exactly. The
+segment is cut into 4096-entry tiles; each block of the grid takes a contiguous range of the
+tiles. In a tile, warp w holds entries [512 w, 512 w + 512), 16 per thread, and each thread sums
+its squares in two 64-bit bands below its own largest entry: an entry with e' = e_band + d
+(d <= 6) adds the 64-bit product of its significand shifted left by d with itself,
+(m 2^d)^2 = m^2 4^d, which needs m 2^d to fit 32 bits. The thread's largest e' is read off its
+largest |x| bits (a thread that holds inf or NaN counts as 254). The warp adds its threads' band
+sums into a 128-bit window anchored 68 bits below its largest square. Anything lower, and the
+warp's window itself, goes to the block's 32-bit digits held in 64-bit words (shared memory).
+When a block is done with the segment, its digits, carries propagated, are added to the
+segment's words in global memory. One thread per segment then propagates the carries and
+rounds once to binary64.
 
 This model takes the same steps with Python integers and asserts the bounds the kernels rely
-on: a shifted significand below 2^30, a band sum below 2^64, a window term below 2^118 and the
-window below 2^127, and a word below 2^55. Its S must equal the oracle's, the exact sum rounded
-once (the DGC review's local gradient clipping; the pages fix no order of summation). It checks
-the scheme; the GPU parity tests check the kernels themselves against the oracle, S included.
+on: a shifted significand below 2^30, a band sum below 2^64, a window term below 2^118 and a
+warp window below 2^124, a block word below 2^56 and a global word below 2^42. Its S must equal
+the oracle's, the exact sum rounded once (the DGC review's local gradient clipping; the pages
+fix no order of summation). It checks the scheme; the GPU parity tests check the kernels
+themselves against the oracle, S included.
 """
 import math
 import struct
@@ -22,7 +26,8 @@ import struct
 import numpy as np
 import pytest
 
-TILE, THREADS, PER = 4096, 256, 16
+TILE, THREADS, PER, WARP = 4096, 256, 16, 32
+GRID = 608  # blocks of the kernel's grid (4 per SM on 152 SMs)
 DIGITS = 20  # 32-bit digits of X = sum M 2^(2e'-2) < 2^586
 
 
@@ -35,71 +40,76 @@ def _digits_add(words, i, sh, x):
     words[i + 2] += hi >> 32
 
 
-def _tile(seg_words, bits):
-    """One block's work on one tile (|x| bits, zero-padded to 4096); returns its inf/NaN flags."""
+def _tile(block_words, bits):
+    """One tile (|x| bits, zero-padded to 4096) into a block's digits; returns inf/NaN flags."""
     bits = list(bits) + [0] * (TILE - len(bits))
     threads = [bits[PER * t:PER * t + PER] for t in range(THREADS)]
     # the thread's largest e' from its largest |x| bits; inf or NaN counts as 254
     et = [max(min(max(th) >> 23, 254), 1) for th in threads]
-    em = max(et)
-    lo = max(2 * em - 68, 0)  # the window's lowest bit of X
-    low = [0] * DIGITS
-    window, flags = 0, 0
+    flags = 0
+    for w0 in range(0, THREADS, WARP):
+        em = max(et[w0:w0 + WARP])
+        lo = max(2 * em - 68, 0)  # the warp window's lowest bit of X
+        window = 0
 
-    def place(v, bit):
-        nonlocal window, flags
-        if v == 0:
-            return
-        if bit >= lo:
-            assert v << (bit - lo) < 2**118
-            window += v << (bit - lo)
-        else:
-            flags |= 1
-            _digits_add(low, bit >> 5, bit & 31, v)
+        def place(v, bit):
+            nonlocal window
+            if v == 0:
+                return
+            if bit >= lo:
+                assert v << (bit - lo) < 2**118
+                window += v << (bit - lo)
+            else:
+                _digits_add(block_words, bit >> 5, bit & 31, v)
 
-    for t, th in enumerate(threads):
-        if any((a >> 23) == 255 for a in th):  # a thread holding inf or NaN: entry by entry
+        for t in range(w0, w0 + WARP):
+            th = threads[t]
+            if any((a >> 23) == 255 for a in th):  # a thread holding inf or NaN: entry by entry
+                for a in th:
+                    e = a >> 23
+                    if e == 255:
+                        flags |= 4 if a & 0x7FFFFF else 2
+                        continue
+                    m = (a & 0x7FFFFF) | 0x800000 if e else a
+                    place(m * m, 2 * max(e, 1) - 2)
+                continue
+            ea = max(et[t], 7) - 6  # band 1: e' in [ea, ea + 6]
+            eb = max(ea, 8) - 7     # band 2: e' in [eb, ea - 1]
+            A1 = A2 = 0
             for a in th:
-                e = a >> 23
-                if e == 255:
-                    flags |= 4 if a & 0x7FFFFF else 2
-                    continue
-                m = (a & 0x7FFFFF) | 0x800000 if e else a
-                place(m * m, 2 * max(e, 1) - 2)
-            continue
-        ea = max(et[t], 7) - 6  # band 1: e' in [ea, ea + 6]
-        eb = max(ea, 8) - 7     # band 2: e' in [eb, ea - 1]
-        A1 = A2 = 0
-        for a in th:
-            ep = max(a >> 23, 1)
-            m = a - ((ep - 1) << 23)  # the significand, hidden bit included when normal
-            assert m < 2**24
-            if ep >= eb:
-                sh = ep - (ea if ep >= ea else eb)
-                assert 0 <= sh <= 6
-                mm = m << sh
-                assert mm < 2**30
-                if ep >= ea:
-                    A1 += mm * mm
-                else:
-                    A2 += mm * mm
-            elif m:
-                flags |= 1
-                _digits_add(low, (2 * ep - 2) >> 5, (2 * ep - 2) & 31, m * m)
-        assert A1 < 2**64 and A2 < 2**64
-        place(A1, 2 * ea - 2)
-        place(A2, 2 * eb - 2)
-    assert window < 2**127
-    _digits_add(seg_words, lo >> 5, lo & 31, window & (2**64 - 1))
-    _digits_add(seg_words, (lo >> 5) + 2, lo & 31, window >> 64)
-    if flags & 1:  # the block's low words, carries propagated first
-        carry = 0
-        for j in range(DIGITS):
-            s = low[j] + carry
-            seg_words[j] += s & 0xFFFFFFFF
-            carry = s >> 32
-        assert carry == 0
-    return flags & 6
+                ep = max(a >> 23, 1)
+                m = a - ((ep - 1) << 23)  # the significand, hidden bit included when normal
+                assert m < 2**24
+                if ep >= eb:
+                    sh = ep - (ea if ep >= ea else eb)
+                    assert 0 <= sh <= 6
+                    mm = m << sh
+                    assert mm < 2**30
+                    if ep >= ea:
+                        A1 += mm * mm
+                    else:
+                        A2 += mm * mm
+                elif m:
+                    _digits_add(block_words, (2 * ep - 2) >> 5, (2 * ep - 2) & 31, m * m)
+            assert A1 < 2**64 and A2 < 2**64
+            place(A1, 2 * ea - 2)
+            place(A2, 2 * eb - 2)
+        assert window < 2**124
+        _digits_add(block_words, lo >> 5, lo & 31, window & (2**64 - 1))
+        _digits_add(block_words, (lo >> 5) + 2, lo & 31, window >> 64)
+    return flags
+
+
+def _flush(seg_words, block_words):
+    """A block's digits, carries propagated, into the segment's words (one add per digit)."""
+    assert max(block_words) < 2**56
+    carry = 0
+    for j in range(DIGITS):
+        s = block_words[j] + carry
+        seg_words[j] += s & 0xFFFFFFFF
+        carry = s >> 32
+        block_words[j] = 0
+    assert carry == 0
 
 
 def _round(words):
@@ -126,12 +136,19 @@ def _round(words):
     return math.ldexp(mant, low - 298)
 
 
-def model_sumsq(g):
+def model_sumsq(g, grid=GRID):
+    """One segment through the kernels' steps: its tiles shared out as contiguous ranges over
+    the blocks of a grid (as many as tiles, at most `grid`)."""
     bits = (np.asarray(g, np.float32).view(np.uint32) & 0x7FFFFFFF).tolist()
+    tiles = [bits[t0:t0 + TILE] for t0 in range(0, len(bits), TILE)]
     words, flags = [0] * DIGITS, 0
-    for t0 in range(0, len(bits), TILE):
-        flags |= _tile(words, bits[t0:t0 + TILE])
-    assert max(words) < 2**55
+    G = max(1, min(len(tiles), grid))
+    for b in range(G):
+        block = [0] * DIGITS
+        for c in range(len(tiles) * b // G, len(tiles) * (b + 1) // G):
+            flags |= _tile(block, tiles[c])
+        _flush(words, block)
+    assert max(words) < 2**42
     if flags & 4:
         return math.nan
     if flags & 2:
@@ -142,7 +159,7 @@ def model_sumsq(g):
 def _cases():
     rng = np.random.default_rng(31)
     out = []
-    for n in (1, 17, 4096, 5000):
+    for n in (1, 17, 4096, 5000, 40_003):  # the last spans ten tiles over several blocks
         out.append(("normal", (rng.standard_normal(n) * 1e-3).astype(np.float32)))
         out.append(("60 binades", (rng.standard_normal(n) * 2.0 ** rng.integers(-30, 30, n))
                     .astype(np.float32)))
@@ -165,6 +182,16 @@ def _cases():
 
 @pytest.mark.parametrize("name,g", _cases(), ids=lambda x: x if isinstance(x, str) else "")
 def test_kernel_scheme_reaches_the_oracle(orc, name, g):
-    want, got = orc.sumsq(g), model_sumsq(g)
-    assert (math.isnan(want) and math.isnan(got)) or \
-        struct.pack("<d", want) == struct.pack("<d", got), (name, want, got)
+    want = orc.sumsq(g)
+    for grid in (GRID, 1, 2):  # one block per tile, one block for all tiles, two blocks
+        got = model_sumsq(g, grid)
+        assert (math.isnan(want) and math.isnan(got)) or \
+            struct.pack("<d", want) == struct.pack("<d", got), (name, grid, want, got)
+
+
+def test_block_words_bound_at_the_largest_share():
+    # the most tiles a block of the 608-block grid sums for one segment (n < 2^32 entries, so
+    # fewer than 2^20 tiles), each adding at most 8 x 2 + 4096 shared adds of under 2^33 to a word
+    tiles_per_block = -(-(2**20) // GRID) + 1
+    assert tiles_per_block * (8 * 2 + 4096) * 2**33 < 2**56
+    assert GRID * 2**32 < 2**42  # one add of a 32-bit digit per block
