@@ -33,7 +33,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kEncBlocks = 512;
 constexpr int kEncPer = 4;
-constexpr int kDecChunk = 2048;  // tokens per position chunk (8 per thread)
+constexpr int kDecChunk = 4096;  // tokens per position chunk (16 per thread)
 constexpr int kDecTile = 4096;   // dense entries per output tile
 constexpr int kDecCap = 1024;    // tokens staged in shared memory at a time
 constexpr uint32_t kEscPos = 0xFFFFFFFFu;
@@ -278,10 +278,11 @@ __global__ void k_dec_init(DecArgs a) {
     }
 }
 
-__global__ void __launch_bounds__(kThreads) k_dec_pos(DecArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) k_dec_pos(DecArgs a) {
     __shared__ uint64_t s_scan[33];
+    __shared__ uint64_t s_lb64[33];
+    __shared__ uint32_t s_lb32[2];
     __shared__ uint32_t s_chunk;
-    __shared__ uint64_t s_base;
     if (threadIdx.x == 0) s_chunk = atomicAdd(&a.ctl->ticket, 1u);
     __syncthreads();
     const uint64_t c = s_chunk;
@@ -298,41 +299,47 @@ __global__ void __launch_bounds__(kThreads) k_dec_pos(DecArgs a) {
     const uint64_t tok1 = umin64(d.T, tok0 + kDecChunk);
     const uint16_t* runs = reinterpret_cast<const uint16_t*>(d.ptr + d.runs_off);
     constexpr int kPer = kDecChunk / kThreads;
-    uint32_t adv[kPer];
+    static_assert(kPer % 2 == 0 && kPer <= 32, "two 16-bit advances per word, one escape bit each");
+    // each token's advance (an escape skips 65535, another token run + 1 <= 65535) in 16 bits,
+    // two per word, and which tokens are escapes
+    uint32_t adv2[kPer / 2];
+    uint32_t esc = 0;
     uint64_t mine = 0;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
         const uint64_t j = tok0 + (uint64_t)threadIdx.x * kPer + i;
-        adv[i] = 0;
+        uint32_t adv = 0;
         if (j < tok1) {
             const uint32_t r = runs[j];
-            adv[i] = (r == kRunEscape) ? kRunEscape : r + 1;
+            adv = (r == kRunEscape) ? kRunEscape : r + 1;
+            if (r == kRunEscape) esc |= 1u << i;
         }
-        mine += adv[i];
+        if (i & 1) adv2[i / 2] |= adv << 16;
+        else adv2[i / 2] = adv;
+        mine += adv;
     }
     uint64_t agg;
     const uint64_t ex = block_excl_scan<kThreads>(mine, s_scan, &agg);
-    if (threadIdx.x < 32) {
-        uint64_t base = 0;
-        if (lc == 0) {
-            if (threadIdx.x == 0) st_relaxed(&a.st[c], kFlagInc | agg);
-        } else {
-            base = lookback_exclusive(a.st, (uint32_t)c, agg, a.spin_limit, a.status, nullptr);
-        }
-        if (threadIdx.x == 0) s_base = base;
+    // a message's first chunk starts at position -1; the others look back over their
+    // predecessors with the whole block (kThreads of them per round trip)
+    uint64_t base = 0;
+    if (lc == 0) {
+        if (threadIdx.x == 0) st_relaxed(&a.st[c], kFlagInc | agg);
+    } else {
+        base = block_lookback<kThreads>(a.st, (uint32_t)c, agg, a.spin_limit, a.status, nullptr,
+                                        s_lb32, s_lb64);
     }
-    __syncthreads();
-    uint64_t P = s_base + ex;  // advances before this thread's first token
+    uint64_t P = base + ex;  // advances before this thread's first token
     bool bad = false;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
         const uint64_t j = tok0 + (uint64_t)threadIdx.x * kPer + i;
         if (j >= tok1) break;
         const int64_t prev = (int64_t)P - 1;  // position of the previous token
-        P += adv[i];
+        P += (i & 1) ? (adv2[i / 2] >> 16) : (adv2[i / 2] & 0xFFFFu);
         const int64_t p = (int64_t)P - 1;
         if ((uint64_t)p >= a.n) bad = true;
-        a.pos[d.tok_base + j] = (runs[j] == kRunEscape) ? kEscPos : (uint32_t)p;
+        a.pos[d.tok_base + j] = ((esc >> i) & 1u) ? kEscPos : (uint32_t)p;
         // tiles whose first token of this message is j
         int64_t t0 = (prev < 0) ? 0 : prev / kDecTile + 1;
         int64_t t1 = p / kDecTile;
@@ -462,11 +469,7 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
             if (threadIdx.x < nw && cnt > 0) {
                 const DecStream& d = a.tab[wb + threadIdx.x];
                 const uint32_t at = (uint32_t)ex;
-#pragma unroll 4
-                for (uint32_t q = 0; q < cnt; ++q) {
-                    const uint64_t j = (uint64_t)first + q;
-                    const uint32_t p = a.pos[d.tok_base + j];
-                    const uint32_t raw = dec_value(a, d, j);
+                auto stage = [&](uint32_t q, uint32_t p, uint32_t raw) {
                     const bool in = p != kEscPos && p >= p0 && p < p0 + len;
                     if (kInt) {
                         if (in) {
@@ -478,6 +481,22 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
                         s_val[at + q] = raw;
                         s_msg[at + q] = (uint32_t)threadIdx.x;
                     }
+                };
+                // the first kBatch tokens' loads all in flight before any is used
+                constexpr uint32_t kBatch = 8;
+                uint32_t pb[kBatch], rb[kBatch];
+#pragma unroll
+                for (uint32_t q = 0; q < kBatch; ++q)
+                    if (q < cnt) {
+                        pb[q] = a.pos[d.tok_base + first + q];
+                        rb[q] = dec_value(a, d, (uint64_t)first + q);
+                    }
+#pragma unroll
+                for (uint32_t q = 0; q < kBatch; ++q)
+                    if (q < cnt) stage(q, pb[q], rb[q]);
+                for (uint32_t q = kBatch; q < cnt; ++q) {
+                    const uint64_t j = (uint64_t)first + q;
+                    stage(q, a.pos[d.tok_base + j], dec_value(a, d, j));
                 }
             }
             __syncthreads();

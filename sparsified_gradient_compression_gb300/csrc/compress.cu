@@ -101,6 +101,9 @@ constexpr int kSqLimbs = 10;   // 640-bit exact sum of squares, 64-bit limbs (wh
 constexpr int kSqDigits = 20;  // the same sum as 32-bit digits, each in a 64-bit word
 constexpr int kSqWords = kSqDigits + 1;  // + one word of flags (2: +inf seen, 4: NaN seen)
 constexpr int kHistBins = 2048;
+// DGC pass: a streaming tile with at most this many candidates stores them as sent (v, and u with
+// masking, zeroed) and keeps their values in its slots; the emit step puts back the unsent ones
+constexpr uint32_t kSpecSlots = 64;
 constexpr uint64_t kExactSamplePpb = 10000000;    // exact mode samples 1% to bound t from below
 constexpr uint32_t kExactWholeBelow = 8192;       // smaller segments: every entry is a candidate
 
@@ -148,7 +151,7 @@ struct Ctl {
     uint32_t ncomp;         // sample keys kept by the sample select's second level
     uint32_t bar_count;     // grid barrier of the cooperative select: arrivals, generation
     uint32_t bar_gen;
-    uint32_t pad;
+    uint32_t unspec;        // the speculative zeros were undone (exact mode's re-compaction)
 };
 
 // Header of the sample-position cache kept in the workspace between calls.
@@ -162,8 +165,8 @@ constexpr int kBucketShift = 10;  // cache order: 1024-entry buckets, segment by
 struct Layout {
     size_t ctl, scache, segs, seg_start, samp_off, clip_off, cand_off, clip_acc, skeys, spos,
         bcount, histA, histB;
-    size_t st_collect, st_compact, st_emit, cidx, sidx, tcount, tseg, eseg, clip_cnt, dlist,
-        binmax, total;
+    size_t st_collect, st_compact, st_emit, cidx, sidx, sval, su, tcount, tseg, eseg, clip_cnt,
+        dlist, binmax, total;
     uint64_t max_samples, max_clip_tiles, fused_tiles, emit_tiles, ptiles, cgroups, nbuckets,
         max_bins;
 };
@@ -177,6 +180,7 @@ struct HostParams {
     uint64_t seed;
     float bin_inv;  // AdaComp: 1/bin rounded to binary32 (used while bin < the tile length)
     float leak;     // v <- fma(leak, v, u); 1 is the plain sum
+    uint32_t nospec;  // no speculative sends (a caller-given index set: no candidates)
 };
 
 int check_params(const dgc_params* p, HostParams* hp) {
@@ -246,6 +250,10 @@ Layout make_layout(int64_t n, int32_t nseg, const HostParams& hp) {
     L.st_emit = take(sizeof(uint64_t) * (size_t)(L.emit_tiles + 1));
     L.cidx = take(sizeof(uint32_t) * (size_t)un);
     L.sidx = take(sizeof(uint32_t) * (size_t)un);
+    const size_t spec_slots =
+        (hp.bin || hp.nospec) ? 0 : (size_t)L.ptiles * kSpecSlots;  // DGC selection only
+    L.sval = take(sizeof(float) * spec_slots);
+    L.su = take(sizeof(float) * spec_slots);
     L.tcount = take(sizeof(uint32_t) * (size_t)(L.ptiles + 1));
     L.tseg = take(sizeof(uint32_t) * (size_t)(L.ptiles + 1));
     L.eseg = take(sizeof(uint32_t) * 2 * (size_t)(L.emit_tiles + 1));
@@ -304,6 +312,8 @@ struct Args {
     uint32_t* cidx;   // candidates, ascending index
     uint32_t* sidx;   // per-tile candidate slots of the streaming pass
     float* cval;      // candidate values v[cidx[f]] (in sidx's memory, once the slots are moved)
+    float* sval;      // DGC pass: per tile with <= kSpecSlots candidates, their v values, by rank
+    float* su;        // ... and their u values (kept with masking)
     uint32_t* tcount; // per-tile candidate counts, then (k_collect) each tile's first position
     uint32_t* tseg;   // streaming tile t starts in segment tseg[t]; tseg[ptiles] = nseg - 1
     uint32_t* eseg;   // emit tile t's candidates lie in segments [eseg[2t], eseg[2t + 1]]
@@ -508,6 +518,13 @@ __device__ double limbs_round(const unsigned long long* x) {
     return __longlong_as_double((long long)bits);
 }
 
+// x << sh for any sh: PTX shl.b32 gives 0 for shift amounts past 31
+__device__ __forceinline__ uint32_t shl32(uint32_t x, uint32_t sh) {
+    uint32_t r;
+    asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(sh));
+    return r;
+}
+
 // (w1:w0) += (p1:p0), 128 bits
 __device__ __forceinline__ void add128(unsigned long long& w0, unsigned long long& w1,
                                        unsigned long long p0, unsigned long long p1) {
@@ -528,7 +545,7 @@ __device__ __forceinline__ void add128(unsigned long long& w0, unsigned long lon
 // 2^33). When the block moves to another segment, and at its end, one thread propagates the
 // carries of the shared words into 32-bit digits and adds those to the segment's words in global
 // memory (each below 2^32, at most one add per block and segment).
-__global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
+__global__ void __launch_bounds__(kThreads, 4) k_clip_tiles(Args a) {
     __shared__ unsigned long long s_dig[kSqDigits];  // the block's share of the current segment
     __shared__ uint32_t s_flags;                     // 2: +inf seen; 4: NaN seen
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -615,29 +632,32 @@ __global__ void __launch_bounds__(kThreads) k_clip_tiles(Args a) {
             // go to the shared digits one by one after the loop
             const uint32_t ea = max(et, 7u) - 6u;
             const uint32_t eb = max(ea, 8u) - 7u;
+            // A band holds normal entries only (eb >= 1): there the significand is the fraction
+            // with its hidden bit. Band membership is read off the raw exponent e, so zeros and
+            // subnormals (e = 0) join the entries below the bands.
             unsigned long long A1 = 0ull, A2 = 0ull;
             bool below = false;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const uint32_t ax = xb[i];
-                const uint32_t ep = max(ax >> 23, 1u);
-                const uint32_t m = ax - ((ep - 1u) << 23);  // significand (hidden bit if normal)
-                const bool in1 = ep >= ea, in2 = ep >= eb;
-                const uint32_t sh = ep - (in1 ? ea : eb);   // <= 6 whenever in2
-                const uint32_t mm = m << (sh & 7u);
+                const uint32_t e = ax >> 23;
+                const uint32_t m = (ax & 0x7FFFFFu) | 0x800000u;
+                const bool in1 = e >= ea, in2 = e >= eb;
+                const uint32_t sh = e - (in1 ? ea : eb);  // <= 6 in a band, anything outside
+                const uint32_t mm = shl32(m, sh);         // (0 for shifts past 31: unused)
                 const unsigned long long V = (unsigned long long)mm * mm;
                 if (in1) A1 += V;
                 else if (in2) A2 += V;
-                below |= !in2 && m != 0u;
+                below |= !in2 && ax != 0u;
             }
             if (below) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const uint32_t ax = xb[i];
-                    const uint32_t ep = max(ax >> 23, 1u);
-                    const uint32_t m = ax - ((ep - 1u) << 23);
-                    if (ep < eb && m != 0u) {
-                        const int at = 2 * (int)ep - 2;
+                    const uint32_t e = ax >> 23;
+                    if (e < eb && ax != 0u) {
+                        const uint32_t m = e ? ((ax & 0x7FFFFFu) | 0x800000u) : ax;
+                        const int at = 2 * (int)max(e, 1u) - 2;
                         digits_add(s_dig, at >> 5, at & 31, (unsigned long long)m * m);
                     }
                 }
@@ -1517,6 +1537,26 @@ __device__ __forceinline__ void stream_compute(const Args& a, const float* sg, u
     }
 }
 
+// Row r of a thread's updated u and v back to memory: one 16-byte store each, entry by entry
+// in the ragged last tile.
+__device__ __forceinline__ void store_uv(const Args& a, uint64_t base, uint32_t len, int r,
+                                         int tid, const float4& u4, const float4& v4) {
+    const uint32_t off = 4u * (r * kThreads + tid);
+    if (off + 4 <= len) {
+        *reinterpret_cast<float4*>(a.u + base + off) = u4;
+        *reinterpret_cast<float4*>(a.v + base + off) = v4;
+    } else {
+        const float* u2 = reinterpret_cast<const float*>(&u4);
+        const float* v2 = reinterpret_cast<const float*>(&v4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (off + e < len) {
+                a.u[base + off + e] = u2[e];
+                a.v[base + off + e] = v2[e];
+            }
+    }
+}
+
 // kSel 0: candidates are the entries at or above the segment's threshold key (DGC). kSel 1
 // (AdaComp): candidates are the entries at the largest key of their bin within the tile; the
 // tile also raises each bin's global maximum, and the emit step keeps the candidates that
@@ -1742,7 +1782,6 @@ __global__ void __launch_bounds__(kThreads, stream_blocks_per_sm<kSel>()) k_stre
         uint32_t word[kPRows];
 #pragma unroll
         for (int r = 0; r < kPRows; ++r) {
-            const uint32_t off = 4u * (r * kThreads + tid);
             uint32_t x = ((flags >> (4 * r)) & 0xFu) << (4 * (lane & 7));
             x |= __shfl_xor_sync(kFull, x, 1);
             x |= __shfl_xor_sync(kFull, x, 2);
@@ -1752,19 +1791,7 @@ __global__ void __launch_bounds__(kThreads, stream_blocks_per_sm<kSel>()) k_stre
             const uint32_t rc = __shfl_sync(kFull, pc, 0) + __shfl_sync(kFull, pc, 8) +
                                 __shfl_sync(kFull, pc, 16) + __shfl_sync(kFull, pc, 24);
             if (lane == 0) s_rc[it & 1][r * kWarps + warp] = rc;
-            if (off + 4 <= len) {
-                *reinterpret_cast<float4*>(a.u + base + off) = uu[r];
-                *reinterpret_cast<float4*>(a.v + base + off) = vv[r];
-            } else {
-                const float* u2 = reinterpret_cast<const float*>(&uu[r]);
-                const float* v2 = reinterpret_cast<const float*>(&vv[r]);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (off + e < len) {
-                        a.u[base + off + e] = u2[e];
-                        a.v[base + off + e] = v2[e];
-                    }
-            }
+            if constexpr (kSel != 0) store_uv(a, base, len, r, tid, uu[r], vv[r]);
         }
         __syncthreads();  // the stage's data is in registers, the per-(row, warp) counts in place
         if (tid == 0) {
@@ -1775,6 +1802,11 @@ __global__ void __launch_bounds__(kThreads, stream_blocks_per_sm<kSel>()) k_stre
         const uint32_t cv = (lane < kPRows * kWarps) ? s_rc[it & 1][lane] : 0u;
         const uint32_t cinc = warp_incl_scan(cv);
         const uint32_t tile_total = __shfl_sync(kFull, cinc, 31);
+        // DGC pass: a tile with few candidates (nearly every tile at high sparsity) sends them
+        // speculatively -- v (and u, with masking) is stored as 0 there, the values go to the
+        // tile's kSpecSlots value slots -- so the emit step need not scatter the zeros; it puts
+        // back the few candidates the selection then leaves out
+        const bool spec = (kSel == 0) && tile_total <= kSpecSlots;
 #pragma unroll
         for (int r = 0; r < kPRows; ++r) {  // every lane joins the shuffles, candidates or not
             const uint32_t f4 = (flags >> (4 * r)) & 0xFu;
@@ -1789,13 +1821,25 @@ __global__ void __launch_bounds__(kThreads, stream_blocks_per_sm<kSel>()) k_stre
             before += (grp > 0 ? p0 : 0) + (grp > 1 ? p1 : 0) + (grp > 2 ? p2 : 0);
             const uint32_t sh = 4u * (lane & 7);
             if (f4) {
+                float* up = reinterpret_cast<float*>(&uu[r]);
+                float* vp = reinterpret_cast<float*>(&vv[r]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     if (f4 & (1u << e)) {
                         const uint32_t rank = before + __popc(word[r] & ((1u << (sh + e)) - 1u));
                         a.sidx[base + rank] = (uint32_t)(base + 4u * (r * kThreads + tid) + e);
+                        if (spec) {
+                            const size_t slot = (size_t)tile * kSpecSlots + rank;
+                            a.sval[slot] = vp[e];
+                            vp[e] = 0.0f;
+                            if (a.hp.mask) {
+                                a.su[slot] = up[e];
+                                up[e] = 0.0f;
+                            }
+                        }
                     }
             }
+            if constexpr (kSel == 0) store_uv(a, base, len, r, tid, uu[r], vv[r]);
         }
         if (tid == 0) a.tcount[tile] = tile_total;
     }
@@ -1902,13 +1946,29 @@ __global__ void __launch_bounds__(kThreads) k_collect_copy(Args a) {
     }
 }
 
-// Every candidate's value v[cidx[f]], gathered once by the whole grid into cval (the slot
-// array's memory, free once k_collect / k_collect_copy have moved the slots): the selects and
-// the emit step then read values in list order, instead of each block gathering its segment's
-// share from one SM.
+// The value slot of candidate f (list position; index idx) when its streaming tile sent it
+// speculatively (kept its v and u there and stored zeros), else -1: AdaComp, tiles with more than
+// kSpecSlots candidates, and every tile once the exact mode's re-compaction has undone the zeros.
+// After k_collect, tcount[t] is tile t's first list position, and its candidates follow in rank
+// order, so f - tcount[t] is the rank the streaming pass gave f.
+__device__ __forceinline__ int64_t spec_slot(const Args& a, uint64_t f, uint32_t idx,
+                                             uint32_t total, bool unspec) {
+    if (a.hp.bin || a.hp.nospec || unspec) return -1;
+    const uint32_t t = idx / kPTile;
+    const uint32_t first = a.tcount[t];
+    const uint32_t next = (t + 1 < (uint32_t)a.ptiles) ? a.tcount[t + 1] : total;
+    if (next - first > kSpecSlots) return -1;
+    return (int64_t)t * kSpecSlots + (int64_t)(f - first);
+}
+
+// Every candidate's value, gathered once by the whole grid into cval (the slot array's memory,
+// free once k_collect / k_collect_copy have moved the slots): from its tile's value slots when
+// it was sent speculatively (v holds 0 there), else from v. The selects and the emit step then
+// read values in list order, instead of each block gathering its segment's share from one SM.
 __global__ void __launch_bounds__(kThreads) k_cval(Args a) {
     if (ld_relaxed_u32((const uint32_t*)&a.ctl->abort)) return;
     const uint64_t total = a.ctl->total_cand;
+    const bool unspec = ld_relaxed_u32(&a.ctl->unspec) != 0;
     const uint64_t stride = (uint64_t)gridDim.x * kThreads;
     constexpr int kB = 4;  // gathers in flight per thread
     for (uint64_t f0 = (uint64_t)blockIdx.x * kThreads + threadIdx.x; f0 < total; f0 += kB * stride) {
@@ -1917,11 +1977,37 @@ __global__ void __launch_bounds__(kThreads) k_cval(Args a) {
         for (int r = 0; r < kB; ++r) idx[r] = (f0 + r * stride < total) ? a.cidx[f0 + r * stride] : 0u;
         float x[kB];
 #pragma unroll
-        for (int r = 0; r < kB; ++r) x[r] = (f0 + r * stride < total) ? a.v[idx[r]] : 0.0f;
+        for (int r = 0; r < kB; ++r) {
+            const uint64_t f = f0 + r * stride;
+            x[r] = 0.0f;
+            if (f < total) {
+                const int64_t slot = spec_slot(a, f, idx[r], (uint32_t)total, unspec);
+                x[r] = slot >= 0 ? a.sval[slot] : a.v[idx[r]];
+            }
+        }
 #pragma unroll
         for (int r = 0; r < kB; ++r)
             if (f0 + r * stride < total) a.cval[f0 + r * stride] = x[r];
     }
+}
+
+// Exact mode, only when a segment's sampled bound admitted fewer than k candidates: before the
+// re-compaction reads v again, every speculatively sent candidate gets its v and u back, and no
+// later kernel of the call treats any tile as speculative.
+__global__ void __launch_bounds__(kThreads) k_unspec(Args a) {
+    if (ld_relaxed_u32((const uint32_t*)&a.ctl->abort) || !ld_relaxed_u32(&a.ctl->any_failed))
+        return;
+    const uint32_t total = a.ctl->total_cand;
+    for (uint64_t f = (uint64_t)blockIdx.x * kThreads + threadIdx.x; f < total;
+         f += (uint64_t)gridDim.x * kThreads) {
+        const uint32_t idx = a.cidx[f];
+        const int64_t slot = spec_slot(a, f, idx, total, false);
+        if (slot >= 0) {
+            a.v[idx] = a.sval[slot];
+            if (a.hp.mask) a.u[idx] = a.su[slot];
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) a.ctl->unspec = 1;
 }
 
 // ------------------------------------------------------------------- candidate ranges
@@ -2030,6 +2116,7 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
     __syncthreads();
     const bool ok = s_ok;
     const uint32_t total = a.ctl->total_cand;
+    const bool unspec = ld_relaxed_u32(&a.ctl->unspec) != 0;
     const uint32_t ntiles = (total + kEmitTile - 1) / kEmitTile;
     while (ok) {
         if (threadIdx.x == 0) s_tile = atomicAdd(&a.ctl->ticket_emit, 1u);
@@ -2111,8 +2198,17 @@ __global__ void __launch_bounds__(kThreads) k_emit(Args a) {
                     a.out_idx[pos] = idx[q];
                     a.out_val[pos] = val[q];
                 }
-                a.v[idx[q]] = 0.0f;
-                if (a.hp.mask) a.u[idx[q]] = 0.0f;
+                if (spec_slot(a, i, idx[q], total, unspec) < 0) {  // not yet stored as sent
+                    a.v[idx[q]] = 0.0f;
+                    if (a.hp.mask) a.u[idx[q]] = 0.0f;
+                }
+            } else {
+                // a candidate the selection leaves out: put back what a speculative send stored
+                const int64_t slot = spec_slot(a, i, idx[q], total, unspec);
+                if (slot >= 0) {
+                    a.v[idx[q]] = val[q];
+                    if (a.hp.mask) a.u[idx[q]] = a.su[slot];
+                }
             }
         }
         {
@@ -2278,6 +2374,8 @@ Args make_args(const float* g, float* u, float* v, int64_t n, const int64_t* seg
     a.cidx = reinterpret_cast<uint32_t*>(w + L.cidx);
     a.sidx = reinterpret_cast<uint32_t*>(w + L.sidx);
     a.cval = reinterpret_cast<float*>(w + L.sidx);
+    a.sval = reinterpret_cast<float*>(w + L.sval);
+    a.su = reinterpret_cast<float*>(w + L.su);
     a.tcount = reinterpret_cast<uint32_t*>(w + L.tcount);
     a.tseg = reinterpret_cast<uint32_t*>(w + L.tseg);
     a.eseg = reinterpret_cast<uint32_t*>(w + L.eseg);
@@ -2449,6 +2547,7 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
     L1(k_collect_copy, (unsigned)sms * 8, kThreads, a);
     L1(k_candoff, 1, 1024, a, 0);
     if (hp.mode == DGC_SELECT_EXACT) {
+        L1(k_unspec, (unsigned)sms * 8, kThreads, a);
         L1(k_recompact, (unsigned)L.fused_tiles, kThreads, a);
         L1(k_candoff, 1, 1024, a, 1);
     }
@@ -2482,6 +2581,7 @@ extern "C" int dgc_compress_shared(const float* g, float* u, float* v, int64_t n
     hp.mode = DGC_SELECT_EXACT;
     hp.d_ppb = 0;
     hp.bin = 0;
+    hp.nospec = 1;
     if (!seg_off || !count || !status || !ws) return DGC_EINVAL;
     if (max_count > 0 && (!idx || !out_val)) return DGC_EINVAL;
     if (n > 0 && (!g || !u || !v || !aligned16(g) || !aligned16(u) || !aligned16(v)))

@@ -77,19 +77,21 @@ def _tile(block_words, bits):
             eb = max(ea, 8) - 7     # band 2: e' in [eb, ea - 1]
             A1 = A2 = 0
             for a in th:
-                ep = max(a >> 23, 1)
-                m = a - ((ep - 1) << 23)  # the significand, hidden bit included when normal
-                assert m < 2**24
-                if ep >= eb:
-                    sh = ep - (ea if ep >= ea else eb)
+                e = a >> 23  # band membership by the raw exponent: zeros and subnormals below
+                if e >= eb:
+                    assert e >= 1
+                    m = (a & 0x7FFFFF) | 0x800000  # a normal entry's significand
+                    sh = e - (ea if e >= ea else eb)
                     assert 0 <= sh <= 6
                     mm = m << sh
                     assert mm < 2**30
-                    if ep >= ea:
+                    if e >= ea:
                         A1 += mm * mm
                     else:
                         A2 += mm * mm
-                elif m:
+                elif a:
+                    ep = max(e, 1)
+                    m = (a & 0x7FFFFF) | 0x800000 if e else a
                     _digits_add(block_words, (2 * ep - 2) >> 5, (2 * ep - 2) & 31, m * m)
             assert A1 < 2**64 and A2 < 2**64
             place(A1, 2 * ea - 2)
@@ -168,6 +170,9 @@ def _cases():
         c = rng.standard_normal(n).astype(np.float32)
         c[::7] = np.float32(1e-44)
         out.append(("subnormals among normals", c))
+        c = (rng.standard_normal(n) * 1e-39).astype(np.float32)  # tiny normals and subnormals
+        c[::5] = np.float32(0.0)
+        out.append(("near the subnormal range, with zeros", c))
         out.append(("largest binary32", np.full(n, np.finfo(np.float32).max, np.float32)))
         out.append(("least subnormal", np.full(n, np.float32(2.0**-149))))
         c = rng.standard_normal(n).astype(np.float32)

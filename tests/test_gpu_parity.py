@@ -348,6 +348,29 @@ def test_learner_compress_full_size():
                   mode=dgc.SELECT_EXACT, sparsity=0.999, momentum=0.9)
 
 
+@pytest.mark.parametrize("mode", [dgc.SELECT_EXACT, dgc.SELECT_SAMPLED])
+@pytest.mark.parametrize("mask", [True, False])
+def test_candidate_clusters_around_the_speculative_send_limit(mode, mask):
+    # Streaming tiles with at most 64 candidates store them as sent and keep their values aside;
+    # the emit step puts back the ones the selection leaves out, and other tiles are masked as
+    # before. Clusters of 55..75 large entries in 21 tiles put tiles on both sides of that limit
+    # (and exact mode's re-selection leaves some candidates out), next to tiles with a few.
+    n = 1 << 20
+    off = np.array([0, n])
+    rng = np.random.default_rng(77 + 2 * mode + mask)
+
+    def grads(t):
+        g = workloads.misc([90, mode, int(mask), t], n, 0.01)
+        for c, size in enumerate(range(55, 76)):
+            tile = 3 + 23 * c
+            at = tile * 2048 + np.sort(rng.choice(2048, size=size, replace=False))
+            g[at] = np.float32(50.0) * (1 + rng.random(size)).astype(np.float32)
+        return g
+
+    run_steps(grads, off, 3, mode=mode, sparsity=0.998, momentum=0.9, mask_momentum=mask,
+              sample_ratio=0.01, reselect_factor=1.3, seed=5)
+
+
 # --------------------------------------------------------------------- shapes and edges
 EDGE_N = [1, 3, 15, 17, 4095, 8191, 8192, 8193, 40_000, 100_003]
 
