@@ -196,6 +196,7 @@ int check_params(const dgc_params* p, HostParams* hp) {
     if (std::isnan(p->clip_norm)) return DGC_EINVAL;
     if (!(p->leak >= 0.0f && p->leak <= 1.0f)) return DGC_EINVAL;
     hp->leak = p->leak == 0.0f ? 1.0f : p->leak;  // 0: no filter
+    hp->nospec = 0;
     hp->mode = p->mode;
     hp->mask = (p->flags & DGC_FLAG_MASK_MOMENTUM) ? 1u : 0u;
     hp->clip_on = (p->clip_norm > 0.0f && !std::isinf(p->clip_norm)) ? 1u : 0u;
@@ -1806,7 +1807,7 @@ __global__ void __launch_bounds__(kThreads, stream_blocks_per_sm<kSel>()) k_stre
         // speculatively -- v (and u, with masking) is stored as 0 there, the values go to the
         // tile's kSpecSlots value slots -- so the emit step need not scatter the zeros; it puts
         // back the few candidates the selection then leaves out
-        const bool spec = (kSel == 0) && tile_total <= kSpecSlots;
+        const bool spec = (kSel == 0) && !a.hp.nospec && tile_total <= kSpecSlots;
 #pragma unroll
         for (int r = 0; r < kPRows; ++r) {  // every lane joins the shuffles, candidates or not
             const uint32_t f4 = (flags >> (4 * r)) & 0xFu;
@@ -1856,10 +1857,10 @@ constexpr uint32_t kCollectDirect = 16;  // a tile with at most this many candid
 constexpr uint32_t kCollectWarp = 256;   // up to this many: one warp; more: one block
 
 __global__ void __launch_bounds__(kThreads) k_collect(Args a) {
-    __shared__ uint32_t s_ex[kCGroup + 1];
     __shared__ uint32_t s_scan[33];
+    __shared__ uint64_t s_lb64[33];
+    __shared__ uint32_t s_lb32[2];
     __shared__ uint32_t s_group;
-    __shared__ uint64_t s_base;
     __shared__ int s_skip;
     const int tid = threadIdx.x;
     const uint32_t ntiles = (uint32_t)a.ptiles;
@@ -1876,15 +1877,9 @@ __global__ void __launch_bounds__(kThreads) k_collect(Args a) {
     const uint32_t c = (t < ntiles) ? a.tcount[t] : 0u;
     uint32_t total;
     const uint32_t ex = block_excl_scan<kThreads>(c, s_scan, &total);
-    s_ex[tid] = ex;
-    if (tid == 0) s_ex[kCGroup] = total;
-    if (tid < 32) {
-        const uint64_t b = lookback_exclusive(a.st_collect, grp, total, a.spin_limit, a.status,
-                                              &a.ctl->abort);
-        if (tid == 0) s_base = b;
-    }
-    __syncthreads();
-    const uint64_t gbase = s_base;
+    // the group's offset: a look-back walked by the whole block (kThreads groups per round trip)
+    const uint64_t gbase = block_lookback<kThreads>(a.st_collect, grp, total, a.spin_limit,
+                                                    a.status, &a.ctl->abort, s_lb32, s_lb64);
     // the tile's count becomes its first position in the list. A tile with few candidates (the
     // common case) has its slots copied by its own thread; the others are listed for
     // k_collect_copy, which spreads each over a whole block.
@@ -2318,7 +2313,7 @@ extern "C" void dgc_profile_stream_pass(dgc_event_t begin, dgc_event_t end) {
 
 extern "C" int dgc_compress_workspace(int64_t n, int32_t nseg, const dgc_params* params,
                                       size_t* bytes) {
-    HostParams hp;
+    HostParams hp{};
     if (!bytes || nseg < 1 || n < 0) return DGC_EINVAL;
     if (n > 0xFFFFFFFFll || nseg > (1 << 28)) return DGC_EUNSUPPORTED;
     const int rc = check_params(params, &hp);
@@ -2329,7 +2324,7 @@ extern "C" int dgc_compress_workspace(int64_t n, int32_t nseg, const dgc_params*
 
 extern "C" int dgc_compress_max_out(int64_t n, int32_t nseg, const dgc_params* params,
                                     int64_t* max_out) {
-    HostParams hp;
+    HostParams hp{};
     if (!max_out || nseg < 1 || n < 0) return DGC_EINVAL;
     if (n > 0xFFFFFFFFll || nseg > (1 << 28)) return DGC_EUNSUPPORTED;
     const int rc = check_params(params, &hp);
@@ -2462,7 +2457,7 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
                             float* out_val, int64_t out_cap, int64_t* out_count,
                             dgc_seg_stats* stats, int32_t* status, void* ws, size_t ws_bytes,
                             dgc_stream_t stream) {
-    HostParams hp;
+    HostParams hp{};
     if (n < 0 || nseg < 1) return DGC_EINVAL;
     if (n > 0xFFFFFFFFll || nseg > (1 << 28)) return DGC_EUNSUPPORTED;
     int rc = check_params(params, &hp);
@@ -2572,7 +2567,7 @@ extern "C" int dgc_compress_shared(const float* g, float* u, float* v, int64_t n
                                    const uint32_t* idx, const int64_t* count, int64_t max_count,
                                    float* out_val, int32_t* status, void* ws, size_t ws_bytes,
                                    dgc_stream_t stream) {
-    HostParams hp;
+    HostParams hp{};
     if (n < 0 || nseg < 1 || max_count < 0) return DGC_EINVAL;
     if (n > 0xFFFFFFFFll || nseg > (1 << 28)) return DGC_EUNSUPPORTED;
     int rc = check_params(params, &hp);
