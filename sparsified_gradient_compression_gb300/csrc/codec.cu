@@ -283,14 +283,18 @@ __global__ void __launch_bounds__(kThreads, 3) k_dec_pos(DecArgs a) {
     __shared__ uint64_t s_lb64[33];
     __shared__ uint32_t s_lb32[2];
     __shared__ uint32_t s_chunk;
+    __shared__ uint64_t s_cb[kThreads];  // the messages' first chunks, when W <= kThreads
     if (threadIdx.x == 0) s_chunk = atomicAdd(&a.ctl->ticket, 1u);
+    const bool staged = a.W <= kThreads;
+    if (staged && threadIdx.x < a.W) s_cb[threadIdx.x] = a.tab[threadIdx.x].chunk_base;
     __syncthreads();
     const uint64_t c = s_chunk;
-    // the message that owns chunk c
+    // the message that owns chunk c: the last one starting at or before c (empty ones own
+    // nothing), searched in shared memory (one parallel load instead of a chain of them)
     int lo = 0, hi = a.W;
-    while (hi - lo > 1) {  // the last message starting at or before c (empty ones own nothing)
+    while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (a.tab[mid].chunk_base <= c) lo = mid; else hi = mid;
+        if ((staged ? s_cb[mid] : a.tab[mid].chunk_base) <= c) lo = mid; else hi = mid;
     }
     const int w = lo;
     const DecStream d = a.tab[w];
@@ -390,6 +394,7 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
     __shared__ uint32_t s_off[kThreads + 1];
     __shared__ uint32_t s_first[kThreads];
     __shared__ uint64_t s_scan[33];
+    __shared__ uint32_t s_fill;  // staging slots claimed by the warps (one-pass path)
     float* s_acc = reinterpret_cast<float*>(s_accw);
     int32_t* s_acci = reinterpret_cast<int32_t*>(s_accw);
     if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
@@ -417,7 +422,100 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
                 s_acc[i] = (load && i < len) ? a.dense[p0 + i] : 0.0f;
         }
     }
-    for (int wb = 0; wb < a.W; wb += kThreads) {
+    if (threadIdx.x == 0) s_fill = 0;
+    __syncthreads();  // the cleared tile, s_minw and s_fill before any staging
+    // the staged tokens this thread owns in the rounds: slots tid + k kThreads
+    auto rounds = [&](uint32_t m) {
+        uint32_t act = 0;
+#pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+            if (i < m && s_pos[i] != kNoPos) act |= 1u << k;
+        }
+        // every position still owed a value takes the token of its smallest message; a
+        // barrier closes each round (s_minw is kNoPos everywhere between rounds)
+        do {
+#pragma unroll
+            for (int k = 0; k < kPerThread; ++k) {
+                const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+                if (act & (1u << k)) atomicMin(&s_minw[s_pos[i]], s_msg[i]);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < kPerThread; ++k) {
+                const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+                if (!(act & (1u << k))) continue;
+                const uint32_t lp = s_pos[i];
+                // the one token of the smallest message left at lp (another token there
+                // may already see the cleared word: it never equals a message index)
+                if (s_minw[lp] == s_msg[i]) {
+                    s_acc[lp] = __fadd_rn(s_acc[lp], __uint_as_float(s_val[i]));
+                    s_minw[lp] = kNoPos;
+                    act &= ~(1u << k);
+                }
+            }
+        } while (__syncthreads_or(act != 0));
+    };
+    // Up to kThreads messages: thread w owns message w. It reads the message's first and end
+    // token in this tile from the table; a warp scan places the warp's tokens, one shared atomic
+    // per warp claims a region of the staging slots, and every thread stages its own message's
+    // tokens there (integer messages are added at once: their sum does not depend on order). The
+    // order of the regions does not matter, since a round adds by message index. When the tile's
+    // tokens do not fit the staging slots, the chunked path below stages them message-major.
+    bool done = false;
+    if (a.W <= kThreads) {
+        const int w = threadIdx.x;
+        uint32_t cnt = 0, first = 0;
+        if (w < a.W && a.tab[w].T > 0) {
+            first = a.ts[t * a.W + w];
+            cnt = a.ts[(t + 1) * a.W + w] - first;
+        }
+        const int lane = threadIdx.x & 31;
+        const uint32_t incl = warp_incl_scan(cnt);
+        const uint32_t wtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        uint32_t base = 0;
+        if (lane == 31 && !kInt && wtot) base = atomicAdd(&s_fill, wtot);
+        base = __shfl_sync(0xFFFFFFFFu, base, 31);
+        const bool fits = kInt || base + wtot <= (uint32_t)kDecCap;
+        if (cnt > 0 && fits) {
+            const DecStream& d = a.tab[w];
+            const uint32_t at = base + incl - cnt;
+            auto stage = [&](uint32_t q, uint32_t p, uint32_t raw) {
+                const bool in = p != kEscPos && p >= p0 && p < p0 + len;
+                if (kInt) {
+                    if (in) {
+                        atomicAdd(&s_acci[p - p0], (int32_t)raw);
+                        s_touch[p - p0] = 1;
+                    }
+                } else {
+                    s_pos[at + q] = in ? (uint32_t)(p - p0) : kNoPos;
+                    s_val[at + q] = raw;
+                    s_msg[at + q] = (uint32_t)w;
+                }
+            };
+            constexpr uint32_t kBatch = 8;  // loads in flight before any is used
+            uint32_t pb[kBatch], rb[kBatch];
+#pragma unroll
+            for (uint32_t q = 0; q < kBatch; ++q)
+                if (q < cnt) {
+                    pb[q] = a.pos[d.tok_base + first + q];
+                    rb[q] = dec_value(a, d, (uint64_t)first + q);
+                }
+#pragma unroll
+            for (uint32_t q = 0; q < kBatch; ++q)
+                if (q < cnt) stage(q, pb[q], rb[q]);
+            for (uint32_t q = kBatch; q < cnt; ++q) {
+                const uint64_t j = (uint64_t)first + q;
+                stage(q, a.pos[d.tok_base + j], dec_value(a, d, j));
+            }
+        }
+        const bool overflow = __syncthreads_or(!fits);
+        if (!overflow) {
+            if (!kInt && s_fill > 0) rounds(s_fill);
+            done = true;
+        }
+    }
+    for (int wb = 0; !done && wb < a.W; wb += kThreads) {
         const int w = wb + threadIdx.x;
         uint32_t cnt = 0, first = 0;
         if (w < a.W && a.tab[w].T > 0) {
@@ -431,38 +529,6 @@ __global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
         if (threadIdx.x == 0) s_off[kThreads] = (uint32_t)total;
         __syncthreads();
         const int nw = min(kThreads, a.W - wb);
-        // the staged tokens this thread owns in the rounds: slots tid + k kThreads
-        auto rounds = [&](uint32_t m) {
-            uint32_t act = 0;
-#pragma unroll
-            for (int k = 0; k < kPerThread; ++k) {
-                const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
-                if (i < m && s_pos[i] != kNoPos) act |= 1u << k;
-            }
-            // every position still owed a value takes the token of its smallest message; a
-            // barrier closes each round (s_minw is kNoPos everywhere between rounds)
-            do {
-#pragma unroll
-                for (int k = 0; k < kPerThread; ++k) {
-                    const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
-                    if (act & (1u << k)) atomicMin(&s_minw[s_pos[i]], s_msg[i]);
-                }
-                __syncthreads();
-#pragma unroll
-                for (int k = 0; k < kPerThread; ++k) {
-                    const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
-                    if (!(act & (1u << k))) continue;
-                    const uint32_t lp = s_pos[i];
-                    // the one token of the smallest message left at lp (another token there
-                    // may already see the cleared word: it never equals a message index)
-                    if (s_minw[lp] == s_msg[i]) {
-                        s_acc[lp] = __fadd_rn(s_acc[lp], __uint_as_float(s_val[i]));
-                        s_minw[lp] = kNoPos;
-                        act &= ~(1u << k);
-                    }
-                }
-            } while (__syncthreads_or(act != 0));
-        };
         if (total <= kDecCap) {
             // one chunk (the common case): each message's own thread stages its few tokens at
             // the message's offset, so no token searches for its message
