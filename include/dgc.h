@@ -276,6 +276,28 @@ int dgc_decode_apply(const uint8_t* const* streams, const uint64_t* stream_bytes
                      float* w, int64_t n, float lr, int32_t* status, void* ws, size_t ws_bytes,
                      dgc_stream_t stream);
 
+/* The decoders with the message sizes in device memory. [DGC] Abstract (the learners' updates
+ * are exchanged and summed): a message's size is known on the device once the message is there,
+ * for instance after an all-gather of the sizes, or right after dgc_encode wrote it. These calls
+ * take the sizes from there, so nothing waits for them on the host, and with at most 96 messages
+ * the call enqueues only a memset and kernels (its message table travels in kernel parameters),
+ * so it can be captured in a CUDA graph together with dgc_compress and dgc_encode.
+ *   stream_bytes  device, W uint64 sizes (8-byte aligned); dgc_encode's out_bytes fits.
+ *   max_bytes     host, W upper bounds on those sizes (for instance dgc_encode_max_bytes of the
+ *                 encoder's max_count); the workspace is laid out for them.
+ * A size that no binary32 message can have, or that exceeds its bound, sets *status to
+ * DGC_ECORRUPT and leaves dense (w) as it was, like any malformed message. Everything else --
+ * arguments, order of the sum, results, errors -- as dgc_decode_accumulate / dgc_decode_apply.
+ * Workspace: dgc_decode_workspace_bound(W, max_bytes, n). */
+int dgc_decode_workspace_bound(int32_t W, const uint64_t* max_bytes, int64_t n, size_t* bytes);
+int dgc_decode_accumulate_dev(const uint8_t* const* streams, const uint64_t* stream_bytes,
+                              const uint64_t* max_bytes, int32_t W, float* dense, int64_t n,
+                              int32_t accumulate, int32_t* status, void* ws, size_t ws_bytes,
+                              dgc_stream_t stream);
+int dgc_decode_apply_dev(const uint8_t* const* streams, const uint64_t* stream_bytes,
+                         const uint64_t* max_bytes, int32_t W, float* w, int64_t n, float lr,
+                         int32_t* status, void* ws, size_t ws_bytes, dgc_stream_t stream);
+
 /* Workspace for the version-2 decoders: W messages of `bits`-bit values with the given sizes. */
 int dgc_decode_workspace_quant(int32_t W, const uint64_t* stream_bytes, int64_t n, int32_t bits,
                                size_t* bytes);

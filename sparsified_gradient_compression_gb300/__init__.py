@@ -18,6 +18,7 @@ __all__ = [
     "dgc_compress_workspace", "dgc_compress_max_out", "dgc_compress", "dgc_compress_noalloc",
     "dgc_encode_max_bytes", "dgc_encode_workspace", "dgc_encode",
     "dgc_decode_workspace", "dgc_decode_accumulate", "dgc_decode_apply",
+    "dgc_decode_workspace_bound", "dgc_decode_accumulate_dev", "dgc_decode_apply_dev",
     "dgc_encode_quant", "dgc_decode_workspace_quant", "dgc_decode_accumulate_quant",
     "dgc_decode_apply_quant", "dgc_compress_shared", "dgc_sum_shared_workspace",
     "dgc_sum_shared",
@@ -95,6 +96,10 @@ def lib():
         L.dgc_decode_workspace.argtypes = [i32, vp, i64, P(sz)]
         L.dgc_decode_accumulate.argtypes = [vp, vp, i32, vp, i64, i32, vp, vp, sz, vp]
         L.dgc_decode_apply.argtypes = [vp, vp, i32, vp, i64, ctypes.c_float, vp, vp, sz, vp]
+        L.dgc_decode_workspace_bound.argtypes = [i32, vp, i64, P(sz)]
+        L.dgc_decode_accumulate_dev.argtypes = [vp, vp, vp, i32, vp, i64, i32, vp, vp, sz, vp]
+        L.dgc_decode_apply_dev.argtypes = [vp, vp, vp, i32, vp, i64, ctypes.c_float, vp, vp, sz,
+                                           vp]
         f32 = ctypes.c_float
         L.dgc_encode_quant.argtypes = [vp, vp, vp, i64, i64, f32, i32, vp, vp, u64, vp, vp, vp,
                                        sz, vp]
@@ -120,6 +125,8 @@ def lib():
                   "dgc_compress_noalloc",
                   "dgc_encode_max_bytes", "dgc_encode_workspace", "dgc_encode",
                   "dgc_decode_workspace", "dgc_decode_accumulate", "dgc_decode_apply",
+                  "dgc_decode_workspace_bound", "dgc_decode_accumulate_dev",
+                  "dgc_decode_apply_dev",
                   "dgc_encode_quant", "dgc_decode_workspace_quant",
                   "dgc_decode_accumulate_quant", "dgc_decode_apply_quant",
                   "dgc_compress_shared", "dgc_sum_shared_workspace", "dgc_sum_shared",
@@ -276,6 +283,43 @@ def dgc_decode_apply(streams, stream_bytes, w, n: int, lr: float, status, ws,
                                          ctypes.cast(sizes, ctypes.c_void_p), W, _ptr(w), int(n),
                                          float(lr), _ptr(status), _ptr(ws), int(ws_bytes),
                                          _stream(stream)), "dgc_decode_apply")
+
+
+def dgc_decode_workspace_bound(max_bytes, n: int) -> int:
+    """Workspace of the _dev decoders for W messages of at most max_bytes[w] bytes each."""
+    W = len(max_bytes)
+    arr = (ctypes.c_uint64 * max(W, 1))(*[int(b) for b in max_bytes])
+    out = ctypes.c_size_t(0)
+    _check(lib().dgc_decode_workspace_bound(W, ctypes.cast(arr, ctypes.c_void_p), int(n),
+                                            ctypes.byref(out)), "dgc_decode_workspace_bound")
+    return out.value
+
+
+def dgc_decode_accumulate_dev(streams, stream_bytes, max_bytes, dense, n: int, accumulate: bool,
+                              status, ws, ws_bytes: int | None = None, stream=None) -> int:
+    """streams: device addresses or uint8 CUDA tensors; stream_bytes: a CUDA tensor of W 8-byte
+    sizes (int64 or uint64, e.g. dgc_encode's out_bytes); max_bytes: host bounds on them."""
+    W = len(max_bytes)
+    ptrs = (ctypes.c_void_p * max(W, 1))(*[_ptr(s) for s in streams])
+    bounds = (ctypes.c_uint64 * max(W, 1))(*[int(b) for b in max_bytes])
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    return _check(lib().dgc_decode_accumulate_dev(
+        ctypes.cast(ptrs, ctypes.c_void_p), _ptr(stream_bytes), ctypes.cast(bounds, ctypes.c_void_p),
+        W, _ptr(dense), int(n), 1 if accumulate else 0, _ptr(status), _ptr(ws), int(ws_bytes),
+        _stream(stream)), "dgc_decode_accumulate_dev")
+
+
+def dgc_decode_apply_dev(streams, stream_bytes, max_bytes, w, n: int, lr: float, status, ws,
+                         ws_bytes: int | None = None, stream=None) -> int:
+    """dgc_decode_apply with the message sizes in device memory (see dgc_decode_accumulate_dev)."""
+    W = len(max_bytes)
+    ptrs = (ctypes.c_void_p * max(W, 1))(*[_ptr(s) for s in streams])
+    bounds = (ctypes.c_uint64 * max(W, 1))(*[int(b) for b in max_bytes])
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    return _check(lib().dgc_decode_apply_dev(
+        ctypes.cast(ptrs, ctypes.c_void_p), _ptr(stream_bytes), ctypes.cast(bounds, ctypes.c_void_p),
+        W, _ptr(w), int(n), float(lr), _ptr(status), _ptr(ws), int(ws_bytes), _stream(stream)),
+        "dgc_decode_apply_dev")
 
 
 def dgc_encode_quant(idx, val, count, n: int, alpha: float, bits: int, v, out, out_bytes, status,

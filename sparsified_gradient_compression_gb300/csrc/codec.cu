@@ -35,7 +35,7 @@ constexpr int kEncBlocks = 512;
 constexpr int kEncPer = 4;
 constexpr int kDecChunk = 4096;  // tokens per position chunk (16 per thread)
 constexpr int kDecTile = 4096;   // dense entries per output tile
-constexpr int kDecCap = 1024;    // tokens staged in shared memory at a time
+constexpr int kDecCap = 512;     // tokens staged in shared memory at a time
 constexpr uint32_t kEscPos = 0xFFFFFFFFu;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -217,6 +217,25 @@ __global__ void __launch_bounds__(kThreads) k_enc_write(EncArgs a) {
     }
 }
 
+// tokens of a message of `bytes` bytes; false when no message of that kind has that size
+__host__ __device__ inline bool stream_tokens(uint64_t bytes, int qbits, uint64_t* T) {
+    if (bytes < 32) return false;
+    if (!qbits) {
+        const uint64_t t = (bytes - 32) / 6;
+        if (32 + 6 * t + ((t & 1) ? 2 : 0) != bytes) return false;
+        *T = t;
+        return true;
+    }
+    const uint64_t per = (uint64_t)qbits / 8 + 2;  // bytes per token; padding adds at most 4
+    const uint64_t t0 = (bytes - 32) / per;
+    for (uint64_t t = t0 > 2 ? t0 - 2 : 0; t <= t0; ++t)
+        if (q_size(t, qbits) == bytes) {
+            *T = t;
+            return true;
+        }
+    return false;
+}
+
 // ------------------------------------------------------------------------------ decode
 struct DecStream {
     const uint8_t* ptr;
@@ -247,6 +266,7 @@ struct DecArgs {
     uint32_t* pos;
     uint64_t* st;
     uint32_t* ts;  // (ntiles + 1) x W first-token table
+    const uint64_t* dev_bytes;  // the message sizes in device memory, or null (sizes on the host)
     uint64_t ntiles;
     uint64_t nchunks;
     uint32_t spin_limit;
@@ -258,16 +278,45 @@ __device__ __forceinline__ void mark_bad(const DecArgs& a, int w) {
     report(a.status, DGC_ECORRUPT);
 }
 
-// Zeroes the look-back words and checks every header (ctl was zeroed before this kernel).
-__global__ void k_dec_init(DecArgs a) {
+// The message table by value, for calls with at most kDecInline messages: it travels with the
+// launch (W + 1 entries within the 4 KB of kernel parameters), so no host memory is read when
+// the call replays from a CUDA graph. Larger calls copy the table to the workspace instead.
+constexpr int kDecInline = 96;
+struct DecTabInline {
+    DecStream e[kDecInline + 1];
+};
+static_assert(sizeof(DecTabInline) + sizeof(DecArgs) <= 4096, "within the kernel parameter space");
+
+// Zeroes the look-back words, writes the message table into the workspace when it comes with
+// the launch, and checks every header (ctl was zeroed before this kernel).
+__global__ void k_dec_init(DecArgs a, const __grid_constant__ DecTabInline t) {
     const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     for (uint64_t i = tid; i <= a.nchunks; i += stride) a.st[i] = 0;
+    const bool inl = a.W <= kDecInline;
+    DecStream* tab = const_cast<DecStream*>(a.tab);
+    if (inl)
+        for (uint64_t w = tid; w <= (uint64_t)a.W; w += stride) tab[w] = t.e[w];
     for (uint64_t w = tid; w < (uint64_t)a.W; w += stride) {
-        const DecStream d = a.tab[w];
+        DecStream d = inl ? t.e[w] : a.tab[w];  // (the same thread wrote tab[w] above)
+        a.bad[w] = 0;
+        if (a.dev_bytes) {
+            // sizes in device memory: the table holds each message's bound on T (from its bound
+            // on bytes); the real T comes from the size, which must be a message's and within
+            // the bound, else the call fails as for a malformed message
+            uint64_t T = 0;
+            if (!stream_tokens(a.dev_bytes[w], 0, &T) || T > d.T) {
+                tab[w].T = 0;
+                mark_bad(a, (int)w);
+                continue;
+            }
+            d.T = T;
+            d.runs_off = 32 + 4 * T;
+            tab[w].T = T;
+            tab[w].runs_off = d.runs_off;
+        }
         const uint64_t* h = reinterpret_cast<const uint64_t*>(d.ptr);
         const uint64_t h0 = h[0];
-        a.bad[w] = 0;
         bool ok = (uint32_t)h0 == kMagic && h[1] == a.n && h[2] == d.T;
         if (a.qbits)  // version 2: the receiver's width and alpha, bit for bit
             ok = ok && ((h0 >> 32) & 0xFFFFu) == 2u && (h0 >> 48) == (uint64_t)a.qbits &&
@@ -300,6 +349,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_dec_pos(DecArgs a) {
     const DecStream d = a.tab[w];
     const uint64_t lc = c - d.chunk_base;
     const uint64_t tok0 = lc * kDecChunk;
+    // with sizes in device memory the chunks are laid out for each message's bound on T: the
+    // chunks past its real end have nothing to do (and no later chunk of it looks back to them)
+    if (tok0 >= d.T && lc > 0) return;
     const uint64_t tok1 = umin64(d.T, tok0 + kDecChunk);
     const uint16_t* runs = reinterpret_cast<const uint16_t*>(d.ptr + d.runs_off);
     constexpr int kPer = kDecChunk / kThreads;
@@ -382,7 +434,7 @@ __device__ __forceinline__ float dequant(int32_t S, float alpha) {
 // order too.
 constexpr uint32_t kNoPos = 0xFFFFFFFFu;
 template <bool kInt>
-__global__ void __launch_bounds__(kThreads) k_dec_tiles(DecArgs a) {
+__global__ void __launch_bounds__(kThreads, 5) k_dec_tiles(DecArgs a) {
     constexpr int kPerThread = kDecCap / kThreads;  // staged tokens per thread
     static_assert(kPerThread * kThreads == kDecCap && kPerThread <= 32, "staging layout");
     __shared__ __align__(16) uint32_t s_accw[kDecTile];  // binary32 sums, or int32 sums
@@ -732,32 +784,16 @@ struct DecLayout {
     uint64_t sum_T, nchunks, ntiles;
 };
 
-// tokens of a message of `bytes` bytes; false when no message of that kind has that size
-bool stream_tokens(uint64_t bytes, int qbits, uint64_t* T) {
-    if (bytes < 32) return false;
-    if (!qbits) {
-        const uint64_t t = (bytes - 32) / 6;
-        if (32 + 6 * t + ((t & 1) ? 2 : 0) != bytes) return false;
-        *T = t;
-        return true;
-    }
-    const uint64_t per = (uint64_t)qbits / 8 + 2;  // bytes per token; padding adds at most 4
-    const uint64_t t0 = (bytes - 32) / per;
-    for (uint64_t t = t0 > 2 ? t0 - 2 : 0; t <= t0; ++t)
-        if (q_size(t, qbits) == bytes) {
-            *T = t;
-            return true;
-        }
-    return false;
-}
-
+// bounds: stream_bytes are upper bounds on binary32 messages' sizes (their T found on the
+// device); else the sizes themselves
 int dec_layout(int32_t W, const uint64_t* stream_bytes, int64_t n, int qbits, DecLayout* L,
-               std::vector<DecStream>* tab) {
+               std::vector<DecStream>* tab, bool bounds = false) {
     L->sum_T = 0;
     L->nchunks = 0;
     for (int w = 0; w < W; ++w) {
         uint64_t T;
-        if (!stream_tokens(stream_bytes[w], qbits, &T)) return DGC_ECORRUPT;
+        if (bounds) T = stream_bytes[w] >= 32 ? (stream_bytes[w] - 32) / 6 : 0;
+        else if (!stream_tokens(stream_bytes[w], qbits, &T)) return DGC_ECORRUPT;
         const uint64_t ro = qbits ? q_runs_offset(T, qbits) : 32 + 4 * T;
         if (tab) (*tab)[w] = DecStream{nullptr, T, L->sum_T, L->nchunks, ro};
         L->sum_T += T;
@@ -861,11 +897,11 @@ extern "C" int dgc_encode_quant(const uint32_t* idx, const float* val, const int
 
 namespace {
 int decode_workspace_impl(int32_t W, const uint64_t* stream_bytes, int64_t n, int32_t qbits,
-                          size_t* bytes) {
+                          size_t* bytes, bool bounds = false) {
     if (!bytes || W < 0 || n < 0 || (W > 0 && !stream_bytes)) return DGC_EINVAL;
     if (n > 0xFFFFFFFFll) return DGC_EUNSUPPORTED;
     DecLayout L;
-    const int rc = dec_layout(W, stream_bytes, n, qbits, &L, nullptr);
+    const int rc = dec_layout(W, stream_bytes, n, qbits, &L, nullptr, bounds);
     if (rc) return rc;
     *bytes = L.total;
     return DGC_OK;
@@ -877,6 +913,11 @@ extern "C" int dgc_decode_workspace(int32_t W, const uint64_t* stream_bytes, int
     return decode_workspace_impl(W, stream_bytes, n, 0, bytes);
 }
 
+extern "C" int dgc_decode_workspace_bound(int32_t W, const uint64_t* max_bytes, int64_t n,
+                                          size_t* bytes) {
+    return decode_workspace_impl(W, max_bytes, n, 0, bytes, true);
+}
+
 extern "C" int dgc_decode_workspace_quant(int32_t W, const uint64_t* stream_bytes, int64_t n,
                                           int32_t bits, size_t* bytes) {
     if (bits != 8 && bits != 16) return DGC_EINVAL;
@@ -884,10 +925,11 @@ extern "C" int dgc_decode_workspace_quant(int32_t W, const uint64_t* stream_byte
 }
 
 namespace {
+// dev_bytes: the message sizes in device memory (stream_bytes then holds host bounds on them)
 int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int32_t W,
                 float* dense, int64_t n, int32_t accumulate, int32_t apply, float lr,
                 int32_t qbits, float alpha, int32_t* status, void* ws, size_t ws_bytes,
-                dgc_stream_t stream) {
+                dgc_stream_t stream, const uint64_t* dev_bytes = nullptr) {
     if (W < 0 || n < 0) return DGC_EINVAL;
     if (n > 0xFFFFFFFFll) return DGC_EUNSUPPORTED;
     if (W > 0 && (!streams || !stream_bytes)) return DGC_EINVAL;
@@ -895,9 +937,10 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
     if (((uintptr_t)ws & 255u) != 0) return DGC_EINVAL;
     for (int w = 0; w < W; ++w)
         if (!streams[w] || ((uintptr_t)streams[w] & 15u) != 0) return DGC_EINVAL;
+    if (W > 0 && dev_bytes && ((uintptr_t)dev_bytes & 7u) != 0) return DGC_EINVAL;
     std::vector<DecStream> tab((size_t)W + 1);
     DecLayout L;
-    int rc = dec_layout(W, stream_bytes, n, qbits, &L, &tab);
+    int rc = dec_layout(W, stream_bytes, n, qbits, &L, &tab, dev_bytes != nullptr);
     if (rc) return rc;
     if (L.sum_T > 0xFFFFFFFFull) return DGC_EUNSUPPORTED;
     if (ws_bytes < L.total) return DGC_EINVAL;
@@ -919,19 +962,24 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
     a.pos = reinterpret_cast<uint32_t*>(p + L.pos);
     a.st = reinterpret_cast<uint64_t*>(p + L.st);
     a.ts = reinterpret_cast<uint32_t*>(p + L.ts);
+    a.dev_bytes = dev_bytes;
     a.ntiles = L.ntiles;
     a.nchunks = L.nchunks;
     a.spin_limit = kDefaultSpinLimit;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // the table of messages goes to the device with the call (a pageable copy: staged before
-    // this function returns, so the host vector may go away)
-    if (cudaMemcpyAsync(p + L.tab, tab.data(), sizeof(DecStream) * tab.size(),
-                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+    // the table of messages goes with the first kernel's parameters when it is small; else by a
+    // pageable copy (staged before this function returns, so the host vector may go away)
+    DecTabInline inl{};
+    if (W <= kDecInline) {
+        for (int w = 0; w <= W; ++w) inl.e[w] = tab[w];
+    } else if (cudaMemcpyAsync(p + L.tab, tab.data(), sizeof(DecStream) * tab.size(),
+                               cudaMemcpyHostToDevice, s) != cudaSuccess) {
         return DGC_ECUDA;
+    }
     if (cudaMemsetAsync(p + L.ctl, 0, sizeof(DecCtl), s) != cudaSuccess) return DGC_ECUDA;
     uint64_t launches = 0;
-    const uint64_t init_work = std::max<uint64_t>(L.nchunks + 1, (uint64_t)W);
-    k_dec_init<<<(unsigned)std::min<uint64_t>((init_work + 255) / 256, 1024), 256, 0, s>>>(a);
+    const uint64_t init_work = std::max<uint64_t>(L.nchunks + 1, (uint64_t)W + 1);
+    k_dec_init<<<(unsigned)std::min<uint64_t>((init_work + 255) / 256, 1024), 256, 0, s>>>(a, inl);
     ++launches;
     if (L.nchunks > 0) {
         k_dec_pos<<<(unsigned)L.nchunks, kThreads, 0, s>>>(a);
@@ -963,6 +1011,26 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
     return DGC_OK;
 }
 }  // namespace
+
+extern "C" int dgc_decode_accumulate_dev(const uint8_t* const* streams,
+                                         const uint64_t* stream_bytes, const uint64_t* max_bytes,
+                                         int32_t W, float* dense, int64_t n, int32_t accumulate,
+                                         int32_t* status, void* ws, size_t ws_bytes,
+                                         dgc_stream_t stream) {
+    if (W > 0 && !stream_bytes) return DGC_EINVAL;
+    return decode_impl(streams, max_bytes, W, dense, n, accumulate, 0, 0.0f, 0, 0.0f, status, ws,
+                       ws_bytes, stream, stream_bytes);
+}
+
+extern "C" int dgc_decode_apply_dev(const uint8_t* const* streams, const uint64_t* stream_bytes,
+                                    const uint64_t* max_bytes, int32_t W, float* w, int64_t n,
+                                    float lr, int32_t* status, void* ws, size_t ws_bytes,
+                                    dgc_stream_t stream) {
+    if (W > 0 && !stream_bytes) return DGC_EINVAL;
+    if (!std::isfinite(lr) || std::signbit(lr)) return DGC_EINVAL;
+    return decode_impl(streams, max_bytes, W, w, n, 0, 1, lr, 0, 0.0f, status, ws, ws_bytes,
+                       stream, stream_bytes);
+}
 
 extern "C" int dgc_decode_accumulate(const uint8_t* const* streams, const uint64_t* stream_bytes,
                                      int32_t W, float* dense, int64_t n, int32_t accumulate,

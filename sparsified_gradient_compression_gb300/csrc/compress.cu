@@ -1792,7 +1792,10 @@ __global__ void __launch_bounds__(kThreads, stream_blocks_per_sm<kSel>()) k_stre
             const uint32_t rc = __shfl_sync(kFull, pc, 0) + __shfl_sync(kFull, pc, 8) +
                                 __shfl_sync(kFull, pc, 16) + __shfl_sync(kFull, pc, 24);
             if (lane == 0) s_rc[it & 1][r * kWarps + warp] = rc;
-            if constexpr (kSel != 0) store_uv(a, base, len, r, tid, uu[r], vv[r]);
+            // rows without a candidate of this thread store now; the DGC pass stores the others
+            // once the tile's count has decided whether they are sent speculatively
+            if (kSel != 0 || ((flags >> (4 * r)) & 0xFu) == 0u)
+                store_uv(a, base, len, r, tid, uu[r], vv[r]);
         }
         __syncthreads();  // the stage's data is in registers, the per-(row, warp) counts in place
         if (tid == 0) {
@@ -1840,7 +1843,7 @@ __global__ void __launch_bounds__(kThreads, stream_blocks_per_sm<kSel>()) k_stre
                         }
                     }
             }
-            if constexpr (kSel == 0) store_uv(a, base, len, r, tid, uu[r], vv[r]);
+            if (kSel == 0 && f4) store_uv(a, base, len, r, tid, uu[r], vv[r]);
         }
         if (tid == 0) a.tcount[tile] = tile_total;
     }

@@ -662,6 +662,126 @@ def test_decode_collisions_and_crowded_tiles(case):
     assert same_bits(got, exp)
 
 
+@pytest.mark.parametrize("W", [1, 7, 64, 100])
+def test_decode_with_sizes_in_device_memory(W):
+    # The _dev decoders read each message's size from device memory and lay their workspace
+    # out for host bounds on the sizes; with up to 96 messages the table travels in kernel
+    # parameters, with more it is copied. Results must equal the host-size calls bit for bit.
+    rng = np.random.default_rng(500 + W)
+    n = int(rng.integers(1, 2_000_000))
+    msgs = []
+    for w in range(W):
+        k = 0 if (w % 5 == 3) else int(rng.integers(0, min(n, 30_000) + 1))  # some empty
+        idx = np.sort(rng.choice(n, size=k, replace=False)).astype(np.uint32)
+        val = (rng.standard_normal(k) * 10.0 ** rng.integers(-3, 3, k)).astype(np.float32)
+        msgs.append(oracle.encode(idx, val, n))
+    bufs = []
+    for m in msgs:
+        t = torch.zeros(len(m) + 16, dtype=torch.uint8, device="cuda")
+        t[: len(m)] = torch.frombuffer(bytearray(m), dtype=torch.uint8).cuda()
+        bufs.append(t)
+    sizes = [len(m) for m in msgs]
+    bounds = [sz + int(rng.integers(0, 3)) * 6 + int(rng.integers(0, 5)) for sz in sizes]
+    dsizes = torch.tensor(sizes, dtype=torch.int64, device="cuda")
+    ws_bytes = dgc.dgc_decode_workspace_bound(bounds, n)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    base = rng.standard_normal(n).astype(np.float32)
+    for acc in (False, True):
+        dense = dev_f32(base)
+        dgc.dgc_decode_accumulate_dev(bufs, dsizes, bounds, dense, n, acc, status, ws,
+                                      ws_bytes=ws_bytes)
+        assert dgc.dgc_read_status(status) == 0
+        rc, ref = decode(msgs, n, dense=dev_f32(base), accumulate=acc)
+        assert rc == 0 and same_bits(host_f32(dense), host_f32(ref)), acc
+        _, odense = oracle.decode_accumulate(msgs, n, dense=base, accumulate=acc)
+        assert same_bits(host_f32(dense), odense), acc
+    w = dev_f32(base)
+    dgc.dgc_decode_apply_dev(bufs, dsizes, bounds, w, n, 0.25, status, ws, ws_bytes=ws_bytes)
+    assert dgc.dgc_read_status(status) == 0
+    _, w_orc = oracle.decode_apply(msgs, n, base, np.float32(0.25))
+    assert same_bits(host_f32(w), w_orc)
+
+
+def test_decode_with_sizes_in_device_memory_rejects_bad_sizes():
+    n = 10_000
+    good = oracle.encode(np.array([5, 999, 4000], np.uint32),
+                         np.array([1.0, -2.0, 3.5], np.float32), n)
+    buf = torch.zeros(len(good) + 64, dtype=torch.uint8, device="cuda")
+    buf[: len(good)] = torch.frombuffer(bytearray(good), dtype=torch.uint8).cuda()
+    base = np.arange(n, dtype=np.float32)
+    for size, bound in ((len(good) + 1, len(good) + 64),  # no message has that size
+                        (len(good), len(good) - 6),       # above its bound
+                        (len(good) + 4, len(good) + 64),  # 4 tokens by size, the header says 3
+                        (31, 64)):                        # shorter than a header
+        dsizes = torch.tensor([size], dtype=torch.int64, device="cuda")
+        ws_bytes = dgc.dgc_decode_workspace_bound([bound], n)
+        ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        dense = dev_f32(base)
+        dgc.dgc_decode_accumulate_dev([buf], dsizes, [bound], dense, n, False, status, ws,
+                                      ws_bytes=ws_bytes)
+        assert dgc.dgc_read_status(status) == dgc.ECORRUPT, (size, bound)
+        assert same_bits(host_f32(dense), base), (size, bound)
+
+
+def test_whole_step_in_one_cuda_graph():
+    # compress, encode and a decode that reads the message size from device memory, captured as
+    # one CUDA graph and replayed on fresh gradients: every step against the oracle
+    n = 1_048_576
+    off = np.array([0, n])
+    pd, po = params_pair(mode=dgc.SELECT_SAMPLED, sparsity=0.999, momentum=0.9,
+                         sample_ratio=0.01, reselect_factor=1.3, seed=21)
+    comp = Compressor(n, off, pd)
+    enc = Encoder(comp.cap, n)
+    u_d = torch.zeros(n, device="cuda")
+    v_d = torch.zeros(n, device="cuda")
+    g_d = torch.zeros(n, device="cuda")
+    dense = torch.zeros(n, device="cuda")
+    bound = enc.cap
+    ws_bytes = dgc.dgc_decode_workspace_bound([bound], n)
+    dws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    dstatus = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step():
+        comp(g_d, u_d, v_d)
+        enc(comp.out_idx, comp.out_val, comp.out_count)
+        dgc.dgc_decode_accumulate_dev([enc.out], enc.out_bytes, [bound], dense, n, False, dstatus,
+                                      dws, ws_bytes=ws_bytes)
+
+    u_h = np.zeros(n, np.float32)
+    v_h = np.zeros(n, np.float32)
+
+    def check(t, g_h):
+        oidx, oval, _ = oracle.compress(g_h, u_h, v_h, off, po)
+        assert comp.status_code() == 0 and dgc.dgc_read_status(dstatus) == 0
+        msg = enc.message()
+        assert msg == oracle.encode(oidx, oval, n), t
+        _, odense = oracle.decode_accumulate([msg], n)
+        assert same_bits(host_f32(dense), odense), t
+        assert same_bits(host_f32(v_d), v_h) and same_bits(host_f32(u_d), u_h), t
+
+    g0 = workloads.gradient("single", 0)
+    g_d.copy_(dev_f32(g0))
+    step()  # one call outside capture: the sample cache and every lookup are set up
+    torch.cuda.synchronize()
+    check(0, g0)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for t in range(1, 4):
+        g = workloads.gradient("single", t)
+        g_d.copy_(dev_f32(g))
+        graph.replay()
+        torch.cuda.synchronize()
+        check(t, g)
+
+
 @pytest.mark.parametrize("acc", [False, True])
 def test_decode_single_message_both_modes(acc):
     # one message: the decoder clears dense (unless accumulating) and adds each value once
