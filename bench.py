@@ -289,9 +289,16 @@ class Pipeline:
                             self.msg_bytes, self.status, self.ews, max_count=self.cap,
                             out_cap=self.msg_cap, ws_bytes=self.ews_bytes)
 
-    def decode(self):
-        self.dgc.dgc_decode_accumulate_dev([self.msg], self.msg_bytes, [self.msg_cap], self.dense,
-                                           self.n, False, self.status, self.dws,
+    def bound(self, p) -> int:
+        """The largest message a compress call with params p can lead to: the decoder's bound."""
+        return self.dgc.dgc_encode_max_bytes(
+            self.dgc.dgc_compress_max_out(self.n, self.nseg, p), self.n)
+
+    def decode(self, p):
+        # the decoder's grids follow the bound on the message, so it is the bound of this
+        # step's sparsity (the warm-up schedule's lower sparsities have far larger ones)
+        self.dgc.dgc_decode_accumulate_dev([self.msg], self.msg_bytes, [self.bound(p)],
+                                           self.dense, self.n, False, self.status, self.dws,
                                            ws_bytes=self.dws_bytes)
 
     def message_size(self) -> int:
@@ -314,7 +321,7 @@ class Pipeline:
             with torch.cuda.graph(graphs[1], stream=side):
                 self.encode()
             with torch.cuda.graph(graphs[2], stream=side):
-                self.decode()
+                self.decode(p)
         torch.cuda.current_stream(self.dev).wait_stream(side)
         return graphs
 
@@ -338,7 +345,7 @@ class Pipeline:
         if graphs:
             graphs[2].replay()
         else:
-            self.decode()
+            self.decode(p)
         if ev:
             ev[3].record()
 
