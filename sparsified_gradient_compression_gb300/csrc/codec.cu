@@ -434,7 +434,7 @@ __device__ __forceinline__ float dequant(int32_t S, float alpha) {
 // order too.
 constexpr uint32_t kNoPos = 0xFFFFFFFFu;
 template <bool kInt>
-__global__ void __launch_bounds__(kThreads, 4) k_dec_tiles(DecArgs a) {
+__global__ void __launch_bounds__(kThreads, 5) k_dec_tiles(DecArgs a) {
     constexpr int kPerThread = kDecCap / kThreads;  // staged tokens per thread
     static_assert(kPerThread * kThreads == kDecCap && kPerThread <= 32, "staging layout");
     __shared__ __align__(16) uint32_t s_accw[kDecTile];  // binary32 sums, or int32 sums
@@ -450,48 +450,22 @@ __global__ void __launch_bounds__(kThreads, 4) k_dec_tiles(DecArgs a) {
     float* s_acc = reinterpret_cast<float*>(s_accw);
     int32_t* s_acci = reinterpret_cast<int32_t*>(s_accw);
     if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
+    const uint64_t t = blockIdx.x;
+    const uint64_t p0 = t * kDecTile;
+    const uint32_t len = (uint32_t)umin64(kDecTile, a.n - p0);
+    const bool vec = (len == kDecTile) && ((reinterpret_cast<uintptr_t>(a.dense) & 15u) == 0);
     const bool load = !kInt && a.accumulate && !a.apply;  // apply mode sums from +0
-    if (!kInt)  // kNoPos everywhere; every round restores the words it used
+    if (kInt) {
+        for (uint32_t i = threadIdx.x; i < kDecTile; i += kThreads) {
+            s_acci[i] = 0;
+            s_touch[i] = 0;
+        }
+    } else {
         for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
             reinterpret_cast<uint4*>(s_minw)[i] = make_uint4(kNoPos, kNoPos, kNoPos, kNoPos);
-    // Persistent blocks walk the tiles. With up to kThreads messages thread w keeps message w's
-    // table entry, and the first-token entries of its next tile are read while this one is
-    // summed.
-    const bool few = a.W <= kThreads;
-    // this thread's message: its bytes, its first token's index among all positions, its tokens
-    // (all below 2^32: the call checks the sum of T)
-    const uint8_t* m_ptr = nullptr;
-    uint32_t m_base = 0, m_T = 0;
-    if (few && (int)threadIdx.x < a.W) {
-        const DecStream d = a.tab[threadIdx.x];
-        m_ptr = d.ptr;
-        m_base = (uint32_t)d.tok_base;
-        m_T = (uint32_t)d.T;
-    }
-    auto tile_tokens = [&](uint64_t tt, uint32_t& first, uint32_t& cnt) {
-        first = 0;
-        cnt = 0;
-        if (few && tt < a.ntiles && (int)threadIdx.x < a.W && m_T > 0) {
-            first = a.ts[tt * a.W + threadIdx.x];
-            cnt = a.ts[(tt + 1) * a.W + threadIdx.x] - first;
-        }
-    };
-    uint32_t nfirst, ncnt;
-    tile_tokens(blockIdx.x, nfirst, ncnt);
-    for (uint64_t t = blockIdx.x; t < a.ntiles; t += gridDim.x) {
-        const uint64_t p0 = t * kDecTile;
-        const uint32_t len = (uint32_t)umin64(kDecTile, a.n - p0);
-        const bool vec = (len == kDecTile) && ((reinterpret_cast<uintptr_t>(a.dense) & 15u) == 0);
-        // the tile's sums start from +0 or, accumulating, from dense
-        if (kInt) {
-            for (uint32_t i = threadIdx.x; i < kDecTile; i += kThreads) {
-                s_acci[i] = 0;
-                s_touch[i] = 0;
-            }
-        } else if (vec && load) {
+        if (vec && load) {
             for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
-                reinterpret_cast<float4*>(s_acc)[i] =
-                    reinterpret_cast<const float4*>(a.dense + p0)[i];
+                reinterpret_cast<float4*>(s_acc)[i] = reinterpret_cast<const float4*>(a.dense + p0)[i];
         } else if (vec) {
             for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
                 reinterpret_cast<float4*>(s_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -499,64 +473,120 @@ __global__ void __launch_bounds__(kThreads, 4) k_dec_tiles(DecArgs a) {
             for (uint32_t i = threadIdx.x; i < kDecTile; i += kThreads)
                 s_acc[i] = (load && i < len) ? a.dense[p0 + i] : 0.0f;
         }
-        if (threadIdx.x == 0) s_fill = 0;
-        __syncthreads();  // the cleared tile, s_minw and s_fill before any staging
-        // the staged tokens this thread owns in the rounds: slots tid + k kThreads
-        auto rounds = [&](uint32_t m) {
-            uint32_t act = 0;
+    }
+    if (threadIdx.x == 0) s_fill = 0;
+    __syncthreads();  // the cleared tile, s_minw and s_fill before any staging
+    // the staged tokens this thread owns in the rounds: slots tid + k kThreads
+    auto rounds = [&](uint32_t m) {
+        uint32_t act = 0;
+#pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+            if (i < m && s_pos[i] != kNoPos) act |= 1u << k;
+        }
+        // every position still owed a value takes the token of its smallest message; a
+        // barrier closes each round (s_minw is kNoPos everywhere between rounds)
+        do {
 #pragma unroll
             for (int k = 0; k < kPerThread; ++k) {
                 const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
-                if (i < m && s_pos[i] != kNoPos) act |= 1u << k;
+                if (act & (1u << k)) atomicMin(&s_minw[s_pos[i]], s_msg[i]);
             }
-            // every position still owed a value takes the token of its smallest message; a
-            // barrier closes each round (s_minw is kNoPos everywhere between rounds)
-            do {
+            __syncthreads();
 #pragma unroll
-                for (int k = 0; k < kPerThread; ++k) {
-                    const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
-                    if (act & (1u << k)) atomicMin(&s_minw[s_pos[i]], s_msg[i]);
+            for (int k = 0; k < kPerThread; ++k) {
+                const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+                if (!(act & (1u << k))) continue;
+                const uint32_t lp = s_pos[i];
+                // the one token of the smallest message left at lp (another token there
+                // may already see the cleared word: it never equals a message index)
+                if (s_minw[lp] == s_msg[i]) {
+                    s_acc[lp] = __fadd_rn(s_acc[lp], __uint_as_float(s_val[i]));
+                    s_minw[lp] = kNoPos;
+                    act &= ~(1u << k);
                 }
-                __syncthreads();
-#pragma unroll
-                for (int k = 0; k < kPerThread; ++k) {
-                    const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
-                    if (!(act & (1u << k))) continue;
-                    const uint32_t lp = s_pos[i];
-                    // the one token of the smallest message left at lp (another token there
-                    // may already see the cleared word: it never equals a message index)
-                    if (s_minw[lp] == s_msg[i]) {
-                        s_acc[lp] = __fadd_rn(s_acc[lp], __uint_as_float(s_val[i]));
-                        s_minw[lp] = kNoPos;
-                        act &= ~(1u << k);
+            }
+        } while (__syncthreads_or(act != 0));
+    };
+    // Up to kThreads messages: thread w owns message w. It reads the message's first and end
+    // token in this tile from the table; a warp scan places the warp's tokens, one shared atomic
+    // per warp claims a region of the staging slots, and every thread stages its own message's
+    // tokens there (integer messages are added at once: their sum does not depend on order). The
+    // order of the regions does not matter, since a round adds by message index. When the tile's
+    // tokens do not fit the staging slots, the chunked path below stages them message-major.
+    bool done = false;
+    if (a.W <= kThreads) {
+        const int w = threadIdx.x;
+        uint32_t cnt = 0, first = 0;
+        if (w < a.W && a.tab[w].T > 0) {
+            first = a.ts[t * a.W + w];
+            cnt = a.ts[(t + 1) * a.W + w] - first;
+        }
+        const int lane = threadIdx.x & 31;
+        const uint32_t incl = warp_incl_scan(cnt);
+        const uint32_t wtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        uint32_t base = 0;
+        if (lane == 31 && !kInt && wtot) base = atomicAdd(&s_fill, wtot);
+        base = __shfl_sync(0xFFFFFFFFu, base, 31);
+        const bool fits = kInt || base + wtot <= (uint32_t)kDecCap;
+        if (cnt > 0 && fits) {
+            const DecStream& d = a.tab[w];
+            const uint32_t at = base + incl - cnt;
+            auto stage = [&](uint32_t q, uint32_t p, uint32_t raw) {
+                const bool in = p != kEscPos && p >= p0 && p < p0 + len;
+                if (kInt) {
+                    if (in) {
+                        atomicAdd(&s_acci[p - p0], (int32_t)raw);
+                        s_touch[p - p0] = 1;
                     }
+                } else {
+                    s_pos[at + q] = in ? (uint32_t)(p - p0) : kNoPos;
+                    s_val[at + q] = raw;
+                    s_msg[at + q] = (uint32_t)w;
                 }
-            } while (__syncthreads_or(act != 0));
-        };
-        // Up to kThreads messages: thread w owns message w. It reads the message's first and
-        // end token in this tile from the table; a warp scan places the warp's tokens, one
-        // shared atomic per warp claims a region of the staging slots, and every thread stages
-        // its own message's tokens there (integer messages are added at once: their sum does not
-        // depend on order). The order of the regions does not matter, since a round adds by
-        // message index. When the tile's tokens do not fit the staging slots, the chunked path
-        // below stages them message-major.
-        bool done = false;
-        if (few) {
-            const int w = threadIdx.x;
-            const uint32_t first = nfirst, cnt = ncnt;
-            tile_tokens(t + gridDim.x, nfirst, ncnt);  // the block's next tile, read ahead
-            const int lane = threadIdx.x & 31;
-            const uint32_t incl = warp_incl_scan(cnt);
-            const uint32_t wtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-            uint32_t base = 0;
-            if (lane == 31 && !kInt && wtot) base = atomicAdd(&s_fill, wtot);
-            base = __shfl_sync(0xFFFFFFFFu, base, 31);
-            const bool fits = kInt || base + wtot <= (uint32_t)kDecCap;
-            if (cnt > 0 && fits) {
-                DecStream d{};
-                d.ptr = m_ptr;
-                d.tok_base = m_base;
-                const uint32_t at = base + incl - cnt;
+            };
+            constexpr uint32_t kBatch = 8;  // loads in flight before any is used
+            uint32_t pb[kBatch], rb[kBatch];
+#pragma unroll
+            for (uint32_t q = 0; q < kBatch; ++q)
+                if (q < cnt) {
+                    pb[q] = a.pos[d.tok_base + first + q];
+                    rb[q] = dec_value(a, d, (uint64_t)first + q);
+                }
+#pragma unroll
+            for (uint32_t q = 0; q < kBatch; ++q)
+                if (q < cnt) stage(q, pb[q], rb[q]);
+            for (uint32_t q = kBatch; q < cnt; ++q) {
+                const uint64_t j = (uint64_t)first + q;
+                stage(q, a.pos[d.tok_base + j], dec_value(a, d, j));
+            }
+        }
+        const bool overflow = __syncthreads_or(!fits);
+        if (!overflow) {
+            if (!kInt && s_fill > 0) rounds(s_fill);
+            done = true;
+        }
+    }
+    for (int wb = 0; !done && wb < a.W; wb += kThreads) {
+        const int w = wb + threadIdx.x;
+        uint32_t cnt = 0, first = 0;
+        if (w < a.W && a.tab[w].T > 0) {
+            first = a.ts[t * a.W + w];
+            cnt = a.ts[(t + 1) * a.W + w] - first;
+        }
+        uint64_t total;
+        const uint64_t ex = block_excl_scan<kThreads>((uint64_t)cnt, s_scan, &total);
+        s_off[threadIdx.x] = (uint32_t)ex;
+        s_first[threadIdx.x] = first;
+        if (threadIdx.x == 0) s_off[kThreads] = (uint32_t)total;
+        __syncthreads();
+        const int nw = min(kThreads, a.W - wb);
+        if (total <= kDecCap) {
+            // one chunk (the common case): each message's own thread stages its few tokens at
+            // the message's offset, so no token searches for its message
+            if (threadIdx.x < nw && cnt > 0) {
+                const DecStream& d = a.tab[wb + threadIdx.x];
+                const uint32_t at = (uint32_t)ex;
                 auto stage = [&](uint32_t q, uint32_t p, uint32_t raw) {
                     const bool in = p != kEscPos && p >= p0 && p < p0 + len;
                     if (kInt) {
@@ -567,10 +597,11 @@ __global__ void __launch_bounds__(kThreads, 4) k_dec_tiles(DecArgs a) {
                     } else {
                         s_pos[at + q] = in ? (uint32_t)(p - p0) : kNoPos;
                         s_val[at + q] = raw;
-                        s_msg[at + q] = (uint32_t)w;
+                        s_msg[at + q] = (uint32_t)threadIdx.x;
                     }
                 };
-                constexpr uint32_t kBatch = 8;  // loads in flight before any is used
+                // the first kBatch tokens' loads all in flight before any is used
+                constexpr uint32_t kBatch = 8;
                 uint32_t pb[kBatch], rb[kBatch];
 #pragma unroll
                 for (uint32_t q = 0; q < kBatch; ++q)
@@ -586,152 +617,93 @@ __global__ void __launch_bounds__(kThreads, 4) k_dec_tiles(DecArgs a) {
                     stage(q, a.pos[d.tok_base + j], dec_value(a, d, j));
                 }
             }
-            const bool overflow = __syncthreads_or(!fits);
-            if (!overflow) {
-                if (!kInt && s_fill > 0) rounds(s_fill);
-                done = true;
-            }
-        }
-        for (int wb = 0; !done && wb < a.W; wb += kThreads) {
-            const int w = wb + threadIdx.x;
-            uint32_t cnt = 0, first = 0;
-            if (w < a.W && a.tab[w].T > 0) {
-                first = a.ts[t * a.W + w];
-                cnt = a.ts[(t + 1) * a.W + w] - first;
-            }
-            uint64_t total;
-            const uint64_t ex = block_excl_scan<kThreads>((uint64_t)cnt, s_scan, &total);
-            s_off[threadIdx.x] = (uint32_t)ex;
-            s_first[threadIdx.x] = first;
-            if (threadIdx.x == 0) s_off[kThreads] = (uint32_t)total;
             __syncthreads();
-            const int nw = min(kThreads, a.W - wb);
-            if (total <= kDecCap) {
-                // one chunk (the common case): each message's own thread stages its few tokens at
-                // the message's offset, so no token searches for its message
-                if (threadIdx.x < nw && cnt > 0) {
-                    const DecStream& d = a.tab[wb + threadIdx.x];
-                    const uint32_t at = (uint32_t)ex;
-                    auto stage = [&](uint32_t q, uint32_t p, uint32_t raw) {
-                        const bool in = p != kEscPos && p >= p0 && p < p0 + len;
-                        if (kInt) {
-                            if (in) {
-                                atomicAdd(&s_acci[p - p0], (int32_t)raw);
-                                s_touch[p - p0] = 1;
-                            }
-                        } else {
-                            s_pos[at + q] = in ? (uint32_t)(p - p0) : kNoPos;
-                            s_val[at + q] = raw;
-                            s_msg[at + q] = (uint32_t)threadIdx.x;
-                        }
-                    };
-                    // the first kBatch tokens' loads all in flight before any is used
-                    constexpr uint32_t kBatch = 8;
-                    uint32_t pb[kBatch], rb[kBatch];
-#pragma unroll
-                    for (uint32_t q = 0; q < kBatch; ++q)
-                        if (q < cnt) {
-                            pb[q] = a.pos[d.tok_base + first + q];
-                            rb[q] = dec_value(a, d, (uint64_t)first + q);
-                        }
-#pragma unroll
-                    for (uint32_t q = 0; q < kBatch; ++q)
-                        if (q < cnt) stage(q, pb[q], rb[q]);
-                    for (uint32_t q = kBatch; q < cnt; ++q) {
-                        const uint64_t j = (uint64_t)first + q;
-                        stage(q, a.pos[d.tok_base + j], dec_value(a, d, j));
-                    }
-                }
-                __syncthreads();
-                if (!kInt && total > 0) rounds((uint32_t)total);
-                continue;
-            }
-            for (uint32_t r0 = 0; r0 < total; r0 += kDecCap) {
-                const uint32_t m = (uint32_t)umin64(kDecCap, total - r0);
-#pragma unroll
-                for (int k = 0; k < kPerThread; ++k) {
-                    const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
-                    if (i >= m) break;
-                    const uint32_t f = r0 + i;
-                    int l = 0, h = nw;  // message of flattened token f
-                    while (h - l > 1) {
-                        const int mid = (l + h) >> 1;
-                        if (s_off[mid] <= f) l = mid; else h = mid;
-                    }
-                    const DecStream& d = a.tab[wb + l];
-                    const uint64_t j = s_first[l] + (f - s_off[l]);
-                    const uint32_t p = a.pos[d.tok_base + j];
-                    const uint32_t raw = dec_value(a, d, j);
-                    const bool in = p != kEscPos && p >= p0 && p < p0 + len;
-                    if (kInt) {
-                        if (in) {
-                            atomicAdd(&s_acci[p - p0], (int32_t)raw);
-                            s_touch[p - p0] = 1;
-                        }
-                    } else {
-                        s_pos[i] = in ? (uint32_t)(p - p0) : kNoPos;
-                        s_val[i] = raw;
-                        s_msg[i] = (uint32_t)l;
-                    }
-                }
-                if (!kInt) rounds(m);  // each thread reads back only slots it staged itself
-                else __syncthreads();  // the staged chunk is consumed before the next one is staged
-            }
+            if (!kInt && total > 0) rounds((uint32_t)total);
+            continue;
         }
-        __syncthreads();
-        // Modes that read the output first (the SGD step, accumulation of integer sums) load every
-        // value this thread needs before any arithmetic, so a tile costs one round trip to memory
-        // instead of one per entry; only the entries that change are written.
-        constexpr int kOut = kDecTile / kThreads;
-        if (kInt) {
-            if (a.apply || a.accumulate) {
-                float o[kOut];
+        for (uint32_t r0 = 0; r0 < total; r0 += kDecCap) {
+            const uint32_t m = (uint32_t)umin64(kDecCap, total - r0);
 #pragma unroll
-                for (int k = 0; k < kOut; ++k) {
-                    const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
-                    const bool need = i < len && (a.apply ? s_acci[i] != 0 : s_touch[i] != 0);
-                    o[k] = need ? a.dense[p0 + i] : 0.0f;
+            for (int k = 0; k < kPerThread; ++k) {
+                const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+                if (i >= m) break;
+                const uint32_t f = r0 + i;
+                int l = 0, h = nw;  // message of flattened token f
+                while (h - l > 1) {
+                    const int mid = (l + h) >> 1;
+                    if (s_off[mid] <= f) l = mid; else h = mid;
                 }
-#pragma unroll
-                for (int k = 0; k < kOut; ++k) {
-                    const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
-                    if (i >= len) break;
-                    const int32_t S = s_acci[i];
-                    if (a.apply) {  // S == 0: the step is the identity
-                        if (S) a.dense[p0 + i] = __fmaf_rn(a.neg_lr, dequant(S, a.alpha), o[k]);
-                    } else if (s_touch[i]) {  // one addition where a message landed
-                        a.dense[p0 + i] = __fadd_rn(o[k], dequant(S, a.alpha));
+                const DecStream& d = a.tab[wb + l];
+                const uint64_t j = s_first[l] + (f - s_off[l]);
+                const uint32_t p = a.pos[d.tok_base + j];
+                const uint32_t raw = dec_value(a, d, j);
+                const bool in = p != kEscPos && p >= p0 && p < p0 + len;
+                if (kInt) {
+                    if (in) {
+                        atomicAdd(&s_acci[p - p0], (int32_t)raw);
+                        s_touch[p - p0] = 1;
                     }
+                } else {
+                    s_pos[i] = in ? (uint32_t)(p - p0) : kNoPos;
+                    s_val[i] = raw;
+                    s_msg[i] = (uint32_t)l;
                 }
-            } else {
-                for (uint32_t i = threadIdx.x; i < len; i += kThreads)
-                    a.dense[p0 + i] = dequant(s_acci[i], a.alpha);
             }
-        } else if (a.apply) {
-            // a sum that starts at +0 is +0 wherever no message lands (x + y is -0 only for two
-            // -0 addends), and fma(neg_lr, +0, w) == w for a finite neg_lr with its sign bit
-            // set: those entries are left alone, the others take the step
+            if (!kInt) rounds(m);  // each thread reads back only slots it staged itself
+            else __syncthreads();  // the staged chunk is consumed before the next one is staged
+        }
+    }
+    __syncthreads();
+    // Modes that read the output first (the SGD step, accumulation of integer sums) load every
+    // value this thread needs before any arithmetic, so a tile costs one round trip to memory
+    // instead of one per entry; only the entries that change are written.
+    constexpr int kOut = kDecTile / kThreads;
+    if (kInt) {
+        if (a.apply || a.accumulate) {
             float o[kOut];
 #pragma unroll
             for (int k = 0; k < kOut; ++k) {
                 const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
-                o[k] = (i < len && __float_as_uint(s_acc[i]) != 0u) ? a.dense[p0 + i] : 0.0f;
+                const bool need = i < len && (a.apply ? s_acci[i] != 0 : s_touch[i] != 0);
+                o[k] = need ? a.dense[p0 + i] : 0.0f;
             }
 #pragma unroll
             for (int k = 0; k < kOut; ++k) {
                 const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
                 if (i >= len) break;
-                const float t = s_acc[i];
-                if (__float_as_uint(t) != 0u) a.dense[p0 + i] = __fmaf_rn(a.neg_lr, t, o[k]);
+                const int32_t S = s_acci[i];
+                if (a.apply) {  // S == 0: the step is the identity
+                    if (S) a.dense[p0 + i] = __fmaf_rn(a.neg_lr, dequant(S, a.alpha), o[k]);
+                } else if (s_touch[i]) {  // one addition where a message landed
+                    a.dense[p0 + i] = __fadd_rn(o[k], dequant(S, a.alpha));
+                }
             }
-        } else if (vec) {
-            for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
-                reinterpret_cast<float4*>(a.dense + p0)[i] =
-                    reinterpret_cast<const float4*>(s_acc)[i];
         } else {
-            for (uint32_t i = threadIdx.x; i < len; i += kThreads) a.dense[p0 + i] = s_acc[i];
+            for (uint32_t i = threadIdx.x; i < len; i += kThreads)
+                a.dense[p0 + i] = dequant(s_acci[i], a.alpha);
         }
-        __syncthreads();  // this tile's sums are all read before the next tile clears them
+    } else if (a.apply) {
+        // a sum that starts at +0 is +0 wherever no message lands (x + y is -0 only for two -0
+        // addends), and fma(neg_lr, +0, w) == w for a finite neg_lr with its sign bit set: those
+        // entries are left alone, the others take the step
+        float o[kOut];
+#pragma unroll
+        for (int k = 0; k < kOut; ++k) {
+            const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+            o[k] = (i < len && __float_as_uint(s_acc[i]) != 0u) ? a.dense[p0 + i] : 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < kOut; ++k) {
+            const uint32_t i = threadIdx.x + (uint32_t)k * kThreads;
+            if (i >= len) break;
+            const float t = s_acc[i];
+            if (__float_as_uint(t) != 0u) a.dense[p0 + i] = __fmaf_rn(a.neg_lr, t, o[k]);
+        }
+    } else if (vec) {
+        for (uint32_t i = threadIdx.x; i < kDecTile / 4; i += kThreads)
+            reinterpret_cast<float4*>(a.dense + p0)[i] = reinterpret_cast<const float4*>(s_acc)[i];
+    } else {
+        for (uint32_t i = threadIdx.x; i < len; i += kThreads) a.dense[p0 + i] = s_acc[i];
     }
 }
 
@@ -1025,14 +997,10 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
             ++launches;
         }
     } else if (L.ntiles > 0) {
-        // persistent blocks, 4 per SM (the kernel's register budget)
-        const int sms = dgc_internal_sm_count();
-        if (sms <= 0) return DGC_ECUDA;
-        const unsigned grid = (unsigned)std::min<uint64_t>(L.ntiles, (uint64_t)sms * 4);
         if (qbits)
-            k_dec_tiles<true><<<grid, kThreads, 0, s>>>(a);
+            k_dec_tiles<true><<<(unsigned)L.ntiles, kThreads, 0, s>>>(a);
         else
-            k_dec_tiles<false><<<grid, kThreads, 0, s>>>(a);
+            k_dec_tiles<false><<<(unsigned)L.ntiles, kThreads, 0, s>>>(a);
         ++launches;
     }
     dgc_internal_count_launches(launches);
