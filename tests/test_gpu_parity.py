@@ -621,7 +621,7 @@ def test_decode_many_learners_and_accumulate(seed):
 
 
 @pytest.mark.parametrize("case", ["same set, 300 learners", "dense messages, 40 learners",
-                                  "half shared, 70 learners"])
+                                  "half shared, 70 learners", "shared positions, 8 learners"])
 def test_decode_collisions_and_crowded_tiles(case):
     # The worst cases of the ordered multi-message sum: every learner at the same positions (as
     # many values meet at one position as there are learners, across the 256-message groups),
@@ -642,6 +642,18 @@ def test_decode_collisions_and_crowded_tiles(case):
             val = (rng.standard_normal(n) * 10.0 ** rng.integers(-3, 3, n)).astype(np.float32)
             val[rng.random(n) < 0.05] = np.float32(-0.0)
             msgs.append(oracle.encode(idx, val, n))
+    elif case.startswith("shared positions"):
+        # few tokens per tile, but in odd tiles 8 learners meet at 12 positions (96 tokens at
+        # shared positions) and in even tiles at 4 (32): a warp orders the second kind itself
+        # and leaves the first kind to the block decoder
+        n, W = 40_000, 8
+        common = np.concatenate([t * 4096 + 300 * np.arange(12 if t % 2 else 4)
+                                 for t in range(n // 4096)])
+        for _ in range(W):
+            own = rng.choice(n, size=40, replace=False)
+            idx = np.unique(np.concatenate([common, own])).astype(np.uint32)
+            val = (rng.standard_normal(idx.size) * 10.0 ** rng.integers(-3, 3, idx.size))
+            msgs.append(oracle.encode(idx, val.astype(np.float32), n))
     else:
         n, W = 100_000, 70
         common = rng.choice(n, size=4000, replace=False)
