@@ -724,8 +724,10 @@ __global__ void __launch_bounds__(kThreads, 5) k_dec_tiles(DecArgs a) {
 // nothing and is flagged for k_dec_tiles, which then takes only the flagged tiles.
 constexpr int kWarpTiles = 4;    // warps (tiles) per block
 constexpr int kWarpMsgs = 64;    // messages per call (two per lane)
-constexpr int kWarpCap = 256;    // tokens a warp stages for its tile
-constexpr int kWarpShared = 64;  // tokens at shared positions a warp puts in order
+constexpr int kWarpCap = 512;    // tokens a warp stages for its tile (64 learners: ~262)
+constexpr int kWarpShared = 96;  // tokens at shared positions a warp puts in order
+constexpr int kWarpSharedPerLane = kWarpShared / 32;
+static_assert(kWarpSharedPerLane * 32 == kWarpShared, "whole lanes");
 constexpr int kWarpBatch = 6;    // loads of a message's tokens in flight at once
 
 __global__ void __launch_bounds__(32 * kWarpTiles, 8) k_dec_warp(DecArgs a) {
@@ -851,10 +853,12 @@ __global__ void __launch_bounds__(32 * kWarpTiles, 8) k_dec_warp(DecArgs a) {
     if (nsh == 0) return;
     // shared positions: rank among the position's tokens (by message), and the owner (rank 0)
     float* ssum = s_sum[wi];
-    uint32_t rank[2] = {0, 0}, owner[2] = {0, 0}, maxr = 0;
+    uint32_t rank[kWarpSharedPerLane], owner[kWarpSharedPerLane], maxr = 0;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < kWarpSharedPerLane; ++k) {
         const uint32_t c = lane + 32 * k;
+        rank[k] = 0;
+        owner[k] = 0;
         if (c >= nsh) continue;
         const uint32_t i = sh[c], lp = spos[i], m = smsg[i];
         uint32_t own = c, ownm = m;
@@ -877,7 +881,7 @@ __global__ void __launch_bounds__(32 * kWarpTiles, 8) k_dec_warp(DecArgs a) {
     for (uint32_t r = 1; r <= maxr; ++r) {  // one token per position and rank
         __syncwarp();
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < kWarpSharedPerLane; ++k) {
             const uint32_t c = lane + 32 * k;
             if (c < nsh && rank[k] == r)
                 ssum[owner[k]] = __fadd_rn(ssum[owner[k]], __uint_as_float(sval[sh[c]]));
@@ -885,7 +889,7 @@ __global__ void __launch_bounds__(32 * kWarpTiles, 8) k_dec_warp(DecArgs a) {
     }
     __syncwarp();
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < kWarpSharedPerLane; ++k) {
         const uint32_t c = lane + 32 * k;
         if (c < nsh && rank[k] == 0) {
             const uint32_t lp = spos[sh[c]];
