@@ -283,20 +283,24 @@ __device__ __forceinline__ void mark_bad(const DecArgs& a, int w) {
 // launch (W + 1 entries within the 4 KB of kernel parameters), so no host memory is read when
 // the call replays from a CUDA graph. Larger calls copy the table to the workspace instead.
 constexpr int kDecInline = 96;
+template <int kMax>
 struct DecTabInline {
-    DecStream e[kDecInline + 1];
+    DecStream e[kMax + 1];
 };
-static_assert(sizeof(DecTabInline) + sizeof(DecArgs) <= 4096, "within the kernel parameter space");
+static_assert(sizeof(DecTabInline<kDecInline>) + sizeof(DecArgs) <= 4096,
+              "within the kernel parameter space");
 
 // Zeroes the look-back words, writes the message table into the workspace when it comes with
-// the launch, and checks every header (ctl was zeroed before this kernel).
-__global__ void k_dec_init(DecArgs a, const __grid_constant__ DecTabInline t) {
+// the launch (kMax entries at most: one message, or up to kDecInline), and checks every header
+// (ctl was zeroed before this kernel).
+template <int kMax>
+__global__ void k_dec_init(DecArgs a, const __grid_constant__ DecTabInline<kMax> t) {
     const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     for (uint64_t i = tid; i <= a.nchunks; i += stride) a.st[i] = 0;
     if (a.redo)
         for (uint64_t i = tid; i <= a.ntiles; i += stride) a.redo[i] = 0;
-    const bool inl = a.W <= kDecInline;
+    const bool inl = a.W <= kMax;
     DecStream* tab = const_cast<DecStream*>(a.tab);
     if (inl)
         for (uint64_t w = tid; w <= (uint64_t)a.W; w += stride) tab[w] = t.e[w];
@@ -1163,17 +1167,24 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // the table of messages goes with the first kernel's parameters when it is small; else by a
     // pageable copy (staged before this function returns, so the host vector may go away)
-    DecTabInline inl{};
-    if (W <= kDecInline) {
-        for (int w = 0; w <= W; ++w) inl.e[w] = tab[w];
-    } else if (cudaMemcpyAsync(p + L.tab, tab.data(), sizeof(DecStream) * tab.size(),
-                               cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    if (W > kDecInline && cudaMemcpyAsync(p + L.tab, tab.data(), sizeof(DecStream) * tab.size(),
+                                          cudaMemcpyHostToDevice, s) != cudaSuccess)
         return DGC_ECUDA;
-    }
     if (cudaMemsetAsync(p + L.ctl, 0, sizeof(DecCtl), s) != cudaSuccess) return DGC_ECUDA;
     uint64_t launches = 0;
-    const uint64_t init_work = std::max<uint64_t>(L.nchunks + 1, (uint64_t)W + 1);
-    k_dec_init<<<(unsigned)std::min<uint64_t>((init_work + 255) / 256, 1024), 256, 0, s>>>(a, inl);
+    const uint64_t init_work = std::max<uint64_t>(std::max<uint64_t>(L.nchunks, L.ntiles) + 1,
+                                                  (uint64_t)W + 1);
+    const unsigned init_grid = (unsigned)std::min<uint64_t>((init_work + 255) / 256, 1024);
+    if (W <= 1) {  // the table of one message: a small launch
+        DecTabInline<1> inl{};
+        for (int w = 0; w <= W; ++w) inl.e[w] = tab[w];
+        k_dec_init<1><<<init_grid, 256, 0, s>>>(a, inl);
+    } else {
+        DecTabInline<kDecInline> inl{};
+        if (W <= kDecInline)
+            for (int w = 0; w <= W; ++w) inl.e[w] = tab[w];
+        k_dec_init<kDecInline><<<init_grid, 256, 0, s>>>(a, inl);
+    }
     ++launches;
     if (L.nchunks > 0) {
         k_dec_pos<<<(unsigned)L.nchunks, kThreads, 0, s>>>(a);

@@ -101,7 +101,6 @@ constexpr int kSqLimbs = 10;   // 640-bit exact sum of squares, 64-bit limbs (wh
 constexpr int kSqDigits = 20;  // the same sum as 32-bit digits, each in a 64-bit word
 constexpr int kSqWords = kSqDigits + 1;  // + one word of flags (2: +inf seen, 4: NaN seen)
 constexpr int kHistBins = 2048;
-constexpr int kCGroup = kThreads;  // streaming tiles per collect group
 // DGC pass: a streaming tile with at most this many candidates stores them as sent (v, and u with
 // masking, zeroed) and keeps their values in its slots; the emit step puts back the unsent ones
 constexpr uint32_t kSpecSlots = 64;
@@ -141,7 +140,7 @@ struct Ctl {
     int32_t abort;
     uint32_t active;
     uint32_t any_failed;
-    uint32_t ticket_fused, ticket_compact, ticket_emit;
+    uint32_t ticket_fused, ticket_compact, ticket_emit, ticket_collect;
     uint32_t ndense;        // tiles whose slots k_collect_copy moves: up to kCollectWarp ...
     uint32_t nlarge;        // ... and more (listed from the end of dlist)
     uint32_t total_samples, total_clip_tiles, total_cand, total_sent;
@@ -166,7 +165,7 @@ constexpr int kBucketShift = 10;  // cache order: 1024-entry buckets, segment by
 struct Layout {
     size_t ctl, scache, segs, seg_start, samp_off, clip_off, cand_off, clip_acc, skeys, spos,
         bcount, histA, histB;
-    size_t gcount, st_compact, st_emit, cidx, sidx, sval, su, tcount, tseg, eseg, clip_cnt,
+    size_t st_collect, st_compact, st_emit, cidx, sidx, sval, su, tcount, tseg, eseg, clip_cnt,
         dlist, binmax, total;
     uint64_t max_samples, max_clip_tiles, fused_tiles, emit_tiles, ptiles, cgroups, nbuckets,
         max_bins;
@@ -247,7 +246,7 @@ Layout make_layout(int64_t n, int32_t nseg, const HostParams& hp) {
     L.bcount = take(sizeof(uint32_t) * (size_t)L.nbuckets);
     L.histA = take(sizeof(uint32_t) * (size_t)nseg * kHistBins);
     L.histB = take(sizeof(uint32_t) * (size_t)nseg * kHistBins);
-    L.gcount = take(sizeof(uint64_t) * (size_t)(L.cgroups + 1));
+    L.st_collect = take(sizeof(uint64_t) * (size_t)(L.cgroups + 1));
     L.st_compact = take(sizeof(uint64_t) * (size_t)(L.fused_tiles + 1));
     L.st_emit = take(sizeof(uint64_t) * (size_t)(L.emit_tiles + 1));
     L.cidx = take(sizeof(uint32_t) * (size_t)un);
@@ -308,7 +307,7 @@ struct Args {
     uint32_t* bcount;  // per-bucket counts, then cursors, while the cache is rebuilt
     uint32_t* histA;
     uint32_t* histB;
-    uint64_t* gcount;  // candidates of every group of kCGroup streaming tiles
+    uint64_t* st_collect;
     uint64_t* st_compact;
     uint64_t* st_emit;
     uint32_t* cidx;   // candidates, ascending index
@@ -442,7 +441,7 @@ __global__ void __launch_bounds__(1024) k_plan(Args a) {
         a.histB[i] = 0;
     }
     for (size_t i = tid; i <= a.fused_tiles; i += stride) a.st_compact[i] = 0;
-    for (size_t i = tid; i <= a.cgroups; i += stride) a.gcount[i] = 0;
+    for (size_t i = tid; i <= a.cgroups; i += stride) a.st_collect[i] = 0;
     for (size_t i = tid; i <= a.emit_tiles; i += stride) a.st_emit[i] = 0;
     for (size_t i = tid; i < a.nbuckets; i += stride) a.bcount[i] = 0;
     for (size_t i = tid; i < a.max_bins; i += stride) a.binmax[i] = 0;
@@ -1846,39 +1845,44 @@ __global__ void __launch_bounds__(kThreads, stream_blocks_per_sm<kSel>()) k_stre
             }
             if (kSel == 0 && f4) store_uv(a, base, len, r, tid, uu[r], vv[r]);
         }
-        if (tid == 0) {
-            a.tcount[tile] = tile_total;
-            // the group's total, for the collect step's offsets (an add nobody waits for)
-            if (tile_total) atomicAdd((unsigned long long*)&a.gcount[tile / kCGroup], tile_total);
-        }
+        if (tid == 0) a.tcount[tile] = tile_total;
     }
 }
 
 // ------------------------------------------------------------------------- collect
 // Turns the streaming pass's per-tile slots into one index-ordered candidate list. Block b owns
-// kCGroup consecutive tiles: it scans their counts, and the group's first list position is the
-// sum of the earlier groups' totals, which the streaming pass added up (no block waits on
-// another); each tile's count is replaced by its first list position. A tile's few candidates
-// are copied to cidx by its own thread; tiles with more are listed for k_collect_copy.
+// kCGroup consecutive tiles: it scans their counts and gets the group's global offset from a
+// decoupled look-back over groups; each tile's count is replaced by its first list position. A
+// tile's few candidates are copied to cidx by its own thread; tiles with more are listed for
+// k_collect_copy.
+constexpr int kCGroup = kThreads;  // tiles per collect block
 constexpr uint32_t kCollectDirect = 16;  // a tile with at most this many candidates: copied in place
 constexpr uint32_t kCollectWarp = 256;   // up to this many: one warp; more: one block
 
 __global__ void __launch_bounds__(kThreads) k_collect(Args a) {
     __shared__ uint32_t s_scan[33];
-    __shared__ uint64_t s_sum[33];
+    __shared__ uint64_t s_lb64[33];
+    __shared__ uint32_t s_lb32[2];
+    __shared__ uint32_t s_group;
+    __shared__ int s_skip;
     const int tid = threadIdx.x;
     const uint32_t ntiles = (uint32_t)a.ptiles;
     const uint32_t ngroups = (ntiles + kCGroup - 1) / kCGroup;
-    if (ld_relaxed_u32((const uint32_t*)&a.ctl->abort)) return;  // the same in every thread
-    const uint32_t grp = blockIdx.x;
+    if (tid == 0) {
+        s_skip = ld_relaxed_u32((const uint32_t*)&a.ctl->abort);
+        if (!s_skip) s_group = atomicAdd(&a.ctl->ticket_collect, 1u);
+    }
+    __syncthreads();
+    if (s_skip) return;
+    const uint32_t grp = s_group;
     if (grp >= ngroups) return;
     const uint32_t t = grp * kCGroup + tid;
     const uint32_t c = (t < ntiles) ? a.tcount[t] : 0u;
     uint32_t total;
     const uint32_t ex = block_excl_scan<kThreads>(c, s_scan, &total);
-    uint64_t part = 0;
-    for (uint32_t g2 = tid; g2 < grp; g2 += kThreads) part += a.gcount[g2];
-    const uint64_t gbase = block_sum64(part, s_sum);
+    // the group's offset: a look-back walked by the whole block (kThreads groups per round trip)
+    const uint64_t gbase = block_lookback<kThreads>(a.st_collect, grp, total, a.spin_limit,
+                                                    a.status, &a.ctl->abort, s_lb32, s_lb64);
     // the tile's count becomes its first position in the list. A tile with few candidates (the
     // common case) has its slots copied by its own thread; the others are listed for
     // k_collect_copy, which spreads each over a whole block.
@@ -2362,7 +2366,7 @@ Args make_args(const float* g, float* u, float* v, int64_t n, const int64_t* seg
     a.bcount = reinterpret_cast<uint32_t*>(w + L.bcount);
     a.histA = reinterpret_cast<uint32_t*>(w + L.histA);
     a.histB = reinterpret_cast<uint32_t*>(w + L.histB);
-    a.gcount = reinterpret_cast<uint64_t*>(w + L.gcount);
+    a.st_collect = reinterpret_cast<uint64_t*>(w + L.st_collect);
     a.st_compact = reinterpret_cast<uint64_t*>(w + L.st_compact);
     a.st_emit = reinterpret_cast<uint64_t*>(w + L.st_emit);
     a.cidx = reinterpret_cast<uint32_t*>(w + L.cidx);
