@@ -266,7 +266,6 @@ struct DecArgs {
     uint32_t* pos;
     uint64_t* st;
     uint32_t* ts;  // (ntiles + 1) x W first-token table
-    uint32_t* redo;  // tiles the warp decoder left to the block decoder (or null: every tile)
     const uint64_t* dev_bytes;  // the message sizes in device memory, or null (sizes on the host)
     uint64_t ntiles;
     uint64_t nchunks;
@@ -298,8 +297,6 @@ __global__ void k_dec_init(DecArgs a, const __grid_constant__ DecTabInline<kMax>
     const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     for (uint64_t i = tid; i <= a.nchunks; i += stride) a.st[i] = 0;
-    if (a.redo)
-        for (uint64_t i = tid; i <= a.ntiles; i += stride) a.redo[i] = 0;
     const bool inl = a.W <= kMax;
     DecStream* tab = const_cast<DecStream*>(a.tab);
     if (inl)
@@ -458,7 +455,6 @@ __global__ void __launch_bounds__(kThreads, 5) k_dec_tiles(DecArgs a) {
     int32_t* s_acci = reinterpret_cast<int32_t*>(s_accw);
     if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
     const uint64_t t = blockIdx.x;
-    if (a.redo && !a.redo[t]) return;  // the warp decoder wrote this tile
     const uint64_t p0 = t * kDecTile;
     const uint32_t len = (uint32_t)umin64(kDecTile, a.n - p0);
     const bool vec = (len == kDecTile) && ((reinterpret_cast<uintptr_t>(a.dense) & 15u) == 0);
@@ -715,193 +711,6 @@ __global__ void __launch_bounds__(kThreads, 5) k_dec_tiles(DecArgs a) {
     }
 }
 
-// Binary32 messages, at most kWarpMsgs of them: one warp per 4096-entry dense tile, no block
-// barrier. Lane l reads the tile's first and end token of messages l and l + 32 from the table
-// and stages their tokens (position, value, message) in the warp's shared memory. A bitmap of
-// the tile's positions (one atomicOr per token) finds the positions more than one message
-// reaches. The warp then writes the tile straight to memory: zeros first (the plain sum), then
-// every token at a position only it reaches -- one binary32 addition onto +0, onto dense, or the
-// SGD step -- and the tokens at shared positions in the learners' order: each such token counts
-// the tokens at its position from smaller messages (its rank) and finds the one of rank 0, which
-// owns the position's sum; rank by rank the tokens add into their owner's sum, and the owner
-// writes it. A tile with more tokens or shared-position tokens than the warp stages writes
-// nothing and is flagged for k_dec_tiles, which then takes only the flagged tiles.
-constexpr int kWarpTiles = 4;    // warps (tiles) per block
-constexpr int kWarpMsgs = 64;    // messages per call (two per lane)
-constexpr int kWarpCap = 512;    // tokens a warp stages for its tile (64 learners: ~262)
-constexpr int kWarpShared = 96;  // tokens at shared positions a warp puts in order
-constexpr int kWarpSharedPerLane = kWarpShared / 32;
-static_assert(kWarpSharedPerLane * 32 == kWarpShared, "whole lanes");
-constexpr int kWarpBatch = 6;    // loads of a message's tokens in flight at once
-
-__global__ void __launch_bounds__(32 * kWarpTiles, 8) k_dec_warp(DecArgs a) {
-    __shared__ uint32_t s_pos[kWarpTiles][kWarpCap];  // tile-local position, or kNoPos
-    __shared__ uint32_t s_val[kWarpTiles][kWarpCap];
-    __shared__ uint8_t s_msg[kWarpTiles][kWarpCap];
-    __shared__ uint32_t s_bit[kWarpTiles][2][kDecTile / 32];  // reached; reached again
-    __shared__ uint16_t s_sh[kWarpTiles][kWarpShared];        // staging slots of shared tokens
-    __shared__ float s_sum[kWarpTiles][kWarpShared];          // owners' sums
-    if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
-    const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
-    const uint64_t t = (uint64_t)blockIdx.x * kWarpTiles + wi;
-    if (t >= a.ntiles) return;  // the whole warp
-    uint32_t* spos = s_pos[wi];
-    uint32_t* sval = s_val[wi];
-    uint8_t* smsg = s_msg[wi];
-    uint32_t* bitA = s_bit[wi][0];
-    uint32_t* bitB = s_bit[wi][1];
-    const uint64_t p0 = t * kDecTile;
-    const uint32_t len = (uint32_t)umin64(kDecTile, a.n - p0);
-    for (int i = lane; i < kDecTile / 32; i += 32) {
-        bitA[i] = 0;
-        bitB[i] = 0;
-    }
-    // the tile's tokens of messages lane and lane + 32 (a message without tokens has no table
-    // entries: its count is forced to 0)
-    uint32_t first[2], cnt[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int w = lane + 32 * k;
-        first[k] = 0;
-        cnt[k] = 0;
-        if (w < a.W) {
-            const uint32_t f = __ldg(a.ts + t * a.W + w), e = __ldg(a.ts + (t + 1) * a.W + w);
-            if (a.tab[w].T > 0) {
-                first[k] = f;
-                cnt[k] = e - f;
-            }
-        }
-    }
-    const uint32_t mine = cnt[0] + cnt[1];
-    const uint32_t incl = warp_incl_scan(mine);
-    const uint32_t total = __shfl_sync(kFull, incl, 31);
-    if (total > (uint32_t)kWarpCap) {  // too many tokens: the block decoder takes the tile
-        if (lane == 0) a.redo[t] = 1;
-        return;
-    }
-    uint32_t at = incl - mine;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int w = lane + 32 * k;
-        if (cnt[k] == 0) continue;
-        const DecStream& d = a.tab[w];
-        for (uint32_t q0 = 0; q0 < cnt[k]; q0 += kWarpBatch) {
-            uint32_t pb[kWarpBatch], rb[kWarpBatch];
-#pragma unroll
-            for (int r = 0; r < kWarpBatch; ++r)
-                if (q0 + r < cnt[k]) {
-                    const uint64_t j = (uint64_t)first[k] + q0 + r;
-                    pb[r] = __ldg(a.pos + d.tok_base + j);
-                    rb[r] = __ldg(reinterpret_cast<const uint32_t*>(d.ptr + 32) + j);
-                }
-#pragma unroll
-            for (int r = 0; r < kWarpBatch; ++r)
-                if (q0 + r < cnt[k]) {
-                    const uint32_t p = pb[r];
-                    const bool in = p != kEscPos && p >= p0 && p < p0 + len;
-                    spos[at + q0 + r] = in ? (uint32_t)(p - p0) : kNoPos;
-                    sval[at + q0 + r] = rb[r];
-                    smsg[at + q0 + r] = (uint8_t)w;
-                }
-        }
-        at += cnt[k];
-    }
-    __syncwarp();
-    // positions reached more than once
-    for (uint32_t i = lane; i < total; i += 32) {
-        const uint32_t lp = spos[i];
-        if (lp == kNoPos) continue;
-        const uint32_t bit = 1u << (lp & 31);
-        if (atomicOr(&bitA[lp >> 5], bit) & bit) atomicOr(&bitB[lp >> 5], bit);
-    }
-    __syncwarp();
-    // the tokens at shared positions, listed in staging order
-    uint16_t* sh = s_sh[wi];
-    uint32_t nsh = 0;
-    for (uint32_t i0 = 0; i0 < total; i0 += 32) {
-        const uint32_t i = i0 + lane;
-        bool shared = false;
-        if (i < total) {
-            const uint32_t lp = spos[i];
-            shared = lp != kNoPos && ((bitB[lp >> 5] >> (lp & 31)) & 1u);
-        }
-        const unsigned b = __ballot_sync(kFull, shared);
-        const uint32_t slot = nsh + __popc(b & ((1u << lane) - 1u));
-        if (shared && slot < (uint32_t)kWarpShared) sh[slot] = (uint16_t)i;
-        nsh += __popc(b);
-    }
-    if (nsh > (uint32_t)kWarpShared) {  // too many: nothing written yet, the block decoder
-        if (lane == 0) a.redo[t] = 1;    // takes the tile
-        return;
-    }
-    float* dense = a.dense + p0;
-    const bool plain = !a.accumulate && !a.apply;
-    if (plain) {  // the sum starts at +0 everywhere
-        if (len == kDecTile && (reinterpret_cast<uintptr_t>(dense) & 15u) == 0) {
-            for (uint32_t i = lane; i < kDecTile / 4; i += 32)
-                reinterpret_cast<float4*>(dense)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-            for (uint32_t i = lane; i < len; i += 32) dense[i] = 0.0f;
-        }
-        __syncwarp();  // the zeros before any value lands on them
-    }
-    // tokens at positions only they reach: one operation each, in any order
-    for (uint32_t i = lane; i < total; i += 32) {
-        const uint32_t lp = spos[i];
-        if (lp == kNoPos || ((bitB[lp >> 5] >> (lp & 31)) & 1u)) continue;
-        const float x = __uint_as_float(sval[i]);
-        if (plain) dense[lp] = __fadd_rn(0.0f, x);
-        else if (a.apply) dense[lp] = __fmaf_rn(a.neg_lr, __fadd_rn(0.0f, x), dense[lp]);
-        else dense[lp] = __fadd_rn(dense[lp], x);
-    }
-    if (nsh == 0) return;
-    // shared positions: rank among the position's tokens (by message), and the owner (rank 0)
-    float* ssum = s_sum[wi];
-    uint32_t rank[kWarpSharedPerLane], owner[kWarpSharedPerLane], maxr = 0;
-#pragma unroll
-    for (int k = 0; k < kWarpSharedPerLane; ++k) {
-        const uint32_t c = lane + 32 * k;
-        rank[k] = 0;
-        owner[k] = 0;
-        if (c >= nsh) continue;
-        const uint32_t i = sh[c], lp = spos[i], m = smsg[i];
-        uint32_t own = c, ownm = m;
-        for (uint32_t c2 = 0; c2 < nsh; ++c2) {
-            const uint32_t i2 = sh[c2];
-            if (spos[i2] != lp) continue;
-            const uint32_t m2 = smsg[i2];
-            if (m2 < m) ++rank[k];
-            if (m2 < ownm) {
-                ownm = m2;
-                own = c2;
-            }
-        }
-        owner[k] = own;
-        maxr = max(maxr, rank[k]);
-        if (rank[k] == 0)  // the owner starts the sum: from +0, or from dense when accumulating
-            ssum[c] = __fadd_rn(a.accumulate ? dense[lp] : 0.0f, __uint_as_float(sval[i]));
-    }
-    maxr = __reduce_max_sync(kFull, maxr);
-    for (uint32_t r = 1; r <= maxr; ++r) {  // one token per position and rank
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < kWarpSharedPerLane; ++k) {
-            const uint32_t c = lane + 32 * k;
-            if (c < nsh && rank[k] == r)
-                ssum[owner[k]] = __fadd_rn(ssum[owner[k]], __uint_as_float(sval[sh[c]]));
-        }
-    }
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < kWarpSharedPerLane; ++k) {
-        const uint32_t c = lane + 32 * k;
-        if (c < nsh && rank[k] == 0) {
-            const uint32_t lp = spos[sh[c]];
-            dense[lp] = a.apply ? __fmaf_rn(a.neg_lr, ssum[c], dense[lp]) : ssum[c];
-        }
-    }
-}
-
 // One message (W = 1): its positions are distinct, so its values can be added in parallel. The
 // dense output is first cleared by a streaming store pass (unless accumulating), then each value
 // token adds itself to its position: the same single binary32 addition per value as the tile
@@ -975,7 +784,7 @@ __global__ void __launch_bounds__(kThreads) k_sum_shared(const float* const* val
 }
 
 struct DecLayout {
-    size_t ctl, tab, bad, pos, st, ts, redo, total;
+    size_t ctl, tab, bad, pos, st, ts, total;
     uint64_t sum_T, nchunks, ntiles;
 };
 
@@ -1004,7 +813,6 @@ int dec_layout(int32_t W, const uint64_t* stream_bytes, int64_t n, int qbits, De
     L->pos = take(sizeof(uint32_t) * (size_t)L->sum_T);
     L->st = take(sizeof(uint64_t) * (size_t)(L->nchunks + 1));
     L->ts = take(sizeof(uint32_t) * (size_t)(L->ntiles + 1) * (size_t)(W > 0 ? W : 1));
-    L->redo = take(sizeof(uint32_t) * (size_t)(L->ntiles + 1));
     L->total = o;
     return DGC_OK;
 }
@@ -1158,8 +966,6 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
     a.pos = reinterpret_cast<uint32_t*>(p + L.pos);
     a.st = reinterpret_cast<uint64_t*>(p + L.st);
     a.ts = reinterpret_cast<uint32_t*>(p + L.ts);
-    a.redo = (!qbits && W > 1 && W <= kWarpMsgs) ? reinterpret_cast<uint32_t*>(p + L.redo)
-                                                 : nullptr;
     a.dev_bytes = dev_bytes;
     a.ntiles = L.ntiles;
     a.nchunks = L.nchunks;
@@ -1172,8 +978,7 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
         return DGC_ECUDA;
     if (cudaMemsetAsync(p + L.ctl, 0, sizeof(DecCtl), s) != cudaSuccess) return DGC_ECUDA;
     uint64_t launches = 0;
-    const uint64_t init_work = std::max<uint64_t>(std::max<uint64_t>(L.nchunks, L.ntiles) + 1,
-                                                  (uint64_t)W + 1);
+    const uint64_t init_work = std::max<uint64_t>(L.nchunks + 1, (uint64_t)W + 1);
     const unsigned init_grid = (unsigned)std::min<uint64_t>((init_work + 255) / 256, 1024);
     if (W <= 1) {  // the table of one message: a small launch
         DecTabInline<1> inl{};
@@ -1202,11 +1007,6 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
             ++launches;
         }
     } else if (L.ntiles > 0) {
-        if (!qbits && W <= kWarpMsgs) {  // a warp per tile; the block decoder for the tiles left
-            k_dec_warp<<<(unsigned)((L.ntiles + kWarpTiles - 1) / kWarpTiles), 32 * kWarpTiles,
-                         0, s>>>(a);
-            ++launches;
-        }
         if (qbits)
             k_dec_tiles<true><<<(unsigned)L.ntiles, kThreads, 0, s>>>(a);
         else
