@@ -519,37 +519,81 @@ __device__ double limbs_round(const unsigned long long* x) {
     return __longlong_as_double((long long)bits);
 }
 
-// x << sh for any sh: PTX shl.b32 gives 0 for shift amounts past 31
-__device__ __forceinline__ uint32_t shl32(uint32_t x, uint32_t sh) {
-    uint32_t r;
-    asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(sh));
-    return r;
-}
-
 // (w1:w0) += (p1:p0), 128 bits
 __device__ __forceinline__ void add128(unsigned long long& w0, unsigned long long& w1,
                                        unsigned long long p0, unsigned long long p1) {
     asm("add.cc.u64 %0, %0, %2;\n\taddc.u64 %1, %1, %3;" : "+l"(w0), "+l"(w1) : "l"(p0), "l"(p1));
 }
 
+// m << (sh mod 32), truncated to 32 bits (a funnel shift in wrap mode)
+__device__ __forceinline__ uint32_t shl_wrap(uint32_t m, uint32_t sh) {
+    uint32_t r;
+    asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(0u), "r"(m), "r"(sh));
+    return r;
+}
+
+// An entry with raw exponent e and significand m into a band: band 1 (e >= ea) adds
+// (m 2^(e - ea))^2 to A1, anything else adds (m 2^((e - eb) mod 32) mod 2^32)^2 to A2, modulo
+// 2^64. For an entry of band 2 that is its exact (m 2^(e - eb))^2; an entry below band 2 adds a
+// term of no meaning, which the caller takes back out (A2 is exact modulo 2^64, and the true
+// band sum is below 2^64).
+__device__ __forceinline__ void band_add(uint32_t e, uint32_t m, uint32_t ea, uint32_t eb,
+                                         unsigned long long& A1, unsigned long long& A2) {
+    asm("{\n\t.reg .pred p;\n\t.reg .u32 b, d, mm;\n\t"
+        "setp.ge.u32 p, %2, %4;\n\t"
+        "selp.u32 b, %4, %5, p;\n\t"
+        "sub.u32 d, %2, b;\n\t"
+        "shf.l.wrap.b32 mm, 0, %3, d;\n\t"
+        "@p mad.wide.u32 %0, mm, mm, %0;\n\t"
+        "@!p mad.wide.u32 %1, mm, mm, %1;\n\t}"
+        : "+l"(A1), "+l"(A2)
+        : "r"(e), "r"(m), "r"(ea), "r"(eb));
+}
+
+// 16 bytes from global to this thread's own shared memory, asynchronously (cp.async); the
+// thread reads them back itself after cp.async.wait_group, so no block barrier is involved
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
+}
+
+constexpr uint32_t kWinTiles = 16;  // tiles a warp window holds before it is flushed
+constexpr int kClipStages = 2;      // tiles of copies in flight per block, plus the one summed
+constexpr size_t kClipSmem = (size_t)kClipStages * 4 * kThreads * 16;
+
 // 4096-entry tiles of one segment each. Block b takes a contiguous range of the tiles (so its
 // segment changes only at segment boundaries), and its warps work without block barriers: warp w
-// of a tile holds entries [512 w, 512 w + 512), 16 per thread. The warp finds the largest
-// exponent e_max of its entries (from the largest |x| bits) and sums into a 128-bit window whose
-// lowest bit is bit lo = max(2 e_max - 68, 0) of X. Each thread first sums its 16 squares in two
-// 64-bit bands below its own largest entry, then places the two band sums in the window (each
-// below 2^118 there, 64 of them below 2^124). An entry of band b with e' = eb + d (d <= 6) adds
-// (m 2^d)^2 = M 4^d: a 32-bit shift of the significand (m 2^d < 2^30) and one 32 x 32 -> 64-bit
-// multiply, so a band sum stays below 16 x 2^60 = 2^64. What starts below lo, or lies more than
-// 13 binades under the thread's largest entry, is added to the block's digit words in shared
-// memory at once; lane 0 then adds the warp's window there too (shared atomic adds, each below
-// 2^33). When the block moves to another segment, and at its end, one thread propagates the
-// carries of the shared words into 32-bit digits and adds those to the segment's words in global
-// memory (each below 2^32, at most one add per block and segment).
+// of a tile holds entries [512 w, 512 w + 512), 16 per thread. Each thread copies its 16 entries
+// of the next tile into its own shared-memory slots (cp.async) while it sums the current one.
+//
+// A thread sums its 16 squares in two 64-bit bands below its own largest entry: an entry of band
+// b with e' = eb + d (d <= 6) adds (m 2^d)^2 = M 4^d, a 32-bit shift of the significand
+// (m 2^d < 2^30) and one 32 x 32 -> 64-bit multiply-add, so a band sum stays below 2^64.
+// What lies more than 13 binades under the thread's largest entry (rare) goes to the block's
+// digit words in shared memory at once. The band sums then go into the thread's 128-bit window,
+// whose lowest bit is bit lo = max(2 E - 68, 0) of X, where E is the largest e' the warp has
+// seen since it opened the window (each term below 2^118 there). A warp keeps its window over
+// up to kWinTiles tiles of a segment and reopens it when a tile brings a larger e' or the
+// segment ends: the threads' windows are then summed across the warp (below 2^128: at most
+// 2 kWinTiles terms per thread, or 16 per tile below 2^114 for a thread holding inf or NaN) and
+// lane 0 adds the sum to the block's digits (shared atomic adds, each below 2^33). Band sums
+// whose bit lies below lo go to the digits directly. When the block moves to another segment,
+// and at its end, one thread propagates the carries of the shared words into 32-bit digits and
+// adds those to the segment's words in global memory (each below 2^32, at most one add per
+// block and segment).
 __global__ void __launch_bounds__(kThreads, 4) k_clip_tiles(Args a) {
     __shared__ unsigned long long s_dig[kSqDigits];  // the block's share of the current segment
     __shared__ uint32_t s_flags;                     // 2: +inf seen; 4: NaN seen
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // each thread's slots of kClipStages tiles: [stage][4][kThreads] 16-byte words
+    extern __shared__ __align__(16) uint4 s_buf[];
+    const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) s_flags = 0;
     if (threadIdx.x < kSqDigits) s_dig[threadIdx.x] = 0ull;
     if (a.ctl->abort) return;  // written only by earlier kernels: the same in every thread
@@ -576,122 +620,181 @@ __global__ void __launch_bounds__(kThreads, 4) k_clip_tiles(Args a) {
         }
         __syncthreads();
     };
-    for (uint32_t c = c0; c < c1; ++c) {
-        if (s + 1 < a.nseg && a.clip_off[s + 1] <= c) {  // block-uniform: a new segment
-            flush(s);
-            while (s + 1 < a.nseg && a.clip_off[s + 1] <= c) ++s;
-        }
-        const SegInfo& d = a.segs[s];
-        const uint64_t base = (uint64_t)d.start + (uint64_t)(c - a.clip_off[s]) * kClipTile +
-                              16u * threadIdx.x;
-        uint32_t xb[16];  // |x| bits
-        if ((base & 3u) == 0 && base + 16 <= d.end) {  // 16-byte aligned and whole: four float4
-            const uint4* g4 = reinterpret_cast<const uint4*>(a.g + base);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint4 x = g4[j];
-                xb[4 * j] = x.x & 0x7FFFFFFFu;
-                xb[4 * j + 1] = x.y & 0x7FFFFFFFu;
-                xb[4 * j + 2] = x.z & 0x7FFFFFFFu;
-                xb[4 * j + 3] = x.w & 0x7FFFFFFFu;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint64_t e = base + i;
-                xb[i] = (e < d.end) ? (__float_as_uint(a.g[e]) & 0x7FFFFFFFu) : 0u;
-            }
-        }
-        uint32_t amax = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) amax = max(amax, xb[i]);
-        const bool nonfinite = amax >= 0x7F800000u;
-        // the thread's largest e' (inf and NaN count as 254: the sum is then inf or NaN anyway,
-        // and every bound below still holds)
-        const uint32_t et = max(min(amax >> 23, 254u), 1u);
-        const uint32_t em = __reduce_max_sync(kFull, et);
-        const int lo = max(2 * (int)em - 68, 0);
-        unsigned long long w0 = 0ull, w1 = 0ull;
-        uint32_t fl = 0;
-        // v 2^bit into the window when bit >= lo, else into the block's digits. In the window
-        // v 2^r stays below 2^118: a band sum (v < 2^64) has r <= 54, a single square
-        // (v < 2^48) r <= 66.
-        auto place = [&](unsigned long long v, int bit) {
-            if (v == 0ull) return;
-            const int r = bit - lo;
-            if (r >= 0) {
-                const unsigned long long p0 = (r < 64) ? (v << r) : 0ull;
-                const unsigned long long p1 =
-                    (r == 0) ? 0ull : (r < 64) ? (v >> (64 - r)) : (v << (r - 64));
-                add128(w0, w1, p0, p1);
-            } else {
-                digits_add(s_dig, bit >> 5, bit & 31, v);
-            }
-        };
-        if (!nonfinite) {
-            // band 1: e' in [ea, ea + 6]; band 2: e' in [eb, ea - 1]; smaller entries (rare)
-            // go to the shared digits one by one after the loop
-            const uint32_t ea = max(et, 7u) - 6u;
-            const uint32_t eb = max(ea, 8u) - 7u;
-            // A band holds normal entries only (eb >= 1): there the significand is the fraction
-            // with its hidden bit. Band membership is read off the raw exponent e, so zeros and
-            // subnormals (e = 0) join the entries below the bands.
-            unsigned long long A1 = 0ull, A2 = 0ull;
-            bool below = false;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t ax = xb[i];
-                const uint32_t e = ax >> 23;
-                const uint32_t m = (ax & 0x7FFFFFu) | 0x800000u;
-                const bool in1 = e >= ea, in2 = e >= eb;
-                const uint32_t sh = e - (in1 ? ea : eb);  // <= 6 in a band, anything outside
-                const uint32_t mm = shl32(m, sh);         // (0 for shifts past 31: unused)
-                const unsigned long long V = (unsigned long long)mm * mm;
-                if (in1) A1 += V;
-                else if (in2) A2 += V;
-                below |= !in2 && ax != 0u;
-            }
-            if (below) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const uint32_t ax = xb[i];
-                    const uint32_t e = ax >> 23;
-                    if (e < eb && ax != 0u) {
-                        const uint32_t m = e ? ((ax & 0x7FFFFFu) | 0x800000u) : ax;
-                        const int at = 2 * (int)max(e, 1u) - 2;
-                        digits_add(s_dig, at >> 5, at & 31, (unsigned long long)m * m);
-                    }
-                }
-            }
-            place(A1, 2 * (int)ea - 2);
-            place(A2, 2 * (int)eb - 2);
-        } else {  // a thread holding inf or NaN: entry by entry
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t ax = xb[i];
-                const uint32_t e = ax >> 23;
-                if (e == 0xFFu) {
-                    fl |= (ax & 0x7FFFFFu) ? 4u : 2u;
-                    continue;
-                }
-                const uint32_t m = e ? ((ax & 0x7FFFFFu) | 0x800000u) : ax;
-                place((unsigned long long)m * m, 2 * (int)max(e, 1u) - 2);
-            }
-        }
-        if (fl) atomicOr(&s_flags, fl);
+    // the warp's window: E, its lowest bit lo, the tiles it holds (0: closed), this thread's part
+    uint32_t E = 0, ntw = 0;
+    int lo = 0;
+    unsigned long long w0 = 0ull, w1 = 0ull;
+    auto warp_flush = [&]() {  // warp-uniform: every lane has the same ntw
+        if (ntw == 0) return;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const unsigned long long o0 = __shfl_down_sync(kFull, w0, off);
             const unsigned long long o1 = __shfl_down_sync(kFull, w1, off);
             add128(w0, w1, o0, o1);
         }
-        if (lane == 0) {  // W 2^lo: W < 2^124 in five 32-bit pieces from word lo / 32
+        if (lane == 0) {  // W 2^lo: W < 2^128 in five 32-bit pieces from word lo / 32
             const int i = lo >> 5, sh = lo & 31;
             digits_add(s_dig, i, sh, w0);
             digits_add(s_dig, i + 2, sh, w1);
         }
-        (void)warp;
+        w0 = w1 = 0ull;
+        ntw = 0;
+    };
+    // v 2^bit into the window when bit >= lo, else into the block's digits (v 2^(bit - lo) is
+    // below 2^118: a band sum, v < 2^64, has bit - lo <= 54, a single square, v < 2^48, <= 66)
+    auto place = [&](unsigned long long v, int bit) {
+        if (v == 0ull) return;
+        const int r = bit - lo;
+        if (r >= 0) {
+            const unsigned long long p0 = (r < 64) ? (v << r) : 0ull;
+            const unsigned long long p1 =
+                (r == 0) ? 0ull : (r < 64) ? (v >> (64 - r)) : (v << (r - 64));
+            add128(w0, w1, p0, p1);
+        } else {
+            digits_add(s_dig, bit >> 5, bit & 31, v);
+        }
+    };
+    // A segment in registers: its tiles [t0, t1), its entries [beg, beg + rm). A thread's 16
+    // entries of a tile start at offset off in the segment (below 2^32: a segment has fewer than
+    // 2^32 entries); they come by cp.async when they are 16 whole entries on a 16-byte boundary,
+    // else by plain loads. The copies run kClipStages - 1 tiles ahead of the sums, with their
+    // own segment registers.
+    auto seg_regs = [&](int seg, uint32_t& t0, uint32_t& t1, uint32_t& beg, uint32_t& rm) {
+        t0 = a.clip_off[seg];
+        t1 = a.clip_off[seg + 1];
+        beg = a.segs[seg].start;
+        rm = a.segs[seg].end - beg;
+    };
+    auto whole = [](uint32_t beg, uint32_t rm, uint32_t off) {
+        return ((beg + off) & 3u) == 0 && rm >= 16u && off <= rm - 16u;
+    };
+    uint32_t sc0, sc1, sbeg, rem;  // the segment being summed
+    seg_regs(s, sc0, sc1, sbeg, rem);
+    uint32_t ic = c0, ic0 = sc0, ic1 = sc1, ibeg = sbeg, irem = rem;  // the next tile to copy
+    int is = s, istage = 0;
+    auto issue_next = [&]() {  // one commit group per tile, empty past the block's last tile
+        if (ic < c1) {
+            if (ic == ic1) {
+                while (is + 1 < a.nseg && a.clip_off[is + 1] <= ic) ++is;
+                seg_regs(is, ic0, ic1, ibeg, irem);
+            }
+            const uint32_t o = (ic - ic0) * kClipTile + 16u * threadIdx.x;
+            if (whole(ibeg, irem, o)) {
+                const uint4* src = reinterpret_cast<const uint4*>(a.g + ((uint64_t)ibeg + o));
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    cp_async16(&s_buf[(istage * 4 + j) * kThreads + threadIdx.x], src + j);
+            }
+        }
+        cp_async_commit();
+        ++ic;
+        istage = (istage + 1 == kClipStages) ? 0 : istage + 1;
+    };
+#pragma unroll
+    for (int k = 0; k < kClipStages - 1; ++k) issue_next();
+    int stage = 0;
+    for (uint32_t c = c0; c < c1; ++c) {
+        if (c == sc1) {  // block-uniform: the next segment with tiles
+            warp_flush();
+            flush(s);
+            while (s + 1 < a.nseg && a.clip_off[s + 1] <= c) ++s;
+            seg_regs(s, sc0, sc1, sbeg, rem);
+        }
+        issue_next();  // tile c + kClipStages - 1
+        cp_async_wait<kClipStages - 1>();  // tile c's copies have landed
+        const uint32_t off = (c - sc0) * kClipTile + 16u * threadIdx.x;
+        const bool fast = whole(sbeg, rem, off);
+        // the tile's 16 entries sit in this thread's slots (entries past the segment's end as 0);
+        // they are read from there twice: for the largest and smallest, then for the bands
+        uint4* my = &s_buf[stage * 4 * kThreads + threadIdx.x];
+        if (!fast) {
+            uint32_t t[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t e = off + (uint32_t)i;  // (off + i cannot wrap: off < 2^32 - 15)
+                t[i] = (e < rem) ? __float_as_uint(a.g[(uint64_t)sbeg + e]) : 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                my[j * kThreads] = make_uint4(t[4 * j], t[4 * j + 1], t[4 * j + 2], t[4 * j + 3]);
+        }
+        // the largest and smallest |x| bits, each shifted left by one (the sign bit dropped)
+        uint32_t amax = 0, amin = 0xFFFFFFFFu;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 x = my[j * kThreads];
+            const uint32_t v[4] = {x.x << 1, x.y << 1, x.z << 1, x.w << 1};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                amax = max(amax, v[q]);
+                amin = min(amin, v[q]);
+            }
+        }
+        const bool nonfinite = amax >= 0xFF000000u;
+        // the thread's largest e' (inf and NaN count as 254: the sum is then inf or NaN anyway,
+        // and every bound below still holds)
+        const uint32_t et = max(min(amax >> 24, 254u), 1u);
+        const uint32_t em = __reduce_max_sync(kFull, et);
+        if (ntw == kWinTiles || (ntw != 0 && em > E)) warp_flush();
+        if (ntw == 0) {
+            E = em;
+            lo = max(2 * (int)em - 68, 0);
+        }
+        ++ntw;
+        uint32_t fl = 0;
+        // entry by entry from the slots: raw exponent e and significand m (with its hidden bit)
+        auto each = [&](auto&& f) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 x = my[j * kThreads];
+                const uint32_t v[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    f((v[q] << 1) >> 24, (v[q] & 0x7FFFFFu) | 0x800000u, v[q] & 0x7FFFFFFFu);
+            }
+        };
+        if (!nonfinite) {
+            // band 1: e' in [ea, ea + 6]; band 2: e' in [eb, ea - 1]; smaller entries go to the
+            // shared digits one by one
+            const uint32_t ea = max(et, 7u) - 6u;
+            const uint32_t eb = max(ea, 8u) - 7u;
+            // A band holds normal entries only (eb >= 1): there the significand is the fraction
+            // with its hidden bit. Band membership is read off the raw exponent e, so zeros and
+            // subnormals (e = 0) fall below the bands.
+            unsigned long long A1 = 0ull, A2 = 0ull;
+            each([&](uint32_t e, uint32_t m, uint32_t) { band_add(e, m, ea, eb, A1, A2); });
+            // the smallest entry's exponent below eb: some entry, maybe a zero, lies below the
+            // bands (rare for gradients without exact zeros). Each such entry takes its term
+            // back out of A2 and adds its square to the shared digits.
+            if ((amin >> 24) < eb) {
+                each([&](uint32_t e, uint32_t mb, uint32_t ax) {
+                    if (e < eb) {
+                        const uint32_t w = shl_wrap(mb, e - eb);
+                        A2 -= (unsigned long long)w * w;
+                        if (ax != 0u) {
+                            const uint32_t m = e ? mb : ax;
+                            const int at = 2 * (int)max(e, 1u) - 2;
+                            digits_add(s_dig, at >> 5, at & 31, (unsigned long long)m * m);
+                        }
+                    }
+                });
+            }
+            place(A1, 2 * (int)ea - 2);
+            place(A2, 2 * (int)eb - 2);
+        } else {  // a thread holding inf or NaN: entry by entry
+            each([&](uint32_t e, uint32_t, uint32_t ax) {
+                if (e == 0xFFu) {
+                    fl |= (ax & 0x7FFFFFu) ? 4u : 2u;
+                    return;
+                }
+                const uint32_t m = e ? ((ax & 0x7FFFFFu) | 0x800000u) : ax;
+                place((unsigned long long)m * m, 2 * (int)max(e, 1u) - 2);
+            });
+        }
+        if (fl) atomicOr(&s_flags, fl);
+        stage = (stage + 1 == kClipStages) ? 0 : stage + 1;
     }
+    warp_flush();
     flush(s);
 }
 
@@ -2414,6 +2517,8 @@ void set_kernel_attributes() {
                              (int)kSmallBytes);
         cudaFuncSetAttribute(k_select_small<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmallBytes);
+        cudaFuncSetAttribute(k_clip_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kClipSmem);
         attr_set[dev] = true;
     }
 }
@@ -2495,11 +2600,13 @@ extern "C" int dgc_compress(const float* g, float* u, float* v, int64_t n, const
                              L.nbuckets + L.max_bins + L.ptiles + 3;
     const unsigned plan_grid = (unsigned)std::min<size_t>((zero_work + 1023) / 1024 + 1,
                                                           (size_t)sms * 2);
+    set_kernel_attributes();  // before the first launch that needs more than 48 KiB
     L1(k_plan, plan_grid, 1024, a);
     if (hp.clip_on) {
-        L1(k_clip_tiles, (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(L.max_clip_tiles,
-                                                                            (uint64_t)sms * 4)),
-           kThreads, a);
+        k_clip_tiles<<<(unsigned)std::max<uint64_t>(
+                           1, std::min<uint64_t>(L.max_clip_tiles, (uint64_t)sms * 4)),
+                       kThreads, kClipSmem, s>>>(a);
+        ++launches;
         L1(k_clip_round, (unsigned)((nseg + 127) / 128), 128, a);
     }
     bool launch_failed = false;
@@ -2605,12 +2712,14 @@ extern "C" int dgc_compress_shared(const float* g, float* u, float* v, int64_t n
                                                           (size_t)sms * 2);
     const unsigned jgrid = (unsigned)std::max<uint64_t>(
         1, std::min<uint64_t>((uint64_t)sms * 4, ((uint64_t)max_count + kThreads - 1) / kThreads));
+    set_kernel_attributes();  // before the first launch that needs more than 48 KiB
     L1(k_plan, plan_grid, 1024, a);
     L1(k_shared_check, jgrid, kThreads, a, idx, count, (uint64_t)max_count);
     if (hp.clip_on) {
-        L1(k_clip_tiles, (unsigned)std::max<uint64_t>(1, std::min<uint64_t>(L.max_clip_tiles,
-                                                                            (uint64_t)sms * 4)),
-           kThreads, a);
+        k_clip_tiles<<<(unsigned)std::max<uint64_t>(
+                           1, std::min<uint64_t>(L.max_clip_tiles, (uint64_t)sms * 4)),
+                       kThreads, kClipSmem, s>>>(a);
+        ++launches;
         L1(k_clip_round, (unsigned)((nseg + 127) / 128), 128, a);
     }
     const cudaEvent_t pb = g_prof_begin, pe = g_prof_end;

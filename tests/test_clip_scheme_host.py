@@ -6,16 +6,18 @@ tiles. In a tile, warp w holds entries [512 w, 512 w + 512), 16 per thread, and 
 its squares in two 64-bit bands below its own largest entry: an entry with e' = e_band + d
 (d <= 6) adds the 64-bit product of its significand shifted left by d with itself,
 (m 2^d)^2 = m^2 4^d, which needs m 2^d to fit 32 bits. The thread's largest e' is read off its
-largest |x| bits (a thread that holds inf or NaN counts as 254). The warp adds its threads' band
-sums into a 128-bit window anchored 68 bits below its largest square. Anything lower, and the
-warp's window itself, goes to the block's 32-bit digits held in 64-bit words (shared memory).
-When a block is done with the segment, its digits, carries propagated, are added to the
-segment's words in global memory. One thread per segment then propagates the carries and
-rounds once to binary64.
+largest |x| bits (a thread that holds inf or NaN counts as 254). Each thread adds its band sums
+into its own 128-bit window, anchored 68 bits below the square of the largest e' its warp has
+seen since the window opened. A warp keeps its window over up to 16 tiles of a segment and
+flushes it (the threads' windows summed, then added to the block's digits) when a tile brings a
+larger e', after 16 tiles, and when the block leaves the segment. Anything below the window goes
+to the block's 32-bit digits held in 64-bit words (shared memory) at once. When a block is done
+with the segment, its digits, carries propagated, are added to the segment's words in global
+memory. One thread per segment then propagates the carries and rounds once to binary64.
 
 This model takes the same steps with Python integers and asserts the bounds the kernels rely
 on: a shifted significand below 2^30, a band sum below 2^64, a window term below 2^118 and a
-warp window below 2^124, a block word below 2^56 and a global word below 2^42. Its S must equal
+warp window below 2^128, a block word below 2^56 and a global word below 2^42. Its S must equal
 the oracle's, the exact sum rounded once (the DGC review's local gradient clipping; the pages
 fix no order of summation). It checks the scheme; the GPU parity tests check the kernels
 themselves against the oracle, S included.
@@ -29,6 +31,7 @@ import pytest
 TILE, THREADS, PER, WARP = 4096, 256, 16, 32
 GRID = 608  # blocks of the kernel's grid (4 per SM on 152 SMs)
 DIGITS = 20  # 32-bit digits of X = sum M 2^(2e'-2) < 2^586
+WIN_TILES = 16  # tiles a warp window holds before it is flushed
 
 
 def _digits_add(words, i, sh, x):
@@ -40,29 +43,52 @@ def _digits_add(words, i, sh, x):
     words[i + 2] += hi >> 32
 
 
-def _tile(block_words, bits):
-    """One tile (|x| bits, zero-padded to 4096) into a block's digits; returns inf/NaN flags."""
+class _Warp:
+    """A warp's window: its anchor E, lowest bit lo, tiles held, one part per thread."""
+
+    def __init__(self):
+        self.E, self.lo, self.ntw, self.win = 0, 0, 0, [0] * WARP
+
+    def flush(self, block_words):
+        if self.ntw == 0:
+            return
+        W = sum(self.win)
+        assert W < 2**128
+        _digits_add(block_words, self.lo >> 5, self.lo & 31, W & (2**64 - 1))
+        _digits_add(block_words, (self.lo >> 5) + 2, self.lo & 31, W >> 64)
+        self.ntw, self.win = 0, [0] * WARP
+
+
+def _tile(block_words, bits, warps):
+    """One tile (|x| bits, zero-padded to 4096) into its warps' windows and the block's digits;
+    returns inf/NaN flags."""
     bits = list(bits) + [0] * (TILE - len(bits))
     threads = [bits[PER * t:PER * t + PER] for t in range(THREADS)]
     # the thread's largest e' from its largest |x| bits; inf or NaN counts as 254
     et = [max(min(max(th) >> 23, 254), 1) for th in threads]
     flags = 0
-    for w0 in range(0, THREADS, WARP):
+    for wi, w0 in enumerate(range(0, THREADS, WARP)):
+        wp = warps[wi]
         em = max(et[w0:w0 + WARP])
-        lo = max(2 * em - 68, 0)  # the warp window's lowest bit of X
-        window = 0
-
-        def place(v, bit):
-            nonlocal window
-            if v == 0:
-                return
-            if bit >= lo:
-                assert v << (bit - lo) < 2**118
-                window += v << (bit - lo)
-            else:
-                _digits_add(block_words, bit >> 5, bit & 31, v)
+        if wp.ntw == WIN_TILES or (wp.ntw and em > wp.E):
+            wp.flush(block_words)
+        if wp.ntw == 0:
+            wp.E, wp.lo = em, max(2 * em - 68, 0)  # the window's lowest bit of X
+        wp.ntw += 1
+        lo = wp.lo
 
         for t in range(w0, w0 + WARP):
+            lane = t - w0
+
+            def place(v, bit):
+                if v == 0:
+                    return
+                if bit >= lo:
+                    assert v << (bit - lo) < 2**118
+                    wp.win[lane] += v << (bit - lo)
+                else:
+                    _digits_add(block_words, bit >> 5, bit & 31, v)
+
             th = threads[t]
             if any((a >> 23) == 255 for a in th):  # a thread holding inf or NaN: entry by entry
                 for a in th:
@@ -76,6 +102,17 @@ def _tile(block_words, bits):
             ea = max(et[t], 7) - 6  # band 1: e' in [ea, ea + 6]
             eb = max(ea, 8) - 7     # band 2: e' in [eb, ea - 1]
             A1 = A2 = 0
+            # the kernel's A2 in 64-bit words: every entry outside band 1 adds the square of its
+            # significand shifted by (e - eb) mod 32, truncated to 32 bits; the entries below
+            # band 2 then take their terms back out, so A2 ends exact modulo 2^64
+            A2w = 0
+            for a in th:
+                e = a >> 23
+                if e < ea:
+                    w = (((a & 0x7FFFFF) | 0x800000) << ((e - eb) % 32)) % 2**32
+                    A2w = (A2w + w * w) % 2**64
+                    if e < eb:
+                        A2w = (A2w - w * w) % 2**64
             for a in th:
                 e = a >> 23  # band membership by the raw exponent: zeros and subnormals below
                 if e >= eb:
@@ -93,12 +130,10 @@ def _tile(block_words, bits):
                     ep = max(e, 1)
                     m = (a & 0x7FFFFF) | 0x800000 if e else a
                     _digits_add(block_words, (2 * ep - 2) >> 5, (2 * ep - 2) & 31, m * m)
-            assert A1 < 2**64 and A2 < 2**64
+            assert A1 < 2**64 and A2 < 2**64 and A2w == A2
             place(A1, 2 * ea - 2)
             place(A2, 2 * eb - 2)
-        assert window < 2**124
-        _digits_add(block_words, lo >> 5, lo & 31, window & (2**64 - 1))
-        _digits_add(block_words, (lo >> 5) + 2, lo & 31, window >> 64)
+        assert max(wp.win) < 2**128
     return flags
 
 
@@ -146,9 +181,11 @@ def model_sumsq(g, grid=GRID):
     words, flags = [0] * DIGITS, 0
     G = max(1, min(len(tiles), grid))
     for b in range(G):
-        block = [0] * DIGITS
+        block, warps = [0] * DIGITS, [_Warp() for _ in range(THREADS // WARP)]
         for c in range(len(tiles) * b // G, len(tiles) * (b + 1) // G):
-            flags |= _tile(block, tiles[c])
+            flags |= _tile(block, tiles[c], warps)
+        for wp in warps:
+            wp.flush(block)
         _flush(words, block)
     assert max(words) < 2**42
     if flags & 4:
@@ -182,6 +219,15 @@ def _cases():
         c = rng.standard_normal(n).astype(np.float32)
         c[::3] = -np.inf
         out.append(("inf", c))
+    # 22 tiles: one block's warps hold a window over 16 tiles, then flush and reopen it; the
+    # scale rises tile by tile (each tile reopens the window), falls, or jumps once
+    n = 22 * TILE + 77
+    ramp = np.arange(n) // TILE
+    base = rng.standard_normal(n)
+    out.append(("22 tiles", (base * 1e-2).astype(np.float32)))
+    out.append(("22 tiles, rising", (base * 2.0 ** (3 * ramp - 30)).astype(np.float32)))
+    out.append(("22 tiles, falling", (base * 2.0 ** (30 - 3 * ramp)).astype(np.float32)))
+    out.append(("22 tiles, one jump", (base * np.where(ramp < 9, 1e-6, 1e6)).astype(np.float32)))
     return out
 
 
@@ -197,6 +243,11 @@ def test_kernel_scheme_reaches_the_oracle(orc, name, g):
 def test_block_words_bound_at_the_largest_share():
     # the most tiles a block of the 608-block grid sums for one segment (n < 2^32 entries, so
     # fewer than 2^20 tiles), each adding at most 8 x 2 + 4096 shared adds of under 2^33 to a word
+    # (two per warp flush, at most one flush per warp and tile; one per entry below the bands or
+    # the window), and the warps' last flushes
     tiles_per_block = -(-(2**20) // GRID) + 1
-    assert tiles_per_block * (8 * 2 + 4096) * 2**33 < 2**56
+    assert (tiles_per_block * (8 * 2 + 4096) + 8 * 2) * 2**33 < 2**56
+    # a warp window: 32 threads x WIN_TILES tiles x (two terms below 2^118, or 16 single
+    # squares below 2^114 for a thread holding inf or NaN)
+    assert WARP * WIN_TILES * max(2 * 2**118, 16 * 2**114) <= 2**128
     assert GRID * 2**32 < 2**42  # one add of a 32-bit digit per block

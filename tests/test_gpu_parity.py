@@ -441,6 +441,24 @@ def test_clip_extreme_magnitudes(case):
               sample_ratio=0.1, seed=case)
 
 
+@pytest.mark.slow
+def test_clip_long_tile_ranges():
+    # more 4096-entry clipping tiles than 17 per block of the 608-block grid: a warp keeps its
+    # window over 16 tiles, then flushes it; the scale changes from tile to tile (rising ramps
+    # reopen the window every tile, falling ones keep it), and the segments end mid-range
+    n = 45_000_000
+    off = np.array([0, 13_000_001, 31_000_000, n], dtype=np.int64)
+    tile = np.arange(n, dtype=np.int64) // 4096
+    ramp = np.where(tile % 60 < 30, tile % 30, 30 - tile % 30) - 15
+
+    def grads(t):
+        r = np.random.default_rng([4242, t])
+        return (r.standard_normal(n) * np.exp2(ramp - 8.0)).astype(np.float32)
+
+    run_steps(grads, off, 2, mode=dgc.SELECT_SAMPLED, sparsity=0.999, momentum=0.9,
+              clip_norm=1.0, sample_ratio=0.01, seed=3)
+
+
 @pytest.mark.parametrize("mode", ["exact", "sampled", "adacomp"])
 def test_many_segments(mode):
     # ~6000 segments of 1-300 entries around a few large ones: more segments than one wave of
