@@ -331,8 +331,16 @@ __global__ void k_dec_init(DecArgs a, const __grid_constant__ DecTabInline<kMax>
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 3) k_dec_pos(DecArgs a) {
-    __shared__ uint64_t s_scan[33];
+// Token positions, one chunk of kDecChunk tokens of one message per block (16 contiguous tokens
+// per thread). Token j advances the running position by run + 1 (an escape by 65535) and sits at
+// the position the advance reaches, less one. Within the chunk every sum is taken in 32 bits
+// (a chunk advances by less than 2^28); the chunk's base comes from a decoupled look-back over
+// the message's earlier chunks, in 64 bits. Each token's end e = position + 1 is checked against
+// n once; e <= n makes the 32-bit position exact. A token is the first of its message in the
+// tiles t with e_prev <= t kDecTile < e (e_prev the previous token's end, 0 before the first),
+// and the message's last token also fills the table for every later tile.
+__global__ void __launch_bounds__(kThreads, 4) k_dec_pos(DecArgs a) {
+    __shared__ uint32_t s_scan[33];
     __shared__ uint64_t s_lb64[33];
     __shared__ uint32_t s_lb32[2];
     __shared__ uint32_t s_chunk;
@@ -352,36 +360,55 @@ __global__ void __launch_bounds__(kThreads, 3) k_dec_pos(DecArgs a) {
     const int w = lo;
     const DecStream d = a.tab[w];
     const uint64_t lc = c - d.chunk_base;
-    const uint64_t tok0 = lc * kDecChunk;
     // with sizes in device memory the chunks are laid out for each message's bound on T: the
     // chunks past its real end have nothing to do (and no later chunk of it looks back to them)
-    if (tok0 >= d.T && lc > 0) return;
-    const uint64_t tok1 = umin64(d.T, tok0 + kDecChunk);
-    const uint16_t* runs = reinterpret_cast<const uint16_t*>(d.ptr + d.runs_off);
+    if (lc * kDecChunk >= d.T && lc > 0) return;
     constexpr int kPer = kDecChunk / kThreads;
-    static_assert(kPer % 2 == 0 && kPer <= 32, "two 16-bit advances per word, one escape bit each");
+    static_assert(kPer % 4 == 0 && kPer <= 32, "pairs of advances per word, one escape bit each");
+    // this thread's tokens [j0, j0 + cnt) of the message
+    const uint64_t j0 = lc * kDecChunk + (uint64_t)threadIdx.x * kPer;
+    const uint32_t cnt = (uint32_t)(j0 >= d.T ? 0 : umin64(kPer, d.T - j0));
     // each token's advance (an escape skips 65535, another token run + 1 <= 65535) in 16 bits,
     // two per word, and which tokens are escapes
     uint32_t adv2[kPer / 2];
-    uint32_t esc = 0;
-    uint64_t mine = 0;
+    uint32_t esc = 0, mine = 0;
+    const uint8_t* runs_b = d.ptr + d.runs_off;
+    if (!a.qbits && cnt == kPer) {
+        // binary32 messages keep their runs block on a 4-byte boundary and pad the message to a
+        // multiple of 4 bytes: the runs come two per 32-bit load
+        const uint32_t* r2 = reinterpret_cast<const uint32_t*>(runs_b) + j0 / 2;
+        uint32_t raw[kPer / 2];
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-        const uint64_t j = tok0 + (uint64_t)threadIdx.x * kPer + i;
-        uint32_t adv = 0;
-        if (j < tok1) {
-            const uint32_t r = runs[j];
-            adv = (r == kRunEscape) ? kRunEscape : r + 1;
-            if (r == kRunEscape) esc |= 1u << i;
+        for (int k = 0; k < kPer / 2; ++k) raw[k] = r2[k];
+#pragma unroll
+        for (int k = 0; k < kPer / 2; ++k) {
+            const uint32_t r0 = raw[k] & 0xFFFFu, r1 = raw[k] >> 16;
+            const uint32_t a0 = (r0 == kRunEscape) ? kRunEscape : r0 + 1;
+            const uint32_t a1 = (r1 == kRunEscape) ? kRunEscape : r1 + 1;
+            esc |= (uint32_t)(r0 == kRunEscape) << (2 * k);
+            esc |= (uint32_t)(r1 == kRunEscape) << (2 * k + 1);
+            adv2[k] = a0 | (a1 << 16);
+            mine += a0 + a1;
         }
-        if (i & 1) adv2[i / 2] |= adv << 16;
-        else adv2[i / 2] = adv;
-        mine += adv;
+    } else {
+        const uint16_t* runs = reinterpret_cast<const uint16_t*>(runs_b);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            uint32_t adv = 0;
+            if ((uint32_t)i < cnt) {
+                const uint32_t r = runs[j0 + i];
+                adv = (r == kRunEscape) ? kRunEscape : r + 1;
+                esc |= (uint32_t)(r == kRunEscape) << i;
+            }
+            if (i & 1) adv2[i / 2] |= adv << 16;
+            else adv2[i / 2] = adv;
+            mine += adv;
+        }
     }
-    uint64_t agg;
-    const uint64_t ex = block_excl_scan<kThreads>(mine, s_scan, &agg);
-    // a message's first chunk starts at position -1; the others look back over their
-    // predecessors with the whole block (kThreads of them per round trip)
+    uint32_t agg;
+    const uint32_t ex = block_excl_scan<kThreads>(mine, s_scan, &agg);
+    // a message's first chunk starts at end 0; the others look back over their predecessors
+    // with the whole block (kThreads of them per round trip)
     uint64_t base = 0;
     if (lc == 0) {
         if (threadIdx.x == 0) st_relaxed(&a.st[c], kFlagInc | agg);
@@ -389,27 +416,54 @@ __global__ void __launch_bounds__(kThreads, 3) k_dec_pos(DecArgs a) {
         base = block_lookback<kThreads>(a.st, (uint32_t)c, agg, a.spin_limit, a.status, nullptr,
                                         s_lb32, s_lb64);
     }
-    uint64_t P = base + ex;  // advances before this thread's first token
+    if (cnt == 0) return;
+    const uint64_t start = base + ex;  // the end of the token before this thread's first
+    // ends up to lim (<= n) are positions inside the dense array
+    const uint32_t lim = (start >= a.n) ? 0u : (uint32_t)umin64(a.n - start, 0xFFFFFFFFull);
+    const uint32_t s32 = (uint32_t)start;  // exact while start < n
+    uint32_t pos[kPer];
+    uint32_t cum = 0;  // advances of this thread's tokens so far
     bool bad = false;
+    const uint32_t ntiles = (uint32_t)a.ntiles;
+    uint32_t* ts_w = a.ts + w;  // ts[t * W + w]
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-        const uint64_t j = tok0 + (uint64_t)threadIdx.x * kPer + i;
-        if (j >= tok1) break;
-        const int64_t prev = (int64_t)P - 1;  // position of the previous token
-        P += (i & 1) ? (adv2[i / 2] >> 16) : (adv2[i / 2] & 0xFFFFu);
-        const int64_t p = (int64_t)P - 1;
-        if ((uint64_t)p >= a.n) bad = true;
-        a.pos[d.tok_base + j] = ((esc >> i) & 1u) ? kEscPos : (uint32_t)p;
-        // tiles whose first token of this message is j
-        int64_t t0 = (prev < 0) ? 0 : prev / kDecTile + 1;
-        int64_t t1 = p / kDecTile;
-        if (t1 > (int64_t)a.ntiles) t1 = (int64_t)a.ntiles;
-        for (int64_t t = t0; t <= t1; ++t) a.ts[(uint64_t)t * a.W + w] = (uint32_t)j;
-        if (j == d.T - 1)
-            for (int64_t t = p / kDecTile + 1; t <= (int64_t)a.ntiles; ++t)
-                a.ts[(uint64_t)t * a.W + w] = (uint32_t)d.T;
+        pos[i] = 0;
+        if ((uint32_t)i >= cnt || bad) continue;
+        const uint32_t adv = (i & 1) ? (adv2[i / 2] >> 16) : (adv2[i / 2] & 0xFFFFu);
+        const uint32_t cprev = cum;
+        cum += adv;
+        if (cum > lim) {  // past the end of the dense array: a malformed message
+            bad = true;
+            continue;
+        }
+        const uint32_t e = s32 + cum, ep = s32 + cprev;  // this token's and the previous end
+        pos[i] = ((esc >> i) & 1u) ? kEscPos : e - 1u;
+        // tiles whose first token of this message is this one
+        const uint32_t t0 = ep / kDecTile + ((ep % kDecTile) != 0);
+        const uint32_t t1 = min((e - 1u) / kDecTile, ntiles);
+        for (uint32_t t = t0; t <= t1; ++t) ts_w[(uint64_t)t * a.W] = (uint32_t)(j0 + i);
+        if (j0 + i == d.T - 1)
+            for (uint32_t t = (e - 1u) / kDecTile + 1; t <= ntiles; ++t)
+                ts_w[(uint64_t)t * a.W] = (uint32_t)d.T;
     }
-    if (bad) mark_bad(a, w);
+    if (bad) {
+        mark_bad(a, w);
+        return;
+    }
+    // the positions: four 16-byte stores when the thread's 16 tokens are whole (message bases
+    // in the position array are multiples of 4)
+    uint32_t* out = a.pos + d.tok_base + j0;
+    if (cnt == kPer) {
+#pragma unroll
+        for (int k = 0; k < kPer / 4; ++k)
+            reinterpret_cast<uint4*>(out)[k] =
+                make_uint4(pos[4 * k], pos[4 * k + 1], pos[4 * k + 2], pos[4 * k + 3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+            if ((uint32_t)i < cnt) out[i] = pos[i];
+    }
 }
 
 // token j's value: binary32 bits (version 1) or the integer, sign-extended (version 2)
@@ -711,6 +765,180 @@ __global__ void __launch_bounds__(kThreads, 5) k_dec_tiles(DecArgs a) {
     }
 }
 
+// Binary32 sums of several messages into the dense array (not the SGD step, not integer
+// messages), one tile of kSumTile entries (kSumTile / kDecTile rows of the first-token table)
+// per block of kSumThreads threads. The block first stores +0 over its tile (unless
+// accumulating). The tile's tokens are staged in shared memory, kSumCap at a time, message-major
+// and spread over all threads, so neighbouring threads load neighbouring tokens of a message.
+// Staging marks each position in two bitmaps: one token landed, a second one landed. After a
+// barrier, a token whose position holds no other adds its value onto the position's value (+0
+// in the first round of a plain sum, the stored value otherwise) and stores it; the rest, where
+// several messages meet, go to a short list, and there the token of the smallest message adds
+// the position's values in message order. A message reaches a position at most once, so the
+// smallest message is unique. Messages go in groups of kSumThreads, and a group whose tokens
+// exceed the staging slots goes in message-major rounds; groups and rounds follow the message
+// order and every round adds onto what the earlier ones stored, so each position's sum takes the
+// learners' order throughout.
+constexpr int kSumTile = 4 * kDecTile;
+constexpr int kSumRows = kSumTile / kDecTile;  // first-token table rows per tile
+constexpr int kSumThreads = 256;
+constexpr int kSumCap = 2048;  // tokens staged per round
+constexpr int kSumWords = kSumTile / 32;
+constexpr uint16_t kNoLp = 0xFFFFu;  // an escape, or a position outside the tile
+static_assert(kSumCap <= 0xFFFF && kSumTile < 0xFFFF, "16-bit slots and positions");
+
+__global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
+    constexpr int kPer = kSumCap / kSumThreads;  // staged slots per thread
+    __shared__ uint32_t s_val[kSumCap];
+    __shared__ uint16_t s_lp[kSumCap];     // position within the tile, or kNoLp
+    __shared__ uint16_t s_msg[kSumCap];    // message index within the group
+    __shared__ uint16_t s_multi[kSumCap];  // slots whose position holds several tokens
+    __shared__ uint16_t s_sorted[kSumCap]; // the same slots by (position, message)
+    __shared__ uint32_t s_one[kSumWords];  // a token landed at the position
+    __shared__ uint32_t s_two[kSumWords];  // a second token landed there
+    __shared__ uint64_t s_tb[kSumThreads];          // the group's messages: position base
+    __shared__ const uint32_t* s_vp[kSumThreads];   // and their values (binary32)
+    __shared__ uint32_t s_scan[33];
+    __shared__ uint32_t s_nmulti;
+    if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
+    const uint64_t p0 = (uint64_t)blockIdx.x * kSumTile;
+    const uint32_t len = (uint32_t)umin64(kSumTile, a.n - p0);
+    const uint64_t row0 = (uint64_t)blockIdx.x * kSumRows;
+    const uint64_t row1 = umin64(row0 + kSumRows, a.ntiles);
+    float* out = a.dense + p0;
+    // the plain sum starts from +0 everywhere: the tile is cleared once, after the first
+    // round's loads are in flight (they would wait behind the stores otherwise) and before the
+    // barrier that precedes every store of a sum
+    bool cleared = a.accumulate != 0;
+    auto clear_tile = [&]() {
+        if (len == kSumTile && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+#pragma unroll 4
+            for (uint32_t i = threadIdx.x; i < kSumTile / 4; i += kSumThreads)
+                reinterpret_cast<float4*>(out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            for (uint32_t i = threadIdx.x; i < len; i += kSumThreads) out[i] = 0.0f;
+        }
+        cleared = true;
+    };
+    auto clear_marks = [&]() {
+        for (uint32_t i = threadIdx.x; i < kSumWords; i += kSumThreads) {
+            s_one[i] = 0;
+            s_two[i] = 0;
+        }
+        if (threadIdx.x == 0) s_nmulti = 0;
+    };
+    clear_marks();
+    bool first = !a.accumulate;  // no round has stored a sum yet: they start from +0
+    for (int wb = 0; wb < a.W; wb += kSumThreads) {
+        const int w = wb + (int)threadIdx.x;
+        uint32_t cnt = 0, j0 = 0;
+        if (w < a.W && a.tab[w].T > 0) {
+            j0 = a.ts[row0 * a.W + w];
+            cnt = a.ts[row1 * a.W + w] - j0;
+        }
+        if (w < a.W) {  // where the message's positions and values start
+            const DecStream& d = a.tab[w];
+            s_tb[threadIdx.x] = d.tok_base;
+            s_vp[threadIdx.x] = reinterpret_cast<const uint32_t*>(d.ptr + 32);
+        }
+        uint32_t total;
+        const uint32_t ex = block_excl_scan<kSumThreads>(cnt, s_scan, &total);
+        const int nw = min(kSumThreads, a.W - wb);
+        for (uint32_t r0 = 0; r0 < total; r0 += kSumCap) {
+            const uint32_t m = min((uint32_t)kSumCap, total - r0);
+            // stage in two steps: each message's own thread writes, for its tokens among this
+            // round's, the message and the token's index into their slots; then every thread
+            // loads the position and value of its slots (neighbouring slots, neighbouring tokens
+            // of one message), all of its loads issued before any is used
+            if ((int)threadIdx.x < nw && ex < r0 + m && ex + cnt > r0) {
+                const uint32_t f0 = max(ex, r0), f1 = min(ex + cnt, r0 + m);  // flattened
+                for (uint32_t f = f0; f < f1; ++f) {
+                    s_val[f - r0] = j0 + (f - ex);
+                    s_msg[f - r0] = (uint16_t)threadIdx.x;
+                }
+            }
+            __syncthreads();  // the round's slots name their tokens
+            uint32_t pv[kPer], rv[kPer];
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const uint32_t i = threadIdx.x + (uint32_t)k * kSumThreads;
+                if (i >= m) continue;
+                const uint32_t l = s_msg[i], j = s_val[i];
+                pv[k] = a.pos[s_tb[l] + j];
+                rv[k] = s_vp[l][j];
+            }
+            if (!cleared) clear_tile();
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const uint32_t i = threadIdx.x + (uint32_t)k * kSumThreads;
+                if (i >= m) continue;
+                const uint32_t p = pv[k];
+                const bool in = p != kEscPos && p >= p0 && p < p0 + len;
+                const uint32_t lp = in ? (uint32_t)(p - p0) : kNoLp;
+                s_lp[i] = (uint16_t)lp;
+                s_val[i] = rv[k];
+                if (in) {
+                    const uint32_t bit = 1u << (lp & 31);
+                    if (atomicOr(&s_one[lp >> 5], bit) & bit) atomicOr(&s_two[lp >> 5], bit);
+                }
+            }
+            __syncthreads();  // the round's tokens and marks
+            // a position with one token of the round: that token's value, added on
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const uint32_t i = threadIdx.x + (uint32_t)k * kSumThreads;
+                if (i >= m) continue;
+                const uint32_t lp = s_lp[i];
+                if (lp == kNoLp) continue;
+                if (s_two[lp >> 5] & (1u << (lp & 31))) {
+                    s_multi[atomicAdd(&s_nmulti, 1u)] = (uint16_t)i;
+                    continue;
+                }
+                out[lp] = __fadd_rn(first ? 0.0f : out[lp], __uint_as_float(s_val[i]));
+            }
+            __syncthreads();  // the list of tokens at shared positions
+            // positions several messages reach: those tokens sorted by (position, message), each
+            // by its rank among them; then the first token of each position adds the position's
+            // values in message order
+            const uint32_t nm = s_nmulti;
+            if (nm > 0) {  // block-uniform
+                for (uint32_t k = threadIdx.x; k < nm; k += kSumThreads) {
+                    const uint32_t i = s_multi[k];
+                    const uint32_t key = ((uint32_t)s_lp[i] << 16) | s_msg[i];
+                    uint32_t rank = 0;
+                    for (uint32_t q = 0; q < nm; ++q) {
+                        const uint32_t iq = s_multi[q];
+                        rank += (((uint32_t)s_lp[iq] << 16) | s_msg[iq]) < key;
+                    }
+                    s_sorted[rank] = (uint16_t)i;  // keys are distinct: ranks are too
+                }
+                __syncthreads();
+                for (uint32_t r = threadIdx.x; r < nm; r += kSumThreads) {
+                    const uint32_t i = s_sorted[r];
+                    const uint32_t lp = s_lp[i];
+                    if (r > 0 && s_lp[s_sorted[r - 1]] == lp) continue;
+                    float acc = __fadd_rn(first ? 0.0f : out[lp], __uint_as_float(s_val[i]));
+                    for (uint32_t r2 = r + 1; r2 < nm; ++r2) {
+                        const uint32_t i2 = s_sorted[r2];
+                        if (s_lp[i2] != lp) break;
+                        acc = __fadd_rn(acc, __uint_as_float(s_val[i2]));
+                    }
+                    out[lp] = acc;
+                }
+            }
+            first = false;
+            if (r0 + kSumCap < total || wb + kSumThreads < a.W) {
+                // another round follows: its staging waits for every use of this one, and its
+                // marks start clear (the stored sums are visible to it after the barriers)
+                __syncthreads();
+                clear_marks();
+                __syncthreads();
+            }
+        }
+    }
+    if (!cleared) clear_tile();  // a tile no token reaches
+}
+
 // One message (W = 1): its positions are distinct, so its values can be added in parallel. The
 // dense output is first cleared by a streaming store pass (unless accumulating), then each value
 // token adds itself to its position: the same single binary32 addition per value as the tile
@@ -785,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads) k_sum_shared(const float* const* val
 
 struct DecLayout {
     size_t ctl, tab, bad, pos, st, ts, total;
-    uint64_t sum_T, nchunks, ntiles;
+    uint64_t sum_T, pos_len, nchunks, ntiles;
 };
 
 // bounds: stream_bytes are upper bounds on binary32 messages' sizes (their T found on the
@@ -793,24 +1021,27 @@ struct DecLayout {
 int dec_layout(int32_t W, const uint64_t* stream_bytes, int64_t n, int qbits, DecLayout* L,
                std::vector<DecStream>* tab, bool bounds = false) {
     L->sum_T = 0;
+    L->pos_len = 0;
     L->nchunks = 0;
     for (int w = 0; w < W; ++w) {
         uint64_t T;
         if (bounds) T = stream_bytes[w] >= 32 ? (stream_bytes[w] - 32) / 6 : 0;
         else if (!stream_tokens(stream_bytes[w], qbits, &T)) return DGC_ECORRUPT;
         const uint64_t ro = qbits ? q_runs_offset(T, qbits) : 32 + 4 * T;
-        if (tab) (*tab)[w] = DecStream{nullptr, T, L->sum_T, L->nchunks, ro};
+        // a message's positions start on a multiple of 4 entries (16-byte stores)
+        if (tab) (*tab)[w] = DecStream{nullptr, T, L->pos_len, L->nchunks, ro};
         L->sum_T += T;
+        L->pos_len += (T + 3) & ~3ull;
         L->nchunks += (T + kDecChunk - 1) / kDecChunk;
     }
-    if (tab) (*tab)[W] = DecStream{nullptr, 0, L->sum_T, L->nchunks, 0};
+    if (tab) (*tab)[W] = DecStream{nullptr, 0, L->pos_len, L->nchunks, 0};
     L->ntiles = ((uint64_t)n + kDecTile - 1) / kDecTile;
     size_t o = 0;
     auto take = [&](size_t b) { size_t at = o; o = align256(o + b); return at; };
     L->ctl = take(sizeof(DecCtl));
     L->tab = take(sizeof(DecStream) * (size_t)(W + 1));
     L->bad = take(sizeof(uint32_t) * (size_t)(W > 0 ? W : 1));
-    L->pos = take(sizeof(uint32_t) * (size_t)L->sum_T);
+    L->pos = take(sizeof(uint32_t) * (size_t)L->pos_len);
     L->st = take(sizeof(uint64_t) * (size_t)(L->nchunks + 1));
     L->ts = take(sizeof(uint32_t) * (size_t)(L->ntiles + 1) * (size_t)(W > 0 ? W : 1));
     L->total = o;
@@ -995,7 +1226,12 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
         k_dec_pos<<<(unsigned)L.nchunks, kThreads, 0, s>>>(a);
         ++launches;
     }
-    if (W == 1) {  // runs after the positions are checked: a malformed message changes nothing
+    if (!qbits && !apply) {  // binary32 sums, one message or several
+        if (L.ntiles > 0) {
+            k_dec_sum<<<(unsigned)((L.ntiles + kSumRows - 1) / kSumRows), kSumThreads, 0, s>>>(a);
+            ++launches;
+        }
+    } else if (W == 1) {  // runs after the positions are checked: a malformed message changes nothing
         if (!accumulate && !apply && n > 0) {
             const int sms = dgc_internal_sm_count();
             if (sms <= 0) return DGC_ECUDA;
