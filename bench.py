@@ -857,11 +857,37 @@ def run_aggregation(dev, peak, W=64, n=25_557_032, reps=20, flush=None):
     dense = torch.empty(n, dtype=torch.float32, device=dev)
     w_vec = torch.zeros(n, dtype=torch.float32, device=dev)
     l0 = dgc.dgc_launch_count()
-    t_dec = median_ms(lambda: dgc.dgc_decode_accumulate(msgs, sizes, dense, n, False, status, ws,
-                                                        ws_bytes=ws_bytes), reps, flush)
+    t_dec_call = median_ms(lambda: dgc.dgc_decode_accumulate(msgs, sizes, dense, n, False, status,
+                                                             ws, ws_bytes=ws_bytes), reps, flush)
     launches_dec = (dgc.dgc_launch_count() - l0) // (reps + 3)
-    t_app = median_ms(lambda: dgc.dgc_decode_apply(msgs, sizes, w_vec, n, 0.01 / W, status, ws,
-                                                   ws_bytes=ws_bytes), reps, flush)
+    t_app_call = median_ms(lambda: dgc.dgc_decode_apply(msgs, sizes, w_vec, n, 0.01 / W, status,
+                                                        ws, ws_bytes=ws_bytes), reps, flush)
+    # the same two calls as a trainer replays them each step: the sizes in device memory (as
+    # dgc_encode leaves them), each call captured once into a CUDA graph (the message table
+    # travels in the kernels' parameters up to 96 messages)
+    t_dec, t_app, launch = t_dec_call, t_app_call, "host calls"
+    if W <= 96:
+        sizes_dev = torch.tensor(sizes, dtype=torch.int64, device=dev)
+        ws_dev = torch.empty(dgc.dgc_decode_workspace_bound(sizes, n), dtype=torch.uint8,
+                             device=dev)
+        acc_call = lambda: dgc.dgc_decode_accumulate_dev(  # noqa: E731
+            msgs, sizes_dev, sizes, dense, n, False, status, ws_dev)
+        app_call = lambda: dgc.dgc_decode_apply_dev(  # noqa: E731
+            msgs, sizes_dev, sizes, w_vec, n, 0.01 / W, status, ws_dev)
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        graphs = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph())
+        with torch.cuda.stream(side):
+            acc_call()
+            app_call()
+            with torch.cuda.graph(graphs[0], stream=side):
+                acc_call()
+            with torch.cuda.graph(graphs[1], stream=side):
+                app_call()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        t_dec = median_ms(graphs[0].replay, reps, flush)
+        t_app = median_ms(graphs[1].replay, reps, flush)
+        launch = "CUDA graph replays of dgc_decode_accumulate_dev / dgc_decode_apply_dev"
     if dgc.dgc_read_status(status) != 0:
         raise RuntimeError("aggregation: decode reported an error")
     tokens = sum((s - 32) // 6 for s in sizes)  # values + escapes (the pad is under 6 bytes)
@@ -886,7 +912,8 @@ def run_aggregation(dev, peak, W=64, n=25_557_032, reps=20, flush=None):
                                      "frac": round(app_bytes / (t_app / 1e3) / 1e9 / peak, 4),
                                      "bytes_rule": "messages read + 8 B per token + 8 B per "
                                                    "touched weight (read and write)"},
-           "touched": touched, "launches_per_decode": launches_dec,
+           "touched": touched, "launches_per_decode": launches_dec, "launch": launch,
+           "host_call_ms": {"decode": round(t_dec_call, 4), "decode_apply": round(t_app_call, 4)},
            "l2": "L2 flushed before every call (the 102 MB dense array fits in L2)"}
     del msgs, ws, dense, w_vec
     torch.cuda.empty_cache()

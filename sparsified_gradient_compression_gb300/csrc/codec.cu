@@ -251,7 +251,7 @@ struct DecCtl {
 };
 
 struct DecArgs {
-    const DecStream* tab;  // W + 1 entries (the last holds the totals)
+    DecStream* tab;  // W + 1 entries (the last holds the totals), in the workspace
     int32_t W;
     uint64_t n;
     float* dense;      // the dense sum, or the weights w when apply is set
@@ -262,7 +262,6 @@ struct DecArgs {
     float alpha;       // version 2: the shared scale every message must carry
     int32_t* status;
     DecCtl* ctl;
-    uint32_t* bad;
     uint32_t* pos;
     uint64_t* st;
     uint32_t* ts;  // (ntiles + 1) x W first-token table
@@ -272,8 +271,7 @@ struct DecArgs {
     uint32_t spin_limit;
 };
 
-__device__ __forceinline__ void mark_bad(const DecArgs& a, int w) {
-    a.bad[w] = 1;
+__device__ __forceinline__ void mark_bad(const DecArgs& a) {
     atomicExch(&a.ctl->any_bad, 1u);
     report(a.status, DGC_ECORRUPT);
 }
@@ -289,46 +287,18 @@ struct DecTabInline {
 static_assert(sizeof(DecTabInline<kDecInline>) + sizeof(DecArgs) <= 4096,
               "within the kernel parameter space");
 
-// Zeroes the look-back words, writes the message table into the workspace when it comes with
-// the launch (kMax entries at most: one message, or up to kDecInline), and checks every header
-// (ctl was zeroed before this kernel).
-template <int kMax>
-__global__ void k_dec_init(DecArgs a, const __grid_constant__ DecTabInline<kMax> t) {
-    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-    for (uint64_t i = tid; i <= a.nchunks; i += stride) a.st[i] = 0;
-    const bool inl = a.W <= kMax;
-    DecStream* tab = const_cast<DecStream*>(a.tab);
-    if (inl)
-        for (uint64_t w = tid; w <= (uint64_t)a.W; w += stride) tab[w] = t.e[w];
-    for (uint64_t w = tid; w < (uint64_t)a.W; w += stride) {
-        DecStream d = inl ? t.e[w] : a.tab[w];  // (the same thread wrote tab[w] above)
-        a.bad[w] = 0;
-        if (a.dev_bytes) {
-            // sizes in device memory: the table holds each message's bound on T (from its bound
-            // on bytes); the real T comes from the size, which must be a message's and within
-            // the bound, else the call fails as for a malformed message
-            uint64_t T = 0;
-            if (!stream_tokens(a.dev_bytes[w], 0, &T) || T > d.T) {
-                tab[w].T = 0;
-                mark_bad(a, (int)w);
-                continue;
-            }
-            d.T = T;
-            d.runs_off = 32 + 4 * T;
-            tab[w].T = T;
-            tab[w].runs_off = d.runs_off;
-        }
-        const uint64_t* h = reinterpret_cast<const uint64_t*>(d.ptr);
-        const uint64_t h0 = h[0];
-        bool ok = (uint32_t)h0 == kMagic && h[1] == a.n && h[2] == d.T;
-        if (a.qbits)  // version 2: the receiver's width and alpha, bit for bit
-            ok = ok && ((h0 >> 32) & 0xFFFFu) == 2u && (h0 >> 48) == (uint64_t)a.qbits &&
-                 (uint32_t)h[3] == __float_as_uint(a.alpha);
-        else
-            ok = ok && ((h0 >> 32) & 0xFFFFu) == 1u;
-        if (!ok) mark_bad(a, (int)w);
-    }
+// A message's header: magic, version, n and T (version 2: also the receiver's width and
+// alpha, bit for bit).
+__device__ bool header_ok(const DecArgs& a, const DecStream& d) {
+    const uint64_t* h = reinterpret_cast<const uint64_t*>(d.ptr);
+    const uint64_t h0 = h[0];
+    bool ok = (uint32_t)h0 == kMagic && h[1] == a.n && h[2] == d.T;
+    if (a.qbits)
+        ok = ok && ((h0 >> 32) & 0xFFFFu) == 2u && (h0 >> 48) == (uint64_t)a.qbits &&
+             (uint32_t)h[3] == __float_as_uint(a.alpha);
+    else
+        ok = ok && ((h0 >> 32) & 0xFFFFu) == 1u;
+    return ok;
 }
 
 // Token positions, one chunk of kDecChunk tokens of one message per block (16 contiguous tokens
@@ -339,30 +309,66 @@ __global__ void k_dec_init(DecArgs a, const __grid_constant__ DecTabInline<kMax>
 // n once; e <= n makes the 32-bit position exact. A token is the first of its message in the
 // tiles t with e_prev <= t kDecTile < e (e_prev the previous token's end, 0 before the first),
 // and the message's last token also fills the table for every later tile.
-__global__ void __launch_bounds__(kThreads, 4) k_dec_pos(DecArgs a) {
+//
+// Every message owns at least one chunk, and the block of its first chunk also checks the
+// message's header and writes its entry of the workspace table for the kernels that follow
+// (with the token count read from device memory when the sizes are there); for a message
+// without tokens it fills the message's column of the first-token table with 0.
+template <int kMax>
+__global__ void __launch_bounds__(kThreads, 4)
+    k_dec_pos(DecArgs a, const __grid_constant__ DecTabInline<kMax> t) {
     __shared__ uint32_t s_scan[33];
     __shared__ uint64_t s_lb64[33];
     __shared__ uint32_t s_lb32[2];
     __shared__ uint32_t s_chunk;
     __shared__ uint64_t s_cb[kThreads];  // the messages' first chunks, when W <= kThreads
+    // the host's table: with the launch (up to kMax messages), else copied to the workspace
+    const DecStream* tin = (a.W <= kMax) ? t.e : a.tab;
     if (threadIdx.x == 0) s_chunk = atomicAdd(&a.ctl->ticket, 1u);
     const bool staged = a.W <= kThreads;
-    if (staged && threadIdx.x < a.W) s_cb[threadIdx.x] = a.tab[threadIdx.x].chunk_base;
+    if (staged && threadIdx.x < a.W) s_cb[threadIdx.x] = tin[threadIdx.x].chunk_base;
     __syncthreads();
     const uint64_t c = s_chunk;
-    // the message that owns chunk c: the last one starting at or before c (empty ones own
-    // nothing), searched in shared memory (one parallel load instead of a chain of them)
+    // the message that owns chunk c: the last one starting at or before c, searched in shared
+    // memory (one parallel load instead of a chain of them)
     int lo = 0, hi = a.W;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if ((staged ? s_cb[mid] : a.tab[mid].chunk_base) <= c) lo = mid; else hi = mid;
+        if ((staged ? s_cb[mid] : tin[mid].chunk_base) <= c) lo = mid; else hi = mid;
     }
     const int w = lo;
-    const DecStream d = a.tab[w];
+    DecStream d = tin[w];
+    bool size_ok = true;
+    if (a.dev_bytes) {
+        // sizes in device memory: the table holds each message's bound on T (from its bound on
+        // bytes); the real T comes from the size, which must be a message's and within the
+        // bound, else the call fails as for a malformed message (and the message counts as
+        // empty). Every block of the message reads it alike.
+        uint64_t T = 0;
+        size_ok = stream_tokens(a.dev_bytes[w], 0, &T) && T <= d.T;
+        d.T = size_ok ? T : 0;
+        d.runs_off = 32 + 4 * d.T;
+    }
     const uint64_t lc = c - d.chunk_base;
-    // with sizes in device memory the chunks are laid out for each message's bound on T: the
-    // chunks past its real end have nothing to do (and no later chunk of it looks back to them)
-    if (lc * kDecChunk >= d.T && lc > 0) return;
+    if (lc == 0) {
+        if (threadIdx.x == 0) {
+            // (with more than kMax messages and sizes in device memory, the other chunks of the
+            // message may read this entry as it changes: they take only fields that stay the
+            // same, and T from the size themselves)
+            if (a.W <= kMax || a.dev_bytes) a.tab[w] = d;
+            if (!size_ok || !header_ok(a, d)) mark_bad(a);
+        }
+        if (d.T == 0) {  // no token: its first token in every tile is 0 (= T)
+            for (uint64_t tt = threadIdx.x; tt <= a.ntiles; tt += kThreads)
+                a.ts[tt * a.W + w] = 0;
+            return;  // (no later chunk of this message looks back to this one)
+        }
+    } else if (lc * kDecChunk >= d.T) {
+        // with sizes in device memory the chunks are laid out for each message's bound on T: the
+        // chunks past its real end have nothing to do (and no later chunk of it looks back to
+        // them)
+        return;
+    }
     constexpr int kPer = kDecChunk / kThreads;
     static_assert(kPer % 4 == 0 && kPer <= 32, "pairs of advances per word, one escape bit each");
     // this thread's tokens [j0, j0 + cnt) of the message
@@ -448,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_dec_pos(DecArgs a) {
                 ts_w[(uint64_t)t * a.W] = (uint32_t)d.T;
     }
     if (bad) {
-        mark_bad(a, w);
+        mark_bad(a);
         return;
     }
     // the positions: four 16-byte stores when the thread's 16 tokens are whole (message bases
@@ -1012,7 +1018,7 @@ __global__ void __launch_bounds__(kThreads) k_sum_shared(const float* const* val
 }
 
 struct DecLayout {
-    size_t ctl, tab, bad, pos, st, ts, total;
+    size_t ctl, tab, pos, st, ts, clear, total;
     uint64_t sum_T, pos_len, nchunks, ntiles;
 };
 
@@ -1032,17 +1038,18 @@ int dec_layout(int32_t W, const uint64_t* stream_bytes, int64_t n, int qbits, De
         if (tab) (*tab)[w] = DecStream{nullptr, T, L->pos_len, L->nchunks, ro};
         L->sum_T += T;
         L->pos_len += (T + 3) & ~3ull;
-        L->nchunks += (T + kDecChunk - 1) / kDecChunk;
+        L->nchunks += std::max<uint64_t>(1, (T + kDecChunk - 1) / kDecChunk);  // one at least
     }
     if (tab) (*tab)[W] = DecStream{nullptr, 0, L->pos_len, L->nchunks, 0};
     L->ntiles = ((uint64_t)n + kDecTile - 1) / kDecTile;
     size_t o = 0;
     auto take = [&](size_t b) { size_t at = o; o = align256(o + b); return at; };
+    // the control words and the look-back words first: one memset clears both
     L->ctl = take(sizeof(DecCtl));
-    L->tab = take(sizeof(DecStream) * (size_t)(W + 1));
-    L->bad = take(sizeof(uint32_t) * (size_t)(W > 0 ? W : 1));
-    L->pos = take(sizeof(uint32_t) * (size_t)L->pos_len);
     L->st = take(sizeof(uint64_t) * (size_t)(L->nchunks + 1));
+    L->clear = o;
+    L->tab = take(sizeof(DecStream) * (size_t)(W + 1));
+    L->pos = take(sizeof(uint32_t) * (size_t)L->pos_len);
     L->ts = take(sizeof(uint32_t) * (size_t)(L->ntiles + 1) * (size_t)(W > 0 ? W : 1));
     L->total = o;
     return DGC_OK;
@@ -1182,7 +1189,7 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
     for (int w = 0; w < W; ++w) tab[w].ptr = streams[w];
     char* p = static_cast<char*>(ws);
     DecArgs a{};
-    a.tab = reinterpret_cast<const DecStream*>(p + L.tab);
+    a.tab = reinterpret_cast<DecStream*>(p + L.tab);
     a.W = W;
     a.n = (uint64_t)n;
     a.dense = dense;
@@ -1193,7 +1200,6 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
     a.alpha = alpha;
     a.status = status;
     a.ctl = reinterpret_cast<DecCtl*>(p + L.ctl);
-    a.bad = reinterpret_cast<uint32_t*>(p + L.bad);
     a.pos = reinterpret_cast<uint32_t*>(p + L.pos);
     a.st = reinterpret_cast<uint64_t*>(p + L.st);
     a.ts = reinterpret_cast<uint32_t*>(p + L.ts);
@@ -1207,23 +1213,18 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
     if (W > kDecInline && cudaMemcpyAsync(p + L.tab, tab.data(), sizeof(DecStream) * tab.size(),
                                           cudaMemcpyHostToDevice, s) != cudaSuccess)
         return DGC_ECUDA;
-    if (cudaMemsetAsync(p + L.ctl, 0, sizeof(DecCtl), s) != cudaSuccess) return DGC_ECUDA;
+    if (cudaMemsetAsync(p + L.ctl, 0, L.clear - L.ctl, s) != cudaSuccess) return DGC_ECUDA;
     uint64_t launches = 0;
-    const uint64_t init_work = std::max<uint64_t>(L.nchunks + 1, (uint64_t)W + 1);
-    const unsigned init_grid = (unsigned)std::min<uint64_t>((init_work + 255) / 256, 1024);
-    if (W <= 1) {  // the table of one message: a small launch
+    if (W == 1) {  // the table of one message: a small launch
         DecTabInline<1> inl{};
         for (int w = 0; w <= W; ++w) inl.e[w] = tab[w];
-        k_dec_init<1><<<init_grid, 256, 0, s>>>(a, inl);
-    } else {
+        k_dec_pos<1><<<(unsigned)L.nchunks, kThreads, 0, s>>>(a, inl);
+        ++launches;
+    } else if (W > 1) {
         DecTabInline<kDecInline> inl{};
         if (W <= kDecInline)
             for (int w = 0; w <= W; ++w) inl.e[w] = tab[w];
-        k_dec_init<kDecInline><<<init_grid, 256, 0, s>>>(a, inl);
-    }
-    ++launches;
-    if (L.nchunks > 0) {
-        k_dec_pos<<<(unsigned)L.nchunks, kThreads, 0, s>>>(a);
+        k_dec_pos<kDecInline><<<(unsigned)L.nchunks, kThreads, 0, s>>>(a, inl);
         ++launches;
     }
     if (!qbits && !apply) {  // binary32 sums, one message or several
