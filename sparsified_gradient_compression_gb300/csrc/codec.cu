@@ -430,29 +430,33 @@ __global__ void __launch_bounds__(kThreads, 4)
     uint32_t pos[kPer];
     uint32_t cum = 0;  // advances of this thread's tokens so far
     bool bad = false;
-    const uint32_t ntiles = (uint32_t)a.ntiles;
+    const int32_t ntiles = (int32_t)a.ntiles;
     uint32_t* ts_w = a.ts + w;  // ts[t * W + w]
+    // the tile of the previous token's position (-1 before a message's first token): the tiles
+    // after it, up to this token's, have this token as their first
+    int32_t qp = (start == 0) ? -1 : (int32_t)((s32 - 1u) / kDecTile);
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
         pos[i] = 0;
         if ((uint32_t)i >= cnt || bad) continue;
         const uint32_t adv = (i & 1) ? (adv2[i / 2] >> 16) : (adv2[i / 2] & 0xFFFFu);
-        const uint32_t cprev = cum;
         cum += adv;
         if (cum > lim) {  // past the end of the dense array: a malformed message
             bad = true;
             continue;
         }
-        const uint32_t e = s32 + cum, ep = s32 + cprev;  // this token's and the previous end
-        pos[i] = ((esc >> i) & 1u) ? kEscPos : e - 1u;
-        // tiles whose first token of this message is this one
-        const uint32_t t0 = ep / kDecTile + ((ep % kDecTile) != 0);
-        const uint32_t t1 = min((e - 1u) / kDecTile, ntiles);
-        for (uint32_t t = t0; t <= t1; ++t) ts_w[(uint64_t)t * a.W] = (uint32_t)(j0 + i);
-        if (j0 + i == d.T - 1)
-            for (uint32_t t = (e - 1u) / kDecTile + 1; t <= ntiles; ++t)
-                ts_w[(uint64_t)t * a.W] = (uint32_t)d.T;
+        const uint32_t p = s32 + cum - 1u;  // this token's position
+        pos[i] = ((esc >> i) & 1u) ? kEscPos : p;
+        const int32_t q = (int32_t)(p / kDecTile);
+        if (q != qp) {
+            for (int32_t t = qp + 1; t <= min(q, ntiles); ++t)
+                ts_w[(uint64_t)t * a.W] = (uint32_t)(j0 + i);
+            qp = q;
+        }
     }
+    // the message's last token: every later tile has no token of it (its first is T)
+    if (!bad && j0 + cnt == d.T)
+        for (int32_t t = qp + 1; t <= ntiles; ++t) ts_w[(uint64_t)t * a.W] = (uint32_t)d.T;
     if (bad) {
         mark_bad(a);
         return;
@@ -470,6 +474,21 @@ __global__ void __launch_bounds__(kThreads, 4)
         for (int i = 0; i < kPer; ++i)
             if ((uint32_t)i < cnt) out[i] = pos[i];
     }
+}
+
+// A message's tokens in rows [r0, r1) of the first-token table: [*first, *first + count).
+// The table rises from 0 to T down each message's column; an entry that does not is reported as
+// a corrupt call and read as no token, so a token index never leaves the message.
+__device__ __forceinline__ uint32_t table_range(const DecArgs& a, uint64_t r0, uint64_t r1,
+                                                int w, uint64_t T, uint32_t* first) {
+    const uint32_t j0 = a.ts[r0 * a.W + w], j1 = a.ts[r1 * a.W + w];
+    if (j0 > j1 || j1 > T) {
+        report(a.status, DGC_ECORRUPT);
+        *first = 0;
+        return 0;
+    }
+    *first = j0;
+    return j1 - j0;
 }
 
 // token j's value: binary32 bits (version 1) or the integer, sign-extended (version 2)
@@ -583,8 +602,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_dec_tiles(DecArgs a) {
         const int w = threadIdx.x;
         uint32_t cnt = 0, first = 0;
         if (w < a.W && a.tab[w].T > 0) {
-            first = a.ts[t * a.W + w];
-            cnt = a.ts[(t + 1) * a.W + w] - first;
+            cnt = table_range(a, t, t + 1, w, a.tab[w].T, &first);
         }
         const int lane = threadIdx.x & 31;
         const uint32_t incl = warp_incl_scan(cnt);
@@ -635,8 +653,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_dec_tiles(DecArgs a) {
         const int w = wb + threadIdx.x;
         uint32_t cnt = 0, first = 0;
         if (w < a.W && a.tab[w].T > 0) {
-            first = a.ts[t * a.W + w];
-            cnt = a.ts[(t + 1) * a.W + w] - first;
+            cnt = table_range(a, t, t + 1, w, a.tab[w].T, &first);
         }
         uint64_t total;
         const uint64_t ex = block_excl_scan<kThreads>((uint64_t)cnt, s_scan, &total);
@@ -800,6 +817,7 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
     __shared__ uint16_t s_msg[kSumCap];    // message index within the group
     __shared__ uint16_t s_multi[kSumCap];  // slots whose position holds several tokens
     __shared__ uint16_t s_sorted[kSumCap]; // the same slots by (position, message)
+    __shared__ uint32_t s_key[kSumCap];    // their (position, message), in s_multi's order
     __shared__ uint32_t s_one[kSumWords];  // a token landed at the position
     __shared__ uint32_t s_two[kSumWords];  // a second token landed there
     __shared__ uint64_t s_tb[kSumThreads];          // the group's messages: position base
@@ -838,10 +856,8 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
     for (int wb = 0; wb < a.W; wb += kSumThreads) {
         const int w = wb + (int)threadIdx.x;
         uint32_t cnt = 0, j0 = 0;
-        if (w < a.W && a.tab[w].T > 0) {
-            j0 = a.ts[row0 * a.W + w];
-            cnt = a.ts[row1 * a.W + w] - j0;
-        }
+        // (the position kernel writes every message's column, an empty message's too)
+        if (w < a.W) cnt = table_range(a, row0, row1, w, a.tab[w].T, &j0);
         if (w < a.W) {  // where the message's positions and values start
             const DecStream& d = a.tab[w];
             s_tb[threadIdx.x] = d.tok_base;
@@ -897,7 +913,9 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
                 const uint32_t lp = s_lp[i];
                 if (lp == kNoLp) continue;
                 if (s_two[lp >> 5] & (1u << (lp & 31))) {
-                    s_multi[atomicAdd(&s_nmulti, 1u)] = (uint16_t)i;
+                    const uint32_t at = atomicAdd(&s_nmulti, 1u);
+                    s_multi[at] = (uint16_t)i;
+                    s_key[at] = (lp << 16) | s_msg[i];
                     continue;
                 }
                 out[lp] = __fadd_rn(first ? 0.0f : out[lp], __uint_as_float(s_val[i]));
@@ -909,14 +927,10 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
             const uint32_t nm = s_nmulti;
             if (nm > 0) {  // block-uniform
                 for (uint32_t k = threadIdx.x; k < nm; k += kSumThreads) {
-                    const uint32_t i = s_multi[k];
-                    const uint32_t key = ((uint32_t)s_lp[i] << 16) | s_msg[i];
+                    const uint32_t key = s_key[k];
                     uint32_t rank = 0;
-                    for (uint32_t q = 0; q < nm; ++q) {
-                        const uint32_t iq = s_multi[q];
-                        rank += (((uint32_t)s_lp[iq] << 16) | s_msg[iq]) < key;
-                    }
-                    s_sorted[rank] = (uint16_t)i;  // keys are distinct: ranks are too
+                    for (uint32_t q = 0; q < nm; ++q) rank += s_key[q] < key;
+                    s_sorted[rank] = s_multi[k];  // keys are distinct: ranks are too
                 }
                 __syncthreads();
                 for (uint32_t r = threadIdx.x; r < nm; r += kSumThreads) {
