@@ -38,9 +38,10 @@
  *     some of them as cooperative launches) and at most a memset, so a stream capture of them
  *     replays as captured. Make one ordinary dgc_compress or dgc_compress_shared call on the
  *     device first (it sets the kernels' shared-memory attributes and reads the cooperative
- *     kernels' occupancy once per device). The decoders copy their table of
- *     messages from host memory on every call and are not meant for capture. (This note does
- *     not cover dgc_compress_noalloc.)
+ *     kernels' occupancy once per device). The decoders with host sizes read those sizes on
+ *     the host at every call (and copy their table of messages from host memory when there are
+ *     more than 96): capture the _dev decoders below instead. (This note does not cover
+ *     dgc_compress_noalloc.)
  */
 #ifndef DGC_H
 #define DGC_H
