@@ -33,7 +33,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kEncBlocks = 512;
 constexpr int kEncPer = 4;
-constexpr int kDecChunk = 4096;  // tokens per position chunk (16 per thread)
+constexpr int kDecChunk = 4096;  // tokens per position chunk
+constexpr int kPosThreads = 256; // threads of the position kernel (16 tokens each)
 constexpr int kDecTile = 4096;   // dense entries per output tile
 constexpr int kDecCap = 512;     // tokens staged in shared memory at a time
 constexpr uint32_t kEscPos = 0xFFFFFFFFu;
@@ -246,8 +247,8 @@ struct DecStream {
 };
 
 struct DecCtl {
-    uint32_t ticket;
     uint32_t any_bad;
+    uint32_t pad;
 };
 
 struct DecArgs {
@@ -302,33 +303,35 @@ __device__ bool header_ok(const DecArgs& a, const DecStream& d) {
 }
 
 // Token positions, one chunk of kDecChunk tokens of one message per block (16 contiguous tokens
-// per thread). Token j advances the running position by run + 1 (an escape by 65535) and sits at
-// the position the advance reaches, less one. Within the chunk every sum is taken in 32 bits
-// (a chunk advances by less than 2^28); the chunk's base comes from a decoupled look-back over
-// the message's earlier chunks, in 64 bits. Each token's end e = position + 1 is checked against
+// per thread), in two launches. Token j advances the running position by run + 1 (an escape by
+// 65535) and sits at the position the advance reaches, less one. The first launch (kPass 0) sums
+// each chunk's advances and publishes the sum in the chunk's look-back word; the second (kPass
+// 1) finds every word of a chunk's predecessors already written, so its look-back over them
+// reads and never waits (within one launch a chunk's look-back waited microseconds for words
+// its predecessors had written already). Within the chunk every sum is taken in 32 bits (a chunk
+// advances by less than 2^28); the chunk's base, from the look-back, in 64 bits. Each token's end e = position + 1 is checked against
 // n once; e <= n makes the 32-bit position exact. A token is the first of its message in the
 // tiles t with e_prev <= t kDecTile < e (e_prev the previous token's end, 0 before the first),
 // and the message's last token also fills the table for every later tile.
 //
-// Every message owns at least one chunk, and the block of its first chunk also checks the
-// message's header and writes its entry of the workspace table for the kernels that follow
+// Every message owns at least one chunk, and in the first launch the block of its first chunk
+// also checks the message's header and writes its entry of the workspace table for the kernels
+// that follow
 // (with the token count read from device memory when the sizes are there); for a message
 // without tokens it fills the message's column of the first-token table with 0.
-template <int kMax>
-__global__ void __launch_bounds__(kThreads, 4)
+template <int kMax, int kPass>
+__global__ void __launch_bounds__(kPosThreads, 1024 / kPosThreads)
     k_dec_pos(DecArgs a, const __grid_constant__ DecTabInline<kMax> t) {
     __shared__ uint32_t s_scan[33];
     __shared__ uint64_t s_lb64[33];
     __shared__ uint32_t s_lb32[2];
-    __shared__ uint32_t s_chunk;
-    __shared__ uint64_t s_cb[kThreads];  // the messages' first chunks, when W <= kThreads
+    __shared__ uint64_t s_cb[kPosThreads];  // the messages' first chunks, when W <= kPosThreads
     // the host's table: with the launch (up to kMax messages), else copied to the workspace
     const DecStream* tin = (a.W <= kMax) ? t.e : a.tab;
-    if (threadIdx.x == 0) s_chunk = atomicAdd(&a.ctl->ticket, 1u);
-    const bool staged = a.W <= kThreads;
+    const bool staged = a.W <= kPosThreads;
     if (staged && threadIdx.x < a.W) s_cb[threadIdx.x] = tin[threadIdx.x].chunk_base;
     __syncthreads();
-    const uint64_t c = s_chunk;
+    const uint64_t c = blockIdx.x;
     // the message that owns chunk c: the last one starting at or before c, searched in shared
     // memory (one parallel load instead of a chain of them)
     int lo = 0, hi = a.W;
@@ -351,25 +354,25 @@ __global__ void __launch_bounds__(kThreads, 4)
     }
     const uint64_t lc = c - d.chunk_base;
     if (lc == 0) {
-        if (threadIdx.x == 0) {
+        if (kPass == 0) {
             // (with more than kMax messages and sizes in device memory, the other chunks of the
             // message may read this entry as it changes: they take only fields that stay the
             // same, and T from the size themselves)
-            if (a.W <= kMax || a.dev_bytes) a.tab[w] = d;
-            if (!size_ok || !header_ok(a, d)) mark_bad(a);
+            if (threadIdx.x == 0 && (a.W <= kMax || a.dev_bytes)) a.tab[w] = d;
+            if (d.T == 0) {  // no token: its first token in every tile is 0 (= T)
+                if (threadIdx.x == 0 && (!size_ok || !header_ok(a, d))) mark_bad(a);
+                for (uint64_t tt = threadIdx.x; tt <= a.ntiles; tt += kPosThreads)
+                    a.ts[tt * a.W + w] = 0;
+            }
         }
-        if (d.T == 0) {  // no token: its first token in every tile is 0 (= T)
-            for (uint64_t tt = threadIdx.x; tt <= a.ntiles; tt += kThreads)
-                a.ts[tt * a.W + w] = 0;
-            return;  // (no later chunk of this message looks back to this one)
-        }
+        if (d.T == 0) return;
     } else if (lc * kDecChunk >= d.T) {
         // with sizes in device memory the chunks are laid out for each message's bound on T: the
         // chunks past its real end have nothing to do (and no later chunk of it looks back to
         // them)
         return;
     }
-    constexpr int kPer = kDecChunk / kThreads;
+    constexpr int kPer = kDecChunk / kPosThreads;
     static_assert(kPer % 4 == 0 && kPer <= 32, "pairs of advances per word, one escape bit each");
     // this thread's tokens [j0, j0 + cnt) of the message
     const uint64_t j0 = lc * kDecChunk + (uint64_t)threadIdx.x * kPer;
@@ -412,16 +415,22 @@ __global__ void __launch_bounds__(kThreads, 4)
         }
     }
     uint32_t agg;
-    const uint32_t ex = block_excl_scan<kThreads>(mine, s_scan, &agg);
-    // a message's first chunk starts at end 0; the others look back over their predecessors
-    // with the whole block (kThreads of them per round trip)
-    uint64_t base = 0;
-    if (lc == 0) {
-        if (threadIdx.x == 0) st_relaxed(&a.st[c], kFlagInc | agg);
-    } else {
-        base = block_lookback<kThreads>(a.st, (uint32_t)c, agg, a.spin_limit, a.status, nullptr,
-                                        s_lb32, s_lb64);
+    const uint32_t ex = block_excl_scan<kPosThreads>(mine, s_scan, &agg);
+    if (kPass == 0) {
+        // the chunk's advances, published for the position pass (a message's first chunk: its
+        // inclusive prefix); the header
+        if (threadIdx.x == 0) {
+            st_relaxed(&a.st[c], (lc == 0 ? kFlagInc : kFlagAgg) | agg);
+            if (lc == 0 && (!size_ok || !header_ok(a, d))) mark_bad(a);
+        }
+        return;
     }
+    // a message's first chunk starts at end 0; the others look back over their predecessors,
+    // whose words the aggregate pass has all written (kPosThreads of them per round trip)
+    uint64_t base = 0;
+    if (lc > 0)
+        base = block_lookback<kPosThreads>(a.st, (uint32_t)c, agg, a.spin_limit, a.status, nullptr,
+                                           s_lb32, s_lb64, false);
     if (cnt == 0) return;
     const uint64_t start = base + ex;  // the end of the token before this thread's first
     // ends up to lim (<= n) are positions inside the dense array
@@ -1232,14 +1241,16 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
     if (W == 1) {  // the table of one message: a small launch
         DecTabInline<1> inl{};
         for (int w = 0; w <= W; ++w) inl.e[w] = tab[w];
-        k_dec_pos<1><<<(unsigned)L.nchunks, kThreads, 0, s>>>(a, inl);
-        ++launches;
+        k_dec_pos<1, 0><<<(unsigned)L.nchunks, kPosThreads, 0, s>>>(a, inl);
+        k_dec_pos<1, 1><<<(unsigned)L.nchunks, kPosThreads, 0, s>>>(a, inl);
+        launches += 2;
     } else if (W > 1) {
         DecTabInline<kDecInline> inl{};
         if (W <= kDecInline)
             for (int w = 0; w <= W; ++w) inl.e[w] = tab[w];
-        k_dec_pos<kDecInline><<<(unsigned)L.nchunks, kThreads, 0, s>>>(a, inl);
-        ++launches;
+        k_dec_pos<kDecInline, 0><<<(unsigned)L.nchunks, kPosThreads, 0, s>>>(a, inl);
+        k_dec_pos<kDecInline, 1><<<(unsigned)L.nchunks, kPosThreads, 0, s>>>(a, inl);
+        launches += 2;
     }
     if (!qbits && !apply) {  // binary32 sums, one message or several
         if (L.ntiles > 0) {
