@@ -830,7 +830,7 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
     __shared__ uint32_t s_one[kSumWords];  // a token landed at the position
     __shared__ uint32_t s_two[kSumWords];  // a second token landed there
     __shared__ uint64_t s_tb[kSumThreads];          // the group's messages: position base
-    __shared__ const uint32_t* s_vp[kSumThreads];   // and their values (binary32)
+    __shared__ const uint8_t* s_vp[kSumThreads];    // and their values
     __shared__ uint32_t s_scan[33];
     __shared__ uint32_t s_nmulti;
     if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
@@ -870,7 +870,7 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
         if (w < a.W) {  // where the message's positions and values start
             const DecStream& d = a.tab[w];
             s_tb[threadIdx.x] = d.tok_base;
-            s_vp[threadIdx.x] = reinterpret_cast<const uint32_t*>(d.ptr + 32);
+            s_vp[threadIdx.x] = d.ptr + 32;
         }
         uint32_t total;
         const uint32_t ex = block_excl_scan<kSumThreads>(cnt, s_scan, &total);
@@ -896,7 +896,11 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
                 if (i >= m) continue;
                 const uint32_t l = s_msg[i], j = s_val[i];
                 pv[k] = a.pos[s_tb[l] + j];
-                rv[k] = s_vp[l][j];
+                // binary32 bits, or (one integer message) the integer, sign-extended
+                const uint8_t* vb = s_vp[l];
+                rv[k] = a.qbits == 8    ? (uint32_t)(int32_t)reinterpret_cast<const int8_t*>(vb)[j]
+                        : a.qbits == 16 ? (uint32_t)(int32_t)reinterpret_cast<const int16_t*>(vb)[j]
+                                        : reinterpret_cast<const uint32_t*>(vb)[j];
             }
             if (!cleared) clear_tile();
 #pragma unroll
@@ -927,7 +931,12 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
                     s_key[at] = (lp << 16) | s_msg[i];
                     continue;
                 }
-                out[lp] = __fadd_rn(first ? 0.0f : out[lp], __uint_as_float(s_val[i]));
+                if (a.qbits) {  // one message of integers: one dequantization, added on
+                    const float x = dequant((int32_t)s_val[i], a.alpha);
+                    out[lp] = a.accumulate ? __fadd_rn(out[lp], x) : x;
+                } else {
+                    out[lp] = __fadd_rn(first ? 0.0f : out[lp], __uint_as_float(s_val[i]));
+                }
             }
             __syncthreads();  // the list of tokens at shared positions
             // positions several messages reach: those tokens sorted by (position, message), each
@@ -968,42 +977,8 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
     if (!cleared) clear_tile();  // a tile no token reaches
 }
 
-// One message (W = 1): its positions are distinct, so its values can be added in parallel. The
-// dense output is first cleared by a streaming store pass (unless accumulating), then each value
-// token adds itself to its position: the same single binary32 addition per value as the tile
-// kernel performs, onto the same starting value.
-// The dense array to +0 before the one-message scatter: one zeroed 16 KiB shared buffer per
-// block, written out by bulk asynchronous stores (one thread issues them, chunk after chunk);
-// the few entries before the first 16-byte boundary and after the last whole chunk by plain
-// stores.
-constexpr uint32_t kZeroChunk = 4096;  // floats per bulk store
-constexpr int kZeroThreads = 128;
-__global__ void __launch_bounds__(kZeroThreads) k_dec_zero(DecArgs a) {
-    __shared__ __align__(128) float s_zero[kZeroChunk];
-    if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
-    float* dense = a.dense;
-    const uint64_t n = a.n;
-    const uint64_t head = umin64(n, ((16u - ((uintptr_t)dense & 15u)) & 15u) / 4u);
-    const uint64_t nchunks = (n - head) / kZeroChunk;
-    const uint64_t body_end = head + nchunks * kZeroChunk;
-    if (nchunks > 0) {
-        for (uint32_t i = threadIdx.x; i < kZeroChunk; i += kZeroThreads) s_zero[i] = 0.0f;
-        fence_proxy_async_smem();  // the zeros, before the bulk copies read them
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            for (uint64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-                bulk_s2g(dense + head + c * kZeroChunk, s_zero, kZeroChunk * 4u);
-                bulk_commit();
-            }
-            bulk_wait_all();
-        }
-    }
-    const uint64_t tid = (uint64_t)blockIdx.x * kZeroThreads + threadIdx.x;
-    const uint64_t stride = (uint64_t)gridDim.x * kZeroThreads;
-    for (uint64_t i = tid; i < head; i += stride) dense[i] = 0.0f;
-    for (uint64_t i = body_end + tid; i < n; i += stride) dense[i] = 0.0f;
-}
-
+// The SGD step from one message (W = 1): its positions are distinct, so each value token takes
+// the step at its own position (the one-message sum there is +0 + x).
 __global__ void __launch_bounds__(kThreads) k_dec_scatter1(DecArgs a) {
     if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
     const DecStream d = a.tab[0];
@@ -1013,12 +988,7 @@ __global__ void __launch_bounds__(kThreads) k_dec_scatter1(DecArgs a) {
     if (p == kEscPos || p >= a.n) return;
     const uint32_t raw = dec_value(a, d, j);
     const float x = a.qbits ? dequant((int32_t)raw, a.alpha) : __uint_as_float(raw);
-    if (a.apply)  // the one-message sum at p is +0 + x; then the step
-        a.dense[p] = __fmaf_rn(a.neg_lr, __fadd_rn(0.0f, x), a.dense[p]);
-    else if (a.accumulate)
-        a.dense[p] = __fadd_rn(a.dense[p], x);
-    else  // dense[p] was just cleared to +0: the sum is +0 + x, with no read
-        a.dense[p] = __fadd_rn(0.0f, x);
+    a.dense[p] = __fmaf_rn(a.neg_lr, __fadd_rn(0.0f, x), a.dense[p]);
 }
 
 // ---------------------------------------------------------------- shared-set sums
@@ -1257,13 +1227,14 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
             k_dec_sum<<<(unsigned)((L.ntiles + kSumRows - 1) / kSumRows), kSumThreads, 0, s>>>(a);
             ++launches;
         }
-    } else if (W == 1) {  // runs after the positions are checked: a malformed message changes nothing
-        if (!accumulate && !apply && n > 0) {
-            const int sms = dgc_internal_sm_count();
-            if (sms <= 0) return DGC_ECUDA;
-            k_dec_zero<<<(unsigned)sms * 4, kZeroThreads, 0, s>>>(a);
+    } else if (W == 1 && !apply) {
+        // one message of integers: its positions are distinct, so the sum kernel's single-token
+        // path (one dequantization per value, +0 elsewhere) is the whole decode
+        if (L.ntiles > 0) {
+            k_dec_sum<<<(unsigned)((L.ntiles + kSumRows - 1) / kSumRows), kSumThreads, 0, s>>>(a);
             ++launches;
         }
+    } else if (W == 1) {  // the step from one message: one scattered update per value
         if (L.sum_T > 0) {
             k_dec_scatter1<<<(unsigned)((L.sum_T + kThreads - 1) / kThreads), kThreads, 0, s>>>(a);
             ++launches;
