@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import gpu_helpers
 import oracle
 import sparsified_gradient_compression_gb300 as dgc
 import workloads
@@ -990,7 +991,7 @@ def test_launch_counter_counts_kernels():
 @pytest.mark.parametrize("n", [5, 4096, 4099, 3 * 4096 + 7, 100_003])
 def test_decode_clear_any_alignment(shift, n):
     # one message decoded into a dense view that starts 0-3 floats past a 16-byte boundary: the
-    # clear (bulk stores of whole 16 KiB chunks, plain stores around them) covers exactly [0, n)
+    # zeros and values (16-byte stores on a boundary, plain stores otherwise) cover exactly [0, n)
     rng = np.random.default_rng(n + shift)
     k = max(1, n // 100)
     idx = np.sort(rng.choice(n, k, replace=False)).astype(np.uint32)
@@ -1148,6 +1149,46 @@ def test_quant_decode_learners(seed):
     rc, w = decode_apply_quant(msgs, n, bits, alpha, base, 0.37)
     orc_rc, ow = oracle.decode_apply_quant(msgs, n, bits, alpha, base, np.float32(0.37))
     assert rc == 0 and orc_rc == 0 and same_bits(w, ow)
+
+
+@pytest.mark.parametrize("bits", [8, 16])
+@pytest.mark.parametrize("case", ["sparse, escapes", "crowded tiles", "ragged, shifted view"])
+def test_quant_decode_one_message(bits, case):
+    # one message of integers: each value dequantized once where it lands and +0 elsewhere, or
+    # added onto dense when accumulating; gaps past 65535 entries (escape tokens), tiles holding
+    # more tokens than one round stages, and a dense view 1-3 floats off a 16-byte boundary
+    rng = np.random.default_rng(bits + len(case))
+    if case.startswith("sparse"):
+        n = 5_000_003
+        idx = np.sort(rng.choice(n, 60, replace=False)).astype(np.uint32)
+    elif case.startswith("crowded"):
+        n = 70_001
+        idx = np.sort(rng.choice(n, n // 2, replace=False)).astype(np.uint32)
+    else:
+        n = 3 * 16384 + 4101
+        idx = np.sort(rng.choice(n, n // 40, replace=False)).astype(np.uint32)
+    alpha = float(np.float32(rng.choice([0.5, 3.0, 1000.0])))
+    val = (rng.standard_normal(idx.size) * 10.0 ** rng.integers(-3, 2, idx.size)).astype(np.float32)
+    orc_rc, msg, _ = oracle.encode_quant(idx, val, n, alpha, bits)
+    assert orc_rc == 0
+    base = rng.standard_normal(n).astype(np.float32)
+    base[::7] = np.float32(-0.0)
+    shift = int(rng.integers(1, 4)) if case.startswith("ragged") else 0
+    for acc in (False, True):
+        buf = torch.full((n + 8,), float("nan"), dtype=torch.float32, device="cuda")
+        buf[shift:shift + n] = torch.from_numpy(base).cuda()
+        bufs, sizes = gpu_helpers._device_messages([msg])
+        ws_bytes = dgc.dgc_decode_workspace_quant(sizes, n, bits)
+        ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        dgc.dgc_decode_accumulate_quant(bufs, sizes, bits, alpha, buf[shift:shift + n], n, acc,
+                                        status, ws, ws_bytes=ws_bytes)
+        orc_rc, odense = oracle.decode_accumulate_quant([msg], n, bits, alpha, dense=base,
+                                                        accumulate=acc)
+        host = buf.cpu().numpy()
+        assert dgc.dgc_read_status(status) == 0 and orc_rc == 0
+        assert same_bits(host[shift:shift + n], odense), (case, acc)
+        assert np.isnan(host[:shift]).all() and np.isnan(host[shift + n:]).all()
 
 
 def test_quant_nan_and_infinities_on_gpu():
