@@ -816,6 +816,12 @@ constexpr int kSumRows = kSumTile / kDecTile;  // first-token table rows per til
 constexpr int kSumThreads = 256;
 constexpr int kSumCap = 2048;  // tokens staged per round
 constexpr int kSumWords = kSumTile / 32;
+// Order this thread's completed bulk-copy (async-proxy) writes to global memory before its later
+// generic-proxy accesses, so that a barrier after it orders them for the whole block.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 constexpr uint16_t kNoLp = 0xFFFFu;  // an escape, or a position outside the tile
 static_assert(kSumCap <= 0xFFFF && kSumTile < 0xFFFF, "16-bit slots and positions");
 
@@ -833,16 +839,40 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
     __shared__ const uint8_t* s_vp[kSumThreads];    // and their values
     __shared__ uint32_t s_scan[33];
     __shared__ uint32_t s_nmulti;
+    __shared__ __align__(128) float s_zero[1024];  // the source of the tile's zeros
     if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
     const uint64_t p0 = (uint64_t)blockIdx.x * kSumTile;
     const uint32_t len = (uint32_t)umin64(kSumTile, a.n - p0);
     const uint64_t row0 = (uint64_t)blockIdx.x * kSumRows;
     const uint64_t row1 = umin64(row0 + kSumRows, a.ntiles);
     float* out = a.dense + p0;
-    // the plain sum starts from +0 everywhere: the tile is cleared once, after the first
-    // round's loads are in flight (they would wait behind the stores otherwise) and before the
-    // barrier that precedes every store of a sum
+    // the plain sum starts from +0 everywhere: the tile is cleared once, before the barrier that
+    // precedes every store of a sum
     bool cleared = a.accumulate != 0;
+    // a whole, aligned tile of a plain sum: its zeros go out as 16 bulk copies of a zeroed 4 KB
+    // shared buffer, issued by one thread at once; that thread waits for them (and fences them
+    // from the generic stores) before the barrier that precedes the first stored sum
+    const bool bulk = !cleared && len == kSumTile && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+    if (bulk) {
+        for (uint32_t i = threadIdx.x; i < 1024; i += kSumThreads) s_zero[i] = 0.0f;
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int c = 0; c < kSumTile / 1024; ++c) bulk_s2g(out + c * 1024, s_zero, 4096u);
+            bulk_commit();
+        }
+        cleared = true;
+    }
+    bool waited = false;  // (the same in every thread)
+    auto bulk_done = [&]() {
+        if (bulk && !waited && threadIdx.x == 0) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+        }
+        waited = true;
+    };
+    // otherwise (a partial or unaligned tile) plain stores, issued once the first round's loads
+    // are in flight (they would wait behind the stores otherwise)
     auto clear_tile = [&]() {
         if (len == kSumTile && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
 #pragma unroll 4
@@ -917,6 +947,7 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
                     if (atomicOr(&s_one[lp >> 5], bit) & bit) atomicOr(&s_two[lp >> 5], bit);
                 }
             }
+            bulk_done();
             __syncthreads();  // the round's tokens and marks
             // a position with one token of the round: that token's value, added on
 #pragma unroll
@@ -975,6 +1006,7 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
         }
     }
     if (!cleared) clear_tile();  // a tile no token reaches
+    bulk_done();  // (the zeros must be out before the block ends, even with no token)
 }
 
 // The SGD step from one message (W = 1): its positions are distinct, so each value token takes
