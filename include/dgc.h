@@ -281,8 +281,10 @@ int dgc_decode_apply(const uint8_t* const* streams, const uint64_t* stream_bytes
  * are exchanged and summed): a message's size is known on the device once the message is there,
  * for instance after an all-gather of the sizes, or right after dgc_encode wrote it. These calls
  * take the sizes from there, so nothing waits for them on the host, and with at most 96 messages
- * the call enqueues only a memset and kernels (its message table travels in kernel parameters),
- * so it can be captured in a CUDA graph together with dgc_compress and dgc_encode.
+ * the call enqueues only kernels (a memset as well when W = 0; its message table travels in
+ * kernel parameters; every kernel after the first is a programmatic dependent launch, which may
+ * start while the one ahead of it finishes), so it can be captured in a CUDA graph together with
+ * dgc_compress and dgc_encode.
  *   stream_bytes  device, W uint64 sizes (8-byte aligned); dgc_encode's out_bytes fits.
  *   max_bytes     host, W upper bounds on those sizes (for instance dgc_encode_max_bytes of the
  *                 encoder's max_count); the workspace is laid out for them.

@@ -272,6 +272,15 @@ struct DecArgs {
     uint32_t spin_limit;
 };
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may
+// start before the kernel ahead of it in the stream has finished; it waits here before it reads
+// anything that kernel writes (a no-op when it was launched the ordinary way). The kernel ahead
+// lets its dependents launch as soon as each of its blocks has started.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void mark_bad(const DecArgs& a) {
     atomicExch(&a.ctl->any_bad, 1u);
     report(a.status, DGC_ECORRUPT);
@@ -309,16 +318,21 @@ __device__ bool header_ok(const DecArgs& a, const DecStream& d) {
 // 1) finds every word of a chunk's predecessors already written, so its look-back over them
 // reads and never waits (within one launch a chunk's look-back waited microseconds for words
 // its predecessors had written already). Within the chunk every sum is taken in 32 bits (a chunk
-// advances by less than 2^28); the chunk's base, from the look-back, in 64 bits. Each token's end e = position + 1 is checked against
-// n once; e <= n makes the 32-bit position exact. A token is the first of its message in the
-// tiles t with e_prev <= t kDecTile < e (e_prev the previous token's end, 0 before the first),
-// and the message's last token also fills the table for every later tile.
+// advances by less than 2^28); the chunk's base, from the look-back, in 64 bits. Each token's
+// end e = position + 1 is checked against n once; e <= n makes the 32-bit position exact. A
+// token is the first of its message in the tiles t with e_prev <= t kDecTile < e (e_prev the
+// previous token's end, 0 before the first), and the message's last token also fills the table
+// for every later tile.
 //
-// Every message owns at least one chunk, and in the first launch the block of its first chunk
-// also checks the message's header and writes its entry of the workspace table for the kernels
-// that follow
-// (with the token count read from device memory when the sizes are there); for a message
-// without tokens it fills the message's column of the first-token table with 0.
+// Every message owns at least one chunk. In the first launch the block of its first chunk writes
+// its entry of the workspace table for the kernels that follow (with the token count read from
+// device memory when the sizes are there) and, for a message without tokens, fills the message's
+// column of the first-token table with 0; block 0 clears the call's control word. The second
+// launch may start while the first finishes: it reads its chunk's runs and scans them, then
+// waits for the first launch before the look-back, and its first-chunk blocks check the headers
+// (so every mark of a malformed message comes after the clear). The look-back words need no
+// clearing: a chunk reads only the words of its own message's earlier chunks, all written by the
+// first launch of the same call.
 template <int kMax, int kPass>
 __global__ void __launch_bounds__(kPosThreads, 1024 / kPosThreads)
     k_dec_pos(DecArgs a, const __grid_constant__ DecTabInline<kMax> t) {
@@ -326,6 +340,7 @@ __global__ void __launch_bounds__(kPosThreads, 1024 / kPosThreads)
     __shared__ uint64_t s_lb64[33];
     __shared__ uint32_t s_lb32[2];
     __shared__ uint64_t s_cb[kPosThreads];  // the messages' first chunks, when W <= kPosThreads
+    grid_dep_launch();  // the next launch may start once every block here has
     // the host's table: with the launch (up to kMax messages), else copied to the workspace
     const DecStream* tin = (a.W <= kMax) ? t.e : a.tab;
     const bool staged = a.W <= kPosThreads;
@@ -353,17 +368,22 @@ __global__ void __launch_bounds__(kPosThreads, 1024 / kPosThreads)
         d.runs_off = 32 + 4 * d.T;
     }
     const uint64_t lc = c - d.chunk_base;
+    // the call's control word starts clear: the first launch clears it, and every mark comes
+    // from the second launch or the kernels after it
+    if (kPass == 0 && c == 0 && threadIdx.x == 0) a.ctl->any_bad = 0u;
     if (lc == 0) {
         if (kPass == 0) {
             // (with more than kMax messages and sizes in device memory, the other chunks of the
             // message may read this entry as it changes: they take only fields that stay the
             // same, and T from the size themselves)
             if (threadIdx.x == 0 && (a.W <= kMax || a.dev_bytes)) a.tab[w] = d;
-            if (d.T == 0) {  // no token: its first token in every tile is 0 (= T)
-                if (threadIdx.x == 0 && (!size_ok || !header_ok(a, d))) mark_bad(a);
+            if (d.T == 0)  // no token: its first token in every tile is 0 (= T)
                 for (uint64_t tt = threadIdx.x; tt <= a.ntiles; tt += kPosThreads)
                     a.ts[tt * a.W + w] = 0;
-            }
+        } else if (d.T == 0) {
+            // the header of a message without tokens, checked once the first launch is done
+            grid_dep_wait();
+            if (threadIdx.x == 0 && (!size_ok || !header_ok(a, d))) mark_bad(a);
         }
         if (d.T == 0) return;
     } else if (lc * kDecChunk >= d.T) {
@@ -419,12 +439,12 @@ __global__ void __launch_bounds__(kPosThreads, 1024 / kPosThreads)
     if (kPass == 0) {
         // the chunk's advances, published for the position pass (a message's first chunk: its
         // inclusive prefix); the header
-        if (threadIdx.x == 0) {
-            st_relaxed(&a.st[c], (lc == 0 ? kFlagInc : kFlagAgg) | agg);
-            if (lc == 0 && (!size_ok || !header_ok(a, d))) mark_bad(a);
-        }
+        if (threadIdx.x == 0) st_relaxed(&a.st[c], (lc == 0 ? kFlagInc : kFlagAgg) | agg);
         return;
     }
+    // the second launch: the first one's words, and the control word it cleared, from here on
+    grid_dep_wait();
+    if (lc == 0 && threadIdx.x == 0 && (!size_ok || !header_ok(a, d))) mark_bad(a);
     // a message's first chunk starts at end 0; the others look back over their predecessors,
     // whose words the aggregate pass has all written (kPosThreads of them per round trip)
     uint64_t base = 0;
@@ -541,6 +561,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_dec_tiles(DecArgs a) {
     __shared__ uint32_t s_fill;  // staging slots claimed by the warps (one-pass path)
     float* s_acc = reinterpret_cast<float*>(s_accw);
     int32_t* s_acci = reinterpret_cast<int32_t*>(s_accw);
+    grid_dep_wait();
     if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
     const uint64_t t = blockIdx.x;
     const uint64_t p0 = t * kDecTile;
@@ -840,6 +861,7 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
     __shared__ uint32_t s_scan[33];
     __shared__ uint32_t s_nmulti;
     __shared__ __align__(128) float s_zero[1024];  // the source of the tile's zeros
+    grid_dep_wait();
     if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
     const uint64_t p0 = (uint64_t)blockIdx.x * kSumTile;
     const uint32_t len = (uint32_t)umin64(kSumTile, a.n - p0);
@@ -1012,6 +1034,7 @@ __global__ void __launch_bounds__(kSumThreads, 5) k_dec_sum(DecArgs a) {
 // The SGD step from one message (W = 1): its positions are distinct, so each value token takes
 // the step at its own position (the one-message sum there is +0 + x).
 __global__ void __launch_bounds__(kThreads) k_dec_scatter1(DecArgs a) {
+    grid_dep_wait();
     if (ld_relaxed_u32(&a.ctl->any_bad)) return;  // a malformed message: leave dense as it is
     const DecStream d = a.tab[0];
     const uint64_t j = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -1042,8 +1065,26 @@ __global__ void __launch_bounds__(kThreads) k_sum_shared(const float* const* val
     }
 }
 
+// A launch that may overlap the end of the kernel ahead of it in the stream (the kernel waits
+// for it with grid_dep_wait before reading what it wrote).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), uint64_t grid, unsigned block,
+                             cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 struct DecLayout {
-    size_t ctl, tab, pos, st, ts, clear, total;
+    size_t ctl, tab, pos, st, ts, total;
     uint64_t sum_T, pos_len, nchunks, ntiles;
 };
 
@@ -1069,10 +1110,8 @@ int dec_layout(int32_t W, const uint64_t* stream_bytes, int64_t n, int qbits, De
     L->ntiles = ((uint64_t)n + kDecTile - 1) / kDecTile;
     size_t o = 0;
     auto take = [&](size_t b) { size_t at = o; o = align256(o + b); return at; };
-    // the control words and the look-back words first: one memset clears both
     L->ctl = take(sizeof(DecCtl));
     L->st = take(sizeof(uint64_t) * (size_t)(L->nchunks + 1));
-    L->clear = o;
     L->tab = take(sizeof(DecStream) * (size_t)(W + 1));
     L->pos = take(sizeof(uint32_t) * (size_t)L->pos_len);
     L->ts = take(sizeof(uint32_t) * (size_t)(L->ntiles + 1) * (size_t)(W > 0 ? W : 1));
@@ -1238,46 +1277,56 @@ int decode_impl(const uint8_t* const* streams, const uint64_t* stream_bytes, int
     if (W > kDecInline && cudaMemcpyAsync(p + L.tab, tab.data(), sizeof(DecStream) * tab.size(),
                                           cudaMemcpyHostToDevice, s) != cudaSuccess)
         return DGC_ECUDA;
-    if (cudaMemsetAsync(p + L.ctl, 0, L.clear - L.ctl, s) != cudaSuccess) return DGC_ECUDA;
+    // the control word: cleared by the first position launch when there is one; the look-back
+    // words need no clearing (the second launch reads only words the first wrote in this call)
+    if (W == 0 && cudaMemsetAsync(p + L.ctl, 0, sizeof(DecCtl), s) != cudaSuccess)
+        return DGC_ECUDA;
+    // the first launch is ordinary (it reads what came before the call); every later one may
+    // start while the one ahead of it finishes
     uint64_t launches = 0;
+    cudaError_t e = cudaSuccess;
+    auto ok = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
     if (W == 1) {  // the table of one message: a small launch
         DecTabInline<1> inl{};
         for (int w = 0; w <= W; ++w) inl.e[w] = tab[w];
         k_dec_pos<1, 0><<<(unsigned)L.nchunks, kPosThreads, 0, s>>>(a, inl);
-        k_dec_pos<1, 1><<<(unsigned)L.nchunks, kPosThreads, 0, s>>>(a, inl);
+        ok(launch_dependent(k_dec_pos<1, 1>, L.nchunks, kPosThreads, s, a, inl));
         launches += 2;
     } else if (W > 1) {
         DecTabInline<kDecInline> inl{};
         if (W <= kDecInline)
             for (int w = 0; w <= W; ++w) inl.e[w] = tab[w];
         k_dec_pos<kDecInline, 0><<<(unsigned)L.nchunks, kPosThreads, 0, s>>>(a, inl);
-        k_dec_pos<kDecInline, 1><<<(unsigned)L.nchunks, kPosThreads, 0, s>>>(a, inl);
+        ok(launch_dependent(k_dec_pos<kDecInline, 1>, L.nchunks, kPosThreads, s, a, inl));
         launches += 2;
     }
+    const uint64_t sum_grid = (L.ntiles + kSumRows - 1) / kSumRows;
     if (!qbits && !apply) {  // binary32 sums, one message or several
         if (L.ntiles > 0) {
-            k_dec_sum<<<(unsigned)((L.ntiles + kSumRows - 1) / kSumRows), kSumThreads, 0, s>>>(a);
+            ok(launch_dependent(k_dec_sum, sum_grid, kSumThreads, s, a));
             ++launches;
         }
     } else if (W == 1 && !apply) {
         // one message of integers: its positions are distinct, so the sum kernel's single-token
         // path (one dequantization per value, +0 elsewhere) is the whole decode
         if (L.ntiles > 0) {
-            k_dec_sum<<<(unsigned)((L.ntiles + kSumRows - 1) / kSumRows), kSumThreads, 0, s>>>(a);
+            ok(launch_dependent(k_dec_sum, sum_grid, kSumThreads, s, a));
             ++launches;
         }
     } else if (W == 1) {  // the step from one message: one scattered update per value
         if (L.sum_T > 0) {
-            k_dec_scatter1<<<(unsigned)((L.sum_T + kThreads - 1) / kThreads), kThreads, 0, s>>>(a);
+            ok(launch_dependent(k_dec_scatter1, (L.sum_T + kThreads - 1) / kThreads, kThreads, s,
+                                a));
             ++launches;
         }
     } else if (L.ntiles > 0) {
         if (qbits)
-            k_dec_tiles<true><<<(unsigned)L.ntiles, kThreads, 0, s>>>(a);
+            ok(launch_dependent(k_dec_tiles<true>, L.ntiles, kThreads, s, a));
         else
-            k_dec_tiles<false><<<(unsigned)L.ntiles, kThreads, 0, s>>>(a);
+            ok(launch_dependent(k_dec_tiles<false>, L.ntiles, kThreads, s, a));
         ++launches;
     }
+    if (e != cudaSuccess) return DGC_ECUDA;
     dgc_internal_count_launches(launches);
     if (cudaPeekAtLastError() != cudaSuccess) {
         cudaGetLastError();
