@@ -42,6 +42,8 @@ constexpr uint32_t kEscPos = 0xFFFFFFFFu;
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // ------------------------------------------------------------------------------ encode
+// Written by the scan kernel alone (no clearing before the call): whether the call stops before
+// the write, and the token count.
 struct EncCtl {
     int32_t abort;
     uint32_t pad;
@@ -64,6 +66,15 @@ struct EncArgs {
     float alpha;    // version 2: the shared scale
     float* v;       // version 2: residual that takes back what the integers do not carry
 };
+
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may
+// start before the kernel ahead of it in the stream has finished; it waits here before it reads
+// anything that kernel writes (a no-op when it was launched the ordinary way). The kernel ahead
+// lets its dependents launch as soon as each of its blocks has started.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // version 2 layout: values of qbits/8 bytes, runs from the next even offset, nothing after them
 // (so the size fixes T: the receiver lays the messages out from their sizes)
@@ -103,17 +114,18 @@ __device__ __forceinline__ uint64_t enc_tokens(const EncArgs& a, uint64_t j, boo
     return 1 + (uint64_t)(cur - prev - 1) / kRunEscape;
 }
 
+// a block's token count that marks an index out of range or out of order
+constexpr uint64_t kTotBad = ~0ull;
+
 __global__ void __launch_bounds__(kThreads) k_enc_count(EncArgs a) {
     __shared__ uint64_t s_scan[33];
     __shared__ int s_bad;
+    grid_dep_launch();
     uint64_t lo, hi, cnt;
     if (threadIdx.x == 0) s_bad = 0;
     __syncthreads();
-    if (!enc_range(a, &lo, &hi, &cnt)) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) {
-            report(a.status, DGC_EINVAL);
-            a.ctl->abort = 1;
-        }
+    if (!enc_range(a, &lo, &hi, &cnt)) {  // (the scan kernel finds the count bad as well)
+        if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, DGC_EINVAL);
         return;
     }
     uint64_t t = 0;
@@ -123,21 +135,27 @@ __global__ void __launch_bounds__(kThreads) k_enc_count(EncArgs a) {
     uint64_t total;
     block_excl_scan<kThreads>(t, s_scan, &total);
     if (threadIdx.x == 0) {
-        a.tot[blockIdx.x] = total;
-        if (s_bad) {
-            report(a.status, DGC_EINVAL);
-            a.ctl->abort = 1;
-        }
+        a.tot[blockIdx.x] = s_bad ? kTotBad : total;
+        if (s_bad) report(a.status, DGC_EINVAL);
     }
 }
 
 __global__ void __launch_bounds__(1024) k_enc_scan(EncArgs a, int nblocks) {
     __shared__ uint64_t s_scan[33];
-    if (a.ctl->abort) {
-        if (threadIdx.x == 0) *a.out_bytes = 0;
+    grid_dep_launch();
+    grid_dep_wait();
+    // a count out of range, or a block that found a bad index: no message (the count kernel
+    // reported it)
+    const int64_t c = *a.count;
+    const bool count_ok = c >= 0 && (uint64_t)c <= a.max_count;
+    const uint64_t x = (count_ok && threadIdx.x < nblocks) ? a.tot[threadIdx.x] : 0;
+    if (__syncthreads_or(!count_ok || x == kTotBad)) {
+        if (threadIdx.x == 0) {
+            *a.out_bytes = 0;
+            a.ctl->abort = 1;
+        }
         return;
     }
-    const uint64_t x = threadIdx.x < nblocks ? a.tot[threadIdx.x] : 0;
     uint64_t T;
     const uint64_t ex = block_excl_scan<1024>(x, s_scan, &T);
     if (threadIdx.x < nblocks) a.tot[threadIdx.x] = ex;
@@ -150,6 +168,7 @@ __global__ void __launch_bounds__(1024) k_enc_scan(EncArgs a, int nblocks) {
         return;
     }
     a.ctl->T = T;
+    a.ctl->abort = 0;
     uint64_t* h = reinterpret_cast<uint64_t*>(a.out);
     h[1] = a.n;
     h[2] = T;
@@ -167,16 +186,14 @@ __global__ void __launch_bounds__(1024) k_enc_scan(EncArgs a, int nblocks) {
 
 __global__ void __launch_bounds__(kThreads) k_enc_write(EncArgs a) {
     __shared__ uint64_t s_scan[33];
-    if (a.ctl->abort) return;
     uint64_t lo, hi, cnt;
-    if (!enc_range(a, &lo, &hi, &cnt)) return;
-    const uint64_t T = a.ctl->T;
+    if (!enc_range(a, &lo, &hi, &cnt)) return;  // (the scan kernel stopped the call)
     uint32_t* vals = reinterpret_cast<uint32_t*>(a.out + 32);
     int8_t* vals8 = reinterpret_cast<int8_t*>(a.out + 32);
     int16_t* vals16 = reinterpret_cast<int16_t*>(a.out + 32);
-    uint16_t* runs = reinterpret_cast<uint16_t*>(
-        a.out + (a.qbits ? q_runs_offset(T, a.qbits) : 32 + 4 * T));
-    uint64_t carry = a.tot[blockIdx.x];
+    uint16_t* runs = nullptr;
+    uint64_t carry = 0;
+    bool waited = false;  // (the same in every thread)
     for (uint64_t c = lo; c < hi; c += (uint64_t)kThreads * kEncPer) {
         uint64_t tk[kEncPer];
         uint64_t mine = 0;
@@ -188,7 +205,19 @@ __global__ void __launch_bounds__(kThreads) k_enc_write(EncArgs a) {
             mine += tk[e];
         }
         uint64_t total;
-        uint64_t p = carry + block_excl_scan<kThreads>(mine, s_scan, &total);
+        const uint64_t ex = block_excl_scan<kThreads>(mine, s_scan, &total);
+        if (!waited) {
+            // the block's first tokens are counted (from inputs that came before the call) while
+            // the scan kernel finishes; its results from here on
+            grid_dep_wait();
+            if (ld_relaxed_u32(reinterpret_cast<const uint32_t*>(&a.ctl->abort))) return;
+            const uint64_t T = a.ctl->T;
+            runs = reinterpret_cast<uint16_t*>(
+                a.out + (a.qbits ? q_runs_offset(T, a.qbits) : 32 + 4 * T));
+            carry = a.tot[blockIdx.x];
+            waited = true;
+        }
+        uint64_t p = carry + ex;
 #pragma unroll
         for (int e = 0; e < kEncPer; ++e) {
             const uint64_t j = c + (uint64_t)threadIdx.x * kEncPer + e;
@@ -271,15 +300,6 @@ struct DecArgs {
     uint64_t nchunks;
     uint32_t spin_limit;
 };
-
-// Programmatic dependent launch: a kernel launched with programmatic stream serialization may
-// start before the kernel ahead of it in the stream has finished; it waits here before it reads
-// anything that kernel writes (a no-op when it was launched the ordinary way). The kernel ahead
-// lets its dependents launch as soon as each of its blocks has started.
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 __device__ __forceinline__ void mark_bad(const DecArgs& a) {
     atomicExch(&a.ctl->any_bad, 1u);
@@ -1168,15 +1188,17 @@ int encode_impl(const uint32_t* idx, const float* val, const int64_t* count, int
     a.ctl = reinterpret_cast<EncCtl*>(w);
     a.tot = reinterpret_cast<uint64_t*>(w + align256(sizeof(EncCtl)));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(a.ctl, 0, sizeof(EncCtl), s) != cudaSuccess) return DGC_ECUDA;
     const int sms = dgc_internal_sm_count();
     if (sms <= 0) return DGC_ECUDA;
     const int G = std::min(kEncBlocks, 2 * sms);
+    // no memset: the scan kernel writes the control words; the count kernel is an ordinary
+    // launch (it reads what came before the call), the other two may start while the one ahead
+    // of them finishes
     k_enc_count<<<G, kThreads, 0, s>>>(a);
-    k_enc_scan<<<1, 1024, 0, s>>>(a, G);
-    k_enc_write<<<G, kThreads, 0, s>>>(a);
+    const cudaError_t e1 = launch_dependent(k_enc_scan, 1, 1024, s, a, G);
+    const cudaError_t e2 = launch_dependent(k_enc_write, (uint64_t)G, kThreads, s, a);
     dgc_internal_count_launches(3);
-    if (cudaPeekAtLastError() != cudaSuccess) {
+    if (e1 != cudaSuccess || e2 != cudaSuccess || cudaPeekAtLastError() != cudaSuccess) {
         cudaGetLastError();
         return DGC_ECUDA;
     }
