@@ -308,7 +308,7 @@ class Pipeline:
 
     def capture(self, g, p):
         """CUDA graphs of this pipeline's compress call on g, its encode call and its decode
-        call: each enqueues kernels (and memsets) only, the decode taking the message size from
+        call: each enqueues kernels only, the decode taking the message size from
         device memory, so they replay as they were captured, with no host round trip."""
         import torch
 

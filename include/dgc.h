@@ -34,9 +34,9 @@
  *     rebuilds them when either differs, so using the workspace for anything else in between
  *     is safe and only costs that rebuild.
  *   - Indices are uint32: n must be below 2^32.
- *   - CUDA graphs: dgc_compress, dgc_compress_shared and dgc_encode enqueue kernels (dgc_compress
- *     some of them as cooperative launches) and at most a memset, so a stream capture of them
- *     replays as captured. Make one ordinary dgc_compress or dgc_compress_shared call on the
+ *   - CUDA graphs: dgc_compress, dgc_compress_shared and dgc_encode enqueue kernels only
+ *     (dgc_compress some of them as cooperative launches, dgc_encode its last two as
+ *     programmatic dependent launches), so a stream capture of them replays as captured. Make one ordinary dgc_compress or dgc_compress_shared call on the
  *     device first (it sets the kernels' shared-memory attributes and reads the cooperative
  *     kernels' occupancy once per device). The decoders with host sizes read those sizes on
  *     the host at every call (and copy their table of messages from host memory when there are

@@ -1441,7 +1441,7 @@ def test_l2_fetch_granularity_hint_keeps_results():
 
 
 def test_compress_encode_in_cuda_graph():
-    # dgc_compress and dgc_encode enqueue kernels and a memset only, so a training loop can
+    # dgc_compress and dgc_encode enqueue kernels only, so a training loop can
     # capture them once (after one ordinary call on the device) and replay the graph every step;
     # the replays must give the oracle's results step after step
     n = 3_000_017
