@@ -68,3 +68,32 @@ def test_one_rank_exchange_equals_the_decoders(one_rank_nccl):
     assert sizes == [len(m)] and dgc.dgc_read_status(status) == 0
     _, w_want = oracle.decode_apply([m], n, w0, np.float32(0.05))
     assert np.array_equal(w.cpu().numpy().view(np.uint32), w_want.view(np.uint32))
+
+
+def test_one_rank_shared_set_exchange_equals_the_oracle(one_rank_nccl):
+    # ScaleComp's shared-set path through NCCL on one rank: the set broadcast from rank 0, the
+    # value vector at it gathered, and the rank-ordered sum (dgc_sum_shared) on the device; with
+    # one rank the sum is +0 + x, which must equal the oracle's bit for bit
+    dgc.build()
+    n = 1_048_576
+    off = np.array([0, n], np.int64)
+    g = workloads.gradient("single", 0)
+    po = oracle.make_params(mode=oracle.SAMPLED, sparsity=0.999, momentum=0.9, seed=3, leak=0.9)
+    sidx, val, _ = oracle.compress(g, np.zeros(n, np.float32), np.zeros(n, np.float32), off, po)
+    c = int(sidx.size)
+    cap = c + 64
+    idx = torch.zeros(cap, dtype=torch.int32, device="cuda")
+    idx[:c] = torch.from_numpy(sidx.astype(np.int64)).to(torch.int32).cuda()
+    count = torch.tensor([c], dtype=torch.int64, device="cuda")
+    assert exchange.broadcast_index_set(idx, count, 0) == c
+    assert np.array_equal(idx[:c].cpu().numpy().view(np.uint32), sidx.astype(np.uint32))
+    vals = torch.full((cap,), float("nan"), dtype=torch.float32, device="cuda")
+    vals[:c] = torch.from_numpy(val).cuda()
+    out = torch.full((cap,), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(dgc.dgc_sum_shared_workspace(1), 16), dtype=torch.uint8, device="cuda")
+    assert exchange.exchange_shared_sum(vals, count, out, status, ws) == c
+    assert dgc.dgc_read_status(status) == 0
+    rc, want = oracle.sum_shared([val])
+    assert rc == 0
+    assert np.array_equal(out[:c].cpu().numpy().view(np.uint32), want.view(np.uint32))
