@@ -640,7 +640,8 @@ def test_decode_many_learners_and_accumulate(seed):
 
 
 @pytest.mark.parametrize("case", ["same set, 300 learners", "dense messages, 40 learners",
-                                  "half shared, 70 learners", "shared positions, 8 learners"])
+                                  "half shared, 70 learners", "shared positions, 8 learners",
+                                  "crowded and sparse tiles, 12 learners"])
 def test_decode_collisions_and_crowded_tiles(case):
     # The worst cases of the ordered multi-message sum: every learner at the same positions (as
     # many values meet at one position as there are learners, across the 256-message groups),
@@ -671,6 +672,18 @@ def test_decode_collisions_and_crowded_tiles(case):
         for _ in range(W):
             own = rng.choice(n, size=40, replace=False)
             idx = np.unique(np.concatenate([common, own])).astype(np.uint32)
+            val = (rng.standard_normal(idx.size) * 10.0 ** rng.integers(-3, 3, idx.size))
+            msgs.append(oracle.encode(idx, val.astype(np.float32), n))
+    elif case.startswith("crowded and sparse"):
+        # one crowded 16,384-entry tile (36,000 tokens) among sparse ones, shared positions in
+        # both, and a ragged last tile: in the SGD step the sum kernel takes the sparse tiles and
+        # leaves the crowded one to the round-based kernel
+        n, W = 200_003, 12
+        crowd = np.arange(3 * 16384, 3 * 16384 + 3000)
+        common = rng.choice(n, size=50, replace=False)
+        for _ in range(W):
+            own = rng.choice(n, size=300, replace=False)
+            idx = np.unique(np.concatenate([crowd, common, own])).astype(np.uint32)
             val = (rng.standard_normal(idx.size) * 10.0 ** rng.integers(-3, 3, idx.size))
             msgs.append(oracle.encode(idx, val.astype(np.float32), n))
     else:
